@@ -1,0 +1,167 @@
+/*
+ * bitnet_b300.h — BitNet b1.58 BitLinear hot path for NVIDIA B300 (sm_103a).
+ *
+ * Ternary weights {-1, 0, +1} times int8 activations, int32 accumulation,
+ * binary32 rescale, and the fused BitNet feed-forward block built on it.
+ *
+ * Sources (web pages describing the method):
+ *  [P1] "Microsoft BitNet b1.58 ... 1-bit AI model" (communeify blog),
+ *       "Meet BitNet b1.58 2B4T": W1.58A8, BitLinear, ReLU^2, subln, no bias.
+ *  [P2] "How to run BitNet B1.58 (1-Bit LLM) locally" (onedollarvps), §2
+ *       "Technical background": weights divided by their mean absolute value,
+ *       rounded and clipped to {-1, 0, +1}.
+ *  [P3] "BitNet.cpp deep dive" (dashen-tech), §2.3 "I2_S format" (2 bits per
+ *       weight, 8 weights in 16 bits), §3.1 "integer matrix multiplication"
+ *       (Y = sum_pos - sum_neg, no multiplications).
+ *  [P4] "Microsoft BitNet: 100B models on CPU" (juejin), "CPU-friendly
+ *       matrix multiplication": INT8 activations.
+ *  [P5] "BitNet - 1-bit LLM inference framework" (news.hada.io), HN comment:
+ *       2-bit storage holds four values.
+ *
+ * Conventions for every call:
+ *  - Every array argument is a DEVICE pointer owned by the caller; the
+ *    library never allocates or frees device memory and keeps no state
+ *    across calls other than a per-device error word (bitnet_device_error).
+ *  - Arrays are row-major.  W is [N = out features, K = in features].
+ *  - bf16 arrays are passed as uint16_t bit patterns.
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls are
+ *    asynchronous on it, never synchronise, and may be captured in a CUDA
+ *    graph.
+ *  - Arguments are checked on the host before anything is launched; a bad
+ *    argument returns a status and launches nothing:
+ *      BITNET_ERR_NULL       a required pointer is NULL;
+ *      BITNET_ERR_SHAPE      a size is <= 0, K (or H, F) is not a multiple of
+ *                            64, or a size exceeds the stated maximum;
+ *      BITNET_ERR_ALIGN      a pointer is not 16-byte aligned;
+ *      BITNET_ERR_WORKSPACE  ws_bytes is below the *_workspace() figure;
+ *      BITNET_ERR_UNSUPPORTED the current device is not compute capability
+ *                            10.3 (sm_103);
+ *      BITNET_ERR_CUDA       a CUDA call or launch failed (code in
+ *                            bitnet_last_cuda_error()).
+ *  - Inputs must be finite; see each call for what non-finite input gives.
+ *  - No C++ exception crosses this interface.
+ */
+#ifndef BITNET_B300_H
+#define BITNET_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum bitnet_status {
+  BITNET_OK = 0,
+  BITNET_ERR_NULL = 1,
+  BITNET_ERR_SHAPE = 2,
+  BITNET_ERR_ALIGN = 3,
+  BITNET_ERR_WORKSPACE = 4,
+  BITNET_ERR_UNSUPPORTED = 5,
+  BITNET_ERR_CUDA = 6
+} bitnet_status;
+
+/* Largest K, H or F accepted (int32 partial sums stay exact below it). */
+#define BITNET_MAX_K 65536
+
+/* Static text for a status code; never NULL. */
+const char* bitnet_status_string(int status);
+
+/* The cudaError_t of the last BITNET_ERR_CUDA returned on this host thread. */
+int bitnet_last_cuda_error(void);
+
+/* Interface version (bumped on any incompatible change). */
+int bitnet_abi_version(void);
+
+/* Reads and clears the current device's error word: 0, or a code set by a
+ * kernel whose internal wait ran past its time limit (the kernel then
+ * returns without finishing its output).  Synchronises `stream`. */
+bitnet_status bitnet_device_error(int* code_out, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Weight quantisation ([P2] §2; [P3] §2.3; [P5]).
+ *   gamma   = mean of |W| over all N*K entries, computed exactly and rounded
+ *             once to binary32 (nearest, ties to even);
+ *   w_scale = max(gamma, 1e-5);
+ *   q       = clamp(round_half_even(W / w_scale), -1, 1), IEEE binary32
+ *             division;
+ *   Wq      = codes q + 1 in {0, 1, 2}, 2 bits each, [N, K/4] bytes: weight
+ *             k of row n is in byte n*K/4 + (k/64)*16 + (k%16) at bit shift
+ *             2*((k%64)/16).
+ * W: [N, K] binary32.  Wq: [N*K/4] bytes.  w_scale: one float (device).
+ * ws: scratch of bitnet_quantize_weights_workspace() bytes, no initial
+ * contents required.  If any W entry is Inf or NaN, w_scale becomes NaN
+ * and every code is 1 (q = 0).  Requires K % 64 == 0, N*K < 2^40. */
+size_t bitnet_quantize_weights_workspace(int64_t N, int64_t K);
+bitnet_status bitnet_quantize_weights(const float* W, int64_t N, int64_t K,
+                                      uint8_t* Wq, float* w_scale, void* ws,
+                                      size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Per-token absmax int8 activation quantisation ([P1] "A8"; [P4]).
+ * For each row m of x [M, K] (bf16):
+ *   a = max_k |x|, a' = max(a, 1e-5), inv = 127 / a' (binary32 division),
+ *   xq = clamp(round_half_even(x * inv), -128, 127), x_scale[m] = a' / 127.
+ * xq: [M, K] int8.  x_scale: [M] float.  K % 64 == 0, K <= BITNET_MAX_K. */
+bitnet_status bitnet_quantize_act(const uint16_t* x, int64_t M, int64_t K,
+                                  int8_t* xq, float* x_scale, void* stream);
+
+/* ------------------------------------------------------------------------
+ * BitLinear ([P3] §3.1; rescale: [P1] no bias).
+ *   acc[m,n] = sum over k of q[n,k] * xq[m,k]  (= sum_pos - sum_neg, exact
+ *              int32), q unpacked from Wq;
+ *   y[m,n]   = (float)acc[m,n] * (x_scale[m] * w_scale[0]).
+ * Wq [N, K/4] bytes, w_scale [1], xq [M, K], x_scale [M], y [M, N] float.
+ * acc_out: optional [M, N] int32 copy of acc (NULL to skip).
+ * ws: scratch of bitnet_linear_workspace(M, N, K) bytes, no initial
+ * contents required.  M <= 4096*64 rows per call; K % 64 == 0.
+ * Small M runs a CUDA-core kernel; large M runs the tensor-core kernel;
+ * both give the same bits. */
+size_t bitnet_linear_workspace(int64_t M, int64_t N, int64_t K);
+bitnet_status bitnet_linear(const uint8_t* Wq, const float* w_scale,
+                            const int8_t* xq, const float* x_scale, int64_t M,
+                            int64_t N, int64_t K, float* y, int32_t* acc_out,
+                            void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Fused BitNet feed-forward block ([P1] subln, ReLU^2, no bias):
+ *   r   = (float)(1 / sqrt(ss / H + eps)), ss = sum x^2 (binary64, in the
+ *         order: 32 strided partial sums over k = l (mod 32), increasing k,
+ *         then pairwise p[l] + p[l ^ off] for off = 16, 8, 4, 2, 1);
+ *   nrm = (x * r) * g;                          binary32, per element
+ *   xq, sx = per-token int8 quantisation of nrm (rule of bitnet_quantize_act)
+ *   u   = BitLinear(Wup, s_up; xq, sx)          [M, F]
+ *   v   = BitLinear(Wgate, s_gate; xq, sx)      [M, F]
+ *   h   = (t * t) * u, t = max(v, 0)            binary32
+ *   hq, sh = per-token int8 quantisation of h over F
+ *   y   = BitLinear(Wdown, s_down; hq, sh)      [M, H]
+ * x [M, H] bf16, g [H] float, Wup / Wgate [F, H/4], Wdown [H, F/4] packed,
+ * s_* one float each, y [M, H] float.  H % 64 == 0, F % 64 == 0.
+ * dbg: NULL, or a struct whose non-NULL members receive the named
+ * intermediate (xq [M,H], sx [M], u, v, h [M,F], hq [M,F], sh [M],
+ * acc_down [M,H]).  ws: bitnet_ffn_workspace(M, H, F) bytes, no initial
+ * contents required. */
+typedef struct bitnet_ffn_debug {
+  int8_t* xq;
+  float* sx;
+  float* u;
+  float* v;
+  float* h;
+  int8_t* hq;
+  float* sh;
+  int32_t* acc_down;
+} bitnet_ffn_debug;
+
+size_t bitnet_ffn_workspace(int64_t M, int64_t H, int64_t F);
+bitnet_status bitnet_ffn(const uint16_t* x, const float* g, float eps,
+                         const uint8_t* Wup, const float* s_up,
+                         const uint8_t* Wgate, const float* s_gate,
+                         const uint8_t* Wdown, const float* s_down, int64_t M,
+                         int64_t H, int64_t F, float* y,
+                         const bitnet_ffn_debug* dbg, void* ws,
+                         size_t ws_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif
