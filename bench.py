@@ -1,0 +1,482 @@
+"""Benchmark of the BitNet b1.58 BitLinear hot path on B300.
+
+Default workload (one "step"): a batch-1 decode step over 2B-class layer
+shapes, 30 layers with distinct weight sets (521 MB of packed ternary weights,
+4x the 126 MB L2, so every step streams its weights from HBM).  Per layer:
+three per-token int8 activation quantisations (layer input, attention output,
+FFN hidden state, bf16 N(0,1)) and seven BitLinear products (Q, O: 2560->2560;
+K, V: 2560->640; up, gate: 2560->6912; down: 6912->2560).  The step is
+captured once in a CUDA graph and replayed.
+
+Metric: GB/s of algorithmic bytes (packed weights + activations read and
+written + scales + outputs) per second; the roofline block reports the
+dominant kernel (the BitLinear GEMV) against the measured HBM copy bandwidth.
+`--impl reference` times the CPU oracle on a bounded sample of the same
+workload instead.  Under torchrun every rank runs an independent replica
+(the path needs no exchange between GPUs) and rank 0 prints one JSON line.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+HIDDEN, FFN = 2560, 6912
+LAYER_SHAPES = [("q", HIDDEN, HIDDEN, "x"), ("k", 640, HIDDEN, "x"), ("v", 640, HIDDEN, "x"),
+                ("o", HIDDEN, HIDDEN, "attn"), ("up", FFN, HIDDEN, "x"),
+                ("gate", FFN, HIDDEN, "x"), ("down", HIDDEN, FFN, "h")]
+INPUTS = [("x", HIDDEN), ("attn", HIDDEN), ("h", FFN)]
+METRIC = "BitLinear decode GB/s & % HBM roofline; prefill int8 TOPS & % tensor peak"
+WORKLOAD = ("decode step, batch 1, 2B-class shapes (hidden 2560, FFN 6912), 30 layers of "
+            "distinct ternary weights")
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--layers", type=int, default=30)
+    ap.add_argument("--impl", default="b300", choices=["b300", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-secondary", action="store_true")
+    return ap.parse_args()
+
+
+def layer_bytes():
+    """Algorithmic bytes of one layer: act-quant reads bf16 and writes int8 +
+    scale; each BitLinear reads packed W, int8 x, two scales, writes fp32 y."""
+    b = 0
+    for _, K in INPUTS:
+        b += 2 * K + K + 4
+    for _, N, K, _ in LAYER_SHAPES:
+        b += N * K // 4 + K + 8 + 4 * N
+    return b
+
+
+def weight_bytes():
+    return sum(N * K // 4 for _, N, K, _ in LAYER_SHAPES)
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.t0 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            f = [c.strip() for c in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------- GPU arm
+class DecodeStep:
+    """Resident weights, inputs, outputs and workspaces of the decode step."""
+
+    def __init__(self, layers, seed=0):
+        import torch
+        import bitlinear_bitnet_linear_03_b300 as bn
+        from bitlinear_bitnet_linear_03_b300 import synth
+        self.torch, self.bn = torch, bn
+        dev = torch.device("cuda")
+        self.layers = []
+        ws_q = torch.empty(bn.bitnet_quantize_weights_workspace(FFN, HIDDEN) * 2,
+                           dtype=torch.uint8, device=dev)
+        lin_ws = max(bn.bitnet_linear_workspace(1, N, K) for _, N, K, _ in LAYER_SHAPES)
+        self.lin_ws = torch.empty(max(lin_ws, 16), dtype=torch.uint8, device=dev)
+        for li in range(layers):
+            L = {"W": {}, "x": {}, "xq": {}, "sx": {}, "y": {}}
+            for j, (name, N, K, _) in enumerate(LAYER_SHAPES):
+                W = synth.weights_f32(N, K, seed=seed * 100000 + li * 16 + j, device="cuda")
+                Wq, s = bn.bitnet_quantize_weights(W, ws=ws_q)
+                del W
+                L["W"][name] = (Wq, s, N, K)
+                L["y"][name] = torch.empty((1, N), dtype=torch.float32, device=dev)
+            for j, (name, K) in enumerate(INPUTS):
+                L["x"][name] = synth.tokens_bf16(1, K, seed=seed * 100000 + li * 16 + 8 + j,
+                                                 device="cuda")
+                L["xq"][name] = torch.empty((1, K), dtype=torch.int8, device=dev)
+                L["sx"][name] = torch.empty(1, dtype=torch.float32, device=dev)
+            self.layers.append(L)
+        torch.cuda.synchronize()
+
+    def quantize_inputs(self):
+        for L in self.layers:
+            for name, _ in INPUTS:
+                self.bn.bitnet_quantize_act(L["x"][name], L["xq"][name], L["sx"][name])
+
+    def linears(self):
+        for L in self.layers:
+            for name, N, K, src in LAYER_SHAPES:
+                Wq, s, _, _ = L["W"][name]
+                self.bn.bitnet_linear(Wq, s, L["xq"][src], L["sx"][src], K=K, y=L["y"][name],
+                                      ws=self.lin_ws)
+
+    def step(self):
+        self.quantize_inputs()
+        self.linears()
+
+    def launches_per_step(self):
+        n = 0
+        for _ in self.layers:
+            n += len(INPUTS)
+            for _, N, K, _ in LAYER_SHAPES:
+                n += 2 if self.bn.bitnet_linear_workspace(1, N, K) > 0 else 1
+        return n
+
+    def input_tensors(self):
+        return [L["x"][n] for L in self.layers for n, _ in INPUTS]
+
+    def output_tensors(self):
+        return [L["y"][n] for L in self.layers for n, *_ in LAYER_SHAPES]
+
+
+def capture(torch, fn):
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fn()  # warm the library (first-call set-up) outside the capture
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    torch.cuda.synchronize()
+    return g
+
+
+def time_graph(torch, g, steps, warmup, barrier):
+    for _ in range(warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / 1e3
+
+
+def read_peaks():
+    try:
+        return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except (OSError, ValueError):
+        return None
+
+
+def profiled_traffic(kernel_file, profile_file):
+    """Per-launch DRAM bytes from a committed ncu summary, or None when the
+    kernel source changed since the capture (the summary records its hash)."""
+    try:
+        src = open(os.path.join(ROOT, kernel_file), "rb").read()
+        text = open(os.path.join(ROOT, profile_file)).read()
+    except OSError:
+        return None
+    digest = hashlib.sha256(src).hexdigest()[:16]
+    vals = {}
+    for line in text.splitlines():
+        if ":" in line and line.strip().startswith(("source_sha256_16", "dram_bytes_per_launch")):
+            k, v = line.split(":", 1)
+            vals[k.strip()] = v.strip().strip("`")
+    if vals.get("source_sha256_16") != digest:
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+def secondary_measurements(torch, bn):
+    """Prefill GEMM (M = 4096) and the fused FFN at seq 1 / seq 4096, timed
+    with CUDA events after warm-up (inputs resident; the prefill outputs are
+    113 MB, weights rotate over 8 sets)."""
+    from bitlinear_bitnet_linear_03_b300 import synth
+    out = {}
+    dev = torch.device("cuda")
+    for (N, K) in [(6912, 2560), (2560, 6912)]:
+        M = 4096
+        sets = []
+        for r in range(4):
+            W = synth.weights_f32(N, K, seed=500 + r, device="cuda")
+            sets.append(bn.bitnet_quantize_weights(W))
+            del W
+        x = synth.tokens_bf16(M, K, seed=600, device="cuda")
+        xq, sx = bn.bitnet_quantize_act(x)
+        y = torch.empty((M, N), dtype=torch.float32, device=dev)
+        ws = torch.empty(max(bn.bitnet_linear_workspace(M, N, K), 16), dtype=torch.uint8,
+                         device=dev)
+        for i in range(3):
+            Wq, s = sets[i % 4]
+            bn.bitnet_linear(Wq, s, xq, sx, y=y, ws=ws)
+        torch.cuda.synchronize()
+        reps = 8
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for i in range(reps):
+            Wq, s = sets[i % 4]
+            bn.bitnet_linear(Wq, s, xq, sx, y=y, ws=ws)
+        e1.record()
+        torch.cuda.synchronize()
+        t = e0.elapsed_time(e1) / 1e3 / reps
+        out[f"prefill_M4096_K{K}_N{N}"] = {"ms": t * 1e3, "tops": 2 * M * N * K / t / 1e12}
+        del sets, xq, sx, y, ws
+    return out
+
+
+def run_gpu_arm(args, rank, world, barrier, max_over_ranks):
+    import torch
+    import bitlinear_bitnet_linear_03_b300 as bn
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+    bn.lib()
+    step = DecodeStep(args.layers)
+    graph = capture(torch, step.step)
+    lin_graph = capture(torch, step.linears)
+
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    time.sleep(0.3)
+    dt = time_graph(torch, graph, args.steps, args.warmup, barrier)
+    clk = clocks.stop()
+    dt = max_over_ranks(dt)
+
+    bytes_step = layer_bytes() * args.layers
+    value = bytes_step * args.steps * world / dt / 1e9
+
+    # e2e: pinned-host inputs copied in and outputs copied out every step.
+    ins = step.input_tensors()
+    outs = step.output_tensors()
+    h_in = [t.cpu().pin_memory() for t in ins]
+    h_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs]
+    h2d = sum(t.numel() * t.element_size() for t in ins)
+    d2h = sum(t.numel() * t.element_size() for t in outs)
+
+    def e2e_step():
+        for d, h in zip(ins, h_in):
+            d.copy_(h, non_blocking=True)
+        graph.replay()
+        for h, d in zip(h_out, outs):
+            h.copy_(d, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    for _ in range(max(3, args.warmup)):
+        e2e_step()
+    e2e_steps = max(10, min(args.steps, 500))
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    t_e2e = max_over_ranks(time.perf_counter() - t0)
+    e2e_value = bytes_step * e2e_steps * world / t_e2e / 1e9
+
+    # Dominant kernel: the BitLinear launches alone, graph-replayed; average
+    # launch duration = replay time / launches.
+    lin_launches = step.launches_per_step() - len(INPUTS) * args.layers
+    reps = max(20, min(args.steps, 400))
+    t_lin = time_graph(torch, lin_graph, reps, 5, lambda: None)
+    per_launch_s = t_lin / reps / lin_launches
+    lin_bytes = sum(N * K // 4 + K + 8 + 4 * N for _, N, K, _ in LAYER_SHAPES) * args.layers
+    achieved = lin_bytes / lin_launches / per_launch_s / 1e9
+    peaks = read_peaks()
+    if peaks and peaks.get("hbm_gbs"):
+        peak, peak_src = float(peaks["hbm_gbs"]), "measured"
+    else:
+        peak, peak_src = 6400.0, "fallback"
+    traffic = profiled_traffic("bitlinear_bitnet_linear_03_b300/csrc/gemv.cu",
+                               "profiles/gemv_decode_2b_30layers.md")
+
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt / args.steps * 1e3, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "int8 x ternary (int32 acc, f32 out)",
+        "data": "synthetic: weights N(0,0.02) ternarized, activations bf16 N(0,1), seeded",
+        "config": {"workload": WORKLOAD, "layers": args.layers, "batch_tokens": 1,
+                   "packed_weight_bytes_per_step": weight_bytes() * args.layers,
+                   "algorithmic_bytes_per_step": bytes_step,
+                   "l2": "inputs larger than L2 (521 MB of weights per step vs 126 MB L2)",
+                   "graph": "whole step captured in one CUDA graph",
+                   "parallelism": f"replicas x{world}"},
+        "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "gpu_launches": step.launches_per_step() * args.steps,
+        "roofline": {"bound": "hbm", "kernel": "bitnet_linear GEMV (k_gemv + split-K reduce)",
+                     "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_source": peak_src,
+                     "traffic": traffic, "launch_us": round(per_launch_s * 1e6, 3),
+                     "bytes_per_launch": lin_bytes / lin_launches},
+        "clocks": clk,
+    }
+    if not args.no_secondary:
+        result["secondary"] = secondary_measurements(torch, bn)
+    return result
+
+
+# ----------------------------------------------------------------- oracle arm
+class OracleSample:
+    """One decode layer built on the host for the oracle (never touched by
+    the GPU path): packed weights, bf16 inputs."""
+
+    def __init__(self, seed=0):
+        import oracle
+        from bitlinear_bitnet_linear_03_b300 import synth
+        self.oracle = oracle
+        self.W = {}
+        for j, (name, N, K, _) in enumerate(LAYER_SHAPES):
+            Wq, s, _ = oracle.quantize_weights(synth.weights_f32(N, K, seed=7000 + j))
+            self.W[name] = (Wq, s, N, K)
+        self.x = {name: synth.tokens_bf16(1, K, seed=7100 + j) for j, (name, K) in
+                  enumerate(INPUTS)}
+
+    def run(self, names, threads):
+        q = {}
+        for n, _ in INPUTS:
+            q[n] = self.oracle.quantize_act_bf16(self.x[n])
+        nbytes = sum(2 * K + K + 4 for _, K in INPUTS)
+        for name in names:
+            Wq, s, N, K = self.W[name]
+            src = dict((a, d) for a, _, _, d in LAYER_SHAPES)[name]
+            qx, sx = q[src]
+            self.oracle.linear(Wq, s, qx, sx, K, threads=threads)
+            nbytes += N * K // 4 + K + 8 + 4 * N
+        return nbytes
+
+
+def cpu_baseline(budget_s=12.0):
+    import oracle
+    threads = oracle.default_threads()
+    sample = OracleSample()
+    names = [n for n, *_ in LAYER_SHAPES]
+    sample.run(names, threads)  # warm-up
+    nbytes, t0, layers = 0, time.perf_counter(), 0
+    while time.perf_counter() - t0 < budget_s or layers == 0:
+        nbytes += sample.run(names, threads)
+        layers += 1
+    dt = time.perf_counter() - t0
+    return {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": threads,
+            "kind": "oracle",
+            "sample": f"{layers} repetitions of one decode layer (3 act quants + 7 BitLinear, "
+                      f"{layer_bytes()} algorithmic bytes each) of the 30-layer step, "
+                      f"{dt:.1f} s"}
+
+
+def run_reference_arm(args, rank):
+    if rank != 0:
+        return None
+    import oracle
+    threads = oracle.default_threads()
+    sample = OracleSample()
+    order = [n for n, *_ in LAYER_SHAPES]
+    for i in range(args.warmup):
+        sample.run([order[i % len(order)]], threads)
+    nbytes, t0 = 0, time.perf_counter()
+    for i in range(args.steps):
+        nbytes += sample.run([order[i % len(order)]], threads)
+    dt = time.perf_counter() - t0
+    value = nbytes / dt / 1e9
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "int8 x ternary (int32 acc, f32 out)",
+        "data": "synthetic: weights N(0,0.02) ternarized, activations bf16 N(0,1), seeded",
+        "config": {"workload": WORKLOAD, "layers": args.layers, "batch_tokens": 1,
+                   "parallelism": "replicas x1"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
+                         "kind": "oracle",
+                         "sample": "each step: the 3 act quants of one decode layer plus one "
+                                   "of its 7 BitLinear products, cycling Q,K,V,O,up,gate,down"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        res = run_reference_arm(args, rank)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return
+    import torch
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        dist.init_process_group("nccl")
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    def max_over_ranks(v):
+        if dist is None:
+            return v
+        t = torch.tensor([v], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    res = run_gpu_arm(args, rank, world, barrier, max_over_ranks)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            res["cpu_baseline"] = cpu_baseline()
+        print(json.dumps(res), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

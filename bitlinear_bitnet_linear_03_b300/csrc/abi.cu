@@ -1,0 +1,209 @@
+// abi.cu — the C interface declared in include/bitnet_b300.h: argument
+// checks, workspace sizing, dispatch to the kernels.  Nothing here allocates
+// device memory, synchronises (except bitnet_device_error) or keeps state
+// beyond a per-device capability cache.
+#include <cuda_runtime.h>
+
+#include "../../include/bitnet_b300.h"
+#include "common.cuh"
+#include "gemm_tc.cuh"
+
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+
+bitnet_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return BITNET_OK;
+  g_last_cuda_error = (int)e;
+  return BITNET_ERR_CUDA;
+}
+
+// 1 = sm_103 device, 2 = other device, 0 = not yet asked.
+int g_dev_ok[64];
+
+bitnet_status check_device() {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_status(e);
+  if (dev < 0 || dev >= 64) return BITNET_ERR_UNSUPPORTED;
+  if (g_dev_ok[dev] == 0) {
+    int major = 0, minor = 0;
+    e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    if (e != cudaSuccess) return cuda_status(e);
+    e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (e != cudaSuccess) return cuda_status(e);
+    g_dev_ok[dev] = (major == 10 && minor == 3) ? 1 : 2;
+  }
+  return g_dev_ok[dev] == 1 ? BITNET_OK : BITNET_ERR_UNSUPPORTED;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// The largest M one bitnet_linear / bitnet_ffn call accepts.
+constexpr int64_t kMaxRows = 4096 * 64;
+
+bool valid_inner(int64_t K) { return K > 0 && K % 64 == 0 && K <= BITNET_MAX_K; }
+
+size_t linear_ws(int64_t M, int64_t N, int64_t K) {
+  if (bitnet::gemm_tc_eligible(M, N, K)) return bitnet::gemm_tc_workspace(M, N, K);
+  return bitnet::gemv_workspace(M, N, K);
+}
+
+cudaError_t run_linear(const uint8_t* Wq, const float* w_scale, const int8_t* xq,
+                       const float* x_scale, int64_t M, int64_t N, int64_t K, float* y,
+                       int32_t* acc_out, void* ws, cudaStream_t s) {
+  if (bitnet::gemm_tc_eligible(M, N, K))
+    return bitnet::launch_gemm_tc(Wq, w_scale, xq, x_scale, M, N, K, y, acc_out, ws, s);
+  return bitnet::launch_gemv(Wq, w_scale, xq, x_scale, M, N, K, y, acc_out, ws, s);
+}
+
+// FFN workspace sections, each 256-byte aligned.
+struct FfnLayout {
+  size_t xq, sx, u, v, hq, sh, lin, total;
+};
+FfnLayout ffn_layout(int64_t M, int64_t H, int64_t F) {
+  FfnLayout L;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t o = off;
+    off += round_up(bytes, 256);
+    return o;
+  };
+  L.xq = take((size_t)(M * H));
+  L.sx = take((size_t)M * 4);
+  L.u = take((size_t)(M * F) * 4);
+  L.v = take((size_t)(M * F) * 4);
+  L.hq = take((size_t)(M * F));
+  L.sh = take((size_t)M * 4);
+  size_t a = linear_ws(M, F, H), b = linear_ws(M, H, F);
+  L.lin = take(a > b ? a : b);
+  L.total = off;
+  return L;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* bitnet_status_string(int status) {
+  switch (status) {
+    case BITNET_OK: return "ok";
+    case BITNET_ERR_NULL: return "a required pointer is NULL";
+    case BITNET_ERR_SHAPE: return "a size is out of range or K, H, F is not a multiple of 64";
+    case BITNET_ERR_ALIGN: return "a pointer is not 16-byte aligned";
+    case BITNET_ERR_WORKSPACE: return "workspace is smaller than the *_workspace() figure";
+    case BITNET_ERR_UNSUPPORTED: return "the current device is not compute capability 10.3";
+    case BITNET_ERR_CUDA: return "a CUDA call or kernel launch failed";
+    default: return "unknown status";
+  }
+}
+
+int bitnet_last_cuda_error(void) { return g_last_cuda_error; }
+
+int bitnet_abi_version(void) { return 1; }
+
+bitnet_status bitnet_device_error(int* code_out, void* stream) {
+  if (!code_out) return BITNET_ERR_NULL;
+  bitnet_status st = check_device();
+  if (st != BITNET_OK) return st;
+  return cuda_status(bitnet::read_and_clear_device_error(code_out, (cudaStream_t)stream));
+}
+
+size_t bitnet_quantize_weights_workspace(int64_t N, int64_t K) {
+  if (N <= 0 || K <= 0) return 0;
+  return bitnet::quantize_weights_workspace(N * K);
+}
+
+bitnet_status bitnet_quantize_weights(const float* W, int64_t N, int64_t K, uint8_t* Wq,
+                                      float* w_scale, void* ws, size_t ws_bytes,
+                                      void* stream) {
+  if (!W || !Wq || !w_scale || !ws) return BITNET_ERR_NULL;
+  if (N <= 0 || K <= 0 || K % 64 != 0 || N > ((int64_t)1 << 40) / K) return BITNET_ERR_SHAPE;
+  if (!aligned16(W) || !aligned16(Wq) || !aligned16(ws)) return BITNET_ERR_ALIGN;
+  if (ws_bytes < bitnet::quantize_weights_workspace(N * K)) return BITNET_ERR_WORKSPACE;
+  bitnet_status st = check_device();
+  if (st != BITNET_OK) return st;
+  return cuda_status(
+      bitnet::launch_quantize_weights(W, N * K, Wq, w_scale, ws, (cudaStream_t)stream));
+}
+
+bitnet_status bitnet_quantize_act(const uint16_t* x, int64_t M, int64_t K, int8_t* xq,
+                                  float* x_scale, void* stream) {
+  if (!x || !xq || !x_scale) return BITNET_ERR_NULL;
+  if (M <= 0 || M > kMaxRows || !valid_inner(K)) return BITNET_ERR_SHAPE;
+  if (!aligned16(x) || !aligned16(xq)) return BITNET_ERR_ALIGN;
+  bitnet_status st = check_device();
+  if (st != BITNET_OK) return st;
+  return cuda_status(bitnet::launch_quantize_act_bf16(x, M, K, xq, x_scale, (cudaStream_t)stream));
+}
+
+size_t bitnet_linear_workspace(int64_t M, int64_t N, int64_t K) {
+  if (M <= 0 || N <= 0 || K <= 0) return 0;
+  return linear_ws(M, N, K);
+}
+
+bitnet_status bitnet_linear(const uint8_t* Wq, const float* w_scale, const int8_t* xq,
+                            const float* x_scale, int64_t M, int64_t N, int64_t K, float* y,
+                            int32_t* acc_out, void* ws, size_t ws_bytes, void* stream) {
+  if (!Wq || !w_scale || !xq || !x_scale || !y) return BITNET_ERR_NULL;
+  if (M <= 0 || M > kMaxRows || N <= 0 || N > (1 << 30) || !valid_inner(K))
+    return BITNET_ERR_SHAPE;
+  if (!aligned16(Wq) || !aligned16(xq) || !aligned16(y) || (acc_out && !aligned16(acc_out)))
+    return BITNET_ERR_ALIGN;
+  const size_t need = linear_ws(M, N, K);
+  if (need > 0 && (!ws || ws_bytes < need)) return ws ? BITNET_ERR_WORKSPACE : BITNET_ERR_NULL;
+  if (need > 0 && !aligned16(ws)) return BITNET_ERR_ALIGN;
+  bitnet_status st = check_device();
+  if (st != BITNET_OK) return st;
+  return cuda_status(
+      run_linear(Wq, w_scale, xq, x_scale, M, N, K, y, acc_out, ws, (cudaStream_t)stream));
+}
+
+size_t bitnet_ffn_workspace(int64_t M, int64_t H, int64_t F) {
+  if (M <= 0 || H <= 0 || F <= 0) return 0;
+  return ffn_layout(M, H, F).total;
+}
+
+bitnet_status bitnet_ffn(const uint16_t* x, const float* g, float eps, const uint8_t* Wup,
+                         const float* s_up, const uint8_t* Wgate, const float* s_gate,
+                         const uint8_t* Wdown, const float* s_down, int64_t M, int64_t H,
+                         int64_t F, float* y, const bitnet_ffn_debug* dbg, void* ws,
+                         size_t ws_bytes, void* stream) {
+  if (!x || !g || !Wup || !s_up || !Wgate || !s_gate || !Wdown || !s_down || !y || !ws)
+    return BITNET_ERR_NULL;
+  if (M <= 0 || M > kMaxRows || !valid_inner(H) || !valid_inner(F)) return BITNET_ERR_SHAPE;
+  if (!aligned16(x) || !aligned16(Wup) || !aligned16(Wgate) || !aligned16(Wdown) ||
+      !aligned16(y) || !aligned16(ws))
+    return BITNET_ERR_ALIGN;
+  bitnet_ffn_debug d = {};
+  if (dbg) d = *dbg;
+  if ((d.xq && !aligned16(d.xq)) || (d.u && !aligned16(d.u)) || (d.v && !aligned16(d.v)) ||
+      (d.h && !aligned16(d.h)) || (d.hq && !aligned16(d.hq)) ||
+      (d.acc_down && !aligned16(d.acc_down)))
+    return BITNET_ERR_ALIGN;
+  const FfnLayout L = ffn_layout(M, H, F);
+  if (ws_bytes < L.total) return BITNET_ERR_WORKSPACE;
+  bitnet_status st = check_device();
+  if (st != BITNET_OK) return st;
+
+  char* w = static_cast<char*>(ws);
+  int8_t* xq = d.xq ? d.xq : reinterpret_cast<int8_t*>(w + L.xq);
+  float* sx = d.sx ? d.sx : reinterpret_cast<float*>(w + L.sx);
+  float* u = d.u ? d.u : reinterpret_cast<float*>(w + L.u);
+  float* v = d.v ? d.v : reinterpret_cast<float*>(w + L.v);
+  int8_t* hq = d.hq ? d.hq : reinterpret_cast<int8_t*>(w + L.hq);
+  float* sh = d.sh ? d.sh : reinterpret_cast<float*>(w + L.sh);
+  void* lin = w + L.lin;
+  cudaStream_t s = (cudaStream_t)stream;
+
+  cudaError_t e = bitnet::launch_rmsnorm_quant(x, g, eps, M, H, xq, sx, s);
+  if (e == cudaSuccess) e = run_linear(Wup, s_up, xq, sx, M, F, H, u, nullptr, lin, s);
+  if (e == cudaSuccess) e = run_linear(Wgate, s_gate, xq, sx, M, F, H, v, nullptr, lin, s);
+  if (e == cudaSuccess) e = bitnet::launch_relu2_quant(u, v, M, F, d.h, hq, sh, s);
+  if (e == cudaSuccess) e = run_linear(Wdown, s_down, hq, sh, M, H, F, y, d.acc_down, lin, s);
+  return cuda_status(e);
+}
+
+}  // extern "C"

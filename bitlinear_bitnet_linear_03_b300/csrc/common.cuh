@@ -1,0 +1,120 @@
+// common.cuh — device helpers and the launch functions shared by the
+// library's translation units.  Everything here is internal: the public
+// interface is include/bitnet_b300.h.
+//
+// Floating-point rule for the whole library: every binary32 / binary64 step
+// that decides a stored value is written with an explicit round-to-nearest
+// intrinsic (__fmul_rn, __fdiv_rn, __dadd_rn, ...), and the library is built
+// with -fmad=false, so no multiply-add is ever contracted.  Integer work
+// (codes, dot products, partial sums) is exact by construction.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace bitnet {
+
+// ---------------------------------------------------------------- device helpers
+__device__ __forceinline__ float bf16_bits_to_float(uint32_t b16) {
+  return __uint_as_float(b16 << 16);
+}
+
+// 16-byte streaming load that is not kept in L1 (weights are read once).
+__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
+  uint4 r;
+  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+      : "l"(p));
+  return r;
+}
+
+// Read-only 16-byte load (may be cached).
+__device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
+  uint4 r;
+  asm("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+      : "l"(p));
+  return r;
+}
+
+// acc + sum_t a.byte[t] * b.byte[t], a unsigned bytes, b signed bytes.
+__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int acc) {
+  int d;
+  asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(acc));
+  return d;
+}
+
+// acc + sum_t a.byte[t] * b.byte[t], both signed bytes.
+__device__ __forceinline__ int dp4a_ss(uint32_t a, uint32_t b, int acc) {
+  int d;
+  asm("dp4a.s32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(acc));
+  return d;
+}
+
+__device__ __forceinline__ int warp_sum_i32(int v) {
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+  return v;
+}
+
+// Largest of the lanes' values; fmaxf keeps a non-NaN operand, so a NaN
+// entry never becomes the maximum.
+__device__ __forceinline__ float warp_max_f32(float v) {
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
+  return v;
+}
+
+// round-half-even of v, clipped to [lo, hi]; NaN gives 0.
+__device__ __forceinline__ int round_clip(float v, float lo, float hi) {
+  if (v != v) return 0;
+  float r = rintf(v);
+  r = fminf(fmaxf(r, lo), hi);
+  return (int)r;
+}
+
+// Per-token quantisation constants from the row's largest magnitude a:
+// a' = max(a, 1e-5), inv = 127 / a', scale = a' / 127 (binary32 divisions).
+struct ActScale {
+  float inv;
+  float scale;
+};
+__device__ __forceinline__ ActScale act_scale_from_absmax(float a) {
+  float ap = a > 1e-5f ? a : 1e-5f;
+  ActScale s;
+  s.inv = __fdiv_rn(127.0f, ap);
+  s.scale = __fdiv_rn(ap, 127.0f);
+  return s;
+}
+
+__device__ __forceinline__ uint32_t pack_i8x4(int a, int b, int c, int d) {
+  return (uint32_t)(a & 0xff) | ((uint32_t)(b & 0xff) << 8) | ((uint32_t)(c & 0xff) << 16) |
+         ((uint32_t)(d & 0xff) << 24);
+}
+
+// ---------------------------------------------------------------- launchers
+// Weight quantisation (absmean_weights.cu).
+size_t quantize_weights_workspace(int64_t total);
+cudaError_t launch_quantize_weights(const float* W, int64_t total, uint8_t* Wq, float* w_scale,
+                                    void* ws, cudaStream_t s);
+
+// Activation quantisation (act_quant.cu).
+cudaError_t launch_quantize_act_bf16(const uint16_t* x, int64_t M, int64_t K, int8_t* xq,
+                                     float* x_scale, cudaStream_t s);
+cudaError_t launch_quantize_act_f32(const float* x, int64_t M, int64_t K, int8_t* xq,
+                                    float* x_scale, cudaStream_t s);
+// subln RMSNorm followed by the per-token quantisation (act_quant.cu).
+cudaError_t launch_rmsnorm_quant(const uint16_t* x, const float* g, float eps, int64_t M,
+                                 int64_t H, int8_t* xq, float* x_scale, cudaStream_t s);
+// h = relu(v)^2 * u followed by the per-token quantisation of h (act_quant.cu).
+cudaError_t launch_relu2_quant(const float* u, const float* v, int64_t M, int64_t F, float* h,
+                               int8_t* hq, float* h_scale, cudaStream_t s);
+
+// BitLinear on CUDA cores, any M (gemv.cu).
+size_t gemv_workspace(int64_t M, int64_t N, int64_t K);
+cudaError_t launch_gemv(const uint8_t* Wq, const float* w_scale, const int8_t* xq,
+                        const float* x_scale, int64_t M, int64_t N, int64_t K, float* y,
+                        int32_t* acc_out, void* ws, cudaStream_t s);
+
+}  // namespace bitnet

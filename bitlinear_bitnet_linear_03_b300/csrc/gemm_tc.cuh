@@ -1,0 +1,19 @@
+// gemm_tc.cuh — the tensor-core BitLinear for prefill-sized M (gemm_tc.cu).
+#pragma once
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace bitnet {
+
+// True when (M, N, K) runs on the tensor-core kernel rather than on CUDA cores.
+bool gemm_tc_eligible(int64_t M, int64_t N, int64_t K);
+size_t gemm_tc_workspace(int64_t M, int64_t N, int64_t K);
+cudaError_t launch_gemm_tc(const uint8_t* Wq, const float* w_scale, const int8_t* xq,
+                           const float* x_scale, int64_t M, int64_t N, int64_t K, float* y,
+                           int32_t* acc_out, void* ws, cudaStream_t s);
+
+// Reads and clears the per-device error word that bounded waits set.
+cudaError_t read_and_clear_device_error(int* code, cudaStream_t s);
+
+}  // namespace bitnet

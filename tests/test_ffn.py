@@ -1,0 +1,93 @@
+"""GPU parity of the fused BitNet feed-forward block against the oracle,
+stage by stage (normalised-and-quantised input, up, gate, h, its quantisation,
+the down accumulator) and end to end."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import bitlinear_bitnet_linear_03_b300 as bn
+from bitlinear_bitnet_linear_03_b300 import synth
+from gpu_util import assert_bits_equal, assert_f32_close, dev, dev_bf16, host
+
+pytestmark = pytest.mark.gpu
+
+H, F = 2560, 6912
+
+
+def ffn_inputs(M, seed, H=H, F=F, random_gain=False):
+    Wup = synth.weights_f32(F, H, seed=seed * 10 + 1)
+    Wgate = synth.weights_f32(F, H, seed=seed * 10 + 2)
+    Wdown = synth.weights_f32(H, F, seed=seed * 10 + 3)
+    x = synth.tokens_bf16(M, H, seed=seed * 10 + 4)
+    g = synth.gain_random(H, seed) if random_gain else synth.gain_ones(H)
+    return x, g, [oracle.quantize_weights(W) for W in (Wup, Wgate, Wdown)]
+
+
+def run_gpu(x, g, eps, ws, M, H, F):
+    dbg = dict(xq=torch.empty((M, H), dtype=torch.int8, device="cuda"),
+               sx=torch.empty(M, dtype=torch.float32, device="cuda"),
+               u=torch.empty((M, F), dtype=torch.float32, device="cuda"),
+               v=torch.empty((M, F), dtype=torch.float32, device="cuda"),
+               h=torch.empty((M, F), dtype=torch.float32, device="cuda"),
+               hq=torch.empty((M, F), dtype=torch.int8, device="cuda"),
+               sh=torch.empty(M, dtype=torch.float32, device="cuda"),
+               acc_down=torch.empty((M, H), dtype=torch.int32, device="cuda"))
+    (Wu, su, _), (Wg, sg, _), (Wd, sd, _) = ws
+    f32 = lambda v: dev(np.array([v], np.float32))
+    y = bn.bitnet_ffn(dev_bf16(x), dev(g), eps, dev(Wu), f32(su), dev(Wg), f32(sg), dev(Wd),
+                      f32(sd), debug=dbg)
+    out = {k: host(v) for k, v in dbg.items()}
+    out["y"] = host(y)
+    return out
+
+
+def check_ffn(M, seed, H=H, F=F, random_gain=False, eps=1e-5):
+    x, g, ws = ffn_inputs(M, seed, H, F, random_gain)
+    got = run_gpu(x, g, eps, ws, M, H, F)
+    (Wu, su, _), (Wg, sg, _), (Wd, sd, _) = ws
+    want = oracle.ffn(x, g, eps, Wu, su, Wg, sg, Wd, sd, threads=oracle.default_threads())
+    # stage-wise: each stage of the oracle fed the GPU's previous stage
+    n, _ = oracle.rmsnorm_bf16(x, g, eps)
+    xq_o, sx_o = oracle.quantize_act_f32(n)
+    assert_bits_equal(got["sx"], sx_o, "sx")
+    assert_bits_equal(got["xq"], xq_o, "xq")
+    u_o, _ = oracle.linear(Wu, su, got["xq"], got["sx"], H)
+    v_o, _ = oracle.linear(Wg, sg, got["xq"], got["sx"], H)
+    assert_bits_equal(got["u"], u_o, "u")
+    assert_bits_equal(got["v"], v_o, "v")
+    h_o = oracle.relu2_mul(got["u"], got["v"])
+    assert_bits_equal(got["h"], h_o, "h")
+    hq_o, sh_o = oracle.quantize_act_f32(got["h"])
+    assert_bits_equal(got["sh"], sh_o, "sh")
+    assert_bits_equal(got["hq"], hq_o, "hq")
+    y_o, acc_o = oracle.linear(Wd, sd, got["hq"], got["sh"], F)
+    assert_bits_equal(got["acc_down"], acc_o, "acc_down")
+    # end to end
+    assert_f32_close(got["y"], want["y"], "y")
+    assert_bits_equal(got["y"], want["y"], "y bits")
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_ffn_seq1(seed):
+    check_ffn(1, seed)
+
+
+@pytest.mark.parametrize("M", [3, 64])
+def test_ffn_small_batches(M):
+    check_ffn(M, 0, random_gain=True)
+
+
+def test_ffn_ragged_dims():
+    check_ffn(5, 1, H=192, F=320, random_gain=True)
+
+
+def test_ffn_without_debug_matches():
+    M = 2
+    x, g, ws = ffn_inputs(M, 3)
+    (Wu, su, _), (Wg, sg, _), (Wd, sd, _) = ws
+    f32 = lambda v: dev(np.array([v], np.float32))
+    y = host(bn.bitnet_ffn(dev_bf16(x), dev(g), 1e-5, dev(Wu), f32(su), dev(Wg), f32(sg),
+                           dev(Wd), f32(sd)))
+    want = oracle.ffn(x, g, 1e-5, Wu, su, Wg, sg, Wd, sd)
+    assert_bits_equal(y, want["y"], "y")

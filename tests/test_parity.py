@@ -1,0 +1,235 @@
+"""GPU parity: every C-ABI call against the CPU oracle on the same seeded
+inputs.  Integer outputs (packed bytes, int8 codes, int32 accumulators) and
+the scales must match bit for bit; fp32 outputs must be within a relative
+1e-5 (they are expected to match bit for bit as well).  Sizes span several
+tiles and ragged tails; the full workload sizes are checked on sampled rows
+that the oracle computes one by one."""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import bitlinear_bitnet_linear_03_b300 as bn
+from bitlinear_bitnet_linear_03_b300 import synth
+from gpu_util import assert_bits_equal, assert_f32_close, dev, dev_bf16, host
+
+pytestmark = pytest.mark.gpu
+
+GOLD = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "worked_examples.json")))
+
+
+# ---------------------------------------------------------------- weights
+def gpu_quantize_weights(W: np.ndarray):
+    Wq, ws = bn.bitnet_quantize_weights(dev(W))
+    return host(Wq), host(ws)[0]
+
+
+def check_weights(W: np.ndarray, what: str):
+    Wq_g, s_g = gpu_quantize_weights(W)
+    Wq_o, s_o, _ = oracle.quantize_weights(W)
+    assert_bits_equal(np.array([s_g], np.float32), np.array([s_o], np.float32), what + " w_scale")
+    assert_bits_equal(Wq_g, Wq_o, what + " Wq")
+
+
+@pytest.mark.parametrize("N,K", [(1, 64), (3, 192), (17, 640), (33, 128), (640, 2560),
+                                 (2560, 2560), (6912, 2560), (2560, 6912)])
+def test_quantize_weights_seeded(N, K):
+    check_weights(synth.weights_f32(N, K, seed=N + K), f"W[{N}x{K}]")
+
+
+def test_quantize_weights_worked_examples():
+    # The 2x4 tie example, laid into the first columns of a 2x64 matrix whose
+    # other entries are chosen so that the mean stays 2: |W| sums to 256.
+    W = np.zeros((2, 64), np.float32)
+    W[:, :4] = np.array(GOLD["weights_ties"]["W"], np.float32)
+    W[:, 4:] = np.float32(2.0)          # sum|W| = 16 + 120*2 = 256 = 2 * 128
+    Wq_g, s_g = gpu_quantize_weights(W)
+    assert s_g == np.float32(2.0)
+    q = oracle.unpack(Wq_g, 64)
+    assert q[:, :4].tolist() == GOLD["weights_ties"]["q"]
+    assert (q[:, 4:] == 1).all()
+    check_weights(W, "ties")
+
+
+def test_quantize_weights_special_cases():
+    check_weights(np.zeros((3, 64), np.float32), "zeros")
+    rng = np.random.default_rng(0)
+    s = rng.choice([-1.0, 1.0], size=(32, 128)).astype(np.float32)
+    check_weights(s * np.float32(0.25), "sign pattern")
+    # mixed magnitudes: subnormals to 1e38, so any float sum order would round
+    W = (rng.standard_normal((64, 256)) * np.exp2(rng.integers(-140, 120, (64, 256)))).astype(
+        np.float32)
+    check_weights(W, "mixed exponents")
+    W = np.full((7, 64), 1e-44, np.float32)
+    check_weights(W, "subnormal only")
+    # exact half-ties of the scale in every position
+    W = np.ones((16, 64), np.float32)
+    W[::2, ::3] = 0.5
+    W[1::2, ::5] = -1.5
+    check_weights(W, "half ties")
+
+
+@pytest.mark.parametrize("bad", [np.inf, -np.inf, np.nan])
+def test_quantize_weights_nonfinite(bad):
+    W = synth.weights_f32(5, 128, seed=3)
+    W[2, 77] = bad
+    Wq_g, s_g = gpu_quantize_weights(W)
+    assert np.isnan(s_g)
+    assert (Wq_g == 0x55).all()
+
+
+def test_quantize_weights_full_100b_shape_sampled():
+    N, K = 28672, 8192
+    W = synth.weights_f32(N, K, seed=0)
+    Wq_g, s_g = gpu_quantize_weights(W)
+    gamma = oracle.absmean(W)
+    rows = np.random.default_rng(0).choice(N, 64, replace=False)
+    rows[:2] = [0, N - 1]
+    q, s_o = oracle.ternarize(W[rows], gamma)
+    assert_bits_equal(np.array([s_g], np.float32), np.array([s_o], np.float32), "w_scale")
+    assert_bits_equal(Wq_g[rows], oracle.pack(q), "sampled Wq rows")
+
+
+# ---------------------------------------------------------------- activations
+def check_act(x_bits: np.ndarray, what: str):
+    xq, sx = bn.bitnet_quantize_act(dev_bf16(x_bits))
+    q_o, s_o = oracle.quantize_act_bf16(x_bits)
+    assert_bits_equal(host(sx), s_o, what + " x_scale")
+    assert_bits_equal(host(xq), q_o, what + " xq")
+
+
+@pytest.mark.parametrize("M,K,frac", [(1, 64, 0), (3, 2560, 0), (1, 2560, 0.01), (64, 6912, 0.01),
+                                      (5, 28672, 0.01), (4096, 2560, 0), (4096, 6912, 0),
+                                      (2, 65536, 0.01)])
+def test_quantize_act_seeded(M, K, frac):
+    check_act(synth.tokens_bf16(M, K, seed=M + K, outlier_frac=frac), f"x[{M}x{K}]")
+
+
+def test_quantize_act_worked_example_and_special_rows():
+    x = np.zeros((4, 64), np.float32)
+    x[0, :4] = GOLD["act_ties"]["x"]
+    x[2, :] = 1.0
+    x[3, 5] = -3.0
+    bits = synth.f32_to_bf16_bits(x)
+    xq, sx = bn.bitnet_quantize_act(dev_bf16(bits))
+    q = host(xq)
+    assert q[0, :4].tolist() == GOLD["act_ties"]["q"] and host(sx)[0] == np.float32(1.0)
+    assert (q[1] == 0).all()                          # all-zero token
+    assert (q[2] == 127).all() and (q[3, 5] == -127)
+    check_act(bits, "special rows")
+
+
+def test_quantize_act_nonfinite():
+    bits = synth.tokens_bf16(3, 128, seed=5)
+    bits[0, 3] = 0x7f80  # +inf
+    bits[1, 9] = 0x7fc0  # nan
+    check_act(bits, "non-finite")
+
+
+# ---------------------------------------------------------------- linear
+def linear_inputs(M, N, K, seed, frac=0.0):
+    W = synth.weights_f32(N, K, seed=seed)
+    x = synth.tokens_bf16(M, K, seed=seed + 1000, outlier_frac=frac)
+    Wq, ws, _ = oracle.quantize_weights(W)
+    qx, sx = oracle.quantize_act_bf16(x)
+    return Wq, ws, qx, sx
+
+
+def gpu_linear(Wq, ws, qx, sx, K):
+    M, N = qx.shape[0], Wq.shape[0]
+    acc = torch.empty((M, N), dtype=torch.int32, device="cuda")
+    y = bn.bitnet_linear(dev(Wq), dev(np.array([ws], np.float32)), dev(qx), dev(sx), K=K,
+                         acc_out=acc)
+    return host(y), host(acc)
+
+
+LINEAR_SHAPES = [(1, 1, 64), (1, 7, 64), (2, 65, 192), (3, 640, 2560), (1, 2560, 2560),
+                 (5, 2560, 2560), (8, 6912, 2560), (1, 2560, 6912), (17, 2560, 6912),
+                 (4, 100, 8192), (63, 96, 2560), (64, 33, 128), (65, 130, 640), (129, 64, 320),
+                 (1, 31, 65536)]
+
+
+@pytest.mark.parametrize("M,N,K", LINEAR_SHAPES)
+def test_linear_seeded(M, N, K):
+    Wq, ws, qx, sx = linear_inputs(M, N, K, seed=M * 7 + N, frac=0.01)
+    y_g, acc_g = gpu_linear(Wq, ws, qx, sx, K)
+    y_o, acc_o = oracle.linear(Wq, ws, qx, sx, K)
+    assert_bits_equal(acc_g, acc_o, "acc")
+    assert_f32_close(y_g, y_o, "y")
+    assert_bits_equal(y_g, y_o, "y bits")
+
+
+def test_linear_worked_example():
+    g = GOLD["linear"]
+    q = np.zeros((2, 64), np.int8)
+    q[:, :4] = np.array(g["qw"], np.int8)
+    qx = np.zeros((1, 64), np.int8)
+    qx[0, :4] = g["qx"]
+    y, acc = gpu_linear(oracle.pack(q), np.float32(g["w_scale"]), qx,
+                        np.array([g["sx"]], np.float32), 64)
+    assert acc.ravel().tolist() == g["acc"]
+    assert y.ravel().tolist() == g["y"]
+
+
+def test_linear_extreme_accumulators():
+    K = 65536
+    q = np.ones((2, K), np.int8)
+    q[1] = -1
+    qx = np.full((1, K), -128, np.int8)
+    y, acc = gpu_linear(oracle.pack(q), np.float32(1.0), qx, np.array([1.0], np.float32), K)
+    assert acc.ravel().tolist() == [-128 * K, 128 * K]
+
+
+@pytest.mark.parametrize("M", [1, 4, 16, 64])
+@pytest.mark.parametrize("N,K", [(28672, 8192), (8192, 28672)])
+def test_linear_100b_shapes_sampled(M, N, K):
+    W = synth.weights_f32(N, K, seed=11)
+    x = synth.tokens_bf16(M, K, seed=12, outlier_frac=0.01)
+    Wq_d, ws_d = bn.bitnet_quantize_weights(dev(W))
+    xq_d, sx_d = bn.bitnet_quantize_act(dev_bf16(x))
+    acc = torch.empty((M, N), dtype=torch.int32, device="cuda")
+    y = host(bn.bitnet_linear(Wq_d, ws_d, xq_d, sx_d, acc_out=acc))
+    acc = host(acc)
+    gamma = oracle.absmean(W)
+    rows = np.random.default_rng(M).choice(N, 48, replace=False)
+    rows[:2] = [0, N - 1]
+    q, ws = oracle.ternarize(W[rows], gamma)
+    qx, sx = oracle.quantize_act_bf16(x)
+    y_o, acc_o = oracle.linear(oracle.pack(q), ws, qx, sx, K)
+    assert_bits_equal(acc[:, rows], acc_o, "acc sampled")
+    assert_f32_close(y[:, rows], y_o, "y sampled")
+    assert_bits_equal(y[:, rows], y_o, "y sampled bits")
+
+
+@pytest.mark.parametrize("N,K", [(6912, 2560), (2560, 6912)])
+def test_linear_prefill_shapes_sampled(N, K):
+    M = 4096
+    W = synth.weights_f32(N, K, seed=21)
+    x = synth.tokens_bf16(M, K, seed=22)
+    Wq, ws, _ = oracle.quantize_weights(W)
+    qx, sx = oracle.quantize_act_bf16(x)
+    y_g, acc_g = gpu_linear(Wq, ws, qx, sx, K)
+    rows = np.random.default_rng(1).choice(N, 24, replace=False)
+    rows[:2] = [0, N - 1]
+    y_o, acc_o = oracle.linear(Wq[rows], ws, qx, sx, K, threads=oracle.default_threads())
+    assert_bits_equal(acc_g[:, rows], acc_o, "acc sampled")
+    assert_bits_equal(y_g[:, rows], y_o, "y sampled bits")
+    # every output row: the properties that hold at any size
+    assert np.isfinite(y_g).all()
+    assert (np.abs(acc_g) <= 127 * K).all()
+
+
+def test_quantize_then_linear_chain():
+    M, N, K = 3, 2560, 2560
+    W = synth.weights_f32(N, K, seed=31)
+    x = synth.tokens_bf16(M, K, seed=32, outlier_frac=0.01)
+    Wq_d, ws_d = bn.bitnet_quantize_weights(dev(W))
+    xq_d, sx_d = bn.bitnet_quantize_act(dev_bf16(x))
+    y = host(bn.bitnet_linear(Wq_d, ws_d, xq_d, sx_d))
+    Wq, ws, _ = oracle.quantize_weights(W)
+    qx, sx = oracle.quantize_act_bf16(x)
+    y_o, _ = oracle.linear(Wq, ws, qx, sx, K)
+    assert_bits_equal(y, y_o, "chain y")
