@@ -46,19 +46,25 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--layers", type=int, default=30)
     ap.add_argument("--impl", default="b300", choices=["b300", "reference"])
+    ap.add_argument("--api", default="fused", choices=["fused", "split"],
+                    help="fused: bitnet_linear_bf16 per shared input (3 launches a layer); "
+                         "split: bitnet_quantize_act + bitnet_linear per matrix")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-secondary", action="store_true")
     return ap.parse_args()
 
 
-def layer_bytes():
-    """Algorithmic bytes of one layer: act-quant reads bf16 and writes int8 +
-    scale; each BitLinear reads packed W, int8 x, two scales, writes fp32 y."""
+def layer_bytes(api="fused"):
+    """Algorithmic bytes of one layer.
+    fused: each of the three calls reads its bf16 input once; each BitLinear
+           reads packed W and its scale and writes fp32 y.
+    split: act-quant reads bf16 and writes int8 + scale; each BitLinear reads
+           packed W, int8 x, two scales and writes fp32 y."""
     b = 0
     for _, K in INPUTS:
-        b += 2 * K + K + 4
+        b += 2 * K if api == "fused" else 2 * K + K + 4
     for _, N, K, _ in LAYER_SHAPES:
-        b += N * K // 4 + K + 8 + 4 * N
+        b += N * K // 4 + 4 + 4 * N if api == "fused" else N * K // 4 + K + 8 + 4 * N
     return b
 
 
@@ -118,11 +124,11 @@ class ClockSampler:
 class DecodeStep:
     """Resident weights, inputs, outputs and workspaces of the decode step."""
 
-    def __init__(self, layers, seed=0):
+    def __init__(self, layers, api="fused", seed=0):
         import torch
         import bitlinear_bitnet_linear_03_b300 as bn
         from bitlinear_bitnet_linear_03_b300 import synth
-        self.torch, self.bn = torch, bn
+        self.torch, self.bn, self.api = torch, bn, api
         dev = torch.device("cuda")
         self.layers = []
         ws_q = torch.empty(bn.bitnet_quantize_weights_workspace(FFN, HIDDEN) * 2,
@@ -157,11 +163,23 @@ class DecodeStep:
                 self.bn.bitnet_linear(Wq, s, L["xq"][src], L["sx"][src], K=K, y=L["y"][name],
                                       ws=self.lin_ws)
 
+    def fused(self):
+        for L in self.layers:
+            for src, _ in INPUTS:
+                targets = [(L["W"][n][0], L["W"][n][1], L["y"][n])
+                           for n, _, _, s in LAYER_SHAPES if s == src]
+                self.bn.bitnet_linear_bf16(L["x"][src], targets)
+
     def step(self):
-        self.quantize_inputs()
-        self.linears()
+        if self.api == "fused":
+            self.fused()
+        else:
+            self.quantize_inputs()
+            self.linears()
 
     def launches_per_step(self):
+        if self.api == "fused":
+            return len(INPUTS) * len(self.layers)
         n = 0
         for _ in self.layers:
             n += len(INPUTS)
@@ -279,9 +297,8 @@ def run_gpu_arm(args, rank, world, barrier, max_over_ranks):
     import bitlinear_bitnet_linear_03_b300 as bn
     torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
     bn.lib()
-    step = DecodeStep(args.layers)
+    step = DecodeStep(args.layers, api=args.api)
     graph = capture(torch, step.step)
-    lin_graph = capture(torch, step.linears)
 
     clocks = ClockSampler(torch.cuda.current_device())
     clocks.start()
@@ -290,7 +307,7 @@ def run_gpu_arm(args, rank, world, barrier, max_over_ranks):
     clk = clocks.stop()
     dt = max_over_ranks(dt)
 
-    bytes_step = layer_bytes() * args.layers
+    bytes_step = layer_bytes(args.api) * args.layers
     value = bytes_step * args.steps * world / dt / 1e9
 
     # e2e: pinned-host inputs copied in and outputs copied out every step.
@@ -320,19 +337,25 @@ def run_gpu_arm(args, rank, world, barrier, max_over_ranks):
     e2e_value = bytes_step * e2e_steps * world / t_e2e / 1e9
 
     # Dominant kernel: the BitLinear launches alone, graph-replayed; average
-    # launch duration = replay time / launches.
-    lin_launches = step.launches_per_step() - len(INPUTS) * args.layers
+    # launch duration = replay time / launches (consecutive launches overlap
+    # under programmatic dependent launch, so this is the effective duration).
+    if args.api == "fused":
+        lin_graph, lin_launches = graph, step.launches_per_step()
+        lin_bytes = bytes_step
+    else:
+        lin_graph = capture(torch, step.linears)
+        lin_launches = step.launches_per_step() - len(INPUTS) * args.layers
+        lin_bytes = sum(N * K // 4 + K + 8 + 4 * N for _, N, K, _ in LAYER_SHAPES) * args.layers
     reps = max(20, min(args.steps, 400))
     t_lin = time_graph(torch, lin_graph, reps, 5, lambda: None)
     per_launch_s = t_lin / reps / lin_launches
-    lin_bytes = sum(N * K // 4 + K + 8 + 4 * N for _, N, K, _ in LAYER_SHAPES) * args.layers
     achieved = lin_bytes / lin_launches / per_launch_s / 1e9
     peaks = read_peaks()
     if peaks and peaks.get("hbm_gbs"):
         peak, peak_src = float(peaks["hbm_gbs"]), "measured"
     else:
         peak, peak_src = 6400.0, "fallback"
-    traffic = profiled_traffic("bitlinear_bitnet_linear_03_b300/csrc/gemv.cu",
+    traffic = profiled_traffic("bitlinear_bitnet_linear_03_b300/csrc/gemv_decode.cu",
                                "profiles/gemv_decode_2b_30layers.md")
 
     result = {
@@ -346,11 +369,14 @@ def run_gpu_arm(args, rank, world, barrier, max_over_ranks):
                    "algorithmic_bytes_per_step": bytes_step,
                    "l2": "inputs larger than L2 (521 MB of weights per step vs 126 MB L2)",
                    "graph": "whole step captured in one CUDA graph",
+                   "api": args.api,
                    "parallelism": f"replicas x{world}"},
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps},
         "gpu_launches": step.launches_per_step() * args.steps,
-        "roofline": {"bound": "hbm", "kernel": "bitnet_linear GEMV (k_gemv + split-K reduce)",
+        "roofline": {"bound": "hbm",
+                     "kernel": "k_gemv_decode (bitnet_linear_bf16)" if args.api == "fused"
+                     else "bitnet_linear GEMV",
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_source": peak_src,
                      "traffic": traffic, "launch_us": round(per_launch_s * 1e6, 3),
@@ -382,13 +408,13 @@ class OracleSample:
         q = {}
         for n, _ in INPUTS:
             q[n] = self.oracle.quantize_act_bf16(self.x[n])
-        nbytes = sum(2 * K + K + 4 for _, K in INPUTS)
+        nbytes = sum(2 * K for _, K in INPUTS)
         for name in names:
             Wq, s, N, K = self.W[name]
             src = dict((a, d) for a, _, _, d in LAYER_SHAPES)[name]
             qx, sx = q[src]
             self.oracle.linear(Wq, s, qx, sx, K, threads=threads)
-            nbytes += N * K // 4 + K + 8 + 4 * N
+            nbytes += N * K // 4 + 4 + 4 * N
         return nbytes
 
 
@@ -406,7 +432,7 @@ def cpu_baseline(budget_s=12.0):
     return {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": threads,
             "kind": "oracle",
             "sample": f"{layers} repetitions of one decode layer (3 act quants + 7 BitLinear, "
-                      f"{layer_bytes()} algorithmic bytes each) of the 30-layer step, "
+                      f"{layer_bytes('fused')} algorithmic bytes each) of the 30-layer step, "
                       f"{dt:.1f} s"}
 
 

@@ -33,6 +33,7 @@ SIGNATURES = {
     "bitnet_quantize_act": (_INT, [_P, _I64, _I64, _P, _P, _P]),
     "bitnet_linear_workspace": (_SZ, [_I64, _I64, _I64]),
     "bitnet_linear": (_INT, [_P, _P, _P, _P, _I64, _I64, _I64, _P, _P, _P, _SZ, _P]),
+    "bitnet_linear_bf16": (_INT, [_P, _I64, _I64, _P, _INT, _P, _P, _P]),
     "bitnet_ffn_workspace": (_SZ, [_I64, _I64, _I64]),
     "bitnet_ffn": (_INT, [_P, _P, _F, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _P, _P, _SZ,
                           _P]),
@@ -46,6 +47,11 @@ class BitnetError(RuntimeError):
         if status == 6:
             msg += f", cudaError {cuda_error}"
         super().__init__(msg)
+
+
+class LinearTarget(ctypes.Structure):
+    """bitnet_linear_target: one weight matrix of a grouped decode call."""
+    _fields_ = [("Wq", _P), ("w_scale", _P), ("N", _I64), ("y", _P), ("acc_out", _P)]
 
 
 class FfnDebug(ctypes.Structure):
@@ -167,6 +173,26 @@ def bitnet_linear(Wq, w_scale, xq, x_scale, K=None, y=None, acc_out=None, ws=Non
         _ptr(y, torch.float32, "y"), _ptr(acc_out, torch.int32, "acc_out"),
         _ptr(ws, name="ws"), nb, _stream(stream)))
     return y
+
+
+def bitnet_linear_bf16(x, targets, xq_out=None, x_scale_out=None, stream=None):
+    """Per-token int8 quantisation of bf16 x [M, K] and BitLinear with every
+    (Wq, w_scale, y[, acc_out]) in `targets` (all sharing x), one launch."""
+    M, K = x.shape
+    arr = (LinearTarget * len(targets))()
+    keep = []
+    for i, t in enumerate(targets):
+        Wq, ws, y = t[0], t[1], t[2]
+        acc = t[3] if len(t) > 3 else None
+        arr[i] = LinearTarget(_ptr(Wq, torch.uint8, "Wq"), _ptr(ws, torch.float32, "w_scale"),
+                              Wq.shape[0], _ptr(y, torch.float32, "y"),
+                              _ptr(acc, torch.int32, "acc_out"))
+        keep.append(t)
+    _check("bitnet_linear_bf16", lib().bitnet_linear_bf16(
+        _ptr(x, torch.bfloat16, "x"), M, K, arr, len(targets),
+        _ptr(xq_out, torch.int8, "xq_out"), _ptr(x_scale_out, torch.float32, "x_scale_out"),
+        _stream(stream)))
+    return [t[2] for t in targets]
 
 
 # ------------------------------------------------------------------ FFN

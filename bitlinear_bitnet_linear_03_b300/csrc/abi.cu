@@ -47,6 +47,7 @@ constexpr int64_t kMaxRows = 4096 * 64;
 bool valid_inner(int64_t K) { return K > 0 && K % 64 == 0 && K <= BITNET_MAX_K; }
 
 size_t linear_ws(int64_t M, int64_t N, int64_t K) {
+  if (bitnet::decode_supported(M, K)) return 0;
   if (bitnet::gemm_tc_eligible(M, N, K)) return bitnet::gemm_tc_workspace(M, N, K);
   return bitnet::gemv_workspace(M, N, K);
 }
@@ -54,6 +55,10 @@ size_t linear_ws(int64_t M, int64_t N, int64_t K) {
 cudaError_t run_linear(const uint8_t* Wq, const float* w_scale, const int8_t* xq,
                        const float* x_scale, int64_t M, int64_t N, int64_t K, float* y,
                        int32_t* acc_out, void* ws, cudaStream_t s) {
+  if (bitnet::decode_supported(M, K)) {
+    bitnet::DecodeTarget t = {Wq, w_scale, N, y, acc_out};
+    return bitnet::launch_decode(&t, 1, xq, x_scale, nullptr, M, K, nullptr, nullptr, s);
+  }
   if (bitnet::gemm_tc_eligible(M, N, K))
     return bitnet::launch_gemm_tc(Wq, w_scale, xq, x_scale, M, N, K, y, acc_out, ws, s);
   return bitnet::launch_gemv(Wq, w_scale, xq, x_scale, M, N, K, y, acc_out, ws, s);
@@ -159,6 +164,32 @@ bitnet_status bitnet_linear(const uint8_t* Wq, const float* w_scale, const int8_
   if (st != BITNET_OK) return st;
   return cuda_status(
       run_linear(Wq, w_scale, xq, x_scale, M, N, K, y, acc_out, ws, (cudaStream_t)stream));
+}
+
+bitnet_status bitnet_linear_bf16(const uint16_t* x, int64_t M, int64_t K,
+                                 const bitnet_linear_target* targets, int count, int8_t* xq_out,
+                                 float* x_scale_out, void* stream) {
+  if (!x || !targets) return BITNET_ERR_NULL;
+  if (count < 1 || count > BITNET_MAX_TARGETS || M < 1 || M > BITNET_DECODE_MAX_M ||
+      !valid_inner(K) || !bitnet::decode_supported(M, K))
+    return BITNET_ERR_SHAPE;
+  if (!aligned16(x) || (xq_out && !aligned16(xq_out))) return BITNET_ERR_ALIGN;
+  bitnet::DecodeTarget t[BITNET_MAX_TARGETS];
+  int64_t rows = 0;
+  for (int i = 0; i < count; ++i) {
+    const bitnet_linear_target& g = targets[i];
+    if (!g.Wq || !g.w_scale || !g.y) return BITNET_ERR_NULL;
+    if (g.N < 1) return BITNET_ERR_SHAPE;
+    if (!aligned16(g.Wq) || !aligned16(g.y) || (g.acc_out && !aligned16(g.acc_out)))
+      return BITNET_ERR_ALIGN;
+    rows += g.N;
+    t[i] = {g.Wq, g.w_scale, g.N, g.y, g.acc_out};
+  }
+  if (rows > (1 << 30)) return BITNET_ERR_SHAPE;
+  bitnet_status st = check_device();
+  if (st != BITNET_OK) return st;
+  return cuda_status(bitnet::launch_decode(t, count, nullptr, nullptr, x, M, K, xq_out,
+                                           x_scale_out, (cudaStream_t)stream));
 }
 
 size_t bitnet_ffn_workspace(int64_t M, int64_t H, int64_t F) {

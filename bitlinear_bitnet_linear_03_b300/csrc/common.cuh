@@ -52,6 +52,23 @@ __device__ __forceinline__ int dp4a_ss(uint32_t a, uint32_t b, int acc) {
   return d;
 }
 
+// Programmatic dependent launch.  A kernel launched with the programmatic
+// stream-serialisation attribute may start before its predecessor in the
+// stream has finished; griddep_wait() blocks until that predecessor's memory
+// operations are complete and visible, so every kernel of this library calls
+// it before reading or writing anything the predecessor may touch.
+// griddep_launch_dependents() lets the successor start launching early.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Asks the copy engine to bring [p, p + bytes) into L2 (a hint: no data is
+// returned and nothing is written).  p and bytes must be multiples of 16.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ int warp_sum_i32(int v) {
 #pragma unroll
   for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
@@ -94,6 +111,25 @@ __device__ __forceinline__ uint32_t pack_i8x4(int a, int b, int c, int d) {
 }
 
 // ---------------------------------------------------------------- launchers
+// Launches `kernel` on `s` with programmatic stream serialisation allowed, so
+// it may overlap the tail of the previous kernel on the stream (the kernel
+// itself calls griddep_wait() before touching dependent data).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // Weight quantisation (absmean_weights.cu).
 size_t quantize_weights_workspace(int64_t total);
 cudaError_t launch_quantize_weights(const float* W, int64_t total, uint8_t* Wq, float* w_scale,
@@ -110,6 +146,25 @@ cudaError_t launch_rmsnorm_quant(const uint16_t* x, const float* g, float eps, i
 // h = relu(v)^2 * u followed by the per-token quantisation of h (act_quant.cu).
 cudaError_t launch_relu2_quant(const float* u, const float* v, int64_t M, int64_t F, float* h,
                                int8_t* hq, float* h_scale, cudaStream_t s);
+
+// Decode BitLinear (M <= 4) on CUDA cores: one launch for up to
+// kDecodeMaxTargets weight matrices sharing the same input, which is either
+// int8 (xq, x_scale) or bf16 (quantised per token inside the kernel, bit for
+// bit as launch_quantize_act_bf16).  Returns cudaErrorNotSupported when the
+// shape is outside what the kernel handles (gemv_decode.cu).
+constexpr int kDecodeMaxTargets = 8;
+constexpr int kDecodeMaxM = 4;
+struct DecodeTarget {
+  const uint8_t* Wq;
+  const float* w_scale;
+  int64_t N;
+  float* y;
+  int32_t* acc_out;
+};
+bool decode_supported(int64_t M, int64_t K);
+cudaError_t launch_decode(const DecodeTarget* targets, int count, const int8_t* xq,
+                          const float* x_scale, const uint16_t* x_bf16, int64_t M, int64_t K,
+                          int8_t* xq_out, float* x_scale_out, cudaStream_t s);
 
 // BitLinear on CUDA cores, any M (gemv.cu).
 size_t gemv_workspace(int64_t M, int64_t N, int64_t K);

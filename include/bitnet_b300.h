@@ -124,6 +124,34 @@ bitnet_status bitnet_linear(const uint8_t* Wq, const float* w_scale,
                             void* ws, size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
+ * Decode BitLinear from bf16 activations ([P1] W1.58A8; [P3] §3.1).
+ * For up to BITNET_MAX_TARGETS weight matrices that share the same input
+ * (e.g. the Q, K, V, up and gate projections of one token), in one launch:
+ *   xq, sx  = per-token int8 quantisation of x (the rule of
+ *             bitnet_quantize_act, bit for bit);
+ *   y_i     = BitLinear(Wq_i, w_scale_i; xq, sx)  (the rule of bitnet_linear).
+ * x: [M, K] bf16, 1 <= M <= BITNET_DECODE_MAX_M.  targets[i]: Wq [N_i, K/4]
+ * packed, w_scale [1], y [M, N_i] float, acc_out optional [M, N_i] int32.
+ * xq_out [M, K] and x_scale_out [M] are optional copies of xq and sx.
+ * K % 64 == 0; K <= 65536 for M = 1, 32768 for M = 2, 16384 for M <= 4
+ * (BITNET_ERR_SHAPE beyond); sum of N_i <= 2^30.  Needs no workspace.  The
+ * kernel may start while the previous kernel on `stream` is finishing
+ * (programmatic dependent launch) and waits for it before reading x. */
+#define BITNET_DECODE_MAX_M 4
+#define BITNET_MAX_TARGETS 8
+typedef struct bitnet_linear_target {
+  const uint8_t* Wq;
+  const float* w_scale;
+  int64_t N;
+  float* y;
+  int32_t* acc_out;
+} bitnet_linear_target;
+
+bitnet_status bitnet_linear_bf16(const uint16_t* x, int64_t M, int64_t K,
+                                 const bitnet_linear_target* targets, int count,
+                                 int8_t* xq_out, float* x_scale_out, void* stream);
+
+/* ------------------------------------------------------------------------
  * Fused BitNet feed-forward block ([P1] subln, ReLU^2, no bias):
  *   r   = (float)(1 / sqrt(ss / H + eps)), ss = sum x^2 (binary64, in the
  *         order: 32 strided partial sums over k = l (mod 32), increasing k,

@@ -23,6 +23,8 @@ def host(t: torch.Tensor) -> np.ndarray:
 
 def assert_bits_equal(got: np.ndarray, want: np.ndarray, what: str):
     assert got.shape == want.shape, (what, got.shape, want.shape)
+    got = np.ascontiguousarray(got)
+    want = np.ascontiguousarray(want)
     bad = np.nonzero(got.view(np.uint8).reshape(got.shape + (-1,)) !=
                      want.view(np.uint8).reshape(want.shape + (-1,)))
     if bad[0].size:

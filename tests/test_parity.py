@@ -233,3 +233,47 @@ def test_quantize_then_linear_chain():
     qx, sx = oracle.quantize_act_bf16(x)
     y_o, _ = oracle.linear(Wq, ws, qx, sx, K)
     assert_bits_equal(y, y_o, "chain y")
+
+
+# ---------------------------------------------------------------- grouped decode from bf16
+def check_linear_bf16(M, K, Ns, seed, frac=0.01):
+    x = synth.tokens_bf16(M, K, seed=seed, outlier_frac=frac)
+    packs = [oracle.quantize_weights(synth.weights_f32(N, K, seed=seed + 1 + i))
+             for i, N in enumerate(Ns)]
+    targets = []
+    for (Wq, ws, _), N in zip(packs, Ns):
+        targets.append((dev(Wq), dev(np.array([ws], np.float32)),
+                        torch.empty((M, N), dtype=torch.float32, device="cuda"),
+                        torch.empty((M, N), dtype=torch.int32, device="cuda")))
+    xq_out = torch.empty((M, K), dtype=torch.int8, device="cuda")
+    xs_out = torch.empty(M, dtype=torch.float32, device="cuda")
+    bn.bitnet_linear_bf16(dev_bf16(x), targets, xq_out, xs_out)
+    qx, sx = oracle.quantize_act_bf16(x)
+    assert_bits_equal(host(xq_out), qx, "xq_out")
+    assert_bits_equal(host(xs_out), sx, "x_scale_out")
+    for i, ((Wq, ws, _), t) in enumerate(zip(packs, targets)):
+        y_o, acc_o = oracle.linear(Wq, ws, qx, sx, K)
+        assert_bits_equal(host(t[3]), acc_o, f"acc target {i}")
+        assert_bits_equal(host(t[2]), y_o, f"y target {i}")
+
+
+@pytest.mark.parametrize("M", [1, 2, 3, 4])
+def test_linear_bf16_decode_layer_group(M):
+    # Q, K, V, up, gate of a 2B-class layer share one input
+    check_linear_bf16(M, 2560, [2560, 640, 640, 6912, 6912], seed=40 + M)
+
+
+@pytest.mark.parametrize("M,K,Ns", [(1, 64, [1]), (1, 6912, [2560]), (2, 6912, [33, 2560]),
+                                    (1, 28672, [8192]), (2, 28672, [100]), (4, 16384, [77]),
+                                    (3, 192, [5, 6, 7, 8, 9, 10, 11, 12]), (1, 65536, [40])])
+def test_linear_bf16_shapes(M, K, Ns):
+    check_linear_bf16(M, K, Ns, seed=M * 3 + K)
+
+
+def test_linear_bf16_rejects_unsupported():
+    x = torch.zeros((4, 32768), dtype=torch.bfloat16, device="cuda")
+    Wq = torch.zeros((1, 8192), dtype=torch.uint8, device="cuda")
+    t = [(Wq, torch.ones(1, device="cuda"), torch.empty((4, 1), device="cuda"))]
+    with pytest.raises(bn.BitnetError) as e:
+        bn.bitnet_linear_bf16(x, t)
+    assert e.value.status == 2
