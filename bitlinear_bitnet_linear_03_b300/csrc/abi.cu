@@ -113,7 +113,11 @@ bitnet_status bitnet_device_error(int* code_out, void* stream) {
   if (!code_out) return BITNET_ERR_NULL;
   bitnet_status st = check_device();
   if (st != BITNET_OK) return st;
-  return cuda_status(bitnet::read_and_clear_device_error(code_out, (cudaStream_t)stream));
+  int a = 0, b = 0;
+  cudaError_t e = bitnet::read_and_clear_device_error(&a, (cudaStream_t)stream);
+  if (e == cudaSuccess) e = bitnet::read_and_clear_decode_error(&b, (cudaStream_t)stream);
+  *code_out = a | (b << 8);
+  return cuda_status(e);
 }
 
 size_t bitnet_quantize_weights_workspace(int64_t N, int64_t K) {

@@ -162,6 +162,8 @@ struct DecodeTarget {
   int32_t* acc_out;
 };
 bool decode_supported(int64_t M, int64_t K);
+// Reads and clears the error word of the decode kernel's bounded waits.
+cudaError_t read_and_clear_decode_error(int* code, cudaStream_t s);
 cudaError_t launch_decode(const DecodeTarget* targets, int count, const int8_t* xq,
                           const float* x_scale, const uint16_t* x_bf16, int64_t M, int64_t K,
                           int8_t* xq_out, float* x_scale_out, cudaStream_t s);

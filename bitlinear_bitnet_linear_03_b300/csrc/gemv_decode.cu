@@ -8,32 +8,48 @@
 // the result is exact and order-free.
 //
 // Layout of the work (decode is bound by the packed-weight stream):
-//  * Lane l of a warp owns 64-weight chunks l, l+32, ... of its K-slice for
-//    the whole kernel, so its int8 activations (and their byte sum) sit in
-//    registers from the prologue on; each weight row is then read as 512
-//    contiguous bytes per warp step and never touches shared memory.
-//  * The 8 warps of a CTA split K into `ksplit` slices and the CTA's rows
-//    into 8/ksplit row groups; a row group handles kB rows per step.  Partial
-//    row sums are combined with a reduce-scatter over the lanes (kB*MT values
-//    in log2 steps) and, across K-slices, through shared memory.
-//  * Before waiting on the previous kernel, one thread asks the copy engine
-//    to prefetch the CTA's whole weight range into L2 (weights never depend on
-//    the previous kernel), and the kernel lets its successor launch; with
-//    programmatic dependent launch consecutive decode kernels overlap.
+//  * One producer lane streams the CTA's weight rows into a ring of shared-
+//    memory stages with bulk asynchronous copies (cp.async.bulk, completion
+//    counted on an mbarrier per stage).  A CTA's rows of one matrix are
+//    contiguous in memory, so a stage (R whole rows) is a single copy.
+//  * Eight consumer warps take 4-row quads of the stages in turn.  Within a
+//    quad, an 8-lane group owns a row and lane (l % 8) reads 16-byte chunks
+//    l%8, l%8 + 8, ... of it (128 contiguous bytes per group per step).  The
+//    int8 activations sit in shared memory in a swizzled chunk layout; the
+//    four groups read the same chunk, so each activation read is a broadcast
+//    that touches every bank once.  The row sum is three shuffles.
+//  * Before waiting on the previous kernel the CTA asks for its whole weight
+//    range to be prefetched into L2 (a hint; weights are read only after the
+//    wait) and lets its successor launch: consecutive decode kernels overlap
+//    under programmatic dependent launch.
 //  * Up to kDecodeMaxTargets matrices sharing the same input run in one
-//    launch: their rows are concatenated into one row space.
+//    launch; their rows are concatenated, stages never straddle two matrices.
 //  * The input is int8 with its scales, or bf16: then every CTA forms the
-//    per-token absmax over all of K and quantises its own chunks with the
-//    rule of the activation-quantisation kernel (bit-identical codes).
+//    per-token absmax over all of K and quantises x with the rule of the
+//    activation-quantisation kernel (bit-identical codes).
+//  * Every mbarrier wait is bounded (about a second); on time-out the kernel
+//    records an error code, stops issuing copies, waits (bounded) for the
+//    copies it has in flight and returns.
 #include "common.cuh"
 
 namespace bitnet {
+
+__device__ int g_decode_error;
+
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kWarps = 8;
-constexpr int kB = 4;           // rows per row-group step
+constexpr int kConsumerWarps = 8;
+constexpr int kConsumers = kConsumerWarps * 32;
+constexpr int kThreads = kConsumers + 32;  // + one producer warp
+constexpr int kMaxStages = 8;
+constexpr int kRingBudget = 96 * 1024;
+constexpr int kStageTarget = 24 * 1024;
+constexpr int kMaxSmem = 227 * 1024 - 1024;  // dynamic part; static barriers etc. fit in the rest
 constexpr int kPrefetchMax = 1 << 16;
+constexpr long long kWaitCycles = 2000000000ll;  // ~1 s at 2 GHz
+constexpr int kErrFullWait = 1;
+constexpr int kErrEmptyWait = 2;
+constexpr int kErrDrainWait = 3;
 
 struct Target {
   const uint8_t* Wq;
@@ -54,358 +70,367 @@ struct Args {
   const float* x_scale;  // scales of xq
   int8_t* xq_out;        // optional copy of the quantised bf16 input
   float* xs_out;
-  int M, K, ksplit, slice_chunks;
+  int M, K;
+  int rows_per_stage;
+  int stages;
+  int stage_bytes;
 };
 
-__device__ __forceinline__ uint32_t bf16_pair_lo(uint32_t w) { return w & 0xffffu; }
-__device__ __forceinline__ uint32_t bf16_pair_hi(uint32_t w) { return w >> 16; }
+// ---- mbarrier / bulk-copy primitives (PTX ISA: mbarrier, cp.async.bulk)
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_fence_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait for the phase with the given parity; false on time-out.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity))
+    if (clock64() - t0 > kWaitCycles) return false;
+  return true;
+}
+__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                              uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void consumer_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
+}
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
+}
 
-// Reduce-scatter of V per-lane values over the warp: afterwards every lane
-// holds the warp-wide total of value index(lane) (see value_index).
-template <int V>
-__device__ __forceinline__ int reduce_scatter(int (&v)[V], int lane) {
-  int count = V;
-#pragma unroll
-  for (int off = 16; off >= 1; off >>= 1) {
-    if (count > 1) {
-      const int half = count >> 1;
-      const bool upper = (lane & off) != 0;
-#pragma unroll
-      for (int i = 0; i < V / 2; ++i) {
-        if (i < half) {
-          const int send = upper ? v[i] : v[i + half];
-          const int keep = upper ? v[i + half] : v[i];
-          v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
-        }
-      }
-      count = half;
-    } else {
-      v[0] += __shfl_xor_sync(0xffffffffu, v[0], off);
-    }
+// Byte offset of field s (16 bytes) of chunk c in the swizzled activation row.
+__device__ __forceinline__ int xs_offset(int c, int s) { return 64 * c + 16 * ((s + (c >> 1)) & 3); }
+
+// The CTA's stage sequence: for each matrix overlapping the CTA's rows, the
+// rows in pieces of at most rows_per_stage.  Calls f(p, first_row, nrows).
+template <typename F>
+__device__ __forceinline__ void for_each_stage(const Args& a, int r_begin, int r_end, F&& f) {
+  for (int p = 0; p < a.count; ++p) {
+    const int lo = max(r_begin, a.t[p].row0);
+    const int hi = min(r_end, a.t[p].row0 + a.t[p].N);
+    for (int r = lo; r < hi; r += a.rows_per_stage)
+      if (!f(p, r - a.t[p].row0, min(a.rows_per_stage, hi - r))) return;
   }
-  return v[0];
 }
 
-// Index of the value a lane holds after reduce_scatter<V>: the stage with
-// offset 16 keeps the upper half on lanes with bit 4 set, and so on.
-template <int V>
-__device__ __forceinline__ int value_index(int lane) {
-  int idx = 0, half = V >> 1;
-#pragma unroll
-  for (int off = 16; off >= 1 && half >= 1; off >>= 1, half >>= 1)
-    if (lane & off) idx += half;
-  return idx;
-}
-
-// Lanes that write a value after reduce_scatter<V> (one per index).
-template <int V>
-__device__ __forceinline__ bool value_writer(int lane) {
-  return (lane & (32 / V - 1)) == 0;
-}
-
-template <int MT, int J>
-__global__ void __launch_bounds__(kThreads)
+template <int MT>
+__global__ void __launch_bounds__(kThreads, 2)
 k_gemv_decode(const __grid_constant__ Args a) {
-  __shared__ float s_max[kWarps][MT];
-  __shared__ int s_part[kWarps][kB * MT];
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ __align__(8) uint64_t full_bar[kMaxStages];
+  __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
+  __shared__ float s_max[kConsumerWarps][MT];
+  __shared__ int s_sumx[MT];
+
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r_begin = blockIdx.x * a.rows_per_cta;
   const int r_end = min(r_begin + a.rows_per_cta, a.rows_total);
   const int64_t row_bytes = a.K >> 2;
+  const int quads = a.rows_per_stage >> 2;
+  const uint32_t ring = smem_addr(smem);
+  int8_t* xs = reinterpret_cast<int8_t*>(smem + a.stages * a.stage_bytes);
 
-  // 1. Prefetch this CTA's weight rows into L2 (independent of the
-  //    previous kernel), then let the next kernel launch and wait for ours.
   if (threadIdx.x == 0) {
+    for (int s = 0; s < a.stages; ++s) {
+      mbar_init(smem_addr(&full_bar[s]), 1);
+      mbar_init(smem_addr(&empty_bar[s]), quads);
+    }
+    mbar_fence_init();
+    for (int m = 0; m < MT; ++m) s_sumx[m] = 0;
+    // L2 prefetch hint for this CTA's weights (independent of the previous
+    // kernel; no data is read before griddep_wait).
     for (int p = 0; p < a.count; ++p) {
       const int lo = max(r_begin, a.t[p].row0);
       const int hi = min(r_end, a.t[p].row0 + a.t[p].N);
       if (lo >= hi) continue;
       const uint8_t* base = a.t[p].Wq + (int64_t)(lo - a.t[p].row0) * row_bytes;
-      int64_t bytes = (int64_t)(hi - lo) * row_bytes;
-      for (int64_t off = 0; off < bytes; off += kPrefetchMax) {
-        const int64_t n = bytes - off < kPrefetchMax ? bytes - off : kPrefetchMax;
-        prefetch_l2_bulk(base + off, (uint32_t)n);
-      }
+      const int64_t bytes = (int64_t)(hi - lo) * row_bytes;
+      for (int64_t off = 0; off < bytes; off += kPrefetchMax)
+        prefetch_l2_bulk(base + off, (uint32_t)(bytes - off < kPrefetchMax ? bytes - off
+                                                                              : kPrefetchMax));
     }
   }
   griddep_launch_dependents();
+  __syncthreads();
   griddep_wait();
 
-  const int ks = warp % a.ksplit;
-  const int rg = warp / a.ksplit;
-  const int nrg = kWarps / a.ksplit;
-  const int nch = a.K >> 6;
-  const int c0 = ks * a.slice_chunks;
-  const int c1 = min(c0 + a.slice_chunks, nch);
-
-  // 2. This lane's activation chunks: xr[m][j][s] holds the int8 codes of
-  //    weights 64c + 16s + 4i + {0..3} in word i, c = c0 + lane + 32j.
-  uint4 xr[MT][J][4];
-  int xsum[MT];
-  float xscale[MT];
-#pragma unroll
-  for (int m = 0; m < MT; ++m) {
-    xsum[m] = 0;
-    xscale[m] = 0.0f;
-#pragma unroll
-    for (int j = 0; j < J; ++j)
-#pragma unroll
-      for (int s = 0; s < 4; ++s) xr[m][j][s] = make_uint4(0, 0, 0, 0);
+  // ------------------------------------------------------------ producer
+  if (warp == kConsumerWarps) {
+    if (lane != 0) return;
+    int i = 0;
+    bool ok = true;
+    for_each_stage(a, r_begin, r_end, [&](int p, int row, int nrows) {
+      const int slot = i % a.stages;
+      if (i >= a.stages && !mbar_wait(smem_addr(&empty_bar[slot]), ((i / a.stages) - 1) & 1)) {
+        atomicOr(&g_decode_error, 1 << kErrEmptyWait);
+        ok = false;
+        return false;
+      }
+      const uint32_t bytes = (uint32_t)(nrows * row_bytes);
+      const uint32_t fb = smem_addr(&full_bar[slot]);
+      mbar_arrive_expect_tx(fb, bytes);
+      bulk_copy_g2s(ring + slot * a.stage_bytes, a.t[p].Wq + (int64_t)row * row_bytes, bytes, fb);
+      ++i;
+      return true;
+    });
+    // Never leave the CTA with a copy in flight: wait for the last copy of
+    // every slot to land.
+    const int first = i > a.stages ? i - a.stages : 0;
+    for (int j = first; j < i; ++j)
+      if (!mbar_wait(smem_addr(&full_bar[j % a.stages]), (j / a.stages) & 1)) {
+        atomicOr(&g_decode_error, 1 << kErrDrainWait);
+        break;
+      }
+    (void)ok;
+    return;
   }
 
+  // ------------------------------------------------------------ consumers
+  const int tid = threadIdx.x;  // 0 .. kConsumers-1
+  const int K = a.K;
+  const int nitems = K >> 4;   // 16-byte fields per token row
+  float xscale[MT];
   if (a.xb != nullptr) {
-    // Per-token absmax over the whole of K, shared by the CTA.
-    const int nv = a.K >> 3;
+    const int nv = K >> 3;
 #pragma unroll
     for (int m = 0; m < MT; ++m) {
       float mx = 0.0f;
       if (m < a.M) {
-        const uint4* xrow = reinterpret_cast<const uint4*>(a.xb + (int64_t)m * a.K);
-        for (int v = threadIdx.x; v < nv; v += kThreads) {
-          const uint4 p = ld_nc_v4(xrow + v);
-          const uint32_t w4[4] = {p.x, p.y, p.z, p.w};
+        const uint4* xrow = reinterpret_cast<const uint4*>(a.xb + (int64_t)m * K);
+        for (int v = tid; v < nv; v += kConsumers) {
+          const uint4 q = ld_nc_v4(xrow + v);
+          const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            mx = fmaxf(mx, fabsf(bf16_bits_to_float(bf16_pair_lo(w4[q]))));
-            mx = fmaxf(mx, fabsf(bf16_bits_to_float(bf16_pair_hi(w4[q]))));
+          for (int t = 0; t < 4; ++t) {
+            mx = fmaxf(mx, fabsf(bf16_bits_to_float(w4[t] & 0xffffu)));
+            mx = fmaxf(mx, fabsf(bf16_bits_to_float(w4[t] >> 16)));
           }
         }
       }
       mx = warp_max_f32(mx);
       if (lane == 0) s_max[warp][m] = mx;
     }
-    __syncthreads();
+    consumer_sync();
     float inv[MT];
 #pragma unroll
     for (int m = 0; m < MT; ++m) {
       float mx = s_max[0][m];
 #pragma unroll
-      for (int w = 1; w < kWarps; ++w) mx = fmaxf(mx, s_max[w][m]);
+      for (int w = 1; w < kConsumerWarps; ++w) mx = fmaxf(mx, s_max[w][m]);
       const ActScale sc = act_scale_from_absmax(mx);
       inv[m] = sc.inv;
       xscale[m] = sc.scale;
     }
 #pragma unroll
-    for (int j = 0; j < J; ++j) {
-      const int c = c0 + lane + 32 * j;
-      if (c >= c1) continue;
-#pragma unroll
-      for (int m = 0; m < MT; ++m) {
-        if (m >= a.M) continue;
-        const uint4* src = reinterpret_cast<const uint4*>(a.xb + (int64_t)m * a.K + c * 64);
-#pragma unroll
-        for (int s = 0; s < 4; ++s) {
-          // elements 16s .. 16s+15 of the chunk: two 16-byte loads
-          const uint4 p0 = ld_nc_v4(src + 2 * s), p1 = ld_nc_v4(src + 2 * s + 1);
+    for (int m = 0; m < MT; ++m) {
+      int sum = 0;
+      if (m < a.M) {
+        const uint4* xrow = reinterpret_cast<const uint4*>(a.xb + (int64_t)m * K);
+        for (int f = tid; f < nitems; f += kConsumers) {
+          const uint4 p0 = ld_nc_v4(xrow + 2 * f), p1 = ld_nc_v4(xrow + 2 * f + 1);
           const uint32_t e[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
-          uint32_t words[4];
+          uint32_t wd[4];
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             int q[4];
 #pragma unroll
             for (int t = 0; t < 4; ++t) {
               const int el = 4 * i + t;
-              const uint32_t pair = e[el >> 1];
-              const float f = bf16_bits_to_float((el & 1) ? bf16_pair_hi(pair) : bf16_pair_lo(pair));
-              q[t] = round_clip(__fmul_rn(f, inv[m]), -128.f, 127.f);
+              const uint32_t h = (el & 1) ? (e[el >> 1] >> 16) : (e[el >> 1] & 0xffffu);
+              q[t] = round_clip(__fmul_rn(bf16_bits_to_float(h), inv[m]), -128.f, 127.f);
             }
-            words[i] = pack_i8x4(q[0], q[1], q[2], q[3]);
-            xsum[m] = dp4a_ss(words[i], 0x01010101u, xsum[m]);
+            wd[i] = pack_i8x4(q[0], q[1], q[2], q[3]);
+            sum = dp4a_ss(wd[i], 0x01010101u, sum);
           }
-          xr[m][j][s] = make_uint4(words[0], words[1], words[2], words[3]);
+          const uint4 packed = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+          *reinterpret_cast<uint4*>(xs + (int64_t)m * K + xs_offset(f >> 2, f & 3)) = packed;
+          if (blockIdx.x == 0 && a.xq_out != nullptr)
+            *reinterpret_cast<uint4*>(a.xq_out + (int64_t)m * K + 16 * f) = packed;
         }
       }
-    }
-    // One CTA also stores the quantised input when asked.
-    if (blockIdx.x == 0 && a.xq_out != nullptr) {
-      for (int m = 0; m < a.M && m < MT; ++m) {
-        const uint4* xrow = reinterpret_cast<const uint4*>(a.xb + (int64_t)m * a.K);
-        uint2* qrow = reinterpret_cast<uint2*>(a.xq_out + (int64_t)m * a.K);
-        float im = inv[0];
-#pragma unroll
-        for (int mm = 1; mm < MT; ++mm)
-          if (mm == m) im = inv[mm];
-        for (int v = threadIdx.x; v < nv; v += kThreads) {
-          const uint4 p = ld_nc_v4(xrow + v);
-          const uint32_t w4[4] = {p.x, p.y, p.z, p.w};
-          int q[8];
-#pragma unroll
-          for (int t = 0; t < 4; ++t) {
-            q[2 * t] = round_clip(__fmul_rn(bf16_bits_to_float(bf16_pair_lo(w4[t])), im), -128.f, 127.f);
-            q[2 * t + 1] = round_clip(__fmul_rn(bf16_bits_to_float(bf16_pair_hi(w4[t])), im), -128.f, 127.f);
-          }
-          qrow[v] = make_uint2(pack_i8x4(q[0], q[1], q[2], q[3]), pack_i8x4(q[4], q[5], q[6], q[7]));
-        }
-        if (threadIdx.x == 0 && a.xs_out != nullptr) {
-          float sc = xscale[0];
-#pragma unroll
-          for (int mm = 1; mm < MT; ++mm)
-            if (mm == m) sc = xscale[mm];
-          a.xs_out[m] = sc;
-        }
-      }
+      sum = warp_sum_i32(sum);
+      if (lane == 0 && sum) atomicAdd(&s_sumx[m], sum);
+      if (blockIdx.x == 0 && tid == 0 && a.xs_out != nullptr && m < a.M) a.xs_out[m] = xscale[m];
     }
   } else {
 #pragma unroll
     for (int m = 0; m < MT; ++m) {
-      if (m >= a.M) continue;
-      xscale[m] = a.x_scale[m];
-#pragma unroll
-      for (int j = 0; j < J; ++j) {
-        const int c = c0 + lane + 32 * j;
-        if (c >= c1) continue;
-        const uint4* src = reinterpret_cast<const uint4*>(a.xq + (int64_t)m * a.K + c * 64);
-#pragma unroll
-        for (int s = 0; s < 4; ++s) {
-          const uint4 v = ld_nc_v4(src + s);
-          xr[m][j][s] = v;
-          xsum[m] = dp4a_ss(v.x, 0x01010101u, xsum[m]);
-          xsum[m] = dp4a_ss(v.y, 0x01010101u, xsum[m]);
-          xsum[m] = dp4a_ss(v.z, 0x01010101u, xsum[m]);
-          xsum[m] = dp4a_ss(v.w, 0x01010101u, xsum[m]);
+      int sum = 0;
+      xscale[m] = 0.0f;
+      if (m < a.M) {
+        xscale[m] = a.x_scale[m];
+        const uint4* xrow = reinterpret_cast<const uint4*>(a.xq + (int64_t)m * K);
+        for (int f = tid; f < nitems; f += kConsumers) {
+          const uint4 v = ld_nc_v4(xrow + f);
+          sum = dp4a_ss(v.x, 0x01010101u, sum);
+          sum = dp4a_ss(v.y, 0x01010101u, sum);
+          sum = dp4a_ss(v.z, 0x01010101u, sum);
+          sum = dp4a_ss(v.w, 0x01010101u, sum);
+          *reinterpret_cast<uint4*>(xs + (int64_t)m * K + xs_offset(f >> 2, f & 3)) = v;
         }
       }
+      sum = warp_sum_i32(sum);
+      if (lane == 0 && sum) atomicAdd(&s_sumx[m], sum);
     }
   }
-
-  // 3. Stream the rows.
-  const int per_step = nrg * kB;
-  const int nsteps = (a.rows_per_cta + per_step - 1) / per_step;
-  constexpr int V = kB * MT;
-  const int my_idx = value_index<V>(lane);
-  const bool writer = value_writer<V>(lane);
-
-  for (int step = 0; step < nsteps; ++step) {
-    const uint8_t* wrow[kB];
-    int tgt[kB];
-    int rloc[kB];
+  consumer_sync();
+  int sumx[MT];
 #pragma unroll
-    for (int b = 0; b < kB; ++b) {
-      const int gr = r_begin + step * per_step + rg * kB + b;
-      wrow[b] = nullptr;
-      tgt[b] = -1;
-      rloc[b] = 0;
-      if (gr < r_end) {
+  for (int m = 0; m < MT; ++m) sumx[m] = s_sumx[m];
+
+  const int grp = lane >> 3, sub = lane & 7;
+  const int nch = K >> 6;
+  const uint32_t xs_base = smem_addr(xs);
+  int i = 0, g = 0;
+  for_each_stage(a, r_begin, r_end, [&](int p, int row0, int nrows) {
+    const int slot = i % a.stages;
+    const uint32_t parity = (i / a.stages) & 1;
+    bool waited = false;
+    for (int q = 0; q < quads; ++q, ++g) {
+      if ((g & (kConsumerWarps - 1)) != warp) continue;
+      if (!waited) {
+        if (!mbar_wait(smem_addr(&full_bar[slot]), parity)) {
+          if (lane == 0) atomicOr(&g_decode_error, 1 << kErrFullWait);
+          return false;
+        }
+        waited = true;
+      }
+      const int r = q * 4 + grp;
+      const bool valid = r < nrows;
+      const uint32_t wbase = ring + slot * a.stage_bytes + (uint32_t)(r * row_bytes);
+      int acc[MT][4];
 #pragma unroll
-        for (int p = 0; p < kDecodeMaxTargets; ++p) {
-          if (p < a.count && gr >= a.t[p].row0 && gr < a.t[p].row0 + a.t[p].N) {
-            tgt[b] = p;
-            rloc[b] = gr - a.t[p].row0;
-            wrow[b] = a.t[p].Wq + (int64_t)rloc[b] * row_bytes;
+      for (int m = 0; m < MT; ++m) acc[m][0] = acc[m][1] = acc[m][2] = acc[m][3] = 0;
+      if (valid) {
+#pragma unroll 2
+        for (int c = sub; c < nch; c += 8) {
+          const uint4 wv = lds128(wbase + 16 * c);
+          const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+          for (int m = 0; m < MT; ++m) {
+            const uint32_t xb = xs_base + m * K;
+            const uint4 x0 = lds128(xb + xs_offset(c, 0));
+            const uint4 x1 = lds128(xb + xs_offset(c, 1));
+            const uint4 x2 = lds128(xb + xs_offset(c, 2));
+            const uint4 x3 = lds128(xb + xs_offset(c, 3));
+            const uint32_t f0[4] = {x0.x, x0.y, x0.z, x0.w};
+            const uint32_t f1[4] = {x1.x, x1.y, x1.z, x1.w};
+            const uint32_t f2[4] = {x2.x, x2.y, x2.z, x2.w};
+            const uint32_t f3[4] = {x3.x, x3.y, x3.z, x3.w};
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+              acc[m][0] = dp4a_us(ww[w] & 0x03030303u, f0[w], acc[m][0]);
+              acc[m][1] = dp4a_us(ww[w] & 0x0c0c0c0cu, f1[w], acc[m][1]);
+              acc[m][2] = dp4a_us(ww[w] & 0x30303030u, f2[w], acc[m][2]);
+              acc[m][3] = dp4a_us(ww[w] & 0xc0c0c0c0u, f3[w], acc[m][3]);
+            }
           }
         }
       }
-    }
-    uint4 w[kB][J];
-#pragma unroll
-    for (int b = 0; b < kB; ++b)
-#pragma unroll
-      for (int j = 0; j < J; ++j) {
-        const int c = c0 + lane + 32 * j;
-        w[b][j] = (wrow[b] != nullptr && c < c1) ? ld_stream_v4(wrow[b] + c * 16)
-                                                  : make_uint4(0, 0, 0, 0);
-      }
-    int v[V];
-#pragma unroll
-    for (int b = 0; b < kB; ++b) {
+      const Target& T = a.t[p];
+      const float ws = *T.w_scale;
 #pragma unroll
       for (int m = 0; m < MT; ++m) {
-        int a0 = 0, a1 = 0, a2 = 0, a3 = 0;
-#pragma unroll
-        for (int j = 0; j < J; ++j) {
-          const uint32_t ww[4] = {w[b][j].x, w[b][j].y, w[b][j].z, w[b][j].w};
-          const uint32_t x0[4] = {xr[m][j][0].x, xr[m][j][0].y, xr[m][j][0].z, xr[m][j][0].w};
-          const uint32_t x1[4] = {xr[m][j][1].x, xr[m][j][1].y, xr[m][j][1].z, xr[m][j][1].w};
-          const uint32_t x2[4] = {xr[m][j][2].x, xr[m][j][2].y, xr[m][j][2].z, xr[m][j][2].w};
-          const uint32_t x3[4] = {xr[m][j][3].x, xr[m][j][3].y, xr[m][j][3].z, xr[m][j][3].w};
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            a0 = dp4a_us(ww[i] & 0x03030303u, x0[i], a0);
-            a1 = dp4a_us(ww[i] & 0x0c0c0c0cu, x1[i], a1);
-            a2 = dp4a_us(ww[i] & 0x30303030u, x2[i], a2);
-            a3 = dp4a_us(ww[i] & 0xc0c0c0c0u, x3[i], a3);
-          }
+        int t = acc[m][0] + (acc[m][1] >> 2) + (acc[m][2] >> 4) + (acc[m][3] >> 6);
+        t += __shfl_xor_sync(0xffffffffu, t, 4);
+        t += __shfl_xor_sync(0xffffffffu, t, 2);
+        t += __shfl_xor_sync(0xffffffffu, t, 1);
+        if (sub == 0 && valid && m < a.M) {
+          const int total = t - sumx[m];
+          const int64_t o = (int64_t)m * T.N + row0 + r;
+          T.y[o] = __fmul_rn(__int2float_rn(total), __fmul_rn(xscale[m], ws));
+          if (T.acc_out) T.acc_out[o] = total;
         }
-        v[b * MT + m] = a0 + (a1 >> 2) + (a2 >> 4) + (a3 >> 6) - xsum[m];
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&empty_bar[slot]));
     }
-    int total = reduce_scatter<V>(v, lane);
-    if (a.ksplit > 1) {
-      if (writer) s_part[warp][my_idx] = total;
-      __syncthreads();
-      if (writer && ks == 0) {
-        total = 0;
-        for (int q = 0; q < a.ksplit; ++q) total += s_part[rg * a.ksplit + q][my_idx];
-      }
-      __syncthreads();
-    }
-    if (writer && ks == 0) {
-      const int b = my_idx / MT, m = my_idx % MT;
-      int p = -1, rl = 0;
-#pragma unroll
-      for (int bb = 0; bb < kB; ++bb)
-        if (bb == b) {
-          p = tgt[bb];
-          rl = rloc[bb];
-        }
-      if (p >= 0 && m < a.M) {
-        float sc = xscale[0];
-#pragma unroll
-        for (int mm = 1; mm < MT; ++mm)
-          if (mm == m) sc = xscale[mm];
-        const Target& T = a.t[p];
-        T.y[(int64_t)m * T.N + rl] = __fmul_rn(__int2float_rn(total), __fmul_rn(sc, *T.w_scale));
-        if (T.acc_out) T.acc_out[(int64_t)m * T.N + rl] = total;
-      }
-    }
-  }
+    ++i;
+    return true;
+  });
 }
 
-struct Shape {
-  int mt, j, ksplit, slice_chunks;
+struct Plan {
+  int mt, rows_per_stage, stages, stage_bytes;
+  size_t smem;
 };
 
-// Picks the tokens-per-pass MT, chunks per lane J and the K-split so that a
-// lane's activations stay within 16*MT*J <= 64 registers and ksplit <= 8.
-bool pick_shape(int64_t M, int64_t K, Shape* out) {
-  if (M < 1 || M > kDecodeMaxM || K % 64 != 0) return false;
-  const int nch = (int)(K / 64);
-  const int mt = M <= 1 ? 1 : M <= 2 ? 2 : 4;
-  const int jopts[3] = {2, 4, 1};
-  for (int jo = 0; jo < 3; ++jo) {
-    const int j = jopts[jo];
-    if (16 * mt * j > 64 && !(mt == 1 && j == 4)) continue;
-    if (mt == 4 && j != 1) continue;
-    if (mt == 2 && j != 2) continue;
-    int ks = 1;
-    while (ks <= 8 && (nch + ks - 1) / ks > 32 * j) ks *= 2;
-    if (ks > 8) continue;
-    out->mt = mt;
-    out->j = j;
-    out->ksplit = ks;
-    out->slice_chunks = (nch + ks - 1) / ks;
-    return true;
-  }
-  return false;
+bool make_plan(int64_t M, int64_t K, Plan* pl) {
+  if (M < 1 || M > kDecodeMaxM || K < 64 || K % 64 != 0 || K > 65536) return false;
+  pl->mt = M <= 1 ? 1 : M <= 2 ? 2 : 4;
+  const int64_t row_bytes = K / 4;
+  int64_t R = (kStageTarget / row_bytes) / 4 * 4;
+  if (R < 4) R = 4;
+  if (R > 32) R = 32;
+  pl->rows_per_stage = (int)R;
+  pl->stage_bytes = (int)(R * row_bytes);
+  int64_t S = kRingBudget / pl->stage_bytes;
+  if (S < 2) S = 2;
+  if (S > kMaxStages) S = kMaxStages;
+  pl->stages = (int)S;
+  pl->smem = (size_t)S * pl->stage_bytes + (size_t)pl->mt * (size_t)K;
+  return pl->smem <= (size_t)kMaxSmem;
 }
 
-template <int MT, int J>
-cudaError_t launch_t(const Args& a, int ctas, cudaStream_t s) {
-  return launch_pdl(k_gemv_decode<MT, J>, dim3(ctas), dim3(kThreads), 0, s, a);
+template <int MT>
+cudaError_t launch_t(const Args& a, int ctas, size_t smem, cudaStream_t s) {
+  static bool configured[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 64 && !configured[dev]) {
+    e = cudaFuncSetAttribute(k_gemv_decode<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kMaxSmem);
+    if (e != cudaSuccess) return e;
+    configured[dev] = true;
+  }
+  return launch_pdl(k_gemv_decode<MT>, dim3(ctas), dim3(kThreads), smem, s, a);
 }
 
 }  // namespace
 
 bool decode_supported(int64_t M, int64_t K) {
-  Shape sh;
-  return pick_shape(M, K, &sh);
+  Plan pl;
+  return make_plan(M, K, &pl);
 }
 
 cudaError_t launch_decode(const DecodeTarget* targets, int count, const int8_t* xq,
                           const float* x_scale, const uint16_t* x_bf16, int64_t M, int64_t K,
                           int8_t* xq_out, float* x_scale_out, cudaStream_t s) {
-  Shape sh;
-  if (count < 1 || count > kDecodeMaxTargets || !pick_shape(M, K, &sh))
+  Plan pl;
+  if (count < 1 || count > kDecodeMaxTargets || !make_plan(M, K, &pl))
     return cudaErrorNotSupported;
   Args a = {};
   int64_t rows = 0;
@@ -428,22 +453,28 @@ cudaError_t launch_decode(const DecodeTarget* targets, int count, const int8_t* 
   a.xs_out = x_scale_out;
   a.M = (int)M;
   a.K = (int)K;
-  a.ksplit = sh.ksplit;
-  a.slice_chunks = sh.slice_chunks;
-  // One CTA per SM while the weights are small enough for neighbouring
-  // launches to overlap; two per SM for large matrices.
-  const int64_t bytes = rows * (K / 4);
-  const int per_step = (kWarps / sh.ksplit) * kB;
-  int64_t ctas = bytes > (int64_t)24 << 20 ? 296 : 148;
-  const int64_t max_ctas = (rows + per_step - 1) / per_step;
-  if (ctas > max_ctas) ctas = max_ctas;
+  a.rows_per_stage = pl.rows_per_stage;
+  a.stages = pl.stages;
+  a.stage_bytes = pl.stage_bytes;
+  int64_t ctas = (rows + 3) / 4;
+  if (ctas > 148) ctas = 148;
   a.rows_per_cta = (int)((rows + ctas - 1) / ctas);
   ctas = (rows + a.rows_per_cta - 1) / a.rows_per_cta;
   const int c = (int)ctas;
-  if (sh.mt == 1 && sh.j == 2) return launch_t<1, 2>(a, c, s);
-  if (sh.mt == 1 && sh.j == 4) return launch_t<1, 4>(a, c, s);
-  if (sh.mt == 2) return launch_t<2, 2>(a, c, s);
-  return launch_t<4, 1>(a, c, s);
+  if (pl.mt == 1) return launch_t<1>(a, c, pl.smem, s);
+  if (pl.mt == 2) return launch_t<2>(a, c, pl.smem, s);
+  return launch_t<4>(a, c, pl.smem, s);
+}
+
+cudaError_t read_and_clear_decode_error(int* code, cudaStream_t s) {
+  int zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbolAsync(code, g_decode_error, sizeof(int), 0,
+                                            cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess)
+    e = cudaMemcpyToSymbolAsync(g_decode_error, &zero, sizeof(int), 0, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  return e;
 }
 
 }  // namespace bitnet
