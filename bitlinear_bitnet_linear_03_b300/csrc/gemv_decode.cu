@@ -10,11 +10,15 @@
 // Layout of the work (decode is bound by the packed-weight stream):
 //  * One producer lane streams the CTA's weight rows into a ring of shared-
 //    memory stages with bulk asynchronous copies (cp.async.bulk, completion
-//    counted on an mbarrier per stage).  A CTA's rows of one matrix are
-//    contiguous in memory, so a stage (R whole rows) is a single copy.
-//  * Eight consumer warps take 4-row quads of the stages in turn.  Within a
-//    quad, an 8-lane group owns a row and lane (l % 8) reads 16-byte chunks
-//    l%8, l%8 + 8, ... of it (128 contiguous bytes per group per step).  The
+//    counted on an mbarrier per stage).  A stage is a block of 32 rows times
+//    a K-slice of at most 48 64-weight chunks (24 KB); when the slice is the
+//    whole row the block is one contiguous copy, otherwise one copy per row.
+//  * Every one of the eight consumer warps takes part in every stage, in
+//    order (so the parity of each mbarrier phase is unambiguous): warp w owns
+//    rows 4w .. 4w+3 of each block, an 8-lane group owns a row and lane
+//    (l % 8) reads 16-byte chunks l%8, l%8 + 8, ... of the slice (128
+//    contiguous bytes per group per step); row sums carry across the
+//    K-slices of a block in registers.  The
 //    int8 activations sit in shared memory in a swizzled chunk layout; the
 //    four groups read the same chunk, so each activation read is a broadcast
 //    that touches every bank once.  The row sum is three shuffles.
@@ -71,9 +75,10 @@ struct Args {
   int8_t* xq_out;        // optional copy of the quantised bf16 input
   float* xs_out;
   int M, K;
-  int rows_per_stage;
+  int slice_chunks;  // 64-weight chunks per K-slice (one stage = one block x one slice)
+  int nslices;
   int stages;
-  int stage_bytes;
+  int stage_bytes;   // ring slot size: kBlockRows x slice_chunks x 16 bytes
 };
 
 // ---- mbarrier / bulk-copy primitives (PTX ISA: mbarrier, cp.async.bulk)
@@ -133,15 +138,19 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
 // Byte offset of field s (16 bytes) of chunk c in the swizzled activation row.
 __device__ __forceinline__ int xs_offset(int c, int s) { return 64 * c + 16 * ((s + (c >> 1)) & 3); }
 
-// The CTA's stage sequence: for each matrix overlapping the CTA's rows, the
-// rows in pieces of at most rows_per_stage.  Calls f(p, first_row, nrows).
+// The CTA's stage sequence.  Rows of each matrix overlapping the CTA's range
+// are taken in blocks of kBlockRows; each block is streamed as `nslices`
+// K-slices of slice_chunks 64-weight chunks (the last may be shorter).
+// Calls f(p, first_row, nrows, slice) in order; stops when f returns false.
+constexpr int kBlockRows = 32;
 template <typename F>
 __device__ __forceinline__ void for_each_stage(const Args& a, int r_begin, int r_end, F&& f) {
   for (int p = 0; p < a.count; ++p) {
     const int lo = max(r_begin, a.t[p].row0);
     const int hi = min(r_end, a.t[p].row0 + a.t[p].N);
-    for (int r = lo; r < hi; r += a.rows_per_stage)
-      if (!f(p, r - a.t[p].row0, min(a.rows_per_stage, hi - r))) return;
+    for (int r = lo; r < hi; r += kBlockRows)
+      for (int sl = 0; sl < a.nslices; ++sl)
+        if (!f(p, r - a.t[p].row0, min(kBlockRows, hi - r), sl)) return;
   }
 }
 
@@ -158,14 +167,14 @@ k_gemv_decode(const __grid_constant__ Args a) {
   const int r_begin = blockIdx.x * a.rows_per_cta;
   const int r_end = min(r_begin + a.rows_per_cta, a.rows_total);
   const int64_t row_bytes = a.K >> 2;
-  const int quads = a.rows_per_stage >> 2;
+  const int nch = a.K >> 6;
   const uint32_t ring = smem_addr(smem);
   int8_t* xs = reinterpret_cast<int8_t*>(smem + a.stages * a.stage_bytes);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < a.stages; ++s) {
       mbar_init(smem_addr(&full_bar[s]), 1);
-      mbar_init(smem_addr(&empty_bar[s]), quads);
+      mbar_init(smem_addr(&empty_bar[s]), kConsumerWarps);
     }
     mbar_fence_init();
     for (int m = 0; m < MT; ++m) s_sumx[m] = 0;
@@ -190,18 +199,26 @@ k_gemv_decode(const __grid_constant__ Args a) {
   if (warp == kConsumerWarps) {
     if (lane != 0) return;
     int i = 0;
-    bool ok = true;
-    for_each_stage(a, r_begin, r_end, [&](int p, int row, int nrows) {
+    for_each_stage(a, r_begin, r_end, [&](int p, int row, int nrows, int sl) {
       const int slot = i % a.stages;
       if (i >= a.stages && !mbar_wait(smem_addr(&empty_bar[slot]), ((i / a.stages) - 1) & 1)) {
         atomicOr(&g_decode_error, 1 << kErrEmptyWait);
-        ok = false;
         return false;
       }
-      const uint32_t bytes = (uint32_t)(nrows * row_bytes);
+      const int c0 = sl * a.slice_chunks;
+      const int chunks = min(a.slice_chunks, nch - c0);
+      const uint32_t slice_bytes = (uint32_t)chunks * 16u;
       const uint32_t fb = smem_addr(&full_bar[slot]);
-      mbar_arrive_expect_tx(fb, bytes);
-      bulk_copy_g2s(ring + slot * a.stage_bytes, a.t[p].Wq + (int64_t)row * row_bytes, bytes, fb);
+      const uint32_t dst = ring + slot * a.stage_bytes;
+      const uint8_t* src = a.t[p].Wq + (int64_t)row * row_bytes + c0 * 16;
+      mbar_arrive_expect_tx(fb, slice_bytes * (uint32_t)nrows);
+      if (a.nslices == 1) {
+        // whole rows: the block is one contiguous span
+        bulk_copy_g2s(dst, src, slice_bytes * (uint32_t)nrows, fb);
+      } else {
+        for (int r = 0; r < nrows; ++r)
+          bulk_copy_g2s(dst + r * slice_bytes, src + (int64_t)r * row_bytes, slice_bytes, fb);
+      }
       ++i;
       return true;
     });
@@ -213,7 +230,6 @@ k_gemv_decode(const __grid_constant__ Args a) {
         atomicOr(&g_decode_error, 1 << kErrDrainWait);
         break;
       }
-    (void)ok;
     return;
   }
 
@@ -310,55 +326,58 @@ k_gemv_decode(const __grid_constant__ Args a) {
 #pragma unroll
   for (int m = 0; m < MT; ++m) sumx[m] = s_sumx[m];
 
+  // Warp w owns rows 4w .. 4w+3 of every row block; 8-lane group grp owns
+  // row 4w + grp, lane sub reads chunks sub, sub+8, ... of each slice.
   const int grp = lane >> 3, sub = lane & 7;
-  const int nch = K >> 6;
+  const int r = warp * 4 + grp;
   const uint32_t xs_base = smem_addr(xs);
-  int i = 0, g = 0;
-  for_each_stage(a, r_begin, r_end, [&](int p, int row0, int nrows) {
+  int acc[MT][4];
+  int i = 0;
+  for_each_stage(a, r_begin, r_end, [&](int p, int row0, int nrows, int sl) {
     const int slot = i % a.stages;
-    const uint32_t parity = (i / a.stages) & 1;
-    bool waited = false;
-    for (int q = 0; q < quads; ++q, ++g) {
-      if ((g & (kConsumerWarps - 1)) != warp) continue;
-      if (!waited) {
-        if (!mbar_wait(smem_addr(&full_bar[slot]), parity)) {
-          if (lane == 0) atomicOr(&g_decode_error, 1 << kErrFullWait);
-          return false;
-        }
-        waited = true;
-      }
-      const int r = q * 4 + grp;
-      const bool valid = r < nrows;
-      const uint32_t wbase = ring + slot * a.stage_bytes + (uint32_t)(r * row_bytes);
-      int acc[MT][4];
+    if (!mbar_wait(smem_addr(&full_bar[slot]), (i / a.stages) & 1)) {
+      if (lane == 0) atomicOr(&g_decode_error, 1 << kErrFullWait);
+      return false;
+    }
+    if (sl == 0) {
 #pragma unroll
       for (int m = 0; m < MT; ++m) acc[m][0] = acc[m][1] = acc[m][2] = acc[m][3] = 0;
-      if (valid) {
+    }
+    const bool valid = r < nrows;
+    const int c0 = sl * a.slice_chunks;
+    const int chunks = min(a.slice_chunks, nch - c0);
+    if (valid) {
+      const uint32_t wbase = ring + slot * a.stage_bytes + (uint32_t)(r * chunks * 16);
 #pragma unroll 2
-        for (int c = sub; c < nch; c += 8) {
-          const uint4 wv = lds128(wbase + 16 * c);
-          const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
+      for (int c = sub; c < chunks; c += 8) {
+        const uint4 wv = lds128(wbase + 16 * c);
+        const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
+        const int cg = c0 + c;
 #pragma unroll
-          for (int m = 0; m < MT; ++m) {
-            const uint32_t xb = xs_base + m * K;
-            const uint4 x0 = lds128(xb + xs_offset(c, 0));
-            const uint4 x1 = lds128(xb + xs_offset(c, 1));
-            const uint4 x2 = lds128(xb + xs_offset(c, 2));
-            const uint4 x3 = lds128(xb + xs_offset(c, 3));
-            const uint32_t f0[4] = {x0.x, x0.y, x0.z, x0.w};
-            const uint32_t f1[4] = {x1.x, x1.y, x1.z, x1.w};
-            const uint32_t f2[4] = {x2.x, x2.y, x2.z, x2.w};
-            const uint32_t f3[4] = {x3.x, x3.y, x3.z, x3.w};
+        for (int m = 0; m < MT; ++m) {
+          const uint32_t xb = xs_base + m * K;
+          const uint4 x0 = lds128(xb + xs_offset(cg, 0));
+          const uint4 x1 = lds128(xb + xs_offset(cg, 1));
+          const uint4 x2 = lds128(xb + xs_offset(cg, 2));
+          const uint4 x3 = lds128(xb + xs_offset(cg, 3));
+          const uint32_t f0[4] = {x0.x, x0.y, x0.z, x0.w};
+          const uint32_t f1[4] = {x1.x, x1.y, x1.z, x1.w};
+          const uint32_t f2[4] = {x2.x, x2.y, x2.z, x2.w};
+          const uint32_t f3[4] = {x3.x, x3.y, x3.z, x3.w};
 #pragma unroll
-            for (int w = 0; w < 4; ++w) {
-              acc[m][0] = dp4a_us(ww[w] & 0x03030303u, f0[w], acc[m][0]);
-              acc[m][1] = dp4a_us(ww[w] & 0x0c0c0c0cu, f1[w], acc[m][1]);
-              acc[m][2] = dp4a_us(ww[w] & 0x30303030u, f2[w], acc[m][2]);
-              acc[m][3] = dp4a_us(ww[w] & 0xc0c0c0c0u, f3[w], acc[m][3]);
-            }
+          for (int w = 0; w < 4; ++w) {
+            acc[m][0] = dp4a_us(ww[w] & 0x03030303u, f0[w], acc[m][0]);
+            acc[m][1] = dp4a_us(ww[w] & 0x0c0c0c0cu, f1[w], acc[m][1]);
+            acc[m][2] = dp4a_us(ww[w] & 0x30303030u, f2[w], acc[m][2]);
+            acc[m][3] = dp4a_us(ww[w] & 0xc0c0c0c0u, f3[w], acc[m][3]);
           }
         }
       }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_addr(&empty_bar[slot]));
+    ++i;
+    if (sl == a.nslices - 1) {
       const Target& T = a.t[p];
       const float ws = *T.w_scale;
 #pragma unroll
@@ -374,32 +393,29 @@ k_gemv_decode(const __grid_constant__ Args a) {
           if (T.acc_out) T.acc_out[o] = total;
         }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_addr(&empty_bar[slot]));
     }
-    ++i;
     return true;
   });
 }
 
 struct Plan {
-  int mt, rows_per_stage, stages, stage_bytes;
+  int mt, slice_chunks, nslices, stages, stage_bytes;
   size_t smem;
 };
 
 bool make_plan(int64_t M, int64_t K, Plan* pl) {
   if (M < 1 || M > kDecodeMaxM || K < 64 || K % 64 != 0 || K > 65536) return false;
   pl->mt = M <= 1 ? 1 : M <= 2 ? 2 : 4;
-  const int64_t row_bytes = K / 4;
-  int64_t R = (kStageTarget / row_bytes) / 4 * 4;
-  if (R < 4) R = 4;
-  if (R > 32) R = 32;
-  pl->rows_per_stage = (int)R;
-  pl->stage_bytes = (int)(R * row_bytes);
-  int64_t S = kRingBudget / pl->stage_bytes;
+  const int nch = (int)(K / 64);
+  const int max_chunks = kStageTarget / (kBlockRows * 16);  // 48
+  const int ns = (nch + max_chunks - 1) / max_chunks;
+  pl->nslices = ns;
+  pl->slice_chunks = (nch + ns - 1) / ns;
+  pl->stage_bytes = kBlockRows * pl->slice_chunks * 16;
+  int S = kRingBudget / pl->stage_bytes;
   if (S < 2) S = 2;
   if (S > kMaxStages) S = kMaxStages;
-  pl->stages = (int)S;
+  pl->stages = S;
   pl->smem = (size_t)S * pl->stage_bytes + (size_t)pl->mt * (size_t)K;
   return pl->smem <= (size_t)kMaxSmem;
 }
@@ -453,7 +469,8 @@ cudaError_t launch_decode(const DecodeTarget* targets, int count, const int8_t* 
   a.xs_out = x_scale_out;
   a.M = (int)M;
   a.K = (int)K;
-  a.rows_per_stage = pl.rows_per_stage;
+  a.slice_chunks = pl.slice_chunks;
+  a.nslices = pl.nslices;
   a.stages = pl.stages;
   a.stage_bytes = pl.stage_bytes;
   int64_t ctas = (rows + 3) / 4;
