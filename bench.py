@@ -135,17 +135,28 @@ class DecodeStep:
                            dtype=torch.uint8, device=dev)
         lin_ws = max(bn.bitnet_linear_workspace(1, N, K) for _, N, K, _ in LAYER_SHAPES)
         self.lin_ws = torch.empty(max(lin_ws, 16), dtype=torch.uint8, device=dev)
+        # All step inputs live in one bf16 buffer and all outputs in one fp32
+        # buffer, so the end-to-end timing moves them with one copy each way.
+        in_per_layer = sum(K for _, K in INPUTS)
+        out_per_layer = sum(N for _, N, _, _ in LAYER_SHAPES)
+        self.x_all = torch.empty(layers * in_per_layer, dtype=torch.bfloat16, device=dev)
+        self.y_all = torch.empty(layers * out_per_layer, dtype=torch.float32, device=dev)
         for li in range(layers):
             L = {"W": {}, "x": {}, "xq": {}, "sx": {}, "y": {}}
+            off = li * out_per_layer
             for j, (name, N, K, _) in enumerate(LAYER_SHAPES):
                 W = synth.weights_f32(N, K, seed=seed * 100000 + li * 16 + j, device="cuda")
                 Wq, s = bn.bitnet_quantize_weights(W, ws=ws_q)
                 del W
                 L["W"][name] = (Wq, s, N, K)
-                L["y"][name] = torch.empty((1, N), dtype=torch.float32, device=dev)
+                L["y"][name] = self.y_all[off:off + N].view(1, N)
+                off += N
+            off = li * in_per_layer
             for j, (name, K) in enumerate(INPUTS):
-                L["x"][name] = synth.tokens_bf16(1, K, seed=seed * 100000 + li * 16 + 8 + j,
-                                                 device="cuda")
+                L["x"][name] = self.x_all[off:off + K].view(1, K)
+                L["x"][name].copy_(synth.tokens_bf16(1, K, seed=seed * 100000 + li * 16 + 8 + j,
+                                                     device="cuda"))
+                off += K
                 L["xq"][name] = torch.empty((1, K), dtype=torch.int8, device=dev)
                 L["sx"][name] = torch.empty(1, dtype=torch.float32, device=dev)
             self.layers.append(L)
@@ -168,7 +179,7 @@ class DecodeStep:
             for src, _ in INPUTS:
                 targets = [(L["W"][n][0], L["W"][n][1], L["y"][n])
                            for n, _, _, s in LAYER_SHAPES if s == src]
-                self.bn.bitnet_linear_bf16(L["x"][src], targets)
+                self.bn.bitnet_linear_bf16(L["x"][src], targets, weights_static=True)
 
     def step(self):
         if self.api == "fused":
@@ -188,10 +199,10 @@ class DecodeStep:
         return n
 
     def input_tensors(self):
-        return [L["x"][n] for L in self.layers for n, _ in INPUTS]
+        return [self.x_all]
 
     def output_tensors(self):
-        return [L["y"][n] for L in self.layers for n, *_ in LAYER_SHAPES]
+        return [self.y_all]
 
 
 def capture(torch, fn):

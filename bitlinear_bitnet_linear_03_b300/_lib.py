@@ -33,7 +33,7 @@ SIGNATURES = {
     "bitnet_quantize_act": (_INT, [_P, _I64, _I64, _P, _P, _P]),
     "bitnet_linear_workspace": (_SZ, [_I64, _I64, _I64]),
     "bitnet_linear": (_INT, [_P, _P, _P, _P, _I64, _I64, _I64, _P, _P, _P, _SZ, _P]),
-    "bitnet_linear_bf16": (_INT, [_P, _I64, _I64, _P, _INT, _P, _P, _P]),
+    "bitnet_linear_bf16": (_INT, [_P, _I64, _I64, _P, _INT, _P, _P, ctypes.c_uint, _P]),
     "bitnet_ffn_workspace": (_SZ, [_I64, _I64, _I64]),
     "bitnet_ffn": (_INT, [_P, _P, _F, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _P, _P, _SZ,
                           _P]),
@@ -175,9 +175,15 @@ def bitnet_linear(Wq, w_scale, xq, x_scale, K=None, y=None, acc_out=None, ws=Non
     return y
 
 
-def bitnet_linear_bf16(x, targets, xq_out=None, x_scale_out=None, stream=None):
+BITNET_WEIGHTS_STATIC = 1
+
+
+def bitnet_linear_bf16(x, targets, xq_out=None, x_scale_out=None, weights_static=False,
+                       stream=None):
     """Per-token int8 quantisation of bf16 x [M, K] and BitLinear with every
-    (Wq, w_scale, y[, acc_out]) in `targets` (all sharing x), one launch."""
+    (Wq, w_scale, y[, acc_out]) in `targets` (all sharing x), one launch.
+    weights_static: no work in flight on the stream writes the weights, so
+    they may stream in before the previous kernel has finished."""
     M, K = x.shape
     arr = (LinearTarget * len(targets))()
     keep = []
@@ -191,7 +197,7 @@ def bitnet_linear_bf16(x, targets, xq_out=None, x_scale_out=None, stream=None):
     _check("bitnet_linear_bf16", lib().bitnet_linear_bf16(
         _ptr(x, torch.bfloat16, "x"), M, K, arr, len(targets),
         _ptr(xq_out, torch.int8, "xq_out"), _ptr(x_scale_out, torch.float32, "x_scale_out"),
-        _stream(stream)))
+        BITNET_WEIGHTS_STATIC if weights_static else 0, _stream(stream)))
     return [t[2] for t in targets]
 
 

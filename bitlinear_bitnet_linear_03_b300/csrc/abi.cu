@@ -57,7 +57,7 @@ cudaError_t run_linear(const uint8_t* Wq, const float* w_scale, const int8_t* xq
                        int32_t* acc_out, void* ws, cudaStream_t s) {
   if (bitnet::decode_supported(M, K)) {
     bitnet::DecodeTarget t = {Wq, w_scale, N, y, acc_out};
-    return bitnet::launch_decode(&t, 1, xq, x_scale, nullptr, M, K, nullptr, nullptr, s);
+    return bitnet::launch_decode(&t, 1, xq, x_scale, nullptr, M, K, nullptr, nullptr, false, s);
   }
   if (bitnet::gemm_tc_eligible(M, N, K))
     return bitnet::launch_gemm_tc(Wq, w_scale, xq, x_scale, M, N, K, y, acc_out, ws, s);
@@ -172,8 +172,9 @@ bitnet_status bitnet_linear(const uint8_t* Wq, const float* w_scale, const int8_
 
 bitnet_status bitnet_linear_bf16(const uint16_t* x, int64_t M, int64_t K,
                                  const bitnet_linear_target* targets, int count, int8_t* xq_out,
-                                 float* x_scale_out, void* stream) {
+                                 float* x_scale_out, unsigned flags, void* stream) {
   if (!x || !targets) return BITNET_ERR_NULL;
+  if (flags & ~(unsigned)BITNET_WEIGHTS_STATIC) return BITNET_ERR_SHAPE;
   if (count < 1 || count > BITNET_MAX_TARGETS || M < 1 || M > BITNET_DECODE_MAX_M ||
       !valid_inner(K) || !bitnet::decode_supported(M, K))
     return BITNET_ERR_SHAPE;
@@ -193,7 +194,8 @@ bitnet_status bitnet_linear_bf16(const uint16_t* x, int64_t M, int64_t K,
   bitnet_status st = check_device();
   if (st != BITNET_OK) return st;
   return cuda_status(bitnet::launch_decode(t, count, nullptr, nullptr, x, M, K, xq_out,
-                                           x_scale_out, (cudaStream_t)stream));
+                                           x_scale_out, (flags & BITNET_WEIGHTS_STATIC) != 0,
+                                           (cudaStream_t)stream));
 }
 
 size_t bitnet_ffn_workspace(int64_t M, int64_t H, int64_t F) {

@@ -166,7 +166,8 @@ bool decode_supported(int64_t M, int64_t K);
 cudaError_t read_and_clear_decode_error(int* code, cudaStream_t s);
 cudaError_t launch_decode(const DecodeTarget* targets, int count, const int8_t* xq,
                           const float* x_scale, const uint16_t* x_bf16, int64_t M, int64_t K,
-                          int8_t* xq_out, float* x_scale_out, cudaStream_t s);
+                          int8_t* xq_out, float* x_scale_out, bool weights_static,
+                          cudaStream_t s);
 
 // BitLinear on CUDA cores, any M (gemv.cu).
 size_t gemv_workspace(int64_t M, int64_t N, int64_t K);

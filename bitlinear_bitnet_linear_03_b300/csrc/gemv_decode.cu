@@ -23,9 +23,11 @@
 //    four groups read the same chunk, so each activation read is a broadcast
 //    that touches every bank once.  The row sum is three shuffles.
 //  * Before waiting on the previous kernel the CTA asks for its whole weight
-//    range to be prefetched into L2 (a hint; weights are read only after the
-//    wait) and lets its successor launch: consecutive decode kernels overlap
-//    under programmatic dependent launch.
+//    range to be prefetched into L2 and lets its successor launch:
+//    consecutive decode kernels overlap under programmatic dependent launch.
+//    Weights are read after that wait, unless the caller declared them
+//    static (not written by any work still in flight): then the producer
+//    starts filling the ring at once, while the previous kernel finishes.
 //  * Up to kDecodeMaxTargets matrices sharing the same input run in one
 //    launch; their rows are concatenated, stages never straddle two matrices.
 //  * The input is int8 with its scales, or bf16: then every CTA forms the
@@ -79,6 +81,7 @@ struct Args {
   int nslices;
   int stages;
   int stage_bytes;   // ring slot size: kBlockRows x slice_chunks x 16 bytes
+  int weights_early; // weights may be read before the previous kernel ends
 };
 
 // ---- mbarrier / bulk-copy primitives (PTX ISA: mbarrier, cp.async.bulk)
@@ -193,11 +196,13 @@ k_gemv_decode(const __grid_constant__ Args a) {
   }
   griddep_launch_dependents();
   __syncthreads();
-  griddep_wait();
 
   // ------------------------------------------------------------ producer
   if (warp == kConsumerWarps) {
     if (lane != 0) return;
+    // Weights the caller declared static may stream in while the previous
+    // kernel on the stream is still running; otherwise wait for it first.
+    if (!a.weights_early) griddep_wait();
     int i = 0;
     for_each_stage(a, r_begin, r_end, [&](int p, int row, int nrows, int sl) {
       const int slot = i % a.stages;
@@ -234,11 +239,79 @@ k_gemv_decode(const __grid_constant__ Args a) {
   }
 
   // ------------------------------------------------------------ consumers
+  griddep_wait();
   const int tid = threadIdx.x;  // 0 .. kConsumers-1
   const int K = a.K;
   const int nitems = K >> 4;   // 16-byte fields per token row
   float xscale[MT];
-  if (a.xb != nullptr) {
+  if (a.xb != nullptr && MT <= 2 && nitems <= 2 * kConsumers) {
+    // One pass: each thread keeps its (at most two) 16-element items of x in
+    // registers between the absmax and the quantisation.
+    uint4 held[MT][2][2];
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+      float mx = 0.0f;
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int f = tid + j * kConsumers;
+        held[m][j][0] = held[m][j][1] = make_uint4(0, 0, 0, 0);
+        if (m < a.M && f < nitems) {
+          const uint4* src = reinterpret_cast<const uint4*>(a.xb + (int64_t)m * K) + 2 * f;
+          held[m][j][0] = ld_nc_v4(src);
+          held[m][j][1] = ld_nc_v4(src + 1);
+        }
+        const uint32_t e[8] = {held[m][j][0].x, held[m][j][0].y, held[m][j][0].z,
+                               held[m][j][0].w, held[m][j][1].x, held[m][j][1].y,
+                               held[m][j][1].z, held[m][j][1].w};
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+          mx = fmaxf(mx, fabsf(bf16_bits_to_float(e[t] & 0xffffu)));
+          mx = fmaxf(mx, fabsf(bf16_bits_to_float(e[t] >> 16)));
+        }
+      }
+      mx = warp_max_f32(mx);
+      if (lane == 0) s_max[warp][m] = mx;
+    }
+    consumer_sync();
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+      float mx = s_max[0][m];
+#pragma unroll
+      for (int w = 1; w < kConsumerWarps; ++w) mx = fmaxf(mx, s_max[w][m]);
+      const ActScale sc = act_scale_from_absmax(mx);
+      xscale[m] = sc.scale;
+      int sum = 0;
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int f = tid + j * kConsumers;
+        if (m < a.M && f < nitems) {
+          const uint32_t e[8] = {held[m][j][0].x, held[m][j][0].y, held[m][j][0].z,
+                                 held[m][j][0].w, held[m][j][1].x, held[m][j][1].y,
+                                 held[m][j][1].z, held[m][j][1].w};
+          uint32_t wd[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            int q[4];
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+              const int el = 4 * i + t;
+              const uint32_t h = (el & 1) ? (e[el >> 1] >> 16) : (e[el >> 1] & 0xffffu);
+              q[t] = round_clip(__fmul_rn(bf16_bits_to_float(h), sc.inv), -128.f, 127.f);
+            }
+            wd[i] = pack_i8x4(q[0], q[1], q[2], q[3]);
+            sum = dp4a_ss(wd[i], 0x01010101u, sum);
+          }
+          const uint4 packed = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+          *reinterpret_cast<uint4*>(xs + (int64_t)m * K + xs_offset(f >> 2, f & 3)) = packed;
+          if (blockIdx.x == 0 && a.xq_out != nullptr)
+            *reinterpret_cast<uint4*>(a.xq_out + (int64_t)m * K + 16 * f) = packed;
+        }
+      }
+      sum = warp_sum_i32(sum);
+      if (lane == 0 && sum) atomicAdd(&s_sumx[m], sum);
+      if (blockIdx.x == 0 && tid == 0 && a.xs_out != nullptr && m < a.M) a.xs_out[m] = xscale[m];
+    }
+  } else if (a.xb != nullptr) {
     const int nv = K >> 3;
 #pragma unroll
     for (int m = 0; m < MT; ++m) {
@@ -444,7 +517,8 @@ bool decode_supported(int64_t M, int64_t K) {
 
 cudaError_t launch_decode(const DecodeTarget* targets, int count, const int8_t* xq,
                           const float* x_scale, const uint16_t* x_bf16, int64_t M, int64_t K,
-                          int8_t* xq_out, float* x_scale_out, cudaStream_t s) {
+                          int8_t* xq_out, float* x_scale_out, bool weights_static,
+                          cudaStream_t s) {
   Plan pl;
   if (count < 1 || count > kDecodeMaxTargets || !make_plan(M, K, &pl))
     return cudaErrorNotSupported;
@@ -473,6 +547,7 @@ cudaError_t launch_decode(const DecodeTarget* targets, int count, const int8_t* 
   a.nslices = pl.nslices;
   a.stages = pl.stages;
   a.stage_bytes = pl.stage_bytes;
+  a.weights_early = weights_static ? 1 : 0;
   int64_t ctas = (rows + 3) / 4;
   if (ctas > 148) ctas = 148;
   a.rows_per_cta = (int)((rows + ctas - 1) / ctas);

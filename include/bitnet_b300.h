@@ -136,9 +136,15 @@ bitnet_status bitnet_linear(const uint8_t* Wq, const float* w_scale,
  * K % 64 == 0; K <= 65536 for M <= 2, K <= 32768 for M <= 4
  * (BITNET_ERR_SHAPE beyond); sum of N_i <= 2^30.  Needs no workspace.  The
  * kernel may start while the previous kernel on `stream` is finishing
- * (programmatic dependent launch) and waits for it before reading x. */
+ * (programmatic dependent launch) and waits for it before reading x or
+ * writing any output.
+ * flags: 0, or BITNET_WEIGHTS_STATIC to promise that no work still in flight
+ * on `stream` writes any Wq_i or w_scale_i (true for model weights quantised
+ * ahead of time); the kernel then starts streaming the weights before the
+ * previous kernel has finished.  Any other bit gives BITNET_ERR_SHAPE. */
 #define BITNET_DECODE_MAX_M 4
 #define BITNET_MAX_TARGETS 8
+#define BITNET_WEIGHTS_STATIC 1u
 typedef struct bitnet_linear_target {
   const uint8_t* Wq;
   const float* w_scale;
@@ -149,7 +155,8 @@ typedef struct bitnet_linear_target {
 
 bitnet_status bitnet_linear_bf16(const uint16_t* x, int64_t M, int64_t K,
                                  const bitnet_linear_target* targets, int count,
-                                 int8_t* xq_out, float* x_scale_out, void* stream);
+                                 int8_t* xq_out, float* x_scale_out, unsigned flags,
+                                 void* stream);
 
 /* ------------------------------------------------------------------------
  * Fused BitNet feed-forward block ([P1] subln, ReLU^2, no bias):

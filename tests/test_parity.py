@@ -236,7 +236,7 @@ def test_quantize_then_linear_chain():
 
 
 # ---------------------------------------------------------------- grouped decode from bf16
-def check_linear_bf16(M, K, Ns, seed, frac=0.01):
+def check_linear_bf16(M, K, Ns, seed, frac=0.01, weights_static=False):
     x = synth.tokens_bf16(M, K, seed=seed, outlier_frac=frac)
     packs = [oracle.quantize_weights(synth.weights_f32(N, K, seed=seed + 1 + i))
              for i, N in enumerate(Ns)]
@@ -247,7 +247,7 @@ def check_linear_bf16(M, K, Ns, seed, frac=0.01):
                         torch.empty((M, N), dtype=torch.int32, device="cuda")))
     xq_out = torch.empty((M, K), dtype=torch.int8, device="cuda")
     xs_out = torch.empty(M, dtype=torch.float32, device="cuda")
-    bn.bitnet_linear_bf16(dev_bf16(x), targets, xq_out, xs_out)
+    bn.bitnet_linear_bf16(dev_bf16(x), targets, xq_out, xs_out, weights_static=weights_static)
     qx, sx = oracle.quantize_act_bf16(x)
     assert_bits_equal(host(xq_out), qx, "xq_out")
     assert_bits_equal(host(xs_out), sx, "x_scale_out")
@@ -260,7 +260,8 @@ def check_linear_bf16(M, K, Ns, seed, frac=0.01):
 @pytest.mark.parametrize("M", [1, 2, 3, 4])
 def test_linear_bf16_decode_layer_group(M):
     # Q, K, V, up, gate of a 2B-class layer share one input
-    check_linear_bf16(M, 2560, [2560, 640, 640, 6912, 6912], seed=40 + M)
+    check_linear_bf16(M, 2560, [2560, 640, 640, 6912, 6912], seed=40 + M,
+                      weights_static=(M % 2 == 1))
 
 
 @pytest.mark.parametrize("M,K,Ns", [(1, 64, [1]), (1, 6912, [2560]), (2, 6912, [33, 2560]),
@@ -268,7 +269,7 @@ def test_linear_bf16_decode_layer_group(M):
                                     (2, 65536, [9]), (4, 32768, [70]),
                                     (3, 192, [5, 6, 7, 8, 9, 10, 11, 12]), (1, 65536, [40])])
 def test_linear_bf16_shapes(M, K, Ns):
-    check_linear_bf16(M, K, Ns, seed=M * 3 + K)
+    check_linear_bf16(M, K, Ns, seed=M * 3 + K, weights_static=True)
 
 
 def test_linear_bf16_rejects_unsupported():
