@@ -206,6 +206,10 @@ k_gemv_decode(const __grid_constant__ Args a) {
     int i = 0;
     for_each_stage(a, r_begin, r_end, [&](int p, int row, int nrows, int sl) {
       const int slot = i % a.stages;
+      // With early weights, only the first ring's worth is issued before the
+      // previous kernel has finished, so no bounded wait below can run out
+      // while this grid is still held back by its predecessor.
+      if (i == a.stages && a.weights_early) griddep_wait();
       if (i >= a.stages && !mbar_wait(smem_addr(&empty_bar[slot]), ((i / a.stages) - 1) & 1)) {
         atomicOr(&g_decode_error, 1 << kErrEmptyWait);
         return false;
