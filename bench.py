@@ -3,9 +3,10 @@
 Default workload (one "step"): a batch-1 decode step over 2B-class layer
 shapes, 30 layers with distinct weight sets (521 MB of packed ternary weights,
 4x the 126 MB L2, so every step streams its weights from HBM).  Per layer:
-three per-token int8 activation quantisations (layer input, attention output,
-FFN hidden state, bf16 N(0,1)) and seven BitLinear products (Q, O: 2560->2560;
-K, V: 2560->640; up, gate: 2560->6912; down: 6912->2560).  The step is
+four per-token int8 activation quantisations (layer input, attention output,
+post-attention residual, FFN hidden state; bf16 N(0,1)) and seven BitLinear
+products (Q, O: 2560->2560; K, V: 2560->640; up, gate: 2560->6912; down:
+6912->2560), in four dependent phases (QKV, O, up+gate, down).  The step is
 captured once in a CUDA graph and replayed.
 
 Metric: GB/s of algorithmic bytes (packed weights + activations read and
@@ -30,10 +31,15 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 HIDDEN, FFN = 2560, 6912
+# (name, N, K, input).  The inputs follow the data flow of a decoder layer:
+# Q, K, V read the normed layer input; O reads the attention output; up and
+# gate read the normed post-attention residual; down reads the FFN hidden
+# state.  Each input depends on the previous phase, so a layer is four
+# dependent BitLinear phases.
 LAYER_SHAPES = [("q", HIDDEN, HIDDEN, "x"), ("k", 640, HIDDEN, "x"), ("v", 640, HIDDEN, "x"),
-                ("o", HIDDEN, HIDDEN, "attn"), ("up", FFN, HIDDEN, "x"),
-                ("gate", FFN, HIDDEN, "x"), ("down", HIDDEN, FFN, "h")]
-INPUTS = [("x", HIDDEN), ("attn", HIDDEN), ("h", FFN)]
+                ("o", HIDDEN, HIDDEN, "attn"), ("up", FFN, HIDDEN, "x2"),
+                ("gate", FFN, HIDDEN, "x2"), ("down", HIDDEN, FFN, "h")]
+INPUTS = [("x", HIDDEN), ("attn", HIDDEN), ("x2", HIDDEN), ("h", FFN)]
 METRIC = "BitLinear decode GB/s & % HBM roofline; prefill int8 TOPS & % tensor peak"
 WORKLOAD = ("decode step, batch 1, 2B-class shapes (hidden 2560, FFN 6912), 30 layers of "
             "distinct ternary weights")
@@ -47,7 +53,7 @@ def parse_args():
     ap.add_argument("--layers", type=int, default=30)
     ap.add_argument("--impl", default="b300", choices=["b300", "reference"])
     ap.add_argument("--api", default="fused", choices=["fused", "split"],
-                    help="fused: bitnet_linear_bf16 per shared input (3 launches a layer); "
+                    help="fused: bitnet_linear_bf16 per shared input (4 launches a layer); "
                          "split: bitnet_quantize_act + bitnet_linear per matrix")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-secondary", action="store_true")
@@ -56,7 +62,7 @@ def parse_args():
 
 def layer_bytes(api="fused"):
     """Algorithmic bytes of one layer.
-    fused: each of the three calls reads its bf16 input once; each BitLinear
+    fused: each of the four calls reads its bf16 input once; each BitLinear
            reads packed W and its scale and writes fp32 y.
     split: act-quant reads bf16 and writes int8 + scale; each BitLinear reads
            packed W, int8 x, two scales and writes fp32 y."""
@@ -442,7 +448,7 @@ def cpu_baseline(budget_s=12.0):
     dt = time.perf_counter() - t0
     return {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": threads,
             "kind": "oracle",
-            "sample": f"{layers} repetitions of one decode layer (3 act quants + 7 BitLinear, "
+            "sample": f"{layers} repetitions of one decode layer (4 act quants + 7 BitLinear, "
                       f"{layer_bytes('fused')} algorithmic bytes each) of the 30-layer step, "
                       f"{dt:.1f} s"}
 
@@ -471,7 +477,7 @@ def run_reference_arm(args, rank):
                    "parallelism": "replicas x1"},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
                          "kind": "oracle",
-                         "sample": "each step: the 3 act quants of one decode layer plus one "
+                         "sample": "each step: the 4 act quants of one decode layer plus one "
                                    "of its 7 BitLinear products, cycling Q,K,V,O,up,gate,down"},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
