@@ -44,12 +44,14 @@ __device__ int g_decode_error;
 
 namespace {
 
-constexpr int kConsumerWarps = 8;
+constexpr int kGroups = 2;                  // consumer warp groups, alternating row blocks
+constexpr int kGroupWarps = 8;
+constexpr int kConsumerWarps = kGroups * kGroupWarps;
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kThreads = kConsumers + 32;  // + one producer warp
 constexpr int kMaxStages = 8;
 constexpr int kRingBudget = 96 * 1024;
-constexpr int kStageTarget = 24 * 1024;
+constexpr int kMaxSliceChunks = 48;        // 32 rows x 48 chunks x 16 B = 24 KB per stage
 constexpr int kMaxSmem = 227 * 1024 - 1024;  // dynamic part; static barriers etc. fit in the rest
 constexpr int kPrefetchMax = 1 << 16;
 constexpr long long kWaitCycles = 2000000000ll;  // ~1 s at 2 GHz
@@ -138,27 +140,48 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   return v;
 }
 
-// Byte offset of field s (16 bytes) of chunk c in the swizzled activation row.
+// Byte offset of field s (16 bytes) of chunk c in the swizzled activation
+// row: field s sits in slot (s + c/2) & 3 of the chunk's 64 bytes, so the
+// eight chunks a quarter-warp reads at once land on eight distinct 16-byte
+// bank groups.
 __device__ __forceinline__ int xs_offset(int c, int s) { return 64 * c + 16 * ((s + (c >> 1)) & 3); }
 
 // The CTA's stage sequence.  Rows of each matrix overlapping the CTA's range
-// are taken in blocks of kBlockRows; each block is streamed as `nslices`
-// K-slices of slice_chunks 64-weight chunks (the last may be shorter).
-// Calls f(p, first_row, nrows, slice) in order; stops when f returns false.
+// are taken in blocks of kBlockRows (block b goes to consumer group b % 2);
+// each block is streamed as `nslices` K-slices of slice_chunks 64-weight
+// chunks (the last may be shorter).  Calls f(p, first_row, nrows, slice, b)
+// in order; stops when f returns false.
 constexpr int kBlockRows = 32;
 template <typename F>
 __device__ __forceinline__ void for_each_stage(const Args& a, int r_begin, int r_end, F&& f) {
+  int b = 0;
   for (int p = 0; p < a.count; ++p) {
     const int lo = max(r_begin, a.t[p].row0);
     const int hi = min(r_end, a.t[p].row0 + a.t[p].N);
-    for (int r = lo; r < hi; r += kBlockRows)
+    for (int r = lo; r < hi; r += kBlockRows, ++b)
       for (int sl = 0; sl < a.nslices; ++sl)
-        if (!f(p, r - a.t[p].row0, min(kBlockRows, hi - r), sl)) return;
+        if (!f(p, r - a.t[p].row0, min(kBlockRows, hi - r), sl, b)) return;
   }
 }
 
+// Ring slot and phase of a stage: group g owns slots g*H .. g*H + H-1 and
+// takes its stages in order, so each slot's mbarrier phases are consumed in
+// sequence by one group.
+struct SlotPhase {
+  int slot;
+  int use;  // how many times this slot was filled before
+};
+__device__ __forceinline__ SlotPhase slot_of(const Args& a, int b, int sl) {
+  const int H = a.stages / kGroups;
+  const int ig = (b / kGroups) * a.nslices + sl;  // stage index within the group
+  SlotPhase r;
+  r.slot = (b % kGroups) * H + ig % H;
+  r.use = ig / H;
+  return r;
+}
+
 template <int MT>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
 k_gemv_decode(const __grid_constant__ Args a) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t full_bar[kMaxStages];
@@ -177,7 +200,7 @@ k_gemv_decode(const __grid_constant__ Args a) {
   if (threadIdx.x == 0) {
     for (int s = 0; s < a.stages; ++s) {
       mbar_init(smem_addr(&full_bar[s]), 1);
-      mbar_init(smem_addr(&empty_bar[s]), kConsumerWarps);
+      mbar_init(smem_addr(&empty_bar[s]), kGroupWarps);
     }
     mbar_fence_init();
     for (int m = 0; m < MT; ++m) s_sumx[m] = 0;
@@ -202,23 +225,27 @@ k_gemv_decode(const __grid_constant__ Args a) {
     if (lane != 0) return;
     // Weights the caller declared static may stream in while the previous
     // kernel on the stream is still running; otherwise wait for it first.
-    if (!a.weights_early) griddep_wait();
-    int i = 0;
-    for_each_stage(a, r_begin, r_end, [&](int p, int row, int nrows, int sl) {
-      const int slot = i % a.stages;
-      // With early weights, only the first ring's worth is issued before the
-      // previous kernel has finished, so no bounded wait below can run out
-      // while this grid is still held back by its predecessor.
-      if (i == a.stages && a.weights_early) griddep_wait();
-      if (i >= a.stages && !mbar_wait(smem_addr(&empty_bar[slot]), ((i / a.stages) - 1) & 1)) {
-        atomicOr(&g_decode_error, 1 << kErrEmptyWait);
-        return false;
+    // Either way every bounded wait below starts after the dependency wait.
+    bool dep_done = !a.weights_early;
+    if (dep_done) griddep_wait();
+    int issued[kGroups] = {0, 0};
+    for_each_stage(a, r_begin, r_end, [&](int p, int row, int nrows, int sl, int b) {
+      const SlotPhase sp = slot_of(a, b, sl);
+      if (sp.use > 0) {
+        if (!dep_done) {
+          griddep_wait();
+          dep_done = true;
+        }
+        if (!mbar_wait(smem_addr(&empty_bar[sp.slot]), (sp.use - 1) & 1)) {
+          atomicOr(&g_decode_error, 1 << kErrEmptyWait);
+          return false;
+        }
       }
       const int c0 = sl * a.slice_chunks;
       const int chunks = min(a.slice_chunks, nch - c0);
       const uint32_t slice_bytes = (uint32_t)chunks * 16u;
-      const uint32_t fb = smem_addr(&full_bar[slot]);
-      const uint32_t dst = ring + slot * a.stage_bytes;
+      const uint32_t fb = smem_addr(&full_bar[sp.slot]);
+      const uint32_t dst = ring + sp.slot * a.stage_bytes;
       const uint8_t* src = a.t[p].Wq + (int64_t)row * row_bytes + c0 * 16;
       mbar_arrive_expect_tx(fb, slice_bytes * (uint32_t)nrows);
       if (a.nslices == 1) {
@@ -228,17 +255,21 @@ k_gemv_decode(const __grid_constant__ Args a) {
         for (int r = 0; r < nrows; ++r)
           bulk_copy_g2s(dst + r * slice_bytes, src + (int64_t)r * row_bytes, slice_bytes, fb);
       }
-      ++i;
+      ++issued[b % kGroups];
       return true;
     });
     // Never leave the CTA with a copy in flight: wait for the last copy of
-    // every slot to land.
-    const int first = i > a.stages ? i - a.stages : 0;
-    for (int j = first; j < i; ++j)
-      if (!mbar_wait(smem_addr(&full_bar[j % a.stages]), (j / a.stages) & 1)) {
-        atomicOr(&g_decode_error, 1 << kErrDrainWait);
-        break;
-      }
+    // every slot of both groups to land.
+    const int H = a.stages / kGroups;
+    for (int g = 0; g < kGroups; ++g) {
+      const int first = issued[g] > H ? issued[g] - H : 0;
+      for (int j = first; j < issued[g]; ++j)
+        if (!mbar_wait(smem_addr(&full_bar[g * H + j % H]), (j / H) & 1)) {
+          atomicOr(&g_decode_error, 1 << kErrDrainWait);
+          g = kGroups;
+          break;
+        }
+    }
     return;
   }
 
@@ -403,16 +434,30 @@ k_gemv_decode(const __grid_constant__ Args a) {
 #pragma unroll
   for (int m = 0; m < MT; ++m) sumx[m] = s_sumx[m];
 
-  // Warp w owns rows 4w .. 4w+3 of every row block; 8-lane group grp owns
-  // row 4w + grp, lane sub reads chunks sub, sub+8, ... of each slice.
+  // Group g takes row blocks g, g+2, ...; its warp wl owns rows 4wl .. 4wl+3
+  // of each block, 8-lane group grp row 4wl + grp, and lane sub chunks sub,
+  // sub+8, ... of each slice.  Slices start at multiples of 8 chunks, so the
+  // activation slot k of every chunk this lane reads holds the same field
+  // s_k = (k - sub/2) & 3: the lane masks the weights for that field and
+  // keeps one accumulator per slot, scaled by 4^s_k.
+  const int gw = warp / kGroupWarps, wl = warp % kGroupWarps;
   const int grp = lane >> 3, sub = lane & 7;
-  const int r = warp * 4 + grp;
+  const int r = wl * 4 + grp;
+  const int rot = sub >> 1;
+  uint32_t mask[4];
+  int shift[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int sk = (k - rot) & 3;
+    mask[k] = 0x03030303u << (2 * sk);
+    shift[k] = 2 * sk;
+  }
   const uint32_t xs_base = smem_addr(xs);
   int acc[MT][4];
-  int i = 0;
-  for_each_stage(a, r_begin, r_end, [&](int p, int row0, int nrows, int sl) {
-    const int slot = i % a.stages;
-    if (!mbar_wait(smem_addr(&full_bar[slot]), (i / a.stages) & 1)) {
+  for_each_stage(a, r_begin, r_end, [&](int p, int row0, int nrows, int sl, int b) {
+    if (b % kGroups != gw) return true;
+    const SlotPhase sp = slot_of(a, b, sl);
+    if (!mbar_wait(smem_addr(&full_bar[sp.slot]), sp.use & 1)) {
       if (lane == 0) atomicOr(&g_decode_error, 1 << kErrFullWait);
       return false;
     }
@@ -424,42 +469,40 @@ k_gemv_decode(const __grid_constant__ Args a) {
     const int c0 = sl * a.slice_chunks;
     const int chunks = min(a.slice_chunks, nch - c0);
     if (valid) {
-      const uint32_t wbase = ring + slot * a.stage_bytes + (uint32_t)(r * chunks * 16);
+      uint32_t wp = ring + sp.slot * a.stage_bytes + (uint32_t)(r * chunks * 16) + 16 * sub;
+      uint32_t xp = xs_base + 64 * (c0 + sub);
 #pragma unroll 2
-      for (int c = sub; c < chunks; c += 8) {
-        const uint4 wv = lds128(wbase + 16 * c);
+      for (int c = sub; c < chunks; c += 8, wp += 128, xp += 512) {
+        const uint4 wv = lds128(wp);
         const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
-        const int cg = c0 + c;
 #pragma unroll
         for (int m = 0; m < MT; ++m) {
-          const uint32_t xb = xs_base + m * K;
-          const uint4 x0 = lds128(xb + xs_offset(cg, 0));
-          const uint4 x1 = lds128(xb + xs_offset(cg, 1));
-          const uint4 x2 = lds128(xb + xs_offset(cg, 2));
-          const uint4 x3 = lds128(xb + xs_offset(cg, 3));
+          const uint32_t xm = xp + m * K;
+          const uint4 x0 = lds128(xm), x1 = lds128(xm + 16), x2 = lds128(xm + 32),
+                      x3 = lds128(xm + 48);
           const uint32_t f0[4] = {x0.x, x0.y, x0.z, x0.w};
           const uint32_t f1[4] = {x1.x, x1.y, x1.z, x1.w};
           const uint32_t f2[4] = {x2.x, x2.y, x2.z, x2.w};
           const uint32_t f3[4] = {x3.x, x3.y, x3.z, x3.w};
 #pragma unroll
           for (int w = 0; w < 4; ++w) {
-            acc[m][0] = dp4a_us(ww[w] & 0x03030303u, f0[w], acc[m][0]);
-            acc[m][1] = dp4a_us(ww[w] & 0x0c0c0c0cu, f1[w], acc[m][1]);
-            acc[m][2] = dp4a_us(ww[w] & 0x30303030u, f2[w], acc[m][2]);
-            acc[m][3] = dp4a_us(ww[w] & 0xc0c0c0c0u, f3[w], acc[m][3]);
+            acc[m][0] = dp4a_us(ww[w] & mask[0], f0[w], acc[m][0]);
+            acc[m][1] = dp4a_us(ww[w] & mask[1], f1[w], acc[m][1]);
+            acc[m][2] = dp4a_us(ww[w] & mask[2], f2[w], acc[m][2]);
+            acc[m][3] = dp4a_us(ww[w] & mask[3], f3[w], acc[m][3]);
           }
         }
       }
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(smem_addr(&empty_bar[slot]));
-    ++i;
+    if (lane == 0) mbar_arrive(smem_addr(&empty_bar[sp.slot]));
     if (sl == a.nslices - 1) {
       const Target& T = a.t[p];
       const float ws = *T.w_scale;
 #pragma unroll
       for (int m = 0; m < MT; ++m) {
-        int t = acc[m][0] + (acc[m][1] >> 2) + (acc[m][2] >> 4) + (acc[m][3] >> 6);
+        int t = (acc[m][0] >> shift[0]) + (acc[m][1] >> shift[1]) + (acc[m][2] >> shift[2]) +
+                (acc[m][3] >> shift[3]);
         t += __shfl_xor_sync(0xffffffffu, t, 4);
         t += __shfl_xor_sync(0xffffffffu, t, 2);
         t += __shfl_xor_sync(0xffffffffu, t, 1);
@@ -484,13 +527,20 @@ bool make_plan(int64_t M, int64_t K, Plan* pl) {
   if (M < 1 || M > kDecodeMaxM || K < 64 || K % 64 != 0 || K > 65536) return false;
   pl->mt = M <= 1 ? 1 : M <= 2 ? 2 : 4;
   const int nch = (int)(K / 64);
-  const int max_chunks = kStageTarget / (kBlockRows * 16);  // 48
-  const int ns = (nch + max_chunks - 1) / max_chunks;
-  pl->nslices = ns;
-  pl->slice_chunks = (nch + ns - 1) / ns;
+  if (nch <= kMaxSliceChunks) {
+    pl->nslices = 1;
+    pl->slice_chunks = nch;
+  } else {
+    // slices start on multiples of 8 chunks (see the consumer loop)
+    int ns = (nch + kMaxSliceChunks - 1) / kMaxSliceChunks;
+    int sc = ((nch + ns - 1) / ns + 7) / 8 * 8;
+    pl->slice_chunks = sc;
+    pl->nslices = (nch + sc - 1) / sc;
+  }
   pl->stage_bytes = kBlockRows * pl->slice_chunks * 16;
   int S = kRingBudget / pl->stage_bytes;
-  if (S < 2) S = 2;
+  S = S / kGroups * kGroups;
+  if (S < 2 * kGroups) S = 2 * kGroups;
   if (S > kMaxStages) S = kMaxStages;
   pl->stages = S;
   pl->smem = (size_t)S * pl->stage_bytes + (size_t)pl->mt * (size_t)K;
