@@ -44,7 +44,7 @@ __device__ int g_decode_error;
 
 namespace {
 
-constexpr int kGroups = 2;                  // consumer warp groups, alternating row blocks
+constexpr int kGroups = 1;                  // consumer warp groups, alternating row blocks
 constexpr int kGroupWarps = 8;
 constexpr int kConsumerWarps = kGroups * kGroupWarps;
 constexpr int kConsumers = kConsumerWarps * 32;
@@ -181,7 +181,7 @@ __device__ __forceinline__ SlotPhase slot_of(const Args& a, int b, int sl) {
 }
 
 template <int MT>
-__global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
+__global__ void __launch_bounds__(kThreads, MT <= 2 ? 2 : 1)
 k_gemv_decode(const __grid_constant__ Args a) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t full_bar[kMaxStages];
@@ -228,7 +228,7 @@ k_gemv_decode(const __grid_constant__ Args a) {
     // Either way every bounded wait below starts after the dependency wait.
     bool dep_done = !a.weights_early;
     if (dep_done) griddep_wait();
-    int issued[kGroups] = {0, 0};
+    int issued[kGroups] = {};
     for_each_stage(a, r_begin, r_end, [&](int p, int row, int nrows, int sl, int b) {
       const SlotPhase sp = slot_of(a, b, sl);
       if (sp.use > 0) {
@@ -453,7 +453,11 @@ k_gemv_decode(const __grid_constant__ Args a) {
     shift[k] = 2 * sk;
   }
   const uint32_t xs_base = smem_addr(xs);
-  int acc[MT][4];
+  // acc[m][k][i]: independent dp4a chains per token (slot k, word i % NI).
+  // One token needs 16 chains to keep the issue slots busy; more tokens bring
+  // their own chains.
+  constexpr int NI = MT == 1 ? 4 : 1;
+  int acc[MT][4][NI];
   for_each_stage(a, r_begin, r_end, [&](int p, int row0, int nrows, int sl, int b) {
     if (b % kGroups != gw) return true;
     const SlotPhase sp = slot_of(a, b, sl);
@@ -463,34 +467,63 @@ k_gemv_decode(const __grid_constant__ Args a) {
     }
     if (sl == 0) {
 #pragma unroll
-      for (int m = 0; m < MT; ++m) acc[m][0] = acc[m][1] = acc[m][2] = acc[m][3] = 0;
+      for (int m = 0; m < MT; ++m)
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+#pragma unroll
+          for (int i = 0; i < NI; ++i) acc[m][k][i] = 0;
     }
     const bool valid = r < nrows;
     const int c0 = sl * a.slice_chunks;
     const int chunks = min(a.slice_chunks, nch - c0);
-    if (valid) {
+    if (valid && sub < chunks) {
       uint32_t wp = ring + sp.slot * a.stage_bytes + (uint32_t)(r * chunks * 16) + 16 * sub;
       uint32_t xp = xs_base + 64 * (c0 + sub);
-#pragma unroll 2
-      for (int c = sub; c < chunks; c += 8, wp += 128, xp += 512) {
-        const uint4 wv = lds128(wp);
+      // Operands of the current chunk; the next chunk's are loaded before
+      // the current one is consumed.
+      uint4 wv = lds128(wp);
+      uint4 xv[MT][4];
+#pragma unroll
+      for (int m = 0; m < MT; ++m)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) xv[m][k] = lds128(xp + m * K + 16 * k);
+      // One token: the next chunk's operands are loaded before the current
+      // one is consumed.  More tokens: enough independent loads already.
+      constexpr int NB = MT == 1 ? MT : 1;
+      for (int c = sub;;) {
+        const bool more = c + 8 < chunks;
+        uint4 wn = make_uint4(0, 0, 0, 0);
+        uint4 xn[NB][4];
+        if (MT == 1 && more) {
+          wn = lds128(wp + 128);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) xn[0][k] = lds128(xp + 512 + 16 * k);
+        }
         const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
 #pragma unroll
         for (int m = 0; m < MT; ++m) {
-          const uint32_t xm = xp + m * K;
-          const uint4 x0 = lds128(xm), x1 = lds128(xm + 16), x2 = lds128(xm + 32),
-                      x3 = lds128(xm + 48);
-          const uint32_t f0[4] = {x0.x, x0.y, x0.z, x0.w};
-          const uint32_t f1[4] = {x1.x, x1.y, x1.z, x1.w};
-          const uint32_t f2[4] = {x2.x, x2.y, x2.z, x2.w};
-          const uint32_t f3[4] = {x3.x, x3.y, x3.z, x3.w};
 #pragma unroll
-          for (int w = 0; w < 4; ++w) {
-            acc[m][0] = dp4a_us(ww[w] & mask[0], f0[w], acc[m][0]);
-            acc[m][1] = dp4a_us(ww[w] & mask[1], f1[w], acc[m][1]);
-            acc[m][2] = dp4a_us(ww[w] & mask[2], f2[w], acc[m][2]);
-            acc[m][3] = dp4a_us(ww[w] & mask[3], f3[w], acc[m][3]);
+          for (int k = 0; k < 4; ++k) {
+            const uint32_t xw[4] = {xv[m][k].x, xv[m][k].y, xv[m][k].z, xv[m][k].w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              acc[m][k][i % NI] = dp4a_us(ww[i] & mask[k], xw[i], acc[m][k][i % NI]);
           }
+        }
+        if (!more) break;
+        c += 8;
+        wp += 128;
+        xp += 512;
+        if (MT == 1) {
+          wv = wn;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) xv[0][k] = xn[0][k];
+        } else {
+          wv = lds128(wp);
+#pragma unroll
+          for (int m = 0; m < MT; ++m)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) xv[m][k] = lds128(xp + m * K + 16 * k);
         }
       }
     }
@@ -501,8 +534,15 @@ k_gemv_decode(const __grid_constant__ Args a) {
       const float ws = *T.w_scale;
 #pragma unroll
       for (int m = 0; m < MT; ++m) {
-        int t = (acc[m][0] >> shift[0]) + (acc[m][1] >> shift[1]) + (acc[m][2] >> shift[2]) +
-                (acc[m][3] >> shift[3]);
+        int t = 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+        {
+          int u = 0;
+#pragma unroll
+          for (int i = 0; i < NI; ++i) u += acc[m][k][i];
+          t += u >> shift[k];
+        }
         t += __shfl_xor_sync(0xffffffffu, t, 4);
         t += __shfl_xor_sync(0xffffffffu, t, 2);
         t += __shfl_xor_sync(0xffffffffu, t, 1);
