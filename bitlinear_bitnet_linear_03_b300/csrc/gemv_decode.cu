@@ -436,24 +436,18 @@ k_gemv_decode(const __grid_constant__ Args a) {
 
   // Group g takes row blocks g, g+2, ...; its warp wl owns rows 4wl .. 4wl+3
   // of each block, 8-lane group grp row 4wl + grp, and lane sub chunks sub,
-  // sub+8, ... of each slice.  Slices start at multiples of 8 chunks, so the
-  // activation slot k of every chunk this lane reads holds the same field
-  // s_k = (k - sub/2) & 3: the lane masks the weights for that field and
-  // keeps one accumulator per slot, scaled by 4^s_k.
+  // sub+8, ... of each slice.  Slices start at multiples of 8 chunks, so in
+  // every chunk this lane reads, field s sits at the same slot
+  // (s + sub/2) & 3: xo[s] is its byte offset within the chunk.  The eight
+  // lanes of a quarter-warp then read eight distinct 16-byte bank groups.
   const int gw = warp / kGroupWarps, wl = warp % kGroupWarps;
   const int grp = lane >> 3, sub = lane & 7;
   const int r = wl * 4 + grp;
-  const int rot = sub >> 1;
-  uint32_t mask[4];
-  int shift[4];
+  uint32_t xo[4];
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const int sk = (k - rot) & 3;
-    mask[k] = 0x03030303u << (2 * sk);
-    shift[k] = 2 * sk;
-  }
+  for (int k = 0; k < 4; ++k) xo[k] = 16u * (uint32_t)((k + (sub >> 1)) & 3);
   const uint32_t xs_base = smem_addr(xs);
-  // acc[m][k][i]: independent dp4a chains per token (slot k, word i % NI).
+  // acc[m][k][i]: independent dp4a chains per token (field k, word i % NI).
   // One token needs 16 chains to keep the issue slots busy; more tokens bring
   // their own chains.
   constexpr int NI = MT == 1 ? 4 : 1;
@@ -486,7 +480,7 @@ k_gemv_decode(const __grid_constant__ Args a) {
 #pragma unroll
       for (int m = 0; m < MT; ++m)
 #pragma unroll
-        for (int k = 0; k < 4; ++k) xv[m][k] = lds128(xp + m * K + 16 * k);
+        for (int k = 0; k < 4; ++k) xv[m][k] = lds128(xp + m * K + xo[k]);
       // One token: the next chunk's operands are loaded before the current
       // one is consumed.  More tokens: enough independent loads already.
       constexpr int NB = MT == 1 ? MT : 1;
@@ -497,7 +491,7 @@ k_gemv_decode(const __grid_constant__ Args a) {
         if (MT == 1 && more) {
           wn = lds128(wp + 128);
 #pragma unroll
-          for (int k = 0; k < 4; ++k) xn[0][k] = lds128(xp + 512 + 16 * k);
+          for (int k = 0; k < 4; ++k) xn[0][k] = lds128(xp + 512 + xo[k]);
         }
         const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
 #pragma unroll
@@ -507,7 +501,8 @@ k_gemv_decode(const __grid_constant__ Args a) {
             const uint32_t xw[4] = {xv[m][k].x, xv[m][k].y, xv[m][k].z, xv[m][k].w};
 #pragma unroll
             for (int i = 0; i < 4; ++i)
-              acc[m][k][i % NI] = dp4a_us(ww[i] & mask[k], xw[i], acc[m][k][i % NI]);
+              acc[m][k][i % NI] =
+                  dp4a_us(ww[i] & (0x03030303u << (2 * k)), xw[i], acc[m][k][i % NI]);
           }
         }
         if (!more) break;
@@ -523,7 +518,7 @@ k_gemv_decode(const __grid_constant__ Args a) {
 #pragma unroll
           for (int m = 0; m < MT; ++m)
 #pragma unroll
-            for (int k = 0; k < 4; ++k) xv[m][k] = lds128(xp + m * K + 16 * k);
+            for (int k = 0; k < 4; ++k) xv[m][k] = lds128(xp + m * K + xo[k]);
         }
       }
     }
@@ -541,7 +536,7 @@ k_gemv_decode(const __grid_constant__ Args a) {
           int u = 0;
 #pragma unroll
           for (int i = 0; i < NI; ++i) u += acc[m][k][i];
-          t += u >> shift[k];
+          t += u >> (2 * k);
         }
         t += __shfl_xor_sync(0xffffffffu, t, 4);
         t += __shfl_xor_sync(0xffffffffu, t, 2);
