@@ -2,32 +2,36 @@
 //
 // What is computed is the BitLinear product of "BitNet.cpp deep dive"
 // (dashen-tech), §3.1: acc = sum_pos - sum_neg over the ternary weights of a
-// row, then y = (float)acc * (x_scale * w_scale).  As in gemv.cu the stored
-// code c = q + 1 is used directly, sum q x = sum c x - sum x, with one AND and
-// one byte dot product (dp4a) per four weights; every sum is an integer, so
-// the result is exact and order-free.
+// row, then y = (float)acc * (x_scale * w_scale).  The stored code c = q + 1
+// is used directly, sum q x = sum c x - sum x: in a 16-byte block of the
+// packed layout, word i masked with 0x03030303 << 2s holds 4^s times the
+// codes of weights 16s + 4i + {0..3}, so one AND and one byte dot product
+// (dp4a) cover four weights; field s keeps its own accumulator and the 4^s is
+// removed by an exact shift.  Every sum is an integer: the result is exact
+// and independent of order.
 //
 // Layout of the work (decode is bound by the packed-weight stream):
 //  * One producer lane streams the CTA's weight rows into a ring of shared-
 //    memory stages with bulk asynchronous copies (cp.async.bulk, completion
-//    counted on an mbarrier per stage).  A stage is a block of 32 rows times
-//    a K-slice of at most 48 64-weight chunks (24 KB); when the slice is the
-//    whole row the block is one contiguous copy, otherwise one copy per row.
-//  * Every one of the eight consumer warps takes part in every stage, in
-//    order (so the parity of each mbarrier phase is unambiguous): warp w owns
-//    rows 4w .. 4w+3 of each block, an 8-lane group owns a row and lane
-//    (l % 8) reads 16-byte chunks l%8, l%8 + 8, ... of the slice (128
-//    contiguous bytes per group per step); row sums carry across the
-//    K-slices of a block in registers.  The
-//    int8 activations sit in shared memory in a swizzled chunk layout; the
-//    four groups read the same chunk, so each activation read is a broadcast
-//    that touches every bank once.  The row sum is three shuffles.
+//    counted on an mbarrier per stage).  A stage is R whole rows of one
+//    matrix, i.e. one contiguous copy of about 20-24 KB (the copy engine
+//    sustains full HBM bandwidth only with large copies).
+//  * Eight consumer warps take part in every stage, in order, so the parity
+//    of each mbarrier phase is unambiguous.  The warps split K into `wk`
+//    parts and the stage's rows into 8/wk groups.  Lane l of a warp owns the
+//    64-weight chunks l, l+32, ... of its K part for the whole kernel: their
+//    int8 activations are loaded into registers once, and a row costs the
+//    lane one 16-byte shared load, 16 ANDs and 16 dp4a per chunk; the 32
+//    lanes read 512 contiguous bytes of the row.  A row's lane sums meet in
+//    one warp reduction (redux.sync); with wk > 1 the K parts meet through
+//    shared memory after each stage.
 //  * Before waiting on the previous kernel the CTA asks for its whole weight
 //    range to be prefetched into L2 and lets its successor launch:
 //    consecutive decode kernels overlap under programmatic dependent launch.
 //    Weights are read after that wait, unless the caller declared them
 //    static (not written by any work still in flight): then the producer
-//    starts filling the ring at once, while the previous kernel finishes.
+//    fills the first ring's worth at once, while the previous kernel
+//    finishes.
 //  * Up to kDecodeMaxTargets matrices sharing the same input run in one
 //    launch; their rows are concatenated, stages never straddle two matrices.
 //  * The input is int8 with its scales, or bf16: then every CTA forms the
@@ -44,15 +48,14 @@ __device__ int g_decode_error;
 
 namespace {
 
-constexpr int kGroups = 1;                  // consumer warp groups, alternating row blocks
-constexpr int kGroupWarps = 8;
-constexpr int kConsumerWarps = kGroups * kGroupWarps;
+constexpr int kConsumerWarps = 8;
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kThreads = kConsumers + 32;  // + one producer warp
 constexpr int kMaxStages = 8;
 constexpr int kRingBudget = 96 * 1024;
-constexpr int kMaxSliceChunks = 48;        // 32 rows x 48 chunks x 16 B = 24 KB per stage
-constexpr int kMaxSmem = 227 * 1024 - 1024;  // dynamic part; static barriers etc. fit in the rest
+constexpr int kStageTarget = 24 * 1024;
+constexpr int kMaxRowsPerWarp = 8;         // rows of one stage handled by one warp
+constexpr int kMaxSmem = 227 * 1024 - 4096;  // dynamic part; the static arrays fit in the rest
 constexpr int kPrefetchMax = 1 << 16;
 constexpr long long kWaitCycles = 2000000000ll;  // ~1 s at 2 GHz
 constexpr int kErrFullWait = 1;
@@ -79,11 +82,12 @@ struct Args {
   int8_t* xq_out;        // optional copy of the quantised bf16 input
   float* xs_out;
   int M, K;
-  int slice_chunks;  // 64-weight chunks per K-slice (one stage = one block x one slice)
-  int nslices;
+  int wk;              // warps splitting K (1, 2, 4 or 8)
+  int kpart;           // 64-weight chunks per K part
+  int rows_per_stage;  // R: whole rows per ring slot
   int stages;
-  int stage_bytes;   // ring slot size: kBlockRows x slice_chunks x 16 bytes
-  int weights_early; // weights may be read before the previous kernel ends
+  int stage_bytes;     // R * K / 4
+  int weights_early;   // weights may be read before the previous kernel ends
 };
 
 // ---- mbarrier / bulk-copy primitives (PTX ISA: mbarrier, cp.async.bulk)
@@ -140,47 +144,49 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   return v;
 }
 
-// Byte offset of field s (16 bytes) of chunk c in the swizzled activation
-// row: field s sits in slot (s + c/2) & 3 of the chunk's 64 bytes, so the
-// eight chunks a quarter-warp reads at once land on eight distinct 16-byte
-// bank groups.
-__device__ __forceinline__ int xs_offset(int c, int s) { return 64 * c + 16 * ((s + (c >> 1)) & 3); }
-
-// The CTA's stage sequence.  Rows of each matrix overlapping the CTA's range
-// are taken in blocks of kBlockRows (block b goes to consumer group b % 2);
-// each block is streamed as `nslices` K-slices of slice_chunks 64-weight
-// chunks (the last may be shorter).  Calls f(p, first_row, nrows, slice, b)
-// in order; stops when f returns false.
-constexpr int kBlockRows = 32;
+// The CTA's stage sequence: for each matrix overlapping the CTA's rows, the
+// rows in pieces of at most rows_per_stage.  Calls f(p, first_row, nrows) in
+// order; stops when f returns false.
 template <typename F>
 __device__ __forceinline__ void for_each_stage(const Args& a, int r_begin, int r_end, F&& f) {
-  int b = 0;
   for (int p = 0; p < a.count; ++p) {
     const int lo = max(r_begin, a.t[p].row0);
     const int hi = min(r_end, a.t[p].row0 + a.t[p].N);
-    for (int r = lo; r < hi; r += kBlockRows, ++b)
-      for (int sl = 0; sl < a.nslices; ++sl)
-        if (!f(p, r - a.t[p].row0, min(kBlockRows, hi - r), sl, b)) return;
+    for (int r = lo; r < hi; r += a.rows_per_stage)
+      if (!f(p, r - a.t[p].row0, min(a.rows_per_stage, hi - r))) return;
   }
 }
 
-// Ring slot and phase of a stage: group g owns slots g*H .. g*H + H-1 and
-// takes its stages in order, so each slot's mbarrier phases are consumed in
-// sequence by one group.
-struct SlotPhase {
-  int slot;
-  int use;  // how many times this slot was filled before
-};
-__device__ __forceinline__ SlotPhase slot_of(const Args& a, int b, int sl) {
-  const int H = a.stages / kGroups;
-  const int ig = (b / kGroups) * a.nslices + sl;  // stage index within the group
-  SlotPhase r;
-  r.slot = (b % kGroups) * H + ig % H;
-  r.use = ig / H;
-  return r;
+// Partial dot products of one row for this lane: J chunks, MT tokens, one
+// accumulator per field (scaled by 4^s), folded to one int per token.
+template <int MT, int J>
+__device__ __forceinline__ void row_partial(uint32_t wrow, int valid_j, const uint4 (&xr)[MT][J][4],
+                                            int (&v)[MT]) {
+  int acc[MT][4];
+#pragma unroll
+  for (int m = 0; m < MT; ++m) acc[m][0] = acc[m][1] = acc[m][2] = acc[m][3] = 0;
+#pragma unroll
+  for (int j = 0; j < J; ++j) {
+    if (j < valid_j) {
+      const uint4 w = lds128(wrow + 512 * j);
+      const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int m = 0; m < MT; ++m)
+#pragma unroll
+        for (int s = 0; s < 4; ++s) {
+          const uint32_t xw[4] = {xr[m][j][s].x, xr[m][j][s].y, xr[m][j][s].z, xr[m][j][s].w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            acc[m][s] = dp4a_us(ww[i] & (0x03030303u << (2 * s)), xw[i], acc[m][s]);
+        }
+    }
+  }
+#pragma unroll
+  for (int m = 0; m < MT; ++m)
+    v[m] = acc[m][0] + (acc[m][1] >> 2) + (acc[m][2] >> 4) + (acc[m][3] >> 6);
 }
 
-template <int MT>
+template <int MT, int J>
 __global__ void __launch_bounds__(kThreads, MT <= 2 ? 2 : 1)
 k_gemv_decode(const __grid_constant__ Args a) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -188,19 +194,19 @@ k_gemv_decode(const __grid_constant__ Args a) {
   __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
   __shared__ float s_max[kConsumerWarps][MT];
   __shared__ int s_sumx[MT];
+  __shared__ int s_part[2][kConsumerWarps * kMaxRowsPerWarp * MT];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r_begin = blockIdx.x * a.rows_per_cta;
   const int r_end = min(r_begin + a.rows_per_cta, a.rows_total);
   const int64_t row_bytes = a.K >> 2;
-  const int nch = a.K >> 6;
   const uint32_t ring = smem_addr(smem);
   int8_t* xs = reinterpret_cast<int8_t*>(smem + a.stages * a.stage_bytes);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < a.stages; ++s) {
       mbar_init(smem_addr(&full_bar[s]), 1);
-      mbar_init(smem_addr(&empty_bar[s]), kGroupWarps);
+      mbar_init(smem_addr(&empty_bar[s]), kConsumerWarps);
     }
     mbar_fence_init();
     for (int m = 0; m < MT; ++m) s_sumx[m] = 0;
@@ -224,52 +230,39 @@ k_gemv_decode(const __grid_constant__ Args a) {
   if (warp == kConsumerWarps) {
     if (lane != 0) return;
     // Weights the caller declared static may stream in while the previous
-    // kernel on the stream is still running; otherwise wait for it first.
-    // Either way every bounded wait below starts after the dependency wait.
+    // kernel on the stream is still running (one ring's worth); otherwise
+    // wait for it first.  Either way every bounded wait below starts after
+    // the dependency wait.
     bool dep_done = !a.weights_early;
     if (dep_done) griddep_wait();
-    int issued[kGroups] = {};
-    for_each_stage(a, r_begin, r_end, [&](int p, int row, int nrows, int sl, int b) {
-      const SlotPhase sp = slot_of(a, b, sl);
-      if (sp.use > 0) {
+    int i = 0;
+    for_each_stage(a, r_begin, r_end, [&](int p, int row, int nrows) {
+      const int slot = i % a.stages, use = i / a.stages;
+      if (use > 0) {
         if (!dep_done) {
           griddep_wait();
           dep_done = true;
         }
-        if (!mbar_wait(smem_addr(&empty_bar[sp.slot]), (sp.use - 1) & 1)) {
+        if (!mbar_wait(smem_addr(&empty_bar[slot]), (use - 1) & 1)) {
           atomicOr(&g_decode_error, 1 << kErrEmptyWait);
           return false;
         }
       }
-      const int c0 = sl * a.slice_chunks;
-      const int chunks = min(a.slice_chunks, nch - c0);
-      const uint32_t slice_bytes = (uint32_t)chunks * 16u;
-      const uint32_t fb = smem_addr(&full_bar[sp.slot]);
-      const uint32_t dst = ring + sp.slot * a.stage_bytes;
-      const uint8_t* src = a.t[p].Wq + (int64_t)row * row_bytes + c0 * 16;
-      mbar_arrive_expect_tx(fb, slice_bytes * (uint32_t)nrows);
-      if (a.nslices == 1) {
-        // whole rows: the block is one contiguous span
-        bulk_copy_g2s(dst, src, slice_bytes * (uint32_t)nrows, fb);
-      } else {
-        for (int r = 0; r < nrows; ++r)
-          bulk_copy_g2s(dst + r * slice_bytes, src + (int64_t)r * row_bytes, slice_bytes, fb);
-      }
-      ++issued[b % kGroups];
+      const uint32_t bytes = (uint32_t)(nrows * row_bytes);
+      const uint32_t fb = smem_addr(&full_bar[slot]);
+      mbar_arrive_expect_tx(fb, bytes);
+      bulk_copy_g2s(ring + slot * a.stage_bytes, a.t[p].Wq + (int64_t)row * row_bytes, bytes, fb);
+      ++i;
       return true;
     });
     // Never leave the CTA with a copy in flight: wait for the last copy of
-    // every slot of both groups to land.
-    const int H = a.stages / kGroups;
-    for (int g = 0; g < kGroups; ++g) {
-      const int first = issued[g] > H ? issued[g] - H : 0;
-      for (int j = first; j < issued[g]; ++j)
-        if (!mbar_wait(smem_addr(&full_bar[g * H + j % H]), (j / H) & 1)) {
-          atomicOr(&g_decode_error, 1 << kErrDrainWait);
-          g = kGroups;
-          break;
-        }
-    }
+    // every slot to land.
+    const int first = i > a.stages ? i - a.stages : 0;
+    for (int j = first; j < i; ++j)
+      if (!mbar_wait(smem_addr(&full_bar[j % a.stages]), (j / a.stages) & 1)) {
+        atomicOr(&g_decode_error, 1 << kErrDrainWait);
+        break;
+      }
     return;
   }
 
@@ -277,31 +270,45 @@ k_gemv_decode(const __grid_constant__ Args a) {
   griddep_wait();
   const int tid = threadIdx.x;  // 0 .. kConsumers-1
   const int K = a.K;
-  const int nitems = K >> 4;   // 16-byte fields per token row
+  const int nitems = K >> 4;    // 16-byte pieces per token row
   float xscale[MT];
-  if (a.xb != nullptr && MT <= 2 && nitems <= 2 * kConsumers) {
-    // One pass: each thread keeps its (at most two) 16-element items of x in
-    // registers between the absmax and the quantisation.
+  if (a.xb != nullptr) {
+    // bf16 input: per-token absmax over K, then the quantised row into xs.
+    const bool one_pass = nitems <= 2 * kConsumers && MT <= 2;
     uint4 held[MT][2][2];
 #pragma unroll
     for (int m = 0; m < MT; ++m) {
       float mx = 0.0f;
+      if (m < a.M) {
+        const uint4* xrow = reinterpret_cast<const uint4*>(a.xb + (int64_t)m * K);
+        if (one_pass) {
 #pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const int f = tid + j * kConsumers;
-        held[m][j][0] = held[m][j][1] = make_uint4(0, 0, 0, 0);
-        if (m < a.M && f < nitems) {
-          const uint4* src = reinterpret_cast<const uint4*>(a.xb + (int64_t)m * K) + 2 * f;
-          held[m][j][0] = ld_nc_v4(src);
-          held[m][j][1] = ld_nc_v4(src + 1);
-        }
-        const uint32_t e[8] = {held[m][j][0].x, held[m][j][0].y, held[m][j][0].z,
-                               held[m][j][0].w, held[m][j][1].x, held[m][j][1].y,
-                               held[m][j][1].z, held[m][j][1].w};
+          for (int j = 0; j < 2; ++j) {
+            const int f = tid + j * kConsumers;
+            held[m][j][0] = held[m][j][1] = make_uint4(0, 0, 0, 0);
+            if (f < nitems) {
+              held[m][j][0] = ld_nc_v4(xrow + 2 * f);
+              held[m][j][1] = ld_nc_v4(xrow + 2 * f + 1);
+            }
+            const uint32_t e[8] = {held[m][j][0].x, held[m][j][0].y, held[m][j][0].z,
+                                   held[m][j][0].w, held[m][j][1].x, held[m][j][1].y,
+                                   held[m][j][1].z, held[m][j][1].w};
 #pragma unroll
-        for (int t = 0; t < 8; ++t) {
-          mx = fmaxf(mx, fabsf(bf16_bits_to_float(e[t] & 0xffffu)));
-          mx = fmaxf(mx, fabsf(bf16_bits_to_float(e[t] >> 16)));
+            for (int t = 0; t < 8; ++t) {
+              mx = fmaxf(mx, fabsf(bf16_bits_to_float(e[t] & 0xffffu)));
+              mx = fmaxf(mx, fabsf(bf16_bits_to_float(e[t] >> 16)));
+            }
+          }
+        } else {
+          for (int v = tid; v < (K >> 3); v += kConsumers) {
+            const uint4 q = ld_nc_v4(xrow + v);
+            const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+              mx = fmaxf(mx, fabsf(bf16_bits_to_float(w4[t] & 0xffffu)));
+              mx = fmaxf(mx, fabsf(bf16_bits_to_float(w4[t] >> 16)));
+            }
+          }
         }
       }
       mx = warp_max_f32(mx);
@@ -316,13 +323,22 @@ k_gemv_decode(const __grid_constant__ Args a) {
       const ActScale sc = act_scale_from_absmax(mx);
       xscale[m] = sc.scale;
       int sum = 0;
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const int f = tid + j * kConsumers;
-        if (m < a.M && f < nitems) {
-          const uint32_t e[8] = {held[m][j][0].x, held[m][j][0].y, held[m][j][0].z,
-                                 held[m][j][0].w, held[m][j][1].x, held[m][j][1].y,
-                                 held[m][j][1].z, held[m][j][1].w};
+      if (m < a.M) {
+        const uint4* xrow = reinterpret_cast<const uint4*>(a.xb + (int64_t)m * K);
+        for (int j = 0;; ++j) {
+          const int f = tid + j * kConsumers;
+          if (f >= nitems || (one_pass && j >= 2)) break;
+          uint32_t e[8];
+          if (one_pass) {
+            const uint4 h0 = j == 0 ? held[m][0][0] : held[m][1][0];
+            const uint4 h1 = j == 0 ? held[m][0][1] : held[m][1][1];
+            e[0] = h0.x; e[1] = h0.y; e[2] = h0.z; e[3] = h0.w;
+            e[4] = h1.x; e[5] = h1.y; e[6] = h1.z; e[7] = h1.w;
+          } else {
+            const uint4 h0 = ld_nc_v4(xrow + 2 * f), h1 = ld_nc_v4(xrow + 2 * f + 1);
+            e[0] = h0.x; e[1] = h0.y; e[2] = h0.z; e[3] = h0.w;
+            e[4] = h1.x; e[5] = h1.y; e[6] = h1.z; e[7] = h1.w;
+          }
           uint32_t wd[4];
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
@@ -337,69 +353,7 @@ k_gemv_decode(const __grid_constant__ Args a) {
             sum = dp4a_ss(wd[i], 0x01010101u, sum);
           }
           const uint4 packed = make_uint4(wd[0], wd[1], wd[2], wd[3]);
-          *reinterpret_cast<uint4*>(xs + (int64_t)m * K + xs_offset(f >> 2, f & 3)) = packed;
-          if (blockIdx.x == 0 && a.xq_out != nullptr)
-            *reinterpret_cast<uint4*>(a.xq_out + (int64_t)m * K + 16 * f) = packed;
-        }
-      }
-      sum = warp_sum_i32(sum);
-      if (lane == 0 && sum) atomicAdd(&s_sumx[m], sum);
-      if (blockIdx.x == 0 && tid == 0 && a.xs_out != nullptr && m < a.M) a.xs_out[m] = xscale[m];
-    }
-  } else if (a.xb != nullptr) {
-    const int nv = K >> 3;
-#pragma unroll
-    for (int m = 0; m < MT; ++m) {
-      float mx = 0.0f;
-      if (m < a.M) {
-        const uint4* xrow = reinterpret_cast<const uint4*>(a.xb + (int64_t)m * K);
-        for (int v = tid; v < nv; v += kConsumers) {
-          const uint4 q = ld_nc_v4(xrow + v);
-          const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-          for (int t = 0; t < 4; ++t) {
-            mx = fmaxf(mx, fabsf(bf16_bits_to_float(w4[t] & 0xffffu)));
-            mx = fmaxf(mx, fabsf(bf16_bits_to_float(w4[t] >> 16)));
-          }
-        }
-      }
-      mx = warp_max_f32(mx);
-      if (lane == 0) s_max[warp][m] = mx;
-    }
-    consumer_sync();
-    float inv[MT];
-#pragma unroll
-    for (int m = 0; m < MT; ++m) {
-      float mx = s_max[0][m];
-#pragma unroll
-      for (int w = 1; w < kConsumerWarps; ++w) mx = fmaxf(mx, s_max[w][m]);
-      const ActScale sc = act_scale_from_absmax(mx);
-      inv[m] = sc.inv;
-      xscale[m] = sc.scale;
-    }
-#pragma unroll
-    for (int m = 0; m < MT; ++m) {
-      int sum = 0;
-      if (m < a.M) {
-        const uint4* xrow = reinterpret_cast<const uint4*>(a.xb + (int64_t)m * K);
-        for (int f = tid; f < nitems; f += kConsumers) {
-          const uint4 p0 = ld_nc_v4(xrow + 2 * f), p1 = ld_nc_v4(xrow + 2 * f + 1);
-          const uint32_t e[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
-          uint32_t wd[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            int q[4];
-#pragma unroll
-            for (int t = 0; t < 4; ++t) {
-              const int el = 4 * i + t;
-              const uint32_t h = (el & 1) ? (e[el >> 1] >> 16) : (e[el >> 1] & 0xffffu);
-              q[t] = round_clip(__fmul_rn(bf16_bits_to_float(h), inv[m]), -128.f, 127.f);
-            }
-            wd[i] = pack_i8x4(q[0], q[1], q[2], q[3]);
-            sum = dp4a_ss(wd[i], 0x01010101u, sum);
-          }
-          const uint4 packed = make_uint4(wd[0], wd[1], wd[2], wd[3]);
-          *reinterpret_cast<uint4*>(xs + (int64_t)m * K + xs_offset(f >> 2, f & 3)) = packed;
+          *reinterpret_cast<uint4*>(xs + (int64_t)m * K + 16 * f) = packed;
           if (blockIdx.x == 0 && a.xq_out != nullptr)
             *reinterpret_cast<uint4*>(a.xq_out + (int64_t)m * K + 16 * f) = packed;
         }
@@ -422,7 +376,7 @@ k_gemv_decode(const __grid_constant__ Args a) {
           sum = dp4a_ss(v.y, 0x01010101u, sum);
           sum = dp4a_ss(v.z, 0x01010101u, sum);
           sum = dp4a_ss(v.w, 0x01010101u, sum);
-          *reinterpret_cast<uint4*>(xs + (int64_t)m * K + xs_offset(f >> 2, f & 3)) = v;
+          *reinterpret_cast<uint4*>(xs + (int64_t)m * K + 16 * f) = v;
         }
       }
       sum = warp_sum_i32(sum);
@@ -434,167 +388,154 @@ k_gemv_decode(const __grid_constant__ Args a) {
 #pragma unroll
   for (int m = 0; m < MT; ++m) sumx[m] = s_sumx[m];
 
-  // Group g takes row blocks g, g+2, ...; its warp wl owns rows 4wl .. 4wl+3
-  // of each block, 8-lane group grp row 4wl + grp, and lane sub chunks sub,
-  // sub+8, ... of each slice.  Slices start at multiples of 8 chunks, so in
-  // every chunk this lane reads, field s sits at the same slot
-  // (s + sub/2) & 3: xo[s] is its byte offset within the chunk.  The eight
-  // lanes of a quarter-warp then read eight distinct 16-byte bank groups.
-  const int gw = warp / kGroupWarps, wl = warp % kGroupWarps;
-  const int grp = lane >> 3, sub = lane & 7;
-  const int r = wl * 4 + grp;
-  uint32_t xo[4];
+  // This warp: K part kw (chunks k_lo .. k_hi-1) and row group wr of 8/wk.
+  const int kw = warp % a.wk, wr = warp / a.wk, nwr = kConsumerWarps / a.wk;
+  const int nch = K >> 6;
+  const int k_lo = kw * a.kpart, k_hi = min(nch, k_lo + a.kpart);
+  int valid_j = 0;
+  uint4 xr[MT][J][4];
 #pragma unroll
-  for (int k = 0; k < 4; ++k) xo[k] = 16u * (uint32_t)((k + (sub >> 1)) & 3);
-  const uint32_t xs_base = smem_addr(xs);
-  // acc[m][k][i]: independent dp4a chains per token (field k, word i % NI).
-  // One token needs 16 chains to keep the issue slots busy; more tokens bring
-  // their own chains.
-  constexpr int NI = MT == 1 ? 4 : 1;
-  int acc[MT][4][NI];
-  for_each_stage(a, r_begin, r_end, [&](int p, int row0, int nrows, int sl, int b) {
-    if (b % kGroups != gw) return true;
-    const SlotPhase sp = slot_of(a, b, sl);
-    if (!mbar_wait(smem_addr(&full_bar[sp.slot]), sp.use & 1)) {
+  for (int j = 0; j < J; ++j) {
+    const int c = k_lo + lane + 32 * j;
+    if (c < k_hi) valid_j = j + 1;
+#pragma unroll
+    for (int m = 0; m < MT; ++m)
+#pragma unroll
+      for (int s = 0; s < 4; ++s)
+        xr[m][j][s] = c < k_hi ? *reinterpret_cast<const uint4*>(xs + (int64_t)m * K + 64 * c + 16 * s)
+                               : make_uint4(0, 0, 0, 0);
+  }
+
+  int i = 0;
+  for_each_stage(a, r_begin, r_end, [&](int p, int row0, int nrows) {
+    const int slot = i % a.stages;
+    if (!mbar_wait(smem_addr(&full_bar[slot]), (i / a.stages) & 1)) {
       if (lane == 0) atomicOr(&g_decode_error, 1 << kErrFullWait);
       return false;
     }
-    if (sl == 0) {
+    const Target& T = a.t[p];
+    const int buf = i & 1;
+    const uint32_t sbase = ring + slot * a.stage_bytes + 16 * (k_lo + lane);
+    // Rows wr, wr + nwr, ... of the stage, two at a time.
+    for (int rr = wr; rr < nrows; rr += 2 * nwr) {
+      const int rr2 = rr + nwr;
+      const bool two = rr2 < nrows;
+      int v1[MT], v2[MT];
+      row_partial<MT, J>(sbase + (uint32_t)(rr * row_bytes), valid_j, xr, v1);
+      if (two) row_partial<MT, J>(sbase + (uint32_t)(rr2 * row_bytes), valid_j, xr, v2);
 #pragma unroll
-      for (int m = 0; m < MT; ++m)
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-#pragma unroll
-          for (int i = 0; i < NI; ++i) acc[m][k][i] = 0;
-    }
-    const bool valid = r < nrows;
-    const int c0 = sl * a.slice_chunks;
-    const int chunks = min(a.slice_chunks, nch - c0);
-    if (valid && sub < chunks) {
-      uint32_t wp = ring + sp.slot * a.stage_bytes + (uint32_t)(r * chunks * 16) + 16 * sub;
-      uint32_t xp = xs_base + 64 * (c0 + sub);
-      // Operands of the current chunk; the next chunk's are loaded before
-      // the current one is consumed.
-      uint4 wv = lds128(wp);
-      uint4 xv[MT][4];
-#pragma unroll
-      for (int m = 0; m < MT; ++m)
-#pragma unroll
-        for (int k = 0; k < 4; ++k) xv[m][k] = lds128(xp + m * K + xo[k]);
-      // One token: the next chunk's operands are loaded before the current
-      // one is consumed.  More tokens: enough independent loads already.
-      constexpr int NB = MT == 1 ? MT : 1;
-      for (int c = sub;;) {
-        const bool more = c + 8 < chunks;
-        uint4 wn = make_uint4(0, 0, 0, 0);
-        uint4 xn[NB][4];
-        if (MT == 1 && more) {
-          wn = lds128(wp + 128);
-#pragma unroll
-          for (int k = 0; k < 4; ++k) xn[0][k] = lds128(xp + 512 + xo[k]);
-        }
-        const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
+      for (int m = 0; m < MT; ++m) {
+        v1[m] = __reduce_add_sync(0xffffffffu, v1[m]);
+        v2[m] = two ? __reduce_add_sync(0xffffffffu, v2[m]) : 0;
+      }
+      if (a.wk == 1) {
 #pragma unroll
         for (int m = 0; m < MT; ++m) {
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint32_t xw[4] = {xv[m][k].x, xv[m][k].y, xv[m][k].z, xv[m][k].w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-              acc[m][k][i % NI] =
-                  dp4a_us(ww[i] & (0x03030303u << (2 * k)), xw[i], acc[m][k][i % NI]);
+          if (m < a.M && lane == m) {
+            const float sc = __fmul_rn(xscale[m], *T.w_scale);
+            int tot = v1[m] - sumx[m];
+            int64_t o = (int64_t)m * T.N + row0 + rr;
+            T.y[o] = __fmul_rn(__int2float_rn(tot), sc);
+            if (T.acc_out) T.acc_out[o] = tot;
+            if (two) {
+              tot = v2[m] - sumx[m];
+              o = (int64_t)m * T.N + row0 + rr2;
+              T.y[o] = __fmul_rn(__int2float_rn(tot), sc);
+              if (T.acc_out) T.acc_out[o] = tot;
+            }
           }
         }
-        if (!more) break;
-        c += 8;
-        wp += 128;
-        xp += 512;
-        if (MT == 1) {
-          wv = wn;
+      } else if (lane == 0) {
 #pragma unroll
-          for (int k = 0; k < 4; ++k) xv[0][k] = xn[0][k];
-        } else {
-          wv = lds128(wp);
-#pragma unroll
-          for (int m = 0; m < MT; ++m)
-#pragma unroll
-            for (int k = 0; k < 4; ++k) xv[m][k] = lds128(xp + m * K + xo[k]);
+        for (int m = 0; m < MT; ++m) {
+          s_part[buf][(rr * a.wk + kw) * MT + m] = v1[m];
+          if (two) s_part[buf][(rr2 * a.wk + kw) * MT + m] = v2[m];
         }
       }
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(smem_addr(&empty_bar[sp.slot]));
-    if (sl == a.nslices - 1) {
-      const Target& T = a.t[p];
-      const float ws = *T.w_scale;
+    if (lane == 0) mbar_arrive(smem_addr(&empty_bar[slot]));
+    if (a.wk > 1) {
+      // All K parts of this stage's rows are in s_part[buf]; finish them.
+      // (s_part is double-buffered: the next stage writes the other half.)
+      consumer_sync();
+      for (int e = tid; e < nrows * MT; e += kConsumers) {
+        const int rr = e / MT, m = e % MT;
+        if (m >= a.M) continue;
+        int tot = -sumx[0];
 #pragma unroll
-      for (int m = 0; m < MT; ++m) {
-        int t = 0;
+        for (int mm = 1; mm < MT; ++mm)
+          if (mm == m) tot = -sumx[mm];
+        for (int q = 0; q < a.wk; ++q) tot += s_part[buf][(rr * a.wk + q) * MT + m];
+        float xsc = xscale[0];
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-        {
-          int u = 0;
-#pragma unroll
-          for (int i = 0; i < NI; ++i) u += acc[m][k][i];
-          t += u >> (2 * k);
-        }
-        t += __shfl_xor_sync(0xffffffffu, t, 4);
-        t += __shfl_xor_sync(0xffffffffu, t, 2);
-        t += __shfl_xor_sync(0xffffffffu, t, 1);
-        if (sub == 0 && valid && m < a.M) {
-          const int total = t - sumx[m];
-          const int64_t o = (int64_t)m * T.N + row0 + r;
-          T.y[o] = __fmul_rn(__int2float_rn(total), __fmul_rn(xscale[m], ws));
-          if (T.acc_out) T.acc_out[o] = total;
-        }
+        for (int mm = 1; mm < MT; ++mm)
+          if (mm == m) xsc = xscale[mm];
+        const int64_t o = (int64_t)m * T.N + row0 + rr;
+        T.y[o] = __fmul_rn(__int2float_rn(tot), __fmul_rn(xsc, *T.w_scale));
+        if (T.acc_out) T.acc_out[o] = tot;
       }
     }
+    ++i;
     return true;
   });
 }
 
 struct Plan {
-  int mt, slice_chunks, nslices, stages, stage_bytes;
+  int mt, j, wk, kpart, rows_per_stage, stages, stage_bytes;
   size_t smem;
 };
 
+// Tokens per pass MT, chunks per lane J (activations in 16*MT*J registers),
+// the K split wk and the ring geometry.
 bool make_plan(int64_t M, int64_t K, Plan* pl) {
   if (M < 1 || M > kDecodeMaxM || K < 64 || K % 64 != 0 || K > 65536) return false;
-  pl->mt = M <= 1 ? 1 : M <= 2 ? 2 : 4;
+  const int mt = M <= 1 ? 1 : M <= 2 ? 2 : 4;
   const int nch = (int)(K / 64);
-  if (nch <= kMaxSliceChunks) {
-    pl->nslices = 1;
-    pl->slice_chunks = nch;
-  } else {
-    // slices start on multiples of 8 chunks (see the consumer loop)
-    int ns = (nch + kMaxSliceChunks - 1) / kMaxSliceChunks;
-    int sc = ((nch + ns - 1) / ns + 7) / 8 * 8;
-    pl->slice_chunks = sc;
-    pl->nslices = (nch + sc - 1) / sc;
+  const int jopts[2] = {mt == 4 ? 1 : 2, mt == 1 ? 4 : 0};
+  int j = 0, wk = 0;
+  for (int o = 0; o < 2 && !wk; ++o) {
+    if (jopts[o] == 0) continue;
+    for (int w = 1; w <= 8; w *= 2)
+      if ((nch + w - 1) / w <= 32 * jopts[o]) {
+        j = jopts[o];
+        wk = w;
+        break;
+      }
   }
-  pl->stage_bytes = kBlockRows * pl->slice_chunks * 16;
+  if (!wk) return false;
+  const int nwr = kConsumerWarps / wk;
+  const int64_t row_bytes = K / 4;
+  int64_t R = kStageTarget / row_bytes / nwr * nwr;
+  if (R < nwr) R = nwr;
+  if (R > (int64_t)kMaxRowsPerWarp * nwr) R = (int64_t)kMaxRowsPerWarp * nwr;
+  pl->mt = mt;
+  pl->j = j;
+  pl->wk = wk;
+  pl->kpart = (nch + wk - 1) / wk;
+  pl->rows_per_stage = (int)R;
+  pl->stage_bytes = (int)(R * row_bytes);
   int S = kRingBudget / pl->stage_bytes;
-  S = S / kGroups * kGroups;
-  if (S < 2 * kGroups) S = 2 * kGroups;
+  if (S < 2) S = 2;
   if (S > kMaxStages) S = kMaxStages;
   pl->stages = S;
-  pl->smem = (size_t)S * pl->stage_bytes + (size_t)pl->mt * (size_t)K;
+  pl->smem = (size_t)S * pl->stage_bytes + (size_t)mt * (size_t)K;
   return pl->smem <= (size_t)kMaxSmem;
 }
 
-template <int MT>
+template <int MT, int J>
 cudaError_t launch_t(const Args& a, int ctas, size_t smem, cudaStream_t s) {
   static bool configured[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 64 && !configured[dev]) {
-    e = cudaFuncSetAttribute(k_gemv_decode<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(k_gemv_decode<MT, J>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kMaxSmem);
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
-  return launch_pdl(k_gemv_decode<MT>, dim3(ctas), dim3(kThreads), smem, s, a);
+  return launch_pdl(k_gemv_decode<MT, J>, dim3(ctas), dim3(kThreads), smem, s, a);
 }
 
 }  // namespace
@@ -632,19 +573,19 @@ cudaError_t launch_decode(const DecodeTarget* targets, int count, const int8_t* 
   a.xs_out = x_scale_out;
   a.M = (int)M;
   a.K = (int)K;
-  a.slice_chunks = pl.slice_chunks;
-  a.nslices = pl.nslices;
+  a.wk = pl.wk;
+  a.kpart = pl.kpart;
+  a.rows_per_stage = pl.rows_per_stage;
   a.stages = pl.stages;
   a.stage_bytes = pl.stage_bytes;
   a.weights_early = weights_static ? 1 : 0;
-  int64_t ctas = (rows + 3) / 4;
-  if (ctas > 148) ctas = 148;
+  int64_t ctas = rows < 148 ? rows : 148;
   a.rows_per_cta = (int)((rows + ctas - 1) / ctas);
   ctas = (rows + a.rows_per_cta - 1) / a.rows_per_cta;
   const int c = (int)ctas;
-  if (pl.mt == 1) return launch_t<1>(a, c, pl.smem, s);
-  if (pl.mt == 2) return launch_t<2>(a, c, pl.smem, s);
-  return launch_t<4>(a, c, pl.smem, s);
+  if (pl.mt == 1) return pl.j == 2 ? launch_t<1, 2>(a, c, pl.smem, s) : launch_t<1, 4>(a, c, pl.smem, s);
+  if (pl.mt == 2) return launch_t<2, 2>(a, c, pl.smem, s);
+  return launch_t<4, 1>(a, c, pl.smem, s);
 }
 
 cudaError_t read_and_clear_decode_error(int* code, cudaStream_t s) {

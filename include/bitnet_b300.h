@@ -133,7 +133,7 @@ bitnet_status bitnet_linear(const uint8_t* Wq, const float* w_scale,
  * x: [M, K] bf16, 1 <= M <= BITNET_DECODE_MAX_M.  targets[i]: Wq [N_i, K/4]
  * packed, w_scale [1], y [M, N_i] float, acc_out optional [M, N_i] int32.
  * xq_out [M, K] and x_scale_out [M] are optional copies of xq and sx.
- * K % 64 == 0; K <= 65536 for M <= 2, K <= 32768 for M <= 4
+ * K % 64 == 0; K <= 65536 for M = 1, 32768 for M = 2, 16384 for M <= 4
  * (BITNET_ERR_SHAPE beyond); sum of N_i <= 2^30.  Needs no workspace.  The
  * kernel may start while the previous kernel on `stream` is finishing
  * (programmatic dependent launch) and waits for it before reading x or
