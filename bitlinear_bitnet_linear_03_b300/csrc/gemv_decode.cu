@@ -23,8 +23,9 @@
 //    int8 activations are loaded into registers once, and a row costs the
 //    lane one 16-byte shared load, 16 ANDs and 16 dp4a per chunk; the 32
 //    lanes read 512 contiguous bytes of the row.  A row's lane sums meet in
-//    one warp reduction (redux.sync); with wk > 1 the K parts meet through
-//    shared memory after each stage.
+//    one warp reduction (redux.sync); with wk > 1 the K parts meet in a
+//    64-bit shared-memory atomic per row that also counts the parts, and the
+//    last part to arrive writes the row (no barrier between warps).
 //  * Before waiting on the previous kernel the CTA asks for its whole weight
 //    range to be prefetched into L2 and lets its successor launch:
 //    consecutive decode kernels overlap under programmatic dependent launch.
@@ -55,7 +56,7 @@ constexpr int kMaxStages = 8;
 constexpr int kRingBudget = 96 * 1024;
 constexpr int kStageTarget = 24 * 1024;
 constexpr int kMaxRowsPerWarp = 8;         // rows of one stage handled by one warp
-constexpr int kMaxSmem = 227 * 1024 - 4096;  // dynamic part; the static arrays fit in the rest
+constexpr int kMaxSmem = 227 * 1024 - 10 * 1024;  // dynamic part; the static arrays fit in the rest
 constexpr int kPrefetchMax = 1 << 16;
 constexpr long long kWaitCycles = 2000000000ll;  // ~1 s at 2 GHz
 constexpr int kErrFullWait = 1;
@@ -194,7 +195,10 @@ k_gemv_decode(const __grid_constant__ Args a) {
   __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
   __shared__ float s_max[kConsumerWarps][MT];
   __shared__ int s_sumx[MT];
-  __shared__ int s_part[2][kConsumerWarps * kMaxRowsPerWarp * MT];
+  __shared__ float s_ws[kDecodeMaxTargets];
+  // K-part merge per ring slot and stage row: low 48 bits hold the sum of the
+  // parts' partial dot products, bits 48.. count the parts added so far.
+  __shared__ unsigned long long s_acc[kMaxStages][kConsumerWarps * kMaxRowsPerWarp / 2][MT];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r_begin = blockIdx.x * a.rows_per_cta;
@@ -203,6 +207,10 @@ k_gemv_decode(const __grid_constant__ Args a) {
   const uint32_t ring = smem_addr(smem);
   int8_t* xs = reinterpret_cast<int8_t*>(smem + a.stages * a.stage_bytes);
 
+  if (a.wk > 1)
+    for (int q = threadIdx.x; q < kMaxStages * (kConsumerWarps * kMaxRowsPerWarp / 2) * MT;
+         q += kThreads)
+      (&s_acc[0][0][0])[q] = 0ull;
   if (threadIdx.x == 0) {
     for (int s = 0; s < a.stages; ++s) {
       mbar_init(smem_addr(&full_bar[s]), 1);
@@ -383,6 +391,7 @@ k_gemv_decode(const __grid_constant__ Args a) {
       if (lane == 0 && sum) atomicAdd(&s_sumx[m], sum);
     }
   }
+  if (tid < a.count) s_ws[tid] = *a.t[tid].w_scale;
   consumer_sync();
   int sumx[MT];
 #pragma unroll
@@ -414,7 +423,7 @@ k_gemv_decode(const __grid_constant__ Args a) {
       return false;
     }
     const Target& T = a.t[p];
-    const int buf = i & 1;
+    const float wsc = s_ws[p];
     const uint32_t sbase = ring + slot * a.stage_bytes + 16 * (k_lo + lane);
     // Rows wr, wr + nwr, ... of the stage, two at a time.
     for (int rr = wr; rr < nrows; rr += 2 * nwr) {
@@ -428,54 +437,38 @@ k_gemv_decode(const __grid_constant__ Args a) {
         v1[m] = __reduce_add_sync(0xffffffffu, v1[m]);
         v2[m] = two ? __reduce_add_sync(0xffffffffu, v2[m]) : 0;
       }
-      if (a.wk == 1) {
 #pragma unroll
-        for (int m = 0; m < MT; ++m) {
-          if (m < a.M && lane == m) {
-            const float sc = __fmul_rn(xscale[m], *T.w_scale);
-            int tot = v1[m] - sumx[m];
-            int64_t o = (int64_t)m * T.N + row0 + rr;
-            T.y[o] = __fmul_rn(__int2float_rn(tot), sc);
-            if (T.acc_out) T.acc_out[o] = tot;
-            if (two) {
-              tot = v2[m] - sumx[m];
-              o = (int64_t)m * T.N + row0 + rr2;
-              T.y[o] = __fmul_rn(__int2float_rn(tot), sc);
-              if (T.acc_out) T.acc_out[o] = tot;
+      for (int m = 0; m < MT; ++m) {
+        if (m >= a.M || lane != m) continue;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          if (h == 1 && !two) break;
+          const int row = h == 0 ? rr : rr2;
+          int tot = h == 0 ? v1[m] : v2[m];
+          bool last = true;
+          if (a.wk > 1) {
+            // Merge the K parts: the last part to arrive writes the row.
+            const unsigned long long add =
+                (1ull << 48) + ((unsigned long long)(long long)tot & 0xffffffffffffull);
+            const unsigned long long old = atomicAdd(&s_acc[slot][row][m], add);
+            last = (int)(old >> 48) == a.wk - 1;
+            if (last) {
+              const unsigned long long sum = (old + add) & 0xffffffffffffull;
+              tot = (int)(long long)(sum << 16 >> 16);  // low 48 bits, sign-extended
+              s_acc[slot][row][m] = 0ull;
             }
           }
-        }
-      } else if (lane == 0) {
-#pragma unroll
-        for (int m = 0; m < MT; ++m) {
-          s_part[buf][(rr * a.wk + kw) * MT + m] = v1[m];
-          if (two) s_part[buf][(rr2 * a.wk + kw) * MT + m] = v2[m];
+          if (last) {
+            tot -= sumx[m];
+            const int64_t o = (int64_t)m * T.N + row0 + row;
+            T.y[o] = __fmul_rn(__int2float_rn(tot), __fmul_rn(xscale[m], wsc));
+            if (T.acc_out) T.acc_out[o] = tot;
+          }
         }
       }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_addr(&empty_bar[slot]));
-    if (a.wk > 1) {
-      // All K parts of this stage's rows are in s_part[buf]; finish them.
-      // (s_part is double-buffered: the next stage writes the other half.)
-      consumer_sync();
-      for (int e = tid; e < nrows * MT; e += kConsumers) {
-        const int rr = e / MT, m = e % MT;
-        if (m >= a.M) continue;
-        int tot = -sumx[0];
-#pragma unroll
-        for (int mm = 1; mm < MT; ++mm)
-          if (mm == m) tot = -sumx[mm];
-        for (int q = 0; q < a.wk; ++q) tot += s_part[buf][(rr * a.wk + q) * MT + m];
-        float xsc = xscale[0];
-#pragma unroll
-        for (int mm = 1; mm < MT; ++mm)
-          if (mm == m) xsc = xscale[mm];
-        const int64_t o = (int64_t)m * T.N + row0 + rr;
-        T.y[o] = __fmul_rn(__int2float_rn(tot), __fmul_rn(xsc, *T.w_scale));
-        if (T.acc_out) T.acc_out[o] = tot;
-      }
-    }
     ++i;
     return true;
   });
@@ -579,7 +572,11 @@ cudaError_t launch_decode(const DecodeTarget* targets, int count, const int8_t* 
   a.stages = pl.stages;
   a.stage_bytes = pl.stage_bytes;
   a.weights_early = weights_static ? 1 : 0;
-  int64_t ctas = rows < 148 ? rows : 148;
+  // One CTA per SM leaves room for the next decode kernel to start alongside
+  // (programmatic dependent launch); large matrices take two per SM for more
+  // warps and copies in flight.
+  const int64_t max_ctas = rows * (K / 4) >= ((int64_t)16 << 20) ? 296 : 148;
+  int64_t ctas = rows < max_ctas ? rows : max_ctas;
   a.rows_per_cta = (int)((rows + ctas - 1) / ctas);
   ctas = (rows + a.rows_per_cta - 1) / a.rows_per_cta;
   const int c = (int)ctas;
