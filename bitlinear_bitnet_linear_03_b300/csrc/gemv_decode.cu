@@ -196,8 +196,8 @@ k_gemv_decode(const __grid_constant__ Args a) {
   __shared__ float s_max[kConsumerWarps][MT];
   __shared__ int s_sumx[MT];
   __shared__ float s_ws[kDecodeMaxTargets];
-  // K-part merge per ring slot and stage row: low 48 bits hold the sum of the
-  // parts' partial dot products, bits 48.. count the parts added so far.
+  // K-part merge per ring slot and stage row: the low 48 bits hold the sum of
+  // the parts' biased partial dot products, bits 48.. count the parts added.
   __shared__ unsigned long long s_acc[kMaxStages][kConsumerWarps * kMaxRowsPerWarp / 2][MT];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -448,13 +448,16 @@ k_gemv_decode(const __grid_constant__ Args a) {
           bool last = true;
           if (a.wk > 1) {
             // Merge the K parts: the last part to arrive writes the row.
+            // Each part adds 1 << 48 (the count) plus its value biased by
+            // 2^31 (non-negative, below 2^32), so at most 8 parts never
+            // carry out of the low 48 bits.
             const unsigned long long add =
-                (1ull << 48) + ((unsigned long long)(long long)tot & 0xffffffffffffull);
+                (1ull << 48) + (unsigned long long)((long long)tot + 2147483648ll);
             const unsigned long long old = atomicAdd(&s_acc[slot][row][m], add);
             last = (int)(old >> 48) == a.wk - 1;
             if (last) {
-              const unsigned long long sum = (old + add) & 0xffffffffffffull;
-              tot = (int)(long long)(sum << 16 >> 16);  // low 48 bits, sign-extended
+              const long long sum = (long long)((old + add) & 0xffffffffffffull);
+              tot = (int)(sum - (long long)a.wk * 2147483648ll);
               s_acc[slot][row][m] = 0ull;
             }
           }
