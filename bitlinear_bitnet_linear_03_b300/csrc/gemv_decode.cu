@@ -194,8 +194,6 @@ k_gemv_decode(const __grid_constant__ Args a) {
   __shared__ __align__(8) uint64_t full_bar[kMaxStages];
   __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
   __shared__ float s_max[kConsumerWarps][MT];
-  __shared__ int s_sumx[MT];
-  __shared__ float s_ws[kDecodeMaxTargets];
   // K-part merge per ring slot and stage row: the low 48 bits hold the sum of
   // the parts' biased partial dot products, bits 48.. count the parts added.
   __shared__ unsigned long long s_acc[kMaxStages][kConsumerWarps * kMaxRowsPerWarp / 2][MT];
@@ -205,7 +203,6 @@ k_gemv_decode(const __grid_constant__ Args a) {
   const int r_end = min(r_begin + a.rows_per_cta, a.rows_total);
   const int64_t row_bytes = a.K >> 2;
   const uint32_t ring = smem_addr(smem);
-  int8_t* xs = reinterpret_cast<int8_t*>(smem + a.stages * a.stage_bytes);
 
   if (a.wk > 1)
     for (int q = threadIdx.x; q < kMaxStages * (kConsumerWarps * kMaxRowsPerWarp / 2) * MT;
@@ -217,7 +214,6 @@ k_gemv_decode(const __grid_constant__ Args a) {
       mbar_init(smem_addr(&empty_bar[s]), kConsumerWarps);
     }
     mbar_fence_init();
-    for (int m = 0; m < MT; ++m) s_sumx[m] = 0;
     // L2 prefetch hint for this CTA's weights (independent of the previous
     // kernel; no data is read before griddep_wait).
     for (int p = 0; p < a.count; ++p) {
@@ -275,78 +271,86 @@ k_gemv_decode(const __grid_constant__ Args a) {
   }
 
   // ------------------------------------------------------------ consumers
+  // Each warp works on its own: K part kw (chunks k_lo .. k_hi-1) and row
+  // group wr of 8/wk.  Lane l holds the int8 activations of chunks
+  // k_lo + l + 32j (j < J) in registers and the sum of those codes, which it
+  // subtracts from every row's partial (sum q x = sum c x - sum x, taken
+  // part by part), so no warp needs another's activations.
   griddep_wait();
-  const int tid = threadIdx.x;  // 0 .. kConsumers-1
   const int K = a.K;
-  const int nitems = K >> 4;    // 16-byte pieces per token row
+  const int kw = warp % a.wk, wr = warp / a.wk, nwr = kConsumerWarps / a.wk;
+  const int nch = K >> 6;
+  const int k_lo = kw * a.kpart, k_hi = min(nch, k_lo + a.kpart);
+  // Matrix scales: lane p keeps w_scale of matrix p (read with a shuffle).
+  const float ws_lane = lane < a.count ? *a.t[lane].w_scale : 0.0f;
+  int valid_j = 0;
+#pragma unroll
+  for (int j = 0; j < J; ++j)
+    if (k_lo + lane + 32 * j < k_hi) valid_j = j + 1;
+  uint4 xr[MT][J][4];
+  int lsum[MT];
   float xscale[MT];
+#pragma unroll
+  for (int m = 0; m < MT; ++m) {
+    lsum[m] = 0;
+    xscale[m] = 0.0f;
+#pragma unroll
+    for (int j = 0; j < J; ++j)
+#pragma unroll
+      for (int s = 0; s < 4; ++s) xr[m][j][s] = make_uint4(0, 0, 0, 0);
+  }
   if (a.xb != nullptr) {
-    // bf16 input: per-token absmax over K, then the quantised row into xs.
-    const bool one_pass = nitems <= 2 * kConsumers && MT <= 2;
-    uint4 held[MT][2][2];
+    // bf16 input.  Per-token absmax over all of K: each warp scans the row
+    // itself when it is short (L1 serves the other warps), otherwise the
+    // CTA shares one pass through shared memory.
+    const int nv = K >> 3;
+    const bool per_warp = K <= 8192;
+    float inv[MT];
 #pragma unroll
     for (int m = 0; m < MT; ++m) {
       float mx = 0.0f;
       if (m < a.M) {
         const uint4* xrow = reinterpret_cast<const uint4*>(a.xb + (int64_t)m * K);
-        if (one_pass) {
+        const int step = per_warp ? 32 : kConsumers;
+        for (int v = per_warp ? lane : threadIdx.x; v < nv; v += step) {
+          const uint4 q = ld_nc_v4(xrow + v);
+          const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-          for (int j = 0; j < 2; ++j) {
-            const int f = tid + j * kConsumers;
-            held[m][j][0] = held[m][j][1] = make_uint4(0, 0, 0, 0);
-            if (f < nitems) {
-              held[m][j][0] = ld_nc_v4(xrow + 2 * f);
-              held[m][j][1] = ld_nc_v4(xrow + 2 * f + 1);
-            }
-            const uint32_t e[8] = {held[m][j][0].x, held[m][j][0].y, held[m][j][0].z,
-                                   held[m][j][0].w, held[m][j][1].x, held[m][j][1].y,
-                                   held[m][j][1].z, held[m][j][1].w};
-#pragma unroll
-            for (int t = 0; t < 8; ++t) {
-              mx = fmaxf(mx, fabsf(bf16_bits_to_float(e[t] & 0xffffu)));
-              mx = fmaxf(mx, fabsf(bf16_bits_to_float(e[t] >> 16)));
-            }
-          }
-        } else {
-          for (int v = tid; v < (K >> 3); v += kConsumers) {
-            const uint4 q = ld_nc_v4(xrow + v);
-            const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-            for (int t = 0; t < 4; ++t) {
-              mx = fmaxf(mx, fabsf(bf16_bits_to_float(w4[t] & 0xffffu)));
-              mx = fmaxf(mx, fabsf(bf16_bits_to_float(w4[t] >> 16)));
-            }
+          for (int t = 0; t < 4; ++t) {
+            mx = fmaxf(mx, fabsf(bf16_bits_to_float(w4[t] & 0xffffu)));
+            mx = fmaxf(mx, fabsf(bf16_bits_to_float(w4[t] >> 16)));
           }
         }
       }
       mx = warp_max_f32(mx);
-      if (lane == 0) s_max[warp][m] = mx;
+      if (!per_warp && lane == 0) s_max[warp][m] = mx;
+      inv[m] = mx;
     }
-    consumer_sync();
+    if (!per_warp) consumer_sync();
 #pragma unroll
     for (int m = 0; m < MT; ++m) {
-      float mx = s_max[0][m];
+      float mx = inv[m];
+      if (!per_warp) {
+        mx = s_max[0][m];
 #pragma unroll
-      for (int w = 1; w < kConsumerWarps; ++w) mx = fmaxf(mx, s_max[w][m]);
+        for (int w = 1; w < kConsumerWarps; ++w) mx = fmaxf(mx, s_max[w][m]);
+      }
       const ActScale sc = act_scale_from_absmax(mx);
+      inv[m] = sc.inv;
       xscale[m] = sc.scale;
-      int sum = 0;
-      if (m < a.M) {
-        const uint4* xrow = reinterpret_cast<const uint4*>(a.xb + (int64_t)m * K);
-        for (int j = 0;; ++j) {
-          const int f = tid + j * kConsumers;
-          if (f >= nitems || (one_pass && j >= 2)) break;
-          uint32_t e[8];
-          if (one_pass) {
-            const uint4 h0 = j == 0 ? held[m][0][0] : held[m][1][0];
-            const uint4 h1 = j == 0 ? held[m][0][1] : held[m][1][1];
-            e[0] = h0.x; e[1] = h0.y; e[2] = h0.z; e[3] = h0.w;
-            e[4] = h1.x; e[5] = h1.y; e[6] = h1.z; e[7] = h1.w;
-          } else {
-            const uint4 h0 = ld_nc_v4(xrow + 2 * f), h1 = ld_nc_v4(xrow + 2 * f + 1);
-            e[0] = h0.x; e[1] = h0.y; e[2] = h0.z; e[3] = h0.w;
-            e[4] = h1.x; e[5] = h1.y; e[6] = h1.z; e[7] = h1.w;
-          }
+    }
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+      if (m >= a.M) continue;
+#pragma unroll
+      for (int j = 0; j < J; ++j) {
+        if (j >= valid_j) continue;
+        const int c = k_lo + lane + 32 * j;
+        const uint4* src = reinterpret_cast<const uint4*>(a.xb + (int64_t)m * K) + 8 * c;
+#pragma unroll
+        for (int s = 0; s < 4; ++s) {
+          const uint4 h0 = ld_nc_v4(src + 2 * s), h1 = ld_nc_v4(src + 2 * s + 1);
+          const uint32_t e[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
           uint32_t wd[4];
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
@@ -355,64 +359,39 @@ k_gemv_decode(const __grid_constant__ Args a) {
             for (int t = 0; t < 4; ++t) {
               const int el = 4 * i + t;
               const uint32_t h = (el & 1) ? (e[el >> 1] >> 16) : (e[el >> 1] & 0xffffu);
-              q[t] = round_clip(__fmul_rn(bf16_bits_to_float(h), sc.inv), -128.f, 127.f);
+              q[t] = round_clip(__fmul_rn(bf16_bits_to_float(h), inv[m]), -128.f, 127.f);
             }
             wd[i] = pack_i8x4(q[0], q[1], q[2], q[3]);
-            sum = dp4a_ss(wd[i], 0x01010101u, sum);
+            lsum[m] = dp4a_ss(wd[i], 0x01010101u, lsum[m]);
           }
-          const uint4 packed = make_uint4(wd[0], wd[1], wd[2], wd[3]);
-          *reinterpret_cast<uint4*>(xs + (int64_t)m * K + 16 * f) = packed;
-          if (blockIdx.x == 0 && a.xq_out != nullptr)
-            *reinterpret_cast<uint4*>(a.xq_out + (int64_t)m * K + 16 * f) = packed;
+          xr[m][j][s] = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+          if (blockIdx.x == 0 && wr == 0 && a.xq_out != nullptr)
+            *reinterpret_cast<uint4*>(a.xq_out + (int64_t)m * K + 64 * c + 16 * s) = xr[m][j][s];
         }
       }
-      sum = warp_sum_i32(sum);
-      if (lane == 0 && sum) atomicAdd(&s_sumx[m], sum);
-      if (blockIdx.x == 0 && tid == 0 && a.xs_out != nullptr && m < a.M) a.xs_out[m] = xscale[m];
+      if (blockIdx.x == 0 && warp == 0 && lane == 0 && a.xs_out != nullptr) a.xs_out[m] = xscale[m];
     }
   } else {
 #pragma unroll
     for (int m = 0; m < MT; ++m) {
-      int sum = 0;
-      xscale[m] = 0.0f;
-      if (m < a.M) {
-        xscale[m] = a.x_scale[m];
-        const uint4* xrow = reinterpret_cast<const uint4*>(a.xq + (int64_t)m * K);
-        for (int f = tid; f < nitems; f += kConsumers) {
-          const uint4 v = ld_nc_v4(xrow + f);
-          sum = dp4a_ss(v.x, 0x01010101u, sum);
-          sum = dp4a_ss(v.y, 0x01010101u, sum);
-          sum = dp4a_ss(v.z, 0x01010101u, sum);
-          sum = dp4a_ss(v.w, 0x01010101u, sum);
-          *reinterpret_cast<uint4*>(xs + (int64_t)m * K + 16 * f) = v;
+      if (m >= a.M) continue;
+      xscale[m] = a.x_scale[m];
+#pragma unroll
+      for (int j = 0; j < J; ++j) {
+        if (j >= valid_j) continue;
+        const int c = k_lo + lane + 32 * j;
+        const uint4* src = reinterpret_cast<const uint4*>(a.xq + (int64_t)m * K + 64 * c);
+#pragma unroll
+        for (int s = 0; s < 4; ++s) {
+          const uint4 v = ld_nc_v4(src + s);
+          xr[m][j][s] = v;
+          lsum[m] = dp4a_ss(v.x, 0x01010101u, lsum[m]);
+          lsum[m] = dp4a_ss(v.y, 0x01010101u, lsum[m]);
+          lsum[m] = dp4a_ss(v.z, 0x01010101u, lsum[m]);
+          lsum[m] = dp4a_ss(v.w, 0x01010101u, lsum[m]);
         }
       }
-      sum = warp_sum_i32(sum);
-      if (lane == 0 && sum) atomicAdd(&s_sumx[m], sum);
     }
-  }
-  if (tid < a.count) s_ws[tid] = *a.t[tid].w_scale;
-  consumer_sync();
-  int sumx[MT];
-#pragma unroll
-  for (int m = 0; m < MT; ++m) sumx[m] = s_sumx[m];
-
-  // This warp: K part kw (chunks k_lo .. k_hi-1) and row group wr of 8/wk.
-  const int kw = warp % a.wk, wr = warp / a.wk, nwr = kConsumerWarps / a.wk;
-  const int nch = K >> 6;
-  const int k_lo = kw * a.kpart, k_hi = min(nch, k_lo + a.kpart);
-  int valid_j = 0;
-  uint4 xr[MT][J][4];
-#pragma unroll
-  for (int j = 0; j < J; ++j) {
-    const int c = k_lo + lane + 32 * j;
-    if (c < k_hi) valid_j = j + 1;
-#pragma unroll
-    for (int m = 0; m < MT; ++m)
-#pragma unroll
-      for (int s = 0; s < 4; ++s)
-        xr[m][j][s] = c < k_hi ? *reinterpret_cast<const uint4*>(xs + (int64_t)m * K + 64 * c + 16 * s)
-                               : make_uint4(0, 0, 0, 0);
   }
 
   int i = 0;
@@ -423,7 +402,7 @@ k_gemv_decode(const __grid_constant__ Args a) {
       return false;
     }
     const Target& T = a.t[p];
-    const float wsc = s_ws[p];
+    const float wsc = __shfl_sync(0xffffffffu, ws_lane, p);
     const uint32_t sbase = ring + slot * a.stage_bytes + 16 * (k_lo + lane);
     // Rows wr, wr + nwr, ... of the stage, two at a time.
     for (int rr = wr; rr < nrows; rr += 2 * nwr) {
@@ -434,8 +413,8 @@ k_gemv_decode(const __grid_constant__ Args a) {
       if (two) row_partial<MT, J>(sbase + (uint32_t)(rr2 * row_bytes), valid_j, xr, v2);
 #pragma unroll
       for (int m = 0; m < MT; ++m) {
-        v1[m] = __reduce_add_sync(0xffffffffu, v1[m]);
-        v2[m] = two ? __reduce_add_sync(0xffffffffu, v2[m]) : 0;
+        v1[m] = __reduce_add_sync(0xffffffffu, v1[m] - lsum[m]);
+        v2[m] = two ? __reduce_add_sync(0xffffffffu, v2[m] - lsum[m]) : 0;
       }
 #pragma unroll
       for (int m = 0; m < MT; ++m) {
@@ -462,7 +441,6 @@ k_gemv_decode(const __grid_constant__ Args a) {
             }
           }
           if (last) {
-            tot -= sumx[m];
             const int64_t o = (int64_t)m * T.N + row0 + row;
             T.y[o] = __fmul_rn(__int2float_rn(tot), __fmul_rn(xscale[m], wsc));
             if (T.acc_out) T.acc_out[o] = tot;
@@ -515,7 +493,7 @@ bool make_plan(int64_t M, int64_t K, Plan* pl) {
   if (S < 2) S = 2;
   if (S > kMaxStages) S = kMaxStages;
   pl->stages = S;
-  pl->smem = (size_t)S * pl->stage_bytes + (size_t)mt * (size_t)K;
+  pl->smem = (size_t)S * pl->stage_bytes;
   return pl->smem <= (size_t)kMaxSmem;
 }
 
