@@ -271,11 +271,10 @@ k_gemv_decode(const __grid_constant__ Args a) {
   }
 
   // ------------------------------------------------------------ consumers
-  // Each warp works on its own: K part kw (chunks k_lo .. k_hi-1) and row
-  // group wr of 8/wk.  Lane l holds the int8 activations of chunks
-  // k_lo + l + 32j (j < J) in registers and the sum of those codes, which it
-  // subtracts from every row's partial (sum q x = sum c x - sum x, taken
-  // part by part), so no warp needs another's activations.
+  // Warp: K part kw (chunks k_lo .. k_hi-1) and row group wr of 8/wk.  Lane
+  // l holds the int8 activations of chunks k_lo + l + 32j (j < J) in
+  // registers and the sum of those codes, which it subtracts from every
+  // row's partial (sum q x = sum c x - sum x, taken part by part).
   griddep_wait();
   const int K = a.K;
   const int kw = warp % a.wk, wr = warp / a.wk, nwr = kConsumerWarps / a.wk;
@@ -300,45 +299,96 @@ k_gemv_decode(const __grid_constant__ Args a) {
       for (int s = 0; s < 4; ++s) xr[m][j][s] = make_uint4(0, 0, 0, 0);
   }
   if (a.xb != nullptr) {
-    // bf16 input.  Per-token absmax over all of K: each warp scans the row
-    // itself when it is short (L1 serves the other warps), otherwise the
-    // CTA shares one pass through shared memory.
-    const int nv = K >> 3;
-    const bool per_warp = K <= 8192;
-    float inv[MT];
+    // bf16 input: the CTA quantises x once into shared memory (after the
+    // ring), each thread taking 16-element pieces; the row absmax is shared
+    // through s_max.  Then every lane picks up its chunks.
+    int8_t* xs = reinterpret_cast<int8_t*>(smem + a.stages * a.stage_bytes);
+    const int tid = threadIdx.x;
+    const int nitems = K >> 4;
+    const bool one_pass = nitems <= 2 * kConsumers;
+    uint4 held[MT][2][2];
 #pragma unroll
     for (int m = 0; m < MT; ++m) {
       float mx = 0.0f;
       if (m < a.M) {
         const uint4* xrow = reinterpret_cast<const uint4*>(a.xb + (int64_t)m * K);
-        const int step = per_warp ? 32 : kConsumers;
-        for (int v = per_warp ? lane : threadIdx.x; v < nv; v += step) {
-          const uint4 q = ld_nc_v4(xrow + v);
-          const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
+        if (one_pass) {
 #pragma unroll
-          for (int t = 0; t < 4; ++t) {
-            mx = fmaxf(mx, fabsf(bf16_bits_to_float(w4[t] & 0xffffu)));
-            mx = fmaxf(mx, fabsf(bf16_bits_to_float(w4[t] >> 16)));
+          for (int j = 0; j < 2; ++j) {
+            const int f = tid + j * kConsumers;
+            held[m][j][0] = held[m][j][1] = make_uint4(0, 0, 0, 0);
+            if (f < nitems) {
+              held[m][j][0] = ld_nc_v4(xrow + 2 * f);
+              held[m][j][1] = ld_nc_v4(xrow + 2 * f + 1);
+            }
+            const uint32_t e[8] = {held[m][j][0].x, held[m][j][0].y, held[m][j][0].z,
+                                   held[m][j][0].w, held[m][j][1].x, held[m][j][1].y,
+                                   held[m][j][1].z, held[m][j][1].w};
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+              mx = fmaxf(mx, fabsf(bf16_bits_to_float(e[t] & 0xffffu)));
+              mx = fmaxf(mx, fabsf(bf16_bits_to_float(e[t] >> 16)));
+            }
+          }
+        } else {
+          for (int v = tid; v < (K >> 3); v += kConsumers) {
+            const uint4 q = ld_nc_v4(xrow + v);
+            const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+              mx = fmaxf(mx, fabsf(bf16_bits_to_float(w4[t] & 0xffffu)));
+              mx = fmaxf(mx, fabsf(bf16_bits_to_float(w4[t] >> 16)));
+            }
           }
         }
       }
       mx = warp_max_f32(mx);
-      if (!per_warp && lane == 0) s_max[warp][m] = mx;
-      inv[m] = mx;
+      if (lane == 0) s_max[warp][m] = mx;
     }
-    if (!per_warp) consumer_sync();
+    consumer_sync();
 #pragma unroll
     for (int m = 0; m < MT; ++m) {
-      float mx = inv[m];
-      if (!per_warp) {
-        mx = s_max[0][m];
+      float mx = s_max[0][m];
 #pragma unroll
-        for (int w = 1; w < kConsumerWarps; ++w) mx = fmaxf(mx, s_max[w][m]);
-      }
+      for (int w = 1; w < kConsumerWarps; ++w) mx = fmaxf(mx, s_max[w][m]);
       const ActScale sc = act_scale_from_absmax(mx);
-      inv[m] = sc.inv;
       xscale[m] = sc.scale;
+      if (m >= a.M) continue;
+      const uint4* xrow = reinterpret_cast<const uint4*>(a.xb + (int64_t)m * K);
+      for (int j = 0;; ++j) {
+        const int f = tid + j * kConsumers;
+        if (f >= nitems || (one_pass && j >= 2)) break;
+        uint32_t e[8];
+        if (one_pass) {
+          const uint4 h0 = j == 0 ? held[m][0][0] : held[m][1][0];
+          const uint4 h1 = j == 0 ? held[m][0][1] : held[m][1][1];
+          e[0] = h0.x; e[1] = h0.y; e[2] = h0.z; e[3] = h0.w;
+          e[4] = h1.x; e[5] = h1.y; e[6] = h1.z; e[7] = h1.w;
+        } else {
+          const uint4 h0 = ld_nc_v4(xrow + 2 * f), h1 = ld_nc_v4(xrow + 2 * f + 1);
+          e[0] = h0.x; e[1] = h0.y; e[2] = h0.z; e[3] = h0.w;
+          e[4] = h1.x; e[5] = h1.y; e[6] = h1.z; e[7] = h1.w;
+        }
+        uint32_t wd[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          int q[4];
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            const int el = 4 * i + t;
+            const uint32_t h = (el & 1) ? (e[el >> 1] >> 16) : (e[el >> 1] & 0xffffu);
+            q[t] = round_clip(__fmul_rn(bf16_bits_to_float(h), sc.inv), -128.f, 127.f);
+          }
+          wd[i] = pack_i8x4(q[0], q[1], q[2], q[3]);
+        }
+        const uint4 packed = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+        *reinterpret_cast<uint4*>(xs + (int64_t)m * K + 16 * f) = packed;
+        if (blockIdx.x == 0 && a.xq_out != nullptr)
+          *reinterpret_cast<uint4*>(a.xq_out + (int64_t)m * K + 16 * f) = packed;
+      }
+      if (blockIdx.x == 0 && tid == 0 && a.xs_out != nullptr) a.xs_out[m] = xscale[m];
     }
+    consumer_sync();
 #pragma unroll
     for (int m = 0; m < MT; ++m) {
       if (m >= a.M) continue;
@@ -346,30 +396,16 @@ k_gemv_decode(const __grid_constant__ Args a) {
       for (int j = 0; j < J; ++j) {
         if (j >= valid_j) continue;
         const int c = k_lo + lane + 32 * j;
-        const uint4* src = reinterpret_cast<const uint4*>(a.xb + (int64_t)m * K) + 8 * c;
 #pragma unroll
         for (int s = 0; s < 4; ++s) {
-          const uint4 h0 = ld_nc_v4(src + 2 * s), h1 = ld_nc_v4(src + 2 * s + 1);
-          const uint32_t e[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
-          uint32_t wd[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            int q[4];
-#pragma unroll
-            for (int t = 0; t < 4; ++t) {
-              const int el = 4 * i + t;
-              const uint32_t h = (el & 1) ? (e[el >> 1] >> 16) : (e[el >> 1] & 0xffffu);
-              q[t] = round_clip(__fmul_rn(bf16_bits_to_float(h), inv[m]), -128.f, 127.f);
-            }
-            wd[i] = pack_i8x4(q[0], q[1], q[2], q[3]);
-            lsum[m] = dp4a_ss(wd[i], 0x01010101u, lsum[m]);
-          }
-          xr[m][j][s] = make_uint4(wd[0], wd[1], wd[2], wd[3]);
-          if (blockIdx.x == 0 && wr == 0 && a.xq_out != nullptr)
-            *reinterpret_cast<uint4*>(a.xq_out + (int64_t)m * K + 64 * c + 16 * s) = xr[m][j][s];
+          const uint4 v = *reinterpret_cast<const uint4*>(xs + (int64_t)m * K + 64 * c + 16 * s);
+          xr[m][j][s] = v;
+          lsum[m] = dp4a_ss(v.x, 0x01010101u, lsum[m]);
+          lsum[m] = dp4a_ss(v.y, 0x01010101u, lsum[m]);
+          lsum[m] = dp4a_ss(v.z, 0x01010101u, lsum[m]);
+          lsum[m] = dp4a_ss(v.w, 0x01010101u, lsum[m]);
         }
       }
-      if (blockIdx.x == 0 && warp == 0 && lane == 0 && a.xs_out != nullptr) a.xs_out[m] = xscale[m];
     }
   } else {
 #pragma unroll
@@ -493,7 +529,7 @@ bool make_plan(int64_t M, int64_t K, Plan* pl) {
   if (S < 2) S = 2;
   if (S > kMaxStages) S = kMaxStages;
   pl->stages = S;
-  pl->smem = (size_t)S * pl->stage_bytes;
+  pl->smem = (size_t)S * pl->stage_bytes + (size_t)mt * (size_t)K;  // ring + bf16 staging
   return pl->smem <= (size_t)kMaxSmem;
 }
 
