@@ -440,47 +440,61 @@ k_gemv_decode(const __grid_constant__ Args a) {
     const Target& T = a.t[p];
     const float wsc = __shfl_sync(0xffffffffu, ws_lane, p);
     const uint32_t sbase = ring + slot * a.stage_bytes + 16 * (k_lo + lane);
-    // Rows wr, wr + nwr, ... of the stage, two at a time.
-    for (int rr = wr; rr < nrows; rr += 2 * nwr) {
-      const int rr2 = rr + nwr;
-      const bool two = rr2 < nrows;
-      int v1[MT], v2[MT];
-      row_partial<MT, J>(sbase + (uint32_t)(rr * row_bytes), valid_j, xr, v1);
-      if (two) row_partial<MT, J>(sbase + (uint32_t)(rr2 * row_bytes), valid_j, xr, v2);
+    // Rows wr + q*nwr (q < my_rows <= kMaxRowsPerWarp) of the stage, two at
+    // a time; their warp sums are uniform across the lanes.
+    const int my_rows = nrows > wr ? (nrows - wr + nwr - 1) / nwr : 0;
+    int vals[kMaxRowsPerWarp][MT];
 #pragma unroll
-      for (int m = 0; m < MT; ++m) {
-        v1[m] = __reduce_add_sync(0xffffffffu, v1[m] - lsum[m]);
-        v2[m] = two ? __reduce_add_sync(0xffffffffu, v2[m] - lsum[m]) : 0;
+    for (int q = 0; q < kMaxRowsPerWarp; q += 2) {
+      if (q < my_rows) {
+        const bool two = q + 1 < my_rows;
+        int v1[MT], v2[MT];
+        row_partial<MT, J>(sbase + (uint32_t)((wr + q * nwr) * row_bytes), valid_j, xr, v1);
+        if (two)
+          row_partial<MT, J>(sbase + (uint32_t)((wr + (q + 1) * nwr) * row_bytes), valid_j, xr,
+                             v2);
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+          vals[q][m] = __reduce_add_sync(0xffffffffu, v1[m] - lsum[m]);
+          vals[q + 1][m] = two ? __reduce_add_sync(0xffffffffu, v2[m] - lsum[m]) : 0;
+        }
       }
+    }
+    // Lane q*MT + m finishes row q for token m: all rows of the stage at once.
+    {
+      const int q = lane / MT, m = lane % MT;
+      int tot = 0;
 #pragma unroll
-      for (int m = 0; m < MT; ++m) {
-        if (m >= a.M || lane != m) continue;
+      for (int qq = 0; qq < kMaxRowsPerWarp; ++qq)
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          if (h == 1 && !two) break;
-          const int row = h == 0 ? rr : rr2;
-          int tot = h == 0 ? v1[m] : v2[m];
-          bool last = true;
-          if (a.wk > 1) {
-            // Merge the K parts: the last part to arrive writes the row.
-            // Each part adds 1 << 48 (the count) plus its value biased by
-            // 2^31 (non-negative, below 2^32), so at most 8 parts never
-            // carry out of the low 48 bits.
-            const unsigned long long add =
-                (1ull << 48) + (unsigned long long)((long long)tot + 2147483648ll);
-            const unsigned long long old = atomicAdd(&s_acc[slot][row][m], add);
-            last = (int)(old >> 48) == a.wk - 1;
-            if (last) {
-              const long long sum = (long long)((old + add) & 0xffffffffffffull);
-              tot = (int)(sum - (long long)a.wk * 2147483648ll);
-              s_acc[slot][row][m] = 0ull;
-            }
-          }
+        for (int mm = 0; mm < MT; ++mm)
+          if (qq * MT + mm == lane) tot = vals[qq][mm];
+      float xsc = xscale[0];
+#pragma unroll
+      for (int mm = 1; mm < MT; ++mm)
+        if (mm == m) xsc = xscale[mm];
+      if (q < my_rows && q < kMaxRowsPerWarp && m < a.M) {
+        const int row = wr + q * nwr;
+        bool last = true;
+        if (a.wk > 1) {
+          // Merge the K parts: the last part to arrive writes the row.  Each
+          // part adds 1 << 48 (the count) plus its value biased by 2^31
+          // (non-negative, below 2^32), so at most 8 parts never carry out
+          // of the low 48 bits.
+          const unsigned long long add =
+              (1ull << 48) + (unsigned long long)((long long)tot + 2147483648ll);
+          const unsigned long long old = atomicAdd(&s_acc[slot][row][m], add);
+          last = (int)(old >> 48) == a.wk - 1;
           if (last) {
-            const int64_t o = (int64_t)m * T.N + row0 + row;
-            T.y[o] = __fmul_rn(__int2float_rn(tot), __fmul_rn(xscale[m], wsc));
-            if (T.acc_out) T.acc_out[o] = tot;
+            const long long sum = (long long)((old + add) & 0xffffffffffffull);
+            tot = (int)(sum - (long long)a.wk * 2147483648ll);
+            s_acc[slot][row][m] = 0ull;
           }
+        }
+        if (last) {
+          const int64_t o = (int64_t)m * T.N + row0 + row;
+          T.y[o] = __fmul_rn(__int2float_rn(tot), __fmul_rn(xsc, wsc));
+          if (T.acc_out) T.acc_out[o] = tot;
         }
       }
     }
