@@ -30,6 +30,7 @@ SIGNATURES = {
     "bitnet_device_error": (_INT, [_P, _P]),
     "bitnet_quantize_weights_workspace": (_SZ, [_I64, _I64]),
     "bitnet_quantize_weights": (_INT, [_P, _I64, _I64, _P, _P, _P, _SZ, _P]),
+    "bitnet_quantize_weights_noalloc": (_INT, [_P, _I64, _I64, _P, _P, _P]),
     "bitnet_quantize_act": (_INT, [_P, _I64, _I64, _P, _P, _P]),
     "bitnet_linear_workspace": (_SZ, [_I64, _I64, _I64]),
     "bitnet_linear": (_INT, [_P, _P, _P, _P, _I64, _I64, _I64, _P, _P, _P, _SZ, _P]),
@@ -135,6 +136,20 @@ def bitnet_quantize_weights(W, Wq=None, w_scale=None, ws=None, stream=None):
     _check("bitnet_quantize_weights", lib().bitnet_quantize_weights(
         _ptr(W, torch.float32, "W"), N, K, _ptr(Wq, torch.uint8, "Wq"),
         _ptr(w_scale, torch.float32, "w_scale"), _ptr(ws, name="ws"), nb, _stream(stream)))
+    return Wq, w_scale
+
+
+def bitnet_quantize_weights_noalloc(W, Wq=None, w_scale=None, stream=None):
+    """As bitnet_quantize_weights, with the library's own fixed scratch (no
+    workspace argument).  Calls that overlap on the GPU must be serialised."""
+    N, K = W.shape
+    if Wq is None:
+        Wq = torch.empty((N, K // 4), dtype=torch.uint8, device=W.device)
+    if w_scale is None:
+        w_scale = torch.empty(1, dtype=torch.float32, device=W.device)
+    _check("bitnet_quantize_weights_noalloc", lib().bitnet_quantize_weights_noalloc(
+        _ptr(W, torch.float32, "W"), N, K, _ptr(Wq, torch.uint8, "Wq"),
+        _ptr(w_scale, torch.float32, "w_scale"), _stream(stream)))
     return Wq, w_scale
 
 

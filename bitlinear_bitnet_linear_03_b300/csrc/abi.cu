@@ -138,6 +138,19 @@ bitnet_status bitnet_quantize_weights(const float* W, int64_t N, int64_t K, uint
       bitnet::launch_quantize_weights(W, N * K, Wq, w_scale, ws, (cudaStream_t)stream));
 }
 
+bitnet_status bitnet_quantize_weights_noalloc(const float* W, int64_t N, int64_t K, uint8_t* Wq,
+                                              float* w_scale, void* stream) {
+  if (!W || !Wq || !w_scale) return BITNET_ERR_NULL;
+  if (N <= 0 || K <= 0 || K % 64 != 0 || N > ((int64_t)1 << 40) / K) return BITNET_ERR_SHAPE;
+  if (bitnet::quantize_weights_workspace(N * K) > bitnet::quantize_weights_noalloc_limit())
+    return BITNET_ERR_SHAPE;
+  if (!aligned16(W) || !aligned16(Wq)) return BITNET_ERR_ALIGN;
+  bitnet_status st = check_device();
+  if (st != BITNET_OK) return st;
+  return cuda_status(
+      bitnet::launch_quantize_weights_noalloc(W, N * K, Wq, w_scale, (cudaStream_t)stream));
+}
+
 bitnet_status bitnet_quantize_act(const uint16_t* x, int64_t M, int64_t K, int8_t* xq,
                                   float* x_scale, void* stream) {
   if (!x || !xq || !x_scale) return BITNET_ERR_NULL;

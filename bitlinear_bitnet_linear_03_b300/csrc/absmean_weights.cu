@@ -13,6 +13,8 @@
 // in which blocks, warps and threads add.  One thread then forms the exact
 // multi-word sum, divides by N*K and rounds once to binary32 (nearest, ties to
 // even).  No floating-point reduction takes place anywhere.
+#include <mutex>
+
 #include "common.cuh"
 
 namespace bitnet {
@@ -242,6 +244,48 @@ cudaError_t launch_quantize_weights(const float* W, int64_t total, uint8_t* Wq, 
   k_ternary_pack<<<(unsigned)grid, 256, 0, s>>>(reinterpret_cast<const float4*>(W), nblk64,
                                                 w_scale, reinterpret_cast<uint32_t*>(Wq));
   return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant (bitnet_quantize_weights_noalloc).  The stage-1
+// partials live in this file-scope device array instead of caller-provided
+// workspace.  Stage 1 never uses more than kMaxBlocks rows of kRow words,
+// whatever N*K is, so the array covers every accepted size.  Each call writes
+// every word it later reads, so nothing has to start at zero; calls that
+// overlap on the GPU (other streams, other host threads) share the array and
+// race.
+constexpr size_t kNoAllocScratchBytes = (size_t)kMaxBlocks * kRow * sizeof(unsigned long long);
+static __device__ __align__(256) unsigned long long g_absmean_scratch[kMaxBlocks * kRow];
+
+namespace {
+// Device address of g_absmean_scratch per device, looked up once with that
+// device current (a host-side name of a __device__ array is not a device
+// address).
+constexpr int kMaxDevices = 64;
+void* g_scratch_ptr[kMaxDevices];
+std::mutex g_scratch_mutex;
+}  // namespace
+
+size_t quantize_weights_noalloc_limit() { return kNoAllocScratchBytes; }
+
+cudaError_t launch_quantize_weights_noalloc(const float* W, int64_t total, uint8_t* Wq,
+                                            float* w_scale, cudaStream_t s) {
+  if (quantize_weights_workspace(total) > kNoAllocScratchBytes) return cudaErrorInvalidValue;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  void* ptr = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_scratch_mutex);
+    if (g_scratch_ptr[dev] == nullptr) {
+      e = cudaGetSymbolAddress(&ptr, g_absmean_scratch);
+      if (e != cudaSuccess) return e;
+      g_scratch_ptr[dev] = ptr;
+    }
+    ptr = g_scratch_ptr[dev];
+  }
+  return launch_quantize_weights(W, total, Wq, w_scale, ptr, s);
 }
 
 }  // namespace bitnet

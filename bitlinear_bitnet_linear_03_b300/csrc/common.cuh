@@ -135,6 +135,13 @@ size_t quantize_weights_workspace(int64_t total);
 cudaError_t launch_quantize_weights(const float* W, int64_t total, uint8_t* Wq, float* w_scale,
                                     void* ws, cudaStream_t s);
 
+// The same, with its scratch in a device array of the library instead of a
+// caller workspace (absmean_weights.cu); cudaErrorInvalidValue beyond the
+// array's size.
+size_t quantize_weights_noalloc_limit();
+cudaError_t launch_quantize_weights_noalloc(const float* W, int64_t total, uint8_t* Wq,
+                                            float* w_scale, cudaStream_t s);
+
 // Activation quantisation (act_quant.cu).
 cudaError_t launch_quantize_act_bf16(const uint16_t* x, int64_t M, int64_t K, int8_t* xq,
                                      float* x_scale, cudaStream_t s);

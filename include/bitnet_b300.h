@@ -98,6 +98,26 @@ bitnet_status bitnet_quantize_weights(const float* W, int64_t N, int64_t K,
                                       size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
+ * bitnet_quantize_weights without a workspace argument.  The pages have no
+ * counterpart to this call: it exists for callers that cannot allocate
+ * device memory, e.g. a plugin inside a framework that owns the whole device
+ * memory pool, or a latency-critical path where cudaMalloc (which may
+ * synchronise the device) is not allowed.  Results are identical to
+ * bitnet_quantize_weights.
+ * The scratch is a fixed array of 1,212,416 bytes inside the library, held by
+ * every device that loads the library until the process exits; it covers
+ * every N*K the call accepts (N*K < 2^40, K % 64 == 0; anything else gives
+ * BITNET_ERR_SHAPE).  Nothing is allocated or freed.
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  Every call uses the same array: calls whose work overlaps on the
+ * GPU (other streams, other host threads) race and must be serialised by the
+ * caller.  Each call writes all the scratch it reads, so no state carries
+ * over between calls. */
+bitnet_status bitnet_quantize_weights_noalloc(const float* W, int64_t N, int64_t K,
+                                              uint8_t* Wq, float* w_scale, void* stream);
+
+/* ------------------------------------------------------------------------
  * Per-token absmax int8 activation quantisation ([P1] "A8"; [P4]).
  * For each row m of x [M, K] (bf16):
  *   a = max_k |x|, a' = max(a, 1e-5), inv = 127 / a' (binary32 division),
