@@ -1,16 +1,499 @@
-// gemm_tc.cu — tensor-core BitLinear (prefill).  Placeholder until the
-// tcgen05 kernel lands: no shape is eligible, so every call runs on CUDA cores.
+// gemm_tc.cu — tensor-core BitLinear for prefill-sized M.
+//
+// The product is the BitLinear contraction of "BitNet.cpp deep dive"
+// (dashen-tech), §3.1 (acc = sum_pos - sum_neg = sum_k q[n,k] x[m,k]) over a
+// whole block of tokens, with the rescale y = (float)acc * (x_scale *
+// w_scale).  sm_103a has no integer tensor-core MMA (ptxas rejects
+// tcgen05.mma .kind::i8 for this target), so the contraction runs as
+// kind::f16 with bf16 operands: ternary weights and int8 activations are
+// exact in bf16 (integers of magnitude <= 256), every product is exact, and
+// every partial sum is an integer of magnitude <= 128 K < 2^24 for
+// K <= 65536, so the binary32 accumulator is exact and independent of the
+// order of the additions; the epilogue converts it back to int32 without
+// rounding.
+//
+// Pipeline (one CTA per SM, persistent over 128 x 256 output tiles):
+//  * pre-pass kernels expand the packed 2-bit weights once per call into a
+//    K-major bf16 operand B [N, K] and the int8 activations into A [M, K]
+//    bf16, both in the workspace (and largely in L2 during the GEMM);
+//  * warp 0, one lane: TMA (cp.async.bulk.tensor.2d, 128-byte swizzle) loads
+//    the A and B tiles of each 128-byte K step into a 4-stage ring;
+//  * warp 1: allocates 512 TMEM columns (two 256-column fp32
+//    accumulators) and one lane issues tcgen05.mma for each stage, releasing
+//    the stage with tcgen05.commit;
+//  * warps 2-5: tcgen05.ld the finished accumulator (one TMEM lane = one
+//    output row per thread), rescale, store; the other accumulator takes the
+//    next tile meanwhile.
+// Every mbarrier wait is bounded; on time-out the kernel records an error in
+// g_device_error, drains what it issued and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "common.cuh"
 #include "gemm_tc.cuh"
 
 namespace bitnet {
 
 __device__ int g_device_error;
 
-bool gemm_tc_eligible(int64_t, int64_t, int64_t) { return false; }
-size_t gemm_tc_workspace(int64_t, int64_t, int64_t) { return 0; }
-cudaError_t launch_gemm_tc(const uint8_t*, const float*, const int8_t*, const float*, int64_t,
-                           int64_t, int64_t, float*, int32_t*, void*, cudaStream_t) {
-  return cudaErrorNotSupported;
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kBN = 256;
+constexpr int kRowBytes = 128;  // K bytes of one row per stage (one swizzle atom)
+constexpr int kStages = 4;
+constexpr int kATileBytes = kBM * kRowBytes;
+constexpr int kBTileBytes = kBN * kRowBytes;
+constexpr int kStageBytes = kATileBytes + kBTileBytes;
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 512;
+constexpr int kSmemBytes = kStages * kStageBytes + 1024;  // + alignment slack
+constexpr long long kWaitCycles = 2000000000ll;
+constexpr int kErrProducer = 1 << 4, kErrMma = 1 << 5, kErrEpilogue = 1 << 6, kErrDrain = 1 << 7;
+
+// Operand element: bf16 (2 bytes), 64 elements of K per 128-byte stage row.
+template <int KIND>
+struct Kind;
+template <>
+struct Kind<1> {
+  static constexpr int kElem = 2;
+  static constexpr int kKStage = kRowBytes / kElem;  // 64 elements per stage
+  // D f32 (1), A bf16 (1), B bf16 (1), K-major, N/8, M/16.
+  static constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
+                                     ((uint32_t)(kBN >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
+};
+// Every tcgen05.mma consumes 32 bytes of K per row (16 bf16 or 32 int8).
+constexpr int kMmaKBytes = 32;
+
+struct Args {
+  int M, N, K;
+  int m_tiles, n_tiles, k_stages;
+  const float* x_scale;
+  const float* w_scale;
+  float* y;
+  int32_t* acc_out;
+};
+
+// ---- PTX wrappers (PTX ISA: mbarrier, cp.async.bulk.tensor, tcgen05)
+__device__ __forceinline__ uint32_t saddr(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  if (mbar_try(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try(bar, parity))
+    if (clock64() - t0 > kWaitCycles) return false;
+  return true;
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   bar)
+               : "memory");
+}
+template <int KIND>
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(Kind<KIND>::kIdesc), "r"(accumulate)
+      : "memory");
+}
+// Shared-memory matrix descriptor of a K-major operand tile written by TMA
+// with 128-byte swizzle: rows of 128 bytes, 8-row groups 1024 bytes apart
+// (stride byte offset), start address advanced by 32 bytes per K step inside
+// the swizzle atom.  Bits: [0,14) start >> 4, [16,30) leading offset >> 4
+// (unused for swizzled K-major), [32,46) stride offset >> 4, [46,48) = 1,
+// [61,64) = 2 (128-byte swizzle).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t smem_addr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((smem_addr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)(16u >> 4) << 16;
+  d |= (uint64_t)(1024u >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+template <int KIND>
+__global__ void __launch_bounds__(kThreads, 1)
+k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
+          const __grid_constant__ Args a) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t full_bar[kStages];
+  __shared__ __align__(8) uint64_t empty_bar[kStages];
+  __shared__ __align__(8) uint64_t acc_full[2];
+  __shared__ __align__(8) uint64_t acc_empty[2];
+  __shared__ __align__(8) uint64_t drain_bar;
+  __shared__ uint32_t tmem_base_slot;
+  __shared__ int s_abort;
+
+  const uint32_t smem0 = (saddr(smem_raw) + 1023u) & ~1023u;  // 1024-byte aligned tiles
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tiles = a.m_tiles * a.n_tiles;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(saddr(&full_bar[s]), 1);
+      mbar_init(saddr(&empty_bar[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(saddr(&acc_full[b]), 1);
+      mbar_init(saddr(&acc_empty[b]), 4);
+    }
+    mbar_init(saddr(&drain_bar), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    s_abort = 0;
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     saddr(&tmem_base_slot)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_slot;
+  griddep_wait();
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int it = 0, issued = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+        const int m0 = (t % a.m_tiles) * kBM, n0 = (t / a.m_tiles) * kBN;
+        for (int ks = 0; ks < a.k_stages; ++ks, ++it) {
+          const int s = it % kStages;
+          if (it >= kStages && !mbar_wait(saddr(&empty_bar[s]), ((it / kStages) - 1) & 1)) {
+            atomicOr(&g_device_error, kErrProducer);
+            *(volatile int*)&s_abort = 1;
+            ok = false;
+            break;
+          }
+          if (*(volatile int*)&s_abort) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = saddr(&full_bar[s]);
+          const uint32_t sa = smem0 + s * kStageBytes;
+          mbar_expect_tx(fb, kStageBytes);
+          tma_load_2d(sa, &mapA, ks * Kind<KIND>::kKStage, m0, fb);
+          tma_load_2d(sa + kATileBytes, &mapB, ks * Kind<KIND>::kKStage, n0, fb);
+          issued = it + 1;
+        }
+      }
+      // Never return with a copy in flight.
+      for (int j = issued > kStages ? issued - kStages : 0; j < issued; ++j)
+        if (!mbar_wait(saddr(&full_bar[j % kStages]), (j / kStages) & 1)) {
+          atomicOr(&g_device_error, kErrDrain);
+          break;
+        }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int it = 0, lt = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x, ++lt) {
+        const int ab = lt & 1;
+        if (lt >= 2 && !mbar_wait(saddr(&acc_empty[ab]), ((lt >> 1) - 1) & 1)) {
+          atomicOr(&g_device_error, kErrMma);
+          *(volatile int*)&s_abort = 1;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem + (uint32_t)(ab * kBN);
+        for (int ks = 0; ks < a.k_stages; ++ks, ++it) {
+          const int s = it % kStages;
+          if (!mbar_wait(saddr(&full_bar[s]), (it / kStages) & 1) || *(volatile int*)&s_abort) {
+            atomicOr(&g_device_error, kErrMma);
+            *(volatile int*)&s_abort = 1;
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem0 + s * kStageBytes;
+#pragma unroll
+          for (int kk = 0; kk < kRowBytes / kMmaKBytes; ++kk) {
+            const uint64_t ad = sw128_desc(sa + kk * kMmaKBytes);
+            const uint64_t bd = sw128_desc(sa + kATileBytes + kk * kMmaKBytes);
+            tc_mma<KIND>(d, ad, bd, (ks | kk) != 0 ? 1u : 0u);
+          }
+          tc_commit(saddr(&empty_bar[s]));  // frees the stage when these MMAs finish
+        }
+        if (!ok) break;
+        tc_commit(saddr(&acc_full[ab]));    // accumulator ready for the epilogue
+      }
+      // All MMAs issued by this thread have finished before TMEM is freed.
+      tc_commit(saddr(&drain_bar));
+      if (!mbar_wait(saddr(&drain_bar), 0)) atomicOr(&g_device_error, kErrDrain);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int quarter = warp & 3;  // TMEM lanes this warp may access
+    const int row = quarter * 32 + lane;
+    const float ws = *a.w_scale;
+    int lt = 0;
+    for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++lt) {
+      const int ab = lt & 1;
+      if (!mbar_wait(saddr(&acc_full[ab]), (lt >> 1) & 1) || *(volatile int*)&s_abort) {
+        if (lane == 0) atomicOr(&g_device_error, kErrEpilogue);
+        *(volatile int*)&s_abort = 1;
+        break;
+      }
+      tc_fence_after();
+      const int m0 = (t % a.m_tiles) * kBM, n0 = (t / a.m_tiles) * kBN;
+      const int m = m0 + row;
+      const bool mrow = m < a.M;
+      const float c = mrow ? __fmul_rn(a.x_scale[m], ws) : 0.0f;
+      float* yrow = a.y + (int64_t)m * a.N;
+      int32_t* arow = a.acc_out ? a.acc_out + (int64_t)m * a.N : nullptr;
+      const bool vec = (a.N & 3) == 0;
+      for (int cb = 0; cb < kBN; cb += 32) {
+        uint32_t r[32];
+        tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(ab * kBN + cb), r);
+        if (!mrow) continue;
+        int v[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          v[j] = __float2int_rn(__uint_as_float(r[j]));  // exact integer
+        const int nb = n0 + cb;
+        if (vec && nb + 32 <= a.N) {
+#pragma unroll
+          for (int j = 0; j < 32; j += 4) {
+            float4 o = make_float4(__fmul_rn(__int2float_rn(v[j]), c),
+                                   __fmul_rn(__int2float_rn(v[j + 1]), c),
+                                   __fmul_rn(__int2float_rn(v[j + 2]), c),
+                                   __fmul_rn(__int2float_rn(v[j + 3]), c));
+            *reinterpret_cast<float4*>(yrow + nb + j) = o;
+            if (arow) *reinterpret_cast<int4*>(arow + nb + j) = make_int4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (nb + j < a.N) {
+              yrow[nb + j] = __fmul_rn(__int2float_rn(v[j]), c);
+              if (arow) arow[nb + j] = v[j];
+            }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(saddr(&acc_empty[ab]));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(kTmemCols)
+                 : "memory");
+}
+
+// ---- pre-pass kernels
+// B[n, k] = q[n, k] as bf16 from the packed codes (the 16-byte block of 64
+// weights holds, in word i at field s, the codes of weights 16s + 4i + t);
+// q in {-1, 0, 1} is exact in bf16: 0xBF80, 0x0000, 0x3F80.
+__device__ __forceinline__ uint32_t code_to_bf16(uint32_t c) {
+  return c == 0 ? 0xBF80u : (c == 2 ? 0x3F80u : 0u);
+}
+__global__ void k_unpack_bf16(const uint4* __restrict__ Wq, int64_t nblk, uint4* __restrict__ B) {
+  for (int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; b < nblk;
+       b += (int64_t)gridDim.x * blockDim.x) {
+    const uint4 w = Wq[b];
+    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int s = 0; s < 4; ++s)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        uint32_t c[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) c[t] = (ww[i] >> (8 * t + 2 * s)) & 3u;
+        // weights 16s + 4i + {0..3}: 8 bytes of bf16 at element 64b + 16s + 4i
+        uint2 o = make_uint2(code_to_bf16(c[0]) | (code_to_bf16(c[1]) << 16),
+                             code_to_bf16(c[2]) | (code_to_bf16(c[3]) << 16));
+        reinterpret_cast<uint2*>(B)[(b * 64 + 16 * s + 4 * i) / 4] = o;
+      }
+  }
+}
+
+// A[m, k] = (bf16) xq[m, k]; exact for int8.
+__global__ void k_i8_to_bf16(const uint32_t* __restrict__ xq, int64_t n4, uint2* __restrict__ A) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const uint32_t w = xq[i];
+    uint32_t h[4];
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const int v = (int)(int8_t)((w >> (8 * t)) & 0xffu);
+      // |v| <= 128 has at most 8 significant bits: the binary32 value's low
+      // 16 bits are zero and its top half is the exact bf16.
+      h[t] = __float_as_uint(__int2float_rn(v)) >> 16;
+    }
+    A[i] = make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
+  }
+}
+
+// ---- host side
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::mutex g_encode_mutex;
+
+cudaError_t get_encode() {
+  std::lock_guard<std::mutex> lock(g_encode_mutex);
+  if (g_encode) return cudaSuccess;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                   cudaEnableDefault, &q);
+  if (e != cudaSuccess) return e;
+  if (q != cudaDriverEntryPointSuccess || !fn) return cudaErrorSymbolNotFound;
+  g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  return cudaSuccess;
+}
+
+// 2-D K-major operand [rows, K], boxes of (128 bytes of K) x box_rows.
+cudaError_t encode_operand(CUtensorMap* map, const void* base, int64_t rows, int64_t K,
+                           int elem_bytes, int box_rows) {
+  const CUtensorMapDataType dt =
+      elem_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)(K * elem_bytes)};
+  cuuint32_t box[2] = {(cuuint32_t)(kRowBytes / elem_bytes), (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+// Operand kind used for the tensor-core path (bf16; see the top of the file).
+constexpr int kKind = 1;
+
+size_t round1k(size_t v) { return (v + 1023) / 1024 * 1024; }
+
+template <int KIND>
+cudaError_t launch_kind(const uint8_t* Wq, const float* w_scale, const int8_t* xq,
+                        const float* x_scale, int64_t M, int64_t N, int64_t K, float* y,
+                        int32_t* acc_out, void* ws, cudaStream_t s) {
+  cudaError_t e = get_encode();
+  if (e != cudaSuccess) return e;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  void* B = w;
+  const void* A = xq;
+  const int64_t nblk = N * K / 64;
+  int64_t grid = (nblk + 255) / 256;
+  if (grid > 148 * 8) grid = 148 * 8;
+  {
+    k_unpack_bf16<<<(unsigned)grid, 256, 0, s>>>(reinterpret_cast<const uint4*>(Wq), nblk,
+                                                 reinterpret_cast<uint4*>(B));
+    void* Ab = w + round1k((size_t)(N * K * 2));
+    const int64_t n4 = M * K / 4;
+    int64_t g2 = (n4 + 255) / 256;
+    if (g2 > 148 * 8) g2 = 148 * 8;
+    k_i8_to_bf16<<<(unsigned)g2, 256, 0, s>>>(reinterpret_cast<const uint32_t*>(xq), n4,
+                                              reinterpret_cast<uint2*>(Ab));
+    A = Ab;
+  }
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  CUtensorMap mapA, mapB;
+  e = encode_operand(&mapA, A, M, K, Kind<KIND>::kElem, kBM);
+  if (e == cudaSuccess) e = encode_operand(&mapB, B, N, K, Kind<KIND>::kElem, kBN);
+  if (e != cudaSuccess) return e;
+  Args a;
+  a.M = (int)M;
+  a.N = (int)N;
+  a.K = (int)K;
+  a.m_tiles = (int)((M + kBM - 1) / kBM);
+  a.n_tiles = (int)((N + kBN - 1) / kBN);
+  a.k_stages = (int)((K + Kind<KIND>::kKStage - 1) / Kind<KIND>::kKStage);
+  a.x_scale = x_scale;
+  a.w_scale = w_scale;
+  a.y = y;
+  a.acc_out = acc_out;
+  static bool configured[64] = {};
+  int dev = 0;
+  e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 64 && !configured[dev]) {
+    e = cudaFuncSetAttribute(k_gemm_tc<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured[dev] = true;
+  }
+  const int tiles = a.m_tiles * a.n_tiles;
+  const int ctas = tiles < 148 ? tiles : 148;
+  return launch_pdl(k_gemm_tc<KIND>, dim3(ctas), dim3(kThreads), (size_t)kSmemBytes, s, mapA,
+                    mapB, a);
+}
+
+}  // namespace
+
+bool gemm_tc_eligible(int64_t M, int64_t N, int64_t K) {
+  return M >= 64 && N >= 1 && K >= 64 && K % 64 == 0;
+}
+
+size_t gemm_tc_workspace(int64_t M, int64_t N, int64_t K) {
+  return round1k((size_t)(N * K * 2)) + round1k((size_t)(M * K * 2));
+}
+
+cudaError_t launch_gemm_tc(const uint8_t* Wq, const float* w_scale, const int8_t* xq,
+                           const float* x_scale, int64_t M, int64_t N, int64_t K, float* y,
+                           int32_t* acc_out, void* ws, cudaStream_t s) {
+  return launch_kind<kKind>(Wq, w_scale, xq, x_scale, M, N, K, y, acc_out, ws, s);
 }
 
 cudaError_t read_and_clear_device_error(int* code, cudaStream_t s) {
