@@ -272,13 +272,16 @@ def profiled_traffic(kernel_file, profile_file):
         return None
 
 
-def secondary_measurements(torch, bn):
-    """Prefill GEMM (M = 4096) and the fused FFN at seq 1 / seq 4096, timed
-    with CUDA events after warm-up (inputs resident; the prefill outputs are
-    113 MB, weights rotate over 8 sets)."""
+def secondary_measurements(torch, bn, peaks):
+    """Prefill BitLinear (M = 4096 tokens, the pages' maximum context) on the
+    2B-class FFN shapes, timed with CUDA events after warm-up over 4 rotating
+    weight sets; tensor-core roofline against the measured bf16 dense peak
+    (sm_103a has no integer tensor-core MMA, so the exact integer products
+    run as bf16 MMAs with binary32 accumulation)."""
     from bitlinear_bitnet_linear_03_b300 import synth
     out = {}
     dev = torch.device("cuda")
+    peak = float(peaks["bf16_tflops"]) if peaks and peaks.get("bf16_tflops") else 1800.0
     for (N, K) in [(6912, 2560), (2560, 6912)]:
         M = 4096
         sets = []
@@ -295,7 +298,7 @@ def secondary_measurements(torch, bn):
             Wq, s = sets[i % 4]
             bn.bitnet_linear(Wq, s, xq, sx, y=y, ws=ws)
         torch.cuda.synchronize()
-        reps = 8
+        reps = 20
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
         for i in range(reps):
@@ -304,7 +307,12 @@ def secondary_measurements(torch, bn):
         e1.record()
         torch.cuda.synchronize()
         t = e0.elapsed_time(e1) / 1e3 / reps
-        out[f"prefill_M4096_K{K}_N{N}"] = {"ms": t * 1e3, "tops": 2 * M * N * K / t / 1e12}
+        tops = 2 * M * N * K / t / 1e12
+        out[f"prefill_M{M}_K{K}_N{N}"] = {
+            "ms": round(t * 1e3, 4), "tops": round(tops, 1),
+            "roofline": {"bound": "tensor", "achieved": round(tops, 1), "peak": peak,
+                         "unit": "TFLOP/s", "frac": round(tops / peak, 4),
+                         "peak_source": "measured bf16 dense (no int8 tensor MMA on sm_103a)"}}
         del sets, xq, sx, y, ws
     return out
 
@@ -401,7 +409,7 @@ def run_gpu_arm(args, rank, world, barrier, max_over_ranks):
         "clocks": clk,
     }
     if not args.no_secondary:
-        result["secondary"] = secondary_measurements(torch, bn)
+        result["secondary"] = secondary_measurements(torch, bn, peaks)
     return result
 
 
