@@ -12,12 +12,14 @@
 // order of the additions; the epilogue converts it back to int32 without
 // rounding.
 //
-// Pipeline (one CTA per SM, persistent over 128 x 256 output tiles):
+// Pipeline (one CTA per SM, persistent over 128 x BN output tiles, BN = 256
+// or 128, whichever fills the last wave of 148 SMs better):
 //  * pre-pass kernels expand the packed 2-bit weights once per call into a
 //    K-major bf16 operand B [N, K] and the int8 activations into A [M, K]
 //    bf16, both in the workspace (and largely in L2 during the GEMM);
 //  * warp 0, one lane: TMA (cp.async.bulk.tensor.2d, 128-byte swizzle) loads
-//    the A and B tiles of each 128-byte K step into a 4-stage ring;
+//    the A and B tiles of each 128-byte K step into a 192 KB ring (4 stages
+//    for 256-wide tiles, 6 for 128-wide ones);
 //  * warp 1: allocates 512 TMEM columns (two 256-column fp32
 //    accumulators) and one lane issues tcgen05.mma for each stage, releasing
 //    the stage with tcgen05.commit;
@@ -41,15 +43,19 @@ __device__ int g_device_error;
 namespace {
 
 constexpr int kBM = 128;
-constexpr int kBN = 256;
 constexpr int kRowBytes = 128;  // K bytes of one row per stage (one swizzle atom)
-constexpr int kStages = 4;
 constexpr int kATileBytes = kBM * kRowBytes;
-constexpr int kBTileBytes = kBN * kRowBytes;
-constexpr int kStageBytes = kATileBytes + kBTileBytes;
 constexpr int kThreads = 192;
 constexpr uint32_t kTmemCols = 512;
-constexpr int kSmemBytes = kStages * kStageBytes + 1024;  // + alignment slack
+constexpr int kRingBytes = 192 * 1024;
+// Tile N = BN (256 or 128): B tile, stage size, ring depth and shared memory.
+template <int BN>
+struct Tile {
+  static constexpr int kBTileBytes = BN * kRowBytes;
+  static constexpr int kStageBytes = kATileBytes + kBTileBytes;
+  static constexpr int kStages = kRingBytes / kStageBytes;   // 4 or 6
+  static constexpr int kSmemBytes = kStages * kStageBytes + 1024;  // + alignment slack
+};
 constexpr long long kWaitCycles = 2000000000ll;
 constexpr int kErrProducer = 1 << 4, kErrMma = 1 << 5, kErrEpilogue = 1 << 6, kErrDrain = 1 << 7;
 
@@ -60,9 +66,13 @@ template <>
 struct Kind<1> {
   static constexpr int kElem = 2;
   static constexpr int kKStage = kRowBytes / kElem;  // 64 elements per stage
-  // D f32 (1), A bf16 (1), B bf16 (1), K-major, N/8, M/16.
-  static constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
-                                     ((uint32_t)(kBN >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
+  // Instruction descriptor: D f32 (bits 4-5 = 1), A bf16 (bits 7-9 = 1),
+  // B bf16 (bits 10-12 = 1), K-major A and B (bits 15, 16 = 0), M/16 at
+  // bits 24-28; N/8 at bits 17-22 is added per tile shape.
+  static constexpr uint32_t kIdescBase =
+      (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kBM >> 4) << 24);
+  template <int BN>
+  static constexpr uint32_t idesc() { return kIdescBase | ((uint32_t)(BN >> 3) << 17); }
 };
 // Every tcgen05.mma consumes 32 bytes of K per row (16 bf16 or 32 int8).
 constexpr int kMmaKBytes = 32;
@@ -126,13 +136,13 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
                    bar)
                : "memory");
 }
-template <int KIND>
+template <int KIND, int BN>
 __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
                                        uint32_t accumulate) {
   asm volatile(
       "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
       " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(Kind<KIND>::kIdesc), "r"(accumulate)
+      "l"(adesc), "l"(bdesc), "r"(Kind<KIND>::template idesc<BN>()), "r"(accumulate)
       : "memory");
 }
 // Shared-memory matrix descriptor of a K-major operand tile written by TMA
@@ -163,11 +173,13 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-template <int KIND>
+template <int KIND, int BN>
 __global__ void __launch_bounds__(kThreads, 1)
 k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
           const __grid_constant__ Args a) {
   extern __shared__ uint8_t smem_raw[];
+  constexpr int kStages = Tile<BN>::kStages;
+  constexpr int kStageBytes = Tile<BN>::kStageBytes;
   __shared__ __align__(8) uint64_t full_bar[kStages];
   __shared__ __align__(8) uint64_t empty_bar[kStages];
   __shared__ __align__(8) uint64_t acc_full[2];
@@ -212,7 +224,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUte
       int it = 0, issued = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
-        const int m0 = (t % a.m_tiles) * kBM, n0 = (t / a.m_tiles) * kBN;
+        const int m0 = (t % a.m_tiles) * kBM, n0 = (t / a.m_tiles) * BN;
         for (int ks = 0; ks < a.k_stages; ++ks, ++it) {
           const int s = it % kStages;
           if (it >= kStages && !mbar_wait(saddr(&empty_bar[s]), ((it / kStages) - 1) & 1)) {
@@ -253,7 +265,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUte
           break;
         }
         tc_fence_after();
-        const uint32_t d = tmem + (uint32_t)(ab * kBN);
+        const uint32_t d = tmem + (uint32_t)(ab * BN);
         for (int ks = 0; ks < a.k_stages; ++ks, ++it) {
           const int s = it % kStages;
           if (!mbar_wait(saddr(&full_bar[s]), (it / kStages) & 1) || *(volatile int*)&s_abort) {
@@ -268,7 +280,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUte
           for (int kk = 0; kk < kRowBytes / kMmaKBytes; ++kk) {
             const uint64_t ad = sw128_desc(sa + kk * kMmaKBytes);
             const uint64_t bd = sw128_desc(sa + kATileBytes + kk * kMmaKBytes);
-            tc_mma<KIND>(d, ad, bd, (ks | kk) != 0 ? 1u : 0u);
+            tc_mma<KIND, BN>(d, ad, bd, (ks | kk) != 0 ? 1u : 0u);
           }
           tc_commit(saddr(&empty_bar[s]));  // frees the stage when these MMAs finish
         }
@@ -293,16 +305,16 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUte
         break;
       }
       tc_fence_after();
-      const int m0 = (t % a.m_tiles) * kBM, n0 = (t / a.m_tiles) * kBN;
+      const int m0 = (t % a.m_tiles) * kBM, n0 = (t / a.m_tiles) * BN;
       const int m = m0 + row;
       const bool mrow = m < a.M;
       const float c = mrow ? __fmul_rn(a.x_scale[m], ws) : 0.0f;
       float* yrow = a.y + (int64_t)m * a.N;
       int32_t* arow = a.acc_out ? a.acc_out + (int64_t)m * a.N : nullptr;
       const bool vec = (a.N & 3) == 0;
-      for (int cb = 0; cb < kBN; cb += 32) {
+      for (int cb = 0; cb < BN; cb += 32) {
         uint32_t r[32];
-        tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(ab * kBN + cb), r);
+        tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(ab * BN + cb), r);
         if (!mrow) continue;
         int v[32];
 #pragma unroll
@@ -344,46 +356,60 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUte
 }
 
 // ---- pre-pass kernels
-// B[n, k] = q[n, k] as bf16 from the packed codes (the 16-byte block of 64
-// weights holds, in word i at field s, the codes of weights 16s + 4i + t);
-// q in {-1, 0, 1} is exact in bf16: 0xBF80, 0x0000, 0x3F80.
-__device__ __forceinline__ uint32_t code_to_bf16(uint32_t c) {
-  return c == 0 ? 0xBF80u : (c == 2 ? 0x3F80u : 0u);
-}
-__global__ void k_unpack_bf16(const uint4* __restrict__ Wq, int64_t nblk, uint4* __restrict__ B) {
-  for (int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; b < nblk;
-       b += (int64_t)gridDim.x * blockDim.x) {
-    const uint4 w = Wq[b];
-    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-    for (int s = 0; s < 4; ++s)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        uint32_t c[4];
-#pragma unroll
-        for (int t = 0; t < 4; ++t) c[t] = (ww[i] >> (8 * t + 2 * s)) & 3u;
-        // weights 16s + 4i + {0..3}: 8 bytes of bf16 at element 64b + 16s + 4i
-        uint2 o = make_uint2(code_to_bf16(c[0]) | (code_to_bf16(c[1]) << 16),
-                             code_to_bf16(c[2]) | (code_to_bf16(c[3]) << 16));
-        reinterpret_cast<uint2*>(B)[(b * 64 + 16 * s + 4 * i) / 4] = o;
-      }
-  }
+// Two bf16 values from two 2-bit codes held at bits 0-1 and 16-17 of p:
+// code 0, 1, 2 -> q = -1, 0, +1 -> 0xBF80, 0x0000, 0x3F80 (exact).
+__device__ __forceinline__ uint32_t bf16_pair_from_codes(uint32_t p) {
+  const uint32_t t = p ^ 0x00010001u;
+  const uint32_t nz = (t | (t >> 1)) & 0x00010001u;    // code != 1
+  const uint32_t neg = ~(p | (p >> 1)) & 0x00010001u;  // code == 0
+  return nz * 0x3F80u | (neg << 15);
 }
 
-// A[m, k] = (bf16) xq[m, k]; exact for int8.
-__global__ void k_i8_to_bf16(const uint32_t* __restrict__ xq, int64_t n4, uint2* __restrict__ A) {
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
-       i += (int64_t)gridDim.x * blockDim.x) {
-    const uint32_t w = xq[i];
-    uint32_t h[4];
+// Pre-pass, one launch: items [0, nblk) expand a 16-byte packed block (64
+// weights) of Wq into 128 bytes of bf16 B; items [nblk, nblk + nx) widen 16
+// int8 activations into 32 bytes of bf16 A.  In a packed block, chunk c of 8
+// consecutive weights (k = 8c .. 8c+7) is field s = c/2 of words 2(c%2) and
+// 2(c%2)+1.  All stores are 16 bytes wide.
+__global__ void __launch_bounds__(256)
+k_prepass(const uint4* __restrict__ Wq, int64_t nblk, uint4* __restrict__ B,
+          const uint4* __restrict__ xq, int64_t nx, uint4* __restrict__ A) {
+  const int64_t total = nblk + nx;
+  for (int64_t it = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; it < total;
+       it += (int64_t)gridDim.x * blockDim.x) {
+    if (it < nblk) {
+      const uint4 w = Wq[it];
+      const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-    for (int t = 0; t < 4; ++t) {
-      const int v = (int)(int8_t)((w >> (8 * t)) & 0xffu);
-      // |v| <= 128 has at most 8 significant bits: the binary32 value's low
-      // 16 bits are zero and its top half is the exact bf16.
-      h[t] = __float_as_uint(__int2float_rn(v)) >> 16;
+      for (int c = 0; c < 8; ++c) {
+        const int sft = 2 * (c >> 1), h = c & 1;
+        const uint32_t u0 = (ww[2 * h] >> sft) & 0x03030303u;
+        const uint32_t u1 = (ww[2 * h + 1] >> sft) & 0x03030303u;
+        uint4 o;
+        o.x = bf16_pair_from_codes((u0 & 3u) | ((u0 & 0x300u) << 8));
+        o.y = bf16_pair_from_codes(((u0 >> 16) & 3u) | ((u0 >> 8) & 0x30000u));
+        o.z = bf16_pair_from_codes((u1 & 3u) | ((u1 & 0x300u) << 8));
+        o.w = bf16_pair_from_codes(((u1 >> 16) & 3u) | ((u1 >> 8) & 0x30000u));
+        B[it * 8 + c] = o;
+      }
+    } else {
+      const int64_t i = it - nblk;
+      const uint4 v = xq[i];
+      const uint32_t vv[4] = {v.x, v.y, v.z, v.w};
+      uint32_t h[8];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        // |x| <= 128 has at most 8 significant bits: the binary32 value's
+        // low 16 bits are zero and its top half is the exact bf16.
+        const uint32_t b0 = __float_as_uint(__int2float_rn((int)(int8_t)(vv[q] & 0xffu))) >> 16;
+        const uint32_t b1 = __float_as_uint(__int2float_rn((int)(int8_t)((vv[q] >> 8) & 0xffu))) >> 16;
+        const uint32_t b2 = __float_as_uint(__int2float_rn((int)(int8_t)((vv[q] >> 16) & 0xffu))) >> 16;
+        const uint32_t b3 = __float_as_uint(__int2float_rn((int)(int8_t)(vv[q] >> 24))) >> 16;
+        h[2 * q] = b0 | (b1 << 16);
+        h[2 * q + 1] = b2 | (b3 << 16);
+      }
+      A[2 * i] = make_uint4(h[0], h[1], h[2], h[3]);
+      A[2 * i + 1] = make_uint4(h[4], h[5], h[6], h[7]);
     }
-    A[i] = make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
   }
 }
 
@@ -424,7 +450,7 @@ constexpr int kKind = 1;
 
 size_t round1k(size_t v) { return (v + 1023) / 1024 * 1024; }
 
-template <int KIND>
+template <int KIND, int BN>
 cudaError_t launch_kind(const uint8_t* Wq, const float* w_scale, const int8_t* xq,
                         const float* x_scale, int64_t M, int64_t N, int64_t K, float* y,
                         int32_t* acc_out, void* ws, cudaStream_t s) {
@@ -432,33 +458,26 @@ cudaError_t launch_kind(const uint8_t* Wq, const float* w_scale, const int8_t* x
   if (e != cudaSuccess) return e;
   uint8_t* w = static_cast<uint8_t*>(ws);
   void* B = w;
-  const void* A = xq;
-  const int64_t nblk = N * K / 64;
-  int64_t grid = (nblk + 255) / 256;
-  if (grid > 148 * 8) grid = 148 * 8;
-  {
-    k_unpack_bf16<<<(unsigned)grid, 256, 0, s>>>(reinterpret_cast<const uint4*>(Wq), nblk,
-                                                 reinterpret_cast<uint4*>(B));
-    void* Ab = w + round1k((size_t)(N * K * 2));
-    const int64_t n4 = M * K / 4;
-    int64_t g2 = (n4 + 255) / 256;
-    if (g2 > 148 * 8) g2 = 148 * 8;
-    k_i8_to_bf16<<<(unsigned)g2, 256, 0, s>>>(reinterpret_cast<const uint32_t*>(xq), n4,
-                                              reinterpret_cast<uint2*>(Ab));
-    A = Ab;
-  }
+  void* A = w + round1k((size_t)(N * K * 2));
+  const int64_t nblk = N * K / 64, nx = M * K / 16;
+  int64_t grid = (nblk + nx + 255) / 256;
+  if (grid > 148 * 16) grid = 148 * 16;
+  k_prepass<<<(unsigned)grid, 256, 0, s>>>(reinterpret_cast<const uint4*>(Wq), nblk,
+                                           reinterpret_cast<uint4*>(B),
+                                           reinterpret_cast<const uint4*>(xq), nx,
+                                           reinterpret_cast<uint4*>(A));
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   CUtensorMap mapA, mapB;
   e = encode_operand(&mapA, A, M, K, Kind<KIND>::kElem, kBM);
-  if (e == cudaSuccess) e = encode_operand(&mapB, B, N, K, Kind<KIND>::kElem, kBN);
+  if (e == cudaSuccess) e = encode_operand(&mapB, B, N, K, Kind<KIND>::kElem, BN);
   if (e != cudaSuccess) return e;
   Args a;
   a.M = (int)M;
   a.N = (int)N;
   a.K = (int)K;
   a.m_tiles = (int)((M + kBM - 1) / kBM);
-  a.n_tiles = (int)((N + kBN - 1) / kBN);
+  a.n_tiles = (int)((N + BN - 1) / BN);
   a.k_stages = (int)((K + Kind<KIND>::kKStage - 1) / Kind<KIND>::kKStage);
   a.x_scale = x_scale;
   a.w_scale = w_scale;
@@ -469,15 +488,29 @@ cudaError_t launch_kind(const uint8_t* Wq, const float* w_scale, const int8_t* x
   e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 64 && !configured[dev]) {
-    e = cudaFuncSetAttribute(k_gemm_tc<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSmemBytes);
+    e = cudaFuncSetAttribute(k_gemm_tc<KIND, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Tile<BN>::kSmemBytes);
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
   const int tiles = a.m_tiles * a.n_tiles;
   const int ctas = tiles < 148 ? tiles : 148;
-  return launch_pdl(k_gemm_tc<KIND>, dim3(ctas), dim3(kThreads), (size_t)kSmemBytes, s, mapA,
-                    mapB, a);
+  return launch_pdl(k_gemm_tc<KIND, BN>, dim3(ctas), dim3(kThreads),
+                    (size_t)Tile<BN>::kSmemBytes, s, mapA, mapB, a);
+}
+
+// Tile N: 256 unless 128 fills the 148 SMs' last wave clearly better.
+int pick_bn(int64_t M, int64_t N) {
+  const int64_t mt = (M + kBM - 1) / kBM;
+  auto eff = [&](int64_t bn) {
+    const int64_t tiles = mt * ((N + bn - 1) / bn);
+    const int64_t waves = (tiles + 147) / 148;
+    // useful fraction of the CTA-tile slots, and of each tile's columns
+    const double fill = (double)tiles / (double)(waves * 148);
+    const double cols = (double)N / (double)(((N + bn - 1) / bn) * bn);
+    return fill * cols * (bn == 256 ? 1.0 : 0.92);  // a 128-wide tile streams more A per flop
+  };
+  return eff(128) > eff(256) ? 128 : 256;
 }
 
 }  // namespace
@@ -493,7 +526,9 @@ size_t gemm_tc_workspace(int64_t M, int64_t N, int64_t K) {
 cudaError_t launch_gemm_tc(const uint8_t* Wq, const float* w_scale, const int8_t* xq,
                            const float* x_scale, int64_t M, int64_t N, int64_t K, float* y,
                            int32_t* acc_out, void* ws, cudaStream_t s) {
-  return launch_kind<kKind>(Wq, w_scale, xq, x_scale, M, N, K, y, acc_out, ws, s);
+  if (pick_bn(M, N) == 128)
+    return launch_kind<kKind, 128>(Wq, w_scale, xq, x_scale, M, N, K, y, acc_out, ws, s);
+  return launch_kind<kKind, 256>(Wq, w_scale, xq, x_scale, M, N, K, y, acc_out, ws, s);
 }
 
 cudaError_t read_and_clear_device_error(int* code, cudaStream_t s) {
