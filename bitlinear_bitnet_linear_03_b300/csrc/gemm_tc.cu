@@ -12,8 +12,8 @@
 // order of the additions; the epilogue converts it back to int32 without
 // rounding.
 //
-// Pipeline (one CTA per SM, persistent over 128 x BN output tiles, BN = 256
-// or 128, whichever fills the last wave of 148 SMs better):
+// Pipeline (one CTA per SM, persistent over 128 x BN output tiles, BN = 256,
+// or 128 for narrow N):
 //  * pre-pass kernels expand the packed 2-bit weights once per call into a
 //    K-major bf16 operand B [N, K] and the int8 activations into A [M, K]
 //    bf16, both in the workspace (and largely in L2 during the GEMM);
@@ -499,18 +499,13 @@ cudaError_t launch_kind(const uint8_t* Wq, const float* w_scale, const int8_t* x
                     (size_t)Tile<BN>::kSmemBytes, s, mapA, mapB, a);
 }
 
-// Tile N: 256 unless 128 fills the 148 SMs' last wave clearly better.
+// Tile N.  128-wide tiles fill the last wave of 148 SMs better for some
+// shapes, but they stream the bf16 A operand twice as often from L2; measured
+// on B300 (M = 4096, K = 6912, N = 2560) they lose (237 us vs 192 us), so
+// the 256-wide tile is used unless N itself is narrow.
 int pick_bn(int64_t M, int64_t N) {
-  const int64_t mt = (M + kBM - 1) / kBM;
-  auto eff = [&](int64_t bn) {
-    const int64_t tiles = mt * ((N + bn - 1) / bn);
-    const int64_t waves = (tiles + 147) / 148;
-    // useful fraction of the CTA-tile slots, and of each tile's columns
-    const double fill = (double)tiles / (double)(waves * 148);
-    const double cols = (double)N / (double)(((N + bn - 1) / bn) * bn);
-    return fill * cols * (bn == 256 ? 1.0 : 0.92);  // a 128-wide tile streams more A per flop
-  };
-  return eff(128) > eff(256) ? 128 : 256;
+  (void)M;
+  return N <= 128 ? 128 : 256;
 }
 
 }  // namespace
