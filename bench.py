@@ -52,9 +52,11 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--layers", type=int, default=30)
     ap.add_argument("--impl", default="b300", choices=["b300", "reference"])
-    ap.add_argument("--api", default="fused", choices=["fused", "split"],
-                    help="fused: bitnet_linear_bf16 per shared input (4 launches a layer); "
-                         "split: bitnet_quantize_act + bitnet_linear per matrix")
+    ap.add_argument("--api", default="chain", choices=["chain", "fused", "split"],
+                    help="chain: one persistent bitnet_decode_chain_run per step (grid "
+                         "barrier between the 120 dependent phases); fused: "
+                         "bitnet_linear_bf16 per shared input (4 launches a layer); split: "
+                         "bitnet_quantize_act + bitnet_linear per matrix")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-secondary", action="store_true")
     return ap.parse_args()
@@ -62,15 +64,16 @@ def parse_args():
 
 def layer_bytes(api="fused"):
     """Algorithmic bytes of one layer.
-    fused: each of the four calls reads its bf16 input once; each BitLinear
+    fused / chain: each of the four phases reads its bf16 input once; each BitLinear
            reads packed W and its scale and writes fp32 y.
     split: act-quant reads bf16 and writes int8 + scale; each BitLinear reads
            packed W, int8 x, two scales and writes fp32 y."""
+    fused = api in ("fused", "chain")
     b = 0
     for _, K in INPUTS:
-        b += 2 * K if api == "fused" else 2 * K + K + 4
+        b += 2 * K if fused else 2 * K + K + 4
     for _, N, K, _ in LAYER_SHAPES:
-        b += N * K // 4 + 4 + 4 * N if api == "fused" else N * K // 4 + K + 8 + 4 * N
+        b += N * K // 4 + 4 + 4 * N if fused else N * K // 4 + K + 8 + 4 * N
     return b
 
 
@@ -187,14 +190,27 @@ class DecodeStep:
                            for n, _, _, s in LAYER_SHAPES if s == src]
                 self.bn.bitnet_linear_bf16(L["x"][src], targets, weights_static=True)
 
+    def build_chain(self):
+        phases = []
+        for L in self.layers:
+            for src, _ in INPUTS:
+                targets = [(L["W"][n][0], L["W"][n][1], L["y"][n])
+                           for n, _, _, s in LAYER_SHAPES if s == src]
+                phases.append((L["x"][src], targets))
+        self.chain = self.bn.bitnet_decode_chain_build(phases)
+
     def step(self):
-        if self.api == "fused":
+        if self.api == "chain":
+            self.bn.bitnet_decode_chain_run(self.chain)
+        elif self.api == "fused":
             self.fused()
         else:
             self.quantize_inputs()
             self.linears()
 
     def launches_per_step(self):
+        if self.api == "chain":
+            return 1
         if self.api == "fused":
             return len(INPUTS) * len(self.layers)
         n = 0
@@ -323,6 +339,8 @@ def run_gpu_arm(args, rank, world, barrier, max_over_ranks):
     torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
     bn.lib()
     step = DecodeStep(args.layers, api=args.api)
+    if args.api == "chain":
+        step.build_chain()
     graph = capture(torch, step.step)
 
     clocks = ClockSampler(torch.cuda.current_device())
@@ -364,7 +382,7 @@ def run_gpu_arm(args, rank, world, barrier, max_over_ranks):
     # Dominant kernel: the BitLinear launches alone, graph-replayed; average
     # launch duration = replay time / launches (consecutive launches overlap
     # under programmatic dependent launch, so this is the effective duration).
-    if args.api == "fused":
+    if args.api in ("fused", "chain"):
         lin_graph, lin_launches = graph, step.launches_per_step()
         lin_bytes = bytes_step
     else:
@@ -400,8 +418,9 @@ def run_gpu_arm(args, rank, world, barrier, max_over_ranks):
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps},
         "gpu_launches": step.launches_per_step() * args.steps,
         "roofline": {"bound": "hbm",
-                     "kernel": "k_gemv_decode (bitnet_linear_bf16)" if args.api == "fused"
-                     else "bitnet_linear GEMV",
+                     "kernel": {"chain": "k_gemv_decode chain (bitnet_decode_chain_run)",
+                                "fused": "k_gemv_decode (bitnet_linear_bf16)"}.get(
+                                    args.api, "bitnet_linear GEMV"),
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_source": peak_src,
                      "traffic": traffic, "launch_us": round(per_launch_s * 1e6, 3),

@@ -35,6 +35,9 @@ SIGNATURES = {
     "bitnet_linear_workspace": (_SZ, [_I64, _I64, _I64]),
     "bitnet_linear": (_INT, [_P, _P, _P, _P, _I64, _I64, _I64, _P, _P, _P, _SZ, _P]),
     "bitnet_linear_bf16": (_INT, [_P, _I64, _I64, _P, _INT, _P, _P, ctypes.c_uint, _P]),
+    "bitnet_decode_chain_bytes": (_SZ, [_INT]),
+    "bitnet_decode_chain_build": (_INT, [_P, _INT, _I64, _P, _SZ, _P]),
+    "bitnet_decode_chain_run": (_INT, [_P, _P]),
     "bitnet_ffn_workspace": (_SZ, [_I64, _I64, _I64]),
     "bitnet_ffn": (_INT, [_P, _P, _F, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _P, _P, _SZ,
                           _P]),
@@ -53,6 +56,16 @@ class BitnetError(RuntimeError):
 class LinearTarget(ctypes.Structure):
     """bitnet_linear_target: one weight matrix of a grouped decode call."""
     _fields_ = [("Wq", _P), ("w_scale", _P), ("N", _I64), ("y", _P), ("acc_out", _P)]
+
+
+class DecodePhase(ctypes.Structure):
+    """bitnet_decode_phase: one phase of a decode chain."""
+    _fields_ = [("x", _P), ("K", _I64), ("targets", _P), ("count", _INT)]
+
+
+class DecodeChain(ctypes.Structure):
+    """bitnet_decode_chain: filled by bitnet_decode_chain_build."""
+    _fields_ = [("table", _P), ("M", _I64), ("nphases", _INT), ("cfg", _INT * 6)]
 
 
 class FfnDebug(ctypes.Structure):
@@ -214,6 +227,49 @@ def bitnet_linear_bf16(x, targets, xq_out=None, x_scale_out=None, weights_static
         _ptr(xq_out, torch.int8, "xq_out"), _ptr(x_scale_out, torch.float32, "x_scale_out"),
         BITNET_WEIGHTS_STATIC if weights_static else 0, _stream(stream)))
     return [t[2] for t in targets]
+
+
+class DecodeChainHandle:
+    """A built decode chain: its device table (a torch tensor) and the host
+    description bitnet_decode_chain_run needs.  Keeps the target arrays and
+    tensors it was built from alive."""
+
+    def __init__(self, chain, table, keep):
+        self.chain = chain
+        self.table = table
+        self._keep = keep
+
+
+def bitnet_decode_chain_build(phases, device="cuda"):
+    """phases: list of (x bf16 [M, K], [(Wq, w_scale, y[, acc_out]), ...]).
+    Builds the chain table in device memory (synchronous)."""
+    M = phases[0][0].shape[0]
+    n = len(phases)
+    arr = (DecodePhase * n)()
+    keep = []
+    for i, (x, targets) in enumerate(phases):
+        tarr = (LinearTarget * len(targets))()
+        for j, t in enumerate(targets):
+            Wq, ws, y = t[0], t[1], t[2]
+            acc = t[3] if len(t) > 3 else None
+            tarr[j] = LinearTarget(_ptr(Wq, torch.uint8, "Wq"), _ptr(ws, torch.float32, "w_scale"),
+                                   Wq.shape[0], _ptr(y, torch.float32, "y"),
+                                   _ptr(acc, torch.int32, "acc_out"))
+        keep.append((tarr, x, targets))
+        arr[i] = DecodePhase(_ptr(x, torch.bfloat16, "x"), x.shape[1],
+                             ctypes.cast(tarr, ctypes.c_void_p), len(targets))
+    nbytes = int(lib().bitnet_decode_chain_bytes(n))
+    table = torch.zeros(nbytes + 256, dtype=torch.uint8, device=device)
+    base = (table.data_ptr() + 255) // 256 * 256
+    chain = DecodeChain()
+    _check("bitnet_decode_chain_build", lib().bitnet_decode_chain_build(
+        arr, n, M, ctypes.c_void_p(base), nbytes, ctypes.byref(chain)))
+    return DecodeChainHandle(chain, table, keep)
+
+
+def bitnet_decode_chain_run(handle, stream=None):
+    _check("bitnet_decode_chain_run", lib().bitnet_decode_chain_run(
+        ctypes.byref(handle.chain), _stream(stream)))
 
 
 # ------------------------------------------------------------------ FFN

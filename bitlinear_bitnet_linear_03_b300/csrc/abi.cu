@@ -4,6 +4,8 @@
 // beyond a per-device capability cache.
 #include <cuda_runtime.h>
 
+#include <vector>
+
 #include "../../include/bitnet_b300.h"
 #include "common.cuh"
 #include "gemm_tc.cuh"
@@ -209,6 +211,71 @@ bitnet_status bitnet_linear_bf16(const uint16_t* x, int64_t M, int64_t K,
   return cuda_status(bitnet::launch_decode(t, count, nullptr, nullptr, x, M, K, xq_out,
                                            x_scale_out, (flags & BITNET_WEIGHTS_STATIC) != 0,
                                            (cudaStream_t)stream));
+}
+
+size_t bitnet_decode_chain_bytes(int nphases) {
+  if (nphases < 1) return 0;
+  return bitnet::decode_chain_bytes(nphases);
+}
+
+bitnet_status bitnet_decode_chain_build(const bitnet_decode_phase* phases, int nphases, int64_t M,
+                                        void* table, size_t table_bytes,
+                                        bitnet_decode_chain* chain) {
+  if (!phases || !table || !chain) return BITNET_ERR_NULL;
+  if (nphases < 1 || M < 1 || M > BITNET_DECODE_MAX_M) return BITNET_ERR_SHAPE;
+  if ((reinterpret_cast<uintptr_t>(table) & 255u) != 0) return BITNET_ERR_ALIGN;
+  if (table_bytes < bitnet::decode_chain_bytes(nphases)) return BITNET_ERR_WORKSPACE;
+  std::vector<bitnet::DecodeTarget> tg;
+  tg.reserve((size_t)nphases * BITNET_MAX_TARGETS);
+  std::vector<bitnet::DecodePhaseDesc> ph((size_t)nphases);
+  for (int i = 0; i < nphases; ++i) {
+    const bitnet_decode_phase& p = phases[i];
+    if (!p.x || !p.targets) return BITNET_ERR_NULL;
+    if (p.count < 1 || p.count > BITNET_MAX_TARGETS || !valid_inner(p.K) ||
+        !bitnet::decode_supported(M, p.K))
+      return BITNET_ERR_SHAPE;
+    if (!aligned16(p.x)) return BITNET_ERR_ALIGN;
+    const size_t first = tg.size();
+    int64_t rows = 0;
+    for (int j = 0; j < p.count; ++j) {
+      const bitnet_linear_target& g = p.targets[j];
+      if (!g.Wq || !g.w_scale || !g.y) return BITNET_ERR_NULL;
+      if (g.N < 1) return BITNET_ERR_SHAPE;
+      if (!aligned16(g.Wq) || !aligned16(g.y) || (g.acc_out && !aligned16(g.acc_out)))
+        return BITNET_ERR_ALIGN;
+      rows += g.N;
+      tg.push_back({g.Wq, g.w_scale, g.N, g.y, g.acc_out});
+    }
+    if (rows > (1 << 30)) return BITNET_ERR_SHAPE;
+    ph[(size_t)i] = {p.x, p.K, tg.data() + first, p.count};
+  }
+  bitnet_status st = check_device();
+  if (st != BITNET_OK) return st;
+  bitnet::DecodeChainConfig cfg;
+  cudaError_t e = bitnet::build_decode_chain(ph.data(), nphases, M, table, &cfg);
+  if (e == cudaErrorNotSupported) return BITNET_ERR_SHAPE;
+  if (e != cudaSuccess) return cuda_status(e);
+  chain->table = table;
+  chain->M = M;
+  chain->nphases = nphases;
+  chain->cfg[0] = cfg.mt;
+  chain->cfg[1] = cfg.j;
+  chain->cfg[2] = cfg.stages;
+  chain->cfg[3] = cfg.slot_bytes;
+  chain->cfg[4] = cfg.xs_bytes;
+  chain->cfg[5] = cfg.smem;
+  return BITNET_OK;
+}
+
+bitnet_status bitnet_decode_chain_run(const bitnet_decode_chain* chain, void* stream) {
+  if (!chain || !chain->table) return BITNET_ERR_NULL;
+  if (chain->nphases < 1) return BITNET_ERR_SHAPE;
+  bitnet_status st = check_device();
+  if (st != BITNET_OK) return st;
+  bitnet::DecodeChainConfig cfg = {chain->cfg[0], chain->cfg[1], chain->cfg[2],
+                                   chain->cfg[3], chain->cfg[4], chain->cfg[5]};
+  return cuda_status(bitnet::launch_decode_chain(chain->table, chain->nphases, chain->M, cfg,
+                                                 (cudaStream_t)stream));
 }
 
 size_t bitnet_ffn_workspace(int64_t M, int64_t H, int64_t F) {

@@ -169,6 +169,23 @@ struct DecodeTarget {
   int32_t* acc_out;
 };
 bool decode_supported(int64_t M, int64_t K);
+
+// A chain of decode launches run by one persistent cooperative kernel, with a
+// grid-wide barrier between consecutive phases (gemv_decode.cu).
+struct DecodePhaseDesc {
+  const uint16_t* x;  // bf16 [M, K]
+  int64_t K;
+  const DecodeTarget* targets;
+  int count;
+};
+struct DecodeChainConfig {
+  int mt, j, stages, slot_bytes, xs_bytes, smem;
+};
+size_t decode_chain_bytes(int nphases);
+cudaError_t build_decode_chain(const DecodePhaseDesc* phases, int nphases, int64_t M, void* table,
+                               DecodeChainConfig* cfg);
+cudaError_t launch_decode_chain(const void* table, int nphases, int64_t M,
+                                const DecodeChainConfig& cfg, cudaStream_t s);
 // Reads and clears the error word of the decode kernel's bounded waits.
 cudaError_t read_and_clear_decode_error(int* code, cudaStream_t s);
 cudaError_t launch_decode(const DecodeTarget* targets, int count, const int8_t* xq,

@@ -72,7 +72,9 @@ struct Target {
   int N;
 };
 
-struct Args {
+// One decode BitLinear launch: up to kDecodeMaxTargets matrices sharing the
+// input x, and the work split computed on the host.
+struct Phase {
   Target t[kDecodeMaxTargets];
   int count;
   int rows_total;
@@ -82,13 +84,25 @@ struct Args {
   const float* x_scale;  // scales of xq
   int8_t* xq_out;        // optional copy of the quantised bf16 input
   float* xs_out;
-  int M, K;
+  int K;
   int wk;              // warps splitting K (1, 2, 4 or 8)
   int kpart;           // 64-weight chunks per K part
   int rows_per_stage;  // R: whole rows per ring slot
+  int stage_bytes;     // R * K / 4 (<= the ring slot)
+};
+
+// A launch runs one phase (ph0), or a chain of phases from a device table with
+// a grid-wide barrier between consecutive phases.
+struct Args {
+  Phase ph0;
+  const Phase* phases;          // chain table in device memory, or null
+  unsigned long long* barrier;  // chain: generation-counted barrier word
+  int nphases;
+  int M;
   int stages;
-  int stage_bytes;     // R * K / 4
-  int weights_early;   // weights may be read before the previous kernel ends
+  int slot_bytes;
+  int xs_bytes;                 // per-token bf16 staging (max K)
+  int weights_early;            // weights may be read before the previous kernel ends
 };
 
 // ---- mbarrier / bulk-copy primitives (PTX ISA: mbarrier, cp.async.bulk)
@@ -145,17 +159,55 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   return v;
 }
 
-// The CTA's stage sequence: for each matrix overlapping the CTA's rows, the
-// rows in pieces of at most rows_per_stage.  Calls f(p, first_row, nrows) in
-// order; stops when f returns false.
+// The CTA's stage sequence within one phase: for each matrix overlapping the
+// CTA's rows, the rows in pieces of at most rows_per_stage.  Calls
+// f(p, first_row, nrows) in order; returns false if f stopped it.
 template <typename F>
-__device__ __forceinline__ void for_each_stage(const Args& a, int r_begin, int r_end, F&& f) {
-  for (int p = 0; p < a.count; ++p) {
-    const int lo = max(r_begin, a.t[p].row0);
-    const int hi = min(r_end, a.t[p].row0 + a.t[p].N);
-    for (int r = lo; r < hi; r += a.rows_per_stage)
-      if (!f(p, r - a.t[p].row0, min(a.rows_per_stage, hi - r))) return;
+__device__ __forceinline__ bool for_each_stage(const Phase& ph, F&& f) {
+  const int r_begin = blockIdx.x * ph.rows_per_cta;
+  const int r_end = min(r_begin + ph.rows_per_cta, ph.rows_total);
+  for (int p = 0; p < ph.count; ++p) {
+    const int lo = max(r_begin, ph.t[p].row0);
+    const int hi = min(r_end, ph.t[p].row0 + ph.t[p].N);
+    for (int r = lo; r < hi; r += ph.rows_per_stage)
+      if (!f(p, r - ph.t[p].row0, min(ph.rows_per_stage, hi - r))) return false;
   }
+  return true;
+}
+
+// L2 prefetch hint for one phase's weight rows of this CTA.
+__device__ __forceinline__ void prefetch_phase(const Phase& ph) {
+  const int r_begin = blockIdx.x * ph.rows_per_cta;
+  const int r_end = min(r_begin + ph.rows_per_cta, ph.rows_total);
+  const int64_t row_bytes = ph.K >> 2;
+  for (int p = 0; p < ph.count; ++p) {
+    const int lo = max(r_begin, ph.t[p].row0);
+    const int hi = min(r_end, ph.t[p].row0 + ph.t[p].N);
+    if (lo >= hi) continue;
+    const uint8_t* base = ph.t[p].Wq + (int64_t)(lo - ph.t[p].row0) * row_bytes;
+    const int64_t bytes = (int64_t)(hi - lo) * row_bytes;
+    for (int64_t off = 0; off < bytes; off += kPrefetchMax)
+      prefetch_l2_bulk(base + off,
+                       (uint32_t)(bytes - off < kPrefetchMax ? bytes - off : kPrefetchMax));
+  }
+}
+
+// Grid barrier of a chain: a 64-bit counter that every CTA increments once
+// per barrier and that is never reset; barrier b of this launch completes
+// when it reaches base + (b + 1) * gridDim.x.  Bounded wait.
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ bool grid_wait(const unsigned long long* ctr, unsigned long long target) {
+  if (ld_acquire_u64(ctr) >= target) return true;
+  const long long t0 = clock64();
+  while (ld_acquire_u64(ctr) < target) {
+    __nanosleep(64);
+    if (clock64() - t0 > kWaitCycles) return false;
+  }
+  return true;
 }
 
 // Partial dot products of one row for this lane: J chunks, MT tokens, one
@@ -194,38 +246,29 @@ k_gemv_decode(const __grid_constant__ Args a) {
   __shared__ __align__(8) uint64_t full_bar[kMaxStages];
   __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
   __shared__ float s_max[kConsumerWarps][MT];
+  __shared__ int s_abort;
   // K-part merge per ring slot and stage row: the low 48 bits hold the sum of
   // the parts' biased partial dot products, bits 48.. count the parts added.
   __shared__ unsigned long long s_acc[kMaxStages][kConsumerWarps * kMaxRowsPerWarp / 2][MT];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int r_begin = blockIdx.x * a.rows_per_cta;
-  const int r_end = min(r_begin + a.rows_per_cta, a.rows_total);
-  const int64_t row_bytes = a.K >> 2;
   const uint32_t ring = smem_addr(smem);
+  const bool chain = a.phases != nullptr;
+  const Phase* phases = chain ? a.phases : &a.ph0;
 
-  if (a.wk > 1)
-    for (int q = threadIdx.x; q < kMaxStages * (kConsumerWarps * kMaxRowsPerWarp / 2) * MT;
-         q += kThreads)
-      (&s_acc[0][0][0])[q] = 0ull;
+  for (int q = threadIdx.x; q < kMaxStages * (kConsumerWarps * kMaxRowsPerWarp / 2) * MT;
+       q += kThreads)
+    (&s_acc[0][0][0])[q] = 0ull;
   if (threadIdx.x == 0) {
     for (int s = 0; s < a.stages; ++s) {
       mbar_init(smem_addr(&full_bar[s]), 1);
       mbar_init(smem_addr(&empty_bar[s]), kConsumerWarps);
     }
     mbar_fence_init();
-    // L2 prefetch hint for this CTA's weights (independent of the previous
-    // kernel; no data is read before griddep_wait).
-    for (int p = 0; p < a.count; ++p) {
-      const int lo = max(r_begin, a.t[p].row0);
-      const int hi = min(r_end, a.t[p].row0 + a.t[p].N);
-      if (lo >= hi) continue;
-      const uint8_t* base = a.t[p].Wq + (int64_t)(lo - a.t[p].row0) * row_bytes;
-      const int64_t bytes = (int64_t)(hi - lo) * row_bytes;
-      for (int64_t off = 0; off < bytes; off += kPrefetchMax)
-        prefetch_l2_bulk(base + off, (uint32_t)(bytes - off < kPrefetchMax ? bytes - off
-                                                                              : kPrefetchMax));
-    }
+    s_abort = 0;
+    // L2 prefetch hint for the first phase's weights (independent of the
+    // previous kernel; no data is read before the dependency wait).
+    prefetch_phase(phases[0]);
   }
   griddep_launch_dependents();
   __syncthreads();
@@ -236,29 +279,38 @@ k_gemv_decode(const __grid_constant__ Args a) {
     // Weights the caller declared static may stream in while the previous
     // kernel on the stream is still running (one ring's worth); otherwise
     // wait for it first.  Either way every bounded wait below starts after
-    // the dependency wait.
+    // the dependency wait.  In a chain the producer runs ahead across phase
+    // boundaries: weights never depend on earlier phases.
     bool dep_done = !a.weights_early;
     if (dep_done) griddep_wait();
     int i = 0;
-    for_each_stage(a, r_begin, r_end, [&](int p, int row, int nrows) {
-      const int slot = i % a.stages, use = i / a.stages;
-      if (use > 0) {
-        if (!dep_done) {
-          griddep_wait();
-          dep_done = true;
+    for (int ph_i = 0; ph_i < a.nphases; ++ph_i) {
+      const Phase& ph = phases[ph_i];
+      if (ph_i + 1 < a.nphases) prefetch_phase(phases[ph_i + 1]);
+      const int64_t row_bytes = ph.K >> 2;
+      const bool ok = for_each_stage(ph, [&](int p, int row, int nrows) {
+        const int slot = i % a.stages, use = i / a.stages;
+        if (use > 0) {
+          if (!dep_done) {
+            griddep_wait();
+            dep_done = true;
+          }
+          if (!mbar_wait(smem_addr(&empty_bar[slot]), (use - 1) & 1) ||
+              *(volatile int*)&s_abort) {
+            atomicOr(&g_decode_error, 1 << kErrEmptyWait);
+            return false;
+          }
         }
-        if (!mbar_wait(smem_addr(&empty_bar[slot]), (use - 1) & 1)) {
-          atomicOr(&g_decode_error, 1 << kErrEmptyWait);
-          return false;
-        }
-      }
-      const uint32_t bytes = (uint32_t)(nrows * row_bytes);
-      const uint32_t fb = smem_addr(&full_bar[slot]);
-      mbar_arrive_expect_tx(fb, bytes);
-      bulk_copy_g2s(ring + slot * a.stage_bytes, a.t[p].Wq + (int64_t)row * row_bytes, bytes, fb);
-      ++i;
-      return true;
-    });
+        const uint32_t bytes = (uint32_t)(nrows * row_bytes);
+        const uint32_t fb = smem_addr(&full_bar[slot]);
+        mbar_arrive_expect_tx(fb, bytes);
+        bulk_copy_g2s(ring + slot * a.slot_bytes, ph.t[p].Wq + (int64_t)row * row_bytes, bytes,
+                      fb);
+        ++i;
+        return true;
+      });
+      if (!ok) break;
+    }
     // Never leave the CTA with a copy in flight: wait for the last copy of
     // every slot to land.
     const int first = i > a.stages ? i - a.stages : 0;
@@ -271,284 +323,335 @@ k_gemv_decode(const __grid_constant__ Args a) {
   }
 
   // ------------------------------------------------------------ consumers
-  // Warp: K part kw (chunks k_lo .. k_hi-1) and row group wr of 8/wk.  Lane
-  // l holds the int8 activations of chunks k_lo + l + 32j (j < J) in
-  // registers and the sum of those codes, which it subtracts from every
-  // row's partial (sum q x = sum c x - sum x, taken part by part).
   griddep_wait();
-  const int K = a.K;
-  const int kw = warp % a.wk, wr = warp / a.wk, nwr = kConsumerWarps / a.wk;
-  const int nch = K >> 6;
-  const int k_lo = kw * a.kpart, k_hi = min(nch, k_lo + a.kpart);
-  // Matrix scales: lane p keeps w_scale of matrix p (read with a shuffle).
-  const float ws_lane = lane < a.count ? *a.t[lane].w_scale : 0.0f;
-  int valid_j = 0;
-#pragma unroll
-  for (int j = 0; j < J; ++j)
-    if (k_lo + lane + 32 * j < k_hi) valid_j = j + 1;
-  uint4 xr[MT][J][4];
-  int lsum[MT];
-  float xscale[MT];
-#pragma unroll
-  for (int m = 0; m < MT; ++m) {
-    lsum[m] = 0;
-    xscale[m] = 0.0f;
+  const int tid = threadIdx.x;  // 0 .. kConsumers-1
+  int8_t* xs = reinterpret_cast<int8_t*>(smem + a.stages * a.slot_bytes);
+  unsigned long long bar_base = 0;
+  if (chain && tid == 0) bar_base = ld_acquire_u64(a.barrier) / gridDim.x * gridDim.x;
+  int i = 0;  // ring stage counter, shared sequence with the producer
+
+  for (int ph_i = 0; ph_i < a.nphases; ++ph_i) {
+    const Phase& ph = phases[ph_i];
+    if (ph_i > 0) {
+      // Every CTA has finished phase ph_i - 1 before any reads phase ph_i's
+      // input.
+      if (tid == 0 && !grid_wait(a.barrier, bar_base + (unsigned long long)ph_i * gridDim.x)) {
+        atomicOr(&g_decode_error, 1 << kErrFullWait);
+        *(volatile int*)&s_abort = 1;
+      }
+      consumer_sync();
+      if (*(volatile int*)&s_abort) break;
+    }
+    const int K = ph.K;
+    const int64_t row_bytes = K >> 2;
+    // This warp: K part kw (chunks k_lo .. k_hi-1) and row group wr of 8/wk.
+    // Lane l holds the int8 activations of chunks k_lo + l + 32j (j < J) in
+    // registers and the sum of those codes, which it subtracts from every
+    // row's partial (sum q x = sum c x - sum x, taken part by part).
+    const int kw = warp % ph.wk, wr = warp / ph.wk, nwr = kConsumerWarps / ph.wk;
+    const int nch = K >> 6;
+    const int k_lo = kw * ph.kpart, k_hi = min(nch, k_lo + ph.kpart);
+    // Matrix scales: lane p keeps w_scale of matrix p (read with a shuffle).
+    const float ws_lane = lane < ph.count ? *ph.t[lane].w_scale : 0.0f;
+    int valid_j = 0;
 #pragma unroll
     for (int j = 0; j < J; ++j)
-#pragma unroll
-      for (int s = 0; s < 4; ++s) xr[m][j][s] = make_uint4(0, 0, 0, 0);
-  }
-  if (a.xb != nullptr) {
-    // bf16 input: the CTA quantises x once into shared memory (after the
-    // ring), each thread taking 16-element pieces; the row absmax is shared
-    // through s_max.  Then every lane picks up its chunks.
-    int8_t* xs = reinterpret_cast<int8_t*>(smem + a.stages * a.stage_bytes);
-    const int tid = threadIdx.x;
-    const int nitems = K >> 4;
-    const bool one_pass = nitems <= 2 * kConsumers;
-    uint4 held[MT][2][2];
+      if (k_lo + lane + 32 * j < k_hi) valid_j = j + 1;
+    uint4 xr[MT][J][4];
+    int lsum[MT];
+    float xscale[MT];
 #pragma unroll
     for (int m = 0; m < MT; ++m) {
-      float mx = 0.0f;
-      if (m < a.M) {
-        const uint4* xrow = reinterpret_cast<const uint4*>(a.xb + (int64_t)m * K);
-        if (one_pass) {
+      lsum[m] = 0;
+      xscale[m] = 0.0f;
 #pragma unroll
-          for (int j = 0; j < 2; ++j) {
-            const int f = tid + j * kConsumers;
-            held[m][j][0] = held[m][j][1] = make_uint4(0, 0, 0, 0);
-            if (f < nitems) {
-              held[m][j][0] = ld_nc_v4(xrow + 2 * f);
-              held[m][j][1] = ld_nc_v4(xrow + 2 * f + 1);
+      for (int j = 0; j < J; ++j)
+#pragma unroll
+        for (int s = 0; s < 4; ++s) xr[m][j][s] = make_uint4(0, 0, 0, 0);
+    }
+    if (ph.xb != nullptr) {
+      // bf16 input: the CTA quantises x once into shared memory (after the
+      // ring), each thread taking 16-element pieces; the row absmax is shared
+      // through s_max.  Then every lane picks up its chunks.
+      const int nitems = K >> 4;
+      const bool one_pass = nitems <= 2 * kConsumers;
+      uint4 held[MT][2][2];
+#pragma unroll
+      for (int m = 0; m < MT; ++m) {
+        float mx = 0.0f;
+        if (m < a.M) {
+          const uint4* xrow = reinterpret_cast<const uint4*>(ph.xb + (int64_t)m * K);
+          if (one_pass) {
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+              const int f = tid + j * kConsumers;
+              held[m][j][0] = held[m][j][1] = make_uint4(0, 0, 0, 0);
+              if (f < nitems) {
+                held[m][j][0] = ld_nc_v4(xrow + 2 * f);
+                held[m][j][1] = ld_nc_v4(xrow + 2 * f + 1);
+              }
+              const uint32_t e[8] = {held[m][j][0].x, held[m][j][0].y, held[m][j][0].z,
+                                     held[m][j][0].w, held[m][j][1].x, held[m][j][1].y,
+                                     held[m][j][1].z, held[m][j][1].w};
+#pragma unroll
+              for (int t = 0; t < 8; ++t) {
+                mx = fmaxf(mx, fabsf(bf16_bits_to_float(e[t] & 0xffffu)));
+                mx = fmaxf(mx, fabsf(bf16_bits_to_float(e[t] >> 16)));
+              }
             }
-            const uint32_t e[8] = {held[m][j][0].x, held[m][j][0].y, held[m][j][0].z,
-                                   held[m][j][0].w, held[m][j][1].x, held[m][j][1].y,
-                                   held[m][j][1].z, held[m][j][1].w};
+          } else {
+            for (int v = tid; v < (K >> 3); v += kConsumers) {
+              const uint4 q = ld_nc_v4(xrow + v);
+              const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-            for (int t = 0; t < 8; ++t) {
-              mx = fmaxf(mx, fabsf(bf16_bits_to_float(e[t] & 0xffffu)));
-              mx = fmaxf(mx, fabsf(bf16_bits_to_float(e[t] >> 16)));
+              for (int t = 0; t < 4; ++t) {
+                mx = fmaxf(mx, fabsf(bf16_bits_to_float(w4[t] & 0xffffu)));
+                mx = fmaxf(mx, fabsf(bf16_bits_to_float(w4[t] >> 16)));
+              }
             }
           }
-        } else {
-          for (int v = tid; v < (K >> 3); v += kConsumers) {
-            const uint4 q = ld_nc_v4(xrow + v);
-            const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
+        }
+        mx = warp_max_f32(mx);
+        if (lane == 0) s_max[warp][m] = mx;
+      }
+      consumer_sync();
+#pragma unroll
+      for (int m = 0; m < MT; ++m) {
+        float mx = s_max[0][m];
+#pragma unroll
+        for (int w = 1; w < kConsumerWarps; ++w) mx = fmaxf(mx, s_max[w][m]);
+        const ActScale sc = act_scale_from_absmax(mx);
+        xscale[m] = sc.scale;
+        if (m >= a.M) continue;
+        const uint4* xrow = reinterpret_cast<const uint4*>(ph.xb + (int64_t)m * K);
+        for (int j = 0;; ++j) {
+          const int f = tid + j * kConsumers;
+          if (f >= nitems || (one_pass && j >= 2)) break;
+          uint32_t e[8];
+          if (one_pass) {
+            const uint4 h0 = j == 0 ? held[m][0][0] : held[m][1][0];
+            const uint4 h1 = j == 0 ? held[m][0][1] : held[m][1][1];
+            e[0] = h0.x; e[1] = h0.y; e[2] = h0.z; e[3] = h0.w;
+            e[4] = h1.x; e[5] = h1.y; e[6] = h1.z; e[7] = h1.w;
+          } else {
+            const uint4 h0 = ld_nc_v4(xrow + 2 * f), h1 = ld_nc_v4(xrow + 2 * f + 1);
+            e[0] = h0.x; e[1] = h0.y; e[2] = h0.z; e[3] = h0.w;
+            e[4] = h1.x; e[5] = h1.y; e[6] = h1.z; e[7] = h1.w;
+          }
+          uint32_t wd[4];
+#pragma unroll
+          for (int ii = 0; ii < 4; ++ii) {
+            int q[4];
 #pragma unroll
             for (int t = 0; t < 4; ++t) {
-              mx = fmaxf(mx, fabsf(bf16_bits_to_float(w4[t] & 0xffffu)));
-              mx = fmaxf(mx, fabsf(bf16_bits_to_float(w4[t] >> 16)));
+              const int el = 4 * ii + t;
+              const uint32_t h = (el & 1) ? (e[el >> 1] >> 16) : (e[el >> 1] & 0xffffu);
+              q[t] = round_clip(__fmul_rn(bf16_bits_to_float(h), sc.inv), -128.f, 127.f);
+            }
+            wd[ii] = pack_i8x4(q[0], q[1], q[2], q[3]);
+          }
+          const uint4 packed = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+          *reinterpret_cast<uint4*>(xs + (int64_t)m * a.xs_bytes + 16 * f) = packed;
+          if (blockIdx.x == 0 && ph.xq_out != nullptr)
+            *reinterpret_cast<uint4*>(ph.xq_out + (int64_t)m * K + 16 * f) = packed;
+        }
+        if (blockIdx.x == 0 && tid == 0 && ph.xs_out != nullptr) ph.xs_out[m] = xscale[m];
+      }
+      consumer_sync();
+#pragma unroll
+      for (int m = 0; m < MT; ++m) {
+        if (m >= a.M) continue;
+#pragma unroll
+        for (int j = 0; j < J; ++j) {
+          if (j >= valid_j) continue;
+          const int c = k_lo + lane + 32 * j;
+#pragma unroll
+          for (int s = 0; s < 4; ++s) {
+            const uint4 v =
+                *reinterpret_cast<const uint4*>(xs + (int64_t)m * a.xs_bytes + 64 * c + 16 * s);
+            xr[m][j][s] = v;
+            lsum[m] = dp4a_ss(v.x, 0x01010101u, lsum[m]);
+            lsum[m] = dp4a_ss(v.y, 0x01010101u, lsum[m]);
+            lsum[m] = dp4a_ss(v.z, 0x01010101u, lsum[m]);
+            lsum[m] = dp4a_ss(v.w, 0x01010101u, lsum[m]);
+          }
+        }
+      }
+    } else {
+#pragma unroll
+      for (int m = 0; m < MT; ++m) {
+        if (m >= a.M) continue;
+        xscale[m] = ph.x_scale[m];
+#pragma unroll
+        for (int j = 0; j < J; ++j) {
+          if (j >= valid_j) continue;
+          const int c = k_lo + lane + 32 * j;
+          const uint4* src = reinterpret_cast<const uint4*>(ph.xq + (int64_t)m * K + 64 * c);
+#pragma unroll
+          for (int s = 0; s < 4; ++s) {
+            const uint4 v = ld_nc_v4(src + s);
+            xr[m][j][s] = v;
+            lsum[m] = dp4a_ss(v.x, 0x01010101u, lsum[m]);
+            lsum[m] = dp4a_ss(v.y, 0x01010101u, lsum[m]);
+            lsum[m] = dp4a_ss(v.z, 0x01010101u, lsum[m]);
+            lsum[m] = dp4a_ss(v.w, 0x01010101u, lsum[m]);
+          }
+        }
+      }
+    }
+
+    // On a time-out a warp sets s_abort and from then on every warp only
+    // walks the stage sequence (no waits, no work) so that all of them reach
+    // the same named barriers; the phase loop then ends uniformly.
+    for_each_stage(ph, [&](int p, int row0, int nrows) {
+      const int slot = i % a.stages;
+      ++i;
+      if (*(volatile int*)&s_abort) return true;
+      if (!mbar_wait(smem_addr(&full_bar[slot]), ((i - 1) / a.stages) & 1)) {
+        if (lane == 0) atomicOr(&g_decode_error, 1 << kErrFullWait);
+        *(volatile int*)&s_abort = 1;
+        return true;
+      }
+      const Target& T = ph.t[p];
+      const float wsc = __shfl_sync(0xffffffffu, ws_lane, p);
+      const uint32_t sbase = ring + slot * a.slot_bytes + 16 * (k_lo + lane);
+      // Rows wr + q*nwr (q < my_rows <= kMaxRowsPerWarp) of the stage, two at
+      // a time; their warp sums are uniform across the lanes.
+      const int my_rows = nrows > wr ? (nrows - wr + nwr - 1) / nwr : 0;
+      int vals[kMaxRowsPerWarp][MT];
+#pragma unroll
+      for (int q = 0; q < kMaxRowsPerWarp; q += 2) {
+        if (q < my_rows) {
+          const bool two = q + 1 < my_rows;
+          int v1[MT], v2[MT];
+          row_partial<MT, J>(sbase + (uint32_t)((wr + q * nwr) * row_bytes), valid_j, xr, v1);
+          if (two)
+            row_partial<MT, J>(sbase + (uint32_t)((wr + (q + 1) * nwr) * row_bytes), valid_j,
+                               xr, v2);
+#pragma unroll
+          for (int m = 0; m < MT; ++m) {
+            vals[q][m] = __reduce_add_sync(0xffffffffu, v1[m] - lsum[m]);
+            vals[q + 1][m] = two ? __reduce_add_sync(0xffffffffu, v2[m] - lsum[m]) : 0;
+          }
+        }
+      }
+      // Lane q*MT + m finishes row q for token m: all rows of the stage at once.
+      {
+        const int q = lane / MT, m = lane % MT;
+        int tot = 0;
+#pragma unroll
+        for (int qq = 0; qq < kMaxRowsPerWarp; ++qq)
+#pragma unroll
+          for (int mm = 0; mm < MT; ++mm)
+            if (qq * MT + mm == lane) tot = vals[qq][mm];
+        float xsc = xscale[0];
+#pragma unroll
+        for (int mm = 1; mm < MT; ++mm)
+          if (mm == m) xsc = xscale[mm];
+        if (q < my_rows && q < kMaxRowsPerWarp && m < a.M) {
+          const int row = wr + q * nwr;
+          bool last = true;
+          if (ph.wk > 1) {
+            // Merge the K parts: the last part to arrive writes the row.  Each
+            // part adds 1 << 48 (the count) plus its value biased by 2^31
+            // (non-negative, below 2^32), so at most 8 parts never carry out
+            // of the low 48 bits.
+            const unsigned long long add =
+                (1ull << 48) + (unsigned long long)((long long)tot + 2147483648ll);
+            const unsigned long long old = atomicAdd(&s_acc[slot][row][m], add);
+            last = (int)(old >> 48) == ph.wk - 1;
+            if (last) {
+              const long long sum = (long long)((old + add) & 0xffffffffffffull);
+              tot = (int)(sum - (long long)ph.wk * 2147483648ll);
+              s_acc[slot][row][m] = 0ull;
             }
           }
-        }
-      }
-      mx = warp_max_f32(mx);
-      if (lane == 0) s_max[warp][m] = mx;
-    }
-    consumer_sync();
-#pragma unroll
-    for (int m = 0; m < MT; ++m) {
-      float mx = s_max[0][m];
-#pragma unroll
-      for (int w = 1; w < kConsumerWarps; ++w) mx = fmaxf(mx, s_max[w][m]);
-      const ActScale sc = act_scale_from_absmax(mx);
-      xscale[m] = sc.scale;
-      if (m >= a.M) continue;
-      const uint4* xrow = reinterpret_cast<const uint4*>(a.xb + (int64_t)m * K);
-      for (int j = 0;; ++j) {
-        const int f = tid + j * kConsumers;
-        if (f >= nitems || (one_pass && j >= 2)) break;
-        uint32_t e[8];
-        if (one_pass) {
-          const uint4 h0 = j == 0 ? held[m][0][0] : held[m][1][0];
-          const uint4 h1 = j == 0 ? held[m][0][1] : held[m][1][1];
-          e[0] = h0.x; e[1] = h0.y; e[2] = h0.z; e[3] = h0.w;
-          e[4] = h1.x; e[5] = h1.y; e[6] = h1.z; e[7] = h1.w;
-        } else {
-          const uint4 h0 = ld_nc_v4(xrow + 2 * f), h1 = ld_nc_v4(xrow + 2 * f + 1);
-          e[0] = h0.x; e[1] = h0.y; e[2] = h0.z; e[3] = h0.w;
-          e[4] = h1.x; e[5] = h1.y; e[6] = h1.z; e[7] = h1.w;
-        }
-        uint32_t wd[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          int q[4];
-#pragma unroll
-          for (int t = 0; t < 4; ++t) {
-            const int el = 4 * i + t;
-            const uint32_t h = (el & 1) ? (e[el >> 1] >> 16) : (e[el >> 1] & 0xffffu);
-            q[t] = round_clip(__fmul_rn(bf16_bits_to_float(h), sc.inv), -128.f, 127.f);
-          }
-          wd[i] = pack_i8x4(q[0], q[1], q[2], q[3]);
-        }
-        const uint4 packed = make_uint4(wd[0], wd[1], wd[2], wd[3]);
-        *reinterpret_cast<uint4*>(xs + (int64_t)m * K + 16 * f) = packed;
-        if (blockIdx.x == 0 && a.xq_out != nullptr)
-          *reinterpret_cast<uint4*>(a.xq_out + (int64_t)m * K + 16 * f) = packed;
-      }
-      if (blockIdx.x == 0 && tid == 0 && a.xs_out != nullptr) a.xs_out[m] = xscale[m];
-    }
-    consumer_sync();
-#pragma unroll
-    for (int m = 0; m < MT; ++m) {
-      if (m >= a.M) continue;
-#pragma unroll
-      for (int j = 0; j < J; ++j) {
-        if (j >= valid_j) continue;
-        const int c = k_lo + lane + 32 * j;
-#pragma unroll
-        for (int s = 0; s < 4; ++s) {
-          const uint4 v = *reinterpret_cast<const uint4*>(xs + (int64_t)m * K + 64 * c + 16 * s);
-          xr[m][j][s] = v;
-          lsum[m] = dp4a_ss(v.x, 0x01010101u, lsum[m]);
-          lsum[m] = dp4a_ss(v.y, 0x01010101u, lsum[m]);
-          lsum[m] = dp4a_ss(v.z, 0x01010101u, lsum[m]);
-          lsum[m] = dp4a_ss(v.w, 0x01010101u, lsum[m]);
-        }
-      }
-    }
-  } else {
-#pragma unroll
-    for (int m = 0; m < MT; ++m) {
-      if (m >= a.M) continue;
-      xscale[m] = a.x_scale[m];
-#pragma unroll
-      for (int j = 0; j < J; ++j) {
-        if (j >= valid_j) continue;
-        const int c = k_lo + lane + 32 * j;
-        const uint4* src = reinterpret_cast<const uint4*>(a.xq + (int64_t)m * K + 64 * c);
-#pragma unroll
-        for (int s = 0; s < 4; ++s) {
-          const uint4 v = ld_nc_v4(src + s);
-          xr[m][j][s] = v;
-          lsum[m] = dp4a_ss(v.x, 0x01010101u, lsum[m]);
-          lsum[m] = dp4a_ss(v.y, 0x01010101u, lsum[m]);
-          lsum[m] = dp4a_ss(v.z, 0x01010101u, lsum[m]);
-          lsum[m] = dp4a_ss(v.w, 0x01010101u, lsum[m]);
-        }
-      }
-    }
-  }
-
-  int i = 0;
-  for_each_stage(a, r_begin, r_end, [&](int p, int row0, int nrows) {
-    const int slot = i % a.stages;
-    if (!mbar_wait(smem_addr(&full_bar[slot]), (i / a.stages) & 1)) {
-      if (lane == 0) atomicOr(&g_decode_error, 1 << kErrFullWait);
-      return false;
-    }
-    const Target& T = a.t[p];
-    const float wsc = __shfl_sync(0xffffffffu, ws_lane, p);
-    const uint32_t sbase = ring + slot * a.stage_bytes + 16 * (k_lo + lane);
-    // Rows wr + q*nwr (q < my_rows <= kMaxRowsPerWarp) of the stage, two at
-    // a time; their warp sums are uniform across the lanes.
-    const int my_rows = nrows > wr ? (nrows - wr + nwr - 1) / nwr : 0;
-    int vals[kMaxRowsPerWarp][MT];
-#pragma unroll
-    for (int q = 0; q < kMaxRowsPerWarp; q += 2) {
-      if (q < my_rows) {
-        const bool two = q + 1 < my_rows;
-        int v1[MT], v2[MT];
-        row_partial<MT, J>(sbase + (uint32_t)((wr + q * nwr) * row_bytes), valid_j, xr, v1);
-        if (two)
-          row_partial<MT, J>(sbase + (uint32_t)((wr + (q + 1) * nwr) * row_bytes), valid_j, xr,
-                             v2);
-#pragma unroll
-        for (int m = 0; m < MT; ++m) {
-          vals[q][m] = __reduce_add_sync(0xffffffffu, v1[m] - lsum[m]);
-          vals[q + 1][m] = two ? __reduce_add_sync(0xffffffffu, v2[m] - lsum[m]) : 0;
-        }
-      }
-    }
-    // Lane q*MT + m finishes row q for token m: all rows of the stage at once.
-    {
-      const int q = lane / MT, m = lane % MT;
-      int tot = 0;
-#pragma unroll
-      for (int qq = 0; qq < kMaxRowsPerWarp; ++qq)
-#pragma unroll
-        for (int mm = 0; mm < MT; ++mm)
-          if (qq * MT + mm == lane) tot = vals[qq][mm];
-      float xsc = xscale[0];
-#pragma unroll
-      for (int mm = 1; mm < MT; ++mm)
-        if (mm == m) xsc = xscale[mm];
-      if (q < my_rows && q < kMaxRowsPerWarp && m < a.M) {
-        const int row = wr + q * nwr;
-        bool last = true;
-        if (a.wk > 1) {
-          // Merge the K parts: the last part to arrive writes the row.  Each
-          // part adds 1 << 48 (the count) plus its value biased by 2^31
-          // (non-negative, below 2^32), so at most 8 parts never carry out
-          // of the low 48 bits.
-          const unsigned long long add =
-              (1ull << 48) + (unsigned long long)((long long)tot + 2147483648ll);
-          const unsigned long long old = atomicAdd(&s_acc[slot][row][m], add);
-          last = (int)(old >> 48) == a.wk - 1;
           if (last) {
-            const long long sum = (long long)((old + add) & 0xffffffffffffull);
-            tot = (int)(sum - (long long)a.wk * 2147483648ll);
-            s_acc[slot][row][m] = 0ull;
+            const int64_t o = (int64_t)m * T.N + row0 + row;
+            T.y[o] = __fmul_rn(__int2float_rn(tot), __fmul_rn(xsc, wsc));
+            if (T.acc_out) T.acc_out[o] = tot;
           }
         }
-        if (last) {
-          const int64_t o = (int64_t)m * T.N + row0 + row;
-          T.y[o] = __fmul_rn(__int2float_rn(tot), __fmul_rn(xsc, wsc));
-          if (T.acc_out) T.acc_out[o] = tot;
-        }
       }
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(smem_addr(&empty_bar[slot]));
-    ++i;
-    return true;
-  });
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&empty_bar[slot]));
+      return true;
+    });
+    // This CTA's outputs of the phase are written: make them visible to the
+    // other CTAs, then (in a chain) arrive at the grid barrier.
+    __threadfence();
+    consumer_sync();
+    if (*(volatile int*)&s_abort) break;
+    if (chain && ph_i + 1 < a.nphases && tid == 0) atomicAdd(a.barrier, 1ull);
+  }
 }
 
-struct Plan {
-  int mt, j, wk, kpart, rows_per_stage, stages, stage_bytes;
-  size_t smem;
+// Work split of one phase for MT tokens per pass and J chunks per lane.
+struct PhasePlan {
+  int wk, kpart, rows_per_stage, stage_bytes;
 };
 
-// Tokens per pass MT, chunks per lane J (activations in 16*MT*J registers),
-// the K split wk and the ring geometry.
-bool make_plan(int64_t M, int64_t K, Plan* pl) {
-  if (M < 1 || M > kDecodeMaxM || K < 64 || K % 64 != 0 || K > 65536) return false;
-  const int mt = M <= 1 ? 1 : M <= 2 ? 2 : 4;
+int tokens_per_pass(int64_t M) { return M <= 1 ? 1 : M <= 2 ? 2 : 4; }
+
+// Smallest J (chunks per lane) for which 8 warps can split K.
+int min_j(int mt, int64_t K) {
   const int nch = (int)(K / 64);
   const int jopts[2] = {mt == 4 ? 1 : 2, mt == 1 ? 4 : 0};
-  int j = 0, wk = 0;
-  for (int o = 0; o < 2 && !wk; ++o) {
-    if (jopts[o] == 0) continue;
-    for (int w = 1; w <= 8; w *= 2)
-      if ((nch + w - 1) / w <= 32 * jopts[o]) {
-        j = jopts[o];
-        wk = w;
-        break;
-      }
-  }
+  for (int o = 0; o < 2; ++o)
+    if (jopts[o] && (nch + 7) / 8 <= 32 * jopts[o]) return jopts[o];
+  return 0;
+}
+
+bool plan_phase(int64_t K, int j, PhasePlan* pp) {
+  if (K < 64 || K % 64 != 0 || K > 65536) return false;
+  const int nch = (int)(K / 64);
+  int wk = 0;
+  for (int w = 1; w <= 8; w *= 2)
+    if ((nch + w - 1) / w <= 32 * j) {
+      wk = w;
+      break;
+    }
   if (!wk) return false;
   const int nwr = kConsumerWarps / wk;
   const int64_t row_bytes = K / 4;
   int64_t R = kStageTarget / row_bytes / nwr * nwr;
   if (R < nwr) R = nwr;
   if (R > (int64_t)kMaxRowsPerWarp * nwr) R = (int64_t)kMaxRowsPerWarp * nwr;
-  pl->mt = mt;
-  pl->j = j;
-  pl->wk = wk;
-  pl->kpart = (nch + wk - 1) / wk;
-  pl->rows_per_stage = (int)R;
-  pl->stage_bytes = (int)(R * row_bytes);
-  int S = kRingBudget / pl->stage_bytes;
+  pp->wk = wk;
+  pp->kpart = (nch + wk - 1) / wk;
+  pp->rows_per_stage = (int)R;
+  pp->stage_bytes = (int)(R * row_bytes);
+  return true;
+}
+
+// Ring depth and shared memory for a slot size and a staging width.
+int ring_stages(int slot_bytes) {
+  int S = kRingBudget / slot_bytes;
   if (S < 2) S = 2;
   if (S > kMaxStages) S = kMaxStages;
-  pl->stages = S;
-  pl->smem = (size_t)S * pl->stage_bytes + (size_t)mt * (size_t)K;  // ring + bf16 staging
+  return S;
+}
+
+struct Plan {
+  int mt, j;
+  PhasePlan pp;
+  int stages;
+  size_t smem;
+};
+
+bool make_plan(int64_t M, int64_t K, Plan* pl) {
+  if (M < 1 || M > kDecodeMaxM) return false;
+  pl->mt = tokens_per_pass(M);
+  pl->j = min_j(pl->mt, K);
+  if (!pl->j || !plan_phase(K, pl->j, &pl->pp)) return false;
+  pl->stages = ring_stages(pl->pp.stage_bytes);
+  pl->smem = (size_t)pl->stages * pl->pp.stage_bytes + (size_t)pl->mt * (size_t)K;
   return pl->smem <= (size_t)kMaxSmem;
 }
 
 template <int MT, int J>
-cudaError_t launch_t(const Args& a, int ctas, size_t smem, cudaStream_t s) {
+cudaError_t configure(int smem_needed) {
+  (void)smem_needed;
   static bool configured[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -559,8 +662,78 @@ cudaError_t launch_t(const Args& a, int ctas, size_t smem, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
+  return cudaSuccess;
+}
+
+template <int MT, int J>
+cudaError_t launch_t(const Args& a, int ctas, size_t smem, cudaStream_t s) {
+  cudaError_t e = configure<MT, J>((int)smem);
+  if (e != cudaSuccess) return e;
   return launch_pdl(k_gemv_decode<MT, J>, dim3(ctas), dim3(kThreads), smem, s, a);
 }
+
+// Chains run as a cooperative launch (all CTAs resident: the grid barrier
+// needs it).
+template <int MT, int J>
+cudaError_t launch_coop(const Args& a, int ctas, size_t smem, cudaStream_t s) {
+  cudaError_t e = configure<MT, J>((int)smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(ctas);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k_gemv_decode<MT, J>, a);
+}
+
+cudaError_t dispatch(int mt, int j, bool coop, const Args& a, int ctas, size_t smem,
+                     cudaStream_t s) {
+  if (mt == 1 && j == 2) return coop ? launch_coop<1, 2>(a, ctas, smem, s) : launch_t<1, 2>(a, ctas, smem, s);
+  if (mt == 1 && j == 4) return coop ? launch_coop<1, 4>(a, ctas, smem, s) : launch_t<1, 4>(a, ctas, smem, s);
+  if (mt == 2 && j == 2) return coop ? launch_coop<2, 2>(a, ctas, smem, s) : launch_t<2, 2>(a, ctas, smem, s);
+  if (mt == 4 && j == 1) return coop ? launch_coop<4, 1>(a, ctas, smem, s) : launch_t<4, 1>(a, ctas, smem, s);
+  return cudaErrorNotSupported;
+}
+
+// Fills a Phase from the host description; rows split over `ctas` CTAs.
+bool fill_phase(const DecodeTarget* targets, int count, const int8_t* xq, const float* x_scale,
+                const uint16_t* x_bf16, int64_t K, const PhasePlan& pp, int ctas,
+                int8_t* xq_out, float* x_scale_out, Phase* ph) {
+  *ph = Phase{};
+  int64_t rows = 0;
+  for (int p = 0; p < count; ++p) {
+    ph->t[p].Wq = targets[p].Wq;
+    ph->t[p].w_scale = targets[p].w_scale;
+    ph->t[p].y = targets[p].y;
+    ph->t[p].acc_out = targets[p].acc_out;
+    ph->t[p].row0 = (int)rows;
+    ph->t[p].N = (int)targets[p].N;
+    rows += targets[p].N;
+  }
+  if (rows < 1 || rows > (1 << 30)) return false;
+  ph->count = count;
+  ph->rows_total = (int)rows;
+  ph->rows_per_cta = (int)((rows + ctas - 1) / ctas);
+  ph->xb = x_bf16;
+  ph->xq = xq;
+  ph->x_scale = x_scale;
+  ph->xq_out = xq_out;
+  ph->xs_out = x_scale_out;
+  ph->K = (int)K;
+  ph->wk = pp.wk;
+  ph->kpart = pp.kpart;
+  ph->rows_per_stage = pp.rows_per_stage;
+  ph->stage_bytes = pp.stage_bytes;
+  return true;
+}
+
+constexpr int kChainCtas = 148;
+constexpr size_t kChainHeader = 256;  // the barrier word, padded
 
 }  // namespace
 
@@ -576,44 +749,93 @@ cudaError_t launch_decode(const DecodeTarget* targets, int count, const int8_t* 
   Plan pl;
   if (count < 1 || count > kDecodeMaxTargets || !make_plan(M, K, &pl))
     return cudaErrorNotSupported;
-  Args a = {};
   int64_t rows = 0;
-  for (int p = 0; p < count; ++p) {
-    a.t[p].Wq = targets[p].Wq;
-    a.t[p].w_scale = targets[p].w_scale;
-    a.t[p].y = targets[p].y;
-    a.t[p].acc_out = targets[p].acc_out;
-    a.t[p].row0 = (int)rows;
-    a.t[p].N = (int)targets[p].N;
-    rows += targets[p].N;
-  }
-  if (rows > (1 << 30)) return cudaErrorNotSupported;
-  a.count = count;
-  a.rows_total = (int)rows;
-  a.xb = x_bf16;
-  a.xq = xq;
-  a.x_scale = x_scale;
-  a.xq_out = xq_out;
-  a.xs_out = x_scale_out;
-  a.M = (int)M;
-  a.K = (int)K;
-  a.wk = pl.wk;
-  a.kpart = pl.kpart;
-  a.rows_per_stage = pl.rows_per_stage;
-  a.stages = pl.stages;
-  a.stage_bytes = pl.stage_bytes;
-  a.weights_early = weights_static ? 1 : 0;
+  for (int p = 0; p < count; ++p) rows += targets[p].N;
   // One CTA per SM leaves room for the next decode kernel to start alongside
   // (programmatic dependent launch); large matrices take two per SM for more
   // warps and copies in flight.
   const int64_t max_ctas = rows * (K / 4) >= ((int64_t)16 << 20) ? 296 : 148;
   int64_t ctas = rows < max_ctas ? rows : max_ctas;
-  a.rows_per_cta = (int)((rows + ctas - 1) / ctas);
-  ctas = (rows + a.rows_per_cta - 1) / a.rows_per_cta;
-  const int c = (int)ctas;
-  if (pl.mt == 1) return pl.j == 2 ? launch_t<1, 2>(a, c, pl.smem, s) : launch_t<1, 4>(a, c, pl.smem, s);
-  if (pl.mt == 2) return launch_t<2, 2>(a, c, pl.smem, s);
-  return launch_t<4, 1>(a, c, pl.smem, s);
+  const int64_t rpc = (rows + ctas - 1) / ctas;
+  ctas = (rows + rpc - 1) / rpc;
+  Args a = {};
+  if (!fill_phase(targets, count, xq, x_scale, x_bf16, K, pl.pp, (int)ctas, xq_out, x_scale_out,
+                  &a.ph0))
+    return cudaErrorNotSupported;
+  a.phases = nullptr;
+  a.barrier = nullptr;
+  a.nphases = 1;
+  a.M = (int)M;
+  a.stages = pl.stages;
+  a.slot_bytes = pl.pp.stage_bytes;
+  a.xs_bytes = (int)K;
+  a.weights_early = weights_static ? 1 : 0;
+  return dispatch(pl.mt, pl.j, false, a, (int)ctas, pl.smem, s);
+}
+
+size_t decode_chain_bytes(int nphases) {
+  return kChainHeader + (size_t)(nphases > 0 ? nphases : 0) * sizeof(Phase);
+}
+
+cudaError_t build_decode_chain(const DecodePhaseDesc* phases, int nphases, int64_t M,
+                               void* table, DecodeChainConfig* cfg) {
+  if (nphases < 1 || M < 1 || M > kDecodeMaxM) return cudaErrorNotSupported;
+  const int mt = tokens_per_pass(M);
+  int j = 0;
+  int64_t max_k = 0;
+  for (int i = 0; i < nphases; ++i) {
+    const int jj = min_j(mt, phases[i].K);
+    if (!jj || phases[i].count < 1 || phases[i].count > kDecodeMaxTargets)
+      return cudaErrorNotSupported;
+    if (jj > j) j = jj;
+    if (phases[i].K > max_k) max_k = phases[i].K;
+  }
+  Phase* host = new Phase[nphases];
+  int slot = 0;
+  for (int i = 0; i < nphases; ++i) {
+    PhasePlan pp;
+    if (!plan_phase(phases[i].K, j, &pp) ||
+        !fill_phase(phases[i].targets, phases[i].count, nullptr, nullptr, phases[i].x,
+                    phases[i].K, pp, kChainCtas, nullptr, nullptr, &host[i])) {
+      delete[] host;
+      return cudaErrorNotSupported;
+    }
+    if (pp.stage_bytes > slot) slot = pp.stage_bytes;
+  }
+  const int stages = ring_stages(slot);
+  const size_t smem = (size_t)stages * slot + (size_t)mt * (size_t)max_k;
+  if (smem > (size_t)kMaxSmem) {
+    delete[] host;
+    return cudaErrorNotSupported;
+  }
+  uint8_t* t = static_cast<uint8_t*>(table);
+  cudaError_t e = cudaMemset(t, 0, kChainHeader);
+  if (e == cudaSuccess)
+    e = cudaMemcpy(t + kChainHeader, host, (size_t)nphases * sizeof(Phase), cudaMemcpyHostToDevice);
+  delete[] host;
+  if (e != cudaSuccess) return e;
+  cfg->mt = mt;
+  cfg->j = j;
+  cfg->stages = stages;
+  cfg->slot_bytes = slot;
+  cfg->xs_bytes = (int)max_k;
+  cfg->smem = (int)smem;
+  return cudaSuccess;
+}
+
+cudaError_t launch_decode_chain(const void* table, int nphases, int64_t M,
+                                const DecodeChainConfig& cfg, cudaStream_t s) {
+  Args a = {};
+  uint8_t* t = static_cast<uint8_t*>(const_cast<void*>(table));
+  a.phases = reinterpret_cast<const Phase*>(t + kChainHeader);
+  a.barrier = reinterpret_cast<unsigned long long*>(t);
+  a.nphases = nphases;
+  a.M = (int)M;
+  a.stages = cfg.stages;
+  a.slot_bytes = cfg.slot_bytes;
+  a.xs_bytes = cfg.xs_bytes;
+  a.weights_early = 0;
+  return dispatch(cfg.mt, cfg.j, true, a, kChainCtas, (size_t)cfg.smem, s);
 }
 
 cudaError_t read_and_clear_decode_error(int* code, cudaStream_t s) {

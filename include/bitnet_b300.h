@@ -179,6 +179,46 @@ bitnet_status bitnet_linear_bf16(const uint16_t* x, int64_t M, int64_t K,
                                  void* stream);
 
 /* ------------------------------------------------------------------------
+ * A decode chain: a sequence of bitnet_linear_bf16 phases (e.g. the QKV, O,
+ * up+gate and down projections of every layer of a decoder step) run by one
+ * persistent kernel.  Phase p computes, for each of its targets,
+ *   y_i = BitLinear(Wq_i, w_scale_i; quant(x_p))     (rules of bitnet_linear_bf16)
+ * and no CTA reads the input of phase p+1 before every CTA has written all
+ * of its outputs of phase p (a grid-wide barrier): the phases are ordered
+ * exactly as separate dependent launches on one stream would be.  The weights are
+ * streamed ahead across phase boundaries: no work in flight on `stream` may
+ * write any Wq or w_scale of the chain (BITNET_WEIGHTS_STATIC semantics).
+ * phases[p]: x [M, K_p] bf16, 1 <= M <= BITNET_DECODE_MAX_M, targets as in
+ * bitnet_linear_bf16 (1 .. BITNET_MAX_TARGETS, the same K limits).
+ * table: device memory of bitnet_decode_chain_bytes(nphases) bytes, 256-byte
+ * aligned, owned by the caller; _build fills it (synchronously: call it
+ * outside stream capture, it returns after the copy) and zeroes its barrier
+ * word.  `chain` (host) receives what _run needs.  Runs of one table must not
+ * overlap on the GPU.  The kernel needs all of its 148 CTAs resident at once
+ * (cooperative launch); _run returns BITNET_ERR_CUDA if the launch is refused.
+ * After a run that reported a device error (bitnet_device_error), build the
+ * chain again before the next run. */
+typedef struct bitnet_decode_phase {
+  const uint16_t* x;
+  int64_t K;
+  const bitnet_linear_target* targets;
+  int count;
+} bitnet_decode_phase;
+
+typedef struct bitnet_decode_chain {
+  void* table;
+  int64_t M;
+  int nphases;
+  int cfg[6]; /* launch configuration, filled by bitnet_decode_chain_build */
+} bitnet_decode_chain;
+
+size_t bitnet_decode_chain_bytes(int nphases);
+bitnet_status bitnet_decode_chain_build(const bitnet_decode_phase* phases, int nphases,
+                                        int64_t M, void* table, size_t table_bytes,
+                                        bitnet_decode_chain* chain);
+bitnet_status bitnet_decode_chain_run(const bitnet_decode_chain* chain, void* stream);
+
+/* ------------------------------------------------------------------------
  * Fused BitNet feed-forward block ([P1] subln, ReLU^2, no bias):
  *   r   = (float)(1 / sqrt(ss / H + eps)), ss = sum x^2 (binary64, in the
  *         order: 32 strided partial sums over k = l (mod 32), increasing k,

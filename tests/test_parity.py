@@ -279,3 +279,59 @@ def test_linear_bf16_rejects_unsupported():
     with pytest.raises(bn.BitnetError) as e:
         bn.bitnet_linear_bf16(x, t)
     assert e.value.status == 2
+
+
+# ---------------------------------------------------------------- decode chain
+def test_decode_chain_matches_separate_calls():
+    """A chain of phases with different K and target counts, run twice; every
+    output equals the oracle's BitLinear of the phase's own input."""
+    M = 1
+    spec = [(2560, [2560, 640, 640]), (2560, [2560]), (2560, [6912, 6912]), (6912, [2560]),
+            (192, [5, 70]), (28672, [300])]
+    phases, refs = [], []
+    for i, (K, Ns) in enumerate(spec):
+        x = synth.tokens_bf16(M, K, seed=900 + i, outlier_frac=0.01)
+        qx, sx = oracle.quantize_act_bf16(x)
+        targets, want = [], []
+        for j, N in enumerate(Ns):
+            Wq, ws, _ = oracle.quantize_weights(synth.weights_f32(N, K, seed=1000 + 10 * i + j))
+            y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+            acc = torch.empty((M, N), dtype=torch.int32, device="cuda")
+            targets.append((dev(Wq), dev(np.array([ws], np.float32)), y, acc))
+            want.append(oracle.linear(Wq, ws, qx, sx, K))
+        phases.append((dev_bf16(x), targets))
+        refs.append(want)
+    chain = bn.bitnet_decode_chain_build(phases)
+    for run in range(2):
+        for t in (t for _, tg in phases for t in tg):
+            t[2].fill_(float("nan"))
+        bn.bitnet_decode_chain_run(chain)
+        torch.cuda.synchronize()
+        assert bn.bitnet_device_error() == 0
+        for i, ((_, tg), want) in enumerate(zip(phases, refs)):
+            for j, (t, (y_o, acc_o)) in enumerate(zip(tg, want)):
+                assert_bits_equal(host(t[3]), acc_o, f"run {run} phase {i} target {j} acc")
+                assert_bits_equal(host(t[2]), y_o, f"run {run} phase {i} target {j} y")
+
+
+@pytest.mark.parametrize("M", [2, 3])
+def test_decode_chain_multi_token(M):
+    spec = [(2560, [2560, 640]), (6912, [2560]), (2560, [6912])]
+    phases, refs = [], []
+    for i, (K, Ns) in enumerate(spec):
+        x = synth.tokens_bf16(M, K, seed=950 + i)
+        qx, sx = oracle.quantize_act_bf16(x)
+        targets, want = [], []
+        for j, N in enumerate(Ns):
+            Wq, ws, _ = oracle.quantize_weights(synth.weights_f32(N, K, seed=1100 + 10 * i + j))
+            targets.append((dev(Wq), dev(np.array([ws], np.float32)),
+                            torch.empty((M, N), dtype=torch.float32, device="cuda")))
+            want.append(oracle.linear(Wq, ws, qx, sx, K)[0])
+        phases.append((dev_bf16(x), targets))
+        refs.append(want)
+    chain = bn.bitnet_decode_chain_build(phases)
+    bn.bitnet_decode_chain_run(chain)
+    torch.cuda.synchronize()
+    for (_, tg), want in zip(phases, refs):
+        for t, y_o in zip(tg, want):
+            assert_bits_equal(host(t[2]), y_o, "chain y")
