@@ -577,12 +577,16 @@ k_gemv_decode(const __grid_constant__ Args a) {
       if (lane == 0) mbar_arrive(smem_addr(&empty_bar[slot]));
       return true;
     });
-    // This CTA's outputs of the phase are written: make them visible to the
-    // other CTAs, then (in a chain) arrive at the grid barrier.
-    __threadfence();
+    // This CTA's outputs of the phase are written.  In a chain: after the
+    // CTA barrier one thread makes them visible GPU-wide (a fence is
+    // cumulative over what the CTA barrier ordered) and arrives at the grid
+    // barrier.
     consumer_sync();
     if (*(volatile int*)&s_abort) break;
-    if (chain && ph_i + 1 < a.nphases && tid == 0) atomicAdd(a.barrier, 1ull);
+    if (chain && ph_i + 1 < a.nphases && tid == 0) {
+      __threadfence();
+      atomicAdd(a.barrier, 1ull);
+    }
   }
 }
 
