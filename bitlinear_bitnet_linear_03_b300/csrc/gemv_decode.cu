@@ -210,6 +210,14 @@ __device__ __forceinline__ bool grid_wait(const unsigned long long* ctr, unsigne
   return true;
 }
 
+// Copies a phase descriptor with the 32 lanes of a warp.
+__device__ __forceinline__ void copy_phase(const Phase& src, Phase* dst, int lane) {
+  static_assert(sizeof(Phase) % 8 == 0, "phase descriptor is copied in 8-byte words");
+  const unsigned long long* s = reinterpret_cast<const unsigned long long*>(&src);
+  unsigned long long* d = reinterpret_cast<unsigned long long*>(dst);
+  for (int i = lane; i < (int)(sizeof(Phase) / 8); i += 32) d[i] = s[i];
+}
+
 // Partial dot products of one row for this lane: J chunks, MT tokens, one
 // accumulator per field (scaled by 4^s), folded to one int per token.
 template <int MT, int J>
@@ -247,6 +255,10 @@ k_gemv_decode(const __grid_constant__ Args a) {
   __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
   __shared__ float s_max[kConsumerWarps][MT];
   __shared__ int s_abort;
+  // The consumers' copy of the current phase descriptor (read in the hot
+  // loop; shared memory instead of a pointer into the parameter block or the
+  // chain table).
+  __shared__ __align__(16) Phase s_ph;
   // K-part merge per ring slot and stage row: the low 48 bits hold the sum of
   // the parts' biased partial dot products, bits 48.. count the parts added.
   __shared__ unsigned long long s_acc[kMaxStages][kConsumerWarps * kMaxRowsPerWarp / 2][MT];
@@ -259,6 +271,7 @@ k_gemv_decode(const __grid_constant__ Args a) {
   for (int q = threadIdx.x; q < kMaxStages * (kConsumerWarps * kMaxRowsPerWarp / 2) * MT;
        q += kThreads)
     (&s_acc[0][0][0])[q] = 0ull;
+  if (threadIdx.x < 32) copy_phase(phases[0], &s_ph, threadIdx.x);
   if (threadIdx.x == 0) {
     for (int s = 0; s < a.stages; ++s) {
       mbar_init(smem_addr(&full_bar[s]), 1);
@@ -331,10 +344,12 @@ k_gemv_decode(const __grid_constant__ Args a) {
   int i = 0;  // ring stage counter, shared sequence with the producer
 
   for (int ph_i = 0; ph_i < a.nphases; ++ph_i) {
-    const Phase& ph = phases[ph_i];
+    const Phase& ph = s_ph;
     if (ph_i > 0) {
       // Every CTA has finished phase ph_i - 1 before any reads phase ph_i's
-      // input.
+      // input.  Meanwhile warp 1 copies the (static) descriptor of phase
+      // ph_i.
+      if (warp == 1) copy_phase(phases[ph_i], &s_ph, lane);
       if (tid == 0 && !grid_wait(a.barrier, bar_base + (unsigned long long)ph_i * gridDim.x)) {
         atomicOr(&g_decode_error, 1 << kErrFullWait);
         *(volatile int*)&s_abort = 1;
