@@ -288,48 +288,126 @@ def profiled_traffic(kernel_file, profile_file):
         return None
 
 
+def _time_calls(torch, fn, reps, warm=3):
+    for i in range(warm):
+        fn(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(reps):
+        fn(i)
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / 1e3 / reps
+
+
+def _weight_sets(torch, bn, synth, N, K, count, seed):
+    sets = []
+    for r in range(count):
+        W = synth.weights_f32(N, K, seed=seed + r, device="cuda")
+        sets.append(bn.bitnet_quantize_weights(W))
+        del W
+    return sets
+
+
 def secondary_measurements(torch, bn, peaks):
-    """Prefill BitLinear (M = 4096 tokens, the pages' maximum context) on the
-    2B-class FFN shapes, timed with CUDA events after warm-up over 4 rotating
-    weight sets; tensor-core roofline against the measured bf16 dense peak
-    (sm_103a has no integer tensor-core MMA, so the exact integer products
-    run as bf16 MMAs with binary32 accumulation)."""
+    """The other workloads, each timed with CUDA events after warm-up, weights
+    rotated over enough distinct sets that every timed call streams from HBM
+    (more than the 126 MB L2 between reuses), inputs resident:
+      * single GEMV 2560x2560, batch 1 (80 weight sets);
+      * 100B-class shapes 8192->28672 and 28672->8192 at M = 1, 4, 16, 64;
+      * prefill M = 4096 on the 2B FFN shapes (tensor-core roofline against
+        the measured bf16 dense peak: sm_103a has no integer tensor-core MMA,
+        so the exact integer products run as bf16 MMAs);
+      * the fused FFN (hidden 2560, FFN 6912) at seq 1 and seq 4096."""
     from bitlinear_bitnet_linear_03_b300 import synth
     out = {}
     dev = torch.device("cuda")
-    peak = float(peaks["bf16_tflops"]) if peaks and peaks.get("bf16_tflops") else 1800.0
+    hbm = float(peaks["hbm_gbs"]) if peaks and peaks.get("hbm_gbs") else 6400.0
+    tpk = float(peaks["bf16_tflops"]) if peaks and peaks.get("bf16_tflops") else 1800.0
+
+    def hbm_roof(gbs):
+        return {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(gbs / hbm, 4)}
+
+    def tc_roof(tops):
+        return {"bound": "tensor", "achieved": round(tops, 1), "peak": tpk, "unit": "TFLOP/s",
+                "frac": round(tops / tpk, 4),
+                "peak_source": "measured bf16 dense (no int8 tensor MMA on sm_103a)"}
+
+    # single GEMV 2560x2560, M = 1
+    N = K = 2560
+    sets = _weight_sets(torch, bn, synth, N, K, 80, 100)
+    x = synth.tokens_bf16(1, K, seed=0, device="cuda")
+    y = torch.empty((1, N), dtype=torch.float32, device=dev)
+    t = _time_calls(torch, lambda i: bn.bitnet_linear_bf16(x, [(sets[i % 80][0], sets[i % 80][1], y)],
+                                                         weights_static=True), 400)
+    byts = N * K // 4 + 2 * K + 4 + 4 * N
+    out["gemv_2560x2560_M1"] = {"us": round(t * 1e6, 2), "GBps": round(byts / t / 1e9, 1),
+                                "roofline": hbm_roof(byts / t / 1e9)}
+    del sets
+
+    # 100B-class shapes
+    for (N, K) in [(28672, 8192), (8192, 28672)]:
+        sets = _weight_sets(torch, bn, synth, N, K, 3, 200)
+        for M in (1, 4, 16, 64):
+            x = synth.tokens_bf16(M, K, seed=1, outlier_frac=0.01, device="cuda")
+            xq, sx = bn.bitnet_quantize_act(x)
+            y = torch.empty((M, N), dtype=torch.float32, device=dev)
+            ws = torch.empty(max(bn.bitnet_linear_workspace(M, N, K), 16), dtype=torch.uint8,
+                             device=dev)
+            t = _time_calls(torch, lambda i: bn.bitnet_linear(sets[i % 3][0], sets[i % 3][1], xq, sx,
+                                                              y=y, ws=ws), 12)
+            byts = N * K // 4 + M * K + 4 * M * N + 4 * M + 4
+            out[f"100b_M{M}_K{K}_N{N}"] = {
+                "us": round(t * 1e6, 1), "GBps": round(byts / t / 1e9, 1),
+                "tops": round(2 * M * N * K / t / 1e12, 2), "roofline": hbm_roof(byts / t / 1e9)}
+            del ws, y, xq, sx
+        del sets
+
+    # prefill
     for (N, K) in [(6912, 2560), (2560, 6912)]:
         M = 4096
-        sets = []
-        for r in range(4):
-            W = synth.weights_f32(N, K, seed=500 + r, device="cuda")
-            sets.append(bn.bitnet_quantize_weights(W))
-            del W
+        sets = _weight_sets(torch, bn, synth, N, K, 4, 500)
         x = synth.tokens_bf16(M, K, seed=600, device="cuda")
         xq, sx = bn.bitnet_quantize_act(x)
         y = torch.empty((M, N), dtype=torch.float32, device=dev)
         ws = torch.empty(max(bn.bitnet_linear_workspace(M, N, K), 16), dtype=torch.uint8,
                          device=dev)
-        for i in range(3):
-            Wq, s = sets[i % 4]
-            bn.bitnet_linear(Wq, s, xq, sx, y=y, ws=ws)
-        torch.cuda.synchronize()
-        reps = 20
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for i in range(reps):
-            Wq, s = sets[i % 4]
-            bn.bitnet_linear(Wq, s, xq, sx, y=y, ws=ws)
-        e1.record()
-        torch.cuda.synchronize()
-        t = e0.elapsed_time(e1) / 1e3 / reps
+        t = _time_calls(torch, lambda i: bn.bitnet_linear(sets[i % 4][0], sets[i % 4][1], xq, sx,
+                                                          y=y, ws=ws), 20)
         tops = 2 * M * N * K / t / 1e12
-        out[f"prefill_M{M}_K{K}_N{N}"] = {
-            "ms": round(t * 1e3, 4), "tops": round(tops, 1),
-            "roofline": {"bound": "tensor", "achieved": round(tops, 1), "peak": peak,
-                         "unit": "TFLOP/s", "frac": round(tops / peak, 4),
-                         "peak_source": "measured bf16 dense (no int8 tensor MMA on sm_103a)"}}
+        out[f"prefill_M{M}_K{K}_N{N}"] = {"ms": round(t * 1e3, 4), "tops": round(tops, 1),
+                                          "roofline": tc_roof(tops)}
         del sets, xq, sx, y, ws
+
+    # fused FFN
+    H, F = 2560, 6912
+    for M, nsets, reps in [(1, 10, 200), (4096, 2, 6)]:
+        ffn_sets = []
+        for r in range(nsets):
+            ffn_sets.append([bn.bitnet_quantize_weights(synth.weights_f32(n_, k_, seed=700 + 3 * r + j,
+                                                                           device="cuda"))
+                             for j, (n_, k_) in enumerate([(F, H), (F, H), (H, F)])])
+        x = synth.tokens_bf16(M, H, seed=0, device="cuda")
+        g = torch.ones(H, dtype=torch.float32, device=dev)
+        y = torch.empty((M, H), dtype=torch.float32, device=dev)
+        ws = torch.empty(bn.bitnet_ffn_workspace(M, H, F), dtype=torch.uint8, device=dev)
+
+        def ffn_call(i):
+            (wu, su), (wg, sg), (wd, sd) = ffn_sets[i % nsets]
+            bn.bitnet_ffn(x, g, 1e-5, wu, su, wg, sg, wd, sd, y=y, ws=ws)
+        t = _time_calls(torch, ffn_call, reps)
+        packed = 3 * H * F // 4
+        key = f"ffn_seq{M}"
+        if M == 1:
+            byts = packed + 2 * H + 4 * H + 3 * 4
+            out[key] = {"us": round(t * 1e6, 2), "GBps": round(byts / t / 1e9, 1),
+                        "roofline": hbm_roof(byts / t / 1e9)}
+        else:
+            tops = 2 * M * 3 * H * F / t / 1e12
+            out[key] = {"ms": round(t * 1e3, 3), "tops": round(tops, 1), "roofline": tc_roof(tops)}
+        del ffn_sets, ws, y
     return out
 
 
