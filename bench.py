@@ -288,15 +288,26 @@ def profiled_traffic(kernel_file, profile_file):
         return None
 
 
-def _time_calls(torch, fn, reps, warm=3):
+def _time_calls(torch, fn, reps, warm=3, graph=False):
+    """Seconds per call of fn(i), CUDA events after warm-up.  With graph=True
+    the reps calls are captured once in a CUDA graph (short calls: keeps the
+    host's launch cost out of the device time)."""
     for i in range(warm):
         fn(i)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for i in range(reps):
-        fn(i)
-    e1.record()
+    if graph:
+        g = capture(torch, lambda: [fn(i) for i in range(reps)])
+        g.replay()
+        torch.cuda.synchronize()
+        e0.record()
+        g.replay()
+        e1.record()
+    else:
+        e0.record()
+        for i in range(reps):
+            fn(i)
+        e1.record()
     torch.cuda.synchronize()
     return e0.elapsed_time(e1) / 1e3 / reps
 
@@ -341,7 +352,7 @@ def secondary_measurements(torch, bn, peaks):
     x = synth.tokens_bf16(1, K, seed=0, device="cuda")
     y = torch.empty((1, N), dtype=torch.float32, device=dev)
     t = _time_calls(torch, lambda i: bn.bitnet_linear_bf16(x, [(sets[i % 80][0], sets[i % 80][1], y)],
-                                                         weights_static=True), 400)
+                                                         weights_static=True), 400, graph=True)
     byts = N * K // 4 + 2 * K + 4 + 4 * N
     out["gemv_2560x2560_M1"] = {"us": round(t * 1e6, 2), "GBps": round(byts / t / 1e9, 1),
                                 "roofline": hbm_roof(byts / t / 1e9)}
@@ -397,7 +408,7 @@ def secondary_measurements(torch, bn, peaks):
         def ffn_call(i):
             (wu, su), (wg, sg), (wd, sd) = ffn_sets[i % nsets]
             bn.bitnet_ffn(x, g, 1e-5, wu, su, wg, sg, wd, sd, y=y, ws=ws)
-        t = _time_calls(torch, ffn_call, reps)
+        t = _time_calls(torch, ffn_call, reps, graph=(M == 1))
         packed = 3 * H * F // 4
         key = f"ffn_seq{M}"
         if M == 1:

@@ -45,15 +45,19 @@ namespace {
 constexpr int kBM = 128;
 constexpr int kRowBytes = 128;  // K bytes of one row per stage (one swizzle atom)
 constexpr int kATileBytes = kBM * kRowBytes;
-constexpr int kThreads = 192;
+constexpr int kThreads = 192;       // TMA, MMA, 4 epilogue warps
+constexpr int kThreadsFused = 320;  // + 4 warps expanding the packed weights
 constexpr uint32_t kTmemCols = 512;
 constexpr int kRingBytes = 192 * 1024;
 // Tile N = BN (256 or 128): B tile, stage size, ring depth and shared memory.
-template <int BN>
+// FUSED: B arrives as packed 2-bit codes (16 bytes per row per stage, in a
+// staging area after the B tile) and is expanded to bf16 in shared memory.
+template <int BN, bool FUSED = false>
 struct Tile {
   static constexpr int kBTileBytes = BN * kRowBytes;
-  static constexpr int kStageBytes = kATileBytes + kBTileBytes;
-  static constexpr int kStages = kRingBytes / kStageBytes;   // 4 or 6
+  static constexpr int kPackedBytes = FUSED ? BN * 16 : 0;
+  static constexpr int kStageBytes = kATileBytes + kBTileBytes + kPackedBytes;
+  static constexpr int kStages = kRingBytes / kStageBytes;   // 4 or 6; 3 fused
   static constexpr int kSmemBytes = kStages * kStageBytes + 1024;  // + alignment slack
 };
 constexpr long long kWaitCycles = 2000000000ll;
@@ -173,15 +177,49 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-template <int KIND, int BN>
-__global__ void __launch_bounds__(kThreads, 1)
+__device__ __forceinline__ uint32_t bf16_pair_from_codes(uint32_t p);
+
+// Expands the packed 2-bit codes of one stage (BN rows x 64 weights, 16
+// bytes per row) into the bf16 B tile in the 128-byte-swizzled K-major
+// layout the MMA descriptor reads: row r at (r/8)*1024 + (r%8)*128, 16-byte
+// chunk c (weights 8c .. 8c+7) at slot c ^ (r%8).  Thread t of 128 takes rows
+// t, t+128, ...
+template <int BN>
+__device__ __forceinline__ void expand_b_tile(uint32_t packed, uint32_t btile, int t) {
+  for (int r = t; r < BN; r += 128) {
+    uint4 w;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(w.x), "=r"(w.y), "=r"(w.z), "=r"(w.w)
+                 : "r"(packed + 16 * r));
+    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+    const uint32_t rowbase = btile + (uint32_t)((r >> 3) * 1024 + (r & 7) * 128);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const int sft = 2 * (c >> 1), h = c & 1;
+      const uint32_t u0 = (ww[2 * h] >> sft) & 0x03030303u;
+      const uint32_t u1 = (ww[2 * h + 1] >> sft) & 0x03030303u;
+      const uint32_t o0 = bf16_pair_from_codes((u0 & 3u) | ((u0 & 0x300u) << 8));
+      const uint32_t o1 = bf16_pair_from_codes(((u0 >> 16) & 3u) | ((u0 >> 8) & 0x30000u));
+      const uint32_t o2 = bf16_pair_from_codes((u1 & 3u) | ((u1 & 0x300u) << 8));
+      const uint32_t o3 = bf16_pair_from_codes(((u1 >> 16) & 3u) | ((u1 >> 8) & 0x30000u));
+      asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(rowbase + 16u * (uint32_t)(c ^ (r & 7))),
+                   "r"(o0), "r"(o1), "r"(o2), "r"(o3)
+                   : "memory");
+    }
+  }
+}
+
+template <int KIND, int BN, bool FUSED>
+__global__ void __launch_bounds__(FUSED ? kThreadsFused : kThreads, 1)
 k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
           const __grid_constant__ Args a) {
   extern __shared__ uint8_t smem_raw[];
-  constexpr int kStages = Tile<BN>::kStages;
-  constexpr int kStageBytes = Tile<BN>::kStageBytes;
+  constexpr int kStages = Tile<BN, FUSED>::kStages;
+  constexpr int kStageBytes = Tile<BN, FUSED>::kStageBytes;
+  constexpr int kBTileBytesT = Tile<BN, FUSED>::kBTileBytes;
   __shared__ __align__(8) uint64_t full_bar[kStages];
   __shared__ __align__(8) uint64_t empty_bar[kStages];
+  __shared__ __align__(8) uint64_t bready_bar[kStages];  // fused: B tile expanded
   __shared__ __align__(8) uint64_t acc_full[2];
   __shared__ __align__(8) uint64_t acc_empty[2];
   __shared__ __align__(8) uint64_t drain_bar;
@@ -196,6 +234,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUte
     for (int s = 0; s < kStages; ++s) {
       mbar_init(saddr(&full_bar[s]), 1);
       mbar_init(saddr(&empty_bar[s]), 1);
+      mbar_init(saddr(&bready_bar[s]), 4);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(saddr(&acc_full[b]), 1);
@@ -239,9 +278,17 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUte
           }
           const uint32_t fb = saddr(&full_bar[s]);
           const uint32_t sa = smem0 + s * kStageBytes;
-          mbar_expect_tx(fb, kStageBytes);
-          tma_load_2d(sa, &mapA, ks * Kind<KIND>::kKStage, m0, fb);
-          tma_load_2d(sa + kATileBytes, &mapB, ks * Kind<KIND>::kKStage, n0, fb);
+          if (FUSED) {
+            // A tile (bf16) and the packed codes of the B tile (16 bytes per
+            // row = the stage's 64 weights).
+            mbar_expect_tx(fb, kATileBytes + Tile<BN, FUSED>::kPackedBytes);
+            tma_load_2d(sa, &mapA, ks * Kind<KIND>::kKStage, m0, fb);
+            tma_load_2d(sa + kATileBytes + kBTileBytesT, &mapB, ks * 16, n0, fb);
+          } else {
+            mbar_expect_tx(fb, kStageBytes);
+            tma_load_2d(sa, &mapA, ks * Kind<KIND>::kKStage, m0, fb);
+            tma_load_2d(sa + kATileBytes, &mapB, ks * Kind<KIND>::kKStage, n0, fb);
+          }
           issued = it + 1;
         }
       }
@@ -268,7 +315,8 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUte
         const uint32_t d = tmem + (uint32_t)(ab * BN);
         for (int ks = 0; ks < a.k_stages; ++ks, ++it) {
           const int s = it % kStages;
-          if (!mbar_wait(saddr(&full_bar[s]), (it / kStages) & 1) || *(volatile int*)&s_abort) {
+          const uint32_t ready = FUSED ? saddr(&bready_bar[s]) : saddr(&full_bar[s]);
+          if (!mbar_wait(ready, (it / kStages) & 1) || *(volatile int*)&s_abort) {
             atomicOr(&g_device_error, kErrMma);
             *(volatile int*)&s_abort = 1;
             ok = false;
@@ -290,6 +338,29 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUte
       // All MMAs issued by this thread have finished before TMEM is freed.
       tc_commit(saddr(&drain_bar));
       if (!mbar_wait(saddr(&drain_bar), 0)) atomicOr(&g_device_error, kErrDrain);
+    }
+  } else if (FUSED && warp >= 6) {
+    // ------------------------------------------------------------ B expansion
+    const int ct = threadIdx.x - 6 * 32;  // 0 .. 127
+    int it = 0;
+    for (int t = blockIdx.x; t < tiles; t += gridDim.x) {
+      bool ok = true;
+      for (int ks = 0; ks < a.k_stages; ++ks, ++it) {
+        const int s = it % kStages;
+        if (!mbar_wait(saddr(&full_bar[s]), (it / kStages) & 1) || *(volatile int*)&s_abort) {
+          if (lane == 0) atomicOr(&g_device_error, kErrProducer);
+          *(volatile int*)&s_abort = 1;
+          ok = false;
+          break;
+        }
+        const uint32_t sa = smem0 + s * kStageBytes;
+        expand_b_tile<BN>(sa + kATileBytes + kBTileBytesT, sa + kATileBytes, ct);
+        // make the generic-proxy stores visible to the tensor core's reads
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) mbar_arrive(saddr(&bready_bar[s]));
+      }
+      if (!ok) break;
     }
   } else {
     // ------------------------------------------------------------ epilogue
@@ -430,6 +501,20 @@ cudaError_t get_encode() {
   return cudaSuccess;
 }
 
+// Packed weights [N, K/4] bytes as a 2-D uint8 tensor, boxes of 16 bytes (64
+// weights) x box_rows, no swizzle.
+cudaError_t encode_packed(CUtensorMap* map, const void* Wq, int64_t N, int64_t K, int box_rows) {
+  cuuint64_t dims[2] = {(cuuint64_t)(K / 4), (cuuint64_t)N};
+  cuuint64_t strides[1] = {(cuuint64_t)(K / 4)};
+  cuuint32_t box[2] = {16u, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(Wq), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 // 2-D K-major operand [rows, K], boxes of (128 bytes of K) x box_rows.
 cudaError_t encode_operand(CUtensorMap* map, const void* base, int64_t rows, int64_t K,
                            int elem_bytes, int box_rows) {
@@ -450,7 +535,7 @@ constexpr int kKind = 1;
 
 size_t round1k(size_t v) { return (v + 1023) / 1024 * 1024; }
 
-template <int KIND, int BN>
+template <int KIND, int BN, bool FUSED>
 cudaError_t launch_kind(const uint8_t* Wq, const float* w_scale, const int8_t* xq,
                         const float* x_scale, int64_t M, int64_t N, int64_t K, float* y,
                         int32_t* acc_out, void* ws, cudaStream_t s) {
@@ -458,8 +543,8 @@ cudaError_t launch_kind(const uint8_t* Wq, const float* w_scale, const int8_t* x
   if (e != cudaSuccess) return e;
   uint8_t* w = static_cast<uint8_t*>(ws);
   void* B = w;
-  void* A = w + round1k((size_t)(N * K * 2));
-  const int64_t nblk = N * K / 64, nx = M * K / 16;
+  void* A = FUSED ? w : w + round1k((size_t)(N * K * 2));
+  const int64_t nblk = FUSED ? 0 : N * K / 64, nx = M * K / 16;
   int64_t grid = (nblk + nx + 255) / 256;
   if (grid > 148 * 16) grid = 148 * 16;
   k_prepass<<<(unsigned)grid, 256, 0, s>>>(reinterpret_cast<const uint4*>(Wq), nblk,
@@ -470,7 +555,9 @@ cudaError_t launch_kind(const uint8_t* Wq, const float* w_scale, const int8_t* x
   if (e != cudaSuccess) return e;
   CUtensorMap mapA, mapB;
   e = encode_operand(&mapA, A, M, K, Kind<KIND>::kElem, kBM);
-  if (e == cudaSuccess) e = encode_operand(&mapB, B, N, K, Kind<KIND>::kElem, BN);
+  if (e == cudaSuccess)
+    e = FUSED ? encode_packed(&mapB, Wq, N, K, BN)
+              : encode_operand(&mapB, B, N, K, Kind<KIND>::kElem, BN);
   if (e != cudaSuccess) return e;
   Args a;
   a.M = (int)M;
@@ -488,15 +575,17 @@ cudaError_t launch_kind(const uint8_t* Wq, const float* w_scale, const int8_t* x
   e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 64 && !configured[dev]) {
-    e = cudaFuncSetAttribute(k_gemm_tc<KIND, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Tile<BN>::kSmemBytes);
+    e = cudaFuncSetAttribute(k_gemm_tc<KIND, BN, FUSED>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Tile<BN, FUSED>::kSmemBytes);
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
   const int tiles = a.m_tiles * a.n_tiles;
   const int ctas = tiles < 148 ? tiles : 148;
-  return launch_pdl(k_gemm_tc<KIND, BN>, dim3(ctas), dim3(kThreads),
-                    (size_t)Tile<BN>::kSmemBytes, s, mapA, mapB, a);
+  return launch_pdl(k_gemm_tc<KIND, BN, FUSED>, dim3(ctas),
+                    dim3(FUSED ? kThreadsFused : kThreads), (size_t)Tile<BN, FUSED>::kSmemBytes, s,
+                    mapA, mapB, a);
 }
 
 // Tile N.  128-wide tiles fill the last wave of 148 SMs better for some
@@ -511,19 +600,27 @@ int pick_bn(int64_t M, int64_t N) {
 }  // namespace
 
 bool gemm_tc_eligible(int64_t M, int64_t N, int64_t K) {
-  return M >= 64 && N >= 1 && K >= 64 && K % 64 == 0;
+  return M >= 16 && N >= 1 && K >= 64 && K % 64 == 0;
 }
 
+// Small batches expand the packed weights on chip (streaming 2 bits per
+// weight from HBM); large ones expand them once into a bf16 copy that stays
+// in L2 across the many output-tile rows.
+bool use_fused(int64_t M) { return M <= 256; }
+
 size_t gemm_tc_workspace(int64_t M, int64_t N, int64_t K) {
+  if (use_fused(M)) return round1k((size_t)(M * K * 2));
   return round1k((size_t)(N * K * 2)) + round1k((size_t)(M * K * 2));
 }
 
 cudaError_t launch_gemm_tc(const uint8_t* Wq, const float* w_scale, const int8_t* xq,
                            const float* x_scale, int64_t M, int64_t N, int64_t K, float* y,
                            int32_t* acc_out, void* ws, cudaStream_t s) {
+  if (use_fused(M))
+    return launch_kind<kKind, 256, true>(Wq, w_scale, xq, x_scale, M, N, K, y, acc_out, ws, s);
   if (pick_bn(M, N) == 128)
-    return launch_kind<kKind, 128>(Wq, w_scale, xq, x_scale, M, N, K, y, acc_out, ws, s);
-  return launch_kind<kKind, 256>(Wq, w_scale, xq, x_scale, M, N, K, y, acc_out, ws, s);
+    return launch_kind<kKind, 128, false>(Wq, w_scale, xq, x_scale, M, N, K, y, acc_out, ws, s);
+  return launch_kind<kKind, 256, false>(Wq, w_scale, xq, x_scale, M, N, K, y, acc_out, ws, s);
 }
 
 cudaError_t read_and_clear_device_error(int* code, cudaStream_t s) {
