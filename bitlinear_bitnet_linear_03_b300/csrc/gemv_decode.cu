@@ -151,6 +151,19 @@ __device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uin
 __device__ __forceinline__ void consumer_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
 }
+// Consumer barrier that also ORs a flag over the consumers: every consumer
+// leaves with the same answer (an abort decision taken after it is uniform,
+// so no consumer is left waiting at a later barrier).
+__device__ __forceinline__ bool consumer_sync_or(int flag) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.s32 p, %1, 0;\n bar.red.or.pred q, 1, %2, p;\n"
+      " selp.u32 %0, 1, 0, q;\n}"
+      : "=r"(r)
+      : "r"(flag), "n"(kConsumers)
+      : "memory");
+  return r != 0;
+}
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   uint4 v;
   asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
@@ -192,6 +205,15 @@ __device__ __forceinline__ void prefetch_phase(const Phase& ph) {
   }
 }
 
+// L2 prefetch hint for one phase's input x (bf16 or int8, M rows).
+__device__ __forceinline__ void prefetch_x(const Phase& ph, int M) {
+  const void* p = ph.xb != nullptr ? (const void*)ph.xb : (const void*)ph.xq;
+  const int64_t bytes = (int64_t)M * ph.K * (ph.xb != nullptr ? 2 : 1);
+  for (int64_t off = 0; off < bytes; off += kPrefetchMax)
+    prefetch_l2_bulk(static_cast<const uint8_t*>(p) + off,
+                     (uint32_t)(bytes - off < kPrefetchMax ? bytes - off : kPrefetchMax));
+}
+
 // Grid barrier of a chain: a 64-bit counter that every CTA increments once
 // per barrier and that is never reset; barrier b of this launch completes
 // when it reaches base + (b + 1) * gridDim.x.  Bounded wait.
@@ -218,37 +240,70 @@ __device__ __forceinline__ void copy_phase(const Phase& src, Phase* dst, int lan
   for (int i = lane; i < (int)(sizeof(Phase) / 8); i += 32) d[i] = s[i];
 }
 
-// Partial dot products of one row for this lane: J chunks, MT tokens, one
-// accumulator per field (scaled by 4^s), folded to one int per token.
-template <int MT, int J>
-__device__ __forceinline__ void row_partial(uint32_t wrow, int valid_j, const uint4 (&xr)[MT][J][4],
-                                            int (&v)[MT]) {
-  int acc[MT][4];
+// Partial dot products of NR rows (1 or 2; row addresses w[]) for this lane:
+// J chunks, MT tokens, one accumulator per row, token and field (scaled by
+// 4^s), folded to one int per row and token.  With two rows their
+// accumulations alternate, so consecutive dp4a never feed each other.
+template <int MT, int J, int NR>
+__device__ __forceinline__ void row_partials(const uint32_t (&w)[NR], int valid_j,
+                                             const uint4 (&xr)[MT][J][4], int (&v)[NR][MT]) {
+  int acc[NR][MT][4];
 #pragma unroll
-  for (int m = 0; m < MT; ++m) acc[m][0] = acc[m][1] = acc[m][2] = acc[m][3] = 0;
+  for (int r = 0; r < NR; ++r)
+#pragma unroll
+    for (int m = 0; m < MT; ++m)
+#pragma unroll
+      for (int s = 0; s < 4; ++s) acc[r][m][s] = 0;
 #pragma unroll
   for (int j = 0; j < J; ++j) {
     if (j < valid_j) {
-      const uint4 w = lds128(wrow + 512 * j);
-      const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+      uint32_t q[NR][4];
 #pragma unroll
-      for (int m = 0; m < MT; ++m)
+      for (int r = 0; r < NR; ++r) {
+        const uint4 pk = lds128(w[r] + 512 * j);
+        q[r][0] = pk.x;
+        q[r][1] = pk.y;
+        q[r][2] = pk.z;
+        q[r][3] = pk.w;
+      }
 #pragma unroll
-        for (int s = 0; s < 4; ++s) {
-          const uint32_t xw[4] = {xr[m][j][s].x, xr[m][j][s].y, xr[m][j][s].z, xr[m][j][s].w};
+      for (int i = 0; i < 4; ++i)
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
-            acc[m][s] = dp4a_us(ww[i] & (0x03030303u << (2 * s)), xw[i], acc[m][s]);
-        }
+        for (int s = 0; s < 4; ++s)
+#pragma unroll
+          for (int m = 0; m < MT; ++m) {
+            const uint4 xv = xr[m][j][s];
+            const uint32_t xw = i == 0 ? xv.x : i == 1 ? xv.y : i == 2 ? xv.z : xv.w;
+            const uint32_t mask = 0x03030303u << (2 * s);
+#pragma unroll
+            for (int r = 0; r < NR; ++r) acc[r][m][s] = dp4a_us(q[r][i] & mask, xw, acc[r][m][s]);
+          }
     }
   }
 #pragma unroll
-  for (int m = 0; m < MT; ++m)
-    v[m] = acc[m][0] + (acc[m][1] >> 2) + (acc[m][2] >> 4) + (acc[m][3] >> 6);
+  for (int r = 0; r < NR; ++r)
+#pragma unroll
+    for (int m = 0; m < MT; ++m)
+      v[r][m] = acc[r][m][0] + (acc[r][m][1] >> 2) + (acc[r][m][2] >> 4) + (acc[r][m][3] >> 6);
 }
 
-template <int MT, int J>
-__global__ void __launch_bounds__(kThreads, MT <= 2 ? 2 : 1)
+// What the producer records when it fills a ring slot of a single-phase
+// launch, read back when the consumers release the slot and it writes the
+// stage's outputs.
+struct StageRec {
+  int p, row0, nrows;
+};
+
+// CHAIN: a chain of phases (cooperative launch, grid barrier between phases);
+// the consumers write the outputs of every stage (K parts merged through
+// shared-memory atomics) and arrive at the barrier.  Otherwise one phase: the
+// consumers leave each row's K-part results in shared memory and release the
+// slot, and the producer warp writes the stage's outputs while the next
+// stages are consumed.
+// A chain runs one CTA per SM (all resident for the grid barrier): its
+// registers are not shared with a second CTA.
+template <int MT, int J, bool CHAIN>
+__global__ void __launch_bounds__(kThreads, (MT <= 2 && !CHAIN) ? 2 : 1)
 k_gemv_decode(const __grid_constant__ Args a) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t full_bar[kMaxStages];
@@ -259,18 +314,24 @@ k_gemv_decode(const __grid_constant__ Args a) {
   // loop; shared memory instead of a pointer into the parameter block or the
   // chain table).
   __shared__ __align__(16) Phase s_ph;
-  // K-part merge per ring slot and stage row: the low 48 bits hold the sum of
-  // the parts' biased partial dot products, bits 48.. count the parts added.
-  __shared__ unsigned long long s_acc[kMaxStages][kConsumerWarps * kMaxRowsPerWarp / 2][MT];
+  // CHAIN: K-part merge per ring slot and stage row; the low 48 bits hold
+  // the sum of the parts' biased partial dot products, bits 48.. count the
+  // parts added.  Otherwise: each K part's row result (part kw of stage row
+  // r at kw * R + r), the stage records and the activation scales.
+  constexpr int kAccRows = CHAIN ? kConsumerWarps * kMaxRowsPerWarp / 2 : 1;
+  constexpr int kPartRows = CHAIN ? 1 : kConsumerWarps * kMaxRowsPerWarp;
+  __shared__ unsigned long long s_acc[kMaxStages][kAccRows][MT];
+  __shared__ int s_part[kMaxStages][kPartRows][MT];
+  __shared__ StageRec s_stage[kMaxStages];
+  __shared__ float s_xscale[MT];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t ring = smem_addr(smem);
-  const bool chain = a.phases != nullptr;
-  const Phase* phases = chain ? a.phases : &a.ph0;
+  const Phase* phases = CHAIN ? a.phases : &a.ph0;
 
-  for (int q = threadIdx.x; q < kMaxStages * (kConsumerWarps * kMaxRowsPerWarp / 2) * MT;
-       q += kThreads)
-    (&s_acc[0][0][0])[q] = 0ull;
+  if (CHAIN)
+    for (int q = threadIdx.x; q < kMaxStages * kAccRows * MT; q += kThreads)
+      (&s_acc[0][0][0])[q] = 0ull;
   if (threadIdx.x < 32) copy_phase(phases[0], &s_ph, threadIdx.x);
   if (threadIdx.x == 0) {
     for (int s = 0; s < a.stages; ++s) {
@@ -279,16 +340,20 @@ k_gemv_decode(const __grid_constant__ Args a) {
     }
     mbar_fence_init();
     s_abort = 0;
-    // L2 prefetch hint for the first phase's weights (independent of the
-    // previous kernel; no data is read before the dependency wait).
+    // L2 prefetch hints for the first phase's input and weights (no data is
+    // read before the dependency wait).
+    prefetch_x(phases[0], a.M);
     prefetch_phase(phases[0]);
   }
   griddep_launch_dependents();
   __syncthreads();
 
   // ------------------------------------------------------------ producer
+  // Lane 0 fills the ring with bulk copies.  Single phase: the whole warp
+  // also writes the outputs of each stage the consumers have released
+  // (y = acc * (x_scale * w_scale), rows across the lanes).
   if (warp == kConsumerWarps) {
-    if (lane != 0) return;
+    if (CHAIN && lane != 0) return;
     // Weights the caller declared static may stream in while the previous
     // kernel on the stream is still running (one ring's worth); otherwise
     // wait for it first.  Either way every bounded wait below starts after
@@ -296,13 +361,35 @@ k_gemv_decode(const __grid_constant__ Args a) {
     // boundaries: weights never depend on earlier phases.
     bool dep_done = !a.weights_early;
     if (dep_done) griddep_wait();
-    int i = 0;
-    for (int ph_i = 0; ph_i < a.nphases; ++ph_i) {
+    const int S = a.stages;
+    const float ws_lane = (!CHAIN && lane < s_ph.count) ? *s_ph.t[lane].w_scale : 0.0f;
+    auto finish = [&](int slot) {
+      const StageRec rec = s_stage[slot];
+      const Target& T = s_ph.t[rec.p];
+      const float wsc = __shfl_sync(0xffffffffu, ws_lane, rec.p);
+      const int R = s_ph.rows_per_stage, wk = s_ph.wk;
+      for (int m = 0; m < a.M; ++m) {
+        const float c = __fmul_rn(s_xscale[m], wsc);
+        for (int r = lane; r < rec.nrows; r += 32) {
+          int tot = 0;
+          for (int kw = 0; kw < wk; ++kw) tot += s_part[slot][kw * R + r][m];
+          const int64_t o = (int64_t)m * T.N + rec.row0 + r;
+          T.y[o] = __fmul_rn(__int2float_rn(tot), c);
+          if (T.acc_out) T.acc_out[o] = tot;
+        }
+      }
+    };
+    int i = 0, done = 0;
+    bool ok = true;
+    for (int ph_i = 0; ph_i < a.nphases && ok; ++ph_i) {
       const Phase& ph = phases[ph_i];
-      if (ph_i + 1 < a.nphases) prefetch_phase(phases[ph_i + 1]);
+      if (ph_i + 1 < a.nphases) {
+        prefetch_x(phases[ph_i + 1], a.M);
+        prefetch_phase(phases[ph_i + 1]);
+      }
       const int64_t row_bytes = ph.K >> 2;
-      const bool ok = for_each_stage(ph, [&](int p, int row, int nrows) {
-        const int slot = i % a.stages, use = i / a.stages;
+      ok = for_each_stage(ph, [&](int p, int row, int nrows) {
+        const int slot = i % S, use = i / S;
         if (use > 0) {
           if (!dep_done) {
             griddep_wait();
@@ -310,28 +397,51 @@ k_gemv_decode(const __grid_constant__ Args a) {
           }
           if (!mbar_wait(smem_addr(&empty_bar[slot]), (use - 1) & 1) ||
               *(volatile int*)&s_abort) {
-            atomicOr(&g_decode_error, 1 << kErrEmptyWait);
+            if (lane == 0) atomicOr(&g_decode_error, 1 << kErrEmptyWait);
+            *(volatile int*)&s_abort = 1;
             return false;
           }
+          if (!CHAIN) {
+            finish(slot);
+            ++done;
+          }
         }
-        const uint32_t bytes = (uint32_t)(nrows * row_bytes);
-        const uint32_t fb = smem_addr(&full_bar[slot]);
-        mbar_arrive_expect_tx(fb, bytes);
-        bulk_copy_g2s(ring + slot * a.slot_bytes, ph.t[p].Wq + (int64_t)row * row_bytes, bytes,
-                      fb);
+        if (lane == 0) {
+          if (!CHAIN) s_stage[slot] = StageRec{p, row, nrows};
+          const uint32_t bytes = (uint32_t)(nrows * row_bytes);
+          const uint32_t fb = smem_addr(&full_bar[slot]);
+          mbar_arrive_expect_tx(fb, bytes);
+          bulk_copy_g2s(ring + slot * a.slot_bytes, ph.t[p].Wq + (int64_t)row * row_bytes,
+                        bytes, fb);
+        }
+        if (!CHAIN) __syncwarp();
         ++i;
         return true;
       });
-      if (!ok) break;
     }
+    // Single phase: the stages still in the ring.
+    if (!CHAIN)
+      for (; ok && done < i; ++done) {
+        const int slot = done % S;
+        if (!mbar_wait(smem_addr(&empty_bar[slot]), (done / S) & 1) ||
+            *(volatile int*)&s_abort) {
+          if (lane == 0) atomicOr(&g_decode_error, 1 << kErrEmptyWait);
+          *(volatile int*)&s_abort = 1;
+          ok = false;
+          break;
+        }
+        finish(slot);
+      }
     // Never leave the CTA with a copy in flight: wait for the last copy of
     // every slot to land.
-    const int first = i > a.stages ? i - a.stages : 0;
-    for (int j = first; j < i; ++j)
-      if (!mbar_wait(smem_addr(&full_bar[j % a.stages]), (j / a.stages) & 1)) {
-        atomicOr(&g_decode_error, 1 << kErrDrainWait);
-        break;
-      }
+    if (lane == 0) {
+      const int first = i > S ? i - S : 0;
+      for (int j = first > done ? first : done; j < i; ++j)
+        if (!mbar_wait(smem_addr(&full_bar[j % S]), (j / S) & 1)) {
+          atomicOr(&g_decode_error, 1 << kErrDrainWait);
+          break;
+        }
+    }
     return;
   }
 
@@ -340,8 +450,11 @@ k_gemv_decode(const __grid_constant__ Args a) {
   const int tid = threadIdx.x;  // 0 .. kConsumers-1
   int8_t* xs = reinterpret_cast<int8_t*>(smem + a.stages * a.slot_bytes);
   unsigned long long bar_base = 0;
-  if (chain && tid == 0) bar_base = ld_acquire_u64(a.barrier) / gridDim.x * gridDim.x;
-  int i = 0;  // ring stage counter, shared sequence with the producer
+  if (CHAIN && tid == 0) bar_base = ld_acquire_u64(a.barrier) / gridDim.x * gridDim.x;
+  // Ring position (slot and phase parity) of the next stage; the consumers
+  // walk the same stage sequence as the producer.
+  int c_slot = 0;
+  uint32_t c_parity = 0;
 
   for (int ph_i = 0; ph_i < a.nphases; ++ph_i) {
     const Phase& ph = s_ph;
@@ -354,8 +467,7 @@ k_gemv_decode(const __grid_constant__ Args a) {
         atomicOr(&g_decode_error, 1 << kErrFullWait);
         *(volatile int*)&s_abort = 1;
       }
-      consumer_sync();
-      if (*(volatile int*)&s_abort) break;
+      if (consumer_sync_or(*(volatile int*)&s_abort)) break;
     }
     const int K = ph.K;
     const int64_t row_bytes = K >> 2;
@@ -518,36 +630,49 @@ k_gemv_decode(const __grid_constant__ Args a) {
     // On a time-out a warp sets s_abort and from then on every warp only
     // walks the stage sequence (no waits, no work) so that all of them reach
     // the same named barriers; the phase loop then ends uniformly.
+    if (!CHAIN && tid == 0)
+      for (int m = 0; m < MT; ++m) s_xscale[m] = xscale[m];
+    const int full_rows = ph.rows_per_stage / nwr;  // rows of a full stage per warp
     for_each_stage(ph, [&](int p, int row0, int nrows) {
-      const int slot = i % a.stages;
-      ++i;
+      const int slot = c_slot;
+      const uint32_t parity = c_parity;
+      if (++c_slot == a.stages) {
+        c_slot = 0;
+        c_parity ^= 1u;
+      }
       if (*(volatile int*)&s_abort) return true;
-      if (!mbar_wait(smem_addr(&full_bar[slot]), ((i - 1) / a.stages) & 1)) {
+      if (!mbar_wait(smem_addr(&full_bar[slot]), parity)) {
         if (lane == 0) atomicOr(&g_decode_error, 1 << kErrFullWait);
         *(volatile int*)&s_abort = 1;
         return true;
       }
-      const Target& T = ph.t[p];
-      const float wsc = __shfl_sync(0xffffffffu, ws_lane, p);
+      const float wsc = CHAIN ? __shfl_sync(0xffffffffu, ws_lane, p) : 0.0f;
       const uint32_t sbase = ring + slot * a.slot_bytes + 16 * (k_lo + lane);
       // Rows wr + q*nwr (q < my_rows <= kMaxRowsPerWarp) of the stage, two at
       // a time; their warp sums are uniform across the lanes.
-      const int my_rows = nrows > wr ? (nrows - wr + nwr - 1) / nwr : 0;
+      const int my_rows = nrows == ph.rows_per_stage
+                              ? full_rows
+                              : (nrows > wr ? (nrows - wr + nwr - 1) / nwr : 0);
       int vals[kMaxRowsPerWarp][MT];
 #pragma unroll
       for (int q = 0; q < kMaxRowsPerWarp; q += 2) {
-        if (q < my_rows) {
-          const bool two = q + 1 < my_rows;
-          int v1[MT], v2[MT];
-          row_partial<MT, J>(sbase + (uint32_t)((wr + q * nwr) * row_bytes), valid_j, xr, v1);
-          if (two)
-            row_partial<MT, J>(sbase + (uint32_t)((wr + (q + 1) * nwr) * row_bytes), valid_j,
-                               xr, v2);
+        if (q + 1 < my_rows) {
+          const uint32_t w[2] = {sbase + (uint32_t)((wr + q * nwr) * row_bytes),
+                                 sbase + (uint32_t)((wr + (q + 1) * nwr) * row_bytes)};
+          int v[2][MT];
+          row_partials<MT, J, 2>(w, valid_j, xr, v);
 #pragma unroll
           for (int m = 0; m < MT; ++m) {
-            vals[q][m] = __reduce_add_sync(0xffffffffu, v1[m] - lsum[m]);
-            vals[q + 1][m] = two ? __reduce_add_sync(0xffffffffu, v2[m] - lsum[m]) : 0;
+            vals[q][m] = __reduce_add_sync(0xffffffffu, v[0][m] - lsum[m]);
+            vals[q + 1][m] = __reduce_add_sync(0xffffffffu, v[1][m] - lsum[m]);
           }
+        } else if (q < my_rows) {
+          const uint32_t w[1] = {sbase + (uint32_t)((wr + q * nwr) * row_bytes)};
+          int v[1][MT];
+          row_partials<MT, J, 1>(w, valid_j, xr, v);
+#pragma unroll
+          for (int m = 0; m < MT; ++m)
+            vals[q][m] = __reduce_add_sync(0xffffffffu, v[0][m] - lsum[m]);
         }
       }
       // Lane q*MT + m finishes row q for token m: all rows of the stage at once.
@@ -559,11 +684,15 @@ k_gemv_decode(const __grid_constant__ Args a) {
 #pragma unroll
           for (int mm = 0; mm < MT; ++mm)
             if (qq * MT + mm == lane) tot = vals[qq][mm];
-        float xsc = xscale[0];
+        if (!CHAIN) {
+          // The producer sums the K parts and writes the row.
+          if (q < my_rows && q < kMaxRowsPerWarp)
+            s_part[slot][kw * ph.rows_per_stage + wr + q * nwr][m] = tot;
+        } else if (q < my_rows && q < kMaxRowsPerWarp && m < a.M) {
+          float xsc = xscale[0];
 #pragma unroll
-        for (int mm = 1; mm < MT; ++mm)
-          if (mm == m) xsc = xscale[mm];
-        if (q < my_rows && q < kMaxRowsPerWarp && m < a.M) {
+          for (int mm = 1; mm < MT; ++mm)
+            if (mm == m) xsc = xscale[mm];
           const int row = wr + q * nwr;
           bool last = true;
           if (ph.wk > 1) {
@@ -582,6 +711,7 @@ k_gemv_decode(const __grid_constant__ Args a) {
             }
           }
           if (last) {
+            const Target& T = ph.t[p];
             const int64_t o = (int64_t)m * T.N + row0 + row;
             T.y[o] = __fmul_rn(__int2float_rn(tot), __fmul_rn(xsc, wsc));
             if (T.acc_out) T.acc_out[o] = tot;
@@ -596,9 +726,8 @@ k_gemv_decode(const __grid_constant__ Args a) {
     // CTA barrier one thread makes them visible GPU-wide (a fence is
     // cumulative over what the CTA barrier ordered) and arrives at the grid
     // barrier.
-    consumer_sync();
-    if (*(volatile int*)&s_abort) break;
-    if (chain && ph_i + 1 < a.nphases && tid == 0) {
+    if (consumer_sync_or(*(volatile int*)&s_abort)) break;
+    if (CHAIN && ph_i + 1 < a.nphases && tid == 0) {
       __threadfence();
       atomicAdd(a.barrier, 1ull);
     }
@@ -668,7 +797,7 @@ bool make_plan(int64_t M, int64_t K, Plan* pl) {
   return pl->smem <= (size_t)kMaxSmem;
 }
 
-template <int MT, int J>
+template <int MT, int J, bool CHAIN>
 cudaError_t configure(int smem_needed) {
   (void)smem_needed;
   static bool configured[64] = {};
@@ -676,7 +805,7 @@ cudaError_t configure(int smem_needed) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 64 && !configured[dev]) {
-    e = cudaFuncSetAttribute(k_gemv_decode<MT, J>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(k_gemv_decode<MT, J, CHAIN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kMaxSmem);
     if (e != cudaSuccess) return e;
     configured[dev] = true;
@@ -686,16 +815,16 @@ cudaError_t configure(int smem_needed) {
 
 template <int MT, int J>
 cudaError_t launch_t(const Args& a, int ctas, size_t smem, cudaStream_t s) {
-  cudaError_t e = configure<MT, J>((int)smem);
+  cudaError_t e = configure<MT, J, false>((int)smem);
   if (e != cudaSuccess) return e;
-  return launch_pdl(k_gemv_decode<MT, J>, dim3(ctas), dim3(kThreads), smem, s, a);
+  return launch_pdl(k_gemv_decode<MT, J, false>, dim3(ctas), dim3(kThreads), smem, s, a);
 }
 
 // Chains run as a cooperative launch (all CTAs resident: the grid barrier
 // needs it).
 template <int MT, int J>
 cudaError_t launch_coop(const Args& a, int ctas, size_t smem, cudaStream_t s) {
-  cudaError_t e = configure<MT, J>((int)smem);
+  cudaError_t e = configure<MT, J, true>((int)smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(ctas);
@@ -707,7 +836,7 @@ cudaError_t launch_coop(const Args& a, int ctas, size_t smem, cudaStream_t s) {
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k_gemv_decode<MT, J>, a);
+  return cudaLaunchKernelEx(&cfg, k_gemv_decode<MT, J, true>, a);
 }
 
 cudaError_t dispatch(int mt, int j, bool coop, const Args& a, int ctas, size_t smem,

@@ -314,6 +314,35 @@ def test_decode_chain_matches_separate_calls():
                 assert_bits_equal(host(t[2]), y_o, f"run {run} phase {i} target {j} y")
 
 
+def test_decode_chain_phases_without_rows():
+    """Phases so small that most CTAs own no row in them, first, last and
+    several in a row: every output still matches the oracle (the grid barrier
+    counts the CTAs that have nothing to do)."""
+    M = 1
+    spec = [(192, [5]), (192, [7]), (2560, [2560]), (64, [3]), (64, [2]), (128, [1]),
+            (2560, [640]), (64, [4])]
+    phases, refs = [], []
+    for i, (K, Ns) in enumerate(spec):
+        x = synth.tokens_bf16(M, K, seed=1200 + i)
+        qx, sx = oracle.quantize_act_bf16(x)
+        targets, want = [], []
+        for j, N in enumerate(Ns):
+            Wq, ws, _ = oracle.quantize_weights(synth.weights_f32(N, K, seed=1300 + 10 * i + j))
+            targets.append((dev(Wq), dev(np.array([ws], np.float32)),
+                            torch.empty((M, N), dtype=torch.float32, device="cuda")))
+            want.append(oracle.linear(Wq, ws, qx, sx, K)[0])
+        phases.append((dev_bf16(x), targets))
+        refs.append(want)
+    chain = bn.bitnet_decode_chain_build(phases)
+    for run in range(3):
+        bn.bitnet_decode_chain_run(chain)
+    torch.cuda.synchronize()
+    assert bn.bitnet_device_error() == 0
+    for i, ((_, tg), want) in enumerate(zip(phases, refs)):
+        for t, y_o in zip(tg, want):
+            assert_bits_equal(host(t[2]), y_o, f"phase {i} y")
+
+
 @pytest.mark.parametrize("M", [2, 3])
 def test_decode_chain_multi_token(M):
     spec = [(2560, [2560, 640]), (6912, [2560]), (2560, [6912])]
