@@ -848,6 +848,44 @@ cudaError_t dispatch(int mt, int j, bool coop, const Args& a, int ctas, size_t s
   return cudaErrorNotSupported;
 }
 
+// Shared memory of an SM and the fixed part of one single-phase CTA (its
+// static arrays plus the per-block reservation), for the variant (mt, j).
+template <int MT, int J>
+cudaError_t fixed_smem(size_t* fixed) {
+  static size_t cached[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 64 && cached[dev]) {
+    *fixed = cached[dev];
+    return cudaSuccess;
+  }
+  cudaFuncAttributes fa;
+  e = cudaFuncGetAttributes(&fa, k_gemv_decode<MT, J, false>);
+  int reserved = 0;
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev);
+  if (e != cudaSuccess) return e;
+  *fixed = fa.sharedSizeBytes + (size_t)reserved;
+  if (dev < 64) cached[dev] = *fixed;
+  return cudaSuccess;
+}
+
+cudaError_t sm_smem(size_t* cap) {
+  int dev = 0, v = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+  *cap = (size_t)v;
+  return e;
+}
+
+cudaError_t variant_fixed_smem(int mt, int j, size_t* fixed) {
+  if (mt == 1 && j == 2) return fixed_smem<1, 2>(fixed);
+  if (mt == 1 && j == 4) return fixed_smem<1, 4>(fixed);
+  if (mt == 2 && j == 2) return fixed_smem<2, 2>(fixed);
+  if (mt == 4 && j == 1) return fixed_smem<4, 1>(fixed);
+  return cudaErrorNotSupported;
+}
+
 // Fills a Phase from the host description; rows split over `ctas` CTAs.
 bool fill_phase(const DecodeTarget* targets, int count, const int8_t* xq, const float* x_scale,
                 const uint16_t* x_bf16, int64_t K, const PhasePlan& pp, int ctas,
@@ -901,8 +939,21 @@ cudaError_t launch_decode(const DecodeTarget* targets, int count, const int8_t* 
   for (int p = 0; p < count; ++p) rows += targets[p].N;
   // One CTA per SM leaves room for the next decode kernel to start alongside
   // (programmatic dependent launch); large matrices take two per SM for more
-  // warps and copies in flight.
-  const int64_t max_ctas = rows * (K / 4) >= ((int64_t)16 << 20) ? 296 : 148;
+  // warps and copies in flight, with the ring shortened (to no fewer than two
+  // stages) until two CTAs fit in an SM's shared memory.
+  bool two = rows * (K / 4) >= ((int64_t)16 << 20);
+  if (two) {
+    size_t cap = 0, fixed = 0;
+    cudaError_t e = sm_smem(&cap);
+    if (e == cudaSuccess) e = variant_fixed_smem(pl.mt, pl.j, &fixed);
+    if (e != cudaSuccess) return e;
+    while (pl.stages > 2 && 2 * (pl.smem + fixed) > cap) {
+      --pl.stages;
+      pl.smem -= (size_t)pl.pp.stage_bytes;
+    }
+    two = 2 * (pl.smem + fixed) <= cap;
+  }
+  const int64_t max_ctas = two ? 296 : 148;
   int64_t ctas = rows < max_ctas ? rows : max_ctas;
   const int64_t rpc = (rows + ctas - 1) / ctas;
   ctas = (rows + rpc - 1) / rpc;
