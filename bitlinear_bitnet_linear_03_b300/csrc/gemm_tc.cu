@@ -84,11 +84,26 @@ constexpr int kMmaKBytes = 32;
 struct Args {
   int M, N, K;
   int m_tiles, n_tiles, k_stages;
+  // Split K: work item i is tile i % tiles, K stages [s * kps, (s + 1) * kps)
+  // of split s = i / tiles.  With splits > 1 every split adds its exact
+  // partial sums into acc_ws [M, N] (zeroed by the pre-pass) and the last
+  // split of a tile to finish (counted in tile_cnt) writes the outputs.
+  int splits, kps;
+  float* acc_ws;
+  int* tile_cnt;
   const float* x_scale;
   const float* w_scale;
   float* y;
   int32_t* acc_out;
 };
+
+// Work item -> tile and K-stage range.
+__device__ __forceinline__ void item_range(const Args& a, int item, int& tile, int& ks0, int& ks1) {
+  const int tiles = a.m_tiles * a.n_tiles;
+  tile = item % tiles;
+  ks0 = (item / tiles) * a.kps;
+  ks1 = min(a.k_stages, ks0 + a.kps);
+}
 
 // ---- PTX wrappers (PTX ISA: mbarrier, cp.async.bulk.tensor, tcgen05)
 __device__ __forceinline__ uint32_t saddr(const void* p) {
@@ -177,7 +192,63 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-__device__ __forceinline__ uint32_t bf16_pair_from_codes(uint32_t p);
+// Epilogue warps (2-5): named barrier 2 over their 128 threads, optionally
+// OR-reducing a flag (uniform result).
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
+__device__ __forceinline__ bool epi_sync_or(bool flag) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, 2, 128, p;\n"
+      " selp.u32 %0, 1, 0, q;\n}"
+      : "=r"(r)
+      : "r"((uint32_t)flag)
+      : "memory");
+  return r != 0;
+}
+__device__ __forceinline__ void red_add_v4(float* p, uint32_t a, uint32_t b, uint32_t c,
+                                           uint32_t d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(__uint_as_float(a)),
+               "f"(__uint_as_float(b)), "f"(__uint_as_float(c)), "f"(__uint_as_float(d))
+               : "memory");
+}
+__device__ __forceinline__ float ld_cg_f32(const float* p) {
+  float v;
+  asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(p) : "memory");
+  return v;
+}
+// y = acc * c and the accumulators for 32 consecutive outputs of one row.
+__device__ __forceinline__ void store_row32(float* yrow, int32_t* arow, int nb, const int (&v)[32],
+                                            float c, bool full_vec, int N) {
+  if (full_vec) {
+#pragma unroll
+    for (int j = 0; j < 32; j += 4) {
+      float4 o = make_float4(__fmul_rn(__int2float_rn(v[j]), c), __fmul_rn(__int2float_rn(v[j + 1]), c),
+                             __fmul_rn(__int2float_rn(v[j + 2]), c),
+                             __fmul_rn(__int2float_rn(v[j + 3]), c));
+      *reinterpret_cast<float4*>(yrow + nb + j) = o;
+      if (arow) *reinterpret_cast<int4*>(arow + nb + j) = make_int4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (nb + j < N) {
+        yrow[nb + j] = __fmul_rn(__int2float_rn(v[j]), c);
+        if (arow) arow[nb + j] = v[j];
+      }
+  }
+}
+
+// Four bf16 values (two words, in order) from four 2-bit codes held in the
+// low bits of the bytes of u: code 0, 1, 2 -> q = -1, 0, +1 -> 0xBF80, 0x0000,
+// 0x3F80 (exact).  Each code c becomes the byte selectors 4 + c (low byte,
+// from the table 0x80, 0x00, 0x80) and c (high byte, from 0xBF, 0x00, 0x3F)
+// of one byte permute: u * 0x11 puts c in both nibbles of its byte (no
+// carries, c <= 2) and + 0x04 sets the low nibble's table bit.
+__device__ __forceinline__ void bf16x4_from_codes(uint32_t u, uint32_t& lo, uint32_t& hi) {
+  const uint32_t sel = u * 0x11u + 0x04040404u;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(lo) : "r"(0x003F00BFu), "r"(0x00800080u), "r"(sel));
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(hi) : "r"(0x003F00BFu), "r"(0x00800080u), "r"(sel >> 16));
+}
 
 // Expands the packed 2-bit codes of one stage (BN rows x 64 weights, 16
 // bytes per row) into the bf16 B tile in the 128-byte-swizzled K-major
@@ -196,12 +267,9 @@ __device__ __forceinline__ void expand_b_tile(uint32_t packed, uint32_t btile, i
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
       const int sft = 2 * (c >> 1), h = c & 1;
-      const uint32_t u0 = (ww[2 * h] >> sft) & 0x03030303u;
-      const uint32_t u1 = (ww[2 * h + 1] >> sft) & 0x03030303u;
-      const uint32_t o0 = bf16_pair_from_codes((u0 & 3u) | ((u0 & 0x300u) << 8));
-      const uint32_t o1 = bf16_pair_from_codes(((u0 >> 16) & 3u) | ((u0 >> 8) & 0x30000u));
-      const uint32_t o2 = bf16_pair_from_codes((u1 & 3u) | ((u1 & 0x300u) << 8));
-      const uint32_t o3 = bf16_pair_from_codes(((u1 >> 16) & 3u) | ((u1 >> 8) & 0x30000u));
+      uint32_t o0, o1, o2, o3;
+      bf16x4_from_codes((ww[2 * h] >> sft) & 0x03030303u, o0, o1);
+      bf16x4_from_codes((ww[2 * h + 1] >> sft) & 0x03030303u, o2, o3);
       asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(rowbase + 16u * (uint32_t)(c ^ (r & 7))),
                    "r"(o0), "r"(o1), "r"(o2), "r"(o3)
                    : "memory");
@@ -228,7 +296,8 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUte
 
   const uint32_t smem0 = (saddr(smem_raw) + 1023u) & ~1023u;  // 1024-byte aligned tiles
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int tiles = a.m_tiles * a.n_tiles;
+  const int items = a.m_tiles * a.n_tiles * a.splits;
+  __shared__ int s_last;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -262,9 +331,11 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUte
     if (lane == 0) {
       int it = 0, issued = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+      for (int item = blockIdx.x; item < items && ok; item += gridDim.x) {
+        int t, ks0, ks1;
+        item_range(a, item, t, ks0, ks1);
         const int m0 = (t % a.m_tiles) * kBM, n0 = (t / a.m_tiles) * BN;
-        for (int ks = 0; ks < a.k_stages; ++ks, ++it) {
+        for (int ks = ks0; ks < ks1; ++ks, ++it) {
           const int s = it % kStages;
           if (it >= kStages && !mbar_wait(saddr(&empty_bar[s]), ((it / kStages) - 1) & 1)) {
             atomicOr(&g_device_error, kErrProducer);
@@ -304,7 +375,10 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUte
     if (lane == 0) {
       int it = 0, lt = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x, ++lt) {
+      for (int item = blockIdx.x; item < items && ok; item += gridDim.x, ++lt) {
+        int t, ks0, ks1;
+        item_range(a, item, t, ks0, ks1);
+        (void)t;
         const int ab = lt & 1;
         if (lt >= 2 && !mbar_wait(saddr(&acc_empty[ab]), ((lt >> 1) - 1) & 1)) {
           atomicOr(&g_device_error, kErrMma);
@@ -313,7 +387,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUte
         }
         tc_fence_after();
         const uint32_t d = tmem + (uint32_t)(ab * BN);
-        for (int ks = 0; ks < a.k_stages; ++ks, ++it) {
+        for (int ks = ks0; ks < ks1; ++ks, ++it) {
           const int s = it % kStages;
           const uint32_t ready = FUSED ? saddr(&bready_bar[s]) : saddr(&full_bar[s]);
           if (!mbar_wait(ready, (it / kStages) & 1) || *(volatile int*)&s_abort) {
@@ -328,7 +402,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUte
           for (int kk = 0; kk < kRowBytes / kMmaKBytes; ++kk) {
             const uint64_t ad = sw128_desc(sa + kk * kMmaKBytes);
             const uint64_t bd = sw128_desc(sa + kATileBytes + kk * kMmaKBytes);
-            tc_mma<KIND, BN>(d, ad, bd, (ks | kk) != 0 ? 1u : 0u);
+            tc_mma<KIND, BN>(d, ad, bd, (ks != ks0 || kk != 0) ? 1u : 0u);
           }
           tc_commit(saddr(&empty_bar[s]));  // frees the stage when these MMAs finish
         }
@@ -343,9 +417,12 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUte
     // ------------------------------------------------------------ B expansion
     const int ct = threadIdx.x - 6 * 32;  // 0 .. 127
     int it = 0;
-    for (int t = blockIdx.x; t < tiles; t += gridDim.x) {
+    for (int item = blockIdx.x; item < items; item += gridDim.x) {
+      int t, ks0, ks1;
+      item_range(a, item, t, ks0, ks1);
+      (void)t;
       bool ok = true;
-      for (int ks = 0; ks < a.k_stages; ++ks, ++it) {
+      for (int ks = ks0; ks < ks1; ++ks, ++it) {
         const int s = it % kStages;
         if (!mbar_wait(saddr(&full_bar[s]), (it / kStages) & 1) || *(volatile int*)&s_abort) {
           if (lane == 0) atomicOr(&g_device_error, kErrProducer);
@@ -368,9 +445,13 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUte
     const int row = quarter * 32 + lane;
     const float ws = *a.w_scale;
     int lt = 0;
-    for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++lt) {
+    for (int item = blockIdx.x; item < items; item += gridDim.x, ++lt) {
+      int t, ks0, ks1;
+      item_range(a, item, t, ks0, ks1);
       const int ab = lt & 1;
-      if (!mbar_wait(saddr(&acc_full[ab]), (lt >> 1) & 1) || *(volatile int*)&s_abort) {
+      const bool bad =
+          !mbar_wait(saddr(&acc_full[ab]), (lt >> 1) & 1) || *(volatile int*)&s_abort;
+      if (epi_sync_or(bad)) {  // uniform over the epilogue warps
         if (lane == 0) atomicOr(&g_device_error, kErrEpilogue);
         *(volatile int*)&s_abort = 1;
         break;
@@ -382,38 +463,56 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUte
       const float c = mrow ? __fmul_rn(a.x_scale[m], ws) : 0.0f;
       float* yrow = a.y + (int64_t)m * a.N;
       int32_t* arow = a.acc_out ? a.acc_out + (int64_t)m * a.N : nullptr;
+      float* wrow = a.acc_ws + (int64_t)m * a.N;
       const bool vec = (a.N & 3) == 0;
       for (int cb = 0; cb < BN; cb += 32) {
         uint32_t r[32];
         tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(ab * BN + cb), r);
         if (!mrow) continue;
+        const int nb = n0 + cb;
+        if (a.splits > 1) {
+          // Add this split's exact partial sums (integers below 2^24 in
+          // magnitude, whatever the order: fp32 addition is exact here).
+          if (vec && nb + 32 <= a.N) {
+#pragma unroll
+            for (int j = 0; j < 32; j += 4)
+              red_add_v4(wrow + nb + j, r[j], r[j + 1], r[j + 2], r[j + 3]);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (nb + j < a.N) atomicAdd(wrow + nb + j, __uint_as_float(r[j]));
+          }
+          continue;
+        }
         int v[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j)
           v[j] = __float2int_rn(__uint_as_float(r[j]));  // exact integer
-        const int nb = n0 + cb;
-        if (vec && nb + 32 <= a.N) {
-#pragma unroll
-          for (int j = 0; j < 32; j += 4) {
-            float4 o = make_float4(__fmul_rn(__int2float_rn(v[j]), c),
-                                   __fmul_rn(__int2float_rn(v[j + 1]), c),
-                                   __fmul_rn(__int2float_rn(v[j + 2]), c),
-                                   __fmul_rn(__int2float_rn(v[j + 3]), c));
-            *reinterpret_cast<float4*>(yrow + nb + j) = o;
-            if (arow) *reinterpret_cast<int4*>(arow + nb + j) = make_int4(v[j], v[j + 1], v[j + 2], v[j + 3]);
-          }
-        } else {
-#pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (nb + j < a.N) {
-              yrow[nb + j] = __fmul_rn(__int2float_rn(v[j]), c);
-              if (arow) arow[nb + j] = v[j];
-            }
-        }
+        store_row32(yrow, arow, nb, v, c, vec && nb + 32 <= a.N, a.N);
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(saddr(&acc_empty[ab]));
+      if (a.splits > 1) {
+        // The last split of the tile to finish writes the outputs.
+        __threadfence();
+        epi_sync();
+        if (threadIdx.x == 64) s_last = atomicAdd(&a.tile_cnt[t], 1) == a.splits - 1;
+        epi_sync();
+        if (s_last) {
+          __threadfence();
+          if (mrow)
+            for (int cb = 0; cb < BN; cb += 32) {
+              const int nb = n0 + cb;
+              if (nb >= a.N) break;
+              int v[32];
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                v[j] = nb + j < a.N ? __float2int_rn(ld_cg_f32(wrow + nb + j)) : 0;
+              store_row32(yrow, arow, nb, v, c, vec && nb + 32 <= a.N, a.N);
+            }
+        }
+      }
     }
   }
 
@@ -427,24 +526,17 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUte
 }
 
 // ---- pre-pass kernels
-// Two bf16 values from two 2-bit codes held at bits 0-1 and 16-17 of p:
-// code 0, 1, 2 -> q = -1, 0, +1 -> 0xBF80, 0x0000, 0x3F80 (exact).
-__device__ __forceinline__ uint32_t bf16_pair_from_codes(uint32_t p) {
-  const uint32_t t = p ^ 0x00010001u;
-  const uint32_t nz = (t | (t >> 1)) & 0x00010001u;    // code != 1
-  const uint32_t neg = ~(p | (p >> 1)) & 0x00010001u;  // code == 0
-  return nz * 0x3F80u | (neg << 15);
-}
-
-// Pre-pass, one launch: items [0, nblk) expand a 16-byte packed block (64
+// Pre-pass, one launch (items [nblk + nx, + nz) zero 16 bytes of the split-K
+// workspace each): items [0, nblk) expand a 16-byte packed block (64
 // weights) of Wq into 128 bytes of bf16 B; items [nblk, nblk + nx) widen 16
 // int8 activations into 32 bytes of bf16 A.  In a packed block, chunk c of 8
 // consecutive weights (k = 8c .. 8c+7) is field s = c/2 of words 2(c%2) and
 // 2(c%2)+1.  All stores are 16 bytes wide.
 __global__ void __launch_bounds__(256)
 k_prepass(const uint4* __restrict__ Wq, int64_t nblk, uint4* __restrict__ B,
-          const uint4* __restrict__ xq, int64_t nx, uint4* __restrict__ A) {
-  const int64_t total = nblk + nx;
+          const uint4* __restrict__ xq, int64_t nx, uint4* __restrict__ A,
+          uint4* __restrict__ zero, int64_t nz) {
+  const int64_t total = nblk + nx + nz;
   for (int64_t it = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; it < total;
        it += (int64_t)gridDim.x * blockDim.x) {
     if (it < nblk) {
@@ -453,15 +545,13 @@ k_prepass(const uint4* __restrict__ Wq, int64_t nblk, uint4* __restrict__ B,
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
         const int sft = 2 * (c >> 1), h = c & 1;
-        const uint32_t u0 = (ww[2 * h] >> sft) & 0x03030303u;
-        const uint32_t u1 = (ww[2 * h + 1] >> sft) & 0x03030303u;
         uint4 o;
-        o.x = bf16_pair_from_codes((u0 & 3u) | ((u0 & 0x300u) << 8));
-        o.y = bf16_pair_from_codes(((u0 >> 16) & 3u) | ((u0 >> 8) & 0x30000u));
-        o.z = bf16_pair_from_codes((u1 & 3u) | ((u1 & 0x300u) << 8));
-        o.w = bf16_pair_from_codes(((u1 >> 16) & 3u) | ((u1 >> 8) & 0x30000u));
+        bf16x4_from_codes((ww[2 * h] >> sft) & 0x03030303u, o.x, o.y);
+        bf16x4_from_codes((ww[2 * h + 1] >> sft) & 0x03030303u, o.z, o.w);
         B[it * 8 + c] = o;
       }
+    } else if (it >= nblk + nx) {
+      zero[it - nblk - nx] = make_uint4(0, 0, 0, 0);  // split-K sums and tile counters
     } else {
       const int64_t i = it - nblk;
       const uint4 v = xq[i];
@@ -535,22 +625,59 @@ constexpr int kKind = 1;
 
 size_t round1k(size_t v) { return (v + 1023) / 1024 * 1024; }
 
+bool use_fused_m(int64_t M) { return M <= 256; }
+
+// Workspace of one call: [B bf16 N x K (unfused only)] [A bf16 M x K]
+// [split-K sums M x N fp32] [tile counters], each 1 KB aligned.  Split K
+// (fused path only) when the output has fewer tiles than half the SMs: as
+// many splits as fill the SMs, each at least 16 K stages.
+struct WsLayout {
+  size_t b, a, acc, cnt, end;
+  int splits, kps;
+};
+WsLayout ws_layout(int64_t M, int64_t N, int64_t K) {
+  WsLayout L = {};
+  const bool fused = use_fused_m(M);
+  const int bn = fused ? 256 : (N <= 128 ? 128 : 256);
+  const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + bn - 1) / bn);
+  const int k_stages = (int)((K + 63) / 64);
+  int splits = 1;
+  if (fused && tiles < 74) {
+    splits = (int)(148 / tiles);
+    if (splits > k_stages / 16) splits = k_stages / 16;
+    if (splits < 1) splits = 1;
+  }
+  L.kps = (k_stages + splits - 1) / splits;
+  L.splits = (k_stages + L.kps - 1) / L.kps;
+  L.b = 0;
+  L.a = fused ? 0 : round1k((size_t)(N * K * 2));
+  L.acc = L.a + round1k((size_t)(M * K * 2));
+  L.cnt = L.acc + (L.splits > 1 ? round1k((size_t)(M * N * 4)) : 0);
+  L.end = L.cnt + (L.splits > 1 ? round1k((size_t)tiles * 4) : 0);
+  return L;
+}
+
 template <int KIND, int BN, bool FUSED>
 cudaError_t launch_kind(const uint8_t* Wq, const float* w_scale, const int8_t* xq,
                         const float* x_scale, int64_t M, int64_t N, int64_t K, float* y,
                         int32_t* acc_out, void* ws, cudaStream_t s) {
   cudaError_t e = get_encode();
   if (e != cudaSuccess) return e;
+  const WsLayout L = ws_layout(M, N, K);
   uint8_t* w = static_cast<uint8_t*>(ws);
-  void* B = w;
-  void* A = FUSED ? w : w + round1k((size_t)(N * K * 2));
+  void* B = w + L.b;
+  void* A = w + L.a;
+  float* acc_ws = reinterpret_cast<float*>(w + L.acc);
+  int* tile_cnt = reinterpret_cast<int*>(w + L.cnt);
   const int64_t nblk = FUSED ? 0 : N * K / 64, nx = M * K / 16;
-  int64_t grid = (nblk + nx + 255) / 256;
+  const int64_t nz = L.splits > 1 ? (int64_t)(L.end - L.acc) / 16 : 0;
+  int64_t grid = (nblk + nx + nz + 255) / 256;
   if (grid > 148 * 16) grid = 148 * 16;
   k_prepass<<<(unsigned)grid, 256, 0, s>>>(reinterpret_cast<const uint4*>(Wq), nblk,
                                            reinterpret_cast<uint4*>(B),
                                            reinterpret_cast<const uint4*>(xq), nx,
-                                           reinterpret_cast<uint4*>(A));
+                                           reinterpret_cast<uint4*>(A),
+                                           reinterpret_cast<uint4*>(w + L.acc), nz);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   CUtensorMap mapA, mapB;
@@ -566,6 +693,10 @@ cudaError_t launch_kind(const uint8_t* Wq, const float* w_scale, const int8_t* x
   a.m_tiles = (int)((M + kBM - 1) / kBM);
   a.n_tiles = (int)((N + BN - 1) / BN);
   a.k_stages = (int)((K + Kind<KIND>::kKStage - 1) / Kind<KIND>::kKStage);
+  a.splits = L.splits;
+  a.kps = L.kps;
+  a.acc_ws = acc_ws;
+  a.tile_cnt = tile_cnt;
   a.x_scale = x_scale;
   a.w_scale = w_scale;
   a.y = y;
@@ -581,8 +712,8 @@ cudaError_t launch_kind(const uint8_t* Wq, const float* w_scale, const int8_t* x
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
-  const int tiles = a.m_tiles * a.n_tiles;
-  const int ctas = tiles < 148 ? tiles : 148;
+  const int items = a.m_tiles * a.n_tiles * a.splits;
+  const int ctas = items < 148 ? items : 148;
   return launch_pdl(k_gemm_tc<KIND, BN, FUSED>, dim3(ctas),
                     dim3(FUSED ? kThreadsFused : kThreads), (size_t)Tile<BN, FUSED>::kSmemBytes, s,
                     mapA, mapB, a);
@@ -606,12 +737,9 @@ bool gemm_tc_eligible(int64_t M, int64_t N, int64_t K) {
 // Small batches expand the packed weights on chip (streaming 2 bits per
 // weight from HBM); large ones expand them once into a bf16 copy that stays
 // in L2 across the many output-tile rows.
-bool use_fused(int64_t M) { return M <= 256; }
+bool use_fused(int64_t M) { return use_fused_m(M); }
 
-size_t gemm_tc_workspace(int64_t M, int64_t N, int64_t K) {
-  if (use_fused(M)) return round1k((size_t)(M * K * 2));
-  return round1k((size_t)(N * K * 2)) + round1k((size_t)(M * K * 2));
-}
+size_t gemm_tc_workspace(int64_t M, int64_t N, int64_t K) { return ws_layout(M, N, K).end; }
 
 cudaError_t launch_gemm_tc(const uint8_t* Wq, const float* w_scale, const int8_t* xq,
                            const float* x_scale, int64_t M, int64_t N, int64_t K, float* y,

@@ -149,7 +149,9 @@ def gpu_linear(Wq, ws, qx, sx, K):
 LINEAR_SHAPES = [(1, 1, 64), (1, 7, 64), (2, 65, 192), (3, 640, 2560), (1, 2560, 2560),
                  (5, 2560, 2560), (8, 6912, 2560), (1, 2560, 6912), (17, 2560, 6912),
                  (4, 100, 8192), (63, 96, 2560), (64, 33, 128), (65, 130, 640), (129, 64, 320),
-                 (1, 31, 65536)]
+                 (1, 31, 65536),
+                 # tensor-core path with K split over several CTAs (few output tiles)
+                 (20, 300, 4096), (64, 33, 8192), (200, 777, 2048), (16, 2560, 4096)]
 
 
 @pytest.mark.parametrize("M,N,K", LINEAR_SHAPES)
