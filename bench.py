@@ -59,6 +59,9 @@ def parse_args():
                          "bitnet_quantize_act + bitnet_linear per matrix")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--case", default=None, choices=["prefill", "gemv100b", "fused_small_m"],
+                    help="run only this secondary measurement and print it (for profiling "
+                         "one kernel under ncu)")
     return ap.parse_args()
 
 
@@ -321,7 +324,7 @@ def _weight_sets(torch, bn, synth, N, K, count, seed):
     return sets
 
 
-def secondary_measurements(torch, bn, peaks):
+def secondary_measurements(torch, bn, peaks, only=None):
     """The other workloads, each timed with CUDA events after warm-up, weights
     rotated over enough distinct sets that every timed call streams from HBM
     (more than the 126 MB L2 between reuses), inputs resident:
@@ -346,29 +349,38 @@ def secondary_measurements(torch, bn, peaks):
                 "frac": round(tops / tpk, 4),
                 "peak_source": "measured bf16 dense (no int8 tensor MMA on sm_103a)"}
 
+    def want(case):
+        return only is None or only == case
+
     # single GEMV 2560x2560, M = 1
     N = K = 2560
-    sets = _weight_sets(torch, bn, synth, N, K, 80, 100)
-    x = synth.tokens_bf16(1, K, seed=0, device="cuda")
-    y = torch.empty((1, N), dtype=torch.float32, device=dev)
-    t = _time_calls(torch, lambda i: bn.bitnet_linear_bf16(x, [(sets[i % 80][0], sets[i % 80][1], y)],
-                                                         weights_static=True), 400, graph=True)
-    byts = N * K // 4 + 2 * K + 4 + 4 * N
-    out["gemv_2560x2560_M1"] = {"us": round(t * 1e6, 2), "GBps": round(byts / t / 1e9, 1),
-                                "roofline": hbm_roof(byts / t / 1e9)}
-    del sets
+    if not want("gemv2560"):
+        N = K = 0
+    if N:
+        sets = _weight_sets(torch, bn, synth, N, K, 80, 100)
+        x = synth.tokens_bf16(1, K, seed=0, device="cuda")
+        y = torch.empty((1, N), dtype=torch.float32, device=dev)
+        t = _time_calls(torch, lambda i: bn.bitnet_linear_bf16(
+            x, [(sets[i % 80][0], sets[i % 80][1], y)], weights_static=True), 400, graph=True)
+        byts = N * K // 4 + 2 * K + 4 + 4 * N
+        out["gemv_2560x2560_M1"] = {"us": round(t * 1e6, 2), "GBps": round(byts / t / 1e9, 1),
+                                    "roofline": hbm_roof(byts / t / 1e9)}
+        del sets
 
-    # 100B-class shapes
-    for (N, K) in [(28672, 8192), (8192, 28672)]:
+    # 100B-class shapes (each timed as a CUDA graph of calls: the host's
+    # launch cost stays out of the device time)
+    ms_100b = [m for m, c in ((1, "gemv100b"), (4, "gemv100b"), (16, "fused_small_m"),
+                              (64, "fused_small_m")) if want(c)]
+    for (N, K) in ([(28672, 8192), (8192, 28672)] if ms_100b else []):
         sets = _weight_sets(torch, bn, synth, N, K, 3, 200)
-        for M in (1, 4, 16, 64):
+        for M in ms_100b:
             x = synth.tokens_bf16(M, K, seed=1, outlier_frac=0.01, device="cuda")
             xq, sx = bn.bitnet_quantize_act(x)
             y = torch.empty((M, N), dtype=torch.float32, device=dev)
             ws = torch.empty(max(bn.bitnet_linear_workspace(M, N, K), 16), dtype=torch.uint8,
                              device=dev)
             t = _time_calls(torch, lambda i: bn.bitnet_linear(sets[i % 3][0], sets[i % 3][1], xq, sx,
-                                                              y=y, ws=ws), 12)
+                                                              y=y, ws=ws), 12, graph=True)
             byts = N * K // 4 + M * K + 4 * M * N + 4 * M + 4
             out[f"100b_M{M}_K{K}_N{N}"] = {
                 "us": round(t * 1e6, 1), "GBps": round(byts / t / 1e9, 1),
@@ -377,7 +389,7 @@ def secondary_measurements(torch, bn, peaks):
         del sets
 
     # prefill
-    for (N, K) in [(6912, 2560), (2560, 6912)]:
+    for (N, K) in ([(6912, 2560), (2560, 6912)] if want("prefill") else []):
         M = 4096
         sets = _weight_sets(torch, bn, synth, N, K, 4, 500)
         x = synth.tokens_bf16(M, K, seed=600, device="cuda")
@@ -394,7 +406,7 @@ def secondary_measurements(torch, bn, peaks):
 
     # fused FFN
     H, F = 2560, 6912
-    for M, nsets, reps in [(1, 10, 200), (4096, 2, 6)]:
+    for M, nsets, reps in ([(1, 10, 200), (4096, 2, 6)] if want("ffn") else []):
         ffn_sets = []
         for r in range(nsets):
             ffn_sets.append([bn.bitnet_quantize_weights(synth.weights_f32(n_, k_, seed=700 + 3 * r + j,
@@ -627,6 +639,12 @@ def main():
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         return float(t.item())
 
+    if args.case is not None:
+        import bitlinear_bitnet_linear_03_b300 as bn
+        bn.lib()
+        print(json.dumps(secondary_measurements(torch, bn, read_peaks(), only=args.case)),
+              flush=True)
+        return
     res = run_gpu_arm(args, rank, world, barrier, max_over_ranks)
     if rank == 0:
         if not args.no_cpu_baseline:

@@ -12,14 +12,21 @@
 // order of the additions; the epilogue converts it back to int32 without
 // rounding.
 //
-// Pipeline (one CTA per SM, persistent over 128 x BN output tiles, BN = 256,
-// or 128 for narrow N):
-//  * pre-pass kernels expand the packed 2-bit weights once per call into a
-//    K-major bf16 operand B [N, K] and the int8 activations into A [M, K]
+// Pipeline (one CTA per SM, persistent over work items of 128 x BN output
+// tiles, BN = 256, or 128 for narrow N):
+//  * M <= 256 (fused): the TMA brings the A tile (bf16) and the packed 2-bit
+//    codes of the B tile (16 bytes per row per stage); four converter warps
+//    expand the codes into the 128-byte-swizzled bf16 B tile in shared memory
+//    (one multiply-add and two byte permutes per four weights) and signal the
+//    MMA.  When the output has fewer tiles than half the SMs, K is split over
+//    CTAs: each split adds its exact partial sums into a zeroed fp32
+//    workspace (red.global.add.v4.f32; all values are integers below 2^24)
+//    and the last split of a tile to finish writes the outputs;
+//  * M > 256: pre-pass kernels expand the packed weights once per call into
+//    a K-major bf16 operand B [N, K] and the int8 activations into A [M, K]
 //    bf16, both in the workspace (and largely in L2 during the GEMM);
 //  * warp 0, one lane: TMA (cp.async.bulk.tensor.2d, 128-byte swizzle) loads
-//    the A and B tiles of each 128-byte K step into a 192 KB ring (4 stages
-//    for 256-wide tiles, 6 for 128-wide ones);
+//    the tiles of each 128-byte K step into a 192 KB ring;
 //  * warp 1: allocates 512 TMEM columns (two 256-column fp32
 //    accumulators) and one lane issues tcgen05.mma for each stage, releasing
 //    the stage with tcgen05.commit;

@@ -22,12 +22,22 @@
 //    64-weight chunks l, l+32, ... of its K part for the whole kernel: their
 //    int8 activations are loaded into registers once, and a row costs the
 //    lane one 16-byte shared load, 16 ANDs and 16 dp4a per chunk; the 32
-//    lanes read 512 contiguous bytes of the row.  A row's lane sums meet in
-//    one warp reduction (redux.sync); with wk > 1 the K parts meet in a
-//    64-bit shared-memory atomic per row that also counts the parts, and the
-//    last part to arrive writes the row (no barrier between warps).
+//    lanes read 512 contiguous bytes of the row.  Rows go two at a time, their
+//    dp4a chains interleaved.  A row's lane sums meet in one warp reduction
+//    (redux.sync).
+//  * Single launch: the consumers store each row's K-part result in shared
+//    memory and release the slot; the producer warp, when it takes the slot
+//    back for a new copy, sums the parts and writes the stage's outputs
+//    (rows across its lanes, coalesced).  The consumers' per-stage work is
+//    then only the dot products.
+//  * Chain of phases (one CTA per SM, grid barrier between phases): the
+//    consumers write the outputs themselves, so the barrier arrival follows
+//    the last stage directly; with wk > 1 the K parts meet in a 64-bit
+//    shared-memory atomic per row that also counts the parts, and the last
+//    part to arrive writes the row.
 //  * Before waiting on the previous kernel the CTA asks for its whole weight
-//    range to be prefetched into L2 and lets its successor launch:
+//    range and its input to be prefetched into L2 and lets its successor
+//    launch:
 //    consecutive decode kernels overlap under programmatic dependent launch.
 //    Weights are read after that wait, unless the caller declared them
 //    static (not written by any work still in flight): then the producer
@@ -653,7 +663,8 @@ k_gemv_decode(const __grid_constant__ Args a) {
       const int my_rows = nrows == ph.rows_per_stage
                               ? full_rows
                               : (nrows > wr ? (nrows - wr + nwr - 1) / nwr : 0);
-      int vals[kMaxRowsPerWarp][MT];
+      // Lane q*MT + m keeps the (warp-uniform) sum of row q for token m.
+      int tot = 0;
 #pragma unroll
       for (int q = 0; q < kMaxRowsPerWarp; q += 2) {
         if (q + 1 < my_rows) {
@@ -663,27 +674,25 @@ k_gemv_decode(const __grid_constant__ Args a) {
           row_partials<MT, J, 2>(w, valid_j, xr, v);
 #pragma unroll
           for (int m = 0; m < MT; ++m) {
-            vals[q][m] = __reduce_add_sync(0xffffffffu, v[0][m] - lsum[m]);
-            vals[q + 1][m] = __reduce_add_sync(0xffffffffu, v[1][m] - lsum[m]);
+            const int s0 = __reduce_add_sync(0xffffffffu, v[0][m] - lsum[m]);
+            const int s1 = __reduce_add_sync(0xffffffffu, v[1][m] - lsum[m]);
+            if (lane == q * MT + m) tot = s0;
+            if (lane == (q + 1) * MT + m) tot = s1;
           }
         } else if (q < my_rows) {
           const uint32_t w[1] = {sbase + (uint32_t)((wr + q * nwr) * row_bytes)};
           int v[1][MT];
           row_partials<MT, J, 1>(w, valid_j, xr, v);
 #pragma unroll
-          for (int m = 0; m < MT; ++m)
-            vals[q][m] = __reduce_add_sync(0xffffffffu, v[0][m] - lsum[m]);
+          for (int m = 0; m < MT; ++m) {
+            const int s0 = __reduce_add_sync(0xffffffffu, v[0][m] - lsum[m]);
+            if (lane == q * MT + m) tot = s0;
+          }
         }
       }
       // Lane q*MT + m finishes row q for token m: all rows of the stage at once.
       {
         const int q = lane / MT, m = lane % MT;
-        int tot = 0;
-#pragma unroll
-        for (int qq = 0; qq < kMaxRowsPerWarp; ++qq)
-#pragma unroll
-          for (int mm = 0; mm < MT; ++mm)
-            if (qq * MT + mm == lane) tot = vals[qq][mm];
         if (!CHAIN) {
           // The producer sums the K parts and writes the row.
           if (q < my_rows && q < kMaxRowsPerWarp)
@@ -848,25 +857,35 @@ cudaError_t dispatch(int mt, int j, bool coop, const Args& a, int ctas, size_t s
   return cudaErrorNotSupported;
 }
 
-// Shared memory of an SM and the fixed part of one single-phase CTA (its
-// static arrays plus the per-block reservation), for the variant (mt, j).
+// The fixed shared memory of one single-phase CTA (its static arrays plus the
+// per-block reservation) and how many CTAs of the variant (mt, j) the
+// registers allow per SM.
 template <int MT, int J>
-cudaError_t fixed_smem(size_t* fixed) {
+cudaError_t fixed_smem(size_t* fixed, int* reg_ctas) {
   static size_t cached[64] = {};
+  static int cached_ctas[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 64 && cached[dev]) {
     *fixed = cached[dev];
+    *reg_ctas = cached_ctas[dev];
     return cudaSuccess;
   }
   cudaFuncAttributes fa;
   e = cudaFuncGetAttributes(&fa, k_gemv_decode<MT, J, false>);
-  int reserved = 0;
+  int reserved = 0, regs_sm = 0;
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev);
   if (e != cudaSuccess) return e;
   *fixed = fa.sharedSizeBytes + (size_t)reserved;
-  if (dev < 64) cached[dev] = *fixed;
+  // registers are allocated per warp in units of 256
+  const int per_warp = (fa.numRegs * 32 + 255) / 256 * 256;
+  *reg_ctas = regs_sm / (per_warp * ((kThreads + 31) / 32));
+  if (dev < 64) {
+    cached[dev] = *fixed;
+    cached_ctas[dev] = *reg_ctas;
+  }
   return cudaSuccess;
 }
 
@@ -878,11 +897,11 @@ cudaError_t sm_smem(size_t* cap) {
   return e;
 }
 
-cudaError_t variant_fixed_smem(int mt, int j, size_t* fixed) {
-  if (mt == 1 && j == 2) return fixed_smem<1, 2>(fixed);
-  if (mt == 1 && j == 4) return fixed_smem<1, 4>(fixed);
-  if (mt == 2 && j == 2) return fixed_smem<2, 2>(fixed);
-  if (mt == 4 && j == 1) return fixed_smem<4, 1>(fixed);
+cudaError_t variant_fixed_smem(int mt, int j, size_t* fixed, int* reg_ctas) {
+  if (mt == 1 && j == 2) return fixed_smem<1, 2>(fixed, reg_ctas);
+  if (mt == 1 && j == 4) return fixed_smem<1, 4>(fixed, reg_ctas);
+  if (mt == 2 && j == 2) return fixed_smem<2, 2>(fixed, reg_ctas);
+  if (mt == 4 && j == 1) return fixed_smem<4, 1>(fixed, reg_ctas);
   return cudaErrorNotSupported;
 }
 
@@ -944,14 +963,17 @@ cudaError_t launch_decode(const DecodeTarget* targets, int count, const int8_t* 
   bool two = rows * (K / 4) >= ((int64_t)16 << 20);
   if (two) {
     size_t cap = 0, fixed = 0;
+    int reg_ctas = 0;
     cudaError_t e = sm_smem(&cap);
-    if (e == cudaSuccess) e = variant_fixed_smem(pl.mt, pl.j, &fixed);
+    if (e == cudaSuccess) e = variant_fixed_smem(pl.mt, pl.j, &fixed, &reg_ctas);
     if (e != cudaSuccess) return e;
-    while (pl.stages > 2 && 2 * (pl.smem + fixed) > cap) {
-      --pl.stages;
-      pl.smem -= (size_t)pl.pp.stage_bytes;
+    if (reg_ctas >= 2) {
+      while (pl.stages > 2 && 2 * (pl.smem + fixed) > cap) {
+        --pl.stages;
+        pl.smem -= (size_t)pl.pp.stage_bytes;
+      }
     }
-    two = 2 * (pl.smem + fixed) <= cap;
+    two = reg_ctas >= 2 && 2 * (pl.smem + fixed) <= cap;
   }
   const int64_t max_ctas = two ? 296 : 148;
   int64_t ctas = rows < max_ctas ? rows : max_ctas;
