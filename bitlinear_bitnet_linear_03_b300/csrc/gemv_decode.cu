@@ -66,6 +66,11 @@ constexpr int kMaxStages = 8;
 constexpr int kRingBudget = 96 * 1024;
 constexpr int kStageTarget = 24 * 1024;
 constexpr int kMaxRowsPerWarp = 8;         // rows of one stage handled by one warp
+// Stages of a phase the producer issues before the consumers have read that
+// phase's input x, so that the input's loads do not queue behind a full ring
+// of weight copies (measured on B300: 3-4% faster for a 58 MB matrix, neutral
+// for the 2B-shape chain).
+constexpr int kEarlyStages = 1;
 constexpr int kMaxSmem = 227 * 1024 - 10 * 1024;  // dynamic part; the static arrays fit in the rest
 constexpr int kPrefetchMax = 1 << 16;
 constexpr long long kWaitCycles = 2000000000ll;  // ~1 s at 2 GHz
@@ -320,6 +325,7 @@ k_gemv_decode(const __grid_constant__ Args a) {
   __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
   __shared__ float s_max[kConsumerWarps][MT];
   __shared__ int s_abort;
+  __shared__ int s_xgate;  // phases whose input x the consumers have read
   // The consumers' copy of the current phase descriptor (read in the hot
   // loop; shared memory instead of a pointer into the parameter block or the
   // chain table).
@@ -350,6 +356,7 @@ k_gemv_decode(const __grid_constant__ Args a) {
     }
     mbar_fence_init();
     s_abort = 0;
+    s_xgate = 0;
     // L2 prefetch hints for the first phase's input and weights (no data is
     // read before the dependency wait).
     prefetch_x(phases[0], a.M);
@@ -398,8 +405,26 @@ k_gemv_decode(const __grid_constant__ Args a) {
         prefetch_phase(phases[ph_i + 1]);
       }
       const int64_t row_bytes = ph.K >> 2;
+      int k_phase = 0;  // stages of this phase issued so far
       ok = for_each_stage(ph, [&](int p, int row, int nrows) {
         const int slot = i % S, use = i / S;
+        if (k_phase++ == kEarlyStages) {
+          // wait (bounded) until the consumers have this phase's input
+          const long long t0 = clock64();
+          while (*(volatile int*)&s_xgate <= ph_i) {
+            if (*(volatile int*)&s_abort) return false;
+            if (clock64() - t0 > kWaitCycles) {
+              if (lane == 0) atomicOr(&g_decode_error, 1 << kErrEmptyWait);
+              *(volatile int*)&s_abort = 1;
+              return false;
+            }
+            __nanosleep(32);
+          }
+          if (!dep_done) {
+            griddep_wait();
+            dep_done = true;
+          }
+        }
         if (use > 0) {
           if (!dep_done) {
             griddep_wait();
@@ -595,6 +620,7 @@ k_gemv_decode(const __grid_constant__ Args a) {
         if (blockIdx.x == 0 && tid == 0 && ph.xs_out != nullptr) ph.xs_out[m] = xscale[m];
       }
       consumer_sync();
+      if (tid == 0) *(volatile int*)&s_xgate = ph_i + 1;  // x is read: the weights may stream
 #pragma unroll
       for (int m = 0; m < MT; ++m) {
         if (m >= a.M) continue;
@@ -635,6 +661,8 @@ k_gemv_decode(const __grid_constant__ Args a) {
           }
         }
       }
+      consumer_sync();
+      if (tid == 0) *(volatile int*)&s_xgate = ph_i + 1;  // x is read: the weights may stream
     }
 
     // On a time-out a warp sets s_abort and from then on every warp only
