@@ -41,8 +41,9 @@
 //    consecutive decode kernels overlap under programmatic dependent launch.
 //    Weights are read after that wait, unless the caller declared them
 //    static (not written by any work still in flight): then the producer
-//    fills the first ring's worth at once, while the previous kernel
-//    finishes.
+//    issues the first stage while the previous kernel finishes.  The rest
+//    of a phase's stages wait until the consumers have read the phase's
+//    input x, whose loads would otherwise queue behind the weight copies.
 //  * Up to kDecodeMaxTargets matrices sharing the same input run in one
 //    launch; their rows are concatenated, stages never straddle two matrices.
 //  * The input is int8 with its scales, or bf16: then every CTA forms the
@@ -372,10 +373,11 @@ k_gemv_decode(const __grid_constant__ Args a) {
   if (warp == kConsumerWarps) {
     if (CHAIN && lane != 0) return;
     // Weights the caller declared static may stream in while the previous
-    // kernel on the stream is still running (one ring's worth); otherwise
+    // kernel on the stream is still running (the first stage); otherwise
     // wait for it first.  Either way every bounded wait below starts after
     // the dependency wait.  In a chain the producer runs ahead across phase
-    // boundaries: weights never depend on earlier phases.
+    // boundaries (weights never depend on earlier phases), up to the first
+    // stage of a phase whose input the consumers have not read yet.
     bool dep_done = !a.weights_early;
     if (dep_done) griddep_wait();
     const int S = a.stages;
