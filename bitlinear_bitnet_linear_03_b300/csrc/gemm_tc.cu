@@ -57,15 +57,19 @@ constexpr int kThreadsFused = 320;  // + 4 warps expanding the packed weights
 constexpr uint32_t kTmemCols = 512;
 constexpr int kRingBytes = 192 * 1024;
 // Tile N = BN (256 or 128): B tile, stage size, ring depth and shared memory.
-// FUSED: B arrives as packed 2-bit codes (16 bytes per row per stage, in a
-// staging area after the B tile) and is expanded to bf16 in shared memory.
+// Unfused: a TMA stage holds the A and B tiles.  FUSED: a TMA stage holds the
+// A tile and the packed 2-bit codes of the B tile (16 bytes per row), and
+// the codes are expanded into one of two bf16 B buffers after the ring, so
+// the TMA ring is deep (6 stages) while the expanded tiles are only double
+// buffered.
 template <int BN, bool FUSED = false>
 struct Tile {
   static constexpr int kBTileBytes = BN * kRowBytes;
   static constexpr int kPackedBytes = FUSED ? BN * 16 : 0;
-  static constexpr int kStageBytes = kATileBytes + kBTileBytes + kPackedBytes;
-  static constexpr int kStages = kRingBytes / kStageBytes;   // 4 or 6; 3 fused
-  static constexpr int kSmemBytes = kStages * kStageBytes + 1024;  // + alignment slack
+  static constexpr int kStageBytes = kATileBytes + (FUSED ? kPackedBytes : kBTileBytes);
+  static constexpr int kBBufBytes = FUSED ? 2 * kBTileBytes : 0;
+  static constexpr int kStages = (kRingBytes - kBBufBytes) / kStageBytes;  // 4 or 6; 6 fused
+  static constexpr int kSmemBytes = kStages * kStageBytes + kBBufBytes + 1024;  // + alignment
 };
 constexpr long long kWaitCycles = 2000000000ll;
 constexpr int kErrProducer = 1 << 4, kErrMma = 1 << 5, kErrEpilogue = 1 << 6, kErrDrain = 1 << 7;
@@ -294,7 +298,8 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUte
   constexpr int kBTileBytesT = Tile<BN, FUSED>::kBTileBytes;
   __shared__ __align__(8) uint64_t full_bar[kStages];
   __shared__ __align__(8) uint64_t empty_bar[kStages];
-  __shared__ __align__(8) uint64_t bready_bar[kStages];  // fused: B tile expanded
+  __shared__ __align__(8) uint64_t bready_bar[2];  // fused: B buffer expanded
+  __shared__ __align__(8) uint64_t bfree_bar[2];   // fused: MMAs done with the B buffer
   __shared__ __align__(8) uint64_t acc_full[2];
   __shared__ __align__(8) uint64_t acc_empty[2];
   __shared__ __align__(8) uint64_t drain_bar;
@@ -302,6 +307,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUte
   __shared__ int s_abort;
 
   const uint32_t smem0 = (saddr(smem_raw) + 1023u) & ~1023u;  // 1024-byte aligned tiles
+  const uint32_t bbuf0 = smem0 + kStages * kStageBytes;        // fused: expanded B buffers
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int items = a.m_tiles * a.n_tiles * a.splits;
   __shared__ int s_last;
@@ -309,8 +315,12 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUte
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(saddr(&full_bar[s]), 1);
-      mbar_init(saddr(&empty_bar[s]), 1);
-      mbar_init(saddr(&bready_bar[s]), 4);
+      // fused: the four converter warps (packed codes read) and the MMA commit
+      mbar_init(saddr(&empty_bar[s]), FUSED ? 5 : 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(saddr(&bready_bar[b]), 4);
+      mbar_init(saddr(&bfree_bar[b]), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(saddr(&acc_full[b]), 1);
@@ -361,7 +371,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUte
             // row = the stage's 64 weights).
             mbar_expect_tx(fb, kATileBytes + Tile<BN, FUSED>::kPackedBytes);
             tma_load_2d(sa, &mapA, ks * Kind<KIND>::kKStage, m0, fb);
-            tma_load_2d(sa + kATileBytes + kBTileBytesT, &mapB, ks * 16, n0, fb);
+            tma_load_2d(sa + kATileBytes, &mapB, ks * 16, n0, fb);
           } else {
             mbar_expect_tx(fb, kStageBytes);
             tma_load_2d(sa, &mapA, ks * Kind<KIND>::kKStage, m0, fb);
@@ -395,9 +405,12 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUte
         tc_fence_after();
         const uint32_t d = tmem + (uint32_t)(ab * BN);
         for (int ks = ks0; ks < ks1; ++ks, ++it) {
-          const int s = it % kStages;
-          const uint32_t ready = FUSED ? saddr(&bready_bar[s]) : saddr(&full_bar[s]);
-          if (!mbar_wait(ready, (it / kStages) & 1) || *(volatile int*)&s_abort) {
+          const int s = it % kStages, b = it & 1;
+          // fused: the expanded B buffer (and the A tile of the stage, whose
+          // landing the converters waited for and which is checked again)
+          bool ready = mbar_wait(saddr(&full_bar[s]), (it / kStages) & 1);
+          if (FUSED && ready) ready = mbar_wait(saddr(&bready_bar[b]), (it >> 1) & 1);
+          if (!ready || *(volatile int*)&s_abort) {
             atomicOr(&g_device_error, kErrMma);
             *(volatile int*)&s_abort = 1;
             ok = false;
@@ -405,13 +418,15 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUte
           }
           tc_fence_after();
           const uint32_t sa = smem0 + s * kStageBytes;
+          const uint32_t sb = FUSED ? bbuf0 + b * kBTileBytesT : sa + kATileBytes;
 #pragma unroll
           for (int kk = 0; kk < kRowBytes / kMmaKBytes; ++kk) {
             const uint64_t ad = sw128_desc(sa + kk * kMmaKBytes);
-            const uint64_t bd = sw128_desc(sa + kATileBytes + kk * kMmaKBytes);
+            const uint64_t bd = sw128_desc(sb + kk * kMmaKBytes);
             tc_mma<KIND, BN>(d, ad, bd, (ks != ks0 || kk != 0) ? 1u : 0u);
           }
           tc_commit(saddr(&empty_bar[s]));  // frees the stage when these MMAs finish
+          if (FUSED) tc_commit(saddr(&bfree_bar[b]));  // and the expanded B buffer
         }
         if (!ok) break;
         tc_commit(saddr(&acc_full[ab]));    // accumulator ready for the epilogue
@@ -430,19 +445,25 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUte
       (void)t;
       bool ok = true;
       for (int ks = ks0; ks < ks1; ++ks, ++it) {
-        const int s = it % kStages;
-        if (!mbar_wait(saddr(&full_bar[s]), (it / kStages) & 1) || *(volatile int*)&s_abort) {
+        const int s = it % kStages, b = it & 1;
+        bool ready = mbar_wait(saddr(&full_bar[s]), (it / kStages) & 1);
+        // the MMAs of two stages ago have finished reading buffer b
+        if (ready && it >= 2) ready = mbar_wait(saddr(&bfree_bar[b]), ((it >> 1) - 1) & 1);
+        if (!ready || *(volatile int*)&s_abort) {
           if (lane == 0) atomicOr(&g_device_error, kErrProducer);
           *(volatile int*)&s_abort = 1;
           ok = false;
           break;
         }
         const uint32_t sa = smem0 + s * kStageBytes;
-        expand_b_tile<BN>(sa + kATileBytes + kBTileBytesT, sa + kATileBytes, ct);
+        expand_b_tile<BN>(sa + kATileBytes, bbuf0 + b * kBTileBytesT, ct);
         // make the generic-proxy stores visible to the tensor core's reads
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
-        if (lane == 0) mbar_arrive(saddr(&bready_bar[s]));
+        if (lane == 0) {
+          mbar_arrive(saddr(&bready_bar[b]));
+          mbar_arrive(saddr(&empty_bar[s]));  // the packed codes are read
+        }
       }
       if (!ok) break;
     }
