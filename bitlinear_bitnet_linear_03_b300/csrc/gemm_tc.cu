@@ -299,7 +299,6 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUte
   __shared__ __align__(8) uint64_t full_bar[kStages];
   __shared__ __align__(8) uint64_t empty_bar[kStages];
   __shared__ __align__(8) uint64_t bready_bar[2];  // fused: B buffer expanded
-  __shared__ __align__(8) uint64_t bfree_bar[2];   // fused: MMAs done with the B buffer
   __shared__ __align__(8) uint64_t acc_full[2];
   __shared__ __align__(8) uint64_t acc_empty[2];
   __shared__ __align__(8) uint64_t drain_bar;
@@ -318,10 +317,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUte
       // fused: the four converter warps (packed codes read) and the MMA commit
       mbar_init(saddr(&empty_bar[s]), FUSED ? 5 : 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(saddr(&bready_bar[b]), 4);
-      mbar_init(saddr(&bfree_bar[b]), 1);
-    }
+    for (int b = 0; b < 2; ++b) mbar_init(saddr(&bready_bar[b]), 4);
     for (int b = 0; b < 2; ++b) {
       mbar_init(saddr(&acc_full[b]), 1);
       mbar_init(saddr(&acc_empty[b]), 4);
@@ -425,8 +421,9 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUte
             const uint64_t bd = sw128_desc(sb + kk * kMmaKBytes);
             tc_mma<KIND, BN>(d, ad, bd, (ks != ks0 || kk != 0) ? 1u : 0u);
           }
-          tc_commit(saddr(&empty_bar[s]));  // frees the stage when these MMAs finish
-          if (FUSED) tc_commit(saddr(&bfree_bar[b]));  // and the expanded B buffer
+          // frees the stage, and (fused) the expanded B buffer, when these
+          // MMAs finish: one commit per stage
+          tc_commit(saddr(&empty_bar[s]));
         }
         if (!ok) break;
         tc_commit(saddr(&acc_full[ab]));    // accumulator ready for the epilogue
@@ -447,8 +444,10 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUte
       for (int ks = ks0; ks < ks1; ++ks, ++it) {
         const int s = it % kStages, b = it & 1;
         bool ready = mbar_wait(saddr(&full_bar[s]), (it / kStages) & 1);
-        // the MMAs of two stages ago have finished reading buffer b
-        if (ready && it >= 2) ready = mbar_wait(saddr(&bfree_bar[b]), ((it >> 1) - 1) & 1);
+        // the MMAs of two stages ago (which read buffer b) have finished: that
+        // stage's ring slot was released, by them and by these warps
+        if (ready && it >= 2)
+          ready = mbar_wait(saddr(&empty_bar[(it - 2) % kStages]), ((it - 2) / kStages) & 1);
         if (!ready || *(volatile int*)&s_abort) {
           if (lane == 0) atomicOr(&g_device_error, kErrProducer);
           *(volatile int*)&s_abort = 1;
