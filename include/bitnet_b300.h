@@ -133,10 +133,14 @@ bitnet_status bitnet_quantize_act(const uint16_t* x, int64_t M, int64_t K,
  *   y[m,n]   = (float)acc[m,n] * (x_scale[m] * w_scale[0]).
  * Wq [N, K/4] bytes, w_scale [1], xq [M, K], x_scale [M], y [M, N] float.
  * acc_out: optional [M, N] int32 copy of acc (NULL to skip).
- * ws: scratch of bitnet_linear_workspace(M, N, K) bytes, no initial
- * contents required.  M <= 4096*64 rows per call; K % 64 == 0.
- * Small M runs a CUDA-core kernel; large M runs the tensor-core kernel;
- * both give the same bits. */
+ * ws: scratch of bitnet_linear_workspace(M, N, K) bytes (0 when none is
+ * needed), no initial contents required.  M <= 4096*64 rows per call;
+ * K % 64 == 0.  Paths, all giving the same bits: M <= 4 streams the packed
+ * weights through the decode kernel (no workspace); 5 <= M < 16 runs a
+ * CUDA-core kernel; M >= 16 runs the tensor cores (M <= 256: the packed
+ * weights are expanded on chip, and K is split over CTAs when the output
+ * has few 128 x 256 tiles; M > 256: a bf16 copy of the weights is made in
+ * the workspace first). */
 size_t bitnet_linear_workspace(int64_t M, int64_t N, int64_t K);
 bitnet_status bitnet_linear(const uint8_t* Wq, const float* w_scale,
                             const int8_t* xq, const float* x_scale, int64_t M,

@@ -63,6 +63,22 @@ def test_workspace_queries():
     assert L.bitnet_ffn_workspace(M, H, F) >= M * H + 2 * 4 * M * F + M * F
 
 
+def test_linear_workspace_follows_the_dispatch():
+    """Workspace per path: none for decode (M <= 4), the bf16 activations for
+    the fused tensor-core path (16 <= M <= 256) plus the split-K sums when the
+    output has few tiles, the bf16 weights and activations for prefill."""
+    L = bn.lib()
+    assert L.bitnet_linear_workspace(1, 28672, 8192) == 0
+    assert L.bitnet_linear_workspace(4, 2560, 6912) == 0
+    M, N, K = 64, 28672, 8192          # 112 tiles: no split
+    w = L.bitnet_linear_workspace(M, N, K)
+    assert M * K * 2 <= w < M * K * 2 + M * N * 4
+    M, N, K = 64, 8192, 28672          # 32 tiles: K split, fp32 sums + tile counters
+    assert L.bitnet_linear_workspace(M, N, K) >= M * K * 2 + M * N * 4 + 32 * 4
+    M, N, K = 4096, 6912, 2560         # prefill: expanded weights and activations
+    assert L.bitnet_linear_workspace(M, N, K) >= N * K * 2 + M * K * 2
+
+
 FAKE = 0x10000  # 16-byte aligned, never dereferenced: validation fails first
 MIS = 0x10004   # 4-byte aligned only
 
