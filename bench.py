@@ -452,7 +452,7 @@ def run_gpu_arm(args, rank, world, barrier, max_over_ranks):
     dt = max_over_ranks(dt)
 
     bytes_step = layer_bytes(args.api) * args.layers
-    value = bytes_step * args.steps * world / dt / 1e9
+    value = aggregate_rate(bytes_step, args.steps, world, dt) / 1e9
 
     # e2e: pinned-host inputs copied in and outputs copied out every step.
     ins = step.input_tensors()
@@ -478,7 +478,7 @@ def run_gpu_arm(args, rank, world, barrier, max_over_ranks):
     for _ in range(e2e_steps):
         e2e_step()
     t_e2e = max_over_ranks(time.perf_counter() - t0)
-    e2e_value = bytes_step * e2e_steps * world / t_e2e / 1e9
+    e2e_value = aggregate_rate(bytes_step, e2e_steps, world, t_e2e) / 1e9
 
     # Dominant kernel: the BitLinear launches alone, graph-replayed; average
     # launch duration = replay time / launches (consecutive launches overlap
@@ -612,6 +612,29 @@ def run_reference_arm(args, rank):
     }
 
 
+def rank_tools(torch, dist, device):
+    """Barrier and max-over-ranks of the timed region: no-ops with one rank,
+    else collectives of the process group (NCCL on GPUs; gloo in the CPU
+    tests)."""
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    def max_over_ranks(v):
+        if dist is None:
+            return v
+        t = torch.tensor([v], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+    return barrier, max_over_ranks
+
+
+def aggregate_rate(units_per_step, steps, world, seconds):
+    """Whole-job rate with replicas: every rank runs `steps` steps of
+    `units_per_step`, and the job takes the slowest rank's time."""
+    return units_per_step * steps * world / seconds
+
+
 def main():
     args = parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -628,16 +651,7 @@ def main():
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
         dist.init_process_group("nccl")
 
-    def barrier():
-        if dist is not None:
-            dist.barrier()
-
-    def max_over_ranks(v):
-        if dist is None:
-            return v
-        t = torch.tensor([v], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+    barrier, max_over_ranks = rank_tools(torch, dist, "cuda")
 
     if args.case is not None:
         import bitlinear_bitnet_linear_03_b300 as bn
