@@ -652,7 +652,16 @@ constexpr int kKind = 1;
 
 size_t round1k(size_t v) { return (v + 1023) / 1024 * 1024; }
 
-bool use_fused_m(int64_t M) { return M <= 256; }
+// Small batches expand the packed weights on chip (streaming 2 bits per
+// weight from HBM); large ones expand them once into a bf16 copy that stays
+// in L2 across the many output-tile rows.
+bool use_fused(int64_t M) { return M <= 256; }
+
+// Tile N.  128-wide tiles fill the last wave of 148 SMs better for some
+// shapes, but they stream the bf16 A operand twice as often from L2; measured
+// on B300 (M = 4096, K = 6912, N = 2560) they lose (237 us vs 192 us), so
+// the 256-wide tile is used unless N itself is narrow (fused: always 256).
+int pick_bn(int64_t N) { return N <= 128 ? 128 : 256; }
 
 // Workspace of one call: [B bf16 N x K (unfused only)] [A bf16 M x K]
 // [split-K sums M x N fp32] [tile counters], each 1 KB aligned.  Split K
@@ -664,8 +673,8 @@ struct WsLayout {
 };
 WsLayout ws_layout(int64_t M, int64_t N, int64_t K) {
   WsLayout L = {};
-  const bool fused = use_fused_m(M);
-  const int bn = fused ? 256 : (N <= 128 ? 128 : 256);
+  const bool fused = use_fused(M);
+  const int bn = fused ? 256 : pick_bn(N);
   const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + bn - 1) / bn);
   const int k_stages = (int)((K + 63) / 64);
   int splits = 1;
@@ -746,25 +755,11 @@ cudaError_t launch_kind(const uint8_t* Wq, const float* w_scale, const int8_t* x
                     mapA, mapB, a);
 }
 
-// Tile N.  128-wide tiles fill the last wave of 148 SMs better for some
-// shapes, but they stream the bf16 A operand twice as often from L2; measured
-// on B300 (M = 4096, K = 6912, N = 2560) they lose (237 us vs 192 us), so
-// the 256-wide tile is used unless N itself is narrow.
-int pick_bn(int64_t M, int64_t N) {
-  (void)M;
-  return N <= 128 ? 128 : 256;
-}
-
 }  // namespace
 
 bool gemm_tc_eligible(int64_t M, int64_t N, int64_t K) {
   return M >= 16 && N >= 1 && K >= 64 && K % 64 == 0;
 }
-
-// Small batches expand the packed weights on chip (streaming 2 bits per
-// weight from HBM); large ones expand them once into a bf16 copy that stays
-// in L2 across the many output-tile rows.
-bool use_fused(int64_t M) { return use_fused_m(M); }
 
 size_t gemm_tc_workspace(int64_t M, int64_t N, int64_t K) { return ws_layout(M, N, K).end; }
 
@@ -773,7 +768,7 @@ cudaError_t launch_gemm_tc(const uint8_t* Wq, const float* w_scale, const int8_t
                            int32_t* acc_out, void* ws, cudaStream_t s) {
   if (use_fused(M))
     return launch_kind<kKind, 256, true>(Wq, w_scale, xq, x_scale, M, N, K, y, acc_out, ws, s);
-  if (pick_bn(M, N) == 128)
+  if (pick_bn(N) == 128)
     return launch_kind<kKind, 128, false>(Wq, w_scale, xq, x_scale, M, N, K, y, acc_out, ws, s);
   return launch_kind<kKind, 256, false>(Wq, w_scale, xq, x_scale, M, N, K, y, acc_out, ws, s);
 }
