@@ -554,33 +554,32 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUte
 
 // ---- pre-pass kernels
 // Pre-pass, one launch (items [nblk + nx, + nz) zero 16 bytes of the split-K
-// workspace each): items [0, nblk) expand a 16-byte packed block (64
-// weights) of Wq into 128 bytes of bf16 B; items [nblk, nblk + nx) widen 16
-// int8 activations into 32 bytes of bf16 A.  In a packed block, chunk c of 8
-// consecutive weights (k = 8c .. 8c+7) is field s = c/2 of words 2(c%2) and
-// 2(c%2)+1.  All stores are 16 bytes wide.
+// workspace each): items [0, 8 nblk) write one 16-byte chunk of bf16 B each
+// (chunk c of packed block it / 8, so consecutive threads write consecutive
+// chunks); items [8 nblk, 8 nblk + nx) widen 16 int8 activations into 32
+// bytes of bf16 A.  In a packed block, chunk c of 8 consecutive weights
+// (k = 8c .. 8c+7) is field s = c/2 of words 2(c%2) and 2(c%2)+1.  All
+// stores are 16 bytes wide.
 __global__ void __launch_bounds__(256)
 k_prepass(const uint4* __restrict__ Wq, int64_t nblk, uint4* __restrict__ B,
           const uint4* __restrict__ xq, int64_t nx, uint4* __restrict__ A,
           uint4* __restrict__ zero, int64_t nz) {
-  const int64_t total = nblk + nx + nz;
+  const int64_t nb8 = 8 * nblk;
+  const int64_t total = nb8 + nx + nz;
   for (int64_t it = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; it < total;
        it += (int64_t)gridDim.x * blockDim.x) {
-    if (it < nblk) {
-      const uint4 w = Wq[it];
+    if (it < nb8) {
+      const uint4 w = Wq[it >> 3];  // the 8 threads of a block share this load
       const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const int sft = 2 * (c >> 1), h = c & 1;
-        uint4 o;
-        bf16x4_from_codes((ww[2 * h] >> sft) & 0x03030303u, o.x, o.y);
-        bf16x4_from_codes((ww[2 * h + 1] >> sft) & 0x03030303u, o.z, o.w);
-        B[it * 8 + c] = o;
-      }
-    } else if (it >= nblk + nx) {
-      zero[it - nblk - nx] = make_uint4(0, 0, 0, 0);  // split-K sums and tile counters
+      const int c = (int)(it & 7), sft = 2 * (c >> 1), h = c & 1;
+      uint4 o;
+      bf16x4_from_codes((ww[2 * h] >> sft) & 0x03030303u, o.x, o.y);
+      bf16x4_from_codes((ww[2 * h + 1] >> sft) & 0x03030303u, o.z, o.w);
+      B[it] = o;
+    } else if (it >= nb8 + nx) {
+      zero[it - nb8 - nx] = make_uint4(0, 0, 0, 0);  // split-K sums and tile counters
     } else {
-      const int64_t i = it - nblk;
+      const int64_t i = it - nb8;
       const uint4 v = xq[i];
       const uint32_t vv[4] = {v.x, v.y, v.z, v.w};
       uint32_t h[8];
@@ -707,7 +706,7 @@ cudaError_t launch_kind(const uint8_t* Wq, const float* w_scale, const int8_t* x
   int* tile_cnt = reinterpret_cast<int*>(w + L.cnt);
   const int64_t nblk = FUSED ? 0 : N * K / 64, nx = M * K / 16;
   const int64_t nz = L.splits > 1 ? (int64_t)(L.end - L.acc) / 16 : 0;
-  int64_t grid = (nblk + nx + nz + 255) / 256;
+  int64_t grid = (8 * nblk + nx + nz + 255) / 256;
   if (grid > 148 * 16) grid = 148 * 16;
   k_prepass<<<(unsigned)grid, 256, 0, s>>>(reinterpret_cast<const uint4*>(Wq), nblk,
                                            reinterpret_cast<uint4*>(B),
