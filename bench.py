@@ -59,7 +59,8 @@ def parse_args():
                          "bitnet_quantize_act + bitnet_linear per matrix")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-secondary", action="store_true")
-    ap.add_argument("--case", default=None, choices=["prefill", "gemv100b", "fused_small_m"],
+    ap.add_argument("--case", default=None,
+                    choices=["prefill", "gemv100b", "fused_small_m", "ffn", "gemv2560"],
                     help="run only this secondary measurement and print it (for profiling "
                          "one kernel under ncu)")
     return ap.parse_args()

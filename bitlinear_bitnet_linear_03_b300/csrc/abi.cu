@@ -316,8 +316,14 @@ bitnet_status bitnet_ffn(const uint16_t* x, const float* g, float eps, const uin
   cudaStream_t s = (cudaStream_t)stream;
 
   cudaError_t e = bitnet::launch_rmsnorm_quant(x, g, eps, M, H, xq, sx, s);
-  if (e == cudaSuccess) e = run_linear(Wup, s_up, xq, sx, M, F, H, u, nullptr, lin, s);
-  if (e == cudaSuccess) e = run_linear(Wgate, s_gate, xq, sx, M, F, H, v, nullptr, lin, s);
+  if (e == cudaSuccess && bitnet::decode_supported(M, H)) {
+    // decode sizes: up and gate share the quantised input, one launch
+    const bitnet::DecodeTarget t[2] = {{Wup, s_up, F, u, nullptr}, {Wgate, s_gate, F, v, nullptr}};
+    e = bitnet::launch_decode(t, 2, xq, sx, nullptr, M, H, nullptr, nullptr, false, s);
+  } else {
+    if (e == cudaSuccess) e = run_linear(Wup, s_up, xq, sx, M, F, H, u, nullptr, lin, s);
+    if (e == cudaSuccess) e = run_linear(Wgate, s_gate, xq, sx, M, F, H, v, nullptr, lin, s);
+  }
   if (e == cudaSuccess) e = bitnet::launch_relu2_quant(u, v, M, F, d.h, hq, sh, s);
   if (e == cudaSuccess) e = run_linear(Wdown, s_down, hq, sh, M, H, F, y, d.acc_down, lin, s);
   return cuda_status(e);
