@@ -91,3 +91,29 @@ def test_ffn_without_debug_matches():
                            dev(Wd), f32(sd)))
     want = oracle.ffn(x, g, 1e-5, Wu, su, Wg, sg, Wd, sd)
     assert_bits_equal(y, want["y"], "y")
+
+
+@pytest.mark.parametrize("M,seed", [(1, 0), (1, 1), (3, 2), (4, 3)])
+def test_ffn_partial_debug_outputs(M, seed):
+    """Only some intermediate outputs requested (no fp32 h): the codes, scale
+    and accumulators reported, and y, equal the oracle's."""
+    x, g, ws = ffn_inputs(M, seed, random_gain=(seed % 2 == 1))
+    (Wu, su, _), (Wg, sg, _), (Wd, sd, _) = ws
+    dbg = dict(u=torch.empty((M, F), dtype=torch.float32, device="cuda"),
+               v=torch.empty((M, F), dtype=torch.float32, device="cuda"),
+               hq=torch.empty((M, F), dtype=torch.int8, device="cuda"),
+               sh=torch.empty(M, dtype=torch.float32, device="cuda"),
+               acc_down=torch.empty((M, H), dtype=torch.int32, device="cuda"))
+    f32 = lambda v: dev(np.array([v], np.float32))
+    y = host(bn.bitnet_ffn(dev_bf16(x), dev(g), 1e-5, dev(Wu), f32(su), dev(Wg), f32(sg),
+                           dev(Wd), f32(sd), debug=dbg))
+    got = {k: host(v) for k, v in dbg.items()}
+    h_o = oracle.relu2_mul(got["u"], got["v"])
+    hq_o, sh_o = oracle.quantize_act_f32(h_o)
+    assert_bits_equal(got["sh"], sh_o, "sh")
+    assert_bits_equal(got["hq"], hq_o, "hq")
+    y_o, acc_o = oracle.linear(Wd, sd, hq_o, sh_o, F)
+    assert_bits_equal(got["acc_down"], acc_o, "acc_down")
+    assert_bits_equal(y, y_o, "y")
+    want = oracle.ffn(x, g, 1e-5, Wu, su, Wg, sg, Wd, sd)
+    assert_bits_equal(y, want["y"], "y end to end")
