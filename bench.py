@@ -564,19 +564,29 @@ class OracleSample:
         return nbytes
 
 
-def cpu_baseline(budget_s=12.0):
-    import oracle
-    threads = oracle.default_threads()
-    sample = OracleSample()
-    names = [n for n, *_ in LAYER_SHAPES]
+def _oracle_rate(sample, names, threads, budget_s):
+    """GB/s of the oracle over whole decode layers for about budget_s."""
     sample.run(names, threads)  # warm-up
     nbytes, t0, layers = 0, time.perf_counter(), 0
     while time.perf_counter() - t0 < budget_s or layers == 0:
         nbytes += sample.run(names, threads)
         layers += 1
     dt = time.perf_counter() - t0
-    return {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": threads,
+    return nbytes / dt / 1e9, layers, dt
+
+
+def cpu_baseline(budget_s=12.0, single_budget_s=6.0):
+    """The oracle on the host: all cores (the reported value) and one thread."""
+    import oracle
+    threads = oracle.default_threads()
+    sample = OracleSample()
+    names = [n for n, *_ in LAYER_SHAPES]
+    value, layers, dt = _oracle_rate(sample, names, threads, budget_s)
+    one, layers1, dt1 = _oracle_rate(sample, names, 1, single_budget_s)
+    return {"value": round(value, 4), "unit": "GB/s", "cores": threads,
             "kind": "oracle",
+            "single_thread": {"value": round(one, 4), "unit": "GB/s", "cores": 1,
+                              "sample": f"{layers1} layers, {dt1:.1f} s"},
             "sample": f"{layers} repetitions of one decode layer (4 act quants + 7 BitLinear, "
                       f"{layer_bytes('fused')} algorithmic bytes each) of the 30-layer step, "
                       f"{dt:.1f} s"}
