@@ -119,6 +119,42 @@ def test_argument_errors_are_reported_before_launch():
     assert L.bitnet_device_error(None, None) == 1
 
 
+def test_decode_chain_arguments_are_checked_on_the_host():
+    L = bn.lib()
+    TABLE = 0x100000  # 256-byte aligned, never dereferenced
+    need = L.bitnet_decode_chain_bytes(2)
+    assert L.bitnet_decode_chain_bytes(3) - need == need - L.bitnet_decode_chain_bytes(1) > 0
+
+    def phase(x=FAKE, K=2560, count=1, N=64, y=FAKE):
+        tg = (_lib.LinearTarget * max(count, 1))(
+            *[_lib.LinearTarget(FAKE, FAKE, N, y, None) for _ in range(max(count, 1))])
+        return _lib.DecodePhase(x, K, ctypes.cast(tg, ctypes.c_void_p), count), tg
+
+    def build(phases, M=1, table=TABLE, nbytes=None):
+        arr = (_lib.DecodePhase * len(phases))(*[ph for ph, _ in phases])
+        chain = _lib.DecodeChain()
+        n = len(phases)
+        return L.bitnet_decode_chain_build(arr, n, M, p(table),
+                                           L.bitnet_decode_chain_bytes(n) if nbytes is None
+                                           else nbytes, ctypes.byref(chain))
+
+    ok = [phase(), phase(K=6912, count=2)]
+    assert L.bitnet_decode_chain_build(None, 1, 1, p(TABLE), need, None) == 1    # NULL
+    assert build(ok, M=5) == 2                                                   # M > 4
+    assert build(ok, M=0) == 2
+    assert build(ok, table=TABLE + 128) == 3                                     # table alignment
+    assert build(ok, nbytes=need - 1) == 4                                       # table too small
+    assert build([phase(count=9)]) == 2                                          # > 8 targets
+    assert build([phase(count=0)]) == 2
+    assert build([phase(K=100)]) == 2                                            # K % 64 != 0
+    assert build([phase(K=65536 * 2)]) == 2                                      # K too large
+    assert build([phase(N=0)]) == 2                                              # empty matrix
+    assert build([phase(x=MIS)]) == 3                                            # x alignment
+    assert build([phase(y=MIS)]) == 3                                            # y alignment
+    assert build([phase(x=0)]) == 1
+    assert L.bitnet_decode_chain_run(None, None) == 1
+
+
 def test_no_device_reports_unsupported_or_cuda_error():
     import torch
     if torch.cuda.is_available():
