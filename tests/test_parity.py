@@ -48,9 +48,10 @@ def test_quantize_weights_worked_examples():
     W[:, 4:] = np.float32(2.0)          # sum|W| = 16 + 120*2 = 256 = 2 * 128
     Wq_g, s_g = gpu_quantize_weights(W)
     assert s_g == np.float32(2.0)
-    q = oracle.unpack(Wq_g, 64)
-    assert q[:, :4].tolist() == GOLD["weights_ties"]["q"]
-    assert (q[:, 4:] == 1).all()
+    # the worked example's codes, the rest +1, packed by the oracle
+    q_want = np.ones((2, 64), np.int8)
+    q_want[:, :4] = np.array(GOLD["weights_ties"]["q"], np.int8)
+    assert_bits_equal(Wq_g, oracle.pack(q_want), "tie codes")
     check_weights(W, "ties")
 
 
