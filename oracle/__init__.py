@@ -36,6 +36,7 @@ def lib():
             "oracle_linear": (INT, [P, F, P, P, I64, I64, I64, P, P, INT]),
             "oracle_rmsnorm_bf16": (None, [P, P, F, I64, I64, P, P]),
             "oracle_relu2_mul": (None, [P, P, I64, P]),
+            "oracle_f32_to_bf16": (None, [P, I64, P]),
             "oracle_ffn": (INT, [P, P, F, P, F, P, F, P, F, I64, I64, I64, P,
                                  P, P, P, P, P, P, P, P, INT]),
         }
@@ -170,6 +171,14 @@ def relu2_mul(u, v):
     h = np.empty_like(u)
     lib().oracle_relu2_mul(_p(u), _p(v), u.size, _p(h))
     return h
+
+
+def f32_to_bf16(v):
+    """binary32 -> bf16 bit patterns (uint16), nearest, ties to even."""
+    v = _c(v, np.float32)
+    out = np.empty(v.shape, np.uint16)
+    lib().oracle_f32_to_bf16(_p(v), v.size, _p(out))
+    return out
 
 
 def ffn(x_bits, g, eps, Wup, s_up, Wgate, s_gate, Wdown, s_down, threads=1):

@@ -234,23 +234,47 @@ int oracle_linear(const uint8_t* Wq, float w_scale, const int8_t* qx,
 void oracle_rmsnorm_bf16(const uint16_t* x, const float* g, float eps,
                          int64_t M, int64_t H, float* n, float* r_out) {
   for (int64_t m = 0; m < M; ++m) {
-    double p[32] = {0.0};
+    // ss: the exact sum of the binary32 squares, rounded once.
+    Big S(kLimbs, 0);
+    bool any_nan = false, any_inf = false;
     for (int64_t k = 0; k < H; ++k) {
       float xf = bf16_to_float(x[m * H + k]);
-      p[k % 32] += (double)(xf * xf);  // a bf16 square is exact in binary32
+      float t = xf * xf;  // one binary32 product
+      uint32_t u = float_bits(t);
+      uint32_t e = (u >> 23) & 0xffu, f = u & 0x7fffffu;
+      if (e == 255) {
+        if (f) any_nan = true;
+        else any_inf = true;
+      } else if (e == 0) {
+        big_add_shifted(S, f, 0);
+      } else {
+        big_add_shifted(S, f | 0x800000u, (int)e - 1);
+      }
     }
-    for (int off = 16; off >= 1; off /= 2) {
-      double nxt[32];
-      for (int l = 0; l < 32; ++l) nxt[l] = p[l] + p[l ^ off];
-      std::memcpy(p, nxt, sizeof p);
-    }
-    double ss = p[0];
-    float r = (float)(1.0 / std::sqrt(ss / (double)H + (double)eps));
+    float ss = any_nan ? std::nanf("") : any_inf ? INFINITY : round_quotient_to_f32(S, 1);
+    float q = ss / (float)H;
+    float t = q + eps;
+    float s = std::sqrt(t);  // binary32 square root, correctly rounded
+    float r = 1.0f / s;
     if (r_out) r_out[m] = r;
     for (int64_t k = 0; k < H; ++k) {
       float xf = bf16_to_float(x[m * H + k]);
       n[m * H + k] = (xf * r) * g[k];
     }
+  }
+}
+
+void oracle_f32_to_bf16(const float* v, int64_t count, uint16_t* out) {
+  for (int64_t i = 0; i < count; ++i) {
+    uint32_t u = float_bits(v[i]);
+    if ((u & 0x7fffffffu) > 0x7f800000u) {
+      out[i] = (uint16_t)((u >> 16) | 0x40u);  // NaN stays NaN (quiet)
+      continue;
+    }
+    // Keep the top 16 bits; round on the 16 dropped bits, ties to even.
+    uint32_t lower = u & 0xffffu, upper = u >> 16;
+    if (lower > 0x8000u || (lower == 0x8000u && (upper & 1u))) upper += 1;
+    out[i] = (uint16_t)upper;
   }
 }
 

@@ -88,16 +88,24 @@ int oracle_linear(const uint8_t* Wq, float w_scale, const int8_t* qx,
                   const float* sx, int64_t M, int64_t N, int64_t K, float* y,
                   int32_t* acc, int threads);
 
-/* subln RMSNorm of bf16 rows ([P1] "subln"):
- *   ss = sum_k x_k^2, each square exact in binary32, summed in binary64 in
- *        this order: 32 partial sums, partial l taking k = l, l+32, l+64, ...
- *        in increasing k; then for off = 16, 8, 4, 2, 1 every partial l is
- *        replaced by p[l] + p[l ^ off]; ss = p[0].
- *   r  = (float)(1 / sqrt(ss / H + eps)), binary64 throughout, one rounding.
- *   n_k = (x_k * r) * g_k  (binary32).
+/* subln RMSNorm of bf16 rows ([P1] "subln"; the pages give no formula, so
+ * this is the build's reading, order-free like the absmean):
+ *   t_k = x_k * x_k            one binary32 product per element;
+ *   ss  = sum_k t_k            the exact sum, rounded once to binary32
+ *                              (NaN if a t_k is NaN, else +Inf if one is Inf);
+ *   r   = 1 / sqrt(ss / H + eps)   four binary32 operations (division,
+ *                              addition, correctly rounded square root,
+ *                              division), in that order;
+ *   n_k = (x_k * r) * g_k      binary32.
  * r_out (may be NULL) receives r per row. */
 void oracle_rmsnorm_bf16(const uint16_t* x, const float* g, float eps,
                          int64_t M, int64_t H, float* n, float* r_out);
+
+/* Nearest bf16 (ties to even) to each binary32 value: the bf16 output form of
+ * a BitLinear result (the rescale "to fp32/bf16"; the pages fix no rounding,
+ * the reading is round-to-nearest-even).  A value above the largest bf16
+ * rounds to Inf; NaN stays NaN. */
+void oracle_f32_to_bf16(const float* v, int64_t count, uint16_t* out);
 
 /* h = (t * t) * u with t = max(v, 0): ReLU^2 of the gate times the up
  * projection ([P1] ReLU^2). */

@@ -358,22 +358,64 @@ def test_rmsnorm_constant_row():
     assert (q == g["q_all"]).all()
 
 
-def test_rmsnorm_matches_fp64_and_order():
+def _rmsnorm_r_by_fractions(xf32_row, H, eps):
+    """Test-side statement of the reading: exact sum of the binary32 squares
+    (Fractions), one rounding to binary32, then binary32 steps (numpy)."""
+    sq = [np.float32(v) * np.float32(v) for v in xf32_row]
+    ss = rn32(sum((exact(t) for t in sq), Fraction(0)))
+    q = np.float32(ss) / np.float32(H)
+    t = np.float32(q + np.float32(eps))
+    return np.float32(np.float32(1.0) / np.sqrt(t))
+
+
+def test_rmsnorm_exact_sum_and_binary32_steps():
     x = synth.tokens_bf16(8, 2560, seed=9, outlier_frac=0.01)
     gain = synth.gain_random(2560, seed=1)
     eps = np.float32(1e-5)
     n, r = oracle.rmsnorm_bf16(x, gain, eps)
-    xf = synth.bf16_bits_to_f32(x).astype(np.float64)
-    ref = xf / np.sqrt((xf ** 2).mean(axis=1, keepdims=True) + float(eps)) * gain
+    xf = synth.bf16_bits_to_f32(x)
+    ref = xf.astype(np.float64) / np.sqrt((xf.astype(np.float64) ** 2).mean(axis=1, keepdims=True)
+                                          + float(eps)) * gain
     assert np.allclose(n, ref, rtol=3e-7 * 4, atol=0)
-    # r: the stated 32-partial order, then one rounding to binary32
     for m in range(8):
-        p = [0.0] * 32
-        for k in range(2560):
-            p[k % 32] += float(np.float32(xf[m, k]) * np.float32(xf[m, k]))
-        for off in (16, 8, 4, 2, 1):
-            p = [p[l] + p[l ^ off] for l in range(32)]
-        assert r[m] == np.float32(1.0 / math.sqrt(p[0] / 2560 + float(eps)))
+        assert r[m] == _rmsnorm_r_by_fractions(xf[m], 2560, eps), m
+        # n is two binary32 products per element, in this order
+        assert (n[m] == (xf[m] * r[m]) * gain).all()
+
+
+def test_rmsnorm_sum_is_exact_not_sequential():
+    """x = 1490944 (= 182 * 2^13), 256, 256 and 2^-20: the squares 182^2 * 2^26,
+    2^16, 2^16 and 2^-40 sum to just above the tie between two binary32
+    neighbours (2^16 + 2^16 is exactly half an ulp of the first square), so
+    the exact sum rounds up.  A binary64 sum drops 2^-40, lands on the tie
+    and rounds to even (down); a binary32 running sum drops both 2^16 terms.
+    With H = 64 and eps = 0 the two candidate sums give different r."""
+    H = 64
+    row = np.zeros(H, np.float32)
+    row[3], row[20], row[41], row[63] = 1490944.0, 256.0, 256.0, 2.0 ** -20
+    x = synth.f32_to_bf16_bits(row[None, :])
+    assert (synth.bf16_bits_to_f32(x)[0] == row).all()
+    _, r = oracle.rmsnorm_bf16(x, synth.gain_ones(H), np.float32(0.0))
+    sq = [exact(np.float32(v) * np.float32(v)) for v in row]
+    ss_exact = rn32(sum(sq, Fraction(0)))
+    ss_f64 = np.float32(sum(float(t) for t in sq))
+    assert ss_exact != ss_f64
+    r_of = lambda ss: np.float32(np.float32(1.0) / np.sqrt(np.float32(ss / np.float32(H))))
+    assert r[0] == r_of(ss_exact)
+    assert r_of(ss_f64) != r[0]
+    assert r[0] == _rmsnorm_r_by_fractions(row, H, np.float32(0.0))
+
+
+def test_rmsnorm_nonfinite_rows():
+    H = 64
+    x = synth.tokens_bf16(3, H, seed=4)
+    x[0, 7] = 0x7f80          # +inf: ss = inf, r = 0
+    x[1, 9] = 0x7fc0          # nan
+    x[2, :] = 0               # zero row: r = 1/sqrt(eps)
+    n, r = oracle.rmsnorm_bf16(x, synth.gain_ones(H), np.float32(1e-5))
+    assert r[0] == 0.0 and np.isnan(r[1])
+    assert r[2] == np.float32(np.float32(1.0) / np.sqrt(np.float32(1e-5)))
+    assert (n[2] == 0).all()
 
 
 def test_relu2_worked_example():
@@ -416,3 +458,36 @@ def test_ffn_is_the_composition_and_close_to_fp64():
     assert np.allclose(out["y"], y64, rtol=1e-6, atol=1e-6 * np.abs(y64).max())
     # h is relu(v)^2 * u
     assert np.allclose(out["h"], np.maximum(v, 0).astype(np.float64) ** 2 * u, rtol=1e-6)
+
+
+# ---------------------------------------------------------------- bf16 output rounding
+def test_f32_to_bf16_worked_ties():
+    one = 1.0
+    cases = [
+        (one, 0x3F80),
+        (one + 2.0 ** -8, 0x3F80),                 # tie between 1 and 1 + 2^-7: even (down)
+        (one + 3 * 2.0 ** -8, 0x3F82),             # tie between 1 + 2^-7 and 1 + 2^-6: even (up)
+        (one + 2.0 ** -8 + 2.0 ** -20, 0x3F81),    # just above the tie: up
+        (-(one + 2.0 ** -8), 0xBF80),
+        (0.0, 0x0000),
+        (-0.0, 0x8000),
+        (float(np.finfo(np.float32).max), 0x7F80),  # above the largest bf16: Inf
+    ]
+    v = np.array([c[0] for c in cases], np.float32)
+    got = oracle.f32_to_bf16(v)
+    assert got.tolist() == [c[1] for c in cases]
+
+
+def test_f32_to_bf16_is_nearest_even_by_fractions():
+    rng = np.random.default_rng(3)
+    v = (rng.standard_normal(4000) * np.exp2(rng.integers(-130, 120, 4000))).astype(np.float32)
+    got = oracle.f32_to_bf16(v)
+    for x, b in zip(v, got):
+        cand = [int(b) - 1, int(b), int(b) + 1]
+        vals = [exact(synth.bf16_bits_to_f32(np.array([c & 0xFFFF], np.uint16))[0]) for c in cand]
+        d = [abs(val - exact(x)) for val in vals]
+        assert d[1] <= d[0] and d[1] <= d[2]
+        if d[1] in (d[0], d[2]):
+            assert b % 2 == 0  # a tie goes to the even pattern
+    nan = oracle.f32_to_bf16(np.array([np.nan], np.float32))
+    assert np.isnan(synth.bf16_bits_to_f32(nan)[0])
