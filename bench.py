@@ -2,19 +2,24 @@
 
 Default workload (one "step"): a batch-1 decode step over 2B-class layer
 shapes, 30 layers with distinct weight sets (521 MB of packed ternary weights,
-4x the 126 MB L2, so every step streams its weights from HBM).  Per layer:
-four per-token int8 activation quantisations (layer input, attention output,
-post-attention residual, FFN hidden state; bf16 N(0,1)) and seven BitLinear
-products (Q, O: 2560->2560; K, V: 2560->640; up, gate: 2560->6912; down:
-6912->2560), in four dependent phases (QKV, O, up+gate, down).  The step is
-captured once in a CUDA graph and replayed.
+4x the 126 MB L2, so every step streams its weights from HBM).  Per layer,
+four dependent BitLinear phases with the data flow of a decoder layer:
+  QKV   : the layer input (bf16) -> Q (bf16), K, V (binary32);
+  O     : subln(Q) -> O (bf16)   (Q stands in for the attention output,
+          which is not BitLinear);
+  up/gate: subln(O) -> h = relu(gate)^2 * up (binary32);
+  down  : h -> the next layer's input (bf16).
+Every phase quantises its input per token to int8.  The step is one
+bitnet_decode_chain_run (one persistent kernel; each phase reads the previous
+phase's output as it is produced), captured once in a CUDA graph and replayed.
 
-Metric: GB/s of algorithmic bytes (packed weights + activations read and
-written + scales + outputs) per second; the roofline block reports the
-dominant kernel (the BitLinear GEMV) against the measured HBM copy bandwidth.
-`--impl reference` times the CPU oracle on a bounded sample of the same
-workload instead.  Under torchrun every rank runs an independent replica
-(the path needs no exchange between GPUs) and rank 0 prints one JSON line.
+Metric: GB/s of algorithmic bytes (packed weights + scales + norm gains +
+activations read and written in their stated precision) per second; the
+roofline block reports the dominant kernel (the chain) against the measured
+HBM copy bandwidth.  `--impl reference` times the CPU oracle on a bounded
+sample of the same workload instead.  Under torchrun every rank runs an
+independent replica (the path needs no exchange between GPUs) and rank 0
+prints one JSON line.
 """
 import argparse
 import hashlib
@@ -31,18 +36,15 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 HIDDEN, FFN = 2560, 6912
-# (name, N, K, input).  The inputs follow the data flow of a decoder layer:
-# Q, K, V read the normed layer input; O reads the attention output; up and
-# gate read the normed post-attention residual; down reads the FFN hidden
-# state.  Each input depends on the previous phase, so a layer is four
-# dependent BitLinear phases.
-LAYER_SHAPES = [("q", HIDDEN, HIDDEN, "x"), ("k", 640, HIDDEN, "x"), ("v", 640, HIDDEN, "x"),
-                ("o", HIDDEN, HIDDEN, "attn"), ("up", FFN, HIDDEN, "x2"),
-                ("gate", FFN, HIDDEN, "x2"), ("down", HIDDEN, FFN, "h")]
-INPUTS = [("x", HIDDEN), ("attn", HIDDEN), ("x2", HIDDEN), ("h", FFN)]
+EPS = 1e-5
+# (name, N, K, phase) of one decoder layer's BitLinear products.
+LAYER_SHAPES = [("q", HIDDEN, HIDDEN, "qkv"), ("k", 640, HIDDEN, "qkv"), ("v", 640, HIDDEN, "qkv"),
+                ("o", HIDDEN, HIDDEN, "o"), ("up", FFN, HIDDEN, "ffn"),
+                ("gate", FFN, HIDDEN, "ffn"), ("down", HIDDEN, FFN, "down")]
 METRIC = "BitLinear decode GB/s & % HBM roofline; prefill int8 TOPS & % tensor peak"
 WORKLOAD = ("decode step, batch 1, 2B-class shapes (hidden 2560, FFN 6912), 30 layers of "
-            "distinct ternary weights")
+            "distinct ternary weights, dependent phases QKV -> subln O -> subln up/gate "
+            "ReLU^2 -> down")
 
 
 def parse_args():
@@ -52,33 +54,25 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--layers", type=int, default=30)
     ap.add_argument("--impl", default="b300", choices=["b300", "reference"])
-    ap.add_argument("--api", default="chain", choices=["chain", "fused", "split"],
-                    help="chain: one persistent bitnet_decode_chain_run per step (grid "
-                         "barrier between the 120 dependent phases); fused: "
-                         "bitnet_linear_bf16 per shared input (4 launches a layer); split: "
-                         "bitnet_quantize_act + bitnet_linear per matrix")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--case", default=None,
-                    choices=["prefill", "gemv100b", "fused_small_m", "ffn", "gemv2560"],
+                    choices=["prefill", "gemv100b", "fused_small_m", "ffn", "gemv2560", "8b"],
                     help="run only this secondary measurement and print it (for profiling "
                          "one kernel under ncu)")
     return ap.parse_args()
 
 
-def layer_bytes(api="fused"):
-    """Algorithmic bytes of one layer.
-    fused / chain: each of the four phases reads its bf16 input once; each BitLinear
-           reads packed W and its scale and writes fp32 y.
-    split: act-quant reads bf16 and writes int8 + scale; each BitLinear reads
-           packed W, int8 x, two scales and writes fp32 y."""
-    fused = api in ("fused", "chain")
-    b = 0
-    for _, K in INPUTS:
-        b += 2 * K if fused else 2 * K + K + 4
-    for _, N, K, _ in LAYER_SHAPES:
-        b += N * K // 4 + 4 + 4 * N if fused else N * K // 4 + K + 8 + 4 * N
-    return b
+def layer_bytes():
+    """Algorithmic bytes of one layer: packed weights and their scales, the
+    two norm gains, each phase's input read once in its precision (QKV, O,
+    up/gate: bf16 [2560]; down: binary32 h [6912]) and every output written
+    once (Q, O, down: bf16; K, V, h: binary32)."""
+    w = sum(N * K // 4 + 4 for _, N, K, _ in LAYER_SHAPES)
+    gains = 2 * 4 * HIDDEN
+    inputs = 3 * 2 * HIDDEN + 4 * FFN
+    outputs = 2 * HIDDEN + 2 * 4 * 640 + 2 * HIDDEN + 4 * FFN + 2 * HIDDEN
+    return w + gains + inputs + outputs
 
 
 def weight_bytes():
@@ -135,100 +129,88 @@ class ClockSampler:
 
 # ----------------------------------------------------------------- GPU arm
 class DecodeStep:
-    """Resident weights, inputs, outputs and workspaces of the decode step."""
+    """Resident weights, norm gains, activations and the chain of the decode
+    step.  weights: optional per-layer {name: (Wq, w_scale)} device tensors
+    (default: synthetic N(0, 0.02) weights quantised on the GPU); x0: the
+    step input (bf16 [1, HIDDEN]); gains: optional (attention-side, FFN-side)
+    lists of binary32 [HIDDEN] gains per layer."""
 
-    def __init__(self, layers, api="fused", seed=0):
+    def __init__(self, layers, weights=None, x0=None, gains=None, seed=0):
         import torch
         import bitlinear_bitnet_linear_03_b300 as bn
         from bitlinear_bitnet_linear_03_b300 import synth
-        self.torch, self.bn, self.api = torch, bn, api
+        self.torch, self.bn = torch, bn
         dev = torch.device("cuda")
-        self.layers = []
-        ws_q = torch.empty(bn.bitnet_quantize_weights_workspace(FFN, HIDDEN) * 2,
-                           dtype=torch.uint8, device=dev)
-        lin_ws = max(bn.bitnet_linear_workspace(1, N, K) for _, N, K, _ in LAYER_SHAPES)
-        self.lin_ws = torch.empty(max(lin_ws, 16), dtype=torch.uint8, device=dev)
-        # All step inputs live in one bf16 buffer and all outputs in one fp32
-        # buffer, so the end-to-end timing moves them with one copy each way.
-        in_per_layer = sum(K for _, K in INPUTS)
-        out_per_layer = sum(N for _, N, _, _ in LAYER_SHAPES)
-        self.x_all = torch.empty(layers * in_per_layer, dtype=torch.bfloat16, device=dev)
-        self.y_all = torch.empty(layers * out_per_layer, dtype=torch.float32, device=dev)
+        self.layers = layers
+        if weights is None:
+            ws_q = torch.empty(bn.bitnet_quantize_weights_workspace(FFN, HIDDEN) * 2,
+                               dtype=torch.uint8, device=dev)
+            weights = []
+            for li in range(layers):
+                L = {}
+                for j, (name, N, K, _) in enumerate(LAYER_SHAPES):
+                    W = synth.weights_f32(N, K, seed=seed * 100000 + li * 16 + j, device="cuda")
+                    L[name] = bn.bitnet_quantize_weights(W, ws=ws_q)
+                    del W
+                weights.append(L)
+        self.W = weights
+        if gains is None:
+            gains = ([torch.from_numpy(synth.gain_random(HIDDEN, 300 + li)).to(dev)
+                      for li in range(layers)],
+                     [torch.from_numpy(synth.gain_random(HIDDEN, 600 + li)).to(dev)
+                      for li in range(layers)])
+        self.g_attn, self.g_ffn = gains
+        if x0 is None:
+            x0 = synth.tokens_bf16(1, HIDDEN, seed=seed * 100000 + 77, device="cuda")
+        self.x0 = x0.contiguous()
+        bf, f32 = torch.bfloat16, torch.float32
+        self.out = []
         for li in range(layers):
-            L = {"W": {}, "x": {}, "xq": {}, "sx": {}, "y": {}}
-            off = li * out_per_layer
-            for j, (name, N, K, _) in enumerate(LAYER_SHAPES):
-                W = synth.weights_f32(N, K, seed=seed * 100000 + li * 16 + j, device="cuda")
-                Wq, s = bn.bitnet_quantize_weights(W, ws=ws_q)
-                del W
-                L["W"][name] = (Wq, s, N, K)
-                L["y"][name] = self.y_all[off:off + N].view(1, N)
-                off += N
-            off = li * in_per_layer
-            for j, (name, K) in enumerate(INPUTS):
-                L["x"][name] = self.x_all[off:off + K].view(1, K)
-                L["x"][name].copy_(synth.tokens_bf16(1, K, seed=seed * 100000 + li * 16 + 8 + j,
-                                                     device="cuda"))
-                off += K
-                L["xq"][name] = torch.empty((1, K), dtype=torch.int8, device=dev)
-                L["sx"][name] = torch.empty(1, dtype=torch.float32, device=dev)
-            self.layers.append(L)
+            self.out.append(dict(q=torch.empty((1, HIDDEN), dtype=bf, device=dev),
+                                 k=torch.empty((1, 640), dtype=f32, device=dev),
+                                 v=torch.empty((1, 640), dtype=f32, device=dev),
+                                 o=torch.empty((1, HIDDEN), dtype=bf, device=dev),
+                                 h=torch.empty((1, FFN), dtype=f32, device=dev),
+                                 y=torch.empty((1, HIDDEN), dtype=bf, device=dev)))
         torch.cuda.synchronize()
 
-    def quantize_inputs(self):
-        for L in self.layers:
-            for name, _ in INPUTS:
-                self.bn.bitnet_quantize_act(L["x"][name], L["xq"][name], L["sx"][name])
-
-    def linears(self):
-        for L in self.layers:
-            for name, N, K, src in LAYER_SHAPES:
-                Wq, s, _, _ = L["W"][name]
-                self.bn.bitnet_linear(Wq, s, L["xq"][src], L["sx"][src], K=K, y=L["y"][name],
-                                      ws=self.lin_ws)
-
-    def fused(self):
-        for L in self.layers:
-            for src, _ in INPUTS:
-                targets = [(L["W"][n][0], L["W"][n][1], L["y"][n])
-                           for n, _, _, s in LAYER_SHAPES if s == src]
-                self.bn.bitnet_linear_bf16(L["x"][src], targets, weights_static=True)
+    def phases(self):
+        """The 4 phases per layer, as bitnet_decode_chain_build takes them."""
+        ph = []
+        for li in range(self.layers):
+            W, o = self.W[li], self.out[li]
+            x = self.x0 if li == 0 else self.out[li - 1]["y"]
+            ph.append({"x": x, "targets": [(*W["q"], None, None, o["q"]), (*W["k"], o["k"]),
+                                           (*W["v"], o["v"])]})
+            ph.append({"x": o["q"], "norm_gain": self.g_attn[li], "norm_eps": EPS,
+                       "targets": [(*W["o"], None, None, o["o"])]})
+            ph.append({"x": o["o"], "norm_gain": self.g_ffn[li], "norm_eps": EPS, "gated": True,
+                       "h": o["h"], "targets": [(*W["up"], None), (*W["gate"], None)]})
+            ph.append({"x_f32": o["h"], "targets": [(*W["down"], None, None, o["y"])]})
+        return ph
 
     def build_chain(self):
-        phases = []
-        for L in self.layers:
-            for src, _ in INPUTS:
-                targets = [(L["W"][n][0], L["W"][n][1], L["y"][n])
-                           for n, _, _, s in LAYER_SHAPES if s == src]
-                phases.append((L["x"][src], targets))
-        self.chain = self.bn.bitnet_decode_chain_build(phases)
+        self.chain = self.bn.bitnet_decode_chain_build(self.phases())
 
     def step(self):
-        if self.api == "chain":
-            self.bn.bitnet_decode_chain_run(self.chain)
-        elif self.api == "fused":
-            self.fused()
-        else:
-            self.quantize_inputs()
-            self.linears()
+        self.bn.bitnet_decode_chain_run(self.chain)
 
     def launches_per_step(self):
-        if self.api == "chain":
-            return 1
-        if self.api == "fused":
-            return len(INPUTS) * len(self.layers)
-        n = 0
-        for _ in self.layers:
-            n += len(INPUTS)
-            for _, N, K, _ in LAYER_SHAPES:
-                n += 2 if self.bn.bitnet_linear_workspace(1, N, K) > 0 else 1
-        return n
+        return 1
+
+    def layer_outputs(self, li):
+        return self.out[li]
 
     def input_tensors(self):
-        return [self.x_all]
+        return [self.x0]
 
     def output_tensors(self):
-        return [self.y_all]
+        return [t for o in self.out for t in o.values()]
+
+    def result_tensors(self):
+        """What a decode step hands back: the last layer's output and every
+        layer's K and V (the cache entries of this token)."""
+        return [self.out[-1]["y"]] + [o[k] for o in self.out for k in ("k", "v")]
 
 
 def capture(torch, fn):
@@ -440,9 +422,8 @@ def run_gpu_arm(args, rank, world, barrier, max_over_ranks):
     import bitlinear_bitnet_linear_03_b300 as bn
     torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
     bn.lib()
-    step = DecodeStep(args.layers, api=args.api)
-    if args.api == "chain":
-        step.build_chain()
+    step = DecodeStep(args.layers)
+    step.build_chain()
     graph = capture(torch, step.step)
 
     clocks = ClockSampler(torch.cuda.current_device())
@@ -452,12 +433,13 @@ def run_gpu_arm(args, rank, world, barrier, max_over_ranks):
     clk = clocks.stop()
     dt = max_over_ranks(dt)
 
-    bytes_step = layer_bytes(args.api) * args.layers
+    bytes_step = layer_bytes() * args.layers
     value = aggregate_rate(bytes_step, args.steps, world, dt) / 1e9
 
-    # e2e: pinned-host inputs copied in and outputs copied out every step.
+    # e2e: the step input copied in from pinned host memory and the step's
+    # results (last layer output, every layer's K and V) copied out, every step.
     ins = step.input_tensors()
-    outs = step.output_tensors()
+    outs = step.result_tensors()
     h_in = [t.cpu().pin_memory() for t in ins]
     h_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs]
     h2d = sum(t.numel() * t.element_size() for t in ins)
@@ -481,52 +463,41 @@ def run_gpu_arm(args, rank, world, barrier, max_over_ranks):
     t_e2e = max_over_ranks(time.perf_counter() - t0)
     e2e_value = aggregate_rate(bytes_step, e2e_steps, world, t_e2e) / 1e9
 
-    # Dominant kernel: the BitLinear launches alone, graph-replayed; average
-    # launch duration = replay time / launches (consecutive launches overlap
-    # under programmatic dependent launch, so this is the effective duration).
-    if args.api in ("fused", "chain"):
-        lin_graph, lin_launches = graph, step.launches_per_step()
-        lin_bytes = bytes_step
-    else:
-        lin_graph = capture(torch, step.linears)
-        lin_launches = step.launches_per_step() - len(INPUTS) * args.layers
-        lin_bytes = sum(N * K // 4 + K + 8 + 4 * N for _, N, K, _ in LAYER_SHAPES) * args.layers
+    # Dominant kernel: the chain is the step's only kernel; its average launch
+    # duration is the graph replay time (CUDA events on the replaying stream).
     reps = max(20, min(args.steps, 400))
-    t_lin = time_graph(torch, lin_graph, reps, 5, lambda: None)
-    per_launch_s = t_lin / reps / lin_launches
-    achieved = lin_bytes / lin_launches / per_launch_s / 1e9
+    t_lin = time_graph(torch, graph, reps, 5, lambda: None)
+    per_launch_s = t_lin / reps
+    achieved = bytes_step / per_launch_s / 1e9
     peaks = read_peaks()
     if peaks and peaks.get("hbm_gbs"):
         peak, peak_src = float(peaks["hbm_gbs"]), "measured"
     else:
         peak, peak_src = 6400.0, "fallback"
-    traffic = profiled_traffic("bitlinear_bitnet_linear_03_b300/csrc/gemv_decode.cu",
-                               "profiles/gemv_decode_2b_30layers.md")
+    traffic = profiled_traffic("bitlinear_bitnet_linear_03_b300/csrc/decode_chain.cu",
+                               "profiles/decode_chain_2b_30layers.md")
 
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(dt / args.steps * 1e3, 4), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "int8 x ternary (int32 acc, f32 out)",
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "int8 x ternary (int32 acc; f32 / bf16 out)",
         "data": "synthetic: weights N(0,0.02) ternarized, activations bf16 N(0,1), seeded",
         "config": {"workload": WORKLOAD, "layers": args.layers, "batch_tokens": 1,
                    "packed_weight_bytes_per_step": weight_bytes() * args.layers,
                    "algorithmic_bytes_per_step": bytes_step,
                    "l2": "inputs larger than L2 (521 MB of weights per step vs 126 MB L2)",
                    "graph": "whole step captured in one CUDA graph",
-                   "api": args.api,
                    "parallelism": f"replicas x{world}"},
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps},
         "gpu_launches": step.launches_per_step() * args.steps,
-        "roofline": {"bound": "hbm",
-                     "kernel": {"chain": "k_gemv_decode chain (bitnet_decode_chain_run)",
-                                "fused": "k_gemv_decode (bitnet_linear_bf16)"}.get(
-                                    args.api, "bitnet_linear GEMV"),
+        "roofline": {"bound": "hbm", "kernel": "k_decode_chain (bitnet_decode_chain_run)",
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_source": peak_src,
                      "traffic": traffic, "launch_us": round(per_launch_s * 1e6, 3),
-                     "bytes_per_launch": lin_bytes / lin_launches},
+                     "bytes_per_launch": bytes_step},
         "clocks": clk,
     }
     if not args.no_secondary:
@@ -537,7 +508,7 @@ def run_gpu_arm(args, rank, world, barrier, max_over_ranks):
 # ----------------------------------------------------------------- oracle arm
 class OracleSample:
     """One decode layer built on the host for the oracle (never touched by
-    the GPU path): packed weights, bf16 inputs."""
+    the GPU path): packed weights, norm gains, the layer input."""
 
     def __init__(self, seed=0):
         import oracle
@@ -546,30 +517,37 @@ class OracleSample:
         self.W = {}
         for j, (name, N, K, _) in enumerate(LAYER_SHAPES):
             Wq, s, _ = oracle.quantize_weights(synth.weights_f32(N, K, seed=7000 + j))
-            self.W[name] = (Wq, s, N, K)
-        self.x = {name: synth.tokens_bf16(1, K, seed=7100 + j) for j, (name, K) in
-                  enumerate(INPUTS)}
+            self.W[name] = (Wq, s)
+        self.x = synth.tokens_bf16(1, HIDDEN, seed=7100)
+        self.g_attn = synth.gain_random(HIDDEN, 7200)
+        self.g_ffn = synth.gain_random(HIDDEN, 7201)
 
-    def run(self, names, threads):
-        q = {}
-        for n, _ in INPUTS:
-            q[n] = self.oracle.quantize_act_bf16(self.x[n])
-        nbytes = sum(2 * K for _, K in INPUTS)
-        for name in names:
-            Wq, s, N, K = self.W[name]
-            src = dict((a, d) for a, _, _, d in LAYER_SHAPES)[name]
-            qx, sx = q[src]
-            self.oracle.linear(Wq, s, qx, sx, K, threads=threads)
-            nbytes += N * K // 4 + 4 + 4 * N
-        return nbytes
+    def run(self, threads):
+        """The layer's four phases, in order; returns its algorithmic bytes."""
+        o, W = self.oracle, self.W
+        q, s = o.quantize_act_bf16(self.x)
+        Q = o.f32_to_bf16(o.linear(*W["q"], q, s, HIDDEN, threads=threads)[0])
+        o.linear(*W["k"], q, s, HIDDEN, threads=threads)
+        o.linear(*W["v"], q, s, HIDDEN, threads=threads)
+        n, _ = o.rmsnorm_bf16(Q, self.g_attn, EPS)
+        q, s = o.quantize_act_f32(n)
+        O = o.f32_to_bf16(o.linear(*W["o"], q, s, HIDDEN, threads=threads)[0])
+        n, _ = o.rmsnorm_bf16(O, self.g_ffn, EPS)
+        q, s = o.quantize_act_f32(n)
+        u = o.linear(*W["up"], q, s, HIDDEN, threads=threads)[0]
+        v = o.linear(*W["gate"], q, s, HIDDEN, threads=threads)[0]
+        h = o.relu2_mul(u, v)
+        q, s = o.quantize_act_f32(h)
+        o.f32_to_bf16(o.linear(*W["down"], q, s, FFN, threads=threads)[0])
+        return layer_bytes()
 
 
-def _oracle_rate(sample, names, threads, budget_s):
+def _oracle_rate(sample, threads, budget_s):
     """GB/s of the oracle over whole decode layers for about budget_s."""
-    sample.run(names, threads)  # warm-up
+    sample.run(threads)  # warm-up
     nbytes, t0, layers = 0, time.perf_counter(), 0
     while time.perf_counter() - t0 < budget_s or layers == 0:
-        nbytes += sample.run(names, threads)
+        nbytes += sample.run(threads)
         layers += 1
     dt = time.perf_counter() - t0
     return nbytes / dt / 1e9, layers, dt
@@ -580,15 +558,14 @@ def cpu_baseline(budget_s=12.0, single_budget_s=6.0):
     import oracle
     threads = oracle.default_threads()
     sample = OracleSample()
-    names = [n for n, *_ in LAYER_SHAPES]
-    value, layers, dt = _oracle_rate(sample, names, threads, budget_s)
-    one, layers1, dt1 = _oracle_rate(sample, names, 1, single_budget_s)
+    value, layers, dt = _oracle_rate(sample, threads, budget_s)
+    one, layers1, dt1 = _oracle_rate(sample, 1, single_budget_s)
     return {"value": round(value, 4), "unit": "GB/s", "cores": threads,
             "kind": "oracle",
             "single_thread": {"value": round(one, 4), "unit": "GB/s", "cores": 1,
                               "sample": f"{layers1} layers, {dt1:.1f} s"},
-            "sample": f"{layers} repetitions of one decode layer (4 act quants + 7 BitLinear, "
-                      f"{layer_bytes('fused')} algorithmic bytes each) of the 30-layer step, "
+            "sample": f"{layers} repetitions of one decode layer (its 4 dependent phases, "
+                      f"{layer_bytes()} algorithmic bytes each) of the 30-layer step, "
                       f"{dt:.1f} s"}
 
 
@@ -598,26 +575,26 @@ def run_reference_arm(args, rank):
     import oracle
     threads = oracle.default_threads()
     sample = OracleSample()
-    order = [n for n, *_ in LAYER_SHAPES]
-    for i in range(args.warmup):
-        sample.run([order[i % len(order)]], threads)
+    for _ in range(args.warmup):
+        sample.run(threads)
     nbytes, t0 = 0, time.perf_counter()
-    for i in range(args.steps):
-        nbytes += sample.run([order[i % len(order)]], threads)
+    for _ in range(args.steps):
+        nbytes += sample.run(threads)
     dt = time.perf_counter() - t0
     value = nbytes / dt / 1e9
     return {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
         "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "int8 x ternary (int32 acc, f32 out)",
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "int8 x ternary (int32 acc; f32 / bf16 out)",
         "data": "synthetic: weights N(0,0.02) ternarized, activations bf16 N(0,1), seeded",
         "config": {"workload": WORKLOAD, "layers": args.layers, "batch_tokens": 1,
                    "parallelism": "replicas x1"},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
                          "kind": "oracle",
-                         "sample": "each step: the 4 act quants of one decode layer plus one "
-                                   "of its 7 BitLinear products, cycling Q,K,V,O,up,gate,down"},
+                         "sample": "each step: one decode layer of the step (its 4 dependent "
+                                   "phases: QKV, subln O, subln up/gate ReLU^2, down)"},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }

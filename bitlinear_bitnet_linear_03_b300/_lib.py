@@ -15,7 +15,8 @@ from . import build as _build
 
 BITNET_OK = 0
 STATUS = {0: "BITNET_OK", 1: "BITNET_ERR_NULL", 2: "BITNET_ERR_SHAPE", 3: "BITNET_ERR_ALIGN",
-          4: "BITNET_ERR_WORKSPACE", 5: "BITNET_ERR_UNSUPPORTED", 6: "BITNET_ERR_CUDA"}
+          4: "BITNET_ERR_WORKSPACE", 5: "BITNET_ERR_UNSUPPORTED", 6: "BITNET_ERR_CUDA",
+          7: "BITNET_ERR_ALIAS"}
 
 # Every symbol the header declares, with its ctypes signature.
 _P = ctypes.c_void_p
@@ -28,14 +29,15 @@ SIGNATURES = {
     "bitnet_last_cuda_error": (_INT, []),
     "bitnet_abi_version": (_INT, []),
     "bitnet_device_error": (_INT, [_P, _P]),
+    "bitnet_set_wait_limit": (None, [ctypes.c_longlong]),
     "bitnet_quantize_weights_workspace": (_SZ, [_I64, _I64]),
     "bitnet_quantize_weights": (_INT, [_P, _I64, _I64, _P, _P, _P, _SZ, _P]),
     "bitnet_quantize_weights_noalloc": (_INT, [_P, _I64, _I64, _P, _P, _P]),
     "bitnet_quantize_act": (_INT, [_P, _I64, _I64, _P, _P, _P]),
     "bitnet_linear_workspace": (_SZ, [_I64, _I64, _I64]),
-    "bitnet_linear": (_INT, [_P, _P, _P, _P, _I64, _I64, _I64, _P, _P, _P, _SZ, _P]),
+    "bitnet_linear": (_INT, [_P, _P, _P, _P, _I64, _I64, _I64, _P, _P, _P, _P, _SZ, _P]),
     "bitnet_linear_bf16": (_INT, [_P, _I64, _I64, _P, _INT, _P, _P, ctypes.c_uint, _P]),
-    "bitnet_decode_chain_bytes": (_SZ, [_INT]),
+    "bitnet_decode_chain_bytes": (_SZ, [_P, _INT, _I64]),
     "bitnet_decode_chain_build": (_INT, [_P, _INT, _I64, _P, _SZ, _P]),
     "bitnet_decode_chain_run": (_INT, [_P, _P]),
     "bitnet_ffn_workspace": (_SZ, [_I64, _I64, _I64]),
@@ -55,17 +57,20 @@ class BitnetError(RuntimeError):
 
 class LinearTarget(ctypes.Structure):
     """bitnet_linear_target: one weight matrix of a grouped decode call."""
-    _fields_ = [("Wq", _P), ("w_scale", _P), ("N", _I64), ("y", _P), ("acc_out", _P)]
+    _fields_ = [("Wq", _P), ("w_scale", _P), ("N", _I64), ("y", _P), ("acc_out", _P),
+                ("y_bf16", _P)]
 
 
 class DecodePhase(ctypes.Structure):
     """bitnet_decode_phase: one phase of a decode chain."""
-    _fields_ = [("x", _P), ("K", _I64), ("targets", _P), ("count", _INT)]
+    _fields_ = [("x", _P), ("K", _I64), ("targets", _P), ("count", _INT), ("flags", ctypes.c_uint),
+                ("x_f32", _P), ("norm_gain", _P), ("norm_eps", _F), ("h", _P), ("xq_out", _P),
+                ("x_scale_out", _P)]
 
 
 class DecodeChain(ctypes.Structure):
     """bitnet_decode_chain: filled by bitnet_decode_chain_build."""
-    _fields_ = [("table", _P), ("M", _I64), ("nphases", _INT), ("cfg", _INT * 6)]
+    _fields_ = [("table", _P), ("M", _I64), ("nphases", _INT), ("cfg", _INT * 8)]
 
 
 class FfnDebug(ctypes.Structure):
@@ -186,47 +191,57 @@ def bitnet_linear_workspace(M, N, K) -> int:
 
 
 def bitnet_linear(Wq, w_scale, xq, x_scale, K=None, y=None, acc_out=None, ws=None,
-                  stream=None):
-    """Packed ternary Wq [N, K/4] x int8 xq [M, K] -> y float32 [M, N]."""
+                  stream=None, y_bf16=None):
+    """Packed ternary Wq [N, K/4] x int8 xq [M, K] -> y float32 [M, N] and/or
+    y_bf16 bfloat16 [M, N] (y rounded to nearest-even).  With neither given,
+    y is allocated.  Returns y, or y_bf16 when y is None."""
     N = Wq.shape[0]
     M, Kx = xq.shape
     K = Kx if K is None else K
-    if y is None:
+    if y is None and y_bf16 is None:
         y = torch.empty((M, N), dtype=torch.float32, device=xq.device)
     nb = bitnet_linear_workspace(M, N, K)
     ws = _workspace(nb, xq.device, ws)
     _check("bitnet_linear", lib().bitnet_linear(
         _ptr(Wq, torch.uint8, "Wq"), _ptr(w_scale, torch.float32, "w_scale"),
         _ptr(xq, torch.int8, "xq"), _ptr(x_scale, torch.float32, "x_scale"), M, N, K,
-        _ptr(y, torch.float32, "y"), _ptr(acc_out, torch.int32, "acc_out"),
-        _ptr(ws, name="ws"), nb, _stream(stream)))
-    return y
+        _ptr(y, torch.float32, "y"), _ptr(y_bf16, torch.bfloat16, "y_bf16"),
+        _ptr(acc_out, torch.int32, "acc_out"), _ptr(ws, name="ws"), nb, _stream(stream)))
+    return y if y is not None else y_bf16
 
 
 BITNET_WEIGHTS_STATIC = 1
 
 
+def _target(t):
+    """(Wq, w_scale, y[, acc_out[, y_bf16]]) -> LinearTarget; y may be None
+    when y_bf16 is given."""
+    Wq, ws, y = t[0], t[1], t[2]
+    acc = t[3] if len(t) > 3 else None
+    yb = t[4] if len(t) > 4 else None
+    return LinearTarget(_ptr(Wq, torch.uint8, "Wq"), _ptr(ws, torch.float32, "w_scale"),
+                        Wq.shape[0], _ptr(y, torch.float32, "y"), _ptr(acc, torch.int32, "acc_out"),
+                        _ptr(yb, torch.bfloat16, "y_bf16"))
+
+
 def bitnet_linear_bf16(x, targets, xq_out=None, x_scale_out=None, weights_static=False,
                        stream=None):
     """Per-token int8 quantisation of bf16 x [M, K] and BitLinear with every
-    (Wq, w_scale, y[, acc_out]) in `targets` (all sharing x), one launch.
-    weights_static: no work in flight on the stream writes the weights, so
-    they may stream in before the previous kernel has finished."""
+    (Wq, w_scale, y[, acc_out[, y_bf16]]) in `targets` (all sharing x), one
+    launch.  weights_static: no work in flight on the stream writes the
+    weights, so they may stream in before the previous kernel has finished."""
     M, K = x.shape
     arr = (LinearTarget * len(targets))()
-    keep = []
     for i, t in enumerate(targets):
-        Wq, ws, y = t[0], t[1], t[2]
-        acc = t[3] if len(t) > 3 else None
-        arr[i] = LinearTarget(_ptr(Wq, torch.uint8, "Wq"), _ptr(ws, torch.float32, "w_scale"),
-                              Wq.shape[0], _ptr(y, torch.float32, "y"),
-                              _ptr(acc, torch.int32, "acc_out"))
-        keep.append(t)
+        arr[i] = _target(t)
     _check("bitnet_linear_bf16", lib().bitnet_linear_bf16(
         _ptr(x, torch.bfloat16, "x"), M, K, arr, len(targets),
         _ptr(xq_out, torch.int8, "xq_out"), _ptr(x_scale_out, torch.float32, "x_scale_out"),
         BITNET_WEIGHTS_STATIC if weights_static else 0, _stream(stream)))
     return [t[2] for t in targets]
+
+
+BITNET_PHASE_GATED = 1
 
 
 class DecodeChainHandle:
@@ -240,25 +255,45 @@ class DecodeChainHandle:
         self._keep = keep
 
 
+def _phase(spec):
+    """A phase as a dict (keys: x | x_f32, targets, gated, h, norm_gain,
+    norm_eps, xq_out, x_scale_out) or as a tuple (x, targets)."""
+    if not isinstance(spec, dict):
+        spec = {"x": spec[0], "targets": spec[1]}
+    x, xf = spec.get("x"), spec.get("x_f32")
+    src = x if x is not None else xf
+    targets = spec["targets"]
+    tarr = (LinearTarget * len(targets))()
+    for j, t in enumerate(targets):
+        tarr[j] = _target(t)
+    ph = DecodePhase(_ptr(x, torch.bfloat16, "x"), src.shape[1], ctypes.cast(tarr, ctypes.c_void_p),
+                     len(targets), BITNET_PHASE_GATED if spec.get("gated") else 0,
+                     _ptr(xf, torch.float32, "x_f32"),
+                     _ptr(spec.get("norm_gain"), torch.float32, "norm_gain"),
+                     float(spec.get("norm_eps", 0.0)), _ptr(spec.get("h"), torch.float32, "h"),
+                     _ptr(spec.get("xq_out"), torch.int8, "xq_out"),
+                     _ptr(spec.get("x_scale_out"), torch.float32, "x_scale_out"))
+    return ph, (tarr, spec), src.shape[0]
+
+
 def bitnet_decode_chain_build(phases, device="cuda"):
-    """phases: list of (x bf16 [M, K], [(Wq, w_scale, y[, acc_out]), ...]).
+    """phases: list of phase dicts (see _phase) or (x, targets) tuples.
     Builds the chain table in device memory (synchronous)."""
-    M = phases[0][0].shape[0]
     n = len(phases)
     arr = (DecodePhase * n)()
     keep = []
-    for i, (x, targets) in enumerate(phases):
-        tarr = (LinearTarget * len(targets))()
-        for j, t in enumerate(targets):
-            Wq, ws, y = t[0], t[1], t[2]
-            acc = t[3] if len(t) > 3 else None
-            tarr[j] = LinearTarget(_ptr(Wq, torch.uint8, "Wq"), _ptr(ws, torch.float32, "w_scale"),
-                                   Wq.shape[0], _ptr(y, torch.float32, "y"),
-                                   _ptr(acc, torch.int32, "acc_out"))
-        keep.append((tarr, x, targets))
-        arr[i] = DecodePhase(_ptr(x, torch.bfloat16, "x"), x.shape[1],
-                             ctypes.cast(tarr, ctypes.c_void_p), len(targets))
-    nbytes = int(lib().bitnet_decode_chain_bytes(n))
+    M = None
+    for i, spec in enumerate(phases):
+        arr[i], k, m = _phase(spec)
+        keep.append(k)
+        M = m if M is None else M
+    nbytes = int(lib().bitnet_decode_chain_bytes(arr, n, M))
+    if nbytes == 0:
+        # the same checks give the status
+        chain = DecodeChain()
+        _check("bitnet_decode_chain_build", lib().bitnet_decode_chain_build(
+            arr, n, M, None, 0, ctypes.byref(chain)))
+        raise BitnetError("bitnet_decode_chain_bytes", 2)
     table = torch.zeros(nbytes + 256, dtype=torch.uint8, device=device)
     base = (table.data_ptr() + 255) // 256 * 256
     chain = DecodeChain()
@@ -270,6 +305,11 @@ def bitnet_decode_chain_build(phases, device="cuda"):
 def bitnet_decode_chain_run(handle, stream=None):
     _check("bitnet_decode_chain_run", lib().bitnet_decode_chain_run(
         ctypes.byref(handle.chain), _stream(stream)))
+
+
+def bitnet_set_wait_limit(cycles):
+    """Test hook: bound of the kernels' waits in SM clocks (0 = default)."""
+    lib().bitnet_set_wait_limit(int(cycles))
 
 
 # ------------------------------------------------------------------ FFN

@@ -8,7 +8,17 @@
 
 #include "../../include/bitnet_b300.h"
 #include "common.cuh"
+#include "decode_chain.cuh"
 #include "gemm_tc.cuh"
+
+namespace bitnet {
+
+// Bound of the kernels' waits in SM clocks (bitnet_set_wait_limit; 0 = the
+// default of about one second).
+long long g_wait_limit = 0;
+long long wait_limit_cycles() { return g_wait_limit > 0 ? g_wait_limit : 2000000000ll; }
+
+}  // namespace bitnet
 
 namespace {
 
@@ -56,14 +66,17 @@ size_t linear_ws(int64_t M, int64_t N, int64_t K) {
 
 cudaError_t run_linear(const uint8_t* Wq, const float* w_scale, const int8_t* xq,
                        const float* x_scale, int64_t M, int64_t N, int64_t K, float* y,
-                       int32_t* acc_out, void* ws, cudaStream_t s) {
+                       uint16_t* y_bf16, int32_t* acc_out, void* ws, cudaStream_t s) {
+  const long long wait = bitnet::wait_limit_cycles();
   if (bitnet::decode_supported(M, K)) {
-    bitnet::DecodeTarget t = {Wq, w_scale, N, y, acc_out};
-    return bitnet::launch_decode(&t, 1, xq, x_scale, nullptr, M, K, nullptr, nullptr, false, s);
+    bitnet::DecodeTarget t = {Wq, w_scale, N, y, acc_out, y_bf16};
+    return bitnet::launch_decode(&t, 1, xq, x_scale, nullptr, M, K, nullptr, nullptr, false, wait,
+                                 s);
   }
   if (bitnet::gemm_tc_eligible(M, N, K))
-    return bitnet::launch_gemm_tc(Wq, w_scale, xq, x_scale, M, N, K, y, acc_out, ws, s);
-  return bitnet::launch_gemv(Wq, w_scale, xq, x_scale, M, N, K, y, acc_out, ws, s);
+    return bitnet::launch_gemm_tc(Wq, w_scale, xq, x_scale, M, N, K, y, y_bf16, acc_out, ws, wait,
+                                  s);
+  return bitnet::launch_gemv(Wq, w_scale, xq, x_scale, M, N, K, y, y_bf16, acc_out, ws, s);
 }
 
 // FFN workspace sections, each 256-byte aligned.
@@ -103,22 +116,26 @@ const char* bitnet_status_string(int status) {
     case BITNET_ERR_WORKSPACE: return "workspace is smaller than the *_workspace() figure";
     case BITNET_ERR_UNSUPPORTED: return "the current device is not compute capability 10.3";
     case BITNET_ERR_CUDA: return "a CUDA call or kernel launch failed";
+    case BITNET_ERR_ALIAS: return "arrays of a decode chain overlap in a way it does not allow";
     default: return "unknown status";
   }
 }
 
 int bitnet_last_cuda_error(void) { return g_last_cuda_error; }
 
-int bitnet_abi_version(void) { return 1; }
+int bitnet_abi_version(void) { return 2; }
+
+void bitnet_set_wait_limit(long long cycles) { bitnet::g_wait_limit = cycles > 0 ? cycles : 0; }
 
 bitnet_status bitnet_device_error(int* code_out, void* stream) {
   if (!code_out) return BITNET_ERR_NULL;
   bitnet_status st = check_device();
   if (st != BITNET_OK) return st;
-  int a = 0, b = 0;
+  int a = 0, b = 0, c = 0;
   cudaError_t e = bitnet::read_and_clear_device_error(&a, (cudaStream_t)stream);
   if (e == cudaSuccess) e = bitnet::read_and_clear_decode_error(&b, (cudaStream_t)stream);
-  *code_out = a | (b << 8);
+  if (e == cudaSuccess) e = bitnet::read_and_clear_chain_error(&c, (cudaStream_t)stream);
+  *code_out = (a & 0xff) | ((b & 0xff) << 8) | ((c & 0xff) << 16);
   return cuda_status(e);
 }
 
@@ -170,19 +187,21 @@ size_t bitnet_linear_workspace(int64_t M, int64_t N, int64_t K) {
 
 bitnet_status bitnet_linear(const uint8_t* Wq, const float* w_scale, const int8_t* xq,
                             const float* x_scale, int64_t M, int64_t N, int64_t K, float* y,
-                            int32_t* acc_out, void* ws, size_t ws_bytes, void* stream) {
-  if (!Wq || !w_scale || !xq || !x_scale || !y) return BITNET_ERR_NULL;
+                            uint16_t* y_bf16, int32_t* acc_out, void* ws, size_t ws_bytes,
+                            void* stream) {
+  if (!Wq || !w_scale || !xq || !x_scale || (!y && !y_bf16)) return BITNET_ERR_NULL;
   if (M <= 0 || M > kMaxRows || N <= 0 || N > (1 << 30) || !valid_inner(K))
     return BITNET_ERR_SHAPE;
-  if (!aligned16(Wq) || !aligned16(xq) || !aligned16(y) || (acc_out && !aligned16(acc_out)))
+  if (!aligned16(Wq) || !aligned16(xq) || (y && !aligned16(y)) || (y_bf16 && !aligned16(y_bf16)) ||
+      (acc_out && !aligned16(acc_out)))
     return BITNET_ERR_ALIGN;
   const size_t need = linear_ws(M, N, K);
   if (need > 0 && (!ws || ws_bytes < need)) return ws ? BITNET_ERR_WORKSPACE : BITNET_ERR_NULL;
   if (need > 0 && !aligned16(ws)) return BITNET_ERR_ALIGN;
   bitnet_status st = check_device();
   if (st != BITNET_OK) return st;
-  return cuda_status(
-      run_linear(Wq, w_scale, xq, x_scale, M, N, K, y, acc_out, ws, (cudaStream_t)stream));
+  return cuda_status(run_linear(Wq, w_scale, xq, x_scale, M, N, K, y, y_bf16, acc_out, ws,
+                                (cudaStream_t)stream));
 }
 
 bitnet_status bitnet_linear_bf16(const uint16_t* x, int64_t M, int64_t K,
@@ -198,73 +217,70 @@ bitnet_status bitnet_linear_bf16(const uint16_t* x, int64_t M, int64_t K,
   int64_t rows = 0;
   for (int i = 0; i < count; ++i) {
     const bitnet_linear_target& g = targets[i];
-    if (!g.Wq || !g.w_scale || !g.y) return BITNET_ERR_NULL;
+    if (!g.Wq || !g.w_scale || (!g.y && !g.y_bf16)) return BITNET_ERR_NULL;
     if (g.N < 1) return BITNET_ERR_SHAPE;
-    if (!aligned16(g.Wq) || !aligned16(g.y) || (g.acc_out && !aligned16(g.acc_out)))
+    if (!aligned16(g.Wq) || (g.y && !aligned16(g.y)) || (g.y_bf16 && !aligned16(g.y_bf16)) ||
+        (g.acc_out && !aligned16(g.acc_out)))
       return BITNET_ERR_ALIGN;
     rows += g.N;
-    t[i] = {g.Wq, g.w_scale, g.N, g.y, g.acc_out};
+    t[i] = {g.Wq, g.w_scale, g.N, g.y, g.acc_out, g.y_bf16};
   }
   if (rows > (1 << 30)) return BITNET_ERR_SHAPE;
   bitnet_status st = check_device();
   if (st != BITNET_OK) return st;
   return cuda_status(bitnet::launch_decode(t, count, nullptr, nullptr, x, M, K, xq_out,
                                            x_scale_out, (flags & BITNET_WEIGHTS_STATIC) != 0,
-                                           (cudaStream_t)stream));
+                                           bitnet::wait_limit_cycles(), (cudaStream_t)stream));
 }
 
-size_t bitnet_decode_chain_bytes(int nphases) {
-  if (nphases < 1) return 0;
-  return bitnet::decode_chain_bytes(nphases);
+// Pointer and shape checks of a chain description that need no layout.
+bitnet_status check_chain_arrays(const bitnet_decode_phase* phases, int nphases) {
+  for (int i = 0; i < nphases; ++i) {
+    const bitnet_decode_phase& p = phases[i];
+    if (!p.targets) return BITNET_ERR_NULL;
+    if ((p.x && !aligned16(p.x)) || (p.x_f32 && !aligned16(p.x_f32)) ||
+        (p.norm_gain && !aligned16(p.norm_gain)) || (p.h && !aligned16(p.h)) ||
+        (p.xq_out && !aligned16(p.xq_out)))
+      return BITNET_ERR_ALIGN;
+    if (p.count < 1 || p.count > BITNET_MAX_TARGETS) return BITNET_ERR_SHAPE;
+    for (int j = 0; j < p.count; ++j) {
+      const bitnet_linear_target& g = p.targets[j];
+      if (!aligned16(g.Wq) || (g.y && !aligned16(g.y)) || (g.y_bf16 && !aligned16(g.y_bf16)) ||
+          (g.acc_out && !aligned16(g.acc_out)))
+        return BITNET_ERR_ALIGN;
+    }
+  }
+  return BITNET_OK;
+}
+
+size_t bitnet_decode_chain_bytes(const bitnet_decode_phase* phases, int nphases, int64_t M) {
+  if (!phases || nphases < 1) return 0;
+  if (check_chain_arrays(phases, nphases) != BITNET_OK) return 0;
+  size_t bytes = 0;
+  bitnet::check_decode_chain(phases, nphases, M, &bytes);
+  return bytes;
 }
 
 bitnet_status bitnet_decode_chain_build(const bitnet_decode_phase* phases, int nphases, int64_t M,
                                         void* table, size_t table_bytes,
                                         bitnet_decode_chain* chain) {
-  if (!phases || !table || !chain) return BITNET_ERR_NULL;
+  if (!phases || !chain) return BITNET_ERR_NULL;
   if (nphases < 1 || M < 1 || M > BITNET_DECODE_MAX_M) return BITNET_ERR_SHAPE;
-  if ((reinterpret_cast<uintptr_t>(table) & 255u) != 0) return BITNET_ERR_ALIGN;
-  if (table_bytes < bitnet::decode_chain_bytes(nphases)) return BITNET_ERR_WORKSPACE;
-  std::vector<bitnet::DecodeTarget> tg;
-  tg.reserve((size_t)nphases * BITNET_MAX_TARGETS);
-  std::vector<bitnet::DecodePhaseDesc> ph((size_t)nphases);
-  for (int i = 0; i < nphases; ++i) {
-    const bitnet_decode_phase& p = phases[i];
-    if (!p.x || !p.targets) return BITNET_ERR_NULL;
-    if (p.count < 1 || p.count > BITNET_MAX_TARGETS || !valid_inner(p.K) ||
-        !bitnet::decode_supported(M, p.K))
-      return BITNET_ERR_SHAPE;
-    if (!aligned16(p.x)) return BITNET_ERR_ALIGN;
-    const size_t first = tg.size();
-    int64_t rows = 0;
-    for (int j = 0; j < p.count; ++j) {
-      const bitnet_linear_target& g = p.targets[j];
-      if (!g.Wq || !g.w_scale || !g.y) return BITNET_ERR_NULL;
-      if (g.N < 1) return BITNET_ERR_SHAPE;
-      if (!aligned16(g.Wq) || !aligned16(g.y) || (g.acc_out && !aligned16(g.acc_out)))
-        return BITNET_ERR_ALIGN;
-      rows += g.N;
-      tg.push_back({g.Wq, g.w_scale, g.N, g.y, g.acc_out});
-    }
-    if (rows > (1 << 30)) return BITNET_ERR_SHAPE;
-    ph[(size_t)i] = {p.x, p.K, tg.data() + first, p.count};
-  }
-  bitnet_status st = check_device();
+  // The description is checked on the host before anything touches the device.
+  bitnet_status st = check_chain_arrays(phases, nphases);
   if (st != BITNET_OK) return st;
-  bitnet::DecodeChainConfig cfg;
-  cudaError_t e = bitnet::build_decode_chain(ph.data(), nphases, M, table, &cfg);
-  if (e == cudaErrorNotSupported) return BITNET_ERR_SHAPE;
-  if (e != cudaSuccess) return cuda_status(e);
-  chain->table = table;
-  chain->M = M;
-  chain->nphases = nphases;
-  chain->cfg[0] = cfg.mt;
-  chain->cfg[1] = cfg.j;
-  chain->cfg[2] = cfg.stages;
-  chain->cfg[3] = cfg.slot_bytes;
-  chain->cfg[4] = cfg.xs_bytes;
-  chain->cfg[5] = cfg.smem;
-  return BITNET_OK;
+  size_t need = 0;
+  st = bitnet::check_decode_chain(phases, nphases, M, &need);
+  if (st != BITNET_OK) return st;
+  if (!table) return BITNET_ERR_NULL;
+  if ((reinterpret_cast<uintptr_t>(table) & 255u) != 0) return BITNET_ERR_ALIGN;
+  if (table_bytes < need) return BITNET_ERR_WORKSPACE;
+  st = check_device();
+  if (st != BITNET_OK) return st;
+  cudaError_t e = cudaSuccess;
+  st = bitnet::build_decode_chain(phases, nphases, M, table, table_bytes, chain, &e);
+  if (st == BITNET_ERR_CUDA) return cuda_status(e);
+  return st;
 }
 
 bitnet_status bitnet_decode_chain_run(const bitnet_decode_chain* chain, void* stream) {
@@ -272,10 +288,8 @@ bitnet_status bitnet_decode_chain_run(const bitnet_decode_chain* chain, void* st
   if (chain->nphases < 1) return BITNET_ERR_SHAPE;
   bitnet_status st = check_device();
   if (st != BITNET_OK) return st;
-  bitnet::DecodeChainConfig cfg = {chain->cfg[0], chain->cfg[1], chain->cfg[2],
-                                   chain->cfg[3], chain->cfg[4], chain->cfg[5]};
-  return cuda_status(bitnet::launch_decode_chain(chain->table, chain->nphases, chain->M, cfg,
-                                                 (cudaStream_t)stream));
+  return cuda_status(
+      bitnet::launch_decode_chain(chain, bitnet::wait_limit_cycles(), (cudaStream_t)stream));
 }
 
 size_t bitnet_ffn_workspace(int64_t M, int64_t H, int64_t F) {
@@ -318,14 +332,18 @@ bitnet_status bitnet_ffn(const uint16_t* x, const float* g, float eps, const uin
   cudaError_t e = bitnet::launch_rmsnorm_quant(x, g, eps, M, H, xq, sx, s);
   if (e == cudaSuccess && bitnet::decode_supported(M, H)) {
     // decode sizes: up and gate share the quantised input, one launch
-    const bitnet::DecodeTarget t[2] = {{Wup, s_up, F, u, nullptr}, {Wgate, s_gate, F, v, nullptr}};
-    e = bitnet::launch_decode(t, 2, xq, sx, nullptr, M, H, nullptr, nullptr, false, s);
+    const bitnet::DecodeTarget t[2] = {{Wup, s_up, F, u, nullptr, nullptr},
+                                       {Wgate, s_gate, F, v, nullptr, nullptr}};
+    e = bitnet::launch_decode(t, 2, xq, sx, nullptr, M, H, nullptr, nullptr, false,
+                              bitnet::wait_limit_cycles(), s);
   } else {
-    if (e == cudaSuccess) e = run_linear(Wup, s_up, xq, sx, M, F, H, u, nullptr, lin, s);
-    if (e == cudaSuccess) e = run_linear(Wgate, s_gate, xq, sx, M, F, H, v, nullptr, lin, s);
+    if (e == cudaSuccess) e = run_linear(Wup, s_up, xq, sx, M, F, H, u, nullptr, nullptr, lin, s);
+    if (e == cudaSuccess)
+      e = run_linear(Wgate, s_gate, xq, sx, M, F, H, v, nullptr, nullptr, lin, s);
   }
   if (e == cudaSuccess) e = bitnet::launch_relu2_quant(u, v, M, F, d.h, hq, sh, s);
-  if (e == cudaSuccess) e = run_linear(Wdown, s_down, hq, sh, M, H, F, y, d.acc_down, lin, s);
+  if (e == cudaSuccess)
+    e = run_linear(Wdown, s_down, hq, sh, M, H, F, y, nullptr, d.acc_down, lin, s);
   return cuda_status(e);
 }
 

@@ -11,6 +11,7 @@
 // The row maximum is exact whatever the order; every binary32 step is one
 // explicitly rounded operation.
 #include "common.cuh"
+#include "exact_sumsq.cuh"
 
 namespace bitnet {
 namespace {
@@ -88,10 +89,9 @@ k_act_quant_f32(const float4* __restrict__ x, int K, uint32_t* __restrict__ xq,
 }
 
 // subln RMSNorm + quantisation, one warp per token.
-//   ss = sum x^2 in binary64: lane l adds x_k^2 for k = l, l+32, ... in
-//        increasing k (each square exact in binary32), then the lanes are
-//        combined pairwise, p[l] + p[l ^ off] for off = 16, 8, 4, 2, 1;
-//   r  = (float)(1 / sqrt(ss / H + eps)) in binary64, rounded once;
+//   ss = the exact sum of the binary32 squares x_k * x_k, rounded once to
+//        binary32 (exact_sumsq.cuh: order-free, integer arithmetic);
+//   r  = 1 / sqrt(ss / H + eps), four binary32 operations;
 //   n  = (x * r) * g, then the per-token quantisation of n.
 constexpr int kNormWarps = 8;
 __global__ void __launch_bounds__(kNormWarps * 32)
@@ -101,15 +101,14 @@ k_rmsnorm_quant(const uint16_t* __restrict__ x, const float* __restrict__ g, flo
   const int row = blockIdx.x * kNormWarps + (threadIdx.x >> 5);
   if (row >= M) return;
   const uint16_t* xr = x + (int64_t)row * H;
-  double p = 0.0;
+  sumsq::Acc acc;
+  sumsq::zero(acc);
   for (int k = lane; k < H; k += 32) {
-    float f = bf16_bits_to_float(xr[k]);
-    p = __dadd_rn(p, (double)__fmul_rn(f, f));
+    const float f = bf16_bits_to_float(xr[k]);
+    sumsq::add_term(acc, __fmul_rn(f, f));
   }
-#pragma unroll
-  for (int off = 16; off >= 1; off >>= 1) p = __dadd_rn(p, __shfl_xor_sync(0xffffffffu, p, off));
-  const double t = __dadd_rn(__ddiv_rn(p, (double)H), (double)eps);
-  const float r = __double2float_rn(__ddiv_rn(1.0, __dsqrt_rn(t)));
+  sumsq::warp_reduce(acc, 16);
+  const float r = sumsq::rms_scale(sumsq::round_to_f32(acc), H, eps);
 
   float a = 0.0f;
   for (int k = lane; k < H; k += 32) {

@@ -9,6 +9,7 @@
 // (codes, dot products, partial sums) is exact by construction.
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -105,6 +106,11 @@ __device__ __forceinline__ ActScale act_scale_from_absmax(float a) {
   return s;
 }
 
+// Nearest bf16 (ties to even) to a binary32 value, as its bit pattern.
+__device__ __forceinline__ uint16_t f32_to_bf16_rn(float v) {
+  return __bfloat16_as_ushort(__float2bfloat16_rn(v));
+}
+
 __device__ __forceinline__ uint32_t pack_i8x4(int a, int b, int c, int d) {
   return (uint32_t)(a & 0xff) | ((uint32_t)(b & 0xff) << 8) | ((uint32_t)(c & 0xff) << 16) |
          ((uint32_t)(d & 0xff) << 24);
@@ -165,38 +171,27 @@ struct DecodeTarget {
   const uint8_t* Wq;
   const float* w_scale;
   int64_t N;
-  float* y;
-  int32_t* acc_out;
+  float* y;          // binary32 output, or null
+  int32_t* acc_out;  // or null
+  uint16_t* y_bf16;  // bf16 output (nearest, ties to even), or null
 };
 bool decode_supported(int64_t M, int64_t K);
-
-// A chain of decode launches run by one persistent cooperative kernel, with a
-// grid-wide barrier between consecutive phases (gemv_decode.cu).
-struct DecodePhaseDesc {
-  const uint16_t* x;  // bf16 [M, K]
-  int64_t K;
-  const DecodeTarget* targets;
-  int count;
-};
-struct DecodeChainConfig {
-  int mt, j, stages, slot_bytes, xs_bytes, smem;
-};
-size_t decode_chain_bytes(int nphases);
-cudaError_t build_decode_chain(const DecodePhaseDesc* phases, int nphases, int64_t M, void* table,
-                               DecodeChainConfig* cfg);
-cudaError_t launch_decode_chain(const void* table, int nphases, int64_t M,
-                                const DecodeChainConfig& cfg, cudaStream_t s);
-// Reads and clears the error word of the decode kernel's bounded waits.
-cudaError_t read_and_clear_decode_error(int* code, cudaStream_t s);
 cudaError_t launch_decode(const DecodeTarget* targets, int count, const int8_t* xq,
                           const float* x_scale, const uint16_t* x_bf16, int64_t M, int64_t K,
                           int8_t* xq_out, float* x_scale_out, bool weights_static,
-                          cudaStream_t s);
+                          long long wait_cycles, cudaStream_t s);
+// Reads and clears the error word of the decode kernel's bounded waits.
+cudaError_t read_and_clear_decode_error(int* code, cudaStream_t s);
+// The same for decode chains (decode_chain.cu).
+cudaError_t read_and_clear_chain_error(int* code, cudaStream_t s);
+
+// Bound of the kernels' waits, in clocks (abi.cu; bitnet_set_wait_limit).
+long long wait_limit_cycles();
 
 // BitLinear on CUDA cores, any M (gemv.cu).
 size_t gemv_workspace(int64_t M, int64_t N, int64_t K);
 cudaError_t launch_gemv(const uint8_t* Wq, const float* w_scale, const int8_t* xq,
                         const float* x_scale, int64_t M, int64_t N, int64_t K, float* y,
-                        int32_t* acc_out, void* ws, cudaStream_t s);
+                        uint16_t* y_bf16, int32_t* acc_out, void* ws, cudaStream_t s);
 
 }  // namespace bitnet

@@ -1,0 +1,144 @@
+// exact_sumsq.cuh — the subln RMSNorm's sum of squares, exactly.
+//
+// "Microsoft BitNet b1.58 ... 1-bit AI model" (communeify), "Meet BitNet
+// b1.58 2B4T", names subln normalisation and no formula; the library's
+// reading is: t_k = x_k * x_k (one binary32 product), ss = the exact sum of
+// the t_k rounded once to binary32 (ties to even), r = 1 / sqrt(ss / H + eps)
+// in four binary32 operations.  The sum is exact and so independent of the
+// order of the additions: every finite binary32 value is an integer multiple
+// of 2^-149 below 2^277, so a sum of up to 2^16 squares is an integer below
+// 2^293 in those units, held here in five 64-bit limbs and added with carry
+// chains.  A NaN square makes ss NaN; otherwise an infinite square makes it
+// +Inf.  No binary64 arithmetic is involved.
+#pragma once
+
+#include <stdint.h>
+
+namespace bitnet {
+namespace sumsq {
+
+struct Acc {
+  uint64_t w[5];
+  uint32_t nan_, inf_;
+};
+
+__device__ __forceinline__ void zero(Acc& a) {
+#pragma unroll
+  for (int j = 0; j < 5; ++j) a.w[j] = 0;
+  a.nan_ = a.inf_ = 0;
+}
+
+__device__ __forceinline__ void add5(Acc& s, uint64_t a0, uint64_t a1, uint64_t a2, uint64_t a3,
+                                     uint64_t a4) {
+  asm("add.cc.u64 %0, %0, %5;\n\t"
+      "addc.cc.u64 %1, %1, %6;\n\t"
+      "addc.cc.u64 %2, %2, %7;\n\t"
+      "addc.cc.u64 %3, %3, %8;\n\t"
+      "addc.u64 %4, %4, %9;"
+      : "+l"(s.w[0]), "+l"(s.w[1]), "+l"(s.w[2]), "+l"(s.w[3]), "+l"(s.w[4])
+      : "l"(a0), "l"(a1), "l"(a2), "l"(a3), "l"(a4));
+}
+
+// Adds the binary32 value t (>= 0 or NaN/Inf) exactly.
+__device__ __forceinline__ void add_term(Acc& s, float t) {
+  const uint32_t u = __float_as_uint(t);
+  const uint32_t e = (u >> 23) & 0xffu, f = u & 0x7fffffu;
+  if (e == 255u) {
+    if (f) s.nan_ = 1;
+    else s.inf_ = 1;
+    return;
+  }
+  const uint64_t m = e ? (uint64_t)(f | 0x800000u) : (uint64_t)f;
+  const int o = e ? (int)e - 1 : 0;  // t = m * 2^(o - 149)
+  const int i = o >> 6, sh = o & 63;
+  const uint64_t lo = m << sh;
+  const uint64_t hi = sh > 40 ? (m >> (64 - sh)) : 0ull;  // m < 2^24
+  add5(s, i == 0 ? lo : 0ull, i == 1 ? lo : (i == 0 ? hi : 0ull),
+       i == 2 ? lo : (i == 1 ? hi : 0ull), i == 3 ? lo : (i == 2 ? hi : 0ull),
+       i == 3 ? hi : 0ull);
+}
+
+__device__ __forceinline__ uint64_t shfl_xor_u64(uint64_t v, int off, unsigned mask) {
+  const uint32_t lo = __shfl_xor_sync(mask, (uint32_t)v, off);
+  const uint32_t hi = __shfl_xor_sync(mask, (uint32_t)(v >> 32), off);
+  return ((uint64_t)hi << 32) | lo;
+}
+
+// Butterfly over the lanes l ^ off for off = first .. 1 (powers of two): every
+// participating lane ends with the sum of its group.
+__device__ __forceinline__ void warp_reduce(Acc& s, int first) {
+  for (int off = first; off >= 1; off >>= 1) {
+    uint64_t o[5];
+#pragma unroll
+    for (int j = 0; j < 5; ++j) o[j] = shfl_xor_u64(s.w[j], off, 0xffffffffu);
+    add5(s, o[0], o[1], o[2], o[3], o[4]);
+    s.nan_ |= __shfl_xor_sync(0xffffffffu, s.nan_, off);
+    s.inf_ |= __shfl_xor_sync(0xffffffffu, s.inf_, off);
+  }
+}
+
+__device__ __forceinline__ int bit_at(const Acc& s, int pos) {
+  if (pos < 0) return 0;
+  const int L = pos >> 6, b = pos & 63;
+  uint64_t w = 0;
+#pragma unroll
+  for (int j = 0; j < 5; ++j)
+    if (j == L) w = s.w[j];
+  return (int)((w >> b) & 1u);
+}
+
+// True if any bit below position pos is set.
+__device__ __forceinline__ bool any_below(const Acc& s, int pos) {
+  bool any = false;
+#pragma unroll
+  for (int j = 0; j < 5; ++j) {
+    const int lo = 64 * j;
+    if (pos >= lo + 64) any |= s.w[j] != 0;
+    else if (pos > lo) any |= (s.w[j] & ((1ull << (pos - lo)) - 1ull)) != 0;
+  }
+  return any;
+}
+
+// The nearest binary32 (ties to even) to the exact sum.
+__device__ __forceinline__ float round_to_f32(const Acc& s) {
+  if (s.nan_) return __uint_as_float(0x7fc00000u);
+  if (s.inf_) return __uint_as_float(0x7f800000u);
+  int bl = 0;
+#pragma unroll
+  for (int j = 0; j < 5; ++j)
+    if (s.w[j]) bl = 64 * j + 64 - __clzll((long long)s.w[j]);
+  if (bl == 0) return 0.0f;
+  int drop = bl > 24 ? bl - 24 : 0;
+  // bits [drop, drop + 24) of the sum
+  uint64_t lo = 0, hi = 0;
+  const int L = drop >> 6, b = drop & 63;
+#pragma unroll
+  for (int j = 0; j < 5; ++j) {
+    if (j == L) lo = s.w[j];
+    if (j == L + 1) hi = s.w[j];
+  }
+  uint64_t mant = (lo >> b) | (b ? (hi << (64 - b)) : 0ull);
+  mant &= 0xffffffull;
+  const int round_bit = bit_at(s, drop - 1);
+  const bool sticky = any_below(s, drop - 1);
+  if (round_bit && (sticky || (mant & 1u))) mant += 1;
+  if (mant == (1ull << 24)) {
+    mant >>= 1;
+    drop += 1;
+  }
+  // value = mant * 2^(drop - 149)
+  if (mant < (1ull << 23)) return __uint_as_float((uint32_t)mant);  // subnormal (drop == 0)
+  const int e8 = drop + 1;
+  if (e8 >= 255) return __uint_as_float(0x7f800000u);
+  return __uint_as_float(((uint32_t)e8 << 23) | ((uint32_t)mant & 0x7fffffu));
+}
+
+// r = 1 / sqrt(ss / H + eps), four binary32 operations.
+__device__ __forceinline__ float rms_scale(float ss, int H, float eps) {
+  const float q = __fdiv_rn(ss, (float)H);
+  const float t = __fadd_rn(q, eps);
+  return __fdiv_rn(1.0f, __fsqrt_rn(t));
+}
+
+}  // namespace sumsq
+}  // namespace bitnet

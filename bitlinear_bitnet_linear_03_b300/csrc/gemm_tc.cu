@@ -71,7 +71,7 @@ struct Tile {
   static constexpr int kStages = (kRingBytes - kBBufBytes) / kStageBytes;  // 4 or 6; 6 fused
   static constexpr int kSmemBytes = kStages * kStageBytes + kBBufBytes + 1024;  // + alignment
 };
-constexpr long long kWaitCycles = 2000000000ll;
+constexpr long long kDrainCycles = 2000000000ll;  // bound of the final drains (~1 s)
 constexpr int kErrProducer = 1 << 4, kErrMma = 1 << 5, kErrEpilogue = 1 << 6, kErrDrain = 1 << 7;
 
 // Operand element: bf16 (2 bytes), 64 elements of K per 128-byte stage row.
@@ -104,8 +104,10 @@ struct Args {
   int* tile_cnt;
   const float* x_scale;
   const float* w_scale;
-  float* y;
+  float* y;          // binary32 output, or null
+  uint16_t* y_bf16;  // bf16 output, or null
   int32_t* acc_out;
+  long long wait;    // bound of every wait but the final drains, in clocks
 };
 
 // Work item -> tile and K-stage range.
@@ -140,11 +142,11 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, long long limit) {
   if (mbar_try(bar, parity)) return true;
   const long long t0 = clock64();
   while (!mbar_try(bar, parity))
-    if (clock64() - t0 > kWaitCycles) return false;
+    if (clock64() - t0 > limit) return false;
   return true;
 }
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
@@ -227,23 +229,47 @@ __device__ __forceinline__ float ld_cg_f32(const float* p) {
   asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(p) : "memory");
   return v;
 }
-// y = acc * c and the accumulators for 32 consecutive outputs of one row.
-__device__ __forceinline__ void store_row32(float* yrow, int32_t* arow, int nb, const int (&v)[32],
-                                            float c, bool full_vec, int N) {
-  if (full_vec) {
+// y = acc * c (binary32 and/or bf16) and the accumulators for 32 consecutive
+// outputs of one row.  vec4: the 32 outputs are in range and 16-byte aligned
+// as binary32; vec8: also as bf16.
+__device__ __forceinline__ void store_row32(float* yrow, uint16_t* brow, int32_t* arow, int nb,
+                                            const int (&v)[32], float c, bool vec4, bool vec8,
+                                            int N) {
+  if (vec4) {
 #pragma unroll
-    for (int j = 0; j < 32; j += 4) {
-      float4 o = make_float4(__fmul_rn(__int2float_rn(v[j]), c), __fmul_rn(__int2float_rn(v[j + 1]), c),
-                             __fmul_rn(__int2float_rn(v[j + 2]), c),
-                             __fmul_rn(__int2float_rn(v[j + 3]), c));
-      *reinterpret_cast<float4*>(yrow + nb + j) = o;
-      if (arow) *reinterpret_cast<int4*>(arow + nb + j) = make_int4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+    for (int j = 0; j < 32; j += 8) {
+      float o[8];
+#pragma unroll
+      for (int t = 0; t < 8; ++t) o[t] = __fmul_rn(__int2float_rn(v[j + t]), c);
+      if (yrow) {
+        *reinterpret_cast<float4*>(yrow + nb + j) = make_float4(o[0], o[1], o[2], o[3]);
+        *reinterpret_cast<float4*>(yrow + nb + j + 4) = make_float4(o[4], o[5], o[6], o[7]);
+      }
+      if (brow) {
+        uint32_t w[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t)
+          w[t] = (uint32_t)f32_to_bf16_rn(o[2 * t]) | ((uint32_t)f32_to_bf16_rn(o[2 * t + 1]) << 16);
+        if (vec8) {
+          *reinterpret_cast<uint4*>(brow + nb + j) = make_uint4(w[0], w[1], w[2], w[3]);
+        } else {
+#pragma unroll
+          for (int t = 0; t < 8; ++t) brow[nb + j + t] = (uint16_t)(w[t >> 1] >> (16 * (t & 1)));
+        }
+      }
+      if (arow) {
+        *reinterpret_cast<int4*>(arow + nb + j) = make_int4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+        *reinterpret_cast<int4*>(arow + nb + j + 4) =
+            make_int4(v[j + 4], v[j + 5], v[j + 6], v[j + 7]);
+      }
     }
   } else {
 #pragma unroll
     for (int j = 0; j < 32; ++j)
       if (nb + j < N) {
-        yrow[nb + j] = __fmul_rn(__int2float_rn(v[j]), c);
+        const float o = __fmul_rn(__int2float_rn(v[j]), c);
+        if (yrow) yrow[nb + j] = o;
+        if (brow) brow[nb + j] = f32_to_bf16_rn(o);
         if (arow) arow[nb + j] = v[j];
       }
   }
@@ -350,7 +376,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUte
         const int m0 = (t % a.m_tiles) * kBM, n0 = (t / a.m_tiles) * BN;
         for (int ks = ks0; ks < ks1; ++ks, ++it) {
           const int s = it % kStages;
-          if (it >= kStages && !mbar_wait(saddr(&empty_bar[s]), ((it / kStages) - 1) & 1)) {
+          if (it >= kStages && !mbar_wait(saddr(&empty_bar[s]), ((it / kStages) - 1) & 1, a.wait)) {
             atomicOr(&g_device_error, kErrProducer);
             *(volatile int*)&s_abort = 1;
             ok = false;
@@ -378,7 +404,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUte
       }
       // Never return with a copy in flight.
       for (int j = issued > kStages ? issued - kStages : 0; j < issued; ++j)
-        if (!mbar_wait(saddr(&full_bar[j % kStages]), (j / kStages) & 1)) {
+        if (!mbar_wait(saddr(&full_bar[j % kStages]), (j / kStages) & 1, kDrainCycles)) {
           atomicOr(&g_device_error, kErrDrain);
           break;
         }
@@ -393,7 +419,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUte
         item_range(a, item, t, ks0, ks1);
         (void)t;
         const int ab = lt & 1;
-        if (lt >= 2 && !mbar_wait(saddr(&acc_empty[ab]), ((lt >> 1) - 1) & 1)) {
+        if (lt >= 2 && !mbar_wait(saddr(&acc_empty[ab]), ((lt >> 1) - 1) & 1, a.wait)) {
           atomicOr(&g_device_error, kErrMma);
           *(volatile int*)&s_abort = 1;
           break;
@@ -404,8 +430,8 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUte
           const int s = it % kStages, b = it & 1;
           // fused: the expanded B buffer (and the A tile of the stage, whose
           // landing the converters waited for and which is checked again)
-          bool ready = mbar_wait(saddr(&full_bar[s]), (it / kStages) & 1);
-          if (FUSED && ready) ready = mbar_wait(saddr(&bready_bar[b]), (it >> 1) & 1);
+          bool ready = mbar_wait(saddr(&full_bar[s]), (it / kStages) & 1, a.wait);
+          if (FUSED && ready) ready = mbar_wait(saddr(&bready_bar[b]), (it >> 1) & 1, a.wait);
           if (!ready || *(volatile int*)&s_abort) {
             atomicOr(&g_device_error, kErrMma);
             *(volatile int*)&s_abort = 1;
@@ -430,7 +456,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUte
       }
       // All MMAs issued by this thread have finished before TMEM is freed.
       tc_commit(saddr(&drain_bar));
-      if (!mbar_wait(saddr(&drain_bar), 0)) atomicOr(&g_device_error, kErrDrain);
+      if (!mbar_wait(saddr(&drain_bar), 0, kDrainCycles)) atomicOr(&g_device_error, kErrDrain);
     }
   } else if (FUSED && warp >= 6) {
     // ------------------------------------------------------------ B expansion
@@ -443,11 +469,11 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUte
       bool ok = true;
       for (int ks = ks0; ks < ks1; ++ks, ++it) {
         const int s = it % kStages, b = it & 1;
-        bool ready = mbar_wait(saddr(&full_bar[s]), (it / kStages) & 1);
+        bool ready = mbar_wait(saddr(&full_bar[s]), (it / kStages) & 1, a.wait);
         // the MMAs of two stages ago (which read buffer b) have finished: that
         // stage's ring slot was released, by them and by these warps
         if (ready && it >= 2)
-          ready = mbar_wait(saddr(&empty_bar[(it - 2) % kStages]), ((it - 2) / kStages) & 1);
+          ready = mbar_wait(saddr(&empty_bar[(it - 2) % kStages]), ((it - 2) / kStages) & 1, a.wait);
         if (!ready || *(volatile int*)&s_abort) {
           if (lane == 0) atomicOr(&g_device_error, kErrProducer);
           *(volatile int*)&s_abort = 1;
@@ -477,7 +503,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUte
       item_range(a, item, t, ks0, ks1);
       const int ab = lt & 1;
       const bool bad =
-          !mbar_wait(saddr(&acc_full[ab]), (lt >> 1) & 1) || *(volatile int*)&s_abort;
+          !mbar_wait(saddr(&acc_full[ab]), (lt >> 1) & 1, a.wait) || *(volatile int*)&s_abort;
       if (epi_sync_or(bad)) {  // uniform over the epilogue warps
         if (lane == 0) atomicOr(&g_device_error, kErrEpilogue);
         *(volatile int*)&s_abort = 1;
@@ -488,10 +514,12 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUte
       const int m = m0 + row;
       const bool mrow = m < a.M;
       const float c = mrow ? __fmul_rn(a.x_scale[m], ws) : 0.0f;
-      float* yrow = a.y + (int64_t)m * a.N;
+      float* yrow = a.y ? a.y + (int64_t)m * a.N : nullptr;
+      uint16_t* brow = a.y_bf16 ? a.y_bf16 + (int64_t)m * a.N : nullptr;
       int32_t* arow = a.acc_out ? a.acc_out + (int64_t)m * a.N : nullptr;
       float* wrow = a.acc_ws + (int64_t)m * a.N;
       const bool vec = (a.N & 3) == 0;
+      const bool vec8 = (a.N & 7) == 0;
       for (int cb = 0; cb < BN; cb += 32) {
         uint32_t r[32];
         tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(ab * BN + cb), r);
@@ -515,7 +543,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUte
 #pragma unroll
         for (int j = 0; j < 32; ++j)
           v[j] = __float2int_rn(__uint_as_float(r[j]));  // exact integer
-        store_row32(yrow, arow, nb, v, c, vec && nb + 32 <= a.N, a.N);
+        store_row32(yrow, brow, arow, nb, v, c, vec && nb + 32 <= a.N, vec8, a.N);
       }
       tc_fence_before();
       __syncwarp();
@@ -536,7 +564,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUte
 #pragma unroll
               for (int j = 0; j < 32; ++j)
                 v[j] = nb + j < a.N ? __float2int_rn(ld_cg_f32(wrow + nb + j)) : 0;
-              store_row32(yrow, arow, nb, v, c, vec && nb + 32 <= a.N, a.N);
+              store_row32(yrow, brow, arow, nb, v, c, vec && nb + 32 <= a.N, vec8, a.N);
             }
         }
       }
@@ -695,7 +723,8 @@ WsLayout ws_layout(int64_t M, int64_t N, int64_t K) {
 template <int KIND, int BN, bool FUSED>
 cudaError_t launch_kind(const uint8_t* Wq, const float* w_scale, const int8_t* xq,
                         const float* x_scale, int64_t M, int64_t N, int64_t K, float* y,
-                        int32_t* acc_out, void* ws, cudaStream_t s) {
+                        uint16_t* y_bf16, int32_t* acc_out, void* ws, long long wait,
+                        cudaStream_t s) {
   cudaError_t e = get_encode();
   if (e != cudaSuccess) return e;
   const WsLayout L = ws_layout(M, N, K);
@@ -735,7 +764,9 @@ cudaError_t launch_kind(const uint8_t* Wq, const float* w_scale, const int8_t* x
   a.x_scale = x_scale;
   a.w_scale = w_scale;
   a.y = y;
+  a.y_bf16 = y_bf16;
   a.acc_out = acc_out;
+  a.wait = wait;
   static bool configured[64] = {};
   int dev = 0;
   e = cudaGetDevice(&dev);
@@ -764,12 +795,16 @@ size_t gemm_tc_workspace(int64_t M, int64_t N, int64_t K) { return ws_layout(M, 
 
 cudaError_t launch_gemm_tc(const uint8_t* Wq, const float* w_scale, const int8_t* xq,
                            const float* x_scale, int64_t M, int64_t N, int64_t K, float* y,
-                           int32_t* acc_out, void* ws, cudaStream_t s) {
+                           uint16_t* y_bf16, int32_t* acc_out, void* ws, long long wait,
+                           cudaStream_t s) {
   if (use_fused(M))
-    return launch_kind<kKind, 256, true>(Wq, w_scale, xq, x_scale, M, N, K, y, acc_out, ws, s);
+    return launch_kind<kKind, 256, true>(Wq, w_scale, xq, x_scale, M, N, K, y, y_bf16, acc_out,
+                                         ws, wait, s);
   if (pick_bn(N) == 128)
-    return launch_kind<kKind, 128, false>(Wq, w_scale, xq, x_scale, M, N, K, y, acc_out, ws, s);
-  return launch_kind<kKind, 256, false>(Wq, w_scale, xq, x_scale, M, N, K, y, acc_out, ws, s);
+    return launch_kind<kKind, 128, false>(Wq, w_scale, xq, x_scale, M, N, K, y, y_bf16, acc_out,
+                                          ws, wait, s);
+  return launch_kind<kKind, 256, false>(Wq, w_scale, xq, x_scale, M, N, K, y, y_bf16, acc_out, ws,
+                                        wait, s);
 }
 
 cudaError_t read_and_clear_device_error(int* code, cudaStream_t s) {

@@ -11,7 +11,8 @@ bool gemm_tc_eligible(int64_t M, int64_t N, int64_t K);
 size_t gemm_tc_workspace(int64_t M, int64_t N, int64_t K);
 cudaError_t launch_gemm_tc(const uint8_t* Wq, const float* w_scale, const int8_t* xq,
                            const float* x_scale, int64_t M, int64_t N, int64_t K, float* y,
-                           int32_t* acc_out, void* ws, cudaStream_t s);
+                           uint16_t* y_bf16, int32_t* acc_out, void* ws, long long wait,
+                           cudaStream_t s);
 
 // Reads and clears the per-device error word that bounded waits set.
 cudaError_t read_and_clear_device_error(int* code, cudaStream_t s);

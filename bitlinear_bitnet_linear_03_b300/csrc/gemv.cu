@@ -11,7 +11,7 @@
 // accumulator (scaled by 4^s); the scales are removed exactly by arithmetic
 // shifts at the end.  All sums are integers, so the result is exact and
 // independent of order; the rescale y = (float)acc * (x_scale * w_scale) is
-// two binary32 products.
+// two binary32 products, stored as binary32 and/or rounded to bf16.
 //
 // Work split: a CTA owns WARPS*RPW consecutive output rows, MT tokens and one
 // K-slice.  The CTA stages its tokens' int8 activations for the slice in
@@ -35,8 +35,8 @@ template <int MT, int RPW>
 __global__ void __launch_bounds__(kThreads)
 k_gemv(const uint8_t* __restrict__ Wq, const float* __restrict__ w_scale,
        const int8_t* __restrict__ xq, const float* __restrict__ x_scale, int M, int N, int K,
-       int ks_len, float* __restrict__ y, int32_t* __restrict__ acc_out,
-       int32_t* __restrict__ part) {
+       int ks_len, float* __restrict__ y, uint16_t* __restrict__ y_bf16,
+       int32_t* __restrict__ acc_out, int32_t* __restrict__ part) {
   extern __shared__ uint4 xs[];
   __shared__ int sumx[MT];
   const int split = blockIdx.z;
@@ -123,7 +123,9 @@ k_gemv(const uint8_t* __restrict__ Wq, const float* __restrict__ w_scale,
         if (part) {
           part[((int64_t)split * M + mm) * N + n] = a;
         } else {
-          y[(int64_t)mm * N + n] = __fmul_rn(__int2float_rn(a), __fmul_rn(x_scale[mm], ws));
+          const float v = __fmul_rn(__int2float_rn(a), __fmul_rn(x_scale[mm], ws));
+          if (y) y[(int64_t)mm * N + n] = v;
+          if (y_bf16) y_bf16[(int64_t)mm * N + n] = f32_to_bf16_rn(v);
           if (acc_out) acc_out[(int64_t)mm * N + n] = a;
         }
       }
@@ -134,7 +136,7 @@ k_gemv(const uint8_t* __restrict__ Wq, const float* __restrict__ w_scale,
 __global__ void k_splitk_reduce(const int32_t* __restrict__ part, int splits, int M, int N,
                                 const float* __restrict__ w_scale,
                                 const float* __restrict__ x_scale, float* __restrict__ y,
-                                int32_t* __restrict__ acc_out) {
+                                uint16_t* __restrict__ y_bf16, int32_t* __restrict__ acc_out) {
   const int64_t total = (int64_t)M * N;
   const float ws = *w_scale;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
@@ -142,7 +144,9 @@ __global__ void k_splitk_reduce(const int32_t* __restrict__ part, int splits, in
     int a = 0;
     for (int s = 0; s < splits; ++s) a += part[(int64_t)s * total + i];
     const int m = (int)(i / N);
-    y[i] = __fmul_rn(__int2float_rn(a), __fmul_rn(x_scale[m], ws));
+    const float v = __fmul_rn(__int2float_rn(a), __fmul_rn(x_scale[m], ws));
+    if (y) y[i] = v;
+    if (y_bf16) y_bf16[i] = f32_to_bf16_rn(v);
     if (acc_out) acc_out[i] = a;
   }
 }
@@ -177,9 +181,9 @@ Plan make_plan(int64_t M, int64_t N, int64_t K) {
 template <int MT, int RPW>
 void launch_kernel(const Plan& p, cudaStream_t s, const uint8_t* Wq, const float* w_scale,
                    const int8_t* xq, const float* x_scale, int M, int N, int K, float* y,
-                   int32_t* acc_out, int32_t* part) {
+                   uint16_t* y_bf16, int32_t* acc_out, int32_t* part) {
   k_gemv<MT, RPW><<<p.grid, kThreads, p.smem, s>>>(Wq, w_scale, xq, x_scale, M, N, K, p.ks_len,
-                                                   y, acc_out, part);
+                                                   y, y_bf16, acc_out, part);
 }
 
 }  // namespace
@@ -191,15 +195,15 @@ size_t gemv_workspace(int64_t M, int64_t N, int64_t K) {
 
 cudaError_t launch_gemv(const uint8_t* Wq, const float* w_scale, const int8_t* xq,
                         const float* x_scale, int64_t M, int64_t N, int64_t K, float* y,
-                        int32_t* acc_out, void* ws, cudaStream_t s) {
+                        uint16_t* y_bf16, int32_t* acc_out, void* ws, cudaStream_t s) {
   const Plan p = make_plan(M, N, K);
   int32_t* part = p.splits > 1 ? static_cast<int32_t*>(ws) : nullptr;
   const int m = (int)M, n = (int)N, k = (int)K;
   switch (p.mt) {
-    case 1: launch_kernel<1, 4>(p, s, Wq, w_scale, xq, x_scale, m, n, k, y, acc_out, part); break;
-    case 2: launch_kernel<2, 4>(p, s, Wq, w_scale, xq, x_scale, m, n, k, y, acc_out, part); break;
-    case 4: launch_kernel<4, 2>(p, s, Wq, w_scale, xq, x_scale, m, n, k, y, acc_out, part); break;
-    default: launch_kernel<8, 2>(p, s, Wq, w_scale, xq, x_scale, m, n, k, y, acc_out, part); break;
+    case 1: launch_kernel<1, 4>(p, s, Wq, w_scale, xq, x_scale, m, n, k, y, y_bf16, acc_out, part); break;
+    case 2: launch_kernel<2, 4>(p, s, Wq, w_scale, xq, x_scale, m, n, k, y, y_bf16, acc_out, part); break;
+    case 4: launch_kernel<4, 2>(p, s, Wq, w_scale, xq, x_scale, m, n, k, y, y_bf16, acc_out, part); break;
+    default: launch_kernel<8, 2>(p, s, Wq, w_scale, xq, x_scale, m, n, k, y, y_bf16, acc_out, part); break;
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || p.splits == 1) return e;
@@ -207,7 +211,7 @@ cudaError_t launch_gemv(const uint8_t* Wq, const float* w_scale, const int8_t* x
   int64_t grid = (total + 255) / 256;
   if (grid > 148 * 8) grid = 148 * 8;
   k_splitk_reduce<<<(unsigned)grid, 256, 0, s>>>(part, p.splits, m, n, w_scale, x_scale, y,
-                                                 acc_out);
+                                                 y_bf16, acc_out);
   return cudaGetLastError();
 }
 

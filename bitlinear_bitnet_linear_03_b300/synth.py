@@ -40,6 +40,23 @@ def tokens_bf16(M: int, K: int, seed: int, outlier_frac: float = 0.0,
     return xb.view(torch.int16).numpy().view(np.uint16)
 
 
+def ternary_codes(N: int, K: int, seed: int, zero_frac: float = 0.31):
+    """Ternary weights drawn directly (int8 in {-1, 0, +1}; a fraction
+    zero_frac of zeros, the rest +-1 with equal odds): a cheap stand-in for
+    absmean-quantised N(0, sigma) weights, whose zero fraction is about 0.31,
+    for tests that need many large matrices on the host."""
+    g = torch.Generator().manual_seed(seed)
+    u = torch.rand((N, K), generator=g)
+    q = torch.where(u < zero_frac, 0, torch.where(u < (1 + zero_frac) / 2, -1, 1))
+    return q.to(torch.int8).numpy()
+
+
+def weight_scale(seed: int):
+    """A positive binary32 scale near the absmean of N(0, 0.02) weights."""
+    g = torch.Generator().manual_seed(seed)
+    return np.float32(0.016 * (1.0 + 0.05 * torch.rand(1, generator=g).item()))
+
+
 def gain_ones(H: int):
     return np.ones(H, np.float32)
 

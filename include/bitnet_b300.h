@@ -37,7 +37,9 @@
  *      BITNET_ERR_UNSUPPORTED the current device is not compute capability
  *                            10.3 (sm_103);
  *      BITNET_ERR_CUDA       a CUDA call or launch failed (code in
- *                            bitnet_last_cuda_error()).
+ *                            bitnet_last_cuda_error());
+ *      BITNET_ERR_ALIAS      arrays of a decode chain overlap in a way the
+ *                            chain does not allow (bitnet_decode_chain_build).
  *  - Inputs must be finite; see each call for what non-finite input gives.
  *  - No C++ exception crosses this interface.
  */
@@ -58,7 +60,8 @@ typedef enum bitnet_status {
   BITNET_ERR_ALIGN = 3,
   BITNET_ERR_WORKSPACE = 4,
   BITNET_ERR_UNSUPPORTED = 5,
-  BITNET_ERR_CUDA = 6
+  BITNET_ERR_CUDA = 6,
+  BITNET_ERR_ALIAS = 7
 } bitnet_status;
 
 /* Largest K, H or F accepted (int32 partial sums stay exact below it). */
@@ -75,8 +78,19 @@ int bitnet_abi_version(void);
 
 /* Reads and clears the current device's error word: 0, or a code set by a
  * kernel whose internal wait ran past its time limit (the kernel then
- * returns without finishing its output).  Synchronises `stream`. */
+ * returns without finishing its output).  Synchronises `stream`.  Bits 0-7:
+ * tensor-core kernel; bits 8-15: single decode launches; bits 16-23: decode
+ * chains (bit 16: a chain input was not produced in time; 17, 18: the weight
+ * ring; 19: the final wait for copies in flight). */
 bitnet_status bitnet_device_error(int* code_out, void* stream);
+
+/* For tests of the time-out path: the bound, in SM clock cycles, of every
+ * wait inside the library's kernels other than the final wait for their own
+ * copies in flight (which keeps its bound of about one second, so that no
+ * kernel ever returns with a copy outstanding).  0 restores the default
+ * (2e9 cycles, about one second).  Applies to launches made after the call,
+ * on every device; not thread-safe against concurrent launches. */
+void bitnet_set_wait_limit(long long cycles);
 
 /* ------------------------------------------------------------------------
  * Weight quantisation ([P2] §2; [P3] §2.3; [P5]).
@@ -130,9 +144,12 @@ bitnet_status bitnet_quantize_act(const uint16_t* x, int64_t M, int64_t K,
  * BitLinear ([P3] §3.1; rescale: [P1] no bias).
  *   acc[m,n] = sum over k of q[n,k] * xq[m,k]  (= sum_pos - sum_neg, exact
  *              int32), q unpacked from Wq;
- *   y[m,n]   = (float)acc[m,n] * (x_scale[m] * w_scale[0]).
- * Wq [N, K/4] bytes, w_scale [1], xq [M, K], x_scale [M], y [M, N] float.
- * acc_out: optional [M, N] int32 copy of acc (NULL to skip).
+ *   y[m,n]   = (float)acc[m,n] * (x_scale[m] * w_scale[0]);
+ *   y_bf16   = y rounded to the nearest bf16 (ties to even).
+ * Wq [N, K/4] bytes, w_scale [1], xq [M, K], x_scale [M].  Outputs, each
+ * optional but at least one of y / y_bf16 required: y [M, N] float,
+ * y_bf16 [M, N] bf16 (the rescale "to fp32/bf16"; with y NULL the binary32
+ * result is never stored), acc_out [M, N] int32 copy of acc.
  * ws: scratch of bitnet_linear_workspace(M, N, K) bytes (0 when none is
  * needed), no initial contents required.  M <= 4096*64 rows per call;
  * K % 64 == 0.  Paths, all giving the same bits: M <= 4 streams the packed
@@ -144,8 +161,8 @@ bitnet_status bitnet_quantize_act(const uint16_t* x, int64_t M, int64_t K,
 size_t bitnet_linear_workspace(int64_t M, int64_t N, int64_t K);
 bitnet_status bitnet_linear(const uint8_t* Wq, const float* w_scale,
                             const int8_t* xq, const float* x_scale, int64_t M,
-                            int64_t N, int64_t K, float* y, int32_t* acc_out,
-                            void* ws, size_t ws_bytes, void* stream);
+                            int64_t N, int64_t K, float* y, uint16_t* y_bf16,
+                            int32_t* acc_out, void* ws, size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
  * Decode BitLinear from bf16 activations ([P1] W1.58A8; [P3] §3.1).
@@ -155,7 +172,8 @@ bitnet_status bitnet_linear(const uint8_t* Wq, const float* w_scale,
  *             bitnet_quantize_act, bit for bit);
  *   y_i     = BitLinear(Wq_i, w_scale_i; xq, sx)  (the rule of bitnet_linear).
  * x: [M, K] bf16, 1 <= M <= BITNET_DECODE_MAX_M.  targets[i]: Wq [N_i, K/4]
- * packed, w_scale [1], y [M, N_i] float, acc_out optional [M, N_i] int32.
+ * packed, w_scale [1]; outputs y [M, N_i] float and y_bf16 [M, N_i] bf16
+ * (at least one of the two), acc_out optional [M, N_i] int32.
  * xq_out [M, K] and x_scale_out [M] are optional copies of xq and sx.
  * K % 64 == 0; K <= 65536 for M = 1, 32768 for M = 2, 16384 for M <= 4
  * (BITNET_ERR_SHAPE beyond); sum of N_i <= 2^30.  Needs no workspace.  The
@@ -175,6 +193,7 @@ typedef struct bitnet_linear_target {
   int64_t N;
   float* y;
   int32_t* acc_out;
+  uint16_t* y_bf16;
 } bitnet_linear_target;
 
 bitnet_status bitnet_linear_bf16(const uint16_t* x, int64_t M, int64_t K,
@@ -183,40 +202,64 @@ bitnet_status bitnet_linear_bf16(const uint16_t* x, int64_t M, int64_t K,
                                  void* stream);
 
 /* ------------------------------------------------------------------------
- * A decode chain: a sequence of bitnet_linear_bf16 phases (e.g. the QKV, O,
- * up+gate and down projections of every layer of a decoder step) run by one
- * persistent kernel.  Phase p computes, for each of its targets,
- *   y_i = BitLinear(Wq_i, w_scale_i; quant(x_p))     (rules of bitnet_linear_bf16)
- * and no CTA reads the input of phase p+1 before every CTA has written all
- * of its outputs of phase p (a grid-wide barrier): the phases are ordered
- * exactly as separate dependent launches on one stream would be.  The weights are
- * streamed ahead across phase boundaries: no work in flight on `stream` may
- * write any Wq or w_scale of the chain (BITNET_WEIGHTS_STATIC semantics).
- * phases[p]: x [M, K_p] bf16, 1 <= M <= BITNET_DECODE_MAX_M, targets as in
- * bitnet_linear_bf16 (1 .. BITNET_MAX_TARGETS, the same K limits).
- * table: device memory of bitnet_decode_chain_bytes(nphases) bytes, 256-byte
- * aligned, owned by the caller; _build fills it (synchronously: call it
- * outside stream capture, it returns after the copy) and zeroes its barrier
- * word.  `chain` (host) receives what _run needs.  Runs of one table must not
- * overlap on the GPU.  The kernel needs all of its 148 CTAs resident at once
- * (cooperative launch); _run returns BITNET_ERR_CUDA if the launch is refused.
- * After a run that reported a device error (bitnet_device_error), build the
- * chain again before the next run. */
+ * A decode chain: the BitLinear phases of a decoder step (e.g. QKV, O,
+ * up+gate, down of every layer) run by one persistent kernel, one CTA per SM
+ * ([P1] BitLinear, subln, ReLU^2; [P5] HN comment: memory bandwidth is the
+ * bottleneck, so the weights of later phases stream in while earlier phases
+ * compute).  Phase p:
+ *   input   = x [M, K] bf16, or x_f32 [M, K] binary32 (exactly one given);
+ *   norm    = optional subln RMSNorm of a bf16 input with gain norm_gain [K]
+ *             and norm_eps (the rule of bitnet_ffn's normalisation);
+ *   xq, sx  = per-token int8 quantisation of the (normalised) input (the
+ *             rule of bitnet_quantize_act; for a binary32 input the same rule
+ *             on its values);
+ *   targets as in bitnet_linear_bf16 (outputs y, y_bf16, acc_out);
+ *   flags & BITNET_PHASE_GATED: exactly two targets of equal N, up and gate;
+ *             h = (t * t) * u with t = max(v, 0), u and v the two BitLinear
+ *             results (the rule of bitnet_ffn), written to h [M, N]; the
+ *             targets' own outputs are then optional.
+ *   xq_out [M, K], x_scale_out [M]: optional copies of xq and sx.
+ * Links: a phase input that IS an output of an earlier phase (x equal to a
+ * target's y_bf16, or x_f32 equal to a target's y or a gated phase's h, with
+ * N == K) is read as that phase produces it: each value travels with a tag of
+ * the run and phase through the chain's table, and a CTA waits only for the
+ * values it reads.  There is no other ordering between phases: every other
+ * array the chain reads (x, x_f32, norm_gain, Wq, w_scale) must not overlap
+ * any array the chain writes, and the arrays it writes must not overlap one
+ * another (BITNET_ERR_ALIAS otherwise).  A CTA that owns no rows of a phase
+ * skips it.  The weights stream in ahead, across phases.
+ * table: device memory of bitnet_decode_chain_bytes(phases, nphases, M)
+ * bytes, 256-byte aligned, owned by the caller; _build fills it
+ * (synchronously: call it outside stream capture; it returns after the
+ * copy) and clears it.  `chain` (host) receives what _run needs.  Runs of one
+ * table must not overlap on the GPU.  All CTAs must be resident at once
+ * (cooperative launch); _run returns BITNET_ERR_CUDA if the launch is
+ * refused.  After a run that reported a device error (bitnet_device_error),
+ * build the chain again before the next run.  At most 16384 phases. */
+#define BITNET_PHASE_GATED 1u
 typedef struct bitnet_decode_phase {
   const uint16_t* x;
   int64_t K;
   const bitnet_linear_target* targets;
   int count;
+  unsigned flags;
+  const float* x_f32;
+  const float* norm_gain;
+  float norm_eps;
+  float* h;
+  int8_t* xq_out;
+  float* x_scale_out;
 } bitnet_decode_phase;
 
 typedef struct bitnet_decode_chain {
   void* table;
   int64_t M;
   int nphases;
-  int cfg[6]; /* launch configuration, filled by bitnet_decode_chain_build */
+  int cfg[8]; /* launch configuration, filled by bitnet_decode_chain_build */
 } bitnet_decode_chain;
 
-size_t bitnet_decode_chain_bytes(int nphases);
+/* 0 if the description is invalid (the same checks as _build). */
+size_t bitnet_decode_chain_bytes(const bitnet_decode_phase* phases, int nphases, int64_t M);
 bitnet_status bitnet_decode_chain_build(const bitnet_decode_phase* phases, int nphases,
                                         int64_t M, void* table, size_t table_bytes,
                                         bitnet_decode_chain* chain);
@@ -224,9 +267,10 @@ bitnet_status bitnet_decode_chain_run(const bitnet_decode_chain* chain, void* st
 
 /* ------------------------------------------------------------------------
  * Fused BitNet feed-forward block ([P1] subln, ReLU^2, no bias):
- *   r   = (float)(1 / sqrt(ss / H + eps)), ss = sum x^2 (binary64, in the
- *         order: 32 strided partial sums over k = l (mod 32), increasing k,
- *         then pairwise p[l] + p[l ^ off] for off = 16, 8, 4, 2, 1);
+ *   ss  = sum over k of x_k * x_k: each square one binary32 product, the
+ *         sum exact (order-free) and rounded once to binary32;
+ *   r   = 1 / sqrt(ss / H + eps), four binary32 operations in that order
+ *         (division, addition, correctly rounded square root, division);
  *   nrm = (x * r) * g;                          binary32, per element
  *   xq, sx = per-token int8 quantisation of nrm (rule of bitnet_quantize_act)
  *   u   = BitLinear(Wup, s_up; xq, sx)          [M, F]

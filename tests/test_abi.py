@@ -47,8 +47,8 @@ def test_binding_covers_every_symbol():
 
 def test_status_strings_and_version():
     L = bn.lib()
-    assert L.bitnet_abi_version() == 1
-    for s in range(7):
+    assert L.bitnet_abi_version() == 2
+    for s in range(8):
         assert L.bitnet_status_string(s)
     assert L.bitnet_status_string(99) == b"unknown status"
 
@@ -90,21 +90,26 @@ def p(v):
 def test_argument_errors_are_reported_before_launch():
     L = bn.lib()
     # NULL pointers
-    assert L.bitnet_linear(None, p(FAKE), p(FAKE), p(FAKE), 1, 64, 64, p(FAKE), None, None, 0,
-                           None) == 1
+    assert L.bitnet_linear(None, p(FAKE), p(FAKE), p(FAKE), 1, 64, 64, p(FAKE), None, None, None,
+                           0, None) == 1
+    # neither output form requested
+    assert L.bitnet_linear(p(FAKE), p(FAKE), p(FAKE), p(FAKE), 1, 64, 64, None, None, None, None,
+                           0, None) == 1
     assert L.bitnet_quantize_act(None, 1, 64, p(FAKE), p(FAKE), None) == 1
     assert L.bitnet_quantize_weights(p(FAKE), 1, 64, None, p(FAKE), p(FAKE), 1 << 20, None) == 1
     # shapes: K not a multiple of 64, non-positive sizes, K too large
     assert L.bitnet_linear(p(FAKE), p(FAKE), p(FAKE), p(FAKE), 1, 64, 100, p(FAKE), None, None,
-                           0, None) == 2
-    assert L.bitnet_linear(p(FAKE), p(FAKE), p(FAKE), p(FAKE), 0, 64, 64, p(FAKE), None, None, 0,
-                           None) == 2
+                           None, 0, None) == 2
+    assert L.bitnet_linear(p(FAKE), p(FAKE), p(FAKE), p(FAKE), 0, 64, 64, p(FAKE), None, None,
+                           None, 0, None) == 2
     assert L.bitnet_quantize_act(p(FAKE), 1, 65536 + 64, p(FAKE), p(FAKE), None) == 2
     assert L.bitnet_quantize_weights(p(FAKE), 3, 96, p(FAKE), p(FAKE), p(FAKE), 1 << 20,
                                      None) == 2
     # misaligned pointers
-    assert L.bitnet_linear(p(MIS), p(FAKE), p(FAKE), p(FAKE), 1, 64, 64, p(FAKE), None, None, 0,
-                           None) == 3
+    assert L.bitnet_linear(p(MIS), p(FAKE), p(FAKE), p(FAKE), 1, 64, 64, p(FAKE), None, None,
+                           None, 0, None) == 3
+    assert L.bitnet_linear(p(FAKE), p(FAKE), p(FAKE), p(FAKE), 1, 64, 64, None, p(MIS), None,
+                           None, 0, None) == 3
     assert L.bitnet_quantize_act(p(FAKE), 1, 64, p(MIS), p(FAKE), None) == 3
     # workspace too small
     need = L.bitnet_quantize_weights_workspace(64, 64)
@@ -119,40 +124,115 @@ def test_argument_errors_are_reported_before_launch():
     assert L.bitnet_device_error(None, None) == 1
 
 
+class FakeMem:
+    """Distinct fake device addresses (never dereferenced: every check below
+    fails, or passes, on the host before anything touches a device)."""
+
+    def __init__(self):
+        self.next = 0x1000000
+
+    def __call__(self, nbytes):
+        a = self.next
+        self.next += (nbytes + 4095) // 4096 * 4096 + 4096
+        return a
+
+
+def _chain_phase(mem, K=2560, Ns=(64,), M=1, x=None, x_f32=None, gated=False, h=None, ys=None,
+                 ybs=None, norm=False, bf16_out=False):
+    count = len(Ns)
+    ys = ys or [None] * count
+    ybs = ybs or [None] * count
+    tg = (_lib.LinearTarget * count)()
+    for i, N in enumerate(Ns):
+        y = ys[i] if ys[i] is not None else (None if bf16_out else mem(4 * M * N))
+        yb = ybs[i] if ybs[i] is not None else (mem(2 * M * N) if bf16_out else None)
+        tg[i] = _lib.LinearTarget(mem(N * K // 4), mem(16), N, y, None, yb)
+    if x is None and x_f32 is None:
+        x = mem(2 * M * K)
+    ph = _lib.DecodePhase(x, K, ctypes.cast(tg, ctypes.c_void_p), count, 1 if gated else 0, x_f32,
+                          mem(4 * K) if norm else None, 1e-5, h, None, None)
+    return ph, tg
+
+
+def _chain_status(L, phases, M=1, table=0x100000, nbytes=None):
+    arr = (_lib.DecodePhase * len(phases))(*[ph for ph, _ in phases])
+    chain = _lib.DecodeChain()
+    n = len(phases)
+    need = L.bitnet_decode_chain_bytes(arr, n, M)
+    return L.bitnet_decode_chain_build(arr, n, M, p(table) if table else None,
+                                       need if nbytes is None else nbytes,
+                                       ctypes.byref(chain)), need
+
+
 def test_decode_chain_arguments_are_checked_on_the_host():
     L = bn.lib()
-    TABLE = 0x100000  # 256-byte aligned, never dereferenced
-    need = L.bitnet_decode_chain_bytes(2)
-    assert L.bitnet_decode_chain_bytes(3) - need == need - L.bitnet_decode_chain_bytes(1) > 0
-
-    def phase(x=FAKE, K=2560, count=1, N=64, y=FAKE):
-        tg = (_lib.LinearTarget * max(count, 1))(
-            *[_lib.LinearTarget(FAKE, FAKE, N, y, None) for _ in range(max(count, 1))])
-        return _lib.DecodePhase(x, K, ctypes.cast(tg, ctypes.c_void_p), count), tg
-
-    def build(phases, M=1, table=TABLE, nbytes=None):
-        arr = (_lib.DecodePhase * len(phases))(*[ph for ph, _ in phases])
-        chain = _lib.DecodeChain()
-        n = len(phases)
-        return L.bitnet_decode_chain_build(arr, n, M, p(table),
-                                           L.bitnet_decode_chain_bytes(n) if nbytes is None
-                                           else nbytes, ctypes.byref(chain))
-
-    ok = [phase(), phase(K=6912, count=2)]
-    assert L.bitnet_decode_chain_build(None, 1, 1, p(TABLE), need, None) == 1    # NULL
-    assert build(ok, M=5) == 2                                                   # M > 4
-    assert build(ok, M=0) == 2
-    assert build(ok, table=TABLE + 128) == 3                                     # table alignment
-    assert build(ok, nbytes=need - 1) == 4                                       # table too small
-    assert build([phase(count=9)]) == 2                                          # > 8 targets
-    assert build([phase(count=0)]) == 2
-    assert build([phase(K=100)]) == 2                                            # K % 64 != 0
-    assert build([phase(K=65536 * 2)]) == 2                                      # K too large
-    assert build([phase(N=0)]) == 2                                              # empty matrix
-    assert build([phase(x=MIS)]) == 3                                            # x alignment
-    assert build([phase(y=MIS)]) == 3                                            # y alignment
-    assert build([phase(x=0)]) == 1
+    mem = FakeMem()
+    ok = [_chain_phase(mem), _chain_phase(mem, K=6912, Ns=(64, 128))]
+    # a valid description passes the host checks and then stops at the missing
+    # table (no device is touched)
+    st, need = _chain_status(L, ok, table=0)
+    assert need > 0 and st == 1
+    assert L.bitnet_decode_chain_build(None, 1, 1, p(0x100000), need, None) == 1
+    assert _chain_status(L, ok, M=5)[0] == 2                      # M > 4
+    assert _chain_status(L, ok, M=0)[0] == 2
+    assert _chain_status(L, ok, table=0x100080)[0] == 3          # table alignment
+    assert _chain_status(L, ok, nbytes=need - 1)[0] == 4         # table too small
+    assert _chain_status(L, [_chain_phase(mem, Ns=(64,) * 9)])[0] == 2   # > 8 targets
+    assert _chain_status(L, [_chain_phase(mem, K=100)])[0] == 2          # K % 64 != 0
+    assert _chain_status(L, [_chain_phase(mem, K=65536 * 2)])[0] == 2    # K too large
+    assert _chain_status(L, [_chain_phase(mem, Ns=(0,))])[0] == 2        # empty matrix
+    assert _chain_status(L, [_chain_phase(mem, x=MIS)])[0] == 3          # x alignment
+    assert _chain_status(L, [_chain_phase(mem, ys=[MIS])])[0] == 3       # y alignment
+    both = _chain_phase(mem, x_f32=mem(4 * 2560))                        # x and x_f32 both
+    both[0].x = mem(2 * 2560)
+    assert _chain_status(L, [both])[0] == 2
+    none = _chain_phase(mem)
+    none[0].x = None
+    assert _chain_status(L, [none])[0] == 1                              # no input
+    assert _chain_status(L, [_chain_phase(mem, gated=True, Ns=(64, 64))])[0] == 1  # gated: no h
+    h = mem(4 * 64)
+    assert _chain_status(L, [_chain_phase(mem, gated=True, Ns=(64, 128), h=h)])[0] == 2
+    assert _chain_status(L, [_chain_phase(mem, gated=True, Ns=(64,), h=h)])[0] == 2
+    assert _chain_status(L, [_chain_phase(mem, x_f32=mem(4 * 2560), norm=True)])[0] == 2
     assert L.bitnet_decode_chain_run(None, None) == 1
+
+
+def test_decode_chain_links_and_overlaps_are_checked_on_the_host():
+    """A phase input that is exactly an earlier output is a link; any other
+    overlap between an array the chain writes and any array it touches is
+    BITNET_ERR_ALIAS."""
+    L = bn.lib()
+    mem = FakeMem()
+    M, H = 1, 2560
+    yb = mem(2 * M * H)
+    p0 = _chain_phase(mem, Ns=(H,), ybs=[yb], bf16_out=True)
+    p1 = _chain_phase(mem, x=yb, Ns=(H,), norm=True)                 # bf16 link, with norm
+    st, need = _chain_status(L, [p0, p1], table=0)                   # valid: stops at the table
+    assert need > 0 and st == 1
+    # the link buffer lives in the table: a linked chain needs more table
+    p1b = _chain_phase(mem, Ns=(H,))
+    assert _chain_status(L, [p0, p1b], table=0)[1] < need
+    # a gated phase's h read as a binary32 link
+    h = mem(4 * M * 6912)
+    pg = _chain_phase(mem, Ns=(6912, 6912), gated=True, h=h)
+    pd = _chain_phase(mem, K=6912, x_f32=h, Ns=(H,))
+    assert _chain_status(L, [pg, pd], table=0)[0] == 1
+    # overlaps that are not links
+    assert _chain_status(L, [p1, p0])[0] == 7                        # reads a LATER output
+    part = _chain_phase(mem, x=yb + 16, K=2496, Ns=(H,))             # inside an output, not equal
+    assert _chain_status(L, [p0, part])[0] == 7
+    y0 = mem(4 * M * H)
+    q0 = _chain_phase(mem, Ns=(H,), ys=[y0])
+    q1 = _chain_phase(mem, Ns=(H,), ys=[y0 + 64])                    # two outputs overlap
+    assert _chain_status(L, [q0, q1])[0] == 7
+    q2 = _chain_phase(mem, x=y0, Ns=(H,))                            # bf16 x over a binary32 y
+    assert _chain_status(L, [q0, q2])[0] == 7
+    r0 = _chain_phase(mem, Ns=(H,))
+    r0[1][0].y = r0[1][0].Wq                                         # output over the weights
+    assert _chain_status(L, [r0])[0] == 7
+    self_link = _chain_phase(mem, Ns=(H,), ybs=[yb], bf16_out=True)
+    self_link[0].x = yb                                              # reads its own output
+    assert _chain_status(L, [self_link])[0] == 7
 
 
 def test_no_device_reports_unsupported_or_cuda_error():

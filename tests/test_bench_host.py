@@ -1,6 +1,7 @@
 """bench.py's host-side rules, on the CPU: the algorithmic byte counts of the
 decode step (against the shapes of the 2B-class layer worked out by hand),
 and the reader of the ncu traffic recorded under profiles/."""
+import hashlib
 import importlib.util
 import os
 import shutil
@@ -23,26 +24,31 @@ def test_decode_step_byte_counts():
     packed = (2 * 2560 * 2560 + 2 * 640 * 2560 + 3 * 6912 * 2560) // 4
     assert b.weight_bytes() == packed == 17_367_040
     assert b.weight_bytes() * 30 == 521_011_200
-    # each phase reads its bf16 input once (x, attn, x2: 2560; h: 6912), each
-    # matrix its fp32 scale, and every output is written as fp32
-    inputs = 2 * (3 * 2560 + 6912)
-    outputs = 4 * (2560 + 640 + 640 + 2560 + 6912 + 6912 + 2560)
-    assert b.layer_bytes("chain") == b.layer_bytes("fused") == packed + inputs + 7 * 4 + outputs
-    # the unfused path also writes and re-reads the int8 codes and scales
-    assert b.layer_bytes("split") > b.layer_bytes("fused")
+    # 7 fp32 weight scales, 2 fp32 norm gains of 2560; inputs: QKV, O and
+    # up/gate read bf16 [2560], down reads fp32 h [6912]; outputs: Q, O and
+    # down bf16 [2560], K and V fp32 [640], h fp32 [6912]
+    scales, gains = 7 * 4, 2 * 4 * 2560
+    inputs = 3 * 2 * 2560 + 4 * 6912
+    outputs = 3 * 2 * 2560 + 2 * 4 * 640 + 4 * 6912
+    assert b.layer_bytes() == packed + scales + gains + inputs + outputs
 
 
 def test_profiled_traffic_follows_the_kernel_source(tmp_path):
     b = load_bench()
-    kernel = "bitlinear_bitnet_linear_03_b300/csrc/gemv_decode.cu"
-    profile = "profiles/gemv_decode_2b_30layers.md"
-    t = b.profiled_traffic(kernel, profile)
-    assert t is not None and t > 0
-    # traffic close to the algorithmic bytes of a launch (30 layers)
-    assert 1.0 <= t / (b.layer_bytes("chain") * 30) < 1.05
+    kernel = os.path.join(ROOT, "bitlinear_bitnet_linear_03_b300/csrc/decode_chain.cu")
+    digest = hashlib.sha256(open(kernel, "rb").read()).hexdigest()[:16]
+    prof = tmp_path / "p.md"
+    prof.write_text(f"x\n\nsource_sha256_16: `{digest}`\ndram_bytes_per_launch: `123456`\n")
+    assert b.profiled_traffic(kernel, str(prof)) == 123456.0
     # any change to the kernel source voids the recorded figure
     copy = tmp_path / "k.cu"
-    shutil.copy(os.path.join(ROOT, kernel), copy)
+    shutil.copy(kernel, copy)
     with open(copy, "a") as f:
         f.write("\n// changed\n")
-    assert b.profiled_traffic(str(copy), profile) is None
+    assert b.profiled_traffic(str(copy), str(prof)) is None
+    # the committed capture of the decode step, when it matches the source:
+    # traffic close to the algorithmic bytes of a launch (30 layers)
+    t = b.profiled_traffic("bitlinear_bitnet_linear_03_b300/csrc/decode_chain.cu",
+                           "profiles/decode_chain_2b_30layers.md")
+    if t is not None:
+        assert 0.99 <= t / (b.layer_bytes() * 30) < 1.1

@@ -100,3 +100,48 @@ def test_ffn_partial_debug_outputs(M, seed):
     for k in ("u", "v", "sh", "hq", "acc_down"):
         assert_bits_equal(got[k], want[k], k)
     assert_bits_equal(y, want["y"], "y end to end")
+
+
+def test_ffn_norm_special_rows():
+    """Rows that exercise the exact sum of squares: the row whose exact sum
+    rounds differently from a binary64 or running binary32 sum, an all-zero
+    row, subnormal and tiny values, values whose squares overflow binary32
+    (ss = inf, r = 0), and an ordinary row."""
+    M, H, F = 6, 256, 320
+    rows = np.zeros((M, H), np.float32)
+    rows[0, 3], rows[0, 20], rows[0, 41], rows[0, 63] = 1490944.0, 256.0, 256.0, 2.0 ** -20
+    rows[2, ::3] = 2.0 ** -130                      # subnormal bf16 values: squares underflow
+    rows[3, ::5] = 3.0e-20
+    rows[3, 1] = 7.0
+    rows[4, 7] = 3.0e20                             # square above the binary32 range
+    rows[5] = synth.bf16_bits_to_f32(synth.tokens_bf16(1, H, seed=5))[0]
+    x = synth.f32_to_bf16_bits(rows)
+    g = synth.gain_random(H, 3)
+    ws = [oracle.quantize_weights(synth.weights_f32(n, k, seed=80 + i))
+          for i, (n, k) in enumerate([(F, H), (F, H), (H, F)])]
+    got = run_gpu(x, g, 1e-5, ws, M, H, F)
+    n, _ = oracle.rmsnorm_bf16(x, g, np.float32(1e-5))
+    q, s = oracle.quantize_act_f32(n)
+    assert_bits_equal(got["xq"], q, "xq")
+    assert_bits_equal(got["sx"], s, "sx")
+    assert (got["xq"][1] == 0).all() and (got["xq"][4] == 0).all()
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_ffn_seq4096_sampled_tokens(seed):
+    """The prefill-sized FFN (seq 4096, hidden 2560, FFN 6912): the GPU runs
+    every token; the oracle recomputes 24 sampled tokens (the block is
+    independent per token), first and last included, and every intermediate
+    at those tokens must match bit for bit."""
+    M = 4096
+    x, g, ws = ffn_inputs(M, seed, random_gain=(seed % 2 == 1))
+    got = run_gpu(x, g, 1e-5, ws, M, H, F)
+    rows = np.random.default_rng(seed).choice(M, 24, replace=False)
+    rows[:2] = [0, M - 1]
+    (Wu, su, _), (Wg, sg, _), (Wd, sd, _) = ws
+    want = oracle.ffn(x[rows], g, 1e-5, Wu, su, Wg, sg, Wd, sd, threads=oracle.default_threads())
+    for k in ("sx", "xq", "u", "v", "h", "sh", "hq", "acc_down", "y"):
+        assert_bits_equal(got[k][rows], want[k], f"seed {seed} {k}")
+    # every token: the properties that hold at any size
+    assert np.isfinite(got["y"]).all()
+    assert (np.abs(got["xq"]).max(axis=1) == 127).all()

@@ -367,3 +367,102 @@ def test_decode_chain_multi_token(M):
     for (_, tg), want in zip(phases, refs):
         for t, y_o in zip(tg, want):
             assert_bits_equal(host(t[2]), y_o, "chain y")
+
+
+# ---------------------------------------------------------------- bf16 outputs
+def _bf16(t):
+    return host(t.view(torch.int16)).view(np.uint16)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 2560, 2560), (3, 100, 192), (8, 2560, 6912),
+                                   (64, 6912, 2560), (300, 264, 640), (4096, 2560, 2560)])
+def test_linear_bf16_output_every_path(M, N, K):
+    """The bf16 form of the rescaled output (nearest, ties to even) on every
+    path of bitnet_linear: decode (M <= 4), CUDA cores (5..15), fused tensor
+    cores (16..256, split K included), pre-expanded tensor cores (> 256)."""
+    Wq, ws, qx, sx = linear_inputs(M, N, K, seed=M + N, frac=0.01)
+    y_o, acc_o = oracle.linear(Wq, ws, qx, sx, K, threads=oracle.default_threads())
+    yb = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    args = (dev(Wq), dev(np.array([ws], np.float32)), dev(qx), dev(sx))
+    bn.bitnet_linear(*args, K=K, y=None, y_bf16=yb)            # bf16 only
+    assert_bits_equal(_bf16(yb), oracle.f32_to_bf16(y_o), "y_bf16 alone")
+    yb.view(torch.int16).fill_(0x7fc1)
+    bn.bitnet_linear(*args, K=K, y=y, y_bf16=yb)               # both forms
+    assert_bits_equal(host(y), y_o, "y")
+    assert_bits_equal(_bf16(yb), oracle.f32_to_bf16(y_o), "y_bf16 with y")
+
+
+# ---------------------------------------------------------------- dependent launches
+@pytest.mark.parametrize("weights_static", [False, True])
+def test_back_to_back_decode_launches_carry_the_data(weights_static):
+    """Programmatic dependent launch: launch 2 reads, as its bf16 input, the
+    bytes launch 1 writes; launch 3 reads launch 2's output.  With static
+    weights the weight stream starts before the previous launch ends; the
+    input must still be read after it.  Repeated with the outputs poisoned."""
+    H = 2560
+    x = synth.tokens_bf16(1, H, seed=61, outlier_frac=0.01)
+    W = [oracle.quantize_weights(synth.weights_f32(H, H, seed=610 + i))[:2] for i in range(3)]
+    Wd = [(dev(Wq), dev(np.array([ws], np.float32))) for Wq, ws in W]
+    ys = [torch.empty((1, H), dtype=torch.bfloat16, device="cuda") for _ in range(3)]
+    xd = dev_bf16(x)
+    want, cur = [], x
+    for Wq, ws in W:
+        qx, sx = oracle.quantize_act_bf16(cur)
+        cur = oracle.f32_to_bf16(oracle.linear(Wq, ws, qx, sx, H)[0])
+        want.append(cur)
+    for rep in range(5):
+        for t in ys:
+            t.view(torch.int16).fill_(0x7fc1)
+        for i in range(3):
+            bn.bitnet_linear_bf16(xd if i == 0 else ys[i - 1],
+                                  [(*Wd[i], None, None, ys[i])], weights_static=weights_static)
+        for i in range(3):
+            assert_bits_equal(_bf16(ys[i]), want[i], f"rep {rep} launch {i}")
+
+
+# ---------------------------------------------------------------- bounded waits
+def test_waits_that_run_out_report_and_leave_the_context_usable():
+    """With a wait bound far below the time the work needs, the kernels' waits
+    run out: each kernel records its error bit, waits for its own copies in
+    flight and returns (nothing hangs or faults).  bitnet_device_error reports
+    the bits; with the default bound restored the same calls are exact."""
+    H = 2560
+    x = synth.tokens_bf16(1, H, seed=65)
+    packs = [oracle.quantize_weights(synth.weights_f32(H, H, seed=650 + i))[:2] for i in range(2)]
+    Wd = [(dev(Wq), dev(np.array([ws], np.float32))) for Wq, ws in packs]
+    y0 = torch.empty((1, H), dtype=torch.bfloat16, device="cuda")
+    y1 = torch.empty((1, H), dtype=torch.float32, device="cuda")
+    phases = [{"x": dev_bf16(x), "targets": [(*Wd[0], None, None, y0)]},
+              {"x": y0, "targets": [(*Wd[1], y1)]}]
+    chain = bn.bitnet_decode_chain_build(phases)
+    M, K = 64, 8192                                   # fused tensor-core path, split K
+    Wt, wst, qxt, sxt = linear_inputs(M, 300, K, seed=66)
+    targs = (dev(Wt), dev(np.array([wst], np.float32)), dev(qxt), dev(sxt))
+    assert bn.bitnet_device_error() == 0
+    try:
+        bn.bitnet_set_wait_limit(200)                 # ~0.1 us
+        bn.bitnet_decode_chain_run(chain)
+        torch.cuda.synchronize()
+        code = bn.bitnet_device_error()
+        assert code & 0xff0000, hex(code)             # a chain wait ran out
+        bn.bitnet_linear_bf16(dev_bf16(x), [(*Wd[0], y1)])
+        torch.cuda.synchronize()
+        assert bn.bitnet_device_error() & 0xff00      # a decode wait ran out
+        bn.bitnet_linear(*targs, K=K)
+        torch.cuda.synchronize()
+        assert bn.bitnet_device_error() & 0xff        # a tensor-core wait ran out
+    finally:
+        bn.bitnet_set_wait_limit(0)
+    assert bn.bitnet_device_error() == 0
+    chain = bn.bitnet_decode_chain_build(phases)      # rebuilt after the error
+    bn.bitnet_decode_chain_run(chain)
+    torch.cuda.synchronize()
+    assert bn.bitnet_device_error() == 0
+    qx, sx = oracle.quantize_act_bf16(x)
+    y0_o = oracle.f32_to_bf16(oracle.linear(*packs[0], qx, sx, H)[0])
+    assert_bits_equal(_bf16(y0), y0_o, "y0 after the time-outs")
+    qx, sx = oracle.quantize_act_bf16(y0_o)
+    assert_bits_equal(host(y1), oracle.linear(*packs[1], qx, sx, H)[0], "y1 after the time-outs")
+    y_t = host(bn.bitnet_linear(*targs, K=K))
+    assert_bits_equal(y_t, oracle.linear(Wt, wst, qxt, sxt, K)[0], "tensor-core y after")
