@@ -55,6 +55,7 @@ constexpr int kMaxStages = 10;
 constexpr int kRingBudget = 192 * 1024;
 constexpr int kStageTarget = 20 * 1024;
 constexpr int kHold = 4;  // groups of 8 inputs a consumer keeps in registers (K <= 8192)
+constexpr int kPipe = 2;  // groups whose loads are in flight together
 constexpr int kMaxPhases = 16384;
 constexpr int kErrLinkWait = 1, kErrFullWait = 2, kErrEmptyWait = 4, kErrDrain = 8;
 constexpr int kTargets = kDecodeMaxTargets;
@@ -213,6 +214,72 @@ __device__ __forceinline__ void load_gain8(const float* g, int grp, float (&gv)[
   gv[6] = __uint_as_float(b.z); gv[7] = __uint_as_float(b.w);
 }
 
+// The raw words of group g (8 consecutive inputs) of token m, loaded without
+// waiting for them: 4 (bf16), 8 (binary32 or bf16 link) or 16 (binary32
+// link) words.  decode_group turns them into binary32 values and tells
+// whether every tag of a linked group is the current one.  Issuing the loads
+// of all of a thread's groups before looking at any keeps one memory round
+// trip on the critical path instead of one per group.
+struct Raw {
+  uint32_t w[16];
+};
+__device__ __forceinline__ void issue_group(const CPhase& ph, int m, int g, Raw& r) {
+  const int64_t base = (int64_t)m * ph.K + 8 * (int64_t)g;
+  if (ph.in_kind == kInBf16) {
+    const uint4 q = ld_nc_v4(static_cast<const uint16_t*>(ph.x) + base);
+    r.w[0] = q.x; r.w[1] = q.y; r.w[2] = q.z; r.w[3] = q.w;
+  } else if (ph.in_kind == kInF32) {
+    const float* f = static_cast<const float*>(ph.x) + base;
+    const uint4 a = ld_nc_v4(f), b = ld_nc_v4(f + 4);
+    r.w[0] = a.x; r.w[1] = a.y; r.w[2] = a.z; r.w[3] = a.w;
+    r.w[4] = b.x; r.w[5] = b.y; r.w[6] = b.z; r.w[7] = b.w;
+  } else if (ph.in_kind == kInLinkBf16) {
+    const uint32_t* q = static_cast<const uint32_t*>(ph.x) + base;
+    const uint4 a = ld_relaxed_v4(q), b = ld_relaxed_v4(q + 4);
+    r.w[0] = a.x; r.w[1] = a.y; r.w[2] = a.z; r.w[3] = a.w;
+    r.w[4] = b.x; r.w[5] = b.y; r.w[6] = b.z; r.w[7] = b.w;
+  } else {
+    const unsigned long long* q = static_cast<const unsigned long long*>(ph.x) + base;
+#pragma unroll
+    for (int i = 0; i < 8; i += 2) {
+      unsigned long long a, b;
+      ld_relaxed_v2u64(q + i, a, b);
+      r.w[2 * i] = (uint32_t)a;
+      r.w[2 * i + 1] = (uint32_t)(a >> 32);
+      r.w[2 * i + 2] = (uint32_t)b;
+      r.w[2 * i + 3] = (uint32_t)(b >> 32);
+    }
+  }
+}
+__device__ __forceinline__ bool decode_group(const CPhase& ph, const Raw& r, uint32_t tag,
+                                             float (&v)[8]) {
+  bool ok = true;
+  if (ph.in_kind == kInBf16) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      v[2 * i] = bf16_bits_to_float(r.w[i] & 0xffffu);
+      v[2 * i + 1] = bf16_bits_to_float(r.w[i] >> 16);
+    }
+  } else if (ph.in_kind == kInF32) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r.w[i]);
+  } else if (ph.in_kind == kInLinkBf16) {
+    const uint32_t t16 = tag & 0xffffu;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      ok &= (r.w[i] >> 16) == t16;
+      v[i] = bf16_bits_to_float(r.w[i] & 0xffffu);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      ok &= r.w[2 * i + 1] == tag;
+      v[i] = __uint_as_float(r.w[2 * i]);
+    }
+  }
+  return ok;
+}
+
 // One finished output value of a (non-gated) target: every requested form.
 __device__ __forceinline__ void store_out(const CTarget& T, int64_t o, float y, int acc,
                                           uint32_t tag) {
@@ -305,22 +372,51 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_chain(const __grid_const
   const int tid = threadIdx.x;  // 0 .. kConsumers-1
   int c_slot = 0;
   uint32_t c_parity = 0;
+  constexpr int kDescWords = (int)(sizeof(CPhase) / 8);
+  constexpr int kDescPerLane = (kDescWords + 31) / 32;
   for (int p = 0; p < a.nphases; ++p) {
-    // Every consumer has finished phase p-1, so s_ph[p & 1] (copied during
+    // Every consumer has finished phase p-1, so s_ph[p & 1] (written during
     // phase p-1) is complete and s_ph[(p+1) & 1] is free.
     if (p > 0 && consumer_sync_or(*(volatile int*)&s_abort)) break;
-    if (warp == 0 && p + 1 < a.nphases) copy_phase(a.phases[p + 1], &s_ph[(p + 1) & 1], lane);
     const CPhase& ph = s_ph[p & 1];
+    // Loads whose latency overlaps the wait for the input: the next phase's
+    // descriptor (warp 0; stored once the input is quantised), the matrices'
+    // scales and, for a normalised input, the gains of this thread's groups.
+    unsigned long long desc[kDescPerLane];
+    if (warp == 0 && p + 1 < a.nphases) {
+      const unsigned long long* src = reinterpret_cast<const unsigned long long*>(&a.phases[p + 1]);
+#pragma unroll
+      for (int i = 0; i < kDescPerLane; ++i)
+        if (lane + 32 * i < kDescWords) desc[i] = src[lane + 32 * i];
+    }
+    auto store_desc = [&]() {
+      if (warp == 0 && p + 1 < a.nphases) {
+        unsigned long long* dst = reinterpret_cast<unsigned long long*>(&s_ph[(p + 1) & 1]);
+#pragma unroll
+        for (int i = 0; i < kDescPerLane; ++i)
+          if (lane + 32 * i < kDescWords) dst[lane + 32 * i] = desc[i];
+      }
+    };
     int r_begin, r_end;
     cta_rows(ph.rows_total, r_begin, r_end);
-    if (r_begin >= r_end) continue;  // no rows of this phase here: its input is not needed
+    if (r_begin >= r_end) {  // no rows of this phase here: its input is not needed
+      store_desc();
+      continue;
+    }
     const bool reporter = r_begin == 0;  // the one CTA with rows that starts at row 0
+    const float ws_lane = lane < ph.count ? *ph.t[lane].w_scale : 0.0f;
 
     // ---- prologue: the phase input, (normalised,) quantised into xs
     const int K = ph.K;
     const int ngroups = K >> 3;
     const bool norm = ph.g != nullptr;
     const uint32_t in_tag = tag0 + (uint32_t)ph.in_phase;
+    float gh[kHold][8];
+    if (norm) {
+#pragma unroll
+      for (int i = 0; i < kHold; ++i)
+        if (tid + i * kConsumers < ngroups) load_gain8(ph.g, tid + i * kConsumers, gh[i]);
+    }
     float xscale[MT];
     bool stop = false;
 #pragma unroll
@@ -332,7 +428,51 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_chain(const __grid_const
       sumsq::Acc acc;
       sumsq::zero(acc);
       bool bad = false;
-      for (int i = 0;; ++i) {
+      // The held groups (tid + i * kConsumers, i < kHold), kPipe at a time:
+      // their loads first, then the tags; a linked group not yet produced is
+      // polled again.  (Nine warps per CTA leave 168 registers a thread,
+      // which bounds how many raw groups can be in flight.)
+#pragma unroll
+      for (int c = 0; c < kHold; c += kPipe) {
+        if (bad || tid + c * kConsumers >= ngroups) break;
+        Raw raw[kPipe];
+        uint32_t pend = 0;
+#pragma unroll
+        for (int i = 0; i < kPipe; ++i)
+          if (tid + (c + i) * kConsumers < ngroups)
+            issue_group(ph, m, tid + (c + i) * kConsumers, raw[i]);
+#pragma unroll
+        for (int i = 0; i < kPipe; ++i)
+          if (tid + (c + i) * kConsumers < ngroups && !decode_group(ph, raw[i], in_tag, hv[c + i]))
+            pend |= 1u << i;
+        if (pend) {
+          const long long t0 = clock64();
+          while (pend) {
+            __nanosleep(32);
+#pragma unroll
+            for (int i = 0; i < kPipe; ++i)
+              if ((pend >> i) & 1u) issue_group(ph, m, tid + (c + i) * kConsumers, raw[i]);
+#pragma unroll
+            for (int i = 0; i < kPipe; ++i)
+              if (((pend >> i) & 1u) && decode_group(ph, raw[i], in_tag, hv[c + i]))
+                pend &= ~(1u << i);
+            if (pend && (clock64() - t0 > a.wait || *(volatile int*)&s_abort)) {
+              bad = true;
+              break;
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < kHold; ++i)
+        if (tid + i * kConsumers < ngroups)
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            if (norm) sumsq::add_term(acc, __fmul_rn(hv[i][e], hv[i][e]));
+            else mx = fmaxf(mx, fabsf(hv[i][e]));
+          }
+      // Groups beyond the held ones (K > 8 * kHold * kConsumers): one by one.
+      for (int i = kHold; !bad; ++i) {
         const int g = tid + i * kConsumers;
         if (g >= ngroups) break;
         float v[8];
@@ -345,11 +485,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_chain(const __grid_const
           if (norm) sumsq::add_term(acc, __fmul_rn(v[e], v[e]));
           else mx = fmaxf(mx, fabsf(v[e]));
         }
-#pragma unroll
-        for (int h = 0; h < kHold; ++h)
-          if (h == i)
-#pragma unroll
-            for (int e = 0; e < 8; ++e) hv[h][e] = v[e];
       }
       if (bad) {
         atomicOr(&g_chain_error, kErrLinkWait);
@@ -378,30 +513,22 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_chain(const __grid_const
         sumsq::warp_reduce(tot, kConsumerWarps / 2);
         r = __shfl_sync(0xffffffffu, sumsq::rms_scale(sumsq::round_to_f32(tot), K, ph.eps), 0);
         // n = (x * r) * g, then its largest magnitude
-        for (int i = 0;; ++i) {
+#pragma unroll
+        for (int i = 0; i < kHold; ++i)
+          if (tid + i * kConsumers < ngroups)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              hv[i][e] = __fmul_rn(__fmul_rn(hv[i][e], r), gh[i][e]);
+              mx = fmaxf(mx, fabsf(hv[i][e]));
+            }
+        for (int i = kHold;; ++i) {
           const int g = tid + i * kConsumers;
           if (g >= ngroups) break;
           float v[8], gv[8];
-          if (i < kHold) {
-#pragma unroll
-            for (int h = 0; h < kHold; ++h)
-              if (h == i)
-#pragma unroll
-                for (int e = 0; e < 8; ++e) v[e] = hv[h][e];
-          } else {
-            load_group(ph, m, g, in_tag, a.wait, &s_abort, v);
-          }
+          load_group(ph, m, g, in_tag, a.wait, &s_abort, v);
           load_gain8(ph.g, g, gv);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            v[e] = __fmul_rn(__fmul_rn(v[e], r), gv[e]);
-            mx = fmaxf(mx, fabsf(v[e]));
-          }
-#pragma unroll
-          for (int h = 0; h < kHold; ++h)
-            if (h == i)
-#pragma unroll
-              for (int e = 0; e < 8; ++e) hv[h][e] = v[e];
+          for (int e = 0; e < 8; ++e) mx = fmaxf(mx, fabsf(__fmul_rn(__fmul_rn(v[e], r), gv[e])));
         }
       }
       mx = warp_max_f32(mx);
@@ -446,13 +573,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_chain(const __grid_const
       if (reporter && tid == 0 && ph.xs_out) ph.xs_out[m] = sc.scale;
     }
     if (stop || consumer_sync_or(*(volatile int*)&s_abort)) break;
+    store_desc();
 
     // ---- this warp's K part and its activations in registers
     const int wk = ph.wk;
     const int kw = warp % wk, wr = warp / wk, nwr = kConsumerWarps / wk;
     const int nch = K >> 6;
     const int k_lo = kw * ph.kpart, k_hi = min(nch, k_lo + ph.kpart);
-    const float ws_lane = lane < ph.count ? *ph.t[lane].w_scale : 0.0f;
     int valid_j = 0;
 #pragma unroll
     for (int j = 0; j < J; ++j)
