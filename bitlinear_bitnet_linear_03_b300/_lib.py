@@ -70,7 +70,7 @@ class DecodePhase(ctypes.Structure):
 
 class DecodeChain(ctypes.Structure):
     """bitnet_decode_chain: filled by bitnet_decode_chain_build."""
-    _fields_ = [("table", _P), ("M", _I64), ("nphases", _INT), ("cfg", _INT * 8)]
+    _fields_ = [("table", _P), ("M", _I64), ("nphases", _INT), ("cfg", _INT * 12)]
 
 
 class FfnDebug(ctypes.Structure):

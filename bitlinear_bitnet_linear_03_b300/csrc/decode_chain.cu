@@ -7,11 +7,16 @@
 // per-token int8 quantised input ("Microsoft BitNet b1.58 ... 1-bit AI
 // model" (communeify), "Meet BitNet b1.58 2B4T": W1.58A8), optionally
 // preceded by the subln RMSNorm and optionally gated, h = relu(gate)^2 * up
-// (same page: subln, ReLU^2).  The weights do not depend on any phase, so a
-// producer lane streams the weight rows of every phase, in order, into a deep
-// shared-memory ring while the consumers are still on earlier phases ("BitNet
-// - 1-bit LLM inference framework" (news.hada.io), HN comment: memory
-// bandwidth is the bottleneck).
+// (same page: subln, ReLU^2).  The weights do not depend on any phase, so the
+// weight rows of every phase stream, in order, into a deep shared-memory ring
+// while the consumers are still on earlier phases ("BitNet - 1-bit LLM
+// inference framework" (news.hada.io), HN comment: memory bandwidth is the
+// bottleneck).  There is no producer warp: the CTA's whole sequence of bulk
+// copies is listed in the chain's table when the chain is built, thread 0
+// issues the first ring-full, and the warp that releases a slot last (the
+// eighth to finish its stage) issues the copy S stages ahead into it.  With
+// eight warps (two per SM sub-partition) a thread may hold up to 255
+// registers, which the in-register activations and input staging need.
 //
 // Data flow.  A phase input that is an output of an earlier phase (a link)
 // is read through link words in the chain's table: every value is stored
@@ -27,12 +32,21 @@
 //
 // Work split: phase rows (gated: row pairs up n / gate n) are divided evenly
 // over the CTAs; a stage is a run of whole rows of one matrix (gated: the
-// same rows of up, then of gate, two copies into one slot).  Consumer lane l
-// of a warp owns the 64-weight chunks l, l + 32, ... of its K part: their
-// int8 activations sit in registers for the whole phase, and a row costs one
-// 16-byte shared load, 16 ANDs and 16 dp4a per chunk (decode_common.cuh).
-// When several warps split K, their parts meet in shared-memory atomics
-// that also count the parts; the last part writes the row.
+// same rows of up, then of gate, two copies into one slot), up to ~62 KB, so
+// a CTA's share of a phase is usually one stage: every stage costs a release
+// and a refill, and on B300 those latencies, not the dot products, bound a
+// phase.  Consumer lane l of a warp owns the 64-weight chunks l, l + 32, ...
+// of its K part: their int8 activations sit in registers for the whole
+// phase, and a row costs one 16-byte shared load, 16 ANDs and 16 dp4a per
+// chunk (decode_common.cuh).  When several warps split K, their parts meet in
+// shared-memory atomics that also count the parts; the last part writes the
+// row.
+//
+// The subln sum of squares is exact (exact_sumsq.cuh): in 128 bits anchored
+// 88 bits below the largest square of the row, or, for a row whose squares
+// span more than that, in five limbs out of line.  Rarely run code stays out
+// of line and the row loops are not unrolled: the kernel is large, and
+// instruction fetch stalls showed in its profile.
 //
 // Every wait is bounded (a second by default): on time-out the kernel records
 // an error bit, every warp stops at the next uniform point, the producer
@@ -52,10 +66,18 @@ namespace {
 using namespace dec;
 
 constexpr int kMaxStages = 10;
+constexpr int kChainWarps = 8;  // all consumers; no producer warp
+constexpr int kChainThreads = 32 * kChainWarps;
+constexpr int kMaxChainCtas = 1024;
+constexpr int kListMax = 512;  // copies of a CTA's sequence held in shared memory
 constexpr int kRingBudget = 192 * 1024;
-constexpr int kStageTarget = 20 * 1024;
-constexpr int kHold = 4;  // groups of 8 inputs a consumer keeps in registers (K <= 8192)
-constexpr int kPipe = 2;  // groups whose loads are in flight together
+constexpr int kStageTarget = 62 * 1024;  // about one stage per phase per CTA
+// Groups of 8 inputs a thread keeps in registers (all of K <= 8192), and how
+// many of them have their loads in flight together.
+constexpr int kHold = 8192 / (8 * 32 * kChainWarps);
+constexpr int kPipe = kHold;
+// Stage rows whose K parts meet in shared memory (when several warps split K).
+constexpr int kAccRows = kMaxRowsPerWarp * kChainWarps / 2;
 constexpr int kMaxPhases = 16384;
 constexpr int kErrLinkWait = 1, kErrFullWait = 2, kErrEmptyWait = 4, kErrDrain = 8;
 constexpr int kTargets = kDecodeMaxTargets;
@@ -88,20 +110,35 @@ struct CPhase {
   int gated;
   int count;
   int rows_total;  // rows (gated: row pairs) of the phase
+  int rows_q, rows_rem;  // even split over the CTAs: q rows each, one more for the first rem
   int K, wk, kpart, rows_per_stage;
+  int pad;
+};
+
+// One bulk copy of the CTA's copy sequence: a stage of whole weight rows
+// (gated: the same rows of up, then of gate, each `bytes` long).
+struct StageCopy {
+  const uint8_t* src0;
+  const uint8_t* src1;
+  uint32_t bytes;
+  uint32_t pad;
 };
 
 struct Args {
   const CPhase* phases;
   unsigned long long* counter;
+  const StageCopy* copies;    // every CTA's copy sequence, one after another
+  const uint32_t* cta_first;  // [ctas + 1]: where each CTA's sequence starts
   int nphases, M, stages, slot_bytes, xs_stride;
   long long wait;
 };
 
-// This CTA's rows [r0, r1) of a phase: an even split over the grid.
-__device__ __forceinline__ void cta_rows(int rows_total, int& r0, int& r1) {
-  r0 = (int)((long long)blockIdx.x * rows_total / gridDim.x);
-  r1 = (int)((long long)(blockIdx.x + 1) * rows_total / gridDim.x);
+// This CTA's rows [r0, r1) of a phase: q rows each, one more for the first
+// rem CTAs (the host's copy lists follow the same rule).
+__device__ __forceinline__ void cta_rows(const CPhase& ph, int& r0, int& r1) {
+  const int b = (int)blockIdx.x;
+  r0 = b * ph.rows_q + min(b, ph.rows_rem);
+  r1 = r0 + ph.rows_q + (b < ph.rows_rem ? 1 : 0);
 }
 
 // The CTA's stage sequence within one phase: f(target, first row, rows) in
@@ -109,7 +146,7 @@ __device__ __forceinline__ void cta_rows(int rows_total, int& r0, int& r1) {
 template <typename F>
 __device__ __forceinline__ bool for_each_stage(const CPhase& ph, F&& f) {
   int r_begin, r_end;
-  cta_rows(ph.rows_total, r_begin, r_end);
+  cta_rows(ph, r_begin, r_end);
   if (ph.gated) {
     for (int r = r_begin; r < r_end; r += ph.rows_per_stage)
       if (!f(0, r, min(ph.rows_per_stage, r_end - r))) return false;
@@ -129,6 +166,22 @@ __device__ __forceinline__ void copy_phase(const CPhase& src, CPhase* dst, int l
   const unsigned long long* s = reinterpret_cast<const unsigned long long*>(&src);
   unsigned long long* d = reinterpret_cast<unsigned long long*>(dst);
   for (int i = lane; i < (int)(sizeof(CPhase) / 8); i += 32) d[i] = s[i];
+}
+
+// Named barrier 1 over the CTA's warps, optionally ORing a flag (every warp
+// leaves with the same answer).
+__device__ __forceinline__ void chain_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kChainThreads) : "memory");
+}
+__device__ __forceinline__ bool chain_sync_or(int flag) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.s32 p, %1, 0;\n bar.red.or.pred q, 1, %2, p;\n"
+      " selp.u32 %0, 1, 0, q;\n}"
+      : "=r"(r)
+      : "r"(flag), "n"(kChainThreads)
+      : "memory");
+  return r != 0;
 }
 
 // ---- link words
@@ -202,7 +255,6 @@ __device__ __forceinline__ bool load_group(const CPhase& ph, int m, int g, uint3
     if (ok) return true;
     if (tries == 0) t0 = clock64();
     else if (clock64() - t0 > limit || *(volatile const int*)abort_flag) return false;
-    __nanosleep(32);
   }
 }
 
@@ -280,6 +332,16 @@ __device__ __forceinline__ bool decode_group(const CPhase& ph, const Raw& r, uin
   return ok;
 }
 
+// Layout of the quantised input in shared memory: 64-weight chunk c takes 64
+// bytes, its 16-byte quarter s at slot (s + c/2) mod 4, so that the 8 lanes of
+// a quarter-warp reading quarter s of 8 consecutive chunks hit 8 distinct
+// 16-byte bank groups.
+__device__ __forceinline__ int xs_chunk_offset(int c, int s) { return 64 * c + 16 * ((s + (c >> 1)) & 3); }
+// Group g (8 inputs): chunk g/8, quarter (g/2) mod 4, half g mod 2.
+__device__ __forceinline__ int xs_offset(int g) {
+  return xs_chunk_offset(g >> 3, (g >> 1) & 3) + 8 * (g & 1);
+}
+
 // One finished output value of a (non-gated) target: every requested form.
 __device__ __forceinline__ void store_out(const CTarget& T, int64_t o, float y, int acc,
                                           uint32_t tag) {
@@ -293,91 +355,160 @@ __device__ __forceinline__ void store_out(const CTarget& T, int64_t o, float y, 
                                      ((unsigned long long)tag << 32));
 }
 
+// ---- Out of line: inputs wider than the held groups, and the five-limb
+// sum of squares.  They run rarely (K > 8192 at one token, or a row whose
+// squares span more than 2^88), so they stay out of the kernel's hot code.
+
+// Largest |x| (r == 0) or |(x * r) * g| (normalised) over the groups of token
+// m this thread owns beyond the held ones.
+__device__ __noinline__ float wide_absmax(const CPhase& ph, int m, int tid, uint32_t tag,
+                                          long long limit, const int* abort_flag, float r,
+                                          bool* bad) {
+  float mx = 0.0f;
+  const int ngroups = ph.K >> 3;
+  for (int g = tid + kHold * kChainThreads; g < ngroups; g += kChainThreads) {
+    float v[8];
+    if (!load_group(ph, m, g, tag, limit, abort_flag, v)) {
+      *bad = true;
+      break;
+    }
+    if (ph.g) {
+      float gv[8];
+      load_gain8(ph.g, g, gv);
+      for (int e = 0; e < 8; ++e) v[e] = __fmul_rn(__fmul_rn(v[e], r), gv[e]);
+    }
+    for (int e = 0; e < 8; ++e) mx = fmaxf(mx, fabsf(v[e]));
+  }
+  return mx;
+}
+
+// Quantises those groups into xs (and xq_out when given).
+__device__ __noinline__ void wide_quantize(const CPhase& ph, int m, int tid, uint32_t tag,
+                                           long long limit, const int* abort_flag, float r,
+                                           float inv, int8_t* xs_row, int8_t* xq_out) {
+  const int ngroups = ph.K >> 3;
+  for (int g = tid + kHold * kChainThreads; g < ngroups; g += kChainThreads) {
+    float v[8];
+    load_group(ph, m, g, tag, limit, abort_flag, v);
+    if (ph.g) {
+      float gv[8];
+      load_gain8(ph.g, g, gv);
+      for (int e = 0; e < 8; ++e) v[e] = __fmul_rn(__fmul_rn(v[e], r), gv[e]);
+    }
+    int q[8];
+    for (int e = 0; e < 8; ++e) q[e] = round_clip(__fmul_rn(v[e], inv), -128.f, 127.f);
+    const uint2 packed = make_uint2(pack_i8x4(q[0], q[1], q[2], q[3]), pack_i8x4(q[4], q[5], q[6], q[7]));
+    *reinterpret_cast<uint2*>(xs_row + xs_offset(g)) = packed;
+    if (xq_out) *reinterpret_cast<uint2*>(xq_out + (int64_t)m * ph.K + 8 * g) = packed;
+  }
+}
+
+// The exact sum of the squares of token m's inputs in five 64-bit limbs,
+// rounded once (every thread of the CTA calls it; it synchronises them).
+__device__ __noinline__ float exact_row_sumsq(const CPhase& ph, int m, int tid, uint32_t tag,
+                                              long long limit, const int* abort_flag,
+                                              unsigned long long* s_sum, uint32_t* s_flag) {
+  const int warp = tid >> 5, lane = tid & 31;
+  sumsq::Acc acc;
+  sumsq::zero(acc);
+  const int ngroups = ph.K >> 3;
+  for (int g = tid; g < ngroups; g += kChainThreads) {
+    float v[8];
+    load_group(ph, m, g, tag, limit, abort_flag, v);  // already produced: returns at once
+    for (int e = 0; e < 8; ++e) sumsq::add_term(acc, __fmul_rn(v[e], v[e]));
+  }
+  sumsq::warp_reduce(acc, 16);
+  if (lane == 0) {
+    for (int j = 0; j < 5; ++j) s_sum[warp * 5 + j] = acc.w[j];
+    s_flag[warp] = acc.nan_ | (acc.inf_ << 1);
+  }
+  chain_sync();
+  sumsq::Acc tot;
+  sumsq::zero(tot);
+  if (lane < kChainWarps) {
+    for (int j = 0; j < 5; ++j) tot.w[j] = s_sum[lane * 5 + j];
+    tot.nan_ = s_flag[lane] & 1u;
+    tot.inf_ = s_flag[lane] >> 1;
+  }
+  sumsq::warp_reduce(tot, kChainWarps / 2);
+  const float ss = __shfl_sync(0xffffffffu, sumsq::round_to_f32(tot), 0);
+  chain_sync();  // s_sum is free again
+  return ss;
+}
+
 template <int MT, int J>
-__global__ void __launch_bounds__(kThreads, 1) k_decode_chain(const __grid_constant__ Args a) {
+__global__ void __launch_bounds__(kChainThreads, 1) k_decode_chain(const __grid_constant__ Args a) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t full_bar[kMaxStages];
   __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
   __shared__ __align__(16) CPhase s_ph[2];
-  __shared__ float s_max[MT][kConsumerWarps];
-  __shared__ unsigned long long s_sum[MT][kConsumerWarps][5];
-  __shared__ uint32_t s_sumflag[MT][kConsumerWarps];
+  __shared__ float s_max[MT][kChainWarps];
+  __shared__ int s_omax[MT][kChainWarps];
+  __shared__ unsigned long long s_sum128[MT][kChainWarps][2];
+  __shared__ uint32_t s_sumflag[MT][kChainWarps];
+  __shared__ unsigned long long s_sum5[kChainWarps][5];  // the five-limb path
+  __shared__ uint32_t s_sumflag5[kChainWarps];
   // K-part merge per ring slot, stage row and token: count in bits 48.., the
   // parts' biased sums below; gated: the gate's biased sums in s_accv.
-  __shared__ unsigned long long s_acc[kMaxStages][32][MT];
-  __shared__ unsigned long long s_accv[kMaxStages][32][MT];
+  __shared__ unsigned long long s_acc[kMaxStages][kAccRows][MT];
+  __shared__ unsigned long long s_accv[kMaxStages][kAccRows][MT];
+  __shared__ StageCopy s_copies[kListMax];  // the start of the CTA's copy sequence
+  __shared__ int s_rel[kMaxStages];     // warps that have released the slot's stage
+  __shared__ int s_issued[kMaxStages];  // copies issued into the slot
   __shared__ int s_abort;
   __shared__ uint32_t s_run;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t ring = smem_addr(smem);
   int8_t* xs = reinterpret_cast<int8_t*>(smem + a.stages * a.slot_bytes);
+  const int S = a.stages;
+  const uint32_t c_first = a.cta_first[blockIdx.x];
+  const int n_copies = (int)(a.cta_first[blockIdx.x + 1] - c_first);
 
-  for (int q = threadIdx.x; q < kMaxStages * 32 * MT; q += kThreads) {
+  for (int q = threadIdx.x; q < kMaxStages * kAccRows * MT; q += kChainThreads) {
     (&s_acc[0][0][0])[q] = 0ull;
     (&s_accv[0][0][0])[q] = 0ull;
   }
   if (threadIdx.x < 32) copy_phase(a.phases[0], &s_ph[0], lane);
+  for (int i = threadIdx.x; i < n_copies && i < kListMax; i += kChainThreads)
+    s_copies[i] = a.copies[c_first + i];
   if (threadIdx.x == 0) {
-    for (int s = 0; s < a.stages; ++s) {
+    for (int s = 0; s < S; ++s) {
       mbar_init(smem_addr(&full_bar[s]), 1);
-      mbar_init(smem_addr(&empty_bar[s]), kConsumerWarps);
+      mbar_init(smem_addr(&empty_bar[s]), kChainWarps);
+      s_rel[s] = 0;
+      s_issued[s] = 0;
     }
     mbar_fence_init();
     s_abort = 0;
     const unsigned long long old = atomicAdd(a.counter, 1ull);
     s_run = (uint32_t)(old / gridDim.x);
+    // The first ring-full of weight stages.
+    for (int k = 0; k < S && k < n_copies; ++k) {
+      const StageCopy c = a.copies[c_first + k];  // (s_copies is not yet complete)
+      const uint32_t fb = smem_addr(&full_bar[k]);
+      const uint32_t dst = ring + k * a.slot_bytes;
+      mbar_arrive_expect_tx(fb, c.src1 ? 2 * c.bytes : c.bytes);
+      bulk_copy_g2s(dst, c.src0, c.bytes, fb);
+      if (c.src1) bulk_copy_g2s(dst + c.bytes, c.src1, c.bytes, fb);
+      s_issued[k] = 1;
+    }
   }
   __syncthreads();
   // tag of phase p's outputs in this run: tag0 + p
   const uint32_t tag0 = s_run * (uint32_t)a.nphases + 1u;
 
-  // ------------------------------------------------------------ producer
-  if (warp == kConsumerWarps) {
-    if (lane != 0) return;
-    const int S = a.stages;
-    int i = 0;
-    bool ok = true;
-    for (int p = 0; p < a.nphases && ok; ++p) {
-      const CPhase& ph = a.phases[p];
-      const int64_t rb = ph.K >> 2;
-      ok = for_each_stage(ph, [&](int t, int row, int nrows) {
-        const int slot = i % S, use = i / S;
-        if (use > 0 && (!mbar_wait(smem_addr(&empty_bar[slot]), (use - 1) & 1, a.wait) ||
-                        *(volatile int*)&s_abort)) {
-          atomicOr(&g_chain_error, kErrEmptyWait);
-          *(volatile int*)&s_abort = 1;
-          return false;
-        }
-        const uint32_t bytes = (uint32_t)(nrows * rb);
-        const uint32_t fb = smem_addr(&full_bar[slot]);
-        const uint32_t dst = ring + slot * a.slot_bytes;
-        mbar_arrive_expect_tx(fb, ph.gated ? 2 * bytes : bytes);
-        bulk_copy_g2s(dst, ph.t[t].Wq + (int64_t)row * rb, bytes, fb);
-        if (ph.gated) bulk_copy_g2s(dst + bytes, ph.t[1].Wq + (int64_t)row * rb, bytes, fb);
-        ++i;
-        return true;
-      });
-    }
-    // Never leave the CTA with a copy in flight.
-    for (int j = i > S ? i - S : 0; j < i; ++j)
-      if (!mbar_wait(smem_addr(&full_bar[j % S]), (j / S) & 1, kDrainCycles)) {
-        atomicOr(&g_chain_error, kErrDrain);
-        break;
-      }
-    return;
-  }
-
   // ------------------------------------------------------------ consumers
-  const int tid = threadIdx.x;  // 0 .. kConsumers-1
+  const int tid = threadIdx.x;  // 0 .. kChainThreads-1
   int c_slot = 0;
   uint32_t c_parity = 0;
+  int c_k = 0;  // stages of the CTA's sequence consumed so far
   constexpr int kDescWords = (int)(sizeof(CPhase) / 8);
   constexpr int kDescPerLane = (kDescWords + 31) / 32;
   for (int p = 0; p < a.nphases; ++p) {
     // Every consumer has finished phase p-1, so s_ph[p & 1] (written during
     // phase p-1) is complete and s_ph[(p+1) & 1] is free.
-    if (p > 0 && consumer_sync_or(*(volatile int*)&s_abort)) break;
+    if (p > 0 && chain_sync_or(*(volatile int*)&s_abort)) break;
     const CPhase& ph = s_ph[p & 1];
     // Loads whose latency overlaps the wait for the input: the next phase's
     // descriptor (warp 0; stored once the input is quantised), the matrices'
@@ -398,7 +529,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_chain(const __grid_const
       }
     };
     int r_begin, r_end;
-    cta_rows(ph.rows_total, r_begin, r_end);
+    cta_rows(ph, r_begin, r_end);
     if (r_begin >= r_end) {  // no rows of this phase here: its input is not needed
       store_desc();
       continue;
@@ -415,43 +546,43 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_chain(const __grid_const
     if (norm) {
 #pragma unroll
       for (int i = 0; i < kHold; ++i)
-        if (tid + i * kConsumers < ngroups) load_gain8(ph.g, tid + i * kConsumers, gh[i]);
+        if (tid + i * kChainThreads < ngroups) load_gain8(ph.g, tid + i * kChainThreads, gh[i]);
     }
     float xscale[MT];
     bool stop = false;
+    // Inputs beyond the held groups (K > 8 * kHold * kChainThreads) take the
+    // out-of-line paths below.
+    const bool wide = ngroups > kHold * kChainThreads;
 #pragma unroll
     for (int m = 0; m < MT; ++m) {
       xscale[m] = 0.0f;
       if (m >= a.M || stop) continue;
       float hv[kHold][8];
-      float mx = 0.0f;
-      sumsq::Acc acc;
-      sumsq::zero(acc);
       bool bad = false;
-      // The held groups (tid + i * kConsumers, i < kHold), kPipe at a time:
-      // their loads first, then the tags; a linked group not yet produced is
-      // polled again.  (Nine warps per CTA leave 168 registers a thread,
-      // which bounds how many raw groups can be in flight.)
+      // The held groups (tid + i * kChainThreads, i < kHold), kPipe at a
+      // time: their loads first, then the tags; a linked group not yet
+      // produced is polled again.
 #pragma unroll
       for (int c = 0; c < kHold; c += kPipe) {
-        if (bad || tid + c * kConsumers >= ngroups) break;
+        if (bad || tid + c * kChainThreads >= ngroups) break;
         Raw raw[kPipe];
         uint32_t pend = 0;
 #pragma unroll
         for (int i = 0; i < kPipe; ++i)
-          if (tid + (c + i) * kConsumers < ngroups)
-            issue_group(ph, m, tid + (c + i) * kConsumers, raw[i]);
+          if (tid + (c + i) * kChainThreads < ngroups)
+            issue_group(ph, m, tid + (c + i) * kChainThreads, raw[i]);
 #pragma unroll
         for (int i = 0; i < kPipe; ++i)
-          if (tid + (c + i) * kConsumers < ngroups && !decode_group(ph, raw[i], in_tag, hv[c + i]))
+          if (tid + (c + i) * kChainThreads < ngroups && !decode_group(ph, raw[i], in_tag, hv[c + i]))
             pend |= 1u << i;
         if (pend) {
           const long long t0 = clock64();
+          // Spin without sleeping: a sleeping poller can wake microseconds
+          // after its input has landed (measured on B300).
           while (pend) {
-            __nanosleep(32);
 #pragma unroll
             for (int i = 0; i < kPipe; ++i)
-              if ((pend >> i) & 1u) issue_group(ph, m, tid + (c + i) * kConsumers, raw[i]);
+              if ((pend >> i) & 1u) issue_group(ph, m, tid + (c + i) * kChainThreads, raw[i]);
 #pragma unroll
             for (int i = 0; i < kPipe; ++i)
               if (((pend >> i) & 1u) && decode_group(ph, raw[i], in_tag, hv[c + i]))
@@ -463,28 +594,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_chain(const __grid_const
           }
         }
       }
+      float mx = 0.0f;
+      if (!norm) {
 #pragma unroll
-      for (int i = 0; i < kHold; ++i)
-        if (tid + i * kConsumers < ngroups)
+        for (int i = 0; i < kHold; ++i)
+          if (tid + i * kChainThreads < ngroups)
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            if (norm) sumsq::add_term(acc, __fmul_rn(hv[i][e], hv[i][e]));
-            else mx = fmaxf(mx, fabsf(hv[i][e]));
-          }
-      // Groups beyond the held ones (K > 8 * kHold * kConsumers): one by one.
-      for (int i = kHold; !bad; ++i) {
-        const int g = tid + i * kConsumers;
-        if (g >= ngroups) break;
-        float v[8];
-        if (!load_group(ph, m, g, in_tag, a.wait, &s_abort, v)) {
-          bad = true;
-          break;
-        }
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          if (norm) sumsq::add_term(acc, __fmul_rn(v[e], v[e]));
-          else mx = fmaxf(mx, fabsf(v[e]));
-        }
+            for (int e = 0; e < 8; ++e) mx = fmaxf(mx, fabsf(hv[i][e]));
+        if (wide && !bad) mx = fmaxf(mx, wide_absmax(ph, m, tid, in_tag, a.wait, &s_abort, 0.0f, &bad));
       }
       if (bad) {
         atomicOr(&g_chain_error, kErrLinkWait);
@@ -492,92 +609,106 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_chain(const __grid_const
       }
       float r = 0.0f;
       if (norm) {
-        sumsq::warp_reduce(acc, 16);
-        if (lane == 0) {
+        // ss = exact sum of the squares: in 128 bits anchored below the
+        // largest square (exact_sumsq.cuh), or, for a row whose squares span
+        // more than that window (or a wide row), the five-limb exact sum.
+        // the largest square is the square of the largest |x|
+        float xmax = 0.0f;
 #pragma unroll
-          for (int j = 0; j < 5; ++j) s_sum[m][warp][j] = acc.w[j];
-          s_sumflag[m][warp] = acc.nan_ | (acc.inf_ << 1);
-        }
-        if (consumer_sync_or(*(volatile int*)&s_abort)) {
+        for (int i = 0; i < kHold; ++i)
+          if (tid + i * kChainThreads < ngroups)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) xmax = fmaxf(xmax, fabsf(hv[i][e]));
+        const int omax = __reduce_max_sync(0xffffffffu, sumsq::term_offset(__fmul_rn(xmax, xmax)));
+        if (lane == 0) s_omax[m][warp] = omax;
+        if (chain_sync_or(*(volatile int*)&s_abort)) {
           stop = true;
           continue;
         }
-        sumsq::Acc tot;
-        sumsq::zero(tot);
-        if (lane < kConsumerWarps) {
+        int o_all = s_omax[m][0];
 #pragma unroll
-          for (int j = 0; j < 5; ++j) tot.w[j] = s_sum[m][lane][j];
-          tot.nan_ = s_sumflag[m][lane] & 1u;
-          tot.inf_ = s_sumflag[m][lane] >> 1;
+        for (int w = 1; w < kChainWarps; ++w) o_all = max(o_all, s_omax[m][w]);
+        const int anchor = o_all - 88 > 0 ? o_all - 88 : 0;
+        sumsq::Acc128 acc;
+        sumsq::zero(acc);
+#pragma unroll
+        for (int i = 0; i < kHold; ++i)
+          if (tid + i * kChainThreads < ngroups)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) sumsq::add_term(acc, __fmul_rn(hv[i][e], hv[i][e]), anchor);
+        sumsq::warp_reduce(acc, 16);
+        if (lane == 0) {
+          s_sum128[m][warp][0] = acc.lo;
+          s_sum128[m][warp][1] = acc.hi;
+          s_sumflag[m][warp] = acc.nan_ | (acc.inf_ << 1) | (acc.lost << 2);
         }
-        sumsq::warp_reduce(tot, kConsumerWarps / 2);
-        r = __shfl_sync(0xffffffffu, sumsq::rms_scale(sumsq::round_to_f32(tot), K, ph.eps), 0);
+        if (chain_sync_or(*(volatile int*)&s_abort)) {
+          stop = true;
+          continue;
+        }
+        sumsq::Acc128 tot;
+        sumsq::zero(tot);
+        if (lane < kChainWarps) {
+          tot.lo = s_sum128[m][lane][0];
+          tot.hi = s_sum128[m][lane][1];
+          tot.nan_ = s_sumflag[m][lane] & 1u;
+          tot.inf_ = (s_sumflag[m][lane] >> 1) & 1u;
+          tot.lost = s_sumflag[m][lane] >> 2;
+        }
+        sumsq::warp_reduce(tot, kChainWarps / 2);
+        float ss;
+        if (__shfl_sync(0xffffffffu, tot.lost, 0) || wide)  // uniform over the CTA
+          ss = exact_row_sumsq(ph, m, tid, in_tag, a.wait, &s_abort, &s_sum5[0][0], &s_sumflag5[0]);
+        else
+          ss = __shfl_sync(0xffffffffu, sumsq::round_to_f32(tot, anchor), 0);
+        r = sumsq::rms_scale(ss, K, ph.eps);
         // n = (x * r) * g, then its largest magnitude
 #pragma unroll
         for (int i = 0; i < kHold; ++i)
-          if (tid + i * kConsumers < ngroups)
+          if (tid + i * kChainThreads < ngroups)
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
               hv[i][e] = __fmul_rn(__fmul_rn(hv[i][e], r), gh[i][e]);
               mx = fmaxf(mx, fabsf(hv[i][e]));
             }
-        for (int i = kHold;; ++i) {
-          const int g = tid + i * kConsumers;
-          if (g >= ngroups) break;
-          float v[8], gv[8];
-          load_group(ph, m, g, in_tag, a.wait, &s_abort, v);
-          load_gain8(ph.g, g, gv);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) mx = fmaxf(mx, fabsf(__fmul_rn(__fmul_rn(v[e], r), gv[e])));
-        }
+        if (wide) mx = fmaxf(mx, wide_absmax(ph, m, tid, in_tag, a.wait, &s_abort, r, &bad));
       }
       mx = warp_max_f32(mx);
       if (lane == 0) s_max[m][warp] = mx;
-      if (consumer_sync_or(*(volatile int*)&s_abort)) {
+      if (chain_sync_or(*(volatile int*)&s_abort)) {
         stop = true;
         continue;
       }
       float amax = s_max[m][0];
 #pragma unroll
-      for (int w = 1; w < kConsumerWarps; ++w) amax = fmaxf(amax, s_max[m][w]);
+      for (int w = 1; w < kChainWarps; ++w) amax = fmaxf(amax, s_max[m][w]);
       const ActScale sc = act_scale_from_absmax(amax);
       xscale[m] = sc.scale;
-      for (int i = 0;; ++i) {
-        const int g = tid + i * kConsumers;
+      int8_t* xs_row = xs + (int64_t)m * a.xs_stride;
+#pragma unroll
+      for (int i = 0; i < kHold; ++i) {
+        const int g = tid + i * kChainThreads;
         if (g >= ngroups) break;
-        float v[8];
-        if (i < kHold) {
-#pragma unroll
-          for (int h = 0; h < kHold; ++h)
-            if (h == i)
-#pragma unroll
-              for (int e = 0; e < 8; ++e) v[e] = hv[h][e];
-        } else {
-          load_group(ph, m, g, in_tag, a.wait, &s_abort, v);
-          if (norm) {
-            float gv[8];
-            load_gain8(ph.g, g, gv);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) v[e] = __fmul_rn(__fmul_rn(v[e], r), gv[e]);
-          }
-        }
         int q[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) q[e] = round_clip(__fmul_rn(v[e], sc.inv), -128.f, 127.f);
+        for (int e = 0; e < 8; ++e) q[e] = round_clip(__fmul_rn(hv[i][e], sc.inv), -128.f, 127.f);
         const uint2 packed = make_uint2(pack_i8x4(q[0], q[1], q[2], q[3]),
                                         pack_i8x4(q[4], q[5], q[6], q[7]));
-        *reinterpret_cast<uint2*>(xs + (int64_t)m * a.xs_stride + 8 * g) = packed;
+        *reinterpret_cast<uint2*>(xs_row + xs_offset(g)) = packed;
         if (reporter && ph.xq_out)
           *reinterpret_cast<uint2*>(ph.xq_out + (int64_t)m * K + 8 * g) = packed;
       }
+      if (wide)
+        wide_quantize(ph, m, tid, in_tag, a.wait, &s_abort, r, sc.inv, xs_row,
+                      reporter ? ph.xq_out : nullptr);
       if (reporter && tid == 0 && ph.xs_out) ph.xs_out[m] = sc.scale;
     }
-    if (stop || consumer_sync_or(*(volatile int*)&s_abort)) break;
+    if (stop || chain_sync_or(*(volatile int*)&s_abort)) break;
     store_desc();
 
     // ---- this warp's K part and its activations in registers
     const int wk = ph.wk;
-    const int kw = warp % wk, wr = warp / wk, nwr = kConsumerWarps / wk;
+    const int kw = warp % wk, wr = warp / wk, nwr = kChainWarps / wk;
     const int nch = K >> 6;
     const int k_lo = kw * ph.kpart, k_hi = min(nch, k_lo + ph.kpart);
     int valid_j = 0;
@@ -596,7 +727,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_chain(const __grid_const
           uint4 v = make_uint4(0, 0, 0, 0);
           if (m < a.M && j < valid_j)
             v = *reinterpret_cast<const uint4*>(xs + (int64_t)m * a.xs_stride +
-                                                64 * (k_lo + lane + 32 * j) + 16 * s);
+                                                xs_chunk_offset(k_lo + lane + 32 * j, s));
           xr[m][j][s] = v;
           lsum[m] = dp4a_ss(v.x, 0x01010101u, lsum[m]);
           lsum[m] = dp4a_ss(v.y, 0x01010101u, lsum[m]);
@@ -612,22 +743,64 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_chain(const __grid_const
     for_each_stage(ph, [&](int t, int row0, int nrows) {
       const int slot = c_slot;
       const uint32_t parity = c_parity;
-      if (++c_slot == a.stages) {
+      const int k = c_k++;
+      if (++c_slot == S) {
         c_slot = 0;
         c_parity ^= 1u;
       }
-      if (*(volatile int*)&s_abort) return true;
+      // The copy that will refill this slot (stage k + S): from shared
+      // memory, or (past the held start of the sequence) fetched now so that
+      // whichever warp releases the slot last can issue it at once.
+      StageCopy next = {nullptr, nullptr, 0u, 0u};
+      if (lane == 0 && k + S < n_copies)
+        next = k + S < kListMax ? s_copies[k + S] : a.copies[c_first + k + S];
+      auto release = [&]() {
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(smem_addr(&empty_bar[slot]));
+          if (atomicAdd(&s_rel[slot], 1) == kChainWarps - 1) {
+            // The last warp to release the slot refills it.  Its wait on the
+            // slot's empty barrier (every warp arrived, with release semantics)
+            // orders all warps' reads of the slot, and what they saw of
+            // s_abort, before the new copy; a warp that skipped its wait for
+            // the stage's data had seen s_abort set, so no copy is issued then.
+            s_rel[slot] = 0;
+            bool free_slot = next.src0 != nullptr;
+            if (free_slot && !mbar_wait(smem_addr(&empty_bar[slot]), (uint32_t)((k / S) & 1), a.wait)) {
+              atomicOr(&g_chain_error, kErrEmptyWait);
+              *(volatile int*)&s_abort = 1;
+              free_slot = false;
+            }
+            if (free_slot && *(volatile int*)&s_abort) free_slot = false;
+            if (free_slot) {
+              const uint32_t fb = smem_addr(&full_bar[slot]);
+              const uint32_t dst = ring + slot * a.slot_bytes;
+              mbar_arrive_expect_tx(fb, next.src1 ? 2 * next.bytes : next.bytes);
+              bulk_copy_g2s(dst, next.src0, next.bytes, fb);
+              if (next.src1) bulk_copy_g2s(dst + next.bytes, next.src1, next.bytes, fb);
+              ++s_issued[slot];
+            }
+          }
+        }
+      };
+      if (*(volatile int*)&s_abort) {
+        release();
+        return true;
+      }
       if (!mbar_wait(smem_addr(&full_bar[slot]), parity, a.wait)) {
         if (lane == 0) atomicOr(&g_chain_error, kErrFullWait);
         *(volatile int*)&s_abort = 1;
+        release();
         return true;
       }
       const uint32_t sbase = ring + slot * a.slot_bytes + 16 * (k_lo + lane);
       const int my_rows = nrows > wr ? (nrows - wr + nwr - 1) / nwr : 0;
       // Lane q*MT + m keeps the (warp-uniform) sums of row q for token m.
       int tot = 0, totv = 0;
+      // (Row loops are not unrolled: one copy of the dot-product code keeps
+      // the kernel small enough for the instruction cache.)
       if (!ph.gated) {
-#pragma unroll
+#pragma unroll 1
         for (int q = 0; q < kMaxRowsPerWarp; q += 2) {
           if (q + 1 < my_rows) {
             const uint32_t w[2] = {sbase + (uint32_t)((wr + q * nwr) * rb),
@@ -654,7 +827,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_chain(const __grid_const
         }
       } else {
         // row pair q: up row at q, gate row at nrows + q (the slot's second copy)
-#pragma unroll
+#pragma unroll 1
         for (int q = 0; q < kMaxRowsPerWarp; ++q) {
           if (q < my_rows) {
             const uint32_t w[2] = {sbase + (uint32_t)((wr + q * nwr) * rb),
@@ -730,11 +903,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_chain(const __grid_const
           }
         }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_addr(&empty_bar[slot]));
+      release();
       return true;
     });
   }
+  // Never leave the CTA with a copy in flight: wait for the last copy issued
+  // into every slot (already landed unless a wait ran out).
+  chain_sync();
+  if (tid == 0)
+    for (int s = 0; s < S; ++s)
+      if (s_issued[s] > 0 &&
+          !mbar_wait(smem_addr(&full_bar[s]), (uint32_t)((s_issued[s] - 1) & 1), kDrainCycles)) {
+        atomicOr(&g_chain_error, kErrDrain);
+        break;
+      }
 }
 
 // ---------------------------------------------------------------- host side
@@ -757,13 +939,13 @@ bool plan_phase(int64_t K, int j, bool gated, PhasePlan* pp) {
   if (K < 64 || K % 64 != 0 || K > 65536) return false;
   const int nch = (int)(K / 64);
   int wk = 0;
-  for (int w = 1; w <= 8; w *= 2)
+  for (int w = 1; w <= kChainWarps; w *= 2)
     if ((nch + w - 1) / w <= 32 * j) {
       wk = w;
       break;
     }
   if (!wk) return false;
-  const int nwr = kConsumerWarps / wk;
+  const int nwr = kChainWarps / wk;
   const int64_t row_bytes = K / 4 * (gated ? 2 : 1);  // per stage row (gated: a row pair)
   int64_t R = kStageTarget / row_bytes / nwr * nwr;
   if (R < nwr) R = nwr;
@@ -787,7 +969,8 @@ Range rng(const void* p, size_t bytes) {
 bool overlap(const Range& a, const Range& b) { return a.lo < b.hi && b.lo < a.hi; }
 
 // What validating a chain description yields: per phase the input kind and
-// producing phase, and where each link buffer sits in the table.
+// producing phase, where each link buffer sits in the table, and every CTA's
+// sequence of weight copies.
 struct ChainLayout {
   std::vector<int> in_kind, in_phase;
   std::vector<size_t> in_off;                  // table offset of a linked input's words
@@ -795,17 +978,68 @@ struct ChainLayout {
   std::vector<std::vector<size_t>> link32_off;
   std::vector<size_t> hlink_off;
   std::vector<PhasePlan> plan;
-  size_t phases_off, total;
-  int mt, j, slot, stages, xs_stride;
+  std::vector<uint32_t> cta_first;  // [ctas + 1]
+  std::vector<StageCopy> copies;
+  size_t phases_off, first_off, copies_off, total;
+  int ctas, mt, j, slot, stages, xs_stride;
   size_t smem;
 };
 
+// CTA c's rows of a phase with `rows` rows split over `ctas` CTAs (the rule
+// of the kernel's cta_rows).
+void split_rows(int64_t rows, int ctas, int c, int64_t* r0, int64_t* r1) {
+  const int64_t q = rows / ctas, rem = rows % ctas;
+  *r0 = c * q + std::min<int64_t>(c, rem);
+  *r1 = *r0 + q + (c < rem ? 1 : 0);
+}
+
+// Every CTA's copy sequence, in the order of the kernel's for_each_stage.
+void list_copies(const bitnet_decode_phase* ph, int np, ChainLayout* L) {
+  L->cta_first.assign((size_t)L->ctas + 1, 0);
+  L->copies.clear();
+  for (int c = 0; c < L->ctas; ++c) {
+    L->cta_first[(size_t)c] = (uint32_t)L->copies.size();
+    for (int i = 0; i < np; ++i) {
+      const bitnet_decode_phase& p = ph[i];
+      const bool gated = (p.flags & BITNET_PHASE_GATED) != 0;
+      const int64_t rb = p.K / 4, R = L->plan[(size_t)i].rows_per_stage;
+      int64_t rows = 0;
+      for (int t = 0; t < p.count; ++t) rows += p.targets[t].N;
+      if (gated) rows = p.targets[0].N;
+      int64_t r0, r1;
+      split_rows(rows, L->ctas, c, &r0, &r1);
+      if (gated) {
+        for (int64_t r = r0; r < r1; r += R) {
+          const int64_t n = std::min(R, r1 - r);
+          L->copies.push_back({p.targets[0].Wq + r * rb, p.targets[1].Wq + r * rb,
+                               (uint32_t)(n * rb), 0u});
+        }
+        continue;
+      }
+      int64_t row0 = 0;
+      for (int t = 0; t < p.count; ++t) {
+        const int64_t N = p.targets[t].N;
+        const int64_t lo = std::max(r0, row0), hi = std::min(r1, row0 + N);
+        for (int64_t r = lo; r < hi; r += R) {
+          const int64_t n = std::min(R, hi - r);
+          L->copies.push_back({p.targets[t].Wq + (r - row0) * rb, nullptr, (uint32_t)(n * rb), 0u});
+        }
+        row0 += N;
+      }
+    }
+  }
+  L->cta_first[(size_t)L->ctas] = (uint32_t)L->copies.size();
+}
+
 // Checks the description and lays out the table.  BITNET_ERR_* on failure.
-// max_dyn_smem: the dynamic shared memory a CTA of the chain kernel may use.
+// max_dyn_smem: the dynamic shared memory a CTA of the chain kernel may use;
+// ctas: the grid (one CTA per SM).
 bitnet_status layout_chain(const bitnet_decode_phase* ph, int np, int64_t M, size_t max_dyn_smem,
-                           ChainLayout* L) {
+                           int ctas, ChainLayout* L) {
   if (!ph) return BITNET_ERR_NULL;
   if (np < 1 || np > kMaxPhases || M < 1 || M > kDecodeMaxM) return BITNET_ERR_SHAPE;
+  if (ctas < 1 || ctas > kMaxChainCtas) return BITNET_ERR_SHAPE;
+  L->ctas = ctas;
   L->mt = tokens_per_pass(M);
   L->j = 0;
   int64_t max_k = 0;
@@ -882,8 +1116,11 @@ bitnet_status layout_chain(const bitnet_decode_phase* ph, int np, int64_t M, siz
   L->link16_off.assign(np, std::vector<size_t>(kTargets, 0));
   L->link32_off.assign(np, std::vector<size_t>(kTargets, 0));
   L->hlink_off.assign(np, 0);
+  list_copies(ph, np, L);
   L->phases_off = kHeader;
-  size_t off = round256(kHeader + (size_t)np * sizeof(CPhase));
+  L->first_off = round256(kHeader + (size_t)np * sizeof(CPhase));
+  L->copies_off = round256(L->first_off + L->cta_first.size() * sizeof(uint32_t));
+  size_t off = round256(L->copies_off + L->copies.size() * sizeof(StageCopy));
   for (int i = 0; i < np; ++i) {
     const bitnet_decode_phase& p = ph[i];
     const bool bf = p.x != nullptr;
@@ -989,7 +1226,7 @@ cudaError_t configure(int smem, int* resident) {
   cudaError_t e = cudaFuncSetAttribute(k_decode_chain<MT, J>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(resident, k_decode_chain<MT, J>, kThreads,
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(resident, k_decode_chain<MT, J>, kChainThreads,
                                                        smem);
 }
 
@@ -1005,7 +1242,7 @@ template <int MT, int J>
 cudaError_t launch_coop(const Args& a, int ctas, size_t smem, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(ctas);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(kChainThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -1018,10 +1255,17 @@ cudaError_t launch_coop(const Args& a, int ctas, size_t smem, cudaStream_t s) {
 
 }  // namespace
 
+// The grid of a chain on the current device (one CTA per SM); 148 when no
+// device answers (host-only checks).
+int chain_ctas() {
+  int n = 0;
+  return sm_count(&n) == cudaSuccess && n > 0 ? n : 148;
+}
+
 bitnet_status check_decode_chain(const bitnet_decode_phase* phases, int nphases, int64_t M,
                                  size_t* table_bytes) {
   ChainLayout L;  // the table layout does not depend on the ring depth
-  const bitnet_status st = layout_chain(phases, nphases, M, (size_t)1 << 30, &L);
+  const bitnet_status st = layout_chain(phases, nphases, M, (size_t)1 << 30, chain_ctas(), &L);
   *table_bytes = st == BITNET_OK ? L.total : 0;
   return st;
 }
@@ -1032,17 +1276,19 @@ bitnet_status build_decode_chain(const bitnet_decode_phase* phases, int nphases,
   *cuda_err = cudaSuccess;
   ChainLayout L;
   size_t max_dyn = 0;
-  cudaError_t e = max_dynamic_smem(tokens_per_pass(M), chain_j(phases, nphases, M), &max_dyn);
+  int ctas = 0;
+  cudaError_t e = sm_count(&ctas);
+  if (e == cudaSuccess)
+    e = max_dynamic_smem(tokens_per_pass(M), chain_j(phases, nphases, M), &max_dyn);
   if (e != cudaSuccess) {
     *cuda_err = e;
     return BITNET_ERR_CUDA;
   }
-  bitnet_status st = layout_chain(phases, nphases, M, max_dyn, &L);
+  bitnet_status st = layout_chain(phases, nphases, M, max_dyn, ctas, &L);
   if (st != BITNET_OK) return st;
   if (table_bytes < L.total) return BITNET_ERR_WORKSPACE;
-  int ctas = 0, resident = 0;
-  e = sm_count(&ctas);
-  if (e == cudaSuccess) e = configure_variant(L.mt, L.j, (int)L.smem, &resident);
+  int resident = 0;
+  e = configure_variant(L.mt, L.j, (int)L.smem, &resident);
   if (e != cudaSuccess) {
     *cuda_err = e;
     return BITNET_ERR_CUDA;
@@ -1088,15 +1334,24 @@ bitnet_status build_decode_chain(const bitnet_decode_phase* phases, int nphases,
     c.xs_out = p.x_scale_out;
     c.count = p.count;
     c.rows_total = gated ? (int)p.targets[0].N : (int)rows;
+    c.rows_q = c.rows_total / ctas;
+    c.rows_rem = c.rows_total % ctas;
     c.K = (int)p.K;
     c.wk = L.plan[i].wk;
     c.kpart = L.plan[i].kpart;
     c.rows_per_stage = L.plan[i].rows_per_stage;
   }
-  // Clear the header (run counter) and every link word, then the phases.
+  // Clear the header (run counter) and every link word, then the phases and
+  // the copy lists.
   e = cudaMemset(base, 0, L.total);
   if (e == cudaSuccess)
     e = cudaMemcpy(base + L.phases_off, host.data(), host.size() * sizeof(CPhase),
+                   cudaMemcpyHostToDevice);
+  if (e == cudaSuccess)
+    e = cudaMemcpy(base + L.first_off, L.cta_first.data(), L.cta_first.size() * sizeof(uint32_t),
+                   cudaMemcpyHostToDevice);
+  if (e == cudaSuccess && !L.copies.empty())
+    e = cudaMemcpy(base + L.copies_off, L.copies.data(), L.copies.size() * sizeof(StageCopy),
                    cudaMemcpyHostToDevice);
   if (e != cudaSuccess) {
     *cuda_err = e;
@@ -1112,7 +1367,9 @@ bitnet_status build_decode_chain(const bitnet_decode_phase* phases, int nphases,
   chain->cfg[4] = L.xs_stride;
   chain->cfg[5] = (int)L.smem;
   chain->cfg[6] = ctas;
-  chain->cfg[7] = 0;
+  chain->cfg[7] = (int)(L.first_off / 256);
+  chain->cfg[8] = (int)(L.copies_off / 256);
+  for (int i = 9; i < 12; ++i) chain->cfg[i] = 0;
   return BITNET_OK;
 }
 
@@ -1122,6 +1379,8 @@ cudaError_t launch_decode_chain(const bitnet_decode_chain* chain, long long wait
   uint8_t* t = static_cast<uint8_t*>(chain->table);
   a.phases = reinterpret_cast<const CPhase*>(t + kHeader);
   a.counter = reinterpret_cast<unsigned long long*>(t);
+  a.cta_first = reinterpret_cast<const uint32_t*>(t + (size_t)chain->cfg[7] * 256);
+  a.copies = reinterpret_cast<const StageCopy*>(t + (size_t)chain->cfg[8] * 256);
   a.nphases = chain->nphases;
   a.M = (int)chain->M;
   a.stages = chain->cfg[2];

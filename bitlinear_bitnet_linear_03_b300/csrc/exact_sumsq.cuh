@@ -133,6 +133,90 @@ __device__ __forceinline__ float round_to_f32(const Acc& s) {
   return __uint_as_float(((uint32_t)e8 << 23) | ((uint32_t)mant & 0x7fffffu));
 }
 
+// ---- The common case in 128 bits.  With o_max the largest offset of any
+// square (t = m * 2^(o - 149), m < 2^24), the sum is taken in units of
+// 2^(anchor - 149), anchor = max(o_max - 88, 0): every term is then below
+// 2^112 and the sum of up to 2^16 of them below 2^128.  A term with nonzero
+// bits below the anchor (a square 2^88 times smaller than the largest) sets
+// `lost`; the caller then redoes the row with the five-limb sum above.
+struct Acc128 {
+  uint64_t lo, hi;
+  uint32_t nan_, inf_, lost;
+};
+
+__device__ __forceinline__ void zero(Acc128& a) {
+  a.lo = a.hi = 0;
+  a.nan_ = a.inf_ = a.lost = 0;
+}
+
+__device__ __forceinline__ void add2(Acc128& a, uint64_t l, uint64_t h) {
+  asm("add.cc.u64 %0, %0, %2;\n\taddc.u64 %1, %1, %3;" : "+l"(a.lo), "+l"(a.hi) : "l"(l), "l"(h));
+}
+
+// Offset o of a finite nonzero square (-1 for zero or non-finite).
+__device__ __forceinline__ int term_offset(float t) {
+  const uint32_t u = __float_as_uint(t);
+  const uint32_t e = (u >> 23) & 0xffu, f = u & 0x7fffffu;
+  if (e == 255u || (e == 0u && f == 0u)) return -1;
+  return e ? (int)e - 1 : 0;
+}
+
+__device__ __forceinline__ void add_term(Acc128& a, float t, int anchor) {
+  const uint32_t u = __float_as_uint(t);
+  const uint32_t e = (u >> 23) & 0xffu, f = u & 0x7fffffu;
+  const uint64_t m = e ? (uint64_t)(f | 0x800000u) : (uint64_t)f;
+  const int sh = (e ? (int)e - 1 : 0) - anchor;  // <= 88 by the choice of anchor
+  if (e == 255u) {
+    a.nan_ |= f != 0u;
+    a.inf_ |= f == 0u;
+  } else if (sh >= 0) {
+    const uint64_t l = sh < 64 ? m << sh : 0ull;
+    const uint64_t h = sh >= 64 ? m << (sh - 64) : (sh > 40 ? m >> (64 - sh) : 0ull);
+    add2(a, l, h);
+  } else if (m != 0ull) {
+    if (-sh >= 24 || (m & ((1ull << -sh) - 1ull))) a.lost = 1;
+    if (-sh < 24) add2(a, m >> -sh, 0ull);
+  }
+}
+
+__device__ __forceinline__ void warp_reduce(Acc128& a, int first) {
+  for (int off = first; off >= 1; off >>= 1) {
+    const uint64_t ol = shfl_xor_u64(a.lo, off, 0xffffffffu), oh = shfl_xor_u64(a.hi, off, 0xffffffffu);
+    add2(a, ol, oh);
+    a.nan_ |= __shfl_xor_sync(0xffffffffu, a.nan_, off);
+    a.inf_ |= __shfl_xor_sync(0xffffffffu, a.inf_, off);
+    a.lost |= __shfl_xor_sync(0xffffffffu, a.lost, off);
+  }
+}
+
+// Nearest binary32 (ties to even) to S * 2^(anchor - 149), S = hi * 2^64 + lo.
+__device__ __forceinline__ float round_to_f32(const Acc128& a, int anchor) {
+  if (a.nan_) return __uint_as_float(0x7fc00000u);
+  if (a.inf_) return __uint_as_float(0x7f800000u);
+  const unsigned __int128 S = ((unsigned __int128)a.hi << 64) | a.lo;
+  if (S == 0) return 0.0f;
+  const int bl = a.hi ? 128 - __clzll((long long)a.hi) : 64 - __clzll((long long)a.lo);
+  int drop = bl - 24 > -anchor ? bl - 24 : -anchor;  // never keep a bit below 2^-149
+  uint64_t mant;
+  if (drop <= 0) {
+    mant = (uint64_t)(S << (-drop));  // exact
+  } else {
+    mant = (uint64_t)(S >> drop) & 0xffffffull;
+    const bool round_bit = (uint64_t)(S >> (drop - 1)) & 1u;
+    const bool sticky = drop > 1 && (S << (128 - (drop - 1))) != 0;
+    if (round_bit && (sticky || (mant & 1u))) mant += 1;
+    if (mant == (1ull << 24)) {
+      mant >>= 1;
+      drop += 1;
+    }
+  }
+  const int d5 = drop + anchor;  // value = mant * 2^(d5 - 149)
+  if (mant < (1ull << 23)) return __uint_as_float((uint32_t)mant);  // subnormal (d5 == 0)
+  const int e8 = d5 + 1;
+  if (e8 >= 255) return __uint_as_float(0x7f800000u);
+  return __uint_as_float(((uint32_t)e8 << 23) | ((uint32_t)mant & 0x7fffffu));
+}
+
 // r = 1 / sqrt(ss / H + eps), four binary32 operations.
 __device__ __forceinline__ float rms_scale(float ss, int H, float eps) {
   const float q = __fdiv_rn(ss, (float)H);

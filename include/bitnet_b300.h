@@ -229,7 +229,8 @@ bitnet_status bitnet_linear_bf16(const uint16_t* x, int64_t M, int64_t K,
  * another (BITNET_ERR_ALIAS otherwise).  A CTA that owns no rows of a phase
  * skips it.  The weights stream in ahead, across phases.
  * table: device memory of bitnet_decode_chain_bytes(phases, nphases, M)
- * bytes, 256-byte aligned, owned by the caller; _build fills it
+ * bytes (computed for the current device's SM count), 256-byte aligned,
+ * owned by the caller; _build fills it
  * (synchronously: call it outside stream capture; it returns after the
  * copy) and clears it.  `chain` (host) receives what _run needs.  Runs of one
  * table must not overlap on the GPU.  All CTAs must be resident at once
@@ -255,7 +256,7 @@ typedef struct bitnet_decode_chain {
   void* table;
   int64_t M;
   int nphases;
-  int cfg[8]; /* launch configuration, filled by bitnet_decode_chain_build */
+  int cfg[12]; /* launch configuration, filled by bitnet_decode_chain_build */
 } bitnet_decode_chain;
 
 /* 0 if the description is invalid (the same checks as _build). */
