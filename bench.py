@@ -35,12 +35,24 @@ import numpy as np
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-HIDDEN, FFN = 2560, 6912
 EPS = 1e-5
-# (name, N, K, phase) of one decoder layer's BitLinear products.
-LAYER_SHAPES = [("q", HIDDEN, HIDDEN, "qkv"), ("k", 640, HIDDEN, "qkv"), ("v", 640, HIDDEN, "qkv"),
-                ("o", HIDDEN, HIDDEN, "o"), ("up", FFN, HIDDEN, "ffn"),
-                ("gate", FFN, HIDDEN, "ffn"), ("down", HIDDEN, FFN, "down")]
+# Model dimensions: (hidden, FFN, K/V width, layers).  2B: the BitNet b1.58
+# 2B4T shapes the pages describe; 8B: the Llama3-8B-1.58 model the pages list
+# (hidden 4096, FFN 14336, 8 K/V heads of 128 -- the reading of that
+# architecture's dimensions).
+DIMS_2B = (2560, 6912, 640, 30)
+DIMS_8B = (4096, 14336, 1024, 32)
+HIDDEN, FFN = DIMS_2B[0], DIMS_2B[1]
+
+
+def layer_shapes(dims=DIMS_2B):
+    """(name, N, K, phase) of one decoder layer's BitLinear products."""
+    H, F, KV = dims[0], dims[1], dims[2]
+    return [("q", H, H, "qkv"), ("k", KV, H, "qkv"), ("v", KV, H, "qkv"), ("o", H, H, "o"),
+            ("up", F, H, "ffn"), ("gate", F, H, "ffn"), ("down", H, F, "down")]
+
+
+LAYER_SHAPES = layer_shapes(DIMS_2B)
 METRIC = "BitLinear decode GB/s & % HBM roofline; prefill int8 TOPS & % tensor peak"
 WORKLOAD = ("decode step, batch 1, 2B-class shapes (hidden 2560, FFN 6912), 30 layers of "
             "distinct ternary weights, dependent phases QKV -> subln O -> subln up/gate "
@@ -63,20 +75,21 @@ def parse_args():
     return ap.parse_args()
 
 
-def layer_bytes():
+def layer_bytes(dims=DIMS_2B):
     """Algorithmic bytes of one layer: packed weights and their scales, the
     two norm gains, each phase's input read once in its precision (QKV, O,
-    up/gate: bf16 [2560]; down: binary32 h [6912]) and every output written
+    up/gate: bf16 [hidden]; down: binary32 h [FFN]) and every output written
     once (Q, O, down: bf16; K, V, h: binary32)."""
-    w = sum(N * K // 4 + 4 for _, N, K, _ in LAYER_SHAPES)
-    gains = 2 * 4 * HIDDEN
-    inputs = 3 * 2 * HIDDEN + 4 * FFN
-    outputs = 2 * HIDDEN + 2 * 4 * 640 + 2 * HIDDEN + 4 * FFN + 2 * HIDDEN
+    H, F, KV = dims[0], dims[1], dims[2]
+    w = sum(N * K // 4 + 4 for _, N, K, _ in layer_shapes(dims))
+    gains = 2 * 4 * H
+    inputs = 3 * 2 * H + 4 * F
+    outputs = 2 * H + 2 * 4 * KV + 2 * H + 4 * F + 2 * H
     return w + gains + inputs + outputs
 
 
-def weight_bytes():
-    return sum(N * K // 4 for _, N, K, _ in LAYER_SHAPES)
+def weight_bytes(dims=DIMS_2B):
+    return sum(N * K // 4 for _, N, K, _ in layer_shapes(dims))
 
 
 # ----------------------------------------------------------------- clocks
@@ -135,43 +148,45 @@ class DecodeStep:
     step input (bf16 [1, HIDDEN]); gains: optional (attention-side, FFN-side)
     lists of binary32 [HIDDEN] gains per layer."""
 
-    def __init__(self, layers, weights=None, x0=None, gains=None, seed=0):
+    def __init__(self, layers, weights=None, x0=None, gains=None, seed=0, dims=DIMS_2B):
         import torch
         import bitlinear_bitnet_linear_03_b300 as bn
         from bitlinear_bitnet_linear_03_b300 import synth
         self.torch, self.bn = torch, bn
         dev = torch.device("cuda")
         self.layers = layers
+        self.dims = dims
+        H, F, KV = dims[0], dims[1], dims[2]
         if weights is None:
-            ws_q = torch.empty(bn.bitnet_quantize_weights_workspace(FFN, HIDDEN) * 2,
+            ws_q = torch.empty(bn.bitnet_quantize_weights_workspace(F, H) * 2,
                                dtype=torch.uint8, device=dev)
             weights = []
             for li in range(layers):
                 L = {}
-                for j, (name, N, K, _) in enumerate(LAYER_SHAPES):
+                for j, (name, N, K, _) in enumerate(layer_shapes(dims)):
                     W = synth.weights_f32(N, K, seed=seed * 100000 + li * 16 + j, device="cuda")
                     L[name] = bn.bitnet_quantize_weights(W, ws=ws_q)
                     del W
                 weights.append(L)
         self.W = weights
         if gains is None:
-            gains = ([torch.from_numpy(synth.gain_random(HIDDEN, 300 + li)).to(dev)
+            gains = ([torch.from_numpy(synth.gain_random(H, 300 + li)).to(dev)
                       for li in range(layers)],
-                     [torch.from_numpy(synth.gain_random(HIDDEN, 600 + li)).to(dev)
+                     [torch.from_numpy(synth.gain_random(H, 600 + li)).to(dev)
                       for li in range(layers)])
         self.g_attn, self.g_ffn = gains
         if x0 is None:
-            x0 = synth.tokens_bf16(1, HIDDEN, seed=seed * 100000 + 77, device="cuda")
+            x0 = synth.tokens_bf16(1, H, seed=seed * 100000 + 77, device="cuda")
         self.x0 = x0.contiguous()
         bf, f32 = torch.bfloat16, torch.float32
         self.out = []
         for li in range(layers):
-            self.out.append(dict(q=torch.empty((1, HIDDEN), dtype=bf, device=dev),
-                                 k=torch.empty((1, 640), dtype=f32, device=dev),
-                                 v=torch.empty((1, 640), dtype=f32, device=dev),
-                                 o=torch.empty((1, HIDDEN), dtype=bf, device=dev),
-                                 h=torch.empty((1, FFN), dtype=f32, device=dev),
-                                 y=torch.empty((1, HIDDEN), dtype=bf, device=dev)))
+            self.out.append(dict(q=torch.empty((1, H), dtype=bf, device=dev),
+                                 k=torch.empty((1, KV), dtype=f32, device=dev),
+                                 v=torch.empty((1, KV), dtype=f32, device=dev),
+                                 o=torch.empty((1, H), dtype=bf, device=dev),
+                                 h=torch.empty((1, F), dtype=f32, device=dev),
+                                 y=torch.empty((1, H), dtype=bf, device=dev)))
         torch.cuda.synchronize()
 
     def phases(self):
@@ -307,16 +322,82 @@ def _weight_sets(torch, bn, synth, N, K, count, seed):
     return sets
 
 
-def secondary_measurements(torch, bn, peaks, only=None):
+def _cpu_rate(fn, units, budget_s, threads):
+    """Units per second of fn(threads) over about budget_s (at least once)."""
+    fn(threads)
+    n, t0 = 0, time.perf_counter()
+    while n == 0 or time.perf_counter() - t0 < budget_s:
+        fn(threads)
+        n += 1
+    return units * n / (time.perf_counter() - t0)
+
+
+def oracle_secondary_baselines(budget_s=1.5):
+    """The CPU oracle on bounded samples of the secondary workloads (weights as
+    ternary codes drawn directly: the oracle's time does not depend on their
+    values), on all host cores and, for the decode shapes, on one."""
+    import oracle
+    from bitlinear_bitnet_linear_03_b300 import synth
+    allc = oracle.default_threads()
+    out = {}
+
+    def linear_case(key, N, K, M, rows, unit, single=True):
+        q = synth.ternary_codes(rows, K, seed=17)
+        Wq, ws = oracle.pack(q), synth.weight_scale(17)
+        qx, sx = oracle.quantize_act_bf16(synth.tokens_bf16(M, K, seed=18, outlier_frac=0.01))
+        run = lambda th: oracle.linear(Wq, ws, qx, sx, K, threads=th)
+        if unit == "GB/s":
+            units = rows * K / 4 + M * K + 4 * M * rows
+        else:
+            units = 2.0 * M * rows * K / 1e3  # TOPS after the 1e9 below
+        rec = {"value": round(_cpu_rate(run, units, budget_s, allc) / 1e9, 5), "unit": unit,
+               "cores": allc, "kind": "oracle",
+               "sample": f"{rows} of the {N} output rows, M = {M}" + (
+                   " (rate of the slice; the full shape scales with rows)" if rows < N else "")}
+        if single:
+            rec["single_thread"] = round(_cpu_rate(run, units, budget_s, 1) / 1e9, 5)
+        out[key] = rec
+
+    linear_case("gemv_2560x2560_M1", 2560, 2560, 1, 2560, "GB/s")
+    linear_case("100b_M1_K8192_N28672", 28672, 8192, 1, 2048, "GB/s")
+    linear_case("100b_M4_K8192_N28672", 28672, 8192, 4, 2048, "GB/s")
+    linear_case("prefill_M4096_K2560_N6912", 6912, 2560, 256, 6912, "TFLOP/s", single=False)
+    out["prefill_M4096_K2560_N6912"]["sample"] = ("256 of the 4096 tokens, all 6912 rows (rate of "
+                                                 "the slice)")
+    H, F = HIDDEN, FFN
+    ws = [(oracle.pack(synth.ternary_codes(n, k, seed=30 + i)), synth.weight_scale(30 + i))
+          for i, (n, k) in enumerate([(F, H), (F, H), (H, F)])]
+    g = synth.gain_random(H, 3)
+    for M, key, unit in ((1, "ffn_seq1", "GB/s"), (64, "ffn_seq4096", "TFLOP/s")):
+        x = synth.tokens_bf16(M, H, seed=31)
+        run = lambda th, x=x: oracle.ffn(x, g, EPS, ws[0][0], ws[0][1], ws[1][0], ws[1][1],
+                                         ws[2][0], ws[2][1], threads=th)
+        units = (3 * H * F / 4 + 2 * H + 4 * H) if unit == "GB/s" else 2.0 * M * 3 * H * F / 1e3
+        rec = {"value": round(_cpu_rate(run, units, budget_s, allc) / 1e9, 5), "unit": unit,
+               "cores": allc, "kind": "oracle",
+               "sample": "one token" if M == 1 else f"{M} of the 4096 tokens (rate of the slice)"}
+        if M == 1:
+            rec["single_thread"] = round(_cpu_rate(run, units, budget_s, 1) / 1e9, 5)
+        out[key] = rec
+    return out
+
+
+def secondary_measurements(torch, bn, peaks, only=None, cpu=True):
     """The other workloads, each timed with CUDA events after warm-up, weights
     rotated over enough distinct sets that every timed call streams from HBM
     (more than the 126 MB L2 between reuses), inputs resident:
       * single GEMV 2560x2560, batch 1 (80 weight sets);
-      * 100B-class shapes 8192->28672 and 28672->8192 at M = 1, 4, 16, 64;
-      * prefill M = 4096 on the 2B FFN shapes (tensor-core roofline against
-        the measured bf16 dense peak: sm_103a has no integer tensor-core MMA,
-        so the exact integer products run as bf16 MMAs);
-      * the fused FFN (hidden 2560, FFN 6912) at seq 1 and seq 4096."""
+      * 100B-class shapes 8192->28672 and 28672->8192: M = 1 and 4 through
+        bitnet_linear_bf16 (bf16 tokens with 1% outliers quantised in the
+        launch, static weights), M = 16 and 64 through bitnet_linear;
+      * prefill M = 4096 on the 2B FFN shapes, binary32 and bf16 outputs
+        (tensor-core roofline against the measured bf16 dense peak: sm_103a has
+        no integer tensor-core MMA, so the exact integer products run as bf16
+        MMAs);
+      * the fused FFN (hidden 2560, FFN 6912) at seq 1 and seq 4096;
+      * 8B-class shapes (hidden 4096, FFN 14336, K/V 1024): the 32-layer
+        decode step as one chain, and prefill M = 4096;
+    and, with cpu=True, the oracle on bounded samples of the same workloads."""
     from bitlinear_bitnet_linear_03_b300 import synth
     out = {}
     dev = torch.device("cuda")
@@ -336,10 +417,8 @@ def secondary_measurements(torch, bn, peaks, only=None):
         return only is None or only == case
 
     # single GEMV 2560x2560, M = 1
-    N = K = 2560
-    if not want("gemv2560"):
-        N = K = 0
-    if N:
+    if want("gemv2560"):
+        N = K = 2560
         sets = _weight_sets(torch, bn, synth, N, K, 80, 100)
         x = synth.tokens_bf16(1, K, seed=0, device="cuda")
         y = torch.empty((1, N), dtype=torch.float32, device=dev)
@@ -350,45 +429,56 @@ def secondary_measurements(torch, bn, peaks, only=None):
                                     "roofline": hbm_roof(byts / t / 1e9)}
         del sets
 
-    # 100B-class shapes (each timed as a CUDA graph of calls: the host's
-    # launch cost stays out of the device time)
+    # 100B-class shapes (each timed as a CUDA graph of calls)
     ms_100b = [m for m, c in ((1, "gemv100b"), (4, "gemv100b"), (16, "fused_small_m"),
                               (64, "fused_small_m")) if want(c)]
     for (N, K) in ([(28672, 8192), (8192, 28672)] if ms_100b else []):
         sets = _weight_sets(torch, bn, synth, N, K, 3, 200)
         for M in ms_100b:
             x = synth.tokens_bf16(M, K, seed=1, outlier_frac=0.01, device="cuda")
-            xq, sx = bn.bitnet_quantize_act(x)
             y = torch.empty((M, N), dtype=torch.float32, device=dev)
-            ws = torch.empty(max(bn.bitnet_linear_workspace(M, N, K), 16), dtype=torch.uint8,
-                             device=dev)
-            t = _time_calls(torch, lambda i: bn.bitnet_linear(sets[i % 3][0], sets[i % 3][1], xq, sx,
-                                                              y=y, ws=ws), 12, graph=True)
-            byts = N * K // 4 + M * K + 4 * M * N + 4 * M + 4
+            if M <= 4:
+                call = lambda i: bn.bitnet_linear_bf16(x, [(sets[i % 3][0], sets[i % 3][1], y)],
+                                                       weights_static=True)
+                byts = N * K // 4 + 2 * M * K + 4 * M * N + 4 * M + 4
+            else:
+                xq, sx = bn.bitnet_quantize_act(x)
+                ws = torch.empty(max(bn.bitnet_linear_workspace(M, N, K), 16), dtype=torch.uint8,
+                                 device=dev)
+                call = lambda i: bn.bitnet_linear(sets[i % 3][0], sets[i % 3][1], xq, sx, y=y, ws=ws)
+                byts = N * K // 4 + M * K + 4 * M * N + 4 * M + 4
+            t = _time_calls(torch, call, 12, graph=True)
             out[f"100b_M{M}_K{K}_N{N}"] = {
                 "us": round(t * 1e6, 1), "GBps": round(byts / t / 1e9, 1),
-                "tops": round(2 * M * N * K / t / 1e12, 2), "roofline": hbm_roof(byts / t / 1e9)}
-            del ws, y, xq, sx
+                "tops": round(2 * M * N * K / t / 1e12, 2), "roofline": hbm_roof(byts / t / 1e9),
+                "entry": "bitnet_linear_bf16 (static weights)" if M <= 4 else "bitnet_linear"}
         del sets
 
-    # prefill
-    for (N, K) in ([(6912, 2560), (2560, 6912)] if want("prefill") else []):
+    # prefill (2B FFN shapes; binary32 output, and bf16 output for K = 2560)
+    def prefill(N, K, key, sets_seed, out_bf16=False):
         M = 4096
-        sets = _weight_sets(torch, bn, synth, N, K, 4, 500)
+        sets = _weight_sets(torch, bn, synth, N, K, 4, sets_seed)
         x = synth.tokens_bf16(M, K, seed=600, device="cuda")
         xq, sx = bn.bitnet_quantize_act(x)
-        y = torch.empty((M, N), dtype=torch.float32, device=dev)
+        y = torch.empty((M, N), dtype=torch.bfloat16 if out_bf16 else torch.float32, device=dev)
         ws = torch.empty(max(bn.bitnet_linear_workspace(M, N, K), 16), dtype=torch.uint8,
                          device=dev)
-        t = _time_calls(torch, lambda i: bn.bitnet_linear(sets[i % 4][0], sets[i % 4][1], xq, sx,
-                                                          y=y, ws=ws), 20)
+        if out_bf16:
+            call = lambda i: bn.bitnet_linear(sets[i % 4][0], sets[i % 4][1], xq, sx, y=None,
+                                              y_bf16=y, ws=ws)
+        else:
+            call = lambda i: bn.bitnet_linear(sets[i % 4][0], sets[i % 4][1], xq, sx, y=y, ws=ws)
+        t = _time_calls(torch, call, 20)
         tops = 2 * M * N * K / t / 1e12
-        out[f"prefill_M{M}_K{K}_N{N}"] = {"ms": round(t * 1e3, 4), "tops": round(tops, 1),
-                                          "roofline": tc_roof(tops)}
-        del sets, xq, sx, y, ws
+        out[key] = {"ms": round(t * 1e3, 4), "tops": round(tops, 1), "roofline": tc_roof(tops)}
+
+    if want("prefill"):
+        prefill(6912, 2560, "prefill_M4096_K2560_N6912", 500)
+        prefill(2560, 6912, "prefill_M4096_K6912_N2560", 510)
+        prefill(6912, 2560, "prefill_M4096_K2560_N6912_bf16out", 520, out_bf16=True)
 
     # fused FFN
-    H, F = 2560, 6912
+    H, F = HIDDEN, FFN
     for M, nsets, reps in ([(1, 10, 200), (4096, 2, 6)] if want("ffn") else []):
         ffn_sets = []
         for r in range(nsets):
@@ -414,6 +504,24 @@ def secondary_measurements(torch, bn, peaks, only=None):
             tops = 2 * M * 3 * H * F / t / 1e12
             out[key] = {"ms": round(t * 1e3, 3), "tops": round(tops, 1), "roofline": tc_roof(tops)}
         del ffn_sets, ws, y
+
+    # 8B-class shapes
+    if want("8b"):
+        step = DecodeStep(DIMS_8B[3], dims=DIMS_8B)
+        step.build_chain()
+        g8 = capture(torch, step.step)
+        t = time_graph(torch, g8, 50, 5, lambda: None) / 50
+        byts = layer_bytes(DIMS_8B) * DIMS_8B[3]
+        out["decode_8b_32layers"] = {"us": round(t * 1e6, 1), "GBps": round(byts / t / 1e9, 1),
+                                     "roofline": hbm_roof(byts / t / 1e9),
+                                     "packed_weight_bytes": weight_bytes(DIMS_8B) * DIMS_8B[3]}
+        del step, g8
+        prefill(14336, 4096, "prefill_8b_M4096_K4096_N14336", 800)
+        prefill(4096, 14336, "prefill_8b_M4096_K14336_N4096", 810)
+    if cpu and only is None:
+        for k, rec in oracle_secondary_baselines().items():
+            if k in out:
+                out[k]["cpu_baseline"] = rec
     return out
 
 
@@ -510,36 +618,38 @@ class OracleSample:
     """One decode layer built on the host for the oracle (never touched by
     the GPU path): packed weights, norm gains, the layer input."""
 
-    def __init__(self, seed=0):
+    def __init__(self, seed=0, dims=DIMS_2B):
         import oracle
         from bitlinear_bitnet_linear_03_b300 import synth
         self.oracle = oracle
+        self.dims = dims
         self.W = {}
-        for j, (name, N, K, _) in enumerate(LAYER_SHAPES):
+        for j, (name, N, K, _) in enumerate(layer_shapes(dims)):
             Wq, s, _ = oracle.quantize_weights(synth.weights_f32(N, K, seed=7000 + j))
             self.W[name] = (Wq, s)
-        self.x = synth.tokens_bf16(1, HIDDEN, seed=7100)
-        self.g_attn = synth.gain_random(HIDDEN, 7200)
-        self.g_ffn = synth.gain_random(HIDDEN, 7201)
+        self.x = synth.tokens_bf16(1, dims[0], seed=7100)
+        self.g_attn = synth.gain_random(dims[0], 7200)
+        self.g_ffn = synth.gain_random(dims[0], 7201)
 
     def run(self, threads):
         """The layer's four phases, in order; returns its algorithmic bytes."""
         o, W = self.oracle, self.W
+        H, F = self.dims[0], self.dims[1]
         q, s = o.quantize_act_bf16(self.x)
-        Q = o.f32_to_bf16(o.linear(*W["q"], q, s, HIDDEN, threads=threads)[0])
-        o.linear(*W["k"], q, s, HIDDEN, threads=threads)
-        o.linear(*W["v"], q, s, HIDDEN, threads=threads)
+        Q = o.f32_to_bf16(o.linear(*W["q"], q, s, H, threads=threads)[0])
+        o.linear(*W["k"], q, s, H, threads=threads)
+        o.linear(*W["v"], q, s, H, threads=threads)
         n, _ = o.rmsnorm_bf16(Q, self.g_attn, EPS)
         q, s = o.quantize_act_f32(n)
-        O = o.f32_to_bf16(o.linear(*W["o"], q, s, HIDDEN, threads=threads)[0])
+        O = o.f32_to_bf16(o.linear(*W["o"], q, s, H, threads=threads)[0])
         n, _ = o.rmsnorm_bf16(O, self.g_ffn, EPS)
         q, s = o.quantize_act_f32(n)
-        u = o.linear(*W["up"], q, s, HIDDEN, threads=threads)[0]
-        v = o.linear(*W["gate"], q, s, HIDDEN, threads=threads)[0]
+        u = o.linear(*W["up"], q, s, H, threads=threads)[0]
+        v = o.linear(*W["gate"], q, s, H, threads=threads)[0]
         h = o.relu2_mul(u, v)
         q, s = o.quantize_act_f32(h)
-        o.f32_to_bf16(o.linear(*W["down"], q, s, FFN, threads=threads)[0])
-        return layer_bytes()
+        o.f32_to_bf16(o.linear(*W["down"], q, s, F, threads=threads)[0])
+        return layer_bytes(self.dims)
 
 
 def _oracle_rate(sample, threads, budget_s):

@@ -33,6 +33,17 @@ def test_decode_step_byte_counts():
     assert b.layer_bytes() == packed + scales + gains + inputs + outputs
 
 
+def test_decode_step_byte_counts_8b_class():
+    b = load_bench()
+    H, F, KV = 4096, 14336, 1024
+    packed = (2 * H * H + 2 * KV * H + 3 * F * H) // 4
+    assert b.weight_bytes(b.DIMS_8B) == packed == 54_525_952
+    scales, gains = 7 * 4, 2 * 4 * H
+    inputs = 3 * 2 * H + 4 * F
+    outputs = 3 * 2 * H + 2 * 4 * KV + 4 * F
+    assert b.layer_bytes(b.DIMS_8B) == packed + scales + gains + inputs + outputs
+
+
 def test_profiled_traffic_follows_the_kernel_source(tmp_path):
     b = load_bench()
     kernel = os.path.join(ROOT, "bitlinear_bitnet_linear_03_b300/csrc/decode_chain.cu")

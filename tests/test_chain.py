@@ -250,28 +250,29 @@ def oracle_decode_step(host_w, x0, g_attn, g_ffn, layers):
     return out
 
 
-def test_decode_step_30_layers_as_benchmarked_matches_oracle():
-    """The benchmark's 30-layer, 120-phase chain (same builder, shapes, links,
-    norms and gated pairs), with host-made ternary weights: every output of
-    every phase equals the oracle's, over two runs."""
+def check_decode_step(layers, dims, seed):
+    """The benchmark's decode-step chain (same builder, shapes, links, norms
+    and gated pairs) for `layers` layers of the model dims (hidden, FFN, K/V),
+    with host-made ternary weights: every output of every phase equals the
+    oracle's, over two runs."""
     import bench
-    layers = 30
+    H = dims[0]
     host_w, dev_w = [], []
     for li in range(layers):
         Lh, Ld = {}, {}
-        for j, (name, N, K, _) in enumerate(bench.LAYER_SHAPES):
-            q = synth.ternary_codes(N, K, seed=5000 + li * 16 + j)
-            Wq, ws = oracle.pack(q), synth.weight_scale(5000 + li * 16 + j)
+        for j, (name, N, K, _) in enumerate(bench.layer_shapes(dims)):
+            q = synth.ternary_codes(N, K, seed=seed + li * 16 + j)
+            Wq, ws = oracle.pack(q), synth.weight_scale(seed + li * 16 + j)
             Lh[name] = (Wq, ws)
             Ld[name] = on_dev(Wq, ws)
             del q
         host_w.append(Lh)
         dev_w.append(Ld)
-    x0 = synth.tokens_bf16(1, bench.HIDDEN, seed=77)
-    g_attn = [synth.gain_random(bench.HIDDEN, 300 + li) for li in range(layers)]
-    g_ffn = [synth.gain_random(bench.HIDDEN, 600 + li) for li in range(layers)]
+    x0 = synth.tokens_bf16(1, H, seed=seed + 77)
+    g_attn = [synth.gain_random(H, seed + 300 + li) for li in range(layers)]
+    g_ffn = [synth.gain_random(H, seed + 600 + li) for li in range(layers)]
     step = bench.DecodeStep(layers, weights=dev_w, x0=dev_bf16(x0),
-                            gains=([dev(g) for g in g_attn], [dev(g) for g in g_ffn]))
+                            gains=([dev(g) for g in g_attn], [dev(g) for g in g_ffn]), dims=dims)
     step.build_chain()
     want = oracle_decode_step(host_w, x0, g_attn, g_ffn, layers)
     for run in range(2):
@@ -285,3 +286,45 @@ def test_decode_step_30_layers_as_benchmarked_matches_oracle():
                 g = got[k]
                 g = bf16_host(g) if g.dtype == torch.bfloat16 else host(g)
                 assert_bits_equal(g, w, f"run {run} layer {li} {k}")
+
+
+def test_decode_step_30_layers_as_benchmarked_matches_oracle():
+    """The benchmarked 2B-class step: 30 layers, 120 phases."""
+    import bench
+    check_decode_step(30, bench.DIMS_2B, 5000)
+
+
+def test_decode_step_8b_class_layers_match_oracle():
+    """Two layers (8 phases) of the 8B-class step: hidden 4096, FFN 14336,
+    K/V 1024; the down phase reads K = 14336 inputs, more than a CTA's
+    registers hold at one token."""
+    import bench
+    check_decode_step(2, bench.DIMS_8B, 9000)
+
+
+@pytest.mark.parametrize("K", [2560, 16384])
+def test_chain_norm_rows_beyond_the_128_bit_window(K):
+    """Rows whose squares span more than 2^88 (values 2^50 and 2^-30) take the
+    five-limb exact sum; K = 16384 also exercises the inputs beyond those a
+    thread keeps in registers.  Every row must equal the oracle's subln."""
+    M = 2
+    x = synth.tokens_bf16(M, K, seed=97)
+    row = synth.bf16_bits_to_f32(x[1:2]).copy()
+    row[0, 11], row[0, K - 3] = 2.0 ** 50, 2.0 ** -30
+    x[1] = synth.f32_to_bf16_bits(row)[0]
+    g = synth.gain_random(K, 9)
+    W = packed(320, K, 970)
+    y = torch.empty((M, 320), dtype=torch.float32, device="cuda")
+    xq = torch.empty((M, K), dtype=torch.int8, device="cuda")
+    sx = torch.empty(M, dtype=torch.float32, device="cuda")
+    phases = [{"x": dev_bf16(x), "norm_gain": dev(g), "norm_eps": float(EPS),
+               "targets": [(*on_dev(*W), y)], "xq_out": xq, "x_scale_out": sx}]
+    chain = bn.bitnet_decode_chain_build(phases)
+
+    def check(run):
+        n, _ = oracle.rmsnorm_bf16(x, g, EPS)
+        q, s = oracle.quantize_act_f32(n)
+        assert_bits_equal(host(sx), s, f"run {run} scale")
+        assert_bits_equal(host(xq), q, f"run {run} codes")
+        assert_bits_equal(host(y), oracle.linear(W[0], W[1], q, s, K)[0], f"run {run} y")
+    run_twice(chain, [y, xq, sx], check)

@@ -208,8 +208,10 @@ def test_linear_100b_shapes_sampled(M, N, K):
     assert_bits_equal(y[:, rows], y_o, "y sampled bits")
 
 
-@pytest.mark.parametrize("N,K", [(6912, 2560), (2560, 6912)])
+@pytest.mark.parametrize("N,K", [(6912, 2560), (2560, 6912), (14336, 4096), (4096, 14336)])
 def test_linear_prefill_shapes_sampled(N, K):
+    """Prefill at seq 4096 on the 2B-class FFN shapes (hidden 2560, FFN 6912)
+    and the 8B-class ones (hidden 4096, FFN 14336)."""
     M = 4096
     W = synth.weights_f32(N, K, seed=21)
     x = synth.tokens_bf16(M, K, seed=22)
@@ -271,7 +273,9 @@ def test_linear_bf16_decode_layer_group(M):
 @pytest.mark.parametrize("M,K,Ns", [(1, 64, [1]), (1, 6912, [2560]), (2, 6912, [33, 2560]),
                                     (1, 28672, [8192]), (2, 28672, [100]), (4, 16384, [77]),
                                     (2, 32768, [9]), (3, 16384, [70]),
-                                    (3, 192, [5, 6, 7, 8, 9, 10, 11, 12]), (1, 65536, [40])])
+                                    (3, 192, [5, 6, 7, 8, 9, 10, 11, 12]), (1, 65536, [40]),
+                                    (1, 4096, [4096, 1024, 1024]), (1, 4096, [14336, 14336]),
+                                    (1, 14336, [4096])])
 def test_linear_bf16_shapes(M, K, Ns):
     check_linear_bf16(M, K, Ns, seed=M * 3 + K, weights_static=True)
 
