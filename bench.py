@@ -387,9 +387,10 @@ def secondary_measurements(torch, bn, peaks, only=None, cpu=True):
     rotated over enough distinct sets that every timed call streams from HBM
     (more than the 126 MB L2 between reuses), inputs resident:
       * single GEMV 2560x2560, batch 1 (80 weight sets);
-      * 100B-class shapes 8192->28672 and 28672->8192: M = 1 and 4 through
-        bitnet_linear_bf16 (bf16 tokens with 1% outliers quantised in the
-        launch, static weights), M = 16 and 64 through bitnet_linear;
+      * 100B-class shapes 8192->28672 and 28672->8192: M = 1 (and M = 4 at
+        K = 8192) through bitnet_linear_bf16 (bf16 tokens with 1% outliers
+        quantised in the launch, static weights), the rest through
+        bitnet_linear on int8 codes;
       * prefill M = 4096 on the 2B FFN shapes, binary32 and bf16 outputs
         (tensor-core roofline against the measured bf16 dense peak: sm_103a has
         no integer tensor-core MMA, so the exact integer products run as bf16
@@ -437,11 +438,13 @@ def secondary_measurements(torch, bn, peaks, only=None, cpu=True):
         for M in ms_100b:
             x = synth.tokens_bf16(M, K, seed=1, outlier_frac=0.01, device="cuda")
             y = torch.empty((M, N), dtype=torch.float32, device=dev)
-            if M <= 4:
+            if M == 1 or (M <= 4 and K <= 16384):  # bitnet_linear_bf16's K range
                 call = lambda i: bn.bitnet_linear_bf16(x, [(sets[i % 3][0], sets[i % 3][1], y)],
                                                        weights_static=True)
                 byts = N * K // 4 + 2 * M * K + 4 * M * N + 4 * M + 4
+                entry = "bitnet_linear_bf16 (static weights)"
             else:
+                entry = "bitnet_linear"
                 xq, sx = bn.bitnet_quantize_act(x)
                 ws = torch.empty(max(bn.bitnet_linear_workspace(M, N, K), 16), dtype=torch.uint8,
                                  device=dev)
@@ -451,7 +454,7 @@ def secondary_measurements(torch, bn, peaks, only=None, cpu=True):
             out[f"100b_M{M}_K{K}_N{N}"] = {
                 "us": round(t * 1e6, 1), "GBps": round(byts / t / 1e9, 1),
                 "tops": round(2 * M * N * K / t / 1e12, 2), "roofline": hbm_roof(byts / t / 1e9),
-                "entry": "bitnet_linear_bf16 (static weights)" if M <= 4 else "bitnet_linear"}
+                "entry": entry}
         del sets
 
     # prefill (2B FFN shapes; binary32 output, and bf16 output for K = 2560)

@@ -92,6 +92,17 @@ __device__ __forceinline__ int round_clip(float v, float lo, float hi) {
   return (int)r;
 }
 
+// round_clip(v, -128, 127) with full-rate float and integer operations only
+// (the float-to-integer conversion units run at a fraction of that rate):
+// clip (NaN to 0), then add 1.5 * 2^23.  The sum lies in [2^23, 2^24), where
+// the unit in the last place is 1, so the addition's own rounding (to nearest,
+// ties to even) leaves round-half-even of the clipped value in its low bits.
+__device__ __forceinline__ int quant_i8(float v) {
+  float c = fminf(fmaxf(v, -128.0f), 127.0f);
+  c = v == v ? c : 0.0f;
+  return __float_as_int(__fadd_rn(c, 12582912.0f)) - 0x4B400000;
+}
+
 // Per-token quantisation constants from the row's largest magnitude a:
 // a' = max(a, 1e-5), inv = 127 / a', scale = a' / 127 (binary32 divisions).
 struct ActScale {

@@ -115,13 +115,14 @@ struct CPhase {
   int pad;
 };
 
-// One bulk copy of the CTA's copy sequence: a stage of whole weight rows
-// (gated: the same rows of up, then of gate, each `bytes` long).
+// One entry of the CTA's copy sequence: a stage of whole weight rows, in one
+// or two bulk copies placed one after the other in the slot (rows of one
+// target, then of the next; gated: the same rows of up, then of gate).
 struct StageCopy {
   const uint8_t* src0;
-  const uint8_t* src1;
-  uint32_t bytes;
-  uint32_t pad;
+  const uint8_t* src1;  // second piece, or null
+  uint32_t bytes0;
+  uint32_t bytes1;
 };
 
 struct Args {
@@ -141,22 +142,30 @@ __device__ __forceinline__ void cta_rows(const CPhase& ph, int& r0, int& r1) {
   r1 = r0 + ph.rows_q + (b < ph.rows_rem ? 1 : 0);
 }
 
-// The CTA's stage sequence within one phase: f(target, first row, rows) in
-// order; false if f stopped it.
+// The CTA's stage sequence within one phase, in order: f(r, n, t, b) for the
+// stage of phase rows [r, r + n), whose rows [r, b) belong to target t and
+// [b, r + n) to target t + 1 (a stage holds rows of at most two targets, so
+// a CTA whose share crosses a target boundary still takes one stage); false
+// if f stopped it.  Gated: rows are row pairs, t = 0, b = r + n.
 template <typename F>
 __device__ __forceinline__ bool for_each_stage(const CPhase& ph, F&& f) {
   int r_begin, r_end;
   cta_rows(ph, r_begin, r_end);
   if (ph.gated) {
-    for (int r = r_begin; r < r_end; r += ph.rows_per_stage)
-      if (!f(0, r, min(ph.rows_per_stage, r_end - r))) return false;
+    for (int r = r_begin; r < r_end; r += ph.rows_per_stage) {
+      const int n = min(ph.rows_per_stage, r_end - r);
+      if (!f(r, n, 0, r + n)) return false;
+    }
     return true;
   }
-  for (int p = 0; p < ph.count; ++p) {
-    const int lo = max(r_begin, ph.t[p].row0);
-    const int hi = min(r_end, ph.t[p].row0 + ph.t[p].N);
-    for (int r = lo; r < hi; r += ph.rows_per_stage)
-      if (!f(p, r - ph.t[p].row0, min(ph.rows_per_stage, hi - r))) return false;
+  int t = 0;
+  for (int r = r_begin; r < r_end;) {
+    while (t + 1 < ph.count && ph.t[t + 1].row0 <= r) ++t;
+    const int b = t + 1 < ph.count ? ph.t[t + 1].row0 : r_end;
+    const int b2 = t + 2 < ph.count ? ph.t[t + 2].row0 : r_end;
+    const int n = min(min(ph.rows_per_stage, r_end - r), b2 - r);
+    if (!f(r, n, t, min(b, r + n))) return false;
+    r += n;
   }
   return true;
 }
@@ -332,6 +341,35 @@ __device__ __forceinline__ bool decode_group(const CPhase& ph, const Raw& r, uin
   return ok;
 }
 
+// Waits, within the same time limit as its caller (measured from t0), until
+// the last value of group g carries `tag`.  A poller whose groups are not all
+// ready waits here on one 4- or 8-byte word before loading every pending
+// group again, so that while an input is being produced the CTAs do not
+// stream all of it from L2 on every round trip.
+__device__ __forceinline__ void wait_word(const CPhase& ph, int m, int g, uint32_t tag,
+                                          long long t0, long long limit, const int* abort_flag) {
+  const int64_t o = (int64_t)m * ph.K + 8 * (int64_t)g + 7;
+  for (;;) {
+    bool ok;
+    if (ph.in_kind == kInLinkBf16) {
+      uint32_t w;
+      asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];"
+                   : "=r"(w)
+                   : "l"(static_cast<const uint32_t*>(ph.x) + o)
+                   : "memory");
+      ok = (w >> 16) == (tag & 0xffffu);
+    } else {
+      unsigned long long w;
+      asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];"
+                   : "=l"(w)
+                   : "l"(static_cast<const unsigned long long*>(ph.x) + o)
+                   : "memory");
+      ok = (uint32_t)(w >> 32) == tag;
+    }
+    if (ok || clock64() - t0 > limit || *(volatile const int*)abort_flag) return;
+  }
+}
+
 // Layout of the quantised input in shared memory: 64-weight chunk c takes 64
 // bytes, its 16-byte quarter s at slot (s + c/2) mod 4, so that the 8 lanes of
 // a quarter-warp reading quarter s of 8 consecutive chunks hit 8 distinct
@@ -396,7 +434,7 @@ __device__ __noinline__ void wide_quantize(const CPhase& ph, int m, int tid, uin
       for (int e = 0; e < 8; ++e) v[e] = __fmul_rn(__fmul_rn(v[e], r), gv[e]);
     }
     int q[8];
-    for (int e = 0; e < 8; ++e) q[e] = round_clip(__fmul_rn(v[e], inv), -128.f, 127.f);
+    for (int e = 0; e < 8; ++e) q[e] = quant_i8(__fmul_rn(v[e], inv));
     const uint2 packed = make_uint2(pack_i8x4(q[0], q[1], q[2], q[3]), pack_i8x4(q[4], q[5], q[6], q[7]));
     *reinterpret_cast<uint2*>(xs_row + xs_offset(g)) = packed;
     if (xq_out) *reinterpret_cast<uint2*>(xq_out + (int64_t)m * ph.K + 8 * g) = packed;
@@ -443,7 +481,6 @@ __global__ void __launch_bounds__(kChainThreads, 1) k_decode_chain(const __grid_
   __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
   __shared__ __align__(16) CPhase s_ph[2];
   __shared__ float s_max[MT][kChainWarps];
-  __shared__ int s_omax[MT][kChainWarps];
   __shared__ unsigned long long s_sum128[MT][kChainWarps][2];
   __shared__ uint32_t s_sumflag[MT][kChainWarps];
   __shared__ unsigned long long s_sum5[kChainWarps][5];  // the five-limb path
@@ -488,9 +525,9 @@ __global__ void __launch_bounds__(kChainThreads, 1) k_decode_chain(const __grid_
       const StageCopy c = a.copies[c_first + k];  // (s_copies is not yet complete)
       const uint32_t fb = smem_addr(&full_bar[k]);
       const uint32_t dst = ring + k * a.slot_bytes;
-      mbar_arrive_expect_tx(fb, c.src1 ? 2 * c.bytes : c.bytes);
-      bulk_copy_g2s(dst, c.src0, c.bytes, fb);
-      if (c.src1) bulk_copy_g2s(dst + c.bytes, c.src1, c.bytes, fb);
+      mbar_arrive_expect_tx(fb, c.bytes0 + c.bytes1);
+      bulk_copy_g2s(dst, c.src0, c.bytes0, fb);
+      if (c.src1) bulk_copy_g2s(dst + c.bytes0, c.src1, c.bytes1, fb);
       s_issued[k] = 1;
     }
   }
@@ -580,6 +617,8 @@ __global__ void __launch_bounds__(kChainThreads, 1) k_decode_chain(const __grid_
           // Spin without sleeping: a sleeping poller can wake microseconds
           // after its input has landed (measured on B300).
           while (pend) {
+            wait_word(ph, m, tid + (c + __ffs(pend) - 1) * kChainThreads, in_tag, t0, a.wait,
+                      &s_abort);
 #pragma unroll
             for (int i = 0; i < kPipe; ++i)
               if ((pend >> i) & 1u) issue_group(ph, m, tid + (c + i) * kChainThreads, raw[i]);
@@ -609,58 +648,83 @@ __global__ void __launch_bounds__(kChainThreads, 1) k_decode_chain(const __grid_
       }
       float r = 0.0f;
       if (norm) {
-        // ss = exact sum of the squares: in 128 bits anchored below the
-        // largest square (exact_sumsq.cuh), or, for a row whose squares span
-        // more than that window (or a wide row), the five-limb exact sum.
-        // the largest square is the square of the largest |x|
-        float xmax = 0.0f;
+        // ss = exact sum of the squares (exact_sumsq.cuh): each warp sums its
+        // squares t = x * x (binary32) in 128 bits anchored 88 bits below its
+        // largest square; after one barrier every warp brings the eight warp
+        // sums to the common anchor and adds them (hardware warp reductions,
+        // every lane gets the total).  A row whose squares span more than that
+        // window (a nonzero square falls below the anchor), or a wide row,
+        // takes the five-limb sum.  The largest square comes from the bit
+        // patterns (t >= 0; a NaN square, of either sign, or +Inf has an
+        // exponent field of 255 or more).
+        uint32_t tb = 0u;
 #pragma unroll
         for (int i = 0; i < kHold; ++i)
           if (tid + i * kChainThreads < ngroups)
 #pragma unroll
-            for (int e = 0; e < 8; ++e) xmax = fmaxf(xmax, fabsf(hv[i][e]));
-        const int omax = __reduce_max_sync(0xffffffffu, sumsq::term_offset(__fmul_rn(xmax, xmax)));
-        if (lane == 0) s_omax[m][warp] = omax;
-        if (chain_sync_or(*(volatile int*)&s_abort)) {
-          stop = true;
-          continue;
-        }
-        int o_all = s_omax[m][0];
-#pragma unroll
-        for (int w = 1; w < kChainWarps; ++w) o_all = max(o_all, s_omax[m][w]);
-        const int anchor = o_all - 88 > 0 ? o_all - 88 : 0;
+            for (int e = 0; e < 8; ++e) tb = max(tb, __float_as_uint(__fmul_rn(hv[i][e], hv[i][e])));
+        const uint32_t tb_w = __reduce_max_sync(0xffffffffu, tb);
         sumsq::Acc128 acc;
         sumsq::zero(acc);
+        int aw = 0;
+        if ((tb_w >> 23) >= 255u) {  // warp-uniform: ss is NaN or +Inf, no sum needed
 #pragma unroll
-        for (int i = 0; i < kHold; ++i)
-          if (tid + i * kChainThreads < ngroups)
+          for (int i = 0; i < kHold; ++i)
+            if (tid + i * kChainThreads < ngroups)
 #pragma unroll
-            for (int e = 0; e < 8; ++e) sumsq::add_term(acc, __fmul_rn(hv[i][e], hv[i][e]), anchor);
-        sumsq::warp_reduce(acc, 16);
+              for (int e = 0; e < 8; ++e) {
+                const float t = __fmul_rn(hv[i][e], hv[i][e]);
+                acc.nan_ |= t != t;
+                acc.inf_ |= t == __uint_as_float(0x7f800000u);
+              }
+        } else {
+          aw = max(max((int)(tb_w >> 23), 1) - 1 - 88, 0);
+          sumsq::Lean ln = {0ull, 0ull, 0ull, 0u};
+#pragma unroll
+          for (int i = 0; i < kHold; ++i)
+            if (tid + i * kChainThreads < ngroups)
+#pragma unroll
+              for (int e = 0; e < 8; ++e) sumsq::lean_add(ln, __fmul_rn(hv[i][e], hv[i][e]), aw);
+          sumsq::lean_total(ln, acc.lo, acc.hi);
+          acc.lost = ln.lost;
+          sumsq::warp_sum128(acc.lo, acc.hi);
+        }
+        const uint32_t fl_w =
+            __reduce_or_sync(0xffffffffu, acc.nan_ | (acc.inf_ << 1) | (acc.lost << 2));
         if (lane == 0) {
           s_sum128[m][warp][0] = acc.lo;
           s_sum128[m][warp][1] = acc.hi;
-          s_sumflag[m][warp] = acc.nan_ | (acc.inf_ << 1) | (acc.lost << 2);
+          s_sumflag[m][warp] = fl_w | ((uint32_t)aw << 8);
         }
         if (chain_sync_or(*(volatile int*)&s_abort)) {
           stop = true;
           continue;
         }
-        sumsq::Acc128 tot;
-        sumsq::zero(tot);
+        uint64_t lo = 0ull, hi = 0ull;
+        uint32_t fl = 0u;
+        int aj = 0;
         if (lane < kChainWarps) {
-          tot.lo = s_sum128[m][lane][0];
-          tot.hi = s_sum128[m][lane][1];
-          tot.nan_ = s_sumflag[m][lane] & 1u;
-          tot.inf_ = (s_sumflag[m][lane] >> 1) & 1u;
-          tot.lost = s_sumflag[m][lane] >> 2;
+          lo = s_sum128[m][lane][0];
+          hi = s_sum128[m][lane][1];
+          fl = s_sumflag[m][lane] & 0xffu;
+          aj = (int)(s_sumflag[m][lane] >> 8);
         }
-        sumsq::warp_reduce(tot, kChainWarps / 2);
+        const int anchor = __reduce_max_sync(0xffffffffu, aj);
+        if (sumsq::shift_right128(lo, hi, anchor - aj)) fl |= 4u;
+        sumsq::warp_sum128(lo, hi);
+        fl = __reduce_or_sync(0xffffffffu, fl);
         float ss;
-        if (__shfl_sync(0xffffffffu, tot.lost, 0) || wide)  // uniform over the CTA
+        if ((fl & 4u) || wide) {  // uniform over the CTA
           ss = exact_row_sumsq(ph, m, tid, in_tag, a.wait, &s_abort, &s_sum5[0][0], &s_sumflag5[0]);
-        else
-          ss = __shfl_sync(0xffffffffu, sumsq::round_to_f32(tot, anchor), 0);
+        } else {
+          sumsq::Acc128 tot;
+          tot.lo = lo;
+          tot.hi = hi;
+          tot.nan_ = fl & 1u;
+          tot.inf_ = (fl >> 1) & 1u;
+          tot.lost = 0u;
+          ss = sumsq::round_to_f32(tot, anchor);
+        }
         r = sumsq::rms_scale(ss, K, ph.eps);
         // n = (x * r) * g, then its largest magnitude
 #pragma unroll
@@ -673,7 +737,8 @@ __global__ void __launch_bounds__(kChainThreads, 1) k_decode_chain(const __grid_
             }
         if (wide) mx = fmaxf(mx, wide_absmax(ph, m, tid, in_tag, a.wait, &s_abort, r, &bad));
       }
-      mx = warp_max_f32(mx);
+      // mx >= 0 and never NaN, so its bit pattern orders like its value
+      mx = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(mx)));
       if (lane == 0) s_max[m][warp] = mx;
       if (chain_sync_or(*(volatile int*)&s_abort)) {
         stop = true;
@@ -691,7 +756,7 @@ __global__ void __launch_bounds__(kChainThreads, 1) k_decode_chain(const __grid_
         if (g >= ngroups) break;
         int q[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) q[e] = round_clip(__fmul_rn(hv[i][e], sc.inv), -128.f, 127.f);
+        for (int e = 0; e < 8; ++e) q[e] = quant_i8(__fmul_rn(hv[i][e], sc.inv));
         const uint2 packed = make_uint2(pack_i8x4(q[0], q[1], q[2], q[3]),
                                         pack_i8x4(q[4], q[5], q[6], q[7]));
         *reinterpret_cast<uint2*>(xs_row + xs_offset(g)) = packed;
@@ -719,7 +784,7 @@ __global__ void __launch_bounds__(kChainThreads, 1) k_decode_chain(const __grid_
     int lsum[MT];
 #pragma unroll
     for (int m = 0; m < MT; ++m) {
-      lsum[m] = 0;
+      int ls[4] = {0, 0, 0, 0};  // four independent sums (short dependency chains)
 #pragma unroll
       for (int j = 0; j < J; ++j) {
 #pragma unroll
@@ -729,18 +794,19 @@ __global__ void __launch_bounds__(kChainThreads, 1) k_decode_chain(const __grid_
             v = *reinterpret_cast<const uint4*>(xs + (int64_t)m * a.xs_stride +
                                                 xs_chunk_offset(k_lo + lane + 32 * j, s));
           xr[m][j][s] = v;
-          lsum[m] = dp4a_ss(v.x, 0x01010101u, lsum[m]);
-          lsum[m] = dp4a_ss(v.y, 0x01010101u, lsum[m]);
-          lsum[m] = dp4a_ss(v.z, 0x01010101u, lsum[m]);
-          lsum[m] = dp4a_ss(v.w, 0x01010101u, lsum[m]);
+          ls[0] = dp4a_ss(v.x, 0x01010101u, ls[0]);
+          ls[1] = dp4a_ss(v.y, 0x01010101u, ls[1]);
+          ls[2] = dp4a_ss(v.z, 0x01010101u, ls[2]);
+          ls[3] = dp4a_ss(v.w, 0x01010101u, ls[3]);
         }
       }
+      lsum[m] = (ls[0] + ls[1]) + (ls[2] + ls[3]);
     }
     const int64_t rb = K >> 2;
     const uint32_t out_tag = tag0 + (uint32_t)p;
 
     // ---- the stages of this phase
-    for_each_stage(ph, [&](int t, int row0, int nrows) {
+    for_each_stage(ph, [&](int r_st, int nrows, int t_st, int b_st) {
       const int slot = c_slot;
       const uint32_t parity = c_parity;
       const int k = c_k++;
@@ -775,9 +841,9 @@ __global__ void __launch_bounds__(kChainThreads, 1) k_decode_chain(const __grid_
             if (free_slot) {
               const uint32_t fb = smem_addr(&full_bar[slot]);
               const uint32_t dst = ring + slot * a.slot_bytes;
-              mbar_arrive_expect_tx(fb, next.src1 ? 2 * next.bytes : next.bytes);
-              bulk_copy_g2s(dst, next.src0, next.bytes, fb);
-              if (next.src1) bulk_copy_g2s(dst + next.bytes, next.src1, next.bytes, fb);
+              mbar_arrive_expect_tx(fb, next.bytes0 + next.bytes1);
+              bulk_copy_g2s(dst, next.src0, next.bytes0, fb);
+              if (next.src1) bulk_copy_g2s(dst + next.bytes0, next.src1, next.bytes1, fb);
               ++s_issued[slot];
             }
           }
@@ -846,7 +912,10 @@ __global__ void __launch_bounds__(kChainThreads, 1) k_decode_chain(const __grid_
           }
         }
       }
-      const float ws_t = __shfl_sync(0xffffffffu, ws_lane, t);
+      // the row this lane reports (q = lane / MT) and its target
+      const int row_l = wr + (lane / MT) * nwr;
+      const int t_l = r_st + row_l < b_st ? t_st : t_st + 1;
+      const float ws_t = __shfl_sync(0xffffffffu, ws_lane, ph.gated ? 0 : min(t_l, kTargets - 1));
       const float ws_g = __shfl_sync(0xffffffffu, ws_lane, 1);
       {
         const int q = lane / MT, m = lane % MT;
@@ -884,11 +953,11 @@ __global__ void __launch_bounds__(kChainThreads, 1) k_decode_chain(const __grid_
           }
           if (last) {
             if (!ph.gated) {
-              const CTarget& T = ph.t[t];
-              const int64_t o = (int64_t)m * T.N + row0 + row;
+              const CTarget& T = ph.t[t_l];
+              const int64_t o = (int64_t)m * T.N + (r_st + row - T.row0);
               store_out(T, o, __fmul_rn(__int2float_rn(tot), __fmul_rn(xsc, ws_t)), tot, out_tag);
             } else {
-              const int64_t o = (int64_t)m * ph.t[0].N + row0 + row;
+              const int64_t o = (int64_t)m * ph.t[0].N + r_st + row;
               const float u = __fmul_rn(__int2float_rn(tot), __fmul_rn(xsc, ws_t));
               const float v = __fmul_rn(__int2float_rn(totv), __fmul_rn(xsc, ws_g));
               const float tr = v > 0.0f ? v : 0.0f;
@@ -1012,19 +1081,28 @@ void list_copies(const bitnet_decode_phase* ph, int np, ChainLayout* L) {
         for (int64_t r = r0; r < r1; r += R) {
           const int64_t n = std::min(R, r1 - r);
           L->copies.push_back({p.targets[0].Wq + r * rb, p.targets[1].Wq + r * rb,
-                               (uint32_t)(n * rb), 0u});
+                               (uint32_t)(n * rb), (uint32_t)(n * rb)});
         }
         continue;
       }
-      int64_t row0 = 0;
-      for (int t = 0; t < p.count; ++t) {
-        const int64_t N = p.targets[t].N;
-        const int64_t lo = std::max(r0, row0), hi = std::min(r1, row0 + N);
-        for (int64_t r = lo; r < hi; r += R) {
-          const int64_t n = std::min(R, hi - r);
-          L->copies.push_back({p.targets[t].Wq + (r - row0) * rb, nullptr, (uint32_t)(n * rb), 0u});
+      // the kernel's for_each_stage: at most two targets' rows per stage
+      std::vector<int64_t> start((size_t)p.count + 1, 0);
+      for (int t = 0; t < p.count; ++t) start[(size_t)t + 1] = start[(size_t)t] + p.targets[t].N;
+      int t = 0;
+      for (int64_t r = r0; r < r1;) {
+        while (t + 1 < p.count && start[(size_t)t + 1] <= r) ++t;
+        const int64_t b = t + 1 < p.count ? start[(size_t)t + 1] : r1;
+        const int64_t b2 = t + 2 < p.count ? start[(size_t)t + 2] : r1;
+        const int64_t n = std::min(std::min(R, r1 - r), b2 - r);
+        const int64_t split = std::min(b, r + n);
+        StageCopy sc = {p.targets[t].Wq + (r - start[(size_t)t]) * rb, nullptr,
+                        (uint32_t)((split - r) * rb), 0u};
+        if (split < r + n) {
+          sc.src1 = p.targets[t + 1].Wq;
+          sc.bytes1 = (uint32_t)((r + n - split) * rb);
         }
-        row0 += N;
+        L->copies.push_back(sc);
+        r += n;
       }
     }
   }

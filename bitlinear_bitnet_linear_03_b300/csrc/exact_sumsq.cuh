@@ -138,7 +138,10 @@ __device__ __forceinline__ float round_to_f32(const Acc& s) {
 // 2^(anchor - 149), anchor = max(o_max - 88, 0): every term is then below
 // 2^112 and the sum of up to 2^16 of them below 2^128.  A term with nonzero
 // bits below the anchor (a square 2^88 times smaller than the largest) sets
-// `lost`; the caller then redoes the row with the five-limb sum above.
+// `lost`; the caller then redoes the row with the five-limb sum above.  (A
+// caller may anchor each warp's terms at that warp's own largest square and
+// bring the warp sums to the common anchor with shift_right128, again
+// flagging any nonzero bit that falls below it.)
 struct Acc128 {
   uint64_t lo, hi;
   uint32_t nan_, inf_, lost;
@@ -187,6 +190,91 @@ __device__ __forceinline__ void warp_reduce(Acc128& a, int first) {
     a.inf_ |= __shfl_xor_sync(0xffffffffu, a.inf_, off);
     a.lost |= __shfl_xor_sync(0xffffffffu, a.lost, off);
   }
+}
+
+// ---- Lean accumulation of finite squares for one lane.  A term t = m *
+// 2^(o - 149) with sh = o - anchor in [0, 88] is m * 2^sh in units of
+// 2^(anchor - 149); with sh = 32 q + s it goes into accumulator q as
+// m * 2^s, one 32 x 32 -> 64-bit multiply-add (2^s for the two other
+// accumulators is 0: a 32-bit shift of 1 by 32 or more, or by a negative
+// count read as unsigned, gives 0).  Each accumulator receives terms below
+// 2^56, so 32 terms stay below 2^61.  A nonzero term with sh < 0 (2^88 below
+// the anchor's square) is not added and sets `lost`; the caller then takes
+// the five-limb sum.
+struct Lean {
+  uint64_t a0, a1, a2;
+  uint32_t lost;
+};
+
+__device__ __forceinline__ uint32_t shl1(int n) {
+  uint32_t r;
+  asm("shl.b32 %0, 1, %1;" : "=r"(r) : "r"(n));
+  return r;
+}
+__device__ __forceinline__ uint64_t mad_wide(uint32_t a, uint32_t b, uint64_t c) {
+  uint64_t r;
+  asm("mad.wide.u32 %0, %1, %2, %3;" : "=l"(r) : "r"(a), "r"(b), "l"(c));
+  return r;
+}
+
+// t: a finite square (>= 0).
+__device__ __forceinline__ void lean_add(Lean& s, float t, int anchor) {
+  const uint32_t u = __float_as_uint(t);
+  const int o = max((int)(u >> 23), 1) - 1;  // subnormal or zero: o = 0
+  const uint32_t m = u - ((uint32_t)o << 23);  // significand with its leading bit
+  const int sh = o - anchor;
+  s.a0 = mad_wide(m, shl1(sh), s.a0);
+  s.a1 = mad_wide(m, shl1(sh - 32), s.a1);
+  s.a2 = mad_wide(m, shl1(sh - 64), s.a2);
+  s.lost |= (uint32_t)(sh < 0 && m != 0u);
+}
+
+// a0 + a1 * 2^32 + a2 * 2^64 as (lo, hi).
+__device__ __forceinline__ void lean_total(const Lean& s, uint64_t& lo, uint64_t& hi) {
+  const unsigned __int128 v =
+      (unsigned __int128)s.a0 + ((unsigned __int128)s.a1 << 32) + ((unsigned __int128)s.a2 << 64);
+  lo = (uint64_t)v;
+  hi = (uint64_t)(v >> 64);
+}
+
+// The 128-bit values (lo, hi) of the 32 lanes summed exactly, every lane
+// receiving the sum, when each value is below 2^122 (so the sum is below
+// 2^127).  Each value is cut into five 26-bit limbs; one hardware warp
+// reduction per limb adds 32 of them below 2^31, with no carry lost, and the
+// five limb sums are put back together in 128 bits.
+__device__ __forceinline__ void warp_sum128(uint64_t& lo, uint64_t& hi) {
+  constexpr uint32_t M = (1u << 26) - 1u;
+  const uint32_t l0 = __reduce_add_sync(0xffffffffu, (uint32_t)lo & M);
+  const uint32_t l1 = __reduce_add_sync(0xffffffffu, (uint32_t)(lo >> 26) & M);
+  const uint32_t l2 = __reduce_add_sync(0xffffffffu, (uint32_t)((lo >> 52) | (hi << 12)) & M);
+  const uint32_t l3 = __reduce_add_sync(0xffffffffu, (uint32_t)(hi >> 14) & M);
+  const uint32_t l4 = __reduce_add_sync(0xffffffffu, (uint32_t)(hi >> 40));
+  const unsigned __int128 S = (unsigned __int128)l0 + ((unsigned __int128)l1 << 26) +
+                              ((unsigned __int128)l2 << 52) + ((unsigned __int128)l3 << 78) +
+                              ((unsigned __int128)l4 << 104);
+  lo = (uint64_t)S;
+  hi = (uint64_t)(S >> 64);
+}
+
+// (lo, hi) >>= d (d >= 0); true if a nonzero bit was shifted out.
+__device__ __forceinline__ bool shift_right128(uint64_t& lo, uint64_t& hi, int d) {
+  if (d <= 0) return false;
+  if (d >= 128) {
+    const bool lost = (lo | hi) != 0ull;
+    lo = hi = 0ull;
+    return lost;
+  }
+  if (d >= 64) {
+    const int e = d - 64;
+    const bool lost = lo != 0ull || (e > 0 && (hi & ((1ull << e) - 1ull)) != 0ull);
+    lo = hi >> e;
+    hi = 0ull;
+    return lost;
+  }
+  const bool lost = (lo & ((1ull << d) - 1ull)) != 0ull;
+  lo = (lo >> d) | (hi << (64 - d));
+  hi >>= d;
+  return lost;
 }
 
 // Nearest binary32 (ties to even) to S * 2^(anchor - 149), S = hi * 2^64 + lo.

@@ -116,6 +116,34 @@ def test_chain_f32_link_and_mixed_outputs():
     run_twice(chain, [ya, yb32, yb16, yc, xq1, xs1], check)
 
 
+@pytest.mark.parametrize("M,K", [(1, 192), (3, 192), (1, 6912)])
+def test_chain_stages_that_cross_target_boundaries(M, K):
+    """Eight targets of very different sizes in one phase: with a few rows per
+    CTA, many CTAs' stages hold rows of two targets (one stage per CTA where
+    its share crosses one boundary, split where it would cross two); every
+    output form of every target equals the oracle's."""
+    Ns = [3, 1, 7, 2, 40, 5, 1, 300]
+    x = synth.tokens_bf16(M, K, seed=90 + M, outlier_frac=0.01)
+    W = [packed(N, K, seed=900 + i) for i, N in enumerate(Ns)]
+    ys = [torch.empty((M, N), dtype=torch.float32, device="cuda") for N in Ns]
+    accs = [torch.empty((M, N), dtype=torch.int32, device="cuda") for N in Ns]
+    yb = torch.empty((M, 300), dtype=torch.bfloat16, device="cuda")
+    targets = [(*on_dev(*W[i]), ys[i], accs[i]) + ((yb,) if i == 7 else ())
+               for i in range(len(Ns))]
+    phases = [{"x": dev_bf16(x), "targets": targets}]
+    chain = bn.bitnet_decode_chain_build(phases)
+
+    def check(run):
+        qx, sx = oracle.quantize_act_bf16(x)
+        for i in range(len(Ns)):
+            y_o, acc_o = oracle.linear(W[i][0], W[i][1], qx, sx, K)
+            assert_bits_equal(host(accs[i]), acc_o, f"run {run} target {i} acc")
+            assert_bits_equal(host(ys[i]), y_o, f"run {run} target {i} y")
+            if i == 7:
+                assert_bits_equal(bf16_host(yb), oracle.f32_to_bf16(y_o), f"run {run} bf16")
+    run_twice(chain, ys + accs + [yb], check)
+
+
 # ---------------------------------------------------------------- norm + gated pair
 @pytest.mark.parametrize("M,seed", [(1, 0), (1, 1), (2, 2), (4, 3)])
 def test_chain_ffn_block_matches_oracle_ffn(M, seed):
@@ -179,6 +207,65 @@ def test_chain_norm_on_a_linked_input_and_special_rows():
             q, s = oracle.quantize_act_f32(n)
             assert_bits_equal(host(out), oracle.linear(W1[0], W1[1], q, s, H)[0], what)
     run_twice(chain, [y0, y1, y2], check)
+
+
+def special_norm_rows(H):
+    """Rows for the chain's exact sum of squares: a NaN, an infinity, a value
+    whose square overflows binary32, subnormal bf16 values, and warps of very
+    different magnitudes (each warp anchors its own partial sum)."""
+    rows = synth.bf16_bits_to_f32(synth.tokens_bf16(6, H, seed=95)).copy()
+    rows[0, 17] = np.nan
+    rows[1, 900] = np.inf
+    rows[2, 5] = 3.0e20
+    rows[3, :] = 0.0
+    rows[3, ::7] = 2.0 ** -130
+    rows[4, : H // 2] *= 2.0 ** 20          # first half large, second half small
+    rows[4, H // 2:] *= 2.0 ** -12
+    rows[5, ::2] = 0.0
+    return synth.f32_to_bf16_bits(rows)
+
+
+@pytest.mark.parametrize("row", range(6))
+def test_chain_norm_special_rows_one_token(row):
+    H = 2560
+    x = special_norm_rows(H)[row:row + 1]
+    g = synth.gain_random(H, 11)
+    W = packed(320, H, 950)
+    y = torch.empty((1, 320), dtype=torch.float32, device="cuda")
+    xq = torch.empty((1, H), dtype=torch.int8, device="cuda")
+    sx = torch.empty(1, dtype=torch.float32, device="cuda")
+    chain = bn.bitnet_decode_chain_build(
+        [{"x": dev_bf16(x), "norm_gain": dev(g), "norm_eps": float(EPS),
+          "targets": [(*on_dev(*W), y)], "xq_out": xq, "x_scale_out": sx}])
+
+    def check(run):
+        n, _ = oracle.rmsnorm_bf16(x, g, EPS)
+        q, s = oracle.quantize_act_f32(n)
+        assert_bits_equal(host(sx), s, f"run {run} scale")
+        assert_bits_equal(host(xq), q, f"run {run} codes")
+        assert_bits_equal(host(y), oracle.linear(W[0], W[1], q, s, H)[0], f"run {run} y")
+    run_twice(chain, [y, xq, sx], check)
+
+
+def test_chain_norm_special_rows_four_tokens():
+    H = 2560
+    x = special_norm_rows(H)[[0, 2, 3, 4]]
+    g = synth.gain_random(H, 12)
+    W = packed(320, H, 951)
+    y = torch.empty((4, 320), dtype=torch.float32, device="cuda")
+    xq = torch.empty((4, H), dtype=torch.int8, device="cuda")
+    sx = torch.empty(4, dtype=torch.float32, device="cuda")
+    chain = bn.bitnet_decode_chain_build(
+        [{"x": dev_bf16(x), "norm_gain": dev(g), "norm_eps": float(EPS),
+          "targets": [(*on_dev(*W), y)], "xq_out": xq, "x_scale_out": sx}])
+
+    def check(run):
+        n, _ = oracle.rmsnorm_bf16(x, g, EPS)
+        q, s = oracle.quantize_act_f32(n)
+        assert_bits_equal(host(sx), s, f"run {run} scale")
+        assert_bits_equal(host(xq), q, f"run {run} codes")
+        assert_bits_equal(host(y), oracle.linear(W[0], W[1], q, s, H)[0], f"run {run} y")
+    run_twice(chain, [y, xq, sx], check)
 
 
 def test_chain_links_through_phases_most_ctas_skip():
