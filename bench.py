@@ -24,6 +24,7 @@ prints one JSON line.
 import argparse
 import hashlib
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -69,7 +70,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--case", default=None,
-                    choices=["prefill", "gemv100b", "fused_small_m", "ffn", "gemv2560", "8b"],
+                    choices=["prefill", "gemv100b", "fused_small_m", "ffn", "gemv2560", "8b",
+                             "lut"],
                     help="run only this secondary measurement and print it (for profiling "
                          "one kernel under ncu)")
     return ap.parse_args()
@@ -455,6 +457,54 @@ def secondary_measurements(torch, bn, peaks, only=None, cpu=True):
                 "us": round(t * 1e6, 1), "GBps": round(byts / t / 1e9, 1),
                 "tops": round(2 * M * N * K / t / 1e12, 2), "roofline": hbm_roof(byts / t / 1e9),
                 "entry": entry}
+        del sets
+
+    # 100B-class layers through the decode chain: 16 independent phases per
+    # launch (each its own bf16 input and output), cycling over 4 weight sets
+    # (235 MB, so every phase streams its weights from HBM); the weight stream
+    # runs on across phase boundaries instead of ramping up per launch.
+    for (N, K, M) in ([(28672, 8192, 1), (8192, 28672, 1), (28672, 8192, 4)]
+                      if want("gemv100b") else []):
+        nset, nph = 4, 16
+        sets = _weight_sets(torch, bn, synth, N, K, nset, 300)
+        xs = [synth.tokens_bf16(M, K, seed=310 + i, outlier_frac=0.01, device="cuda")
+              for i in range(nph)]
+        ys = [torch.empty((M, N), dtype=torch.float32, device=dev) for _ in range(nph)]
+        chain = bn.bitnet_decode_chain_build(
+            [{"x": xs[i], "targets": [(sets[i % nset][0], sets[i % nset][1], ys[i])]}
+             for i in range(nph)])
+        g = capture(torch, lambda: bn.bitnet_decode_chain_run(chain))
+        t = time_graph(torch, g, 20, 3, lambda: None) / 20 / nph
+        byts = N * K // 4 + 2 * M * K + 4 * M * N + 4 + 4
+        out[f"100b_chain_M{M}_K{K}_N{N}"] = {
+            "us_per_layer": round(t * 1e6, 2), "GBps": round(byts / t / 1e9, 1),
+            "roofline": hbm_roof(byts / t / 1e9),
+            "entry": f"bitnet_decode_chain_run, {nph} independent phases per launch"}
+        del chain, g, sets, xs, ys
+
+    # Lookup-table ablation: one token, the table-lookup inner product, the
+    # dp4a control on the same kernel skeleton, and the production decode path
+    # (bitnet_linear, int8 input), each timed as a graph of calls over weight
+    # sets that exceed L2.
+    for (N, K) in ([(2560, 2560), (6912, 2560), (2560, 6912), (28672, 8192)]
+                   if want("lut") else []):
+        nset = max(2, int(math.ceil(3 * 126e6 / (N * K / 4))))
+        sets = _weight_sets(torch, bn, synth, N, K, nset, 900)
+        xq, sx = bn.bitnet_quantize_act(synth.tokens_bf16(1, K, seed=901, device="cuda"))
+        y = torch.empty((1, N), dtype=torch.float32, device=dev)
+        byts = N * K // 4 + K + 4 * N + 8
+        rec = {}
+        for name, call in (
+                ("lut", lambda i: bn.bitnet_linear_lut(sets[i % nset][0], sets[i % nset][1], xq,
+                                                       sx, variant=0, y=y)),
+                ("dp4a_same_skeleton", lambda i: bn.bitnet_linear_lut(
+                    sets[i % nset][0], sets[i % nset][1], xq, sx, variant=1, y=y)),
+                ("production", lambda i: bn.bitnet_linear(sets[i % nset][0], sets[i % nset][1],
+                                                          xq, sx, y=y))):
+            t = _time_calls(torch, call, 4 * nset, graph=True)
+            rec[name] = {"us": round(t * 1e6, 2), "GBps": round(byts / t / 1e9, 1),
+                         "roofline": hbm_roof(byts / t / 1e9)}
+        out[f"lut_ablation_M1_K{K}_N{N}"] = rec
         del sets
 
     # prefill (2B FFN shapes; binary32 output, and bf16 output for K = 2560)

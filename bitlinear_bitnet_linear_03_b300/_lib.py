@@ -37,6 +37,7 @@ SIGNATURES = {
     "bitnet_linear_workspace": (_SZ, [_I64, _I64, _I64]),
     "bitnet_linear": (_INT, [_P, _P, _P, _P, _I64, _I64, _I64, _P, _P, _P, _P, _SZ, _P]),
     "bitnet_linear_bf16": (_INT, [_P, _I64, _I64, _P, _INT, _P, _P, ctypes.c_uint, _P]),
+    "bitnet_linear_lut": (_INT, [_P, _P, _P, _P, _I64, _I64, _P, _P, _INT, _P]),
     "bitnet_decode_chain_bytes": (_SZ, [_P, _INT, _I64]),
     "bitnet_decode_chain_build": (_INT, [_P, _INT, _I64, _P, _SZ, _P]),
     "bitnet_decode_chain_run": (_INT, [_P, _P]),
@@ -208,6 +209,22 @@ def bitnet_linear(Wq, w_scale, xq, x_scale, K=None, y=None, acc_out=None, ws=Non
         _ptr(y, torch.float32, "y"), _ptr(y_bf16, torch.bfloat16, "y_bf16"),
         _ptr(acc_out, torch.int32, "acc_out"), _ptr(ws, name="ws"), nb, _stream(stream)))
     return y if y is not None else y_bf16
+
+
+def bitnet_linear_lut(Wq, w_scale, xq, x_scale, variant=0, y=None, acc_out=None, stream=None):
+    """One-token BitLinear with the table-lookup (variant 0) or dp4a (variant
+    1) inner product: packed Wq [N, K/4] x int8 xq [1, K] (or [K]) -> y
+    float32 [1, N]."""
+    N = Wq.shape[0]
+    K = xq.shape[-1]
+    if y is None:
+        y = torch.empty((1, N), dtype=torch.float32, device=xq.device)
+    _check("bitnet_linear_lut", lib().bitnet_linear_lut(
+        _ptr(Wq, torch.uint8, "Wq"), _ptr(w_scale, torch.float32, "w_scale"),
+        _ptr(xq, torch.int8, "xq"), _ptr(x_scale, torch.float32, "x_scale"), N, K,
+        _ptr(y, torch.float32, "y"), _ptr(acc_out, torch.int32, "acc_out"), int(variant),
+        _stream(stream)))
+    return y
 
 
 BITNET_WEIGHTS_STATIC = 1

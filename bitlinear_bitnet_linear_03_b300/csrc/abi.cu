@@ -204,6 +204,21 @@ bitnet_status bitnet_linear(const uint8_t* Wq, const float* w_scale, const int8_
                                 (cudaStream_t)stream));
 }
 
+bitnet_status bitnet_linear_lut(const uint8_t* Wq, const float* w_scale, const int8_t* xq,
+                                const float* x_scale, int64_t N, int64_t K, float* y,
+                                int32_t* acc_out, int variant, void* stream) {
+  static_assert(BITNET_LUT_MAX_K == bitnet::kLutMaxK, "header and kernel agree on the K limit");
+  if (!Wq || !w_scale || !xq || !x_scale || !y) return BITNET_ERR_NULL;
+  if (N < 1 || N >= ((int64_t)1 << 31) || K < 64 || K % 64 != 0 || K > BITNET_LUT_MAX_K ||
+      (variant != 0 && variant != 1))
+    return BITNET_ERR_SHAPE;
+  if (!aligned16(Wq) || !aligned16(xq)) return BITNET_ERR_ALIGN;
+  bitnet_status st = check_device();
+  if (st != BITNET_OK) return st;
+  return cuda_status(bitnet::launch_gemv_lut(Wq, w_scale, xq, x_scale, N, K, y, acc_out, variant,
+                                             (cudaStream_t)stream));
+}
+
 bitnet_status bitnet_linear_bf16(const uint16_t* x, int64_t M, int64_t K,
                                  const bitnet_linear_target* targets, int count, int8_t* xq_out,
                                  float* x_scale_out, unsigned flags, void* stream) {

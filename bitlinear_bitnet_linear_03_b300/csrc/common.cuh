@@ -171,6 +171,13 @@ cudaError_t launch_rmsnorm_quant(const uint16_t* x, const float* g, float eps, i
 cudaError_t launch_relu2_quant(const float* u, const float* v, int64_t M, int64_t F, float* h,
                                int8_t* hq, float* h_scale, cudaStream_t s);
 
+// One-token BitLinear with a table-lookup (variant 0) or dp4a (variant 1)
+// inner product on one kernel skeleton (gemv_lut.cu); K <= kLutMaxK.
+constexpr int64_t kLutMaxK = 12288;
+cudaError_t launch_gemv_lut(const uint8_t* Wq, const float* w_scale, const int8_t* xq,
+                            const float* x_scale, int64_t N, int64_t K, float* y,
+                            int32_t* acc_out, int variant, cudaStream_t s);
+
 // Decode BitLinear (M <= 4) on CUDA cores: one launch for up to
 // kDecodeMaxTargets weight matrices sharing the same input, which is either
 // int8 (xq, x_scale) or bf16 (quantised per token inside the kernel, bit for

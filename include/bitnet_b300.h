@@ -165,6 +165,26 @@ bitnet_status bitnet_linear(const uint8_t* Wq, const float* w_scale,
                             int32_t* acc_out, void* ws, size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
+ * One-token BitLinear with a lookup-table inner product: the ablation of the
+ * dp4a kernels against the table-lookup kernel family ([P3] §3.2: I2_S vs
+ * TL1/TL2; [P4] T-MAC section: lookups instead of multiplications).  Same
+ * result as bitnet_linear at M = 1, bit for bit:
+ *   acc[n] = sum_k q[n,k] * xq[k],  y[n] = (float)acc[n] * (x_scale[0] * w_scale[0]).
+ * variant 0: for each pair of activations that shares a nibble of the packed
+ *   weights (two 2-bit codes), a 16-entry table of c0*x0 + c1*x1 is built in
+ *   shared memory; each byte of weights costs two table reads.
+ * variant 1: the masked-field dp4a inner product on the same kernel skeleton
+ *   (the control of the ablation).
+ * Wq [N, K/4] packed, w_scale [1], xq [K] int8, x_scale [1]; y [N] float
+ * (required), acc_out [N] int32 (optional).  K % 64 == 0, 64 <= K <=
+ * BITNET_LUT_MAX_K; 1 <= N < 2^31; variant 0 or 1 (else BITNET_ERR_SHAPE).
+ * No workspace. */
+#define BITNET_LUT_MAX_K 12288
+bitnet_status bitnet_linear_lut(const uint8_t* Wq, const float* w_scale, const int8_t* xq,
+                                const float* x_scale, int64_t N, int64_t K, float* y,
+                                int32_t* acc_out, int variant, void* stream);
+
+/* ------------------------------------------------------------------------
  * Decode BitLinear from bf16 activations ([P1] W1.58A8; [P3] §3.1).
  * For up to BITNET_MAX_TARGETS weight matrices that share the same input
  * (e.g. the Q, K, V, up and gate projections of one token), in one launch:

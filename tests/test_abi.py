@@ -124,6 +124,17 @@ def test_argument_errors_are_reported_before_launch():
     assert L.bitnet_device_error(None, None) == 1
 
 
+def test_lut_entry_checks_its_arguments():
+    L = bn.lib()
+    args = [p(FAKE)] * 4
+    assert L.bitnet_linear_lut(*args, 64, 64, None, None, 0, None) == 1          # y
+    assert L.bitnet_linear_lut(*args, 64, 12288 + 64, p(FAKE), None, 0, None) == 2  # K too large
+    assert L.bitnet_linear_lut(*args, 64, 100, p(FAKE), None, 0, None) == 2        # K % 64
+    assert L.bitnet_linear_lut(*args, 0, 64, p(FAKE), None, 1, None) == 2          # N
+    assert L.bitnet_linear_lut(*args, 64, 64, p(FAKE), None, 2, None) == 2         # variant
+    assert L.bitnet_linear_lut(p(MIS), *args[1:], 64, 64, p(FAKE), None, 0, None) == 3
+
+
 class FakeMem:
     """Distinct fake device addresses (never dereferenced: every check below
     fails, or passes, on the host before anything touches a device)."""
