@@ -4,6 +4,7 @@
 // beyond a per-device capability cache.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <vector>
 
 #include "../../include/bitnet_b300.h"
@@ -80,6 +81,10 @@ cudaError_t run_linear(const uint8_t* Wq, const float* w_scale, const int8_t* xq
 }
 
 // FFN workspace sections, each 256-byte aligned.
+// Prefill sizes run the up and gate products as one gated GEMM whose
+// epilogue forms h (no binary32 u or v written unless asked for).
+bool ffn_gated(int64_t M, int64_t H) { return M > 256 && !bitnet::decode_supported(M, H); }
+
 struct FfnLayout {
   size_t xq, sx, u, v, hq, sh, lin, total;
 };
@@ -98,6 +103,7 @@ FfnLayout ffn_layout(int64_t M, int64_t H, int64_t F) {
   L.hq = take((size_t)(M * F));
   L.sh = take((size_t)M * 4);
   size_t a = linear_ws(M, F, H), b = linear_ws(M, H, F);
+  if (ffn_gated(M, H)) a = std::max(a, bitnet::gemm_tc_gated_workspace(M, F, H));
   L.lin = take(a > b ? a : b);
   L.total = off;
   return L;
@@ -351,6 +357,16 @@ bitnet_status bitnet_ffn(const uint16_t* x, const float* g, float eps, const uin
                                        {Wgate, s_gate, F, v, nullptr, nullptr}};
     e = bitnet::launch_decode(t, 2, xq, sx, nullptr, M, H, nullptr, nullptr, false,
                               bitnet::wait_limit_cycles(), s);
+  } else if (ffn_gated(M, H)) {
+    // one GEMM for up and gate; h goes to d.h or to u's workspace section
+    float* h = d.h ? d.h : reinterpret_cast<float*>(w + L.u);
+    if (e == cudaSuccess)
+      e = bitnet::launch_gemm_tc_gated(Wup, s_up, Wgate, s_gate, xq, sx, M, F, H, d.u, d.v, h, lin,
+                                       bitnet::wait_limit_cycles(), s);
+    if (e == cudaSuccess) e = bitnet::launch_quantize_act_f32(h, M, F, hq, sh, s);
+    if (e == cudaSuccess)
+      e = run_linear(Wdown, s_down, hq, sh, M, H, F, y, nullptr, d.acc_down, lin, s);
+    return cuda_status(e);
   } else {
     if (e == cudaSuccess) e = run_linear(Wup, s_up, xq, sx, M, F, H, u, nullptr, nullptr, lin, s);
     if (e == cudaSuccess)

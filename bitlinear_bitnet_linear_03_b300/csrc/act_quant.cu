@@ -88,40 +88,137 @@ k_act_quant_f32(const float4* __restrict__ x, int K, uint32_t* __restrict__ xq,
   }
 }
 
-// subln RMSNorm + quantisation, one warp per token.
+// subln RMSNorm + quantisation, one CTA of kNormWarps warps per token.
 //   ss = the exact sum of the binary32 squares x_k * x_k, rounded once to
-//        binary32 (exact_sumsq.cuh: order-free, integer arithmetic);
+//        binary32 (exact_sumsq.cuh: order-free, integer arithmetic): each
+//        warp sums its squares in 128 bits anchored 88 bits below its own
+//        largest square, the warp sums are brought to the common anchor and
+//        added; a row whose squares span more than that window takes the
+//        five-limb sum (exact_row_sumsq5);
 //   r  = 1 / sqrt(ss / H + eps), four binary32 operations;
 //   n  = (x * r) * g, then the per-token quantisation of n.
 constexpr int kNormWarps = 8;
-__global__ void __launch_bounds__(kNormWarps * 32)
-k_rmsnorm_quant(const uint16_t* __restrict__ x, const float* __restrict__ g, float eps, int M,
-                int H, int8_t* __restrict__ xq, float* __restrict__ x_scale) {
-  const int lane = threadIdx.x & 31;
-  const int row = blockIdx.x * kNormWarps + (threadIdx.x >> 5);
-  if (row >= M) return;
-  const uint16_t* xr = x + (int64_t)row * H;
+constexpr int kNormThreads = kNormWarps * 32;
+
+// The five-limb exact sum of the row's squares (every thread of the CTA
+// calls it; it synchronises them).
+__device__ __noinline__ float exact_row_sumsq5(const uint16_t* xr, int H,
+                                              unsigned long long (*s5)[5], uint32_t* s5f) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   sumsq::Acc acc;
   sumsq::zero(acc);
-  for (int k = lane; k < H; k += 32) {
+  for (int k = threadIdx.x; k < H; k += kNormThreads) {
     const float f = bf16_bits_to_float(xr[k]);
     sumsq::add_term(acc, __fmul_rn(f, f));
   }
   sumsq::warp_reduce(acc, 16);
-  const float r = sumsq::rms_scale(sumsq::round_to_f32(acc), H, eps);
+  if (lane == 0) {
+    for (int j = 0; j < 5; ++j) s5[warp][j] = acc.w[j];
+    s5f[warp] = acc.nan_ | (acc.inf_ << 1);
+  }
+  __syncthreads();
+  sumsq::Acc tot;
+  sumsq::zero(tot);
+  if (lane < kNormWarps) {
+    for (int j = 0; j < 5; ++j) tot.w[j] = s5[lane][j];
+    tot.nan_ = s5f[lane] & 1u;
+    tot.inf_ = s5f[lane] >> 1;
+  }
+  sumsq::warp_reduce(tot, kNormWarps / 2);
+  return __shfl_sync(0xffffffffu, sumsq::round_to_f32(tot), 0);
+}
+
+__global__ void __launch_bounds__(kNormThreads)
+k_rmsnorm_quant(const uint16_t* __restrict__ x, const float* __restrict__ g, float eps, int M,
+                int H, int8_t* __restrict__ xq, float* __restrict__ x_scale) {
+  __shared__ unsigned long long s_part[kNormWarps][2];
+  __shared__ uint32_t s_meta[kNormWarps];
+  __shared__ float s_max[kNormWarps];
+  __shared__ unsigned long long s5[kNormWarps][5];
+  __shared__ uint32_t s5f[kNormWarps];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row = blockIdx.x;
+  const uint16_t* xr = x + (int64_t)row * H;
+
+  // this warp's largest square (bit patterns: t >= 0; NaN or +Inf >= 255 << 23)
+  uint32_t tb = 0u;
+  for (int k = threadIdx.x; k < H; k += kNormThreads) {
+    const float f = bf16_bits_to_float(xr[k]);
+    tb = max(tb, __float_as_uint(__fmul_rn(f, f)));
+  }
+  tb = __reduce_max_sync(0xffffffffu, tb);
+  uint64_t lo = 0ull, hi = 0ull;
+  uint32_t fl = 0u;
+  int aw = 0;
+  if ((tb >> 23) >= 255u) {  // warp-uniform: ss is NaN or +Inf
+    for (int k = threadIdx.x; k < H; k += kNormThreads) {
+      const float f = bf16_bits_to_float(xr[k]);
+      const float t = __fmul_rn(f, f);
+      fl |= (t != t ? 1u : 0u) | (t == __uint_as_float(0x7f800000u) ? 2u : 0u);
+    }
+  } else {
+    aw = max(max((int)(tb >> 23), 1) - 1 - 88, 0);
+    sumsq::Lean ln = {0ull, 0ull, 0ull, 0u};
+    for (int k = threadIdx.x; k < H; k += kNormThreads) {
+      const float f = bf16_bits_to_float(xr[k]);
+      sumsq::lean_add(ln, __fmul_rn(f, f), aw);
+    }
+    sumsq::lean_total(ln, lo, hi);
+    sumsq::warp_sum128(lo, hi);
+    fl = ln.lost << 2;
+  }
+  fl = __reduce_or_sync(0xffffffffu, fl);
+  if (lane == 0) {
+    s_part[warp][0] = lo;
+    s_part[warp][1] = hi;
+    s_meta[warp] = fl | ((uint32_t)aw << 8);
+  }
+  __syncthreads();
+  lo = hi = 0ull;
+  fl = 0u;
+  int aj = 0;
+  if (lane < kNormWarps) {
+    lo = s_part[lane][0];
+    hi = s_part[lane][1];
+    fl = s_meta[lane] & 0xffu;
+    aj = (int)(s_meta[lane] >> 8);
+  }
+  const int anchor = __reduce_max_sync(0xffffffffu, aj);
+  if (sumsq::shift_right128(lo, hi, anchor - aj)) fl |= 4u;
+  sumsq::warp_sum128(lo, hi);
+  fl = __reduce_or_sync(0xffffffffu, fl);
+  float ss;
+  if (fl & 4u) {  // uniform over the CTA
+    ss = exact_row_sumsq5(xr, H, s5, s5f);
+  } else {
+    sumsq::Acc128 tot;
+    tot.lo = lo;
+    tot.hi = hi;
+    tot.nan_ = fl & 1u;
+    tot.inf_ = (fl >> 1) & 1u;
+    tot.lost = 0u;
+    ss = sumsq::round_to_f32(tot, anchor);
+  }
+  const float r = sumsq::rms_scale(ss, H, eps);
 
   float a = 0.0f;
-  for (int k = lane; k < H; k += 32) {
-    float n = __fmul_rn(__fmul_rn(bf16_bits_to_float(xr[k]), r), g[k]);
+  for (int k = threadIdx.x; k < H; k += kNormThreads) {
+    const float n = __fmul_rn(__fmul_rn(bf16_bits_to_float(xr[k]), r), g[k]);
     a = fmaxf(a, fabsf(n));
   }
-  a = warp_max_f32(a);
+  // a >= 0 and never NaN: its bit pattern orders like its value
+  a = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(a)));
+  if (lane == 0) s_max[warp] = a;
+  __syncthreads();
+  a = s_max[0];
+#pragma unroll
+  for (int w = 1; w < kNormWarps; ++w) a = fmaxf(a, s_max[w]);
   const ActScale sc = act_scale_from_absmax(a);
-  if (lane == 0) x_scale[row] = sc.scale;
+  if (threadIdx.x == 0) x_scale[row] = sc.scale;
   int8_t* qr = xq + (int64_t)row * H;
-  for (int k = lane; k < H; k += 32) {
-    float n = __fmul_rn(__fmul_rn(bf16_bits_to_float(xr[k]), r), g[k]);
-    qr[k] = (int8_t)round_clip(__fmul_rn(n, sc.inv), -128.f, 127.f);
+  for (int k = threadIdx.x; k < H; k += kNormThreads) {
+    const float n = __fmul_rn(__fmul_rn(bf16_bits_to_float(xr[k]), r), g[k]);
+    qr[k] = (int8_t)quant_i8(__fmul_rn(n, sc.inv));
   }
 }
 
@@ -176,8 +273,7 @@ cudaError_t launch_quantize_act_f32(const float* x, int64_t M, int64_t K, int8_t
 
 cudaError_t launch_rmsnorm_quant(const uint16_t* x, const float* g, float eps, int64_t M,
                                  int64_t H, int8_t* xq, float* x_scale, cudaStream_t s) {
-  const unsigned grid = (unsigned)((M + kNormWarps - 1) / kNormWarps);
-  k_rmsnorm_quant<<<grid, kNormWarps * 32, 0, s>>>(x, g, eps, (int)M, (int)H, xq, x_scale);
+  k_rmsnorm_quant<<<(unsigned)M, kNormThreads, 0, s>>>(x, g, eps, (int)M, (int)H, xq, x_scale);
   return cudaGetLastError();
 }
 

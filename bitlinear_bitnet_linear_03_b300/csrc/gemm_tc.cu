@@ -62,11 +62,14 @@ constexpr int kRingBytes = 192 * 1024;
 // the codes are expanded into one of two bf16 B buffers after the ring, so
 // the TMA ring is deep (6 stages) while the expanded tiles are only double
 // buffered.
-template <int BN, bool FUSED = false>
+// GATED (unfused only): a stage holds the A tile and two B tiles (up and
+// gate rows of the same output columns).
+template <int BN, bool FUSED = false, bool GATED = false>
 struct Tile {
   static constexpr int kBTileBytes = BN * kRowBytes;
   static constexpr int kPackedBytes = FUSED ? BN * 16 : 0;
-  static constexpr int kStageBytes = kATileBytes + (FUSED ? kPackedBytes : kBTileBytes);
+  static constexpr int kStageBytes =
+      kATileBytes + (FUSED ? kPackedBytes : (GATED ? 2 : 1) * kBTileBytes);
   static constexpr int kBBufBytes = FUSED ? 2 * kBTileBytes : 0;
   static constexpr int kStages = (kRingBytes - kBBufBytes) / kStageBytes;  // 4 or 6; 6 fused
   static constexpr int kSmemBytes = kStages * kStageBytes + kBBufBytes + 1024;  // + alignment
@@ -104,10 +107,15 @@ struct Args {
   int* tile_cnt;
   const float* x_scale;
   const float* w_scale;
-  float* y;          // binary32 output, or null
+  float* y;          // binary32 output, or null (gated: u, optional)
   uint16_t* y_bf16;  // bf16 output, or null
   int32_t* acc_out;
   long long wait;    // bound of every wait but the final drains, in clocks
+  // gated (the FFN's up and gate products on one A tile): the gate's scale,
+  // its optional binary32 output v, and h = relu(v)^2 * u (required)
+  const float* w_scale2;
+  float* y2;
+  float* h;
 };
 
 // Work item -> tile and K-stage range.
@@ -314,14 +322,37 @@ __device__ __forceinline__ void expand_b_tile(uint32_t packed, uint32_t btile, i
   }
 }
 
-template <int KIND, int BN, bool FUSED>
+// h = relu(v)^2 * u with t = max(v, 0) taken as v > 0 ? v : 0 (binary32).
+__device__ __forceinline__ float relu2_mul(float u, float v) {
+  const float t = v > 0.0f ? v : 0.0f;
+  return __fmul_rn(__fmul_rn(t, t), u);
+}
+
+// 32 consecutive binary32 values of one row; vec4: in range and 16-byte
+// aligned.
+__device__ __forceinline__ void store_f32_32(float* row, int nb, const float (&v)[32], bool vec4,
+                                             int N) {
+  if (vec4) {
+#pragma unroll
+    for (int j = 0; j < 32; j += 4)
+      *reinterpret_cast<float4*>(row + nb + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (nb + j < N) row[nb + j] = v[j];
+  }
+}
+
+template <int KIND, int BN, bool FUSED, bool GATED = false>
 __global__ void __launch_bounds__(FUSED ? kThreadsFused : kThreads, 1)
 k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
-          const __grid_constant__ Args a) {
+          const __grid_constant__ CUtensorMap mapB2, const __grid_constant__ Args a) {
+  static_assert(!(GATED && FUSED), "the gated form reads expanded bf16 weights");
+  static_assert(!GATED || 4 * BN <= (int)kTmemCols, "two accumulators per tile, double buffered");
   extern __shared__ uint8_t smem_raw[];
-  constexpr int kStages = Tile<BN, FUSED>::kStages;
-  constexpr int kStageBytes = Tile<BN, FUSED>::kStageBytes;
-  constexpr int kBTileBytesT = Tile<BN, FUSED>::kBTileBytes;
+  constexpr int kStages = Tile<BN, FUSED, GATED>::kStages;
+  constexpr int kStageBytes = Tile<BN, FUSED, GATED>::kStageBytes;
+  constexpr int kBTileBytesT = Tile<BN, FUSED, GATED>::kBTileBytes;
   __shared__ __align__(8) uint64_t full_bar[kStages];
   __shared__ __align__(8) uint64_t empty_bar[kStages];
   __shared__ __align__(8) uint64_t bready_bar[2];  // fused: B buffer expanded
@@ -398,6 +429,8 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUte
             mbar_expect_tx(fb, kStageBytes);
             tma_load_2d(sa, &mapA, ks * Kind<KIND>::kKStage, m0, fb);
             tma_load_2d(sa + kATileBytes, &mapB, ks * Kind<KIND>::kKStage, n0, fb);
+            if (GATED)
+              tma_load_2d(sa + kATileBytes + kBTileBytesT, &mapB2, ks * Kind<KIND>::kKStage, n0, fb);
           }
           issued = it + 1;
         }
@@ -425,7 +458,8 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUte
           break;
         }
         tc_fence_after();
-        const uint32_t d = tmem + (uint32_t)(ab * BN);
+        // gated: the tile's u accumulator, its v accumulator BN columns on
+        const uint32_t d = tmem + (uint32_t)(ab * (GATED ? 2 : 1) * BN);
         for (int ks = ks0; ks < ks1; ++ks, ++it) {
           const int s = it % kStages, b = it & 1;
           // fused: the expanded B buffer (and the A tile of the stage, whose
@@ -446,6 +480,10 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUte
             const uint64_t ad = sw128_desc(sa + kk * kMmaKBytes);
             const uint64_t bd = sw128_desc(sb + kk * kMmaKBytes);
             tc_mma<KIND, BN>(d, ad, bd, (ks != ks0 || kk != 0) ? 1u : 0u);
+            if (GATED) {
+              const uint64_t bd2 = sw128_desc(sb + kBTileBytesT + kk * kMmaKBytes);
+              tc_mma<KIND, BN>(d + (uint32_t)BN, ad, bd2, (ks != ks0 || kk != 0) ? 1u : 0u);
+            }
           }
           // frees the stage, and (fused) the expanded B buffer, when these
           // MMAs finish: one commit per stage
@@ -497,6 +535,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUte
     const int quarter = warp & 3;  // TMEM lanes this warp may access
     const int row = quarter * 32 + lane;
     const float ws = *a.w_scale;
+    const float ws2 = GATED ? *a.w_scale2 : 0.0f;
     int lt = 0;
     for (int item = blockIdx.x; item < items; item += gridDim.x, ++lt) {
       int t, ks0, ks1;
@@ -520,7 +559,34 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUte
       float* wrow = a.acc_ws + (int64_t)m * a.N;
       const bool vec = (a.N & 3) == 0;
       const bool vec8 = (a.N & 7) == 0;
-      for (int cb = 0; cb < BN; cb += 32) {
+      if (GATED) {
+        // u = f32(acc_u) * (sx * s_up), v = f32(acc_v) * (sx * s_gate),
+        // h = relu(v)^2 * u; the accumulators are exact integers (adding +0
+        // turns a -0 sum into the +0 of the integer's conversion)
+        const float cv = mrow ? __fmul_rn(a.x_scale[m], ws2) : 0.0f;
+        float* vrow = a.y2 ? a.y2 + (int64_t)m * a.N : nullptr;
+        float* hrow = a.h + (int64_t)m * a.N;
+        for (int cb = 0; cb < BN; cb += 32) {
+          uint32_t ru[32], rv[32];
+          const uint32_t ta = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(ab * 2 * BN + cb);
+          tmem_ld32(ta, ru);
+          tmem_ld32(ta + (uint32_t)BN, rv);
+          if (!mrow) continue;
+          const int nb = n0 + cb;
+          float uf[32], vf[32], hf[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            uf[j] = __fmul_rn(__fadd_rn(__uint_as_float(ru[j]), 0.0f), c);
+            vf[j] = __fmul_rn(__fadd_rn(__uint_as_float(rv[j]), 0.0f), cv);
+            hf[j] = relu2_mul(uf[j], vf[j]);
+          }
+          const bool v4 = vec && nb + 32 <= a.N;
+          if (yrow) store_f32_32(yrow, nb, uf, v4, a.N);
+          if (vrow) store_f32_32(vrow, nb, vf, v4, a.N);
+          store_f32_32(hrow, nb, hf, v4, a.N);
+        }
+      }
+      for (int cb = 0; cb < BN && !GATED; cb += 32) {
         uint32_t r[32];
         tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(ab * BN + cb), r);
         if (!mrow) continue;
@@ -767,6 +833,9 @@ cudaError_t launch_kind(const uint8_t* Wq, const float* w_scale, const int8_t* x
   a.y_bf16 = y_bf16;
   a.acc_out = acc_out;
   a.wait = wait;
+  a.w_scale2 = nullptr;
+  a.y2 = nullptr;
+  a.h = nullptr;
   static bool configured[64] = {};
   int dev = 0;
   e = cudaGetDevice(&dev);
@@ -782,10 +851,93 @@ cudaError_t launch_kind(const uint8_t* Wq, const float* w_scale, const int8_t* x
   const int ctas = items < 148 ? items : 148;
   return launch_pdl(k_gemm_tc<KIND, BN, FUSED>, dim3(ctas),
                     dim3(FUSED ? kThreadsFused : kThreads), (size_t)Tile<BN, FUSED>::kSmemBytes, s,
-                    mapA, mapB, a);
+                    mapA, mapB, mapB, a);
+}
+
+// The FFN's up and gate products in one GEMM (M > 256): both weight matrices
+// are expanded once per call into bf16 copies, the activations into bf16 A,
+// and k_gemm_tc<.., GATED> runs 128 x 128 output tiles with two accumulators
+// each (u and v on the same A tile), writing h = relu(v)^2 * u and, when
+// asked, u and v.  Workspace: [B up][B gate][A], each 1 KB aligned.
+size_t gated_ws(int64_t M, int64_t N, int64_t K) {
+  return 2 * round1k((size_t)(N * K * 2)) + round1k((size_t)(M * K * 2));
+}
+
+cudaError_t launch_gated_t(const uint8_t* Wu, const float* su, const uint8_t* Wg, const float* sg,
+                           const int8_t* xq, const float* x_scale, int64_t M, int64_t N,
+                           int64_t K, float* u, float* v, float* h, void* ws, long long wait,
+                           cudaStream_t s) {
+  constexpr int BN = 128;
+  cudaError_t e = get_encode();
+  if (e != cudaSuccess) return e;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  void* Bu = w;
+  void* Bg = w + round1k((size_t)(N * K * 2));
+  void* A = w + 2 * round1k((size_t)(N * K * 2));
+  const int64_t nblk = N * K / 64, nx = M * K / 16;
+  for (int pass = 0; pass < 2; ++pass) {
+    const int64_t n_x = pass == 0 ? nx : 0;
+    int64_t grid = (8 * nblk + n_x + 255) / 256;
+    if (grid > 148 * 16) grid = 148 * 16;
+    k_prepass<<<(unsigned)grid, 256, 0, s>>>(
+        reinterpret_cast<const uint4*>(pass == 0 ? Wu : Wg), nblk,
+        reinterpret_cast<uint4*>(pass == 0 ? Bu : Bg), reinterpret_cast<const uint4*>(xq), n_x,
+        reinterpret_cast<uint4*>(A), nullptr, 0);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  CUtensorMap mapA, mapB, mapB2;
+  e = encode_operand(&mapA, A, M, K, Kind<kKind>::kElem, kBM);
+  if (e == cudaSuccess) e = encode_operand(&mapB, Bu, N, K, Kind<kKind>::kElem, BN);
+  if (e == cudaSuccess) e = encode_operand(&mapB2, Bg, N, K, Kind<kKind>::kElem, BN);
+  if (e != cudaSuccess) return e;
+  Args a = {};
+  a.M = (int)M;
+  a.N = (int)N;
+  a.K = (int)K;
+  a.m_tiles = (int)((M + kBM - 1) / kBM);
+  a.n_tiles = (int)((N + BN - 1) / BN);
+  a.k_stages = (int)((K + Kind<kKind>::kKStage - 1) / Kind<kKind>::kKStage);
+  a.splits = 1;
+  a.kps = a.k_stages;
+  a.acc_ws = nullptr;
+  a.tile_cnt = nullptr;
+  a.x_scale = x_scale;
+  a.w_scale = su;
+  a.y = u;
+  a.y_bf16 = nullptr;
+  a.acc_out = nullptr;
+  a.wait = wait;
+  a.w_scale2 = sg;
+  a.y2 = v;
+  a.h = h;
+  static bool configured[64] = {};
+  int dev = 0;
+  e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 64 && !configured[dev]) {
+    e = cudaFuncSetAttribute(k_gemm_tc<kKind, BN, false, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Tile<BN, false, true>::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured[dev] = true;
+  }
+  const int items = a.m_tiles * a.n_tiles;
+  const int ctas = items < 148 ? items : 148;
+  return launch_pdl(k_gemm_tc<kKind, BN, false, true>, dim3(ctas), dim3(kThreads),
+                    (size_t)Tile<BN, false, true>::kSmemBytes, s, mapA, mapB, mapB2, a);
 }
 
 }  // namespace
+
+size_t gemm_tc_gated_workspace(int64_t M, int64_t N, int64_t K) { return gated_ws(M, N, K); }
+
+cudaError_t launch_gemm_tc_gated(const uint8_t* Wu, const float* su, const uint8_t* Wg,
+                                 const float* sg, const int8_t* xq, const float* x_scale,
+                                 int64_t M, int64_t N, int64_t K, float* u, float* v, float* h,
+                                 void* ws, long long wait, cudaStream_t s) {
+  return launch_gated_t(Wu, su, Wg, sg, xq, x_scale, M, N, K, u, v, h, ws, wait, s);
+}
 
 bool gemm_tc_eligible(int64_t M, int64_t N, int64_t K) {
   return M >= 16 && N >= 1 && K >= 64 && K % 64 == 0;

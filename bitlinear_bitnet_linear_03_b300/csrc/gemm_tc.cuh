@@ -14,6 +14,15 @@ cudaError_t launch_gemm_tc(const uint8_t* Wq, const float* w_scale, const int8_t
                            uint16_t* y_bf16, int32_t* acc_out, void* ws, long long wait,
                            cudaStream_t s);
 
+// The FFN's up and gate products of the same activations in one GEMM
+// (M > 256): u = BitLinear(Wu), v = BitLinear(Wg), h = relu(v)^2 * u, all
+// [M, N] binary32; u and v are optional outputs, h is required.
+size_t gemm_tc_gated_workspace(int64_t M, int64_t N, int64_t K);
+cudaError_t launch_gemm_tc_gated(const uint8_t* Wu, const float* su, const uint8_t* Wg,
+                                 const float* sg, const int8_t* xq, const float* x_scale,
+                                 int64_t M, int64_t N, int64_t K, float* u, float* v, float* h,
+                                 void* ws, long long wait, cudaStream_t s);
+
 // Reads and clears the per-device error word that bounded waits set.
 cudaError_t read_and_clear_device_error(int* code, cudaStream_t s);
 

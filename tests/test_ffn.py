@@ -102,12 +102,14 @@ def test_ffn_partial_debug_outputs(M, seed):
     assert_bits_equal(y, want["y"], "y end to end")
 
 
-def test_ffn_norm_special_rows():
+@pytest.mark.parametrize("H", [256, 2560])
+def test_ffn_norm_special_rows(H):
     """Rows that exercise the exact sum of squares: the row whose exact sum
     rounds differently from a binary64 or running binary32 sum, an all-zero
-    row, subnormal and tiny values, values whose squares overflow binary32
-    (ss = inf, r = 0), and an ordinary row."""
-    M, H, F = 6, 256, 320
+    row, subnormal and tiny values (a row whose squares span more than the
+    128-bit window), values whose squares overflow binary32 (ss = inf,
+    r = 0), and an ordinary row."""
+    M, F = 6, 320
     rows = np.zeros((M, H), np.float32)
     rows[0, 3], rows[0, 20], rows[0, 41], rows[0, 63] = 1490944.0, 256.0, 256.0, 2.0 ** -20
     rows[2, ::3] = 2.0 ** -130                      # subnormal bf16 values: squares underflow
@@ -145,3 +147,26 @@ def test_ffn_seq4096_sampled_tokens(seed):
     # every token: the properties that hold at any size
     assert np.isfinite(got["y"]).all()
     assert (np.abs(got["xq"]).max(axis=1) == 127).all()
+
+
+@pytest.mark.parametrize("M,seed", [(300, 5), (512, 6)])
+def test_ffn_prefill_gated_gemm_without_intermediates(M, seed):
+    """Above 256 tokens the up and gate products run as one GEMM whose
+    epilogue forms h; with no intermediate outputs requested h lives in the
+    workspace.  Sampled tokens (first and last included) must match the
+    oracle bit for bit: the codes and scale of h, the down accumulators, y."""
+    x, g, ws = ffn_inputs(M, seed, random_gain=True)
+    (Wu, su, _), (Wg, sg, _), (Wd, sd, _) = ws
+    dbg = dict(hq=torch.empty((M, F), dtype=torch.int8, device="cuda"),
+               sh=torch.empty(M, dtype=torch.float32, device="cuda"),
+               acc_down=torch.empty((M, H), dtype=torch.int32, device="cuda"))
+    f32 = lambda v: dev(np.array([v], np.float32))
+    y = host(bn.bitnet_ffn(dev_bf16(x), dev(g), 1e-5, dev(Wu), f32(su), dev(Wg), f32(sg),
+                           dev(Wd), f32(sd), debug=dbg))
+    got = {k: host(v) for k, v in dbg.items()}
+    rows = np.random.default_rng(seed).choice(M, 16, replace=False)
+    rows[:2] = [0, M - 1]
+    want = oracle.ffn(x[rows], g, 1e-5, Wu, su, Wg, sg, Wd, sd, threads=oracle.default_threads())
+    for k in ("sh", "hq", "acc_down"):
+        assert_bits_equal(got[k][rows], want[k], k)
+    assert_bits_equal(y[rows], want["y"], "y")
