@@ -27,7 +27,7 @@ constexpr int kMaxBlocks = 592;   // 4 x 148
 constexpr int kStage1Threads = 256;
 constexpr int kLimbs = 7;         // 448-bit exact sum
 
-int stage1_blocks(int64_t total) {
+constexpr int stage1_blocks(int64_t total) {
   int64_t b = (total + 8191) / 8192;
   if (b < 1) b = 1;
   if (b > kMaxBlocks) b = kMaxBlocks;
@@ -270,7 +270,12 @@ size_t quantize_weights_noalloc_limit() { return kNoAllocScratchBytes; }
 
 cudaError_t launch_quantize_weights_noalloc(const float* W, int64_t total, uint8_t* Wq,
                                             float* w_scale, cudaStream_t s) {
-  if (quantize_weights_workspace(total) > kNoAllocScratchBytes) return cudaErrorInvalidValue;
+  // stage1_blocks caps the grid at kMaxBlocks, and the array holds kMaxBlocks
+  // rows: every accepted size fits, so there is no size check here.  (Any
+  // change to stage1_blocks that could exceed the array breaks the build.)
+  static_assert((size_t)stage1_blocks((int64_t)1 << 40) * kRow * sizeof(unsigned long long) <=
+                    kNoAllocScratchBytes,
+                "the array holds the largest stage-1 grid");
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;

@@ -124,7 +124,9 @@ bitnet_status bitnet_quantize_weights(const float* W, int64_t N, int64_t K,
  * BITNET_ERR_SHAPE).  Nothing is allocated or freed.
  * The first call on a device looks up the array's device address (once per
  * device, with that device current); make that first call before any stream
- * capture.  Every call uses the same array: calls whose work overlaps on the
+ * capture.  The address is kept for the life of the process: after a
+ * cudaDeviceReset (which unloads the library's device code, so the array
+ * may move) do not call this entry again in that process.  Every call uses the same array: calls whose work overlaps on the
  * GPU (other streams, other host threads) race and must be serialised by the
  * caller.  Each call writes all the scratch it reads, so no state carries
  * over between calls. */
