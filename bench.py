@@ -614,9 +614,11 @@ def run_gpu_arm(args, rank, world, barrier, max_over_ranks):
             h.copy_(d, non_blocking=True)
         torch.cuda.current_stream().synchronize()
 
-    for _ in range(max(3, args.warmup)):
+    # (a short run is dominated by one-off costs of the first host copies:
+    # warm up at least 20 steps and time at least 100)
+    for _ in range(max(20, args.warmup)):
         e2e_step()
-    e2e_steps = max(10, min(args.steps, 500))
+    e2e_steps = max(100, min(args.steps, 500))
     barrier()
     t0 = time.perf_counter()
     for _ in range(e2e_steps):

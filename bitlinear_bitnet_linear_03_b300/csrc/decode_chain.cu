@@ -31,26 +31,34 @@
 // every CTA increments once at its start (run = old value / CTAs).
 //
 // Work split: phase rows (gated: row pairs up n / gate n) are divided evenly
-// over the CTAs; a stage is a run of whole rows of one matrix (gated: the
-// same rows of up, then of gate, two copies into one slot), up to ~62 KB, so
-// a CTA's share of a phase is usually one stage: every stage costs a release
-// and a refill, and on B300 those latencies, not the dot products, bound a
-// phase.  Consumer lane l of a warp owns the 64-weight chunks l, l + 32, ...
+// over the CTAs; a stage is a run of whole rows of at most two targets (two
+// copies into one slot; gated: the same rows of up, then of gate), up to
+// ~62 KB, so a CTA's share of a phase is one stage even where it crosses a
+// target boundary: every stage costs a release and a refill, and on B300
+// those latencies, not the dot products, bound a phase.  Consumer lane l of a warp owns the 64-weight chunks l, l + 32, ...
 // of its K part: their int8 activations sit in registers for the whole
 // phase, and a row costs one 16-byte shared load, 16 ANDs and 16 dp4a per
 // chunk (decode_common.cuh).  When several warps split K, their parts meet in
 // shared-memory atomics that also count the parts; the last part writes the
 // row.
 //
-// The subln sum of squares is exact (exact_sumsq.cuh): in 128 bits anchored
-// 88 bits below the largest square of the row, or, for a row whose squares
-// span more than that, in five limbs out of line.  Rarely run code stays out
-// of line and the row loops are not unrolled: the kernel is large, and
-// instruction fetch stalls showed in its profile.
+// A thread loads all of its input groups at once and checks their tags; for
+// a group still stale it waits on one word of it before loading the pending
+// groups again, so that pollers do not stream the whole input from L2 while
+// it is being produced.
+//
+// The subln sum of squares is exact (exact_sumsq.cuh): each warp adds its
+// squares with 32 x 32 -> 64-bit multiply-adds in 128 bits anchored 88 bits
+// below its own largest square, the eight warp sums meet after one barrier
+// (hardware warp reductions on 26-bit limbs), and the total is rounded once;
+// a row whose squares span more than the window takes five limbs, out of
+// line.  The quantisers round with a full-rate float add instead of the
+// float-to-integer conversion units.  Rarely run code stays out of line and
+// the row loops are not unrolled, to keep the kernel's code small.
 //
 // Every wait is bounded (a second by default): on time-out the kernel records
-// an error bit, every warp stops at the next uniform point, the producer
-// waits for its copies in flight and the CTA returns.
+// an error bit, every warp stops at the next uniform point, the CTA waits for
+// its copies in flight and returns.
 #include <algorithm>
 #include <vector>
 
