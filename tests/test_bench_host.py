@@ -44,6 +44,14 @@ def test_decode_step_byte_counts_8b_class():
     assert b.layer_bytes(b.DIMS_8B) == packed + scales + gains + inputs + outputs
 
 
+def test_oracle_phase_bytes_add_up_to_the_layer():
+    b = load_bench()
+    sample = b.OracleSample.__new__(b.OracleSample)
+    for dims in (b.DIMS_2B, b.DIMS_8B):
+        sample.dims = dims
+        assert sum(sample.phase_bytes()) == b.layer_bytes(dims)
+
+
 def test_profiled_traffic_follows_the_kernel_source(tmp_path):
     b = load_bench()
     kernel = os.path.join(ROOT, "bitlinear_bitnet_linear_03_b300/csrc/decode_chain.cu")
