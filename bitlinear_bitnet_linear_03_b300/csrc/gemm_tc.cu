@@ -98,11 +98,16 @@ constexpr int kMmaKBytes = 32;
 struct Args {
   int M, N, K;
   int m_tiles, n_tiles, k_stages;
-  // Split K: work item i is tile i % tiles, K stages [s * kps, (s + 1) * kps)
-  // of split s = i / tiles.  With splits > 1 every split adds its exact
-  // partial sums into acc_ws [M, N] (zeroed by the pre-pass) and the last
-  // split of a tile to finish (counted in tile_cnt) writes the outputs.
-  int splits, kps;
+  // Split K.  Items below full_tiles are whole tiles (item = tile).  The
+  // other tiles, rest = tiles - full_tiles of them, are split: item
+  // full_tiles + j is tile full_tiles + j % rest, K stages [s * kps,
+  // (s + 1) * kps) of split s = j / rest.  Every split adds its exact partial
+  // sums into acc_ws (zeroed by the pre-pass) and the last split of a tile to
+  // finish (counted in tile_cnt[tile - full_tiles]) writes the outputs.
+  // acc_ws is [M, N] when full_tiles == 0 (every tile split: few output
+  // tiles), else one 128 x BN block per split tile (only the tiles of a last,
+  // partly filled wave are split, so that the wave keeps every SM busy).
+  int splits, kps, full_tiles;
   float* acc_ws;
   int* tile_cnt;
   const float* x_scale;
@@ -120,10 +125,19 @@ struct Args {
 
 // Work item -> tile and K-stage range.
 __device__ __forceinline__ void item_range(const Args& a, int item, int& tile, int& ks0, int& ks1) {
-  const int tiles = a.m_tiles * a.n_tiles;
-  tile = item % tiles;
-  ks0 = (item / tiles) * a.kps;
+  if (item < a.full_tiles) {
+    tile = item;
+    ks0 = 0;
+    ks1 = a.k_stages;
+    return;
+  }
+  const int j = item - a.full_tiles, rest = a.m_tiles * a.n_tiles - a.full_tiles;
+  tile = a.full_tiles + j % rest;
+  ks0 = (j / rest) * a.kps;
   ks1 = min(a.k_stages, ks0 + a.kps);
+}
+__device__ __forceinline__ int item_count(const Args& a) {
+  return a.full_tiles + (a.m_tiles * a.n_tiles - a.full_tiles) * a.splits;
 }
 
 // ---- PTX wrappers (PTX ISA: mbarrier, cp.async.bulk.tensor, tcgen05)
@@ -365,7 +379,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUte
   const uint32_t smem0 = (saddr(smem_raw) + 1023u) & ~1023u;  // 1024-byte aligned tiles
   const uint32_t bbuf0 = smem0 + kStages * kStageBytes;        // fused: expanded B buffers
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int items = a.m_tiles * a.n_tiles * a.splits;
+  const int items = item_count(a);
   __shared__ int s_last;
 
   if (threadIdx.x == 0) {
@@ -556,7 +570,11 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUte
       float* yrow = a.y ? a.y + (int64_t)m * a.N : nullptr;
       uint16_t* brow = a.y_bf16 ? a.y_bf16 + (int64_t)m * a.N : nullptr;
       int32_t* arow = a.acc_out ? a.acc_out + (int64_t)m * a.N : nullptr;
-      float* wrow = a.acc_ws + (int64_t)m * a.N;
+      const bool split_tile = a.splits > 1 && t >= a.full_tiles;
+      // (acc_ws + row * BN - n0 + nb) addresses the tile's own block
+      float* wrow = a.full_tiles > 0
+                        ? a.acc_ws + ((int64_t)(t - a.full_tiles) * kBM + row) * BN - n0
+                        : a.acc_ws + (int64_t)m * a.N;
       const bool vec = (a.N & 3) == 0;
       const bool vec8 = (a.N & 7) == 0;
       if (GATED) {
@@ -591,7 +609,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUte
         tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(ab * BN + cb), r);
         if (!mrow) continue;
         const int nb = n0 + cb;
-        if (a.splits > 1) {
+        if (split_tile) {
           // Add this split's exact partial sums (integers below 2^24 in
           // magnitude, whatever the order: fp32 addition is exact here).
           if (vec && nb + 32 <= a.N) {
@@ -614,11 +632,11 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUte
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(saddr(&acc_empty[ab]));
-      if (a.splits > 1) {
+      if (split_tile) {
         // The last split of the tile to finish writes the outputs.
         __threadfence();
         epi_sync();
-        if (threadIdx.x == 64) s_last = atomicAdd(&a.tile_cnt[t], 1) == a.splits - 1;
+        if (threadIdx.x == 64) s_last = atomicAdd(&a.tile_cnt[t - a.full_tiles], 1) == a.splits - 1;
         epi_sync();
         if (s_last) {
           __threadfence();
@@ -757,12 +775,20 @@ bool use_fused(int64_t M) { return M <= 256; }
 int pick_bn(int64_t N) { return N <= 128 ? 128 : 256; }
 
 // Workspace of one call: [B bf16 N x K (unfused only)] [A bf16 M x K]
-// [split-K sums M x N fp32] [tile counters], each 1 KB aligned.  Split K
-// (fused path only) when the output has fewer tiles than half the SMs: as
-// many splits as fill the SMs, each at least 16 K stages.
+// [split-K sums] [tile counters], each 1 KB aligned.  Split K:
+//  * fused path, when the output has fewer tiles than half the SMs: every
+//    tile, in as many splits as fill the SMs (each at least 16 K stages);
+//    sums M x N fp32;
+//  * unfused path, when the output is at most three waves of whole tiles
+//    plus a last wave that would fill less than half the SMs: only that
+//    wave's tiles, in as many splits as fill the SMs (each at least 16 K
+//    stages); one 128 x BN fp32 block per split tile.  Measured on B300:
+//    M = 4096, K = 6912, N = 2560 (two waves + 24 tiles) 167 -> 161 us;
+//    K = 14336, N = 4096 (three waves + 68 tiles) 410 -> 399 us; with twelve
+//    waves + 16 tiles (K = 4096, N = 14336) splitting lost 3%.
 struct WsLayout {
   size_t b, a, acc, cnt, end;
-  int splits, kps;
+  int splits, kps, full_tiles;
 };
 WsLayout ws_layout(int64_t M, int64_t N, int64_t K) {
   WsLayout L = {};
@@ -771,18 +797,31 @@ WsLayout ws_layout(int64_t M, int64_t N, int64_t K) {
   const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + bn - 1) / bn);
   const int k_stages = (int)((K + 63) / 64);
   int splits = 1;
+  int64_t split_tiles = tiles;  // tiles that are split when splits > 1
+  L.full_tiles = 0;
   if (fused && tiles < 74) {
     splits = (int)(148 / tiles);
     if (splits > k_stages / 16) splits = k_stages / 16;
     if (splits < 1) splits = 1;
+  } else if (!fused && tiles > 148 && tiles < 4 * 148 && tiles % 148 < 74) {
+    const int64_t rem = tiles % 148;
+    splits = (int)(148 / rem);
+    if (splits > k_stages / 16) splits = k_stages / 16;
+    if (splits < 2) splits = 1;
+    if (splits > 1) {
+      L.full_tiles = (int)(tiles - rem);
+      split_tiles = rem;
+    }
   }
   L.kps = (k_stages + splits - 1) / splits;
   L.splits = (k_stages + L.kps - 1) / L.kps;
+  if (L.splits < 2) L.full_tiles = 0;
   L.b = 0;
   L.a = fused ? 0 : round1k((size_t)(N * K * 2));
   L.acc = L.a + round1k((size_t)(M * K * 2));
-  L.cnt = L.acc + (L.splits > 1 ? round1k((size_t)(M * N * 4)) : 0);
-  L.end = L.cnt + (L.splits > 1 ? round1k((size_t)tiles * 4) : 0);
+  const size_t sums = L.full_tiles > 0 ? (size_t)split_tiles * kBM * bn * 4 : (size_t)(M * N * 4);
+  L.cnt = L.acc + (L.splits > 1 ? round1k(sums) : 0);
+  L.end = L.cnt + (L.splits > 1 ? round1k((size_t)split_tiles * 4) : 0);
   return L;
 }
 
@@ -825,6 +864,7 @@ cudaError_t launch_kind(const uint8_t* Wq, const float* w_scale, const int8_t* x
   a.k_stages = (int)((K + Kind<KIND>::kKStage - 1) / Kind<KIND>::kKStage);
   a.splits = L.splits;
   a.kps = L.kps;
+  a.full_tiles = L.full_tiles;
   a.acc_ws = acc_ws;
   a.tile_cnt = tile_cnt;
   a.x_scale = x_scale;
@@ -847,7 +887,7 @@ cudaError_t launch_kind(const uint8_t* Wq, const float* w_scale, const int8_t* x
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
-  const int items = a.m_tiles * a.n_tiles * a.splits;
+  const int items = a.full_tiles + (a.m_tiles * a.n_tiles - a.full_tiles) * a.splits;
   const int ctas = items < 148 ? items : 148;
   return launch_pdl(k_gemm_tc<KIND, BN, FUSED>, dim3(ctas),
                     dim3(FUSED ? kThreadsFused : kThreads), (size_t)Tile<BN, FUSED>::kSmemBytes, s,
@@ -900,6 +940,7 @@ cudaError_t launch_gated_t(const uint8_t* Wu, const float* su, const uint8_t* Wg
   a.k_stages = (int)((K + Kind<kKind>::kKStage - 1) / Kind<kKind>::kKStage);
   a.splits = 1;
   a.kps = a.k_stages;
+  a.full_tiles = 0;
   a.acc_ws = nullptr;
   a.tile_cnt = nullptr;
   a.x_scale = x_scale;
