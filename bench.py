@@ -434,7 +434,7 @@ def secondary_measurements(torch, bn, peaks, only=None, cpu=True):
 
     # 100B-class shapes (each timed as a CUDA graph of calls)
     ms_100b = [m for m, c in ((1, "gemv100b"), (4, "gemv100b"), (16, "fused_small_m"),
-                              (64, "fused_small_m")) if want(c)]
+                              (32, "fused_small_m"), (64, "fused_small_m")) if want(c)]
     for (N, K) in ([(28672, 8192), (8192, 28672)] if ms_100b else []):
         sets = _weight_sets(torch, bn, synth, N, K, 3, 200)
         for M in ms_100b:

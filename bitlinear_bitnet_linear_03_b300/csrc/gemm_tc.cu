@@ -64,14 +64,21 @@ constexpr int kRingBytes = 192 * 1024;
 // buffered.
 // GATED (unfused only): a stage holds the A tile and two B tiles (up and
 // gate rows of the same output columns).
-template <int BN, bool FUSED = false, bool GATED = false>
+// KIND 2 (e4m3 digits, fused only): a stage row holds 128 weights, so the
+// packed codes are 32 bytes per row per stage, and three e4m3 B buffers
+// follow a 4-stage ring.
+template <int BN, bool FUSED = false, bool GATED = false, int KIND = 1>
 struct Tile {
   static constexpr int kBTileBytes = BN * kRowBytes;
-  static constexpr int kPackedBytes = FUSED ? BN * 16 : 0;
+  static constexpr int kPackedBytes = FUSED ? BN * (KIND == 2 ? 32 : 16) : 0;
   static constexpr int kStageBytes =
       kATileBytes + (FUSED ? kPackedBytes : (GATED ? 2 : 1) * kBTileBytes);
-  static constexpr int kBBufBytes = FUSED ? 2 * kBTileBytes : 0;
-  static constexpr int kStages = (kRingBytes - kBBufBytes) / kStageBytes;  // 4 or 6; 6 fused
+  // expanded B buffers: two (bf16), three (digits: expansion runs on while
+  // the MMAs of the two previous stages are in flight)
+  static constexpr int kNB = KIND == 2 ? 3 : 2;
+  static constexpr int kBBufBytes = FUSED ? kNB * kBTileBytes : 0;
+  static constexpr int kStages = (kRingBytes - kBBufBytes) / kStageBytes;  // 4, 6 fused, 4 digits
+  static_assert(!FUSED || kStages > kNB, "a ring slot is reused only after its B buffer");
   static constexpr int kSmemBytes = kStages * kStageBytes + kBBufBytes + 1024;  // + alignment
 };
 constexpr long long kDrainCycles = 2000000000ll;  // bound of the final drains (~1 s)
@@ -92,8 +99,28 @@ struct Kind<1> {
   template <int BN>
   static constexpr uint32_t idesc() { return kIdescBase | ((uint32_t)(BN >> 3) << 17); }
 };
-// Every tcgen05.mma consumes 32 bytes of K per row (16 bf16 or 32 int8).
+// Operand element: e4m3 (1 byte), 128 elements of K per 128-byte stage row
+// (the exact digit form, fused path with M <= 64 only).  B holds the ternary
+// weights (-1, 0, +1: 0xB8, 0x00, 0x38); the A tile stacks two digit rows
+// per token, hi = x >> 4 in [-8, 7] in rows 0-63 and lo = x & 15 in [0, 15]
+// in rows 64-127.  Every value is exact in e4m3 and every product and
+// partial sum is an integer of magnitude <= 15 K, so the binary32
+// accumulators are exact; the epilogue forms acc = 16 D[m] + D[64 + m] in
+// int32, which is x . q exactly.
+template <>
+struct Kind<2> {
+  static constexpr int kElem = 1;
+  static constexpr int kKStage = kRowBytes / kElem;  // 128 elements per stage
+  // Instruction descriptor: D f32 (bits 4-5 = 1), A and B e4m3 (bits 7-9 and
+  // 10-12 = 0), K-major, M/16 at bits 24-28; N/8 at bits 17-22 per tile.
+  static constexpr uint32_t kIdescBase = (1u << 4) | ((uint32_t)(kBM >> 4) << 24);
+  template <int BN>
+  static constexpr uint32_t idesc() { return kIdescBase | ((uint32_t)(BN >> 3) << 17); }
+};
+// Every tcgen05.mma consumes 32 bytes of K per row (16 bf16 or 32 e4m3).
 constexpr int kMmaKBytes = 32;
+// Digit rows: the lo digits of token m sit in A-tile row kDigitRows + m.
+constexpr int kDigitRows = 64;
 
 struct Args {
   int M, N, K;
@@ -193,11 +220,18 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
 template <int KIND, int BN>
 __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
                                        uint32_t accumulate) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(Kind<KIND>::template idesc<BN>()), "r"(accumulate)
-      : "memory");
+  if (KIND == 2)
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(Kind<KIND>::template idesc<BN>()), "r"(accumulate)
+        : "memory");
+  else
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(Kind<KIND>::template idesc<BN>()), "r"(accumulate)
+        : "memory");
 }
 // Shared-memory matrix descriptor of a K-major operand tile written by TMA
 // with 128-byte swizzle: rows of 128 bytes, 8-row groups 1024 bytes apart
@@ -336,6 +370,49 @@ __device__ __forceinline__ void expand_b_tile(uint32_t packed, uint32_t btile, i
   }
 }
 
+// Digit form, B side.  Masking a packed word with 0x33333333 leaves one code
+// per nibble, and one byte permute over the table {0xB8, 0x00, 0x38} (e4m3 of
+// q = -1, 0, +1, selected by code 0, 1, 2) turns four nibbles into four
+// weights.  Packed word j of block h (bytes 4j .. 4j+3; byte t holds the
+// weights t, 16+t, 32+t, 48+t of the block in bits 0-1, 2-3, 4-5, 6-7)
+// becomes the 16-byte chunk c = 4h + j of the stage row, in this order:
+// chunk byte 4o + i (o = 0..3, i = 0..3) holds block weight 16g + 4j + b with
+// b = 2 (o & 1) + (i >> 1), g = 2 (i & 1) + (o >> 1).  This permutes K inside
+// each 64-weight block; the digit pre-pass writes the activations in the same
+// order, so every product still pairs x[k] with q[k].
+constexpr uint32_t kE4m3Ternary = 0x003800B8u;
+__device__ __forceinline__ uint32_t e4m3_lookup(uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(kE4m3Ternary), "r"(0u), "r"(sel));
+  return d;
+}
+
+// Expands the packed codes of one digit-form stage (BN rows x 128 weights,
+// two packed blocks = 32 bytes per row) into the e4m3 B tile in the
+// 128-byte-swizzled K-major layout: row r at (r/8)*1024 + (r%8)*128, chunk c
+// at slot c ^ (r%8).  Thread t of 128 takes rows t, t+128, ...
+template <int BN>
+__device__ __forceinline__ void expand_b_tile_e4m3(uint32_t packed, uint32_t btile, int t) {
+  for (int r = t; r < BN; r += 128) {
+    uint32_t ww[8];
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(ww[0]), "=r"(ww[1]), "=r"(ww[2]), "=r"(ww[3])
+                 : "r"(packed + 32 * r));
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(ww[4]), "=r"(ww[5]), "=r"(ww[6]), "=r"(ww[7])
+                 : "r"(packed + 32 * r + 16));
+    const uint32_t rowbase = btile + (uint32_t)((r >> 3) * 1024 + (r & 7) * 128);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const uint32_t u = ww[c] & 0x33333333u, v = (ww[c] >> 2) & 0x33333333u;
+      asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(rowbase + 16u * (uint32_t)(c ^ (r & 7))),
+                   "r"(e4m3_lookup(u)), "r"(e4m3_lookup(u >> 16)), "r"(e4m3_lookup(v)),
+                   "r"(e4m3_lookup(v >> 16))
+                   : "memory");
+    }
+  }
+}
+
 // h = relu(v)^2 * u with t = max(v, 0) taken as v > 0 ? v : 0 (binary32).
 __device__ __forceinline__ float relu2_mul(float u, float v) {
   const float t = v > 0.0f ? v : 0.0f;
@@ -363,13 +440,20 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUte
           const __grid_constant__ CUtensorMap mapB2, const __grid_constant__ Args a) {
   static_assert(!(GATED && FUSED), "the gated form reads expanded bf16 weights");
   static_assert(!GATED || 4 * BN <= (int)kTmemCols, "two accumulators per tile, double buffered");
+  static_assert(KIND == 1 || (FUSED && !GATED), "the digit form is fused only");
   extern __shared__ uint8_t smem_raw[];
-  constexpr int kStages = Tile<BN, FUSED, GATED>::kStages;
-  constexpr int kStageBytes = Tile<BN, FUSED, GATED>::kStageBytes;
-  constexpr int kBTileBytesT = Tile<BN, FUSED, GATED>::kBTileBytes;
+  using T = Tile<BN, FUSED, GATED, KIND>;
+  constexpr int kStages = T::kStages;
+  constexpr int kStageBytes = T::kStageBytes;
+  constexpr int kBTileBytesT = T::kBTileBytes;
+  constexpr int kPackedX = Kind<KIND>::kKStage / 4;  // packed bytes of K per stage
+  // digit form: the lo digits' sums (TMEM rows 64-127) handed to the threads
+  // of rows 0-63, 32 columns at a time (row stride 33: no bank conflicts)
+  __shared__ float xbuf[KIND == 2 ? kDigitRows * 33 : 1];
   __shared__ __align__(8) uint64_t full_bar[kStages];
   __shared__ __align__(8) uint64_t empty_bar[kStages];
-  __shared__ __align__(8) uint64_t bready_bar[2];  // fused: B buffer expanded
+  constexpr int kNB = T::kNB;
+  __shared__ __align__(8) uint64_t bready_bar[kNB];  // fused: B buffer expanded
   __shared__ __align__(8) uint64_t acc_full[2];
   __shared__ __align__(8) uint64_t acc_empty[2];
   __shared__ __align__(8) uint64_t drain_bar;
@@ -388,7 +472,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUte
       // fused: the four converter warps (packed codes read) and the MMA commit
       mbar_init(saddr(&empty_bar[s]), FUSED ? 5 : 1);
     }
-    for (int b = 0; b < 2; ++b) mbar_init(saddr(&bready_bar[b]), 4);
+    for (int b = 0; b < kNB; ++b) mbar_init(saddr(&bready_bar[b]), 4);
     for (int b = 0; b < 2; ++b) {
       mbar_init(saddr(&acc_full[b]), 1);
       mbar_init(saddr(&acc_empty[b]), 4);
@@ -434,11 +518,21 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUte
           const uint32_t fb = saddr(&full_bar[s]);
           const uint32_t sa = smem0 + s * kStageBytes;
           if (FUSED) {
-            // A tile (bf16) and the packed codes of the B tile (16 bytes per
-            // row = the stage's 64 weights).
-            mbar_expect_tx(fb, kATileBytes + Tile<BN, FUSED>::kPackedBytes);
-            tma_load_2d(sa, &mapA, ks * Kind<KIND>::kKStage, m0, fb);
-            tma_load_2d(sa + kATileBytes, &mapB, ks * 16, n0, fb);
+            // A tile and the packed codes of the B tile (kPackedX bytes per
+            // row = the stage's weights).  bf16: 128 token rows.  Digits
+            // (M <= 64, one row tile): the operand is [2M, K], hi digits in
+            // rows 0..M-1 and lo digits in rows M..2M-1; a 64-row box from
+            // row 0 fills tile rows 0-63 and one from row M fills rows
+            // 64-127 (rows past a token's own are padding: their outputs are
+            // never stored, and rows past 2M read as zero).
+            mbar_expect_tx(fb, kATileBytes + T::kPackedBytes);
+            if (KIND == 2) {
+              tma_load_2d(sa, &mapA, ks * Kind<KIND>::kKStage, 0, fb);
+              tma_load_2d(sa + kDigitRows * kRowBytes, &mapA, ks * Kind<KIND>::kKStage, a.M, fb);
+            } else {
+              tma_load_2d(sa, &mapA, ks * Kind<KIND>::kKStage, m0, fb);
+            }
+            tma_load_2d(sa + kATileBytes, &mapB, ks * kPackedX, n0, fb);
           } else {
             mbar_expect_tx(fb, kStageBytes);
             tma_load_2d(sa, &mapA, ks * Kind<KIND>::kKStage, m0, fb);
@@ -475,11 +569,11 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUte
         // gated: the tile's u accumulator, its v accumulator BN columns on
         const uint32_t d = tmem + (uint32_t)(ab * (GATED ? 2 : 1) * BN);
         for (int ks = ks0; ks < ks1; ++ks, ++it) {
-          const int s = it % kStages, b = it & 1;
+          const int s = it % kStages, b = it % kNB;
           // fused: the expanded B buffer (and the A tile of the stage, whose
           // landing the converters waited for and which is checked again)
           bool ready = mbar_wait(saddr(&full_bar[s]), (it / kStages) & 1, a.wait);
-          if (FUSED && ready) ready = mbar_wait(saddr(&bready_bar[b]), (it >> 1) & 1, a.wait);
+          if (FUSED && ready) ready = mbar_wait(saddr(&bready_bar[b]), (it / kNB) & 1, a.wait);
           if (!ready || *(volatile int*)&s_abort) {
             atomicOr(&g_device_error, kErrMma);
             *(volatile int*)&s_abort = 1;
@@ -520,12 +614,15 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUte
       (void)t;
       bool ok = true;
       for (int ks = ks0; ks < ks1; ++ks, ++it) {
-        const int s = it % kStages, b = it & 1;
+        const int s = it % kStages, b = it % kNB;
         bool ready = mbar_wait(saddr(&full_bar[s]), (it / kStages) & 1, a.wait);
-        // the MMAs of two stages ago (which read buffer b) have finished: that
-        // stage's ring slot was released, by them and by these warps
-        if (ready && it >= 2)
-          ready = mbar_wait(saddr(&empty_bar[(it - 2) % kStages]), ((it - 2) / kStages) & 1, a.wait);
+        // the MMAs of kNB stages ago (which read buffer b) have finished: that
+        // stage's ring slot was released, by them and by these warps (the slot
+        // cannot have been released again since: kStages > kNB, and the next
+        // use of it needs these warps' arrival at a later stage)
+        if (ready && it >= kNB)
+          ready = mbar_wait(saddr(&empty_bar[(it - kNB) % kStages]), ((it - kNB) / kStages) & 1,
+                            a.wait);
         if (!ready || *(volatile int*)&s_abort) {
           if (lane == 0) atomicOr(&g_device_error, kErrProducer);
           *(volatile int*)&s_abort = 1;
@@ -533,7 +630,10 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUte
           break;
         }
         const uint32_t sa = smem0 + s * kStageBytes;
-        expand_b_tile<BN>(sa + kATileBytes, bbuf0 + b * kBTileBytesT, ct);
+        if (KIND == 2)
+          expand_b_tile_e4m3<BN>(sa + kATileBytes, bbuf0 + b * kBTileBytesT, ct);
+        else
+          expand_b_tile<BN>(sa + kATileBytes, bbuf0 + b * kBTileBytesT, ct);
         // make the generic-proxy stores visible to the tensor core's reads
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
@@ -607,6 +707,24 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUte
       for (int cb = 0; cb < BN && !GATED; cb += 32) {
         uint32_t r[32];
         tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(ab * BN + cb), r);
+        if (KIND == 2) {
+          // acc = 16 * (hi digits' sum, row m) + (lo digits' sum, row 64 + m):
+          // exact integers in binary32, combined in int32.  Rows >= 64 (and
+          // so >= M) only hand their sums over.
+          float* xb = xbuf + (row & (kDigitRows - 1)) * 33;
+          if (row >= kDigitRows) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) xb[j] = __uint_as_float(r[j]);
+          }
+          epi_sync();
+          if (row < kDigitRows) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              r[j] = __float_as_uint(__int2float_rn(16 * __float2int_rn(__uint_as_float(r[j])) +
+                                                    __float2int_rn(xb[j])));
+          }
+          epi_sync();
+        }
         if (!mrow) continue;
         const int nb = n0 + cb;
         if (split_tile) {
@@ -664,18 +782,41 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUte
                  : "memory");
 }
 
+// Two e4m3 bytes (a0 in the low byte) of two small integers, exact: the
+// conversion instruction puts its first source in the high byte.
+__device__ __forceinline__ uint32_t e4m3x2_of(int a0, int a1) {
+  unsigned short d;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(__int2float_rn(a1)),
+      "f"(__int2float_rn(a0)));
+  return d;
+}
+// The e4m3 digits hi = x >> 4 and lo = x & 15 of the four int8 values in w.
+__device__ __forceinline__ void digits4(uint32_t w, uint32_t& hi, uint32_t& lo) {
+  int x[4];
+#pragma unroll
+  for (int b = 0; b < 4; ++b) x[b] = (int)(int8_t)(w >> (8 * b));
+  hi = e4m3x2_of(x[0] >> 4, x[1] >> 4) | (e4m3x2_of(x[2] >> 4, x[3] >> 4) << 16);
+  lo = e4m3x2_of(x[0] & 15, x[1] & 15) | (e4m3x2_of(x[2] & 15, x[3] & 15) << 16);
+}
+
 // ---- pre-pass kernels
 // Pre-pass, one launch (items [nblk + nx, + nz) zero 16 bytes of the split-K
 // workspace each): items [0, 8 nblk) write one 16-byte chunk of bf16 B each
 // (chunk c of packed block it / 8, so consecutive threads write consecutive
 // chunks); items [8 nblk, 8 nblk + nx) widen 16 int8 activations into 32
-// bytes of bf16 A.  In a packed block, chunk c of 8 consecutive weights
-// (k = 8c .. 8c+7) is field s = c/2 of words 2(c%2) and 2(c%2)+1.  All
-// stores are 16 bytes wide.
+// bytes of bf16 A, or (digit_lo > 0) write the e4m3 digits hi = x >> 4 (16
+// bytes at A[i]) and lo = x & 15 (at A[digit_lo + i]) of 16 activations, so
+// that x = 16 hi + lo, in the K order of the expanded digit-form weights:
+// chunk j of a 64-wide block takes the activations 16g + 4j + b (g, b = 0..3)
+// of that block, as four words X_g of four, and places X_g byte b at chunk
+// byte 4o + i with b = 2 (o & 1) + (i >> 1), g = 2 (i & 1) + (o >> 1): the
+// byte permutes (X0, X2 | X1, X3 by 0x5140 | 0x7362).  In a packed block,
+// chunk c of 8 consecutive weights (k = 8c .. 8c+7) is field s = c/2 of words
+// 2(c%2) and 2(c%2)+1.  All stores are 16 bytes wide.
 __global__ void __launch_bounds__(256)
 k_prepass(const uint4* __restrict__ Wq, int64_t nblk, uint4* __restrict__ B,
           const uint4* __restrict__ xq, int64_t nx, uint4* __restrict__ A,
-          uint4* __restrict__ zero, int64_t nz) {
+          uint4* __restrict__ zero, int64_t nz, int64_t digit_lo, int64_t K) {
   const int64_t nb8 = 8 * nblk;
   const int64_t total = nb8 + nx + nz;
   for (int64_t it = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; it < total;
@@ -690,6 +831,20 @@ k_prepass(const uint4* __restrict__ Wq, int64_t nblk, uint4* __restrict__ B,
       B[it] = o;
     } else if (it >= nb8 + nx) {
       zero[it - nb8 - nx] = make_uint4(0, 0, 0, 0);  // split-K sums and tile counters
+    } else if (digit_lo > 0) {
+      const int64_t i = it - nb8;
+      const int64_t f = 16 * i, off = f % K;  // flat start, offset in its row
+      // word index of activation (f - off) + (off & ~63) + 4j, j = chunk in block
+      const uint32_t* xw = reinterpret_cast<const uint32_t*>(xq) + (f - off + (off & ~63ll)) / 4 +
+                           ((off >> 4) & 3);
+      const uint32_t X0 = xw[0], X1 = xw[4], X2 = xw[8], X3 = xw[12];
+      const uint32_t P[4] = {__byte_perm(X0, X2, 0x5140), __byte_perm(X0, X2, 0x7362),
+                             __byte_perm(X1, X3, 0x5140), __byte_perm(X1, X3, 0x7362)};
+      uint32_t hi[4], lo[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) digits4(P[q], hi[q], lo[q]);
+      A[i] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+      A[digit_lo + i] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
     } else {
       const int64_t i = it - nb8;
       const uint4 v = xq[i];
@@ -729,12 +884,13 @@ cudaError_t get_encode() {
   return cudaSuccess;
 }
 
-// Packed weights [N, K/4] bytes as a 2-D uint8 tensor, boxes of 16 bytes (64
-// weights) x box_rows, no swizzle.
-cudaError_t encode_packed(CUtensorMap* map, const void* Wq, int64_t N, int64_t K, int box_rows) {
+// Packed weights [N, K/4] bytes as a 2-D uint8 tensor, boxes of box_bytes
+// (16 or 32: 64 or 128 weights) x box_rows, no swizzle.
+cudaError_t encode_packed(CUtensorMap* map, const void* Wq, int64_t N, int64_t K, int box_bytes,
+                          int box_rows) {
   cuuint64_t dims[2] = {(cuuint64_t)(K / 4), (cuuint64_t)N};
   cuuint64_t strides[1] = {(cuuint64_t)(K / 4)};
-  cuuint32_t box[2] = {16u, (cuuint32_t)box_rows};
+  cuuint32_t box[2] = {(cuuint32_t)box_bytes, (cuuint32_t)box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(Wq), dims,
                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -767,6 +923,10 @@ size_t round1k(size_t v) { return (v + 1023) / 1024 * 1024; }
 // weight from HBM); large ones expand them once into a bf16 copy that stays
 // in L2 across the many output-tile rows.
 bool use_fused(int64_t M) { return M <= 256; }
+// The exact e4m3 digit form (two digit rows per token in one 128-row tile)
+// serves M <= 64 on the fused path: half the MMAs of the bf16 form and
+// 128-deep K stages.
+bool use_digits(int64_t M, int64_t K) { return M <= 64 && K >= 128; }
 
 // Tile N.  128-wide tiles fill the last wave of 148 SMs better for some
 // shapes, but they stream the bf16 A operand twice as often from L2; measured
@@ -795,7 +955,8 @@ WsLayout ws_layout(int64_t M, int64_t N, int64_t K) {
   const bool fused = use_fused(M);
   const int bn = fused ? 256 : pick_bn(N);
   const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + bn - 1) / bn);
-  const int k_stages = (int)((K + 63) / 64);
+  const int kstage = fused && use_digits(M, K) ? 128 : 64;
+  const int k_stages = (int)((K + kstage - 1) / kstage);
   int splits = 1;
   int64_t split_tiles = tiles;  // tiles that are split when splits > 1
   L.full_tiles = 0;
@@ -846,13 +1007,16 @@ cudaError_t launch_kind(const uint8_t* Wq, const float* w_scale, const int8_t* x
                                            reinterpret_cast<uint4*>(B),
                                            reinterpret_cast<const uint4*>(xq), nx,
                                            reinterpret_cast<uint4*>(A),
-                                           reinterpret_cast<uint4*>(w + L.acc), nz);
+                                           reinterpret_cast<uint4*>(w + L.acc), nz,
+                                           KIND == 2 ? nx : 0, K);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   CUtensorMap mapA, mapB;
-  e = encode_operand(&mapA, A, M, K, Kind<KIND>::kElem, kBM);
+  // digits: [2M, K] e4m3 (hi rows, then lo rows), 64-row boxes
+  e = KIND == 2 ? encode_operand(&mapA, A, 2 * M, K, 1, kDigitRows)
+                : encode_operand(&mapA, A, M, K, Kind<KIND>::kElem, kBM);
   if (e == cudaSuccess)
-    e = FUSED ? encode_packed(&mapB, Wq, N, K, BN)
+    e = FUSED ? encode_packed(&mapB, Wq, N, K, Kind<KIND>::kKStage / 4, BN)
               : encode_operand(&mapB, B, N, K, Kind<KIND>::kElem, BN);
   if (e != cudaSuccess) return e;
   Args a;
@@ -883,15 +1047,15 @@ cudaError_t launch_kind(const uint8_t* Wq, const float* w_scale, const int8_t* x
   if (dev < 64 && !configured[dev]) {
     e = cudaFuncSetAttribute(k_gemm_tc<KIND, BN, FUSED>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Tile<BN, FUSED>::kSmemBytes);
+                             Tile<BN, FUSED, false, KIND>::kSmemBytes);
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
   const int items = a.full_tiles + (a.m_tiles * a.n_tiles - a.full_tiles) * a.splits;
   const int ctas = items < 148 ? items : 148;
   return launch_pdl(k_gemm_tc<KIND, BN, FUSED>, dim3(ctas),
-                    dim3(FUSED ? kThreadsFused : kThreads), (size_t)Tile<BN, FUSED>::kSmemBytes, s,
-                    mapA, mapB, mapB, a);
+                    dim3(FUSED ? kThreadsFused : kThreads),
+                    (size_t)Tile<BN, FUSED, false, KIND>::kSmemBytes, s, mapA, mapB, mapB, a);
 }
 
 // The FFN's up and gate products in one GEMM (M > 256): both weight matrices
@@ -922,7 +1086,7 @@ cudaError_t launch_gated_t(const uint8_t* Wu, const float* su, const uint8_t* Wg
     k_prepass<<<(unsigned)grid, 256, 0, s>>>(
         reinterpret_cast<const uint4*>(pass == 0 ? Wu : Wg), nblk,
         reinterpret_cast<uint4*>(pass == 0 ? Bu : Bg), reinterpret_cast<const uint4*>(xq), n_x,
-        reinterpret_cast<uint4*>(A), nullptr, 0);
+        reinterpret_cast<uint4*>(A), nullptr, 0, 0, K);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -990,6 +1154,9 @@ cudaError_t launch_gemm_tc(const uint8_t* Wq, const float* w_scale, const int8_t
                            const float* x_scale, int64_t M, int64_t N, int64_t K, float* y,
                            uint16_t* y_bf16, int32_t* acc_out, void* ws, long long wait,
                            cudaStream_t s) {
+  if (use_fused(M) && use_digits(M, K))
+    return launch_kind<2, 256, true>(Wq, w_scale, xq, x_scale, M, N, K, y, y_bf16, acc_out, ws,
+                                     wait, s);
   if (use_fused(M))
     return launch_kind<kKind, 256, true>(Wq, w_scale, xq, x_scale, M, N, K, y, y_bf16, acc_out,
                                          ws, wait, s);

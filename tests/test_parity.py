@@ -153,7 +153,11 @@ LINEAR_SHAPES = [(1, 1, 64), (1, 7, 64), (2, 65, 192), (3, 640, 2560), (1, 2560,
                  (4, 100, 8192), (63, 96, 2560), (64, 33, 128), (65, 130, 640), (129, 64, 320),
                  (1, 31, 65536),
                  # tensor-core path with K split over several CTAs (few output tiles)
-                 (20, 300, 4096), (64, 33, 8192), (200, 777, 2048), (16, 2560, 4096)]
+                 (20, 300, 4096), (64, 33, 8192), (200, 777, 2048), (16, 2560, 4096),
+                 # e4m3 digit form (16 <= M <= 64, K >= 128): K a half stage past a
+                 # multiple of 128, ragged N, split K, and K = 64 (bf16 form)
+                 (24, 257, 320), (33, 2048, 192), (40, 1000, 1088), (48, 600, 6912),
+                 (16, 8, 64), (64, 4000, 2560)]
 
 
 @pytest.mark.parametrize("M,N,K", LINEAR_SHAPES)
@@ -185,6 +189,31 @@ def test_linear_extreme_accumulators():
     qx = np.full((1, K), -128, np.int8)
     y, acc = gpu_linear(oracle.pack(q), np.float32(1.0), qx, np.array([1.0], np.float32), K)
     assert acc.ravel().tolist() == [-128 * K, 128 * K]
+
+
+def test_linear_digit_form_extremes():
+    """Tokens at the ends of the int8 range (digits hi = -8, lo = 0 and hi = 7,
+    lo = 15) against all +1 / all -1 / alternating weights at K = 65536, and a
+    row whose sum first grows to 2^22 and then moves by single units: every
+    sum must stay exact in the binary32 accumulators of the e4m3 MMAs."""
+    K, M = 65536, 16
+    q = np.ones((3, K), np.int8)
+    q[1] = -1
+    q[2, 1::2] = -1
+    qx = np.random.default_rng(3).integers(-128, 128, (M, K)).astype(np.int8)
+    qx[0] = -128
+    qx[1] = 127
+    qx[2, : K // 2] = 127
+    qx[2, K // 2:] = 1
+    qx[3, : K // 2] = -128
+    qx[3, K // 2:] = np.where(np.arange(K // 2) % 3 == 0, 1, 0)
+    sx = np.ones(M, np.float32)
+    y, acc = gpu_linear(oracle.pack(q), np.float32(1.0), qx, sx, K)
+    y_o, acc_o = oracle.linear(oracle.pack(q), np.float32(1.0), qx, sx, K)
+    assert acc[0].tolist() == [-128 * K, 128 * K, 0]
+    assert acc[1].tolist() == [127 * K, -127 * K, 0]
+    assert_bits_equal(acc, acc_o, "acc")
+    assert_bits_equal(y, y_o, "y bits")
 
 
 @pytest.mark.parametrize("M", [1, 4, 16, 64])
