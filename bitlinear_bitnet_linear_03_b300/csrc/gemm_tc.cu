@@ -285,18 +285,27 @@ __device__ __forceinline__ float ld_cg_f32(const float* p) {
   asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(p) : "memory");
   return v;
 }
+__device__ __forceinline__ void ld_cg_f32x4(const float* p, float& a, float& b, float& c, float& d) {
+  asm volatile("ld.global.cg.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(a), "=f"(b), "=f"(c), "=f"(d)
+               : "l"(p)
+               : "memory");
+}
 // y = acc * c (binary32 and/or bf16) and the accumulators for 32 consecutive
-// outputs of one row.  vec4: the 32 outputs are in range and 16-byte aligned
-// as binary32; vec8: also as bf16.
+// outputs of one row.  f holds the accumulators as binary32: exact integers
+// below 2^24 in magnitude, so f + 0 (which turns a -0 sum into +0) is the
+// binary32 value of the integer, and y = (f + 0) * c is the rescale of it;
+// the int32 accumulators are formed only when asked for.  vec4: the 32
+// outputs are in range and 16-byte aligned as binary32; vec8: also as bf16.
 __device__ __forceinline__ void store_row32(float* yrow, uint16_t* brow, int32_t* arow, int nb,
-                                            const int (&v)[32], float c, bool vec4, bool vec8,
+                                            const float (&f)[32], float c, bool vec4, bool vec8,
                                             int N) {
   if (vec4) {
 #pragma unroll
     for (int j = 0; j < 32; j += 8) {
       float o[8];
 #pragma unroll
-      for (int t = 0; t < 8; ++t) o[t] = __fmul_rn(__int2float_rn(v[j + t]), c);
+      for (int t = 0; t < 8; ++t) o[t] = __fmul_rn(__fadd_rn(f[j + t], 0.0f), c);
       if (yrow) {
         *reinterpret_cast<float4*>(yrow + nb + j) = make_float4(o[0], o[1], o[2], o[3]);
         *reinterpret_cast<float4*>(yrow + nb + j + 4) = make_float4(o[4], o[5], o[6], o[7]);
@@ -314,19 +323,22 @@ __device__ __forceinline__ void store_row32(float* yrow, uint16_t* brow, int32_t
         }
       }
       if (arow) {
-        *reinterpret_cast<int4*>(arow + nb + j) = make_int4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+        *reinterpret_cast<int4*>(arow + nb + j) =
+            make_int4(__float2int_rn(f[j]), __float2int_rn(f[j + 1]), __float2int_rn(f[j + 2]),
+                      __float2int_rn(f[j + 3]));
         *reinterpret_cast<int4*>(arow + nb + j + 4) =
-            make_int4(v[j + 4], v[j + 5], v[j + 6], v[j + 7]);
+            make_int4(__float2int_rn(f[j + 4]), __float2int_rn(f[j + 5]),
+                      __float2int_rn(f[j + 6]), __float2int_rn(f[j + 7]));
       }
     }
   } else {
 #pragma unroll
     for (int j = 0; j < 32; ++j)
       if (nb + j < N) {
-        const float o = __fmul_rn(__int2float_rn(v[j]), c);
+        const float o = __fmul_rn(__fadd_rn(f[j], 0.0f), c);
         if (yrow) yrow[nb + j] = o;
         if (brow) brow[nb + j] = f32_to_bf16_rn(o);
-        if (arow) arow[nb + j] = v[j];
+        if (arow) arow[nb + j] = __float2int_rn(f[j]);
       }
   }
 }
@@ -718,10 +730,11 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUte
           }
           epi_sync();
           if (row < kDigitRows) {
+            // 16 D[m] + D[64 + m]: integers below 2^24, so the fused
+            // multiply-add is exact
 #pragma unroll
             for (int j = 0; j < 32; ++j)
-              r[j] = __float_as_uint(__int2float_rn(16 * __float2int_rn(__uint_as_float(r[j])) +
-                                                    __float2int_rn(xb[j])));
+              r[j] = __float_as_uint(__fmaf_rn(16.0f, __uint_as_float(r[j]), xb[j]));
           }
           epi_sync();
         }
@@ -741,11 +754,10 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUte
           }
           continue;
         }
-        int v[32];
+        float f[32];
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-          v[j] = __float2int_rn(__uint_as_float(r[j]));  // exact integer
-        store_row32(yrow, brow, arow, nb, v, c, vec && nb + 32 <= a.N, vec8, a.N);
+        for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(r[j]);  // exact integers
+        store_row32(yrow, brow, arow, nb, f, c, vec && nb + 32 <= a.N, vec8, a.N);
       }
       tc_fence_before();
       __syncwarp();
@@ -762,11 +774,15 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUte
             for (int cb = 0; cb < BN; cb += 32) {
               const int nb = n0 + cb;
               if (nb >= a.N) break;
-              int v[32];
+              float f[32];
+              if (vec && nb + 32 <= a.N) {
 #pragma unroll
-              for (int j = 0; j < 32; ++j)
-                v[j] = nb + j < a.N ? __float2int_rn(ld_cg_f32(wrow + nb + j)) : 0;
-              store_row32(yrow, brow, arow, nb, v, c, vec && nb + 32 <= a.N, vec8, a.N);
+                for (int j = 0; j < 32; j += 4) ld_cg_f32x4(wrow + nb + j, f[j], f[j + 1], f[j + 2], f[j + 3]);
+              } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) f[j] = nb + j < a.N ? ld_cg_f32(wrow + nb + j) : 0.0f;
+              }
+              store_row32(yrow, brow, arow, nb, f, c, vec && nb + 32 <= a.N, vec8, a.N);
             }
         }
       }
