@@ -459,6 +459,28 @@ def secondary_measurements(torch, bn, peaks, only=None, cpu=True):
                 "entry": entry}
         del sets
 
+    # 2B-class shapes at small M (the tensor-core path: the e4m3 digit form
+    # for 16 <= M <= 64), each timed as a graph of calls over weight sets
+    # that exceed L2.
+    for (N, K) in ([(2560, 2560), (6912, 2560), (2560, 6912)] if want("fused_small_m") else []):
+        nset = min(80, max(3, int(3 * 126e6 / (N * K / 4)) + 1))
+        sets = _weight_sets(torch, bn, synth, N, K, nset, 700)
+        for M in (16, 64):
+            xq, sx = bn.bitnet_quantize_act(synth.tokens_bf16(M, K, seed=701, outlier_frac=0.01,
+                                                              device="cuda"))
+            y = torch.empty((M, N), dtype=torch.float32, device=dev)
+            ws = torch.empty(max(bn.bitnet_linear_workspace(M, N, K), 16), dtype=torch.uint8,
+                             device=dev)
+            t = _time_calls(torch, lambda i: bn.bitnet_linear(sets[i % nset][0], sets[i % nset][1],
+                                                              xq, sx, y=y, ws=ws), 4 * nset,
+                            graph=True)
+            byts = N * K // 4 + M * K + 4 * M * N + 4 * M + 4
+            out[f"2b_M{M}_K{K}_N{N}"] = {
+                "us": round(t * 1e6, 1), "GBps": round(byts / t / 1e9, 1),
+                "tops": round(2 * M * N * K / t / 1e12, 2), "roofline": hbm_roof(byts / t / 1e9),
+                "entry": "bitnet_linear"}
+        del sets
+
     # 100B-class layers through the decode chain: 16 independent phases per
     # launch (each its own bf16 input and output), cycling over 4 weight sets
     # (235 MB, so every phase streams its weights from HBM); the weight stream

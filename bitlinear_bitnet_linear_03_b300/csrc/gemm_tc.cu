@@ -9,19 +9,24 @@
 // exact in bf16 (integers of magnitude <= 256), every product is exact, and
 // every partial sum is an integer of magnitude <= 128 K < 2^24 for
 // K <= 65536, so the binary32 accumulator is exact and independent of the
-// order of the additions; the epilogue converts it back to int32 without
-// rounding.
+// order of the additions; the epilogue rescales that binary32 integer
+// directly (and forms int32 only for the optional accumulator output).
+// For 16 <= M <= 64 the exact e4m3 digit form (kind::f8f6f4) replaces bf16:
+// x = 16 hi + lo with hi in [-8, 7] and lo in [0, 15], each token's two
+// digit rows stacked in one 128-row A tile, so one MMA covers 32 K instead
+// of 16 (Kind<2> below).
 //
 // Pipeline (one CTA per SM, persistent over work items of 128 x BN output
 // tiles, BN = 256, or 128 for narrow N):
-//  * M <= 256 (fused): the TMA brings the A tile (bf16) and the packed 2-bit
-//    codes of the B tile (16 bytes per row per stage); four converter warps
-//    expand the codes into the 128-byte-swizzled bf16 B tile in shared memory
-//    (one multiply-add and two byte permutes per four weights) and signal the
-//    MMA.  When the output has fewer tiles than half the SMs, K is split over
-//    CTAs: each split adds its exact partial sums into a zeroed fp32
-//    workspace (red.global.add.v4.f32; all values are integers below 2^24)
-//    and the last split of a tile to finish writes the outputs;
+//  * M <= 256 (fused): the TMA brings the A tile (bf16, or e4m3 digits) and
+//    the packed 2-bit codes of the B tile (16 or 32 bytes per row per
+//    stage); four converter warps expand the codes into the
+//    128-byte-swizzled B tile in shared memory (bf16: one multiply-add and
+//    two byte permutes per four weights; e4m3: one byte permute per four)
+//    and signal the MMA.  When the output has fewer tiles than half the SMs,
+//    K is split over CTAs: each split adds its exact partial sums into a
+//    zeroed fp32 workspace (red.global.add.v4.f32; all values are integers
+//    below 2^24) and the last split of a tile to finish writes the outputs;
 //  * M > 256: pre-pass kernels expand the packed weights once per call into
 //    a K-major bf16 operand B [N, K] and the int8 activations into A [M, K]
 //    bf16, both in the workspace (and largely in L2 during the GEMM);
@@ -280,17 +285,6 @@ __device__ __forceinline__ void red_add_v4(float* p, uint32_t a, uint32_t b, uin
                "f"(__uint_as_float(b)), "f"(__uint_as_float(c)), "f"(__uint_as_float(d))
                : "memory");
 }
-__device__ __forceinline__ float ld_cg_f32(const float* p) {
-  float v;
-  asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(p) : "memory");
-  return v;
-}
-__device__ __forceinline__ void ld_cg_f32x4(const float* p, float& a, float& b, float& c, float& d) {
-  asm volatile("ld.global.cg.v4.f32 {%0, %1, %2, %3}, [%4];"
-               : "=f"(a), "=f"(b), "=f"(c), "=f"(d)
-               : "l"(p)
-               : "memory");
-}
 // y = acc * c (binary32 and/or bf16) and the accumulators for 32 consecutive
 // outputs of one row.  f holds the accumulators as binary32: exact integers
 // below 2^24 in magnitude, so f + 0 (which turns a -0 sum into +0) is the
@@ -477,6 +471,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUte
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int items = item_count(a);
   __shared__ int s_last;
+  __shared__ float s_rowscale[kBM];  // split K: the last split's row scales
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -770,20 +765,69 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUte
         epi_sync();
         if (s_last) {
           __threadfence();
-          if (mrow)
-            for (int cb = 0; cb < BN; cb += 32) {
-              const int nb = n0 + cb;
-              if (nb >= a.N) break;
-              float f[32];
-              if (vec && nb + 32 <= a.N) {
+          // The 128 epilogue threads sweep the tile's sums together, four
+          // columns per step (16-byte loads and stores when N % 4 == 0), eight
+          // steps' loads in flight per thread; the rows' scales are staged in
+          // shared memory first.
+          const int et = threadIdx.x - 64;  // epilogue warps 2-5
+          const int rows = min(kBM, a.M - m0), cols = min(BN, a.N - n0);
+          const int g4 = (cols + 3) >> 2, total = rows * g4;
+          if (et < rows) s_rowscale[et] = __fmul_rn(a.x_scale[m0 + et], ws);
+          epi_sync();
+          for (int i0 = et; i0 < total; i0 += 128 * 8) {
+            float4 v[8];
 #pragma unroll
-                for (int j = 0; j < 32; j += 4) ld_cg_f32x4(wrow + nb + j, f[j], f[j + 1], f[j + 2], f[j + 3]);
+            for (int u = 0; u < 8; ++u) {
+              const int i = i0 + 128 * u;
+              v[u] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+              if (i < total) {
+                const int rr = i / g4, cc = (i - rr * g4) * 4;
+                const float* src = a.full_tiles > 0
+                                       ? a.acc_ws + ((int64_t)(t - a.full_tiles) * kBM + rr) * BN + cc
+                                       : a.acc_ws + (int64_t)(m0 + rr) * a.N + n0 + cc;
+                if (vec) {
+                  v[u] = __ldcg(reinterpret_cast<const float4*>(src));
+                } else {
+                  v[u].x = __ldcg(src);
+                  if (n0 + cc + 1 < a.N) v[u].y = __ldcg(src + 1);
+                  if (n0 + cc + 2 < a.N) v[u].z = __ldcg(src + 2);
+                  if (n0 + cc + 3 < a.N) v[u].w = __ldcg(src + 3);
+                }
+              }
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const int i = i0 + 128 * u;
+              if (i >= total) break;
+              const int rr = i / g4, cc = (i - rr * g4) * 4;
+              const int mm = m0 + rr, n = n0 + cc;
+              const float cm = s_rowscale[rr];
+              const float f[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+              float o[4];
+#pragma unroll
+              for (int j = 0; j < 4; ++j) o[j] = __fmul_rn(__fadd_rn(f[j], 0.0f), cm);
+              const int64_t off = (int64_t)mm * a.N + n;
+              if (vec) {
+                if (a.y) *reinterpret_cast<float4*>(a.y + off) = make_float4(o[0], o[1], o[2], o[3]);
+                if (a.y_bf16)
+                  *reinterpret_cast<uint2*>(a.y_bf16 + off) =
+                      make_uint2((uint32_t)f32_to_bf16_rn(o[0]) | ((uint32_t)f32_to_bf16_rn(o[1]) << 16),
+                                 (uint32_t)f32_to_bf16_rn(o[2]) | ((uint32_t)f32_to_bf16_rn(o[3]) << 16));
+                if (a.acc_out)
+                  *reinterpret_cast<int4*>(a.acc_out + off) =
+                      make_int4(__float2int_rn(f[0]), __float2int_rn(f[1]), __float2int_rn(f[2]),
+                                __float2int_rn(f[3]));
               } else {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) f[j] = nb + j < a.N ? ld_cg_f32(wrow + nb + j) : 0.0f;
+                for (int j = 0; j < 4; ++j)
+                  if (n + j < a.N) {
+                    if (a.y) a.y[off + j] = o[j];
+                    if (a.y_bf16) a.y_bf16[off + j] = f32_to_bf16_rn(o[j]);
+                    if (a.acc_out) a.acc_out[off + j] = __float2int_rn(f[j]);
+                  }
               }
-              store_row32(yrow, brow, arow, nb, f, c, vec && nb + 32 <= a.N, vec8, a.N);
             }
+          }
         }
       }
     }
@@ -953,8 +997,8 @@ int pick_bn(int64_t N) { return N <= 128 ? 128 : 256; }
 // Workspace of one call: [B bf16 N x K (unfused only)] [A bf16 M x K]
 // [split-K sums] [tile counters], each 1 KB aligned.  Split K:
 //  * fused path, when the output has fewer tiles than half the SMs: every
-//    tile, in as many splits as fill the SMs (each at least 16 K stages);
-//    sums M x N fp32;
+//    tile, in as many splits as fill the SMs (each at least 16 K stages of
+//    64, or 4 of 128 in the digit form); sums M x N fp32;
 //  * unfused path, when the output is at most three waves of whole tiles
 //    plus a last wave that would fill less than half the SMs: only that
 //    wave's tiles, in as many splits as fill the SMs (each at least 16 K
@@ -971,14 +1015,18 @@ WsLayout ws_layout(int64_t M, int64_t N, int64_t K) {
   const bool fused = use_fused(M);
   const int bn = fused ? 256 : pick_bn(N);
   const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + bn - 1) / bn);
-  const int kstage = fused && use_digits(M, K) ? 128 : 64;
-  const int k_stages = (int)((K + kstage - 1) / kstage);
+  const bool digits = fused && use_digits(M, K);
+  const int k_stages = (int)((K + (digits ? 127 : 63)) / (digits ? 128 : 64));
+  // fewest K stages per split: 4 (512 K) in the digit form, 16 (1024 K) in
+  // bf16; measured on B300 (digit form, N x K = 2560 x 2560 .. 2560 x 6912,
+  // M = 16 / 64): 4 stages 13-15 / 22-23 us, 16 stages 19-22 / 22-30 us
+  const int min_split_stages = digits ? 4 : 16;
   int splits = 1;
   int64_t split_tiles = tiles;  // tiles that are split when splits > 1
   L.full_tiles = 0;
   if (fused && tiles < 74) {
     splits = (int)(148 / tiles);
-    if (splits > k_stages / 16) splits = k_stages / 16;
+    if (splits > k_stages / min_split_stages) splits = k_stages / min_split_stages;
     if (splits < 1) splits = 1;
   } else if (!fused && tiles > 148 && tiles < 4 * 148 && tiles % 148 < 74) {
     const int64_t rem = tiles % 148;
