@@ -11,10 +11,15 @@
 // K <= 65536, so the binary32 accumulator is exact and independent of the
 // order of the additions; the epilogue rescales that binary32 integer
 // directly (and forms int32 only for the optional accumulator output).
-// For 16 <= M <= 64 the exact e4m3 digit form (kind::f8f6f4) replaces bf16:
-// x = 16 hi + lo with hi in [-8, 7] and lo in [0, 15], each token's two
-// digit rows stacked in one 128-row A tile, so one MMA covers 32 K instead
-// of 16 (Kind<2> below).
+// The exact e4m3 digit form (kind::f8f6f4) replaces bf16 wherever K >= 128
+// and M is not in 65..256: x = 16 hi + lo with hi in [-8, 7] and lo in
+// [0, 15], both exact in e4m3, as are the ternary weights.
+//  * 16 <= M <= 64 (Kind<2>): each token's two digit rows are stacked in
+//    one 128-row A tile, so one MMA covers 32 K instead of 16;
+//  * M > 256 (Kind<4>): the digits hi' = 16 hi and lo are two A tiles of the
+//    same tokens, both multiplied into one accumulator.  The tensor time
+//    equals bf16's, and the operands of a 128 x 256 tile move 64 KB per 128
+//    K instead of 96 KB (prefill is bound by L2 -> SM traffic).
 //
 // Pipeline (one CTA per SM, persistent over work items of 128 x BN output
 // tiles, BN = 256, or 128 for narrow N):
@@ -27,9 +32,10 @@
 //    K is split over CTAs: each split adds its exact partial sums into a
 //    zeroed fp32 workspace (red.global.add.v4.f32; all values are integers
 //    below 2^24) and the last split of a tile to finish writes the outputs;
-//  * M > 256: pre-pass kernels expand the packed weights once per call into
-//    a K-major bf16 operand B [N, K] and the int8 activations into A [M, K]
-//    bf16, both in the workspace (and largely in L2 during the GEMM);
+//  * M > 256: a pre-pass expands the packed weights once per call into a
+//    K-major e4m3 operand B [N, K] and the int8 activations into the digit
+//    operand A [2M, K] (hi' rows, then lo rows), both in the workspace and
+//    largely in L2 during the GEMM (bf16 copies when K < 128);
 //  * warp 0, one lane: TMA (cp.async.bulk.tensor.2d, 128-byte swizzle) loads
 //    the tiles of each 128-byte K step into a 192 KB ring;
 //  * warp 1: allocates 512 TMEM columns (two 256-column fp32
@@ -76,13 +82,16 @@ template <int BN, bool FUSED = false, bool GATED = false, int KIND = 1>
 struct Tile {
   static constexpr int kBTileBytes = BN * kRowBytes;
   static constexpr int kPackedBytes = FUSED ? BN * (KIND == 2 ? 32 : 16) : 0;
+  // A bytes per stage: one 128-row tile, two for the prefill digit form
+  // (KIND 4: 16 hi and lo digit tiles of the same tokens)
+  static constexpr int kABytes = KIND == 4 ? 2 * kATileBytes : kATileBytes;
   static constexpr int kStageBytes =
-      kATileBytes + (FUSED ? kPackedBytes : (GATED ? 2 : 1) * kBTileBytes);
+      kABytes + (FUSED ? kPackedBytes : (GATED ? 2 : 1) * kBTileBytes);
   // expanded B buffers: two (bf16), three (digits: expansion runs on while
   // the MMAs of the two previous stages are in flight)
   static constexpr int kNB = KIND == 2 ? 3 : 2;
   static constexpr int kBBufBytes = FUSED ? kNB * kBTileBytes : 0;
-  static constexpr int kStages = (kRingBytes - kBBufBytes) / kStageBytes;  // 4, 6 fused, 4 digits
+  static constexpr int kStages = (kRingBytes - kBBufBytes) / kStageBytes;  // 4, 6 fused, 4 digits, 3 prefill digits
   static_assert(!FUSED || kStages > kNB, "a ring slot is reused only after its B buffer");
   static constexpr int kSmemBytes = kStages * kStageBytes + kBBufBytes + 1024;  // + alignment
 };
@@ -122,6 +131,12 @@ struct Kind<2> {
   template <int BN>
   static constexpr uint32_t idesc() { return kIdescBase | ((uint32_t)(BN >> 3) << 17); }
 };
+// The prefill digit form (M > 256): the same e4m3 operands, with the A digits
+// hi' = 16 (x >> 4) in [-128, 112] and lo = x & 15 as two 128-row tiles of the
+// same tokens, both multiplied into one accumulator, so that it holds
+// sum (16 hi + lo) q = sum x q exactly (|partial sums| <= 128 K < 2^24).
+template <>
+struct Kind<4> : Kind<2> {};
 // Every tcgen05.mma consumes 32 bytes of K per row (16 bf16 or 32 e4m3).
 constexpr int kMmaKBytes = 32;
 // Digit rows: the lo digits of token m sit in A-tile row kDigitRows + m.
@@ -225,7 +240,7 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
 template <int KIND, int BN>
 __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
                                        uint32_t accumulate) {
-  if (KIND == 2)
+  if (KIND == 2 || KIND == 4)
     asm volatile(
         "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
         " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
@@ -446,7 +461,8 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUte
           const __grid_constant__ CUtensorMap mapB2, const __grid_constant__ Args a) {
   static_assert(!(GATED && FUSED), "the gated form reads expanded bf16 weights");
   static_assert(!GATED || 4 * BN <= (int)kTmemCols, "two accumulators per tile, double buffered");
-  static_assert(KIND == 1 || (FUSED && !GATED), "the digit form is fused only");
+  static_assert(KIND == 1 || (KIND == 2 && FUSED && !GATED) || (KIND == 4 && !FUSED),
+                "digit forms: fused (2) or unfused (4)");
   extern __shared__ uint8_t smem_raw[];
   using T = Tile<BN, FUSED, GATED, KIND>;
   constexpr int kStages = T::kStages;
@@ -541,11 +557,15 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUte
             }
             tma_load_2d(sa + kATileBytes, &mapB, ks * kPackedX, n0, fb);
           } else {
+            // prefill digits: the operand is [2M, K] (hi' rows, then lo
+            // rows); the hi' box's rows past M and the lo box's rows past
+            // 2M only feed outputs that are never stored
             mbar_expect_tx(fb, kStageBytes);
             tma_load_2d(sa, &mapA, ks * Kind<KIND>::kKStage, m0, fb);
-            tma_load_2d(sa + kATileBytes, &mapB, ks * Kind<KIND>::kKStage, n0, fb);
+            if (KIND == 4) tma_load_2d(sa + kATileBytes, &mapA, ks * Kind<KIND>::kKStage, a.M + m0, fb);
+            tma_load_2d(sa + T::kABytes, &mapB, ks * Kind<KIND>::kKStage, n0, fb);
             if (GATED)
-              tma_load_2d(sa + kATileBytes + kBTileBytesT, &mapB2, ks * Kind<KIND>::kKStage, n0, fb);
+              tma_load_2d(sa + T::kABytes + kBTileBytesT, &mapB2, ks * Kind<KIND>::kKStage, n0, fb);
           }
           issued = it + 1;
         }
@@ -589,15 +609,19 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUte
           }
           tc_fence_after();
           const uint32_t sa = smem0 + s * kStageBytes;
-          const uint32_t sb = FUSED ? bbuf0 + b * kBTileBytesT : sa + kATileBytes;
+          const uint32_t sb = FUSED ? bbuf0 + b * kBTileBytesT : sa + T::kABytes;
 #pragma unroll
           for (int kk = 0; kk < kRowBytes / kMmaKBytes; ++kk) {
             const uint64_t ad = sw128_desc(sa + kk * kMmaKBytes);
             const uint64_t bd = sw128_desc(sb + kk * kMmaKBytes);
             tc_mma<KIND, BN>(d, ad, bd, (ks != ks0 || kk != 0) ? 1u : 0u);
+            if (KIND == 4) tc_mma<KIND, BN>(d, sw128_desc(sa + kATileBytes + kk * kMmaKBytes), bd, 1u);
             if (GATED) {
               const uint64_t bd2 = sw128_desc(sb + kBTileBytesT + kk * kMmaKBytes);
               tc_mma<KIND, BN>(d + (uint32_t)BN, ad, bd2, (ks != ks0 || kk != 0) ? 1u : 0u);
+              if (KIND == 4)
+                tc_mma<KIND, BN>(d + (uint32_t)BN, sw128_desc(sa + kATileBytes + kk * kMmaKBytes),
+                                 bd2, 1u);
             }
           }
           // frees the stage, and (fused) the expanded B buffer, when these
@@ -850,64 +874,106 @@ __device__ __forceinline__ uint32_t e4m3x2_of(int a0, int a1) {
       "f"(__int2float_rn(a0)));
   return d;
 }
-// The e4m3 digits hi = x >> 4 and lo = x & 15 of the four int8 values in w.
-__device__ __forceinline__ void digits4(uint32_t w, uint32_t& hi, uint32_t& lo) {
+// The e4m3 digits hi = (x >> 4) * hs (hs = 1 or 16) and lo = x & 15 of the
+// four int8 values in w.
+__device__ __forceinline__ void digits4(uint32_t w, int hs, uint32_t& hi, uint32_t& lo) {
   int x[4];
 #pragma unroll
   for (int b = 0; b < 4; ++b) x[b] = (int)(int8_t)(w >> (8 * b));
-  hi = e4m3x2_of(x[0] >> 4, x[1] >> 4) | (e4m3x2_of(x[2] >> 4, x[3] >> 4) << 16);
+  hi = e4m3x2_of((x[0] >> 4) * hs, (x[1] >> 4) * hs) |
+       (e4m3x2_of((x[2] >> 4) * hs, (x[3] >> 4) * hs) << 16);
   lo = e4m3x2_of(x[0] & 15, x[1] & 15) | (e4m3x2_of(x[2] & 15, x[3] & 15) << 16);
 }
+// Four e4m3 weights (one word, in order) from the four 2-bit codes in bits
+// 0-1 of the bytes of v (higher bits ignored): code 0, 1, 2 -> q = -1, 0,
+// +1 -> 0xB8, 0x00, 0x38.  Bit 0 of a code is clear exactly when q != 0, and
+// both bits are clear exactly when q = -1.
+__device__ __forceinline__ uint32_t e4m3x4_from_codes(uint32_t v) {
+  const uint32_t nz = ~v & 0x01010101u;
+  const uint32_t neg = ~(v | (v >> 1)) & 0x01010101u;
+  return nz * 0x38u + (neg << 7);
+}
 
-// ---- pre-pass kernels
-// Pre-pass, one launch (items [nblk + nx, + nz) zero 16 bytes of the split-K
-// workspace each): items [0, 8 nblk) write one 16-byte chunk of bf16 B each
-// (chunk c of packed block it / 8, so consecutive threads write consecutive
-// chunks); items [8 nblk, 8 nblk + nx) widen 16 int8 activations into 32
-// bytes of bf16 A, or (digit_lo > 0) write the e4m3 digits hi = x >> 4 (16
-// bytes at A[i]) and lo = x & 15 (at A[digit_lo + i]) of 16 activations, so
-// that x = 16 hi + lo, in the K order of the expanded digit-form weights:
-// chunk j of a 64-wide block takes the activations 16g + 4j + b (g, b = 0..3)
-// of that block, as four words X_g of four, and places X_g byte b at chunk
-// byte 4o + i with b = 2 (o & 1) + (i >> 1), g = 2 (i & 1) + (o >> 1): the
-// byte permutes (X0, X2 | X1, X3 by 0x5140 | 0x7362).  In a packed block,
-// chunk c of 8 consecutive weights (k = 8c .. 8c+7) is field s = c/2 of words
-// 2(c%2) and 2(c%2)+1.  All stores are 16 bytes wide.
-__global__ void __launch_bounds__(256)
-k_prepass(const uint4* __restrict__ Wq, int64_t nblk, uint4* __restrict__ B,
-          const uint4* __restrict__ xq, int64_t nx, uint4* __restrict__ A,
-          uint4* __restrict__ zero, int64_t nz, int64_t digit_lo, int64_t K) {
-  const int64_t nb8 = 8 * nblk;
-  const int64_t total = nb8 + nx + nz;
+// ---- pre-pass kernel
+// One launch.  Items, in order:
+//  * B (nblk packed 64-weight blocks): bf16 mode, eight 16-byte chunks of 8
+//    weights per block (chunk c = field c/2 of words 2(c%2), 2(c%2)+1); e4m3
+//    mode, four 16-byte chunks of 16 weights (chunk c = field c of the
+//    block's 16 bytes, in byte order).  Consecutive threads write
+//    consecutive chunks.
+//  * A (nx groups of 16 int8 activations):
+//    - kABf16: 32 bytes of bf16;
+//    - kADigitsFused: the e4m3 digits hi = x >> 4 (16 bytes at A[i]) and
+//      lo = x & 15 (at A[digit_lo + i]), x = 16 hi + lo, in the K order of
+//      the on-chip e4m3 expansion: chunk j of a 64-wide block takes the
+//      activations 16g + 4j + b (g, b = 0..3) of that block, as four words
+//      X_g of four, and places X_g byte b at chunk byte 4o + i with
+//      b = 2 (o & 1) + (i >> 1), g = 2 (i & 1) + (o >> 1): the byte permutes
+//      (X0, X2 | X1, X3 by 0x5140 | 0x7362);
+//    - kADigitsPrefill: hi' = 16 (x >> 4) and lo = x & 15, in K order.
+//  * nz 16-byte zero stores (split-K sums and tile counters).
+enum AMode { kABf16 = 0, kADigitsFused = 1, kADigitsPrefill = 2 };
+struct Prep {
+  const uint4* Wq;
+  int64_t nblk;
+  uint4* B;
+  int b_e4m3;
+  const uint4* xq;
+  int64_t nx;
+  uint4* A;
+  int a_mode;
+  int64_t digit_lo, K;
+  uint4* zero;
+  int64_t nz;
+};
+__global__ void __launch_bounds__(256) k_prepass(const Prep p) {
+  const int64_t nbi = (p.b_e4m3 ? 4 : 8) * p.nblk;
+  const int64_t total = nbi + p.nx + p.nz;
   for (int64_t it = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; it < total;
        it += (int64_t)gridDim.x * blockDim.x) {
-    if (it < nb8) {
-      const uint4 w = Wq[it >> 3];  // the 8 threads of a block share this load
-      const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-      const int c = (int)(it & 7), sft = 2 * (c >> 1), h = c & 1;
-      uint4 o;
-      bf16x4_from_codes((ww[2 * h] >> sft) & 0x03030303u, o.x, o.y);
-      bf16x4_from_codes((ww[2 * h + 1] >> sft) & 0x03030303u, o.z, o.w);
-      B[it] = o;
-    } else if (it >= nb8 + nx) {
-      zero[it - nb8 - nx] = make_uint4(0, 0, 0, 0);  // split-K sums and tile counters
-    } else if (digit_lo > 0) {
-      const int64_t i = it - nb8;
-      const int64_t f = 16 * i, off = f % K;  // flat start, offset in its row
+    if (it < nbi) {
+      if (p.b_e4m3) {
+        const uint4 w = p.Wq[it >> 2];  // the 4 threads of a block share this load
+        const int sft = 2 * (int)(it & 3);
+        p.B[it] = make_uint4(e4m3x4_from_codes(w.x >> sft), e4m3x4_from_codes(w.y >> sft),
+                             e4m3x4_from_codes(w.z >> sft), e4m3x4_from_codes(w.w >> sft));
+      } else {
+        const uint4 w = p.Wq[it >> 3];  // the 8 threads of a block share this load
+        const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+        const int c = (int)(it & 7), sft = 2 * (c >> 1), h = c & 1;
+        uint4 o;
+        bf16x4_from_codes((ww[2 * h] >> sft) & 0x03030303u, o.x, o.y);
+        bf16x4_from_codes((ww[2 * h + 1] >> sft) & 0x03030303u, o.z, o.w);
+        p.B[it] = o;
+      }
+    } else if (it >= nbi + p.nx) {
+      p.zero[it - nbi - p.nx] = make_uint4(0, 0, 0, 0);
+    } else if (p.a_mode == kADigitsFused) {
+      const int64_t i = it - nbi;
+      const int64_t f = 16 * i, off = f % p.K;  // flat start, offset in its row
       // word index of activation (f - off) + (off & ~63) + 4j, j = chunk in block
-      const uint32_t* xw = reinterpret_cast<const uint32_t*>(xq) + (f - off + (off & ~63ll)) / 4 +
-                           ((off >> 4) & 3);
+      const uint32_t* xw = reinterpret_cast<const uint32_t*>(p.xq) +
+                           (f - off + (off & ~63ll)) / 4 + ((off >> 4) & 3);
       const uint32_t X0 = xw[0], X1 = xw[4], X2 = xw[8], X3 = xw[12];
       const uint32_t P[4] = {__byte_perm(X0, X2, 0x5140), __byte_perm(X0, X2, 0x7362),
                              __byte_perm(X1, X3, 0x5140), __byte_perm(X1, X3, 0x7362)};
       uint32_t hi[4], lo[4];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) digits4(P[q], hi[q], lo[q]);
-      A[i] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-      A[digit_lo + i] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+      for (int q = 0; q < 4; ++q) digits4(P[q], 1, hi[q], lo[q]);
+      p.A[i] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+      p.A[p.digit_lo + i] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    } else if (p.a_mode == kADigitsPrefill) {
+      const int64_t i = it - nbi;
+      const uint4 v = p.xq[i];
+      const uint32_t vv[4] = {v.x, v.y, v.z, v.w};
+      uint32_t hi[4], lo[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) digits4(vv[q], 16, hi[q], lo[q]);
+      p.A[i] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+      p.A[p.digit_lo + i] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
     } else {
-      const int64_t i = it - nb8;
-      const uint4 v = xq[i];
+      const int64_t i = it - nbi;
+      const uint4 v = p.xq[i];
       const uint32_t vv[4] = {v.x, v.y, v.z, v.w};
       uint32_t h[8];
 #pragma unroll
@@ -921,8 +987,8 @@ k_prepass(const uint4* __restrict__ Wq, int64_t nblk, uint4* __restrict__ B,
         h[2 * q] = b0 | (b1 << 16);
         h[2 * q + 1] = b2 | (b3 << 16);
       }
-      A[2 * i] = make_uint4(h[0], h[1], h[2], h[3]);
-      A[2 * i + 1] = make_uint4(h[4], h[5], h[6], h[7]);
+      p.A[2 * i] = make_uint4(h[0], h[1], h[2], h[3]);
+      p.A[2 * i + 1] = make_uint4(h[4], h[5], h[6], h[7]);
     }
   }
 }
@@ -987,6 +1053,10 @@ bool use_fused(int64_t M) { return M <= 256; }
 // serves M <= 64 on the fused path: half the MMAs of the bf16 form and
 // 128-deep K stages.
 bool use_digits(int64_t M, int64_t K) { return M <= 64 && K >= 128; }
+// The prefill digit form (M > 256): e4m3 weights and the two digit tiles of
+// the activations move 64 KB per 128-deep K step of a 128 x 256 tile, where
+// bf16 moves 96 KB, at the same tensor time.
+bool use_prefill_digits(int64_t M, int64_t K) { return M > 256 && K >= 128; }
 
 // Tile N.  128-wide tiles fill the last wave of 148 SMs better for some
 // shapes, but they stream the bf16 A operand twice as often from L2; measured
@@ -1016,7 +1086,8 @@ WsLayout ws_layout(int64_t M, int64_t N, int64_t K) {
   const int bn = fused ? 256 : pick_bn(N);
   const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + bn - 1) / bn);
   const bool digits = fused && use_digits(M, K);
-  const int k_stages = (int)((K + (digits ? 127 : 63)) / (digits ? 128 : 64));
+  const bool pdigits = !fused && use_prefill_digits(M, K);
+  const int k_stages = (int)((K + (digits || pdigits ? 127 : 63)) / (digits || pdigits ? 128 : 64));
   // fewest K stages per split: 4 (512 K) in the digit form, 16 (1024 K) in
   // bf16; measured on B300 (digit form, N x K = 2560 x 2560 .. 2560 x 6912,
   // M = 16 / 64): 4 stages 13-15 / 22-23 us, 16 stages 19-22 / 22-30 us
@@ -1030,8 +1101,9 @@ WsLayout ws_layout(int64_t M, int64_t N, int64_t K) {
     if (splits < 1) splits = 1;
   } else if (!fused && tiles > 148 && tiles < 4 * 148 && tiles % 148 < 74) {
     const int64_t rem = tiles % 148;
+    const int min_stages = pdigits ? 8 : 16;  // 1024 K
     splits = (int)(148 / rem);
-    if (splits > k_stages / 16) splits = k_stages / 16;
+    if (splits > k_stages / min_stages) splits = k_stages / min_stages;
     if (splits < 2) splits = 1;
     if (splits > 1) {
       L.full_tiles = (int)(tiles - rem);
@@ -1042,7 +1114,7 @@ WsLayout ws_layout(int64_t M, int64_t N, int64_t K) {
   L.splits = (k_stages + L.kps - 1) / L.kps;
   if (L.splits < 2) L.full_tiles = 0;
   L.b = 0;
-  L.a = fused ? 0 : round1k((size_t)(N * K * 2));
+  L.a = fused ? 0 : round1k((size_t)(N * K * (pdigits ? 1 : 2)));
   L.acc = L.a + round1k((size_t)(M * K * 2));
   const size_t sums = L.full_tiles > 0 ? (size_t)split_tiles * kBM * bn * 4 : (size_t)(M * N * 4);
   L.cnt = L.acc + (L.splits > 1 ? round1k(sums) : 0);
@@ -1065,20 +1137,30 @@ cudaError_t launch_kind(const uint8_t* Wq, const float* w_scale, const int8_t* x
   int* tile_cnt = reinterpret_cast<int*>(w + L.cnt);
   const int64_t nblk = FUSED ? 0 : N * K / 64, nx = M * K / 16;
   const int64_t nz = L.splits > 1 ? (int64_t)(L.end - L.acc) / 16 : 0;
-  int64_t grid = (8 * nblk + nx + nz + 255) / 256;
+  Prep pp;
+  pp.Wq = reinterpret_cast<const uint4*>(Wq);
+  pp.nblk = nblk;
+  pp.B = reinterpret_cast<uint4*>(B);
+  pp.b_e4m3 = KIND == 4;
+  pp.xq = reinterpret_cast<const uint4*>(xq);
+  pp.nx = nx;
+  pp.A = reinterpret_cast<uint4*>(A);
+  pp.a_mode = KIND == 2 ? kADigitsFused : KIND == 4 ? kADigitsPrefill : kABf16;
+  pp.digit_lo = nx;
+  pp.K = K;
+  pp.zero = reinterpret_cast<uint4*>(w + L.acc);
+  pp.nz = nz;
+  int64_t grid = ((KIND == 4 ? 4 : 8) * nblk + nx + nz + 255) / 256;
   if (grid > 148 * 16) grid = 148 * 16;
-  k_prepass<<<(unsigned)grid, 256, 0, s>>>(reinterpret_cast<const uint4*>(Wq), nblk,
-                                           reinterpret_cast<uint4*>(B),
-                                           reinterpret_cast<const uint4*>(xq), nx,
-                                           reinterpret_cast<uint4*>(A),
-                                           reinterpret_cast<uint4*>(w + L.acc), nz,
-                                           KIND == 2 ? nx : 0, K);
+  k_prepass<<<(unsigned)grid, 256, 0, s>>>(pp);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   CUtensorMap mapA, mapB;
-  // digits: [2M, K] e4m3 (hi rows, then lo rows), 64-row boxes
-  e = KIND == 2 ? encode_operand(&mapA, A, 2 * M, K, 1, kDigitRows)
-                : encode_operand(&mapA, A, M, K, Kind<KIND>::kElem, kBM);
+  // digits: [2M, K] e4m3 (hi rows, then lo rows), 64-row boxes (fused) or
+  // 128-row boxes (prefill)
+  e = KIND == 2   ? encode_operand(&mapA, A, 2 * M, K, 1, kDigitRows)
+      : KIND == 4 ? encode_operand(&mapA, A, 2 * M, K, 1, kBM)
+                  : encode_operand(&mapA, A, M, K, Kind<KIND>::kElem, kBM);
   if (e == cudaSuccess)
     e = FUSED ? encode_packed(&mapB, Wq, N, K, Kind<KIND>::kKStage / 4, BN)
               : encode_operand(&mapB, B, N, K, Kind<KIND>::kElem, BN);
@@ -1127,37 +1209,51 @@ cudaError_t launch_kind(const uint8_t* Wq, const float* w_scale, const int8_t* x
 // and k_gemm_tc<.., GATED> runs 128 x 128 output tiles with two accumulators
 // each (u and v on the same A tile), writing h = relu(v)^2 * u and, when
 // asked, u and v.  Workspace: [B up][B gate][A], each 1 KB aligned.
+// Workspace of the gated GEMM: [B up][B gate][A], each 1 KB aligned: e4m3
+// weights and activation digits (K >= 128), else bf16 copies.
 size_t gated_ws(int64_t M, int64_t N, int64_t K) {
-  return 2 * round1k((size_t)(N * K * 2)) + round1k((size_t)(M * K * 2));
+  const size_t wb = use_prefill_digits(M, K) ? 1 : 2;
+  return 2 * round1k((size_t)(N * K * wb)) + round1k((size_t)(M * K * 2));
 }
 
+template <int KIND>
 cudaError_t launch_gated_t(const uint8_t* Wu, const float* su, const uint8_t* Wg, const float* sg,
                            const int8_t* xq, const float* x_scale, int64_t M, int64_t N,
                            int64_t K, float* u, float* v, float* h, void* ws, long long wait,
                            cudaStream_t s) {
   constexpr int BN = 128;
+  constexpr size_t kWb = KIND == 4 ? 1 : 2;  // bytes per expanded weight
   cudaError_t e = get_encode();
   if (e != cudaSuccess) return e;
   uint8_t* w = static_cast<uint8_t*>(ws);
   void* Bu = w;
-  void* Bg = w + round1k((size_t)(N * K * 2));
-  void* A = w + 2 * round1k((size_t)(N * K * 2));
+  void* Bg = w + round1k((size_t)(N * K) * kWb);
+  void* A = w + 2 * round1k((size_t)(N * K) * kWb);
   const int64_t nblk = N * K / 64, nx = M * K / 16;
   for (int pass = 0; pass < 2; ++pass) {
     const int64_t n_x = pass == 0 ? nx : 0;
-    int64_t grid = (8 * nblk + n_x + 255) / 256;
+    int64_t grid = ((KIND == 4 ? 4 : 8) * nblk + n_x + 255) / 256;
     if (grid > 148 * 16) grid = 148 * 16;
-    k_prepass<<<(unsigned)grid, 256, 0, s>>>(
-        reinterpret_cast<const uint4*>(pass == 0 ? Wu : Wg), nblk,
-        reinterpret_cast<uint4*>(pass == 0 ? Bu : Bg), reinterpret_cast<const uint4*>(xq), n_x,
-        reinterpret_cast<uint4*>(A), nullptr, 0, 0, K);
+    Prep pp = {};
+    pp.Wq = reinterpret_cast<const uint4*>(pass == 0 ? Wu : Wg);
+    pp.nblk = nblk;
+    pp.B = reinterpret_cast<uint4*>(pass == 0 ? Bu : Bg);
+    pp.b_e4m3 = KIND == 4;
+    pp.xq = reinterpret_cast<const uint4*>(xq);
+    pp.nx = n_x;
+    pp.A = reinterpret_cast<uint4*>(A);
+    pp.a_mode = KIND == 4 ? kADigitsPrefill : kABf16;
+    pp.digit_lo = nx;
+    pp.K = K;
+    k_prepass<<<(unsigned)grid, 256, 0, s>>>(pp);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   CUtensorMap mapA, mapB, mapB2;
-  e = encode_operand(&mapA, A, M, K, Kind<kKind>::kElem, kBM);
-  if (e == cudaSuccess) e = encode_operand(&mapB, Bu, N, K, Kind<kKind>::kElem, BN);
-  if (e == cudaSuccess) e = encode_operand(&mapB2, Bg, N, K, Kind<kKind>::kElem, BN);
+  e = KIND == 4 ? encode_operand(&mapA, A, 2 * M, K, 1, kBM)
+                : encode_operand(&mapA, A, M, K, Kind<KIND>::kElem, kBM);
+  if (e == cudaSuccess) e = encode_operand(&mapB, Bu, N, K, Kind<KIND>::kElem, BN);
+  if (e == cudaSuccess) e = encode_operand(&mapB2, Bg, N, K, Kind<KIND>::kElem, BN);
   if (e != cudaSuccess) return e;
   Args a = {};
   a.M = (int)M;
@@ -1165,7 +1261,7 @@ cudaError_t launch_gated_t(const uint8_t* Wu, const float* su, const uint8_t* Wg
   a.K = (int)K;
   a.m_tiles = (int)((M + kBM - 1) / kBM);
   a.n_tiles = (int)((N + BN - 1) / BN);
-  a.k_stages = (int)((K + Kind<kKind>::kKStage - 1) / Kind<kKind>::kKStage);
+  a.k_stages = (int)((K + Kind<KIND>::kKStage - 1) / Kind<KIND>::kKStage);
   a.splits = 1;
   a.kps = a.k_stages;
   a.full_tiles = 0;
@@ -1185,16 +1281,16 @@ cudaError_t launch_gated_t(const uint8_t* Wu, const float* su, const uint8_t* Wg
   e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 64 && !configured[dev]) {
-    e = cudaFuncSetAttribute(k_gemm_tc<kKind, BN, false, true>,
+    e = cudaFuncSetAttribute(k_gemm_tc<KIND, BN, false, true>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Tile<BN, false, true>::kSmemBytes);
+                             Tile<BN, false, true, KIND>::kSmemBytes);
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
   const int items = a.m_tiles * a.n_tiles;
   const int ctas = items < 148 ? items : 148;
-  return launch_pdl(k_gemm_tc<kKind, BN, false, true>, dim3(ctas), dim3(kThreads),
-                    (size_t)Tile<BN, false, true>::kSmemBytes, s, mapA, mapB, mapB2, a);
+  return launch_pdl(k_gemm_tc<KIND, BN, false, true>, dim3(ctas), dim3(kThreads),
+                    (size_t)Tile<BN, false, true, KIND>::kSmemBytes, s, mapA, mapB, mapB2, a);
 }
 
 }  // namespace
@@ -1205,7 +1301,9 @@ cudaError_t launch_gemm_tc_gated(const uint8_t* Wu, const float* su, const uint8
                                  const float* sg, const int8_t* xq, const float* x_scale,
                                  int64_t M, int64_t N, int64_t K, float* u, float* v, float* h,
                                  void* ws, long long wait, cudaStream_t s) {
-  return launch_gated_t(Wu, su, Wg, sg, xq, x_scale, M, N, K, u, v, h, ws, wait, s);
+  if (use_prefill_digits(M, K))
+    return launch_gated_t<4>(Wu, su, Wg, sg, xq, x_scale, M, N, K, u, v, h, ws, wait, s);
+  return launch_gated_t<kKind>(Wu, su, Wg, sg, xq, x_scale, M, N, K, u, v, h, ws, wait, s);
 }
 
 bool gemm_tc_eligible(int64_t M, int64_t N, int64_t K) {
@@ -1224,6 +1322,13 @@ cudaError_t launch_gemm_tc(const uint8_t* Wq, const float* w_scale, const int8_t
   if (use_fused(M))
     return launch_kind<kKind, 256, true>(Wq, w_scale, xq, x_scale, M, N, K, y, y_bf16, acc_out,
                                          ws, wait, s);
+  if (use_prefill_digits(M, K)) {
+    if (pick_bn(N) == 128)
+      return launch_kind<4, 128, false>(Wq, w_scale, xq, x_scale, M, N, K, y, y_bf16, acc_out, ws,
+                                        wait, s);
+    return launch_kind<4, 256, false>(Wq, w_scale, xq, x_scale, M, N, K, y, y_bf16, acc_out, ws,
+                                      wait, s);
+  }
   if (pick_bn(N) == 128)
     return launch_kind<kKind, 128, false>(Wq, w_scale, xq, x_scale, M, N, K, y, y_bf16, acc_out,
                                           ws, wait, s);

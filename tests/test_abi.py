@@ -64,9 +64,10 @@ def test_workspace_queries():
 
 
 def test_linear_workspace_follows_the_dispatch():
-    """Workspace per path: none for decode (M <= 4), the bf16 activations for
-    the fused tensor-core path (16 <= M <= 256) plus the split-K sums when the
-    output has few tiles, the bf16 weights and activations for prefill."""
+    """Workspace per path: none for decode (M <= 4); 2 bytes per activation
+    (bf16, or two e4m3 digits) for the fused tensor-core path (16 <= M <= 256)
+    plus the split-K sums when the output has few tiles; for prefill the e4m3
+    weights (1 byte each) and the activations' two e4m3 digits."""
     L = bn.lib()
     assert L.bitnet_linear_workspace(1, 28672, 8192) == 0
     assert L.bitnet_linear_workspace(4, 2560, 6912) == 0
@@ -75,8 +76,8 @@ def test_linear_workspace_follows_the_dispatch():
     assert M * K * 2 <= w < M * K * 2 + M * N * 4
     M, N, K = 64, 8192, 28672          # 32 tiles: K split, fp32 sums + tile counters
     assert L.bitnet_linear_workspace(M, N, K) >= M * K * 2 + M * N * 4 + 32 * 4
-    M, N, K = 4096, 6912, 2560         # prefill: expanded weights and activations
-    assert L.bitnet_linear_workspace(M, N, K) >= N * K * 2 + M * K * 2
+    M, N, K = 4096, 6912, 2560         # prefill: expanded weights and activation digits
+    assert L.bitnet_linear_workspace(M, N, K) >= N * K + M * K * 2
 
 
 FAKE = 0x10000  # 16-byte aligned, never dereferenced: validation fails first

@@ -157,7 +157,10 @@ LINEAR_SHAPES = [(1, 1, 64), (1, 7, 64), (2, 65, 192), (3, 640, 2560), (1, 2560,
                  # e4m3 digit form (16 <= M <= 64, K >= 128): K a half stage past a
                  # multiple of 128, ragged N, split K, and K = 64 (bf16 form)
                  (24, 257, 320), (33, 2048, 192), (40, 1000, 1088), (48, 600, 6912),
-                 (16, 8, 64), (64, 4000, 2560)]
+                 (16, 8, 64), (64, 4000, 2560),
+                 # prefill digit form (M > 256): ragged K and N, BN = 128, K = 64
+                 # (bf16 form)
+                 (300, 333, 192), (260, 1000, 1088), (257, 100, 640), (300, 64, 64)]
 
 
 @pytest.mark.parametrize("M,N,K", LINEAR_SHAPES)
@@ -191,12 +194,15 @@ def test_linear_extreme_accumulators():
     assert acc.ravel().tolist() == [-128 * K, 128 * K]
 
 
-def test_linear_digit_form_extremes():
+@pytest.mark.parametrize("M", [16, 257])
+def test_linear_digit_form_extremes(M):
     """Tokens at the ends of the int8 range (digits hi = -8, lo = 0 and hi = 7,
     lo = 15) against all +1 / all -1 / alternating weights at K = 65536, and a
     row whose sum first grows to 2^22 and then moves by single units: every
-    sum must stay exact in the binary32 accumulators of the e4m3 MMAs."""
-    K, M = 65536, 16
+    sum must stay exact in the binary32 accumulators of the e4m3 MMAs (M = 16:
+    the small-M digit form; M = 257: the prefill digit form, whose hi digits
+    are scaled by 16, so that its sums reach 2^23)."""
+    K = 65536
     q = np.ones((3, K), np.int8)
     q[1] = -1
     q[2, 1::2] = -1
