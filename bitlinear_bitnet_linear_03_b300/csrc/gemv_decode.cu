@@ -368,13 +368,23 @@ k_gemv_decode(const __grid_constant__ Args a) {
             }
           }
         } else {
-          for (int v = tid; v < (K >> 3); v += kConsumers) {
-            const uint4 q = ld_nc_v4(xrow + v);
-            const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
+          // eight loads in flight per thread, then their maxima (a value
+          // past K reads as 0, which leaves the maximum unchanged)
+          const int nv = K >> 3;
+          for (int v0 = tid; v0 < nv; v0 += 8 * kConsumers) {
+            uint4 q[8];
 #pragma unroll
-            for (int t = 0; t < 4; ++t) {
-              mx = fmaxf(mx, fabsf(bf16_bits_to_float(w4[t] & 0xffffu)));
-              mx = fmaxf(mx, fabsf(bf16_bits_to_float(w4[t] >> 16)));
+            for (int u = 0; u < 8; ++u)
+              q[u] = v0 + u * kConsumers < nv ? ld_nc_v4(xrow + v0 + u * kConsumers)
+                                              : make_uint4(0, 0, 0, 0);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const uint32_t w4[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
+#pragma unroll
+              for (int t = 0; t < 4; ++t) {
+                mx = fmaxf(mx, fabsf(bf16_bits_to_float(w4[t] & 0xffffu)));
+                mx = fmaxf(mx, fabsf(bf16_bits_to_float(w4[t] >> 16)));
+              }
             }
           }
         }
@@ -392,6 +402,9 @@ k_gemv_decode(const __grid_constant__ Args a) {
       xscale[m] = sc.scale;
       if (m >= a.M) continue;
       const uint4* xrow = reinterpret_cast<const uint4*>(ph.xb + (int64_t)m * K);
+      // two-pass inputs: the pieces of four steps are loaded before any is
+      // quantised (the loads of pass two mostly hit in L1)
+      uint4 pre[4][2];
       for (int j = 0;; ++j) {
         const int f = tid + j * kConsumers;
         if (f >= nitems || (one_pass && j >= 2)) break;
@@ -402,7 +415,18 @@ k_gemv_decode(const __grid_constant__ Args a) {
           e[0] = h0.x; e[1] = h0.y; e[2] = h0.z; e[3] = h0.w;
           e[4] = h1.x; e[5] = h1.y; e[6] = h1.z; e[7] = h1.w;
         } else {
-          const uint4 h0 = ld_nc_v4(xrow + 2 * f), h1 = ld_nc_v4(xrow + 2 * f + 1);
+          if ((j & 3) == 0) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int fu = f + u * kConsumers;
+              pre[u][0] = fu < nitems ? ld_nc_v4(xrow + 2 * fu) : make_uint4(0, 0, 0, 0);
+              pre[u][1] = fu < nitems ? ld_nc_v4(xrow + 2 * fu + 1) : make_uint4(0, 0, 0, 0);
+            }
+          }
+          uint4 h0 = pre[0][0], h1 = pre[0][1];
+#pragma unroll
+          for (int u = 1; u < 4; ++u)
+            if ((j & 3) == u) h0 = pre[u][0], h1 = pre[u][1];
           e[0] = h0.x; e[1] = h0.y; e[2] = h0.z; e[3] = h0.w;
           e[4] = h1.x; e[5] = h1.y; e[6] = h1.z; e[7] = h1.w;
         }
