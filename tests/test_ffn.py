@@ -149,6 +149,15 @@ def test_ffn_seq4096_sampled_tokens(seed):
     assert (np.abs(got["xq"]).max(axis=1) == 127).all()
 
 
+@pytest.mark.parametrize("H_,F_", [(64, 192), (128, 64)])
+def test_ffn_prefill_small_dims(H_, F_):
+    """Above 256 tokens with K below 128 on one side: (64, 192) runs the gated
+    up/gate GEMM on bf16 operands and the down GEMM in the e4m3 digit form
+    (K = 192, one and a half 128-deep stages); (128, 64) the reverse.  Every
+    stage, all 300 tokens."""
+    check_ffn(300, 7, H=H_, F=F_, random_gain=True)
+
+
 @pytest.mark.parametrize("M,seed", [(300, 5), (512, 6)])
 def test_ffn_prefill_gated_gemm_without_intermediates(M, seed):
     """Above 256 tokens the up and gate products run as one GEMM whose
