@@ -158,8 +158,13 @@ bitnet_status bitnet_quantize_act(const uint16_t* x, int64_t M, int64_t K,
  * weights through the decode kernel (no workspace); 5 <= M < 16 runs a
  * CUDA-core kernel; M >= 16 runs the tensor cores (M <= 256: the packed
  * weights are expanded on chip, and K is split over CTAs when the output
- * has few 128 x 256 tiles; M > 256: a bf16 copy of the weights is made in
- * the workspace first). */
+ * has few 128 x 256 tiles; M > 256: an expanded copy of the weights is made
+ * in the workspace first).  sm_103a has no integer tensor-core product, so
+ * the tensor cores multiply exact stand-ins: for K >= 128 and M <= 64 or
+ * M > 256, e4m3 copies of the ternary weights and of the two digits of each
+ * activation (x = 16 (x >> 4) + (x & 15)); otherwise bf16 copies.  Every
+ * partial sum is an integer below 2^24, so the binary32 accumulators hold
+ * acc exactly. */
 size_t bitnet_linear_workspace(int64_t M, int64_t N, int64_t K);
 bitnet_status bitnet_linear(const uint8_t* Wq, const float* w_scale,
                             const int8_t* xq, const float* x_scale, int64_t M,
