@@ -391,12 +391,13 @@ def secondary_measurements(torch, bn, peaks, only=None, cpu=True):
       * single GEMV 2560x2560, batch 1 (80 weight sets);
       * 100B-class shapes 8192->28672 and 28672->8192: M = 1 (and M = 4 at
         K = 8192) through bitnet_linear_bf16 (bf16 tokens with 1% outliers
-        quantised in the launch, static weights), the rest through
-        bitnet_linear on int8 codes;
+        quantised in the launch, static weights), the rest (M = 4 at
+        K = 28672, M = 8, 16, 32, 64) through bitnet_linear on int8 codes;
+      * 2B-class shapes at M = 16 and 64 through bitnet_linear;
       * prefill M = 4096 on the 2B FFN shapes, binary32 and bf16 outputs
         (tensor-core roofline against the measured bf16 dense peak: sm_103a has
-        no integer tensor-core MMA, so the exact integer products run as bf16
-        MMAs);
+        no integer tensor-core MMA, so the exact integer products run as e4m3
+        digit MMAs, whose tensor time equals bf16's);
       * the fused FFN (hidden 2560, FFN 6912) at seq 1 and seq 4096;
       * 8B-class shapes (hidden 4096, FFN 14336, K/V 1024): the 32-layer
         decode step as one chain, and prefill M = 4096;
@@ -433,8 +434,9 @@ def secondary_measurements(torch, bn, peaks, only=None, cpu=True):
         del sets
 
     # 100B-class shapes (each timed as a CUDA graph of calls)
-    ms_100b = [m for m, c in ((1, "gemv100b"), (4, "gemv100b"), (16, "fused_small_m"),
-                              (32, "fused_small_m"), (64, "fused_small_m")) if want(c)]
+    ms_100b = [m for m, c in ((1, "gemv100b"), (4, "gemv100b"), (8, "fused_small_m"),
+                              (16, "fused_small_m"), (32, "fused_small_m"),
+                              (64, "fused_small_m")) if want(c)]
     for (N, K) in ([(28672, 8192), (8192, 28672)] if ms_100b else []):
         sets = _weight_sets(torch, bn, synth, N, K, 3, 200)
         for M in ms_100b:

@@ -155,8 +155,9 @@ bitnet_status bitnet_quantize_act(const uint16_t* x, int64_t M, int64_t K,
  * ws: scratch of bitnet_linear_workspace(M, N, K) bytes (0 when none is
  * needed), no initial contents required.  M <= 4096*64 rows per call;
  * K % 64 == 0.  Paths, all giving the same bits: M <= 4 streams the packed
- * weights through the decode kernel (no workspace); 5 <= M < 16 runs a
- * CUDA-core kernel; M >= 16 runs the tensor cores (M <= 256: the packed
+ * weights through the decode kernel (no workspace); 5 <= M < 12 runs a
+ * CUDA-core kernel when the matrix has fewer than 16 Mi weights; larger M
+ * or matrices run the tensor cores (M <= 256: the packed
  * weights are expanded on chip, and K is split over CTAs when the output
  * has few 128 x 256 tiles; M > 256: an expanded copy of the weights is made
  * in the workspace first).  sm_103a has no integer tensor-core product, so

@@ -65,7 +65,7 @@ def test_workspace_queries():
 
 def test_linear_workspace_follows_the_dispatch():
     """Workspace per path: none for decode (M <= 4); 2 bytes per activation
-    (bf16, or two e4m3 digits) for the fused tensor-core path (16 <= M <= 256)
+    (bf16, or two e4m3 digits) for the fused tensor-core path (M <= 256)
     plus the split-K sums when the output has few tiles; for prefill the e4m3
     weights (1 byte each) and the activations' two e4m3 digits."""
     L = bn.lib()

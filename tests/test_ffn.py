@@ -61,7 +61,7 @@ def test_ffn_seq1(seed):
     check_ffn(1, seed)
 
 
-@pytest.mark.parametrize("M", [3, 64])
+@pytest.mark.parametrize("M", [3, 8, 64])
 def test_ffn_small_batches(M):
     check_ffn(M, 0, random_gain=True)
 

@@ -150,11 +150,14 @@ def gpu_linear(Wq, ws, qx, sx, K):
 
 LINEAR_SHAPES = [(1, 1, 64), (1, 7, 64), (2, 65, 192), (3, 640, 2560), (1, 2560, 2560),
                  (5, 2560, 2560), (8, 6912, 2560), (1, 2560, 6912), (17, 2560, 6912),
+                 # 5 <= M < 12: CUDA cores below 16 Mi weights, tensor cores above
+                 (7, 1000, 1088), (11, 640, 2560), (5, 8192, 2048), (9, 4100, 4096),
+                 (12, 100, 640),
                  (4, 100, 8192), (63, 96, 2560), (64, 33, 128), (65, 130, 640), (129, 64, 320),
                  (1, 31, 65536),
                  # tensor-core path with K split over several CTAs (few output tiles)
                  (20, 300, 4096), (64, 33, 8192), (200, 777, 2048), (16, 2560, 4096),
-                 # e4m3 digit form (16 <= M <= 64, K >= 128): K a half stage past a
+                 # e4m3 digit form (M <= 64, K >= 128): K a half stage past a
                  # multiple of 128, ragged N, split K, and K = 64 (bf16 form)
                  (24, 257, 320), (33, 2048, 192), (40, 1000, 1088), (48, 600, 6912),
                  (16, 8, 64), (64, 4000, 2560),
