@@ -86,7 +86,7 @@ cudaError_t run_linear(const uint8_t* Wq, const float* w_scale, const int8_t* xq
 bool ffn_gated(int64_t M, int64_t H) { return M > 256 && !bitnet::decode_supported(M, H); }
 
 struct FfnLayout {
-  size_t xq, sx, u, v, hq, sh, lin, total;
+  size_t xq, sx, u, v, hq, sh, hmax, lin, total;
 };
 FfnLayout ffn_layout(int64_t M, int64_t H, int64_t F) {
   FfnLayout L;
@@ -102,6 +102,7 @@ FfnLayout ffn_layout(int64_t M, int64_t H, int64_t F) {
   L.v = take((size_t)(M * F) * 4);
   L.hq = take((size_t)(M * F));
   L.sh = take((size_t)M * 4);
+  L.hmax = take((size_t)M * 4);  // the gated GEMM's row maxima of |h|
   size_t a = linear_ws(M, F, H), b = linear_ws(M, H, F);
   if (ffn_gated(M, H)) a = std::max(a, bitnet::gemm_tc_gated_workspace(M, F, H));
   L.lin = take(a > b ? a : b);
@@ -360,12 +361,25 @@ bitnet_status bitnet_ffn(const uint16_t* x, const float* g, float eps, const uin
   } else if (ffn_gated(M, H)) {
     // one GEMM for up and gate; h goes to d.h or to u's workspace section
     float* h = d.h ? d.h : reinterpret_cast<float*>(w + L.u);
+    // With the digit-form down projection, the gated GEMM also records each
+    // row's max |h| and the down GEMM's pre-pass quantises h straight into
+    // its operand (hq is written only when asked for); otherwise h is
+    // quantised first.
+    const bool h_direct = bitnet::gemm_tc_from_f32_supported(M, F);
+    unsigned* hmax = h_direct ? reinterpret_cast<unsigned*>(w + L.hmax) : nullptr;
     if (e == cudaSuccess)
-      e = bitnet::launch_gemm_tc_gated(Wup, s_up, Wgate, s_gate, xq, sx, M, F, H, d.u, d.v, h, lin,
-                                       bitnet::wait_limit_cycles(), s);
-    if (e == cudaSuccess) e = bitnet::launch_quantize_act_f32(h, M, F, hq, sh, s);
-    if (e == cudaSuccess)
-      e = run_linear(Wdown, s_down, hq, sh, M, H, F, y, nullptr, d.acc_down, lin, s);
+      e = bitnet::launch_gemm_tc_gated(Wup, s_up, Wgate, s_gate, xq, sx, M, F, H, d.u, d.v, h,
+                                       hmax, lin, bitnet::wait_limit_cycles(), s);
+    if (h_direct) {
+      if (e == cudaSuccess)
+        e = bitnet::launch_gemm_tc_from_f32(Wdown, s_down, h, hmax, M, H, F, y, nullptr,
+                                            d.acc_down, d.hq, sh, lin,
+                                            bitnet::wait_limit_cycles(), s);
+    } else {
+      if (e == cudaSuccess) e = bitnet::launch_quantize_act_f32(h, M, F, hq, sh, s);
+      if (e == cudaSuccess)
+        e = run_linear(Wdown, s_down, hq, sh, M, H, F, y, nullptr, d.acc_down, lin, s);
+    }
     return cuda_status(e);
   } else {
     if (e == cudaSuccess) e = run_linear(Wup, s_up, xq, sx, M, F, H, u, nullptr, nullptr, lin, s);

@@ -168,6 +168,10 @@ struct Args {
   const float* w_scale2;
   float* y2;
   float* h;
+  // optional: the bits of each row's max |h| (fmaxf from 0, so never NaN;
+  // the non-negative binary32 values order as their bit patterns), combined
+  // over the tiles with atomicMax; zeroed before the launch
+  unsigned* hmax;
 };
 
 // Work item -> tile and K-stage range.
@@ -715,6 +719,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUte
         const float cv = mrow ? __fmul_rn(a.x_scale[m], ws2) : 0.0f;
         float* vrow = a.y2 ? a.y2 + (int64_t)m * a.N : nullptr;
         float* hrow = a.h + (int64_t)m * a.N;
+        float hm = 0.0f;
         for (int cb = 0; cb < BN; cb += 32) {
           uint32_t ru[32], rv[32];
           const uint32_t ta = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(ab * 2 * BN + cb);
@@ -733,7 +738,13 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUte
           if (yrow) store_f32_32(yrow, nb, uf, v4, a.N);
           if (vrow) store_f32_32(vrow, nb, vf, v4, a.N);
           store_f32_32(hrow, nb, hf, v4, a.N);
+          if (a.hmax) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (nb + j < a.N) hm = fmaxf(hm, fabsf(hf[j]));
+          }
         }
+        if (a.hmax && mrow) atomicMax(a.hmax + m, __float_as_uint(hm));
       }
       for (int cb = 0; cb < BN && !GATED; cb += 32) {
         uint32_t r[32];
@@ -910,13 +921,20 @@ __device__ __forceinline__ uint32_t e4m3x4_from_codes(uint32_t v) {
 //      X_g of four, and places X_g byte b at chunk byte 4o + i with
 //      b = 2 (o & 1) + (i >> 1), g = 2 (i & 1) + (o >> 1): the byte permutes
 //      (X0, X2 | X1, X3 by 0x5140 | 0x7362);
-//    - kADigitsPrefill: hi' = 16 (x >> 4) and lo = x & 15, in K order.
+//    - kADigitsPrefill: hi' = 16 (x >> 4) and lo = x & 15, in K order;
+//    - kADigitsFromF32: the same digits of x = the per-token int8 codes of
+//      the binary32 rows hf, quantised with the rule of the activation
+//      quantiser (scale from the row's max |hf| in hmax, inv = 127 / a',
+//      x = round_clip(hf * inv)); the item that starts a row writes its
+//      scale, and the codes also go to hq when asked.
 //  * nz 16-byte zero stores (split-K sums and tile counters).
-enum AMode { kABf16 = 0, kADigitsFused = 1, kADigitsPrefill = 2 };
+enum AMode { kABf16 = 0, kADigitsFused = 1, kADigitsPrefill = 2, kADigitsFromF32 = 3 };
 struct Prep {
   const uint4* Wq;
   int64_t nblk;
   uint4* B;
+  const uint4* Wq2;  // optional second matrix of the same shape (into B2)
+  uint4* B2;
   int b_e4m3;
   const uint4* xq;
   int64_t nx;
@@ -925,26 +943,36 @@ struct Prep {
   int64_t digit_lo, K;
   uint4* zero;
   int64_t nz;
+  // kADigitsFromF32
+  const float4* hf;
+  const unsigned* hmax;
+  float* sh;
+  uint4* hq;
 };
 __global__ void __launch_bounds__(256) k_prepass(const Prep p) {
-  const int64_t nbi = (p.b_e4m3 ? 4 : 8) * p.nblk;
+  const int64_t per = (p.b_e4m3 ? 4 : 8) * p.nblk;
+  const int64_t nbi = per * (p.Wq2 ? 2 : 1);
   const int64_t total = nbi + p.nx + p.nz;
   for (int64_t it = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; it < total;
        it += (int64_t)gridDim.x * blockDim.x) {
     if (it < nbi) {
+      const bool second = it >= per;
+      const uint4* Wq = second ? p.Wq2 : p.Wq;
+      uint4* B = second ? p.B2 : p.B;
+      const int64_t jt = second ? it - per : it;
       if (p.b_e4m3) {
-        const uint4 w = p.Wq[it >> 2];  // the 4 threads of a block share this load
-        const int sft = 2 * (int)(it & 3);
-        p.B[it] = make_uint4(e4m3x4_from_codes(w.x >> sft), e4m3x4_from_codes(w.y >> sft),
-                             e4m3x4_from_codes(w.z >> sft), e4m3x4_from_codes(w.w >> sft));
+        const uint4 w = Wq[jt >> 2];  // the 4 threads of a block share this load
+        const int sft = 2 * (int)(jt & 3);
+        B[jt] = make_uint4(e4m3x4_from_codes(w.x >> sft), e4m3x4_from_codes(w.y >> sft),
+                           e4m3x4_from_codes(w.z >> sft), e4m3x4_from_codes(w.w >> sft));
       } else {
-        const uint4 w = p.Wq[it >> 3];  // the 8 threads of a block share this load
+        const uint4 w = Wq[jt >> 3];  // the 8 threads of a block share this load
         const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-        const int c = (int)(it & 7), sft = 2 * (c >> 1), h = c & 1;
+        const int c = (int)(jt & 7), sft = 2 * (c >> 1), h = c & 1;
         uint4 o;
         bf16x4_from_codes((ww[2 * h] >> sft) & 0x03030303u, o.x, o.y);
         bf16x4_from_codes((ww[2 * h + 1] >> sft) & 0x03030303u, o.z, o.w);
-        p.B[it] = o;
+        B[jt] = o;
       }
     } else if (it >= nbi + p.nx) {
       p.zero[it - nbi - p.nx] = make_uint4(0, 0, 0, 0);
@@ -960,6 +988,26 @@ __global__ void __launch_bounds__(256) k_prepass(const Prep p) {
       uint32_t hi[4], lo[4];
 #pragma unroll
       for (int q = 0; q < 4; ++q) digits4(P[q], 1, hi[q], lo[q]);
+      p.A[i] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+      p.A[p.digit_lo + i] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    } else if (p.a_mode == kADigitsFromF32) {
+      const int64_t i = it - nbi;
+      const int64_t f = 16 * i, m = f / p.K;
+      const ActScale sc = act_scale_from_absmax(__uint_as_float(p.hmax[m]));
+      if (f - m * p.K == 0) p.sh[m] = sc.scale;
+      uint32_t w[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float4 v = p.hf[4 * i + q];
+        w[q] = pack_i8x4(round_clip(__fmul_rn(v.x, sc.inv), -128.f, 127.f),
+                         round_clip(__fmul_rn(v.y, sc.inv), -128.f, 127.f),
+                         round_clip(__fmul_rn(v.z, sc.inv), -128.f, 127.f),
+                         round_clip(__fmul_rn(v.w, sc.inv), -128.f, 127.f));
+      }
+      if (p.hq) p.hq[i] = make_uint4(w[0], w[1], w[2], w[3]);
+      uint32_t hi[4], lo[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) digits4(w[q], 16, hi[q], lo[q]);
       p.A[i] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
       p.A[p.digit_lo + i] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
     } else if (p.a_mode == kADigitsPrefill) {
@@ -1122,11 +1170,22 @@ WsLayout ws_layout(int64_t M, int64_t N, int64_t K) {
   return L;
 }
 
+// The activations as binary32 rows to quantise in the pre-pass (the FFN's h
+// before the down projection), with their row maxima; the int8 codes (hq,
+// optional) and scales (sh) are written there too.
+struct FromF32 {
+  const float* h;
+  const unsigned* hmax;
+  int8_t* hq;
+  float* sh;
+};
+
 template <int KIND, int BN, bool FUSED>
 cudaError_t launch_kind(const uint8_t* Wq, const float* w_scale, const int8_t* xq,
                         const float* x_scale, int64_t M, int64_t N, int64_t K, float* y,
                         uint16_t* y_bf16, int32_t* acc_out, void* ws, long long wait,
-                        cudaStream_t s) {
+                        cudaStream_t s, const FromF32* ff = nullptr) {
+  if (ff && KIND != 4) return cudaErrorInvalidValue;
   cudaError_t e = get_encode();
   if (e != cudaSuccess) return e;
   const WsLayout L = ws_layout(M, N, K);
@@ -1141,6 +1200,8 @@ cudaError_t launch_kind(const uint8_t* Wq, const float* w_scale, const int8_t* x
   pp.Wq = reinterpret_cast<const uint4*>(Wq);
   pp.nblk = nblk;
   pp.B = reinterpret_cast<uint4*>(B);
+  pp.Wq2 = nullptr;
+  pp.B2 = nullptr;
   pp.b_e4m3 = KIND == 4;
   pp.xq = reinterpret_cast<const uint4*>(xq);
   pp.nx = nx;
@@ -1150,6 +1211,18 @@ cudaError_t launch_kind(const uint8_t* Wq, const float* w_scale, const int8_t* x
   pp.K = K;
   pp.zero = reinterpret_cast<uint4*>(w + L.acc);
   pp.nz = nz;
+  pp.hf = nullptr;
+  pp.hmax = nullptr;
+  pp.sh = nullptr;
+  pp.hq = nullptr;
+  if (ff) {
+    pp.a_mode = kADigitsFromF32;
+    pp.hf = reinterpret_cast<const float4*>(ff->h);
+    pp.hmax = ff->hmax;
+    pp.sh = ff->sh;
+    pp.hq = reinterpret_cast<uint4*>(ff->hq);
+    x_scale = ff->sh;
+  }
   int64_t grid = ((KIND == 4 ? 4 : 8) * nblk + nx + nz + 255) / 256;
   if (grid > 148 * 16) grid = 148 * 16;
   k_prepass<<<(unsigned)grid, 256, 0, s>>>(pp);
@@ -1186,6 +1259,7 @@ cudaError_t launch_kind(const uint8_t* Wq, const float* w_scale, const int8_t* x
   a.w_scale2 = nullptr;
   a.y2 = nullptr;
   a.h = nullptr;
+  a.hmax = nullptr;
   static bool configured[64] = {};
   int dev = 0;
   e = cudaGetDevice(&dev);
@@ -1219,8 +1293,8 @@ size_t gated_ws(int64_t M, int64_t N, int64_t K) {
 template <int KIND>
 cudaError_t launch_gated_t(const uint8_t* Wu, const float* su, const uint8_t* Wg, const float* sg,
                            const int8_t* xq, const float* x_scale, int64_t M, int64_t N,
-                           int64_t K, float* u, float* v, float* h, void* ws, long long wait,
-                           cudaStream_t s) {
+                           int64_t K, float* u, float* v, float* h, unsigned* hmax, void* ws,
+                           long long wait, cudaStream_t s) {
   constexpr int BN = 128;
   constexpr size_t kWb = KIND == 4 ? 1 : 2;  // bytes per expanded weight
   cudaError_t e = get_encode();
@@ -1230,25 +1304,28 @@ cudaError_t launch_gated_t(const uint8_t* Wu, const float* su, const uint8_t* Wg
   void* Bg = w + round1k((size_t)(N * K) * kWb);
   void* A = w + 2 * round1k((size_t)(N * K) * kWb);
   const int64_t nblk = N * K / 64, nx = M * K / 16;
-  for (int pass = 0; pass < 2; ++pass) {
-    const int64_t n_x = pass == 0 ? nx : 0;
-    int64_t grid = ((KIND == 4 ? 4 : 8) * nblk + n_x + 255) / 256;
-    if (grid > 148 * 16) grid = 148 * 16;
-    Prep pp = {};
-    pp.Wq = reinterpret_cast<const uint4*>(pass == 0 ? Wu : Wg);
-    pp.nblk = nblk;
-    pp.B = reinterpret_cast<uint4*>(pass == 0 ? Bu : Bg);
-    pp.b_e4m3 = KIND == 4;
-    pp.xq = reinterpret_cast<const uint4*>(xq);
-    pp.nx = n_x;
-    pp.A = reinterpret_cast<uint4*>(A);
-    pp.a_mode = KIND == 4 ? kADigitsPrefill : kABf16;
-    pp.digit_lo = nx;
-    pp.K = K;
-    k_prepass<<<(unsigned)grid, 256, 0, s>>>(pp);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-  }
+  // one pre-pass: both weight matrices, the activations, and (when asked)
+  // the zeroed row maxima of h
+  Prep pp = {};
+  pp.Wq = reinterpret_cast<const uint4*>(Wu);
+  pp.nblk = nblk;
+  pp.B = reinterpret_cast<uint4*>(Bu);
+  pp.Wq2 = reinterpret_cast<const uint4*>(Wg);
+  pp.B2 = reinterpret_cast<uint4*>(Bg);
+  pp.b_e4m3 = KIND == 4;
+  pp.xq = reinterpret_cast<const uint4*>(xq);
+  pp.nx = nx;
+  pp.A = reinterpret_cast<uint4*>(A);
+  pp.a_mode = KIND == 4 ? kADigitsPrefill : kABf16;
+  pp.digit_lo = nx;
+  pp.K = K;
+  pp.zero = reinterpret_cast<uint4*>(hmax);
+  pp.nz = hmax ? (M + 3) / 4 : 0;
+  int64_t grid = (2 * (KIND == 4 ? 4 : 8) * nblk + nx + pp.nz + 255) / 256;
+  if (grid > 148 * 16) grid = 148 * 16;
+  k_prepass<<<(unsigned)grid, 256, 0, s>>>(pp);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
   CUtensorMap mapA, mapB, mapB2;
   e = KIND == 4 ? encode_operand(&mapA, A, 2 * M, K, 1, kBM)
                 : encode_operand(&mapA, A, M, K, Kind<KIND>::kElem, kBM);
@@ -1276,6 +1353,7 @@ cudaError_t launch_gated_t(const uint8_t* Wu, const float* su, const uint8_t* Wg
   a.w_scale2 = sg;
   a.y2 = v;
   a.h = h;
+  a.hmax = hmax;
   static bool configured[64] = {};
   int dev = 0;
   e = cudaGetDevice(&dev);
@@ -1300,10 +1378,25 @@ size_t gemm_tc_gated_workspace(int64_t M, int64_t N, int64_t K) { return gated_w
 cudaError_t launch_gemm_tc_gated(const uint8_t* Wu, const float* su, const uint8_t* Wg,
                                  const float* sg, const int8_t* xq, const float* x_scale,
                                  int64_t M, int64_t N, int64_t K, float* u, float* v, float* h,
-                                 void* ws, long long wait, cudaStream_t s) {
+                                 unsigned* hmax, void* ws, long long wait, cudaStream_t s) {
   if (use_prefill_digits(M, K))
-    return launch_gated_t<4>(Wu, su, Wg, sg, xq, x_scale, M, N, K, u, v, h, ws, wait, s);
-  return launch_gated_t<kKind>(Wu, su, Wg, sg, xq, x_scale, M, N, K, u, v, h, ws, wait, s);
+    return launch_gated_t<4>(Wu, su, Wg, sg, xq, x_scale, M, N, K, u, v, h, hmax, ws, wait, s);
+  return launch_gated_t<kKind>(Wu, su, Wg, sg, xq, x_scale, M, N, K, u, v, h, hmax, ws, wait, s);
+}
+
+bool gemm_tc_from_f32_supported(int64_t M, int64_t K) { return use_prefill_digits(M, K); }
+
+cudaError_t launch_gemm_tc_from_f32(const uint8_t* Wq, const float* w_scale, const float* h,
+                                    const unsigned* hmax, int64_t M, int64_t N, int64_t K,
+                                    float* y, uint16_t* y_bf16, int32_t* acc_out, int8_t* hq,
+                                    float* sh, void* ws, long long wait, cudaStream_t s) {
+  if (!use_prefill_digits(M, K)) return cudaErrorInvalidValue;
+  const FromF32 ff = {h, hmax, hq, sh};
+  if (pick_bn(N) == 128)
+    return launch_kind<4, 128, false>(Wq, w_scale, nullptr, nullptr, M, N, K, y, y_bf16, acc_out,
+                                      ws, wait, s, &ff);
+  return launch_kind<4, 256, false>(Wq, w_scale, nullptr, nullptr, M, N, K, y, y_bf16, acc_out, ws,
+                                    wait, s, &ff);
 }
 
 // M >= 12, or M >= 5 on matrices of at least 16 Mi weights: measured on B300
