@@ -182,10 +182,13 @@ class DecodeStep:
         self.x0 = x0.contiguous()
         bf, f32 = torch.bfloat16, torch.float32
         self.out = []
+        # every layer's K and V outputs are views of one block, so that the
+        # step's results leave the device in two copies, not one per array
+        self.kv = torch.empty((layers, 2, 1, KV), dtype=f32, device=dev)
         for li in range(layers):
             self.out.append(dict(q=torch.empty((1, H), dtype=bf, device=dev),
-                                 k=torch.empty((1, KV), dtype=f32, device=dev),
-                                 v=torch.empty((1, KV), dtype=f32, device=dev),
+                                 k=self.kv[li, 0],
+                                 v=self.kv[li, 1],
                                  o=torch.empty((1, H), dtype=bf, device=dev),
                                  h=torch.empty((1, F), dtype=f32, device=dev),
                                  y=torch.empty((1, H), dtype=bf, device=dev)))
@@ -226,8 +229,8 @@ class DecodeStep:
 
     def result_tensors(self):
         """What a decode step hands back: the last layer's output and every
-        layer's K and V (the cache entries of this token)."""
-        return [self.out[-1]["y"]] + [o[k] for o in self.out for k in ("k", "v")]
+        layer's K and V (the cache entries of this token, one block)."""
+        return [self.out[-1]["y"], self.kv]
 
 
 def capture(torch, fn):
