@@ -1,16 +1,17 @@
-// gemm_tc.cu — tensor-core BitLinear for prefill-sized M.
+// gemm_tc.cu — tensor-core BitLinear for blocks of tokens.
 //
 // The product is the BitLinear contraction of "BitNet.cpp deep dive"
 // (dashen-tech), §3.1 (acc = sum_pos - sum_neg = sum_k q[n,k] x[m,k]) over a
 // whole block of tokens, with the rescale y = (float)acc * (x_scale *
 // w_scale).  sm_103a has no integer tensor-core MMA (ptxas rejects
-// tcgen05.mma .kind::i8 for this target), so the contraction runs as
-// kind::f16 with bf16 operands: ternary weights and int8 activations are
-// exact in bf16 (integers of magnitude <= 256), every product is exact, and
-// every partial sum is an integer of magnitude <= 128 K < 2^24 for
-// K <= 65536, so the binary32 accumulator is exact and independent of the
-// order of the additions; the epilogue rescales that binary32 integer
-// directly (and forms int32 only for the optional accumulator output).
+// tcgen05.mma .kind::i8 for this target), so the contraction runs on exact
+// stand-ins: bf16 operands under kind::f16 (ternary weights and int8
+// activations are integers of magnitude <= 256, exact in bf16), or the e4m3
+// digit forms below.  Every product is exact and every partial sum is an
+// integer of magnitude <= 128 K < 2^24 for K <= 65536, so the binary32
+// accumulator is exact and independent of the order of the additions; the
+// epilogue rescales that binary32 integer directly (and forms int32 only for
+// the optional accumulator output).
 // The exact e4m3 digit form (kind::f8f6f4) replaces bf16 wherever K >= 128
 // and M is not in 65..256: x = 16 hi + lo with hi in [-8, 7] and lo in
 // [0, 15], both exact in e4m3, as are the ternary weights.
@@ -68,7 +69,8 @@ constexpr int kThreadsFused = 320;  // + 4 warps expanding the packed weights
 constexpr uint32_t kTmemCols = 512;
 constexpr int kRingBytes = 192 * 1024;
 // Tile N = BN (256 or 128): B tile, stage size, ring depth and shared memory.
-// Unfused: a TMA stage holds the A and B tiles.  FUSED: a TMA stage holds the
+// Unfused: a TMA stage holds the A and B tiles (the prefill digit form: the
+// hi' and lo A tiles and the B tile, 64 KB at BN = 256).  FUSED: a TMA stage holds the
 // A tile and the packed 2-bit codes of the B tile (16 bytes per row), and
 // the codes are expanded into one of two bf16 B buffers after the ring, so
 // the TMA ring is deep (6 stages) while the expanded tiles are only double
@@ -1094,8 +1096,8 @@ constexpr int kKind = 1;
 size_t round1k(size_t v) { return (v + 1023) / 1024 * 1024; }
 
 // Small batches expand the packed weights on chip (streaming 2 bits per
-// weight from HBM); large ones expand them once into a bf16 copy that stays
-// in L2 across the many output-tile rows.
+// weight from HBM); large ones expand them once into an e4m3 (or bf16) copy
+// that stays largely in L2 across the many output-tile rows.
 bool use_fused(int64_t M) { return M <= 256; }
 // The exact e4m3 digit form (two digit rows per token in one 128-row tile)
 // serves M <= 64 on the fused path: half the MMAs of the bf16 form and
@@ -1279,12 +1281,12 @@ cudaError_t launch_kind(const uint8_t* Wq, const float* w_scale, const int8_t* x
 }
 
 // The FFN's up and gate products in one GEMM (M > 256): both weight matrices
-// are expanded once per call into bf16 copies, the activations into bf16 A,
-// and k_gemm_tc<.., GATED> runs 128 x 128 output tiles with two accumulators
-// each (u and v on the same A tile), writing h = relu(v)^2 * u and, when
-// asked, u and v.  Workspace: [B up][B gate][A], each 1 KB aligned.
-// Workspace of the gated GEMM: [B up][B gate][A], each 1 KB aligned: e4m3
-// weights and activation digits (K >= 128), else bf16 copies.
+// are expanded once per call (e4m3, or bf16 when K < 128) and the
+// activations split into digits (or widened to bf16), and k_gemm_tc<..,
+// GATED> runs 128 x 128 output tiles with two accumulators each (u and v on
+// the same A tiles), writing h = relu(v)^2 * u, optionally each row's max
+// |h|, and, when asked, u and v.  Workspace: [B up][B gate][A], each 1 KB
+// aligned.
 size_t gated_ws(int64_t M, int64_t N, int64_t K) {
   const size_t wb = use_prefill_digits(M, K) ? 1 : 2;
   return 2 * round1k((size_t)(N * K * wb)) + round1k((size_t)(M * K * 2));
